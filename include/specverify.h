@@ -1,0 +1,219 @@
+/*
+ * specverify.h — C ABI of the batched speculative-decoding verifier
+ * (rejection sampler) for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes. For every request b the caller has K_b draft tokens
+ * d_1..d_K, the target model's logits for the K_b+1 positions that one
+ * verification pass scores (p_1..p_{K+1}, each conditioned on the drafts
+ * before it) and the draft's law q_1..q_K. The verifier commits the accepted
+ * prefix of the drafts and one more token:
+ *
+ *   - lossless rule: accept d_i with probability min(1, p_i(d_i)/q_i(d_i))
+ *     (outright when q <= p), stop at the first rejection, draw the
+ *     replacement from norm(max(0, p - q)); when all K are accepted draw a
+ *     bonus token from p_{K+1}.
+ *       Sources: "Acceptance Is Not Speed (arXiv:2610.23818)", §1 and §6;
+ *       "RheoSampling 2026", §4 "RheoVerification"; nalar.dev "Speculative
+ *       decoding: memverifikasi token draft sebelum diterima", sections
+ *       "Draft mengubah tebakan serial menjadi batch verifikasi",
+ *       "Semantik penerimaan" and "Penolakan memendekkan pekerjaan
+ *       speculative".
+ *   - greedy (T < 0.05, or rule SPEC_RULE_GREEDY): accept while d_i equals
+ *     argmax p_i (lowest id on ties); the target's argmax replaces the first
+ *     mismatch, or is the bonus token. (nalar.dev, "Semantik penerimaan".)
+ *   - p = softmax(z_t / T), q = softmax(z_d / T) with the request's
+ *     temperature T ("RheoSampling 2026", §1 and §7).
+ *   - top-128 draft truncation: the draft logits keep their 128 largest
+ *     entries (ties to the lower id), the rest is -inf, then the softmax
+ *     ("RheoSampling 2026", §3).
+ *   - tree verification by recursive rejection sampling without replacement
+ *     over siblings ("RheoSampling 2026", §4).
+ *
+ * Random numbers. Every uniform is u = (splitmix64(seed ^ splitmix64(key))
+ * >> 40) * 2^-24 with key = (b << 32) | (pos << 8) | stream, where
+ * splitmix64(x) is the SplitMix64 output function (Steele, Lea & Flood 2014)
+ * of x + 0x9E3779B97F4A7C15. stream 0 = acceptance coin, 1 = residual draw,
+ * 2 = bonus draw. Linear: pos = 1-based position (coin of d_i at i, final
+ * draw at n+1). Tree: the coin of child c at pos = c (local node id), the
+ * final draw at node v at pos = v + 1. A draw at u picks the smallest token
+ * x (ascending id) with u * Z < C_x, C the inclusive prefix sum of the
+ * weights and Z their total.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller unless stated; the
+ *     library allocates nothing and keeps no state between calls. Logit and
+ *     probability buffers must be 16-byte aligned; rows are contiguous with
+ *     a row stride of V elements.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *   - A negative return value is a host-detected error; nothing was
+ *     launched. SPEC_OK means the work was enqueued.
+ *   - Errors found on the device (bad offsets, tokens out of range, a
+ *     temperature that is negative or NaN, a malformed tree, a bounded wait
+ *     that ran out) are written to a status word in the workspace; read it
+ *     with spec_get_status(). Outputs of the affected requests are then
+ *     unspecified.
+ *   - Logits must be finite or -inf; NaN is undefined behaviour. Each row
+ *     needs at least one finite logit.
+ *   - Deterministic: the same inputs and seed give the same bits.
+ *   - Calls that share a workspace must not overlap on the device.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *spec_stream_t;
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = -1, /* bad pointer, size, enum or input value      */
+  SPEC_ERR_UNSUPPORTED = -2, /* valid but outside this build's limits        */
+  SPEC_ERR_WORKSPACE = -3,   /* workspace NULL, misaligned or too small      */
+  SPEC_ERR_CUDA = -4,        /* a CUDA runtime call failed                   */
+  SPEC_ERR_TIMEOUT = -5      /* a bounded device-side wait ran out           */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+typedef enum {
+  SPEC_DRAFT_LOGITS = 0,    /* draft [R_d, V] logits; q = softmax(z/T)       */
+  SPEC_DRAFT_PROBS = 1,     /* draft [R_d, V] probabilities, used as given   */
+  SPEC_DRAFT_SPARSE128 = 2  /* draft [R_d, 128] f32 probs + draft_idx ids    */
+} spec_draft_kind;
+
+typedef enum {
+  SPEC_RULE_STRICT = 0,       /* lossless; requests with T < 0.05 greedy     */
+  SPEC_RULE_GREEDY = 1,       /* every request greedy                        */
+  SPEC_RULE_STRICT_TOP128 = 2 /* lossless, dense draft logits cut to top-128 */
+} spec_rule;
+
+#define SPEC_TOPK 128
+#define SPEC_MAX_K 256          /* drafts per request                        */
+#define SPEC_MAX_V (1 << 24)    /* vocabulary size                           */
+#define SPEC_MAX_TREE_NODES 4096 /* nodes per tree                           */
+#define SPEC_MAX_TREE_DEPTH 64
+#define SPEC_MAX_TREE_BRANCH 64
+#define SPEC_GREEDY_T 0.05f
+
+/* Human-readable name of a spec_status value (static string). */
+const char *spec_status_string(int status);
+
+/* Bytes of workspace spec_verify_linear needs for at most B requests of at
+ * most max_k drafts each over a vocabulary of V (0 on invalid sizes). */
+size_t spec_verify_linear_workspace(int B, int max_k, int V, int rule);
+
+/*
+ * Linear verification of B requests.
+ *
+ *   target       [R_t, V] logits (tdt), R_t = cu_draft[B] + B. Request b's
+ *                rows p_1..p_{K+1} start at row cu_draft[b] + b.
+ *   draft        dk == LOGITS: [R_d, V] logits (ddt); PROBS: [R_d, V]
+ *                probabilities (ddt), no temperature applied; SPARSE128:
+ *                [R_d, 128] f32 probabilities (ddt must be SPEC_F32).
+ *                R_d = cu_draft[B]; request b's rows start at cu_draft[b].
+ *                May be NULL when every request is greedy.
+ *   draft_idx    SPARSE128 only: [R_d, 128] int32 token ids (-1 = empty
+ *                slot, any order, no duplicates); NULL otherwise.
+ *   draft_tokens [R_d] int32 in [0, V).
+ *   cu_draft     [B+1] int32, cu_draft[0] = 0, 0 <= K_b <= max_k.
+ *   temperature  [B] f32, >= 0; T < 0.05 makes the request greedy.
+ *   rule         spec_rule. SPEC_RULE_STRICT_TOP128 needs dk == LOGITS.
+ *   out_tokens   [B, max_k+1] int32: d_1..d_n, the final token, then -1.
+ *   out_accepted [B] int32: n, the number of accepted drafts.
+ *   out_pq       optional [R_d, 2] f32 {p_i(d_i), q_i(d_i)} for every draft
+ *                position (also after the first rejection); greedy
+ *                requests give {1 if d_i == argmax p_i else 0, -1}. NULL to
+ *                skip.
+ *   workspace    device scratch, >= spec_verify_linear_workspace(...) bytes,
+ *                256-byte aligned, contents need no initialisation.
+ * Returns SPEC_OK or a negative spec_status.
+ */
+int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
+                       int dk, const int32_t *draft_idx,
+                       const int32_t *draft_tokens, const int32_t *cu_draft,
+                       const float *temperature, int B, int V, int max_k,
+                       uint64_t seed, int rule, int32_t *out_tokens,
+                       int32_t *out_accepted, float *out_pq, void *workspace,
+                       size_t ws_bytes, spec_stream_t stream);
+
+/* Bytes of workspace spec_verify_tree needs (0 on invalid sizes). */
+size_t spec_verify_tree_workspace(int B, int n_nodes, int V, int max_depth,
+                                  int max_branch);
+
+/*
+ * Tree verification (RRSw) of B request trees.
+ *
+ *   target      [n_nodes, V] logits (tdt). Row n is the target law after the
+ *               path root..n ("RheoSampling 2026", §4).
+ *   draft       [n_nodes, V] logits (dk == LOGITS) or probabilities
+ *               (dk == PROBS) (ddt). Row n is the law node n's children were
+ *               drawn from, without replacement; rows of leaves are unused.
+ *               May be NULL when every tree is greedy.
+ *   node_token  [n_nodes] int32: the token of each node (roots unused).
+ *   parent      [n_nodes] int32: LOCAL parent id, -1 for the root (local
+ *               node 0); parent[c] < c. Siblings carry distinct tokens, in
+ *               the order they were drawn.
+ *   cu_nodes    [B+1] int32 node offsets, cu_nodes[B] = n_nodes, at most
+ *               SPEC_MAX_TREE_NODES nodes per tree.
+ *   max_depth   bound on the depth of every tree (out width max_depth+1).
+ *   max_branch  bound on the children of any node.
+ *   out_tokens  [B, max_depth+1] int32: accepted path tokens, the final
+ *               token, then -1.
+ *   out_accepted [B] int32: number of accepted nodes.
+ *   out_path    [B, max_depth+1] int32: local ids of the accepted nodes, -1
+ *               padded. May be NULL.
+ */
+int spec_verify_tree(const void *target, int tdt, const void *draft, int ddt,
+                     int dk, const int32_t *node_token, const int32_t *parent,
+                     const int32_t *cu_nodes, const float *temperature, int B,
+                     int n_nodes, int V, int max_depth, int max_branch,
+                     uint64_t seed, int32_t *out_tokens, int32_t *out_accepted,
+                     int32_t *out_path, void *workspace, size_t ws_bytes,
+                     spec_stream_t stream);
+
+/* Bytes of workspace draft_topk_softmax needs (0 on invalid sizes). */
+size_t draft_topk_softmax_workspace(int rows, int V);
+
+/*
+ * Sparse top-128 draft law ("RheoSampling 2026", §3): for every draft row the
+ * ids of its 128 largest logits (ties to the lower id) in ascending id order,
+ * and softmax(z/T) over those 128 only. Rows of request b (cu_rows[b] ..
+ * cu_rows[b+1]-1) use temperature[b]; T < 0.05 gives probability 1 on the
+ * argmax. When V < 128 the tail slots hold id -1 and probability 0.
+ *
+ *   draft_logits [rows, V] (dt); cu_rows [B+1] int32 with cu_rows[B] = rows;
+ *   k must be 128; out_idx [rows, 128] int32; out_prob [rows, 128] f32.
+ */
+int draft_topk_softmax(const void *draft_logits, int dt, int rows, int V,
+                       const int32_t *cu_rows, const float *temperature, int B,
+                       int k, int32_t *out_idx, float *out_prob,
+                       void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/*
+ * Synchronises `stream` and reads the device status word that the last call
+ * using `workspace` left: *device_status = SPEC_OK or a negative spec_status.
+ * Returns SPEC_OK or SPEC_ERR_CUDA / SPEC_ERR_INVALID_ARG.
+ */
+int spec_get_status(const void *workspace, spec_stream_t stream,
+                    int *device_status);
+
+/*
+ * The uniforms the verifier draws: out[i] = u(seed, b[i], pos[i], stream[i])
+ * as defined above (device arrays of length n). For reproducing or auditing
+ * a verification.
+ */
+int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos,
+                  const int32_t *stream_id, int n, float *out,
+                  spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,250 @@
+"""GB300-native batched speculative-decoding verifier.
+
+Thin Python binding over the C ABI in include/specverify.h: the functions here
+only marshal arguments (device pointers of torch tensors, the current CUDA
+stream) and raise on a non-zero return code. Every step of the verification
+runs in the CUDA kernels of libspecverify.so; there is no CPU fallback. If
+the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from pathlib import Path
+
+__all__ = [
+    "SPEC_OK", "SPEC_F32", "SPEC_BF16", "SPEC_DRAFT_LOGITS", "SPEC_DRAFT_PROBS",
+    "SPEC_DRAFT_SPARSE128", "SPEC_RULE_STRICT", "SPEC_RULE_GREEDY",
+    "SPEC_RULE_STRICT_TOP128", "SPEC_TOPK", "lib", "spec_status_string",
+    "spec_verify_linear", "spec_verify_linear_workspace", "spec_verify_tree",
+    "spec_verify_tree_workspace", "draft_topk_softmax",
+    "draft_topk_softmax_workspace", "spec_get_status", "spec_uniforms",
+    "SpecError",
+]
+
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = -1
+SPEC_ERR_UNSUPPORTED = -2
+SPEC_ERR_WORKSPACE = -3
+SPEC_ERR_CUDA = -4
+SPEC_ERR_TIMEOUT = -5
+SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS, SPEC_DRAFT_SPARSE128 = 0, 1, 2
+SPEC_RULE_STRICT, SPEC_RULE_GREEDY, SPEC_RULE_STRICT_TOP128 = 0, 1, 2
+SPEC_TOPK = 128
+
+LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
+HEADER = Path(__file__).resolve().parent.parent / "include" / "specverify.h"
+
+_lib = None
+_vp, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+_SIGS = {
+    "spec_status_string": (ctypes.c_char_p, [_i32]),
+    "spec_verify_linear_workspace": (_sz, [_i32, _i32, _i32, _i32]),
+    "spec_verify_linear": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
+                                  _i32, _u64, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify_tree_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "spec_verify_tree": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
+                                _i32, _i32, _i32, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "draft_topk_softmax_workspace": (_sz, [_i32, _i32]),
+    "draft_topk_softmax": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp,
+                                  _sz, _vp]),
+    "spec_get_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+    "spec_uniforms": (_i32, [_u64, _vp, _vp, _vp, _i32, _vp, _vp]),
+}
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {spec_status_string(code)} ({code})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH.name} is not built; run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(str(LIB_PATH))
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/specverify.h declares."""
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def spec_status_string(code: int) -> str:
+    return lib().spec_status_string(int(code)).decode()
+
+
+# ------------------------------------------------------------ marshalling
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the verifier must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the verifier must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != SPEC_OK:
+        raise SpecError(code, where)
+
+
+def _workspace(nbytes: int, device, workspace=None):
+    torch = _torch()
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def spec_verify_linear_workspace(B: int, max_k: int, V: int, rule: int = SPEC_RULE_STRICT) -> int:
+    return int(lib().spec_verify_linear_workspace(B, max_k, V, rule))
+
+
+def spec_verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed: int, *,
+                       max_k: int, rule: int = SPEC_RULE_STRICT,
+                       draft_kind: int = SPEC_DRAFT_LOGITS, draft_idx=None, want_pq=False,
+                       workspace=None, out=None, stream=None):
+    """Verifies a batch of linear drafts on the GPU.
+
+    Returns (tokens [B, max_k+1] int32, accepted [B] int32, pq [R_d, 2] or
+    None, workspace). See include/specverify.h for the semantics.
+    """
+    torch = _torch()
+    B = cu_draft.numel() - 1
+    V = target.shape[1]
+    dev = target.device
+    ws_bytes = spec_verify_linear_workspace(B, max_k, V, rule)
+    if ws_bytes == 0:
+        raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_linear_workspace")
+    ws = _workspace(ws_bytes, dev, workspace)
+    if out is None:
+        tokens = torch.empty(B, max_k + 1, dtype=torch.int32, device=dev)
+        accepted = torch.empty(B, dtype=torch.int32, device=dev)
+        pq = torch.empty(draft_tokens.numel(), 2, dtype=torch.float32, device=dev) if want_pq else None
+    else:
+        tokens, accepted, pq = out
+    ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
+    code = lib().spec_verify_linear(
+        _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(draft_idx),
+        _ptr(draft_tokens), _ptr(cu_draft), _ptr(temperature), B, V, max_k,
+        ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), rule, _ptr(tokens), _ptr(accepted),
+        _ptr(pq), _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check(code, "spec_verify_linear")
+    return tokens, accepted, pq, ws
+
+
+def spec_verify_tree_workspace(B: int, n_nodes: int, V: int, max_depth: int, max_branch: int) -> int:
+    return int(lib().spec_verify_tree_workspace(B, n_nodes, V, max_depth, max_branch))
+
+
+def spec_verify_tree(target, draft, node_token, parent, cu_nodes, temperature, seed: int, *,
+                     max_depth: int, max_branch: int, draft_kind: int = SPEC_DRAFT_LOGITS,
+                     workspace=None, out=None, stream=None):
+    """Verifies a batch of draft trees (RRSw) on the GPU.
+
+    Returns (tokens [B, max_depth+1], accepted [B], path [B, max_depth+1],
+    workspace).
+    """
+    torch = _torch()
+    B = cu_nodes.numel() - 1
+    n_nodes, V = target.shape
+    dev = target.device
+    ws_bytes = spec_verify_tree_workspace(B, n_nodes, V, max_depth, max_branch)
+    if ws_bytes == 0:
+        raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_tree_workspace")
+    ws = _workspace(ws_bytes, dev, workspace)
+    if out is None:
+        tokens = torch.empty(B, max_depth + 1, dtype=torch.int32, device=dev)
+        accepted = torch.empty(B, dtype=torch.int32, device=dev)
+        path = torch.empty(B, max_depth + 1, dtype=torch.int32, device=dev)
+    else:
+        tokens, accepted, path = out
+    ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
+    code = lib().spec_verify_tree(
+        _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(node_token),
+        _ptr(parent), _ptr(cu_nodes), _ptr(temperature), B, n_nodes, V, max_depth, max_branch,
+        ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), _ptr(tokens), _ptr(accepted), _ptr(path),
+        _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check(code, "spec_verify_tree")
+    return tokens, accepted, path, ws
+
+
+def draft_topk_softmax_workspace(rows: int, V: int) -> int:
+    return int(lib().draft_topk_softmax_workspace(rows, V))
+
+
+def draft_topk_softmax(draft_logits, cu_rows, temperature, *, workspace=None, out=None,
+                       stream=None):
+    """Top-128 ids (ascending) and softmax(z/T) over them for every row.
+    Returns (idx [rows, 128] int32, prob [rows, 128] f32, workspace)."""
+    torch = _torch()
+    rows, V = draft_logits.shape
+    B = cu_rows.numel() - 1
+    dev = draft_logits.device
+    ws = _workspace(draft_topk_softmax_workspace(rows, V), dev, workspace)
+    if out is None:
+        idx = torch.empty(rows, SPEC_TOPK, dtype=torch.int32, device=dev)
+        prob = torch.empty(rows, SPEC_TOPK, dtype=torch.float32, device=dev)
+    else:
+        idx, prob = out
+    code = lib().draft_topk_softmax(
+        _ptr(draft_logits), _dtype_code(draft_logits), rows, V, _ptr(cu_rows),
+        _ptr(temperature), B, SPEC_TOPK, _ptr(idx), _ptr(prob), _ptr(ws),
+        ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check(code, "draft_topk_softmax")
+    return idx, prob, ws
+
+
+def spec_get_status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the device status word."""
+    v = ctypes.c_int(0)
+    _check(lib().spec_get_status(_ptr(workspace), _stream(stream), ctypes.byref(v)),
+           "spec_get_status")
+    return v.value
+
+
+def spec_uniforms(seed: int, b, pos, stream_id, stream=None):
+    """The verifier's uniforms u(seed, b[i], pos[i], stream_id[i])."""
+    torch = _torch()
+    out = torch.empty(b.numel(), dtype=torch.float32, device=b.device)
+    _check(lib().spec_uniforms(ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), _ptr(b), _ptr(pos),
+                               _ptr(stream_id), b.numel(), _ptr(out), _stream(stream)),
+           "spec_uniforms")
+    return out

@@ -1,0 +1,252 @@
+// Shared device helpers of the verifier kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------- tiling
+constexpr int TILE_BYTES = 16384;   // one TMA bulk copy = one pipeline stage
+constexpr int CHUNK_BYTES = 65536;  // one unit of dynamic work in the row pass
+constexpr int NSTAGE = 6;           // pipeline depth per CTA (96 KB in flight)
+constexpr int RS_CONS_WARPS = 8;    // consumer warps of the row pass
+constexpr int RS_THREADS = 32 * (1 + RS_CONS_WARPS);
+constexpr int SAMPLE_THREADS = 1024;
+constexpr int SAMPLE_EPT = 16;      // contiguous elements per thread per tile
+constexpr int SAMPLE_TILE = SAMPLE_THREADS * SAMPLE_EPT;
+constexpr int MAX_SAMPLE_TILES = (SPEC_MAX_V + SAMPLE_TILE - 1) / SAMPLE_TILE;
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr unsigned long long WAIT_NS = 2000000000ull;  // bounded waits: 2 s
+
+enum ReqMode : int { MODE_SKIP = 0, MODE_GREEDY = 1, MODE_SAMPLE = 2 };
+
+// ------------------------------------------------------ workspace records
+struct WsHeader {        // first 256 bytes of every workspace
+  int status;            // device-side spec_status (0 = OK)
+  int detail;            // first offending request / row, -1 if none
+  unsigned int work;     // dynamic work counter of the row pass
+  int n_list;            // rows in the row-pass list
+  int pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+struct RowTask {         // one row streamed by the row pass
+  int slot;              // index into the partial-statistics array
+  int row;               // row index within its tensor
+  int which;             // 0 = target tensor, 1 = draft tensor
+  float c;               // log2(e)/T, 0 for argmax-only rows
+};
+
+struct Part {            // statistics of one chunk of one row
+  float m;               // max logit
+  float S;               // sum of 2^((z - m) c)
+  int idx;               // lowest index attaining m
+  int pad;
+};
+
+struct ReqInfo {         // per request, written by the setup kernel
+  int t0;                // first target row
+  int d0;                // first draft row
+  int K;                 // number of drafts
+  int mode;              // ReqMode
+  float c;               // log2(e)/T
+  int n;                 // accepted drafts (written by the accept kernel)
+  int pad[2];
+};
+
+struct RowStat { float m, S; int idx; };
+
+// --------------------------------------------------------------- status
+__device__ __forceinline__ void set_status(WsHeader *h, int code, int detail) {
+  if (atomicCAS(&h->status, 0, code) == 0) atomicExch(&h->detail, detail);
+}
+
+// ------------------------------------------------------ counter uniforms
+// SplitMix64 output function (Steele, Lea & Flood 2014) of x + gamma.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// u = top 24 bits of splitmix64(seed ^ splitmix64(key)) * 2^-24, exact in f32.
+__device__ __forceinline__ float uniform24(uint64_t seed, uint32_t b,
+                                           uint32_t pos, uint32_t stream) {
+  const uint64_t key = ((uint64_t)b << 32) | ((uint64_t)pos << 8) | stream;
+  const uint64_t h = splitmix64(seed ^ splitmix64(key));
+  return (float)(uint32_t)(h >> 40) * 5.9604644775390625e-8f;
+}
+
+// --------------------------------------------------------------- math
+__device__ __forceinline__ float ex2(float x) {   // MUFU 2^x
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float load_elem(const void *row, int dtype, long long i) {
+  if (dtype == SPEC_BF16) {
+    const uint16_t v = __ldg(reinterpret_cast<const unsigned short *>(row) + i);
+    return __uint_as_float((uint32_t)v << 16);
+  }
+  return __ldg(reinterpret_cast<const float *>(row) + i);
+}
+
+__device__ __forceinline__ int dtype_size(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
+
+// Merge (m, S, idx) statistics: m the max, S sum of 2^((z-m)c), idx the
+// lowest index attaining the max.
+__device__ __forceinline__ void merge_stat(float &m, float &S, int &idx, float m2,
+                                           float S2, int i2, float c) {
+  const float M = fmaxf(m, m2);
+  float s = 0.f;
+  if (m != -INFINITY) s += S * ex2((m - M) * c);
+  if (m2 != -INFINITY) s += S2 * ex2((m2 - M) * c);
+  if (m2 > m || (m2 == m && i2 < idx)) idx = i2;
+  m = M;
+  S = s;
+}
+
+__device__ __forceinline__ RowStat combine_parts(const Part *p, int n, float c) {
+  RowStat r{-INFINITY, 0.f, 0x7fffffff};
+  for (int i = 0; i < n; ++i) merge_stat(r.m, r.S, r.idx, p[i].m, p[i].S, p[i].idx, c);
+  return r;
+}
+
+// ----------------------------------------------------- block primitives
+// Exclusive prefix sum of one float per thread over the block; returns the
+// exclusive value, *total gets the block total (= excl of the last thread +
+// its value). `scratch` holds 33 floats. Ends with the block synchronised.
+__device__ __forceinline__ float block_excl_scan(float v, float *scratch, float *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  float x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    float w = lane < nw ? scratch[lane] : 0.f;
+    float s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    scratch[lane] = s - w;   // exclusive offset of each warp
+  }
+  __syncthreads();
+  float xe = __shfl_up_sync(0xffffffffu, x, 1);   // exact in-warp exclusive
+  if (lane == 0) xe = 0.f;
+  const float excl = scratch[warp] + xe;
+  if (threadIdx.x == blockDim.x - 1) scratch[32] = excl + v;
+  __syncthreads();
+  *total = scratch[32];
+  __syncthreads();
+  return excl;
+}
+
+__device__ __forceinline__ int block_excl_scan_int(int v, int *scratch, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? scratch[lane] : 0;
+    int s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    scratch[lane] = s - w;
+    if (lane == 31) scratch[32] = s;
+  }
+  __syncthreads();
+  const int excl = scratch[warp] + (x - v);
+  *total = scratch[32];
+  __syncthreads();
+  return excl;
+}
+
+// ------------------------------------------------- mbarrier / bulk copies
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase of `bar` with `parity` to complete, giving up after
+// WAIT_NS or once *abort is set. Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > WAIT_NS) return false;
+  }
+}
+// 1-D TMA bulk copy global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                        uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint4 lds128(const void *p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
+
+}  // namespace sv

@@ -1,0 +1,46 @@
+// Host-side interfaces between the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+struct WsHeader;
+struct RowTask;
+struct Part;
+
+// Arguments of the row-statistics pass: every listed row is split into
+// CHUNK_BYTES chunks; each consumer warp leaves one Part per chunk at
+// part[(slot * nch_max + chunk) * RS_CONS_WARPS + warp].
+struct RowPassArgs {
+  const char *base[2];      // target / draft tensor
+  long long row_bytes[2];   // V * element size
+  int dtype[2];
+  int nch[2];               // chunks per row of each tensor
+  int nch_max;
+  const RowTask *list;      // rows to stream (count in hdr->n_list)
+  WsHeader *hdr;
+  Part *part;
+};
+
+int num_sms();
+int launch_row_pass(const RowPassArgs &a, cudaStream_t stream);
+int nchunks(int V, int dtype);
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Top-128 select + softmax over draft rows. Row r belongs to the request b
+// with cu_rows[b] <= r < cu_rows[b+1]; rows >= cu_rows[B] are skipped.
+// When `req_mode` is non-NULL, rows of requests whose mode is not
+// sampling are skipped.
+int launch_topk128(const void *logits, int dtype, int rows_bound, int V,
+                   const int32_t *cu_rows, const float *temperature, int B,
+                   int32_t *out_idx, float *out_prob, WsHeader *hdr,
+                   cudaStream_t stream);
+
+bool aligned(const void *p, size_t a);
+
+}  // namespace sv

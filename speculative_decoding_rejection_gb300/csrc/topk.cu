@@ -1,0 +1,393 @@
+// Sparse top-128 draft law ("RheoSampling 2026", §3 "Optimasi Sparse
+// Top-128": the draft logits keep their 128 largest entries, the rest is set
+// to -inf, and the softmax runs over the survivors).
+//
+// One CTA per row. Logits map to order-preserving unsigned keys (-0 folded
+// onto +0, so equal floats give equal keys); d = key(max) - key counts down
+// from the row maximum. The 128-th smallest d is found by an 8-bit radix
+// select. Its first pass only histograms elements with d below one digit
+// (the few hundred keys just under the max), which is where the threshold of
+// a real logit row lies, so almost no shared-memory atomics are contended;
+// rows whose top 128 spread further fall back to a full top-digit pass. The
+// collection pass keeps every d below the threshold and the lowest ids among
+// the ties (a block scan over id-ordered tiles). The 128 survivors are sorted
+// by id (bitonic) and softmaxed at temperature T; T < 0.05 gives a one-hot on
+// the argmax. Rows are re-read from L2 after the first pass.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sv {
+
+constexpr int TK_THREADS = 512;
+constexpr int TK_EPT = 16;
+constexpr int TK_TILE = TK_THREADS * TK_EPT;
+
+struct TopkArgs {
+  const char *logits;
+  int dtype;
+  long long row_bytes;
+  int rows_bound;
+  int V;
+  const int32_t *cu;
+  const float *temp;
+  int B;
+  int32_t *out_idx;
+  float *out_prob;
+  WsHeader *hdr;
+};
+
+struct TopkSmem {
+  unsigned hist[256];
+  int scratch[33];
+  int sel_idx[SPEC_TOPK];
+  float sel_val[SPEC_TOPK];
+  float sel_e[SPEC_TOPK];
+  unsigned kmax;
+  unsigned prefix;
+  int need;
+  int lt_count;
+  int use_fallback;
+  float S;
+};
+
+__device__ __forceinline__ unsigned key_of(uint32_t bits, bool bf16) {
+  if (bf16) {
+    bits &= 0xffffu;
+    if (bits == 0x8000u) bits = 0;
+    return (bits & 0x8000u) ? (~bits & 0xffffu) : (bits | 0x8000u);
+  }
+  if (bits == 0x80000000u) bits = 0;
+  return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+}
+
+__device__ __forceinline__ float value_of_bits(uint32_t bits, bool bf16) {
+  return bf16 ? __uint_as_float((bits & 0xffffu) << 16) : __uint_as_float(bits);
+}
+
+__device__ __forceinline__ uint32_t load_bits(const char *row, bool bf16, int i) {
+  return bf16 ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + i)
+              : __ldg(reinterpret_cast<const uint32_t *>(row) + i);
+}
+
+// Calls f(bits, index) once for every element of the row, spread over the
+// block in no particular order (128-bit loads on the aligned interior).
+template <bool BF16, class F>
+__device__ __forceinline__ void for_each_elem(const char *row, int V, F &&f) {
+  constexpr int ESZ = BF16 ? 2 : 4, PER = 16 / ESZ;
+  const int mis = (int)((uintptr_t)row & 15);
+  const int head = min(V, mis ? (16 - mis) / ESZ : 0);
+  const int nvec = (V - head) / PER;
+  const int tail0 = head + nvec * PER;
+  for (int i = threadIdx.x; i < head; i += blockDim.x) f(load_bits(row, BF16, i), i);
+  const uint4 *vp = reinterpret_cast<const uint4 *>(row + (long long)head * ESZ);
+#pragma unroll 4
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    const uint4 w = __ldg(vp + v);
+    const int e = head + v * PER;
+    if (BF16) {
+      f(w.x & 0xffffu, e + 0); f(w.x >> 16, e + 1); f(w.y & 0xffffu, e + 2); f(w.y >> 16, e + 3);
+      f(w.z & 0xffffu, e + 4); f(w.z >> 16, e + 5); f(w.w & 0xffffu, e + 6); f(w.w >> 16, e + 7);
+    } else {
+      f(w.x, e + 0); f(w.y, e + 1); f(w.z, e + 2); f(w.w, e + 3);
+    }
+  }
+  for (int i = tail0 + threadIdx.x; i < V; i += blockDim.x) f(load_bits(row, BF16, i), i);
+}
+
+// Chooses the digit containing the need-th smallest element from sh.hist;
+// extends sh.prefix by it and lowers sh.need by the count below it.
+__device__ __forceinline__ void pick_digit(TopkSmem &sh) {
+  if (threadIdx.x == 0) {
+    unsigned cum = 0;
+    int g = 0;
+    for (; g < 255; ++g) {
+      if (cum + sh.hist[g] >= (unsigned)sh.need) break;
+      cum += sh.hist[g];
+    }
+    sh.prefix = (sh.prefix << 8) | (unsigned)g;
+    sh.need -= (int)cum;
+  }
+  __syncthreads();
+}
+
+template <bool BF16>
+__device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
+  constexpr int BITS = BF16 ? 16 : 32;
+  const char *row = a.logits + (long long)r * a.row_bytes;
+  const int V = a.V;
+  const int t = threadIdx.x;
+
+  // request of this row -> temperature
+  int lo = 0, hi = a.B;  // largest b with cu[b] <= r
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a.cu[mid] <= r) lo = mid; else hi = mid;
+  }
+  const float T = a.temp[lo];
+  const bool greedy = !(T >= SPEC_GREEDY_T);
+
+  const int ksel = min(SPEC_TOPK, V);
+  if (V <= SPEC_TOPK) {
+    if (t < SPEC_TOPK) {
+      sh.sel_idx[t] = t < V ? t : 0x7fffffff;
+      sh.sel_val[t] = t < V ? value_of_bits(load_bits(row, BF16, t), BF16) : -INFINITY;
+    }
+    __syncthreads();
+  } else {
+    // pass 1: the maximum key
+    if (t == 0) { sh.kmax = 0; sh.lt_count = 0; sh.prefix = 0; sh.need = SPEC_TOPK; }
+    for (int i = t; i < 256; i += blockDim.x) sh.hist[i] = 0;
+    __syncthreads();
+    unsigned km = 0;
+    for_each_elem<BF16>(row, V, [&](uint32_t bits, int) { km = max(km, key_of(bits, BF16)); });
+    atomicMax(&sh.kmax, km);
+    __syncthreads();
+    const unsigned kmax = sh.kmax;
+    // pass 2: fine histogram of the second digit over d < 2^(BITS-8)
+    for_each_elem<BF16>(row, V, [&](uint32_t bits, int) {
+      const unsigned d = kmax - key_of(bits, BF16);
+      if ((d >> (BITS - 8)) == 0) atomicAdd(&sh.hist[(d >> (BITS - 16)) & 0xffu], 1u);
+    });
+    __syncthreads();
+    if (t == 0) {
+      unsigned tot = 0;
+      for (int g = 0; g < 256; ++g) tot += sh.hist[g];
+      sh.use_fallback = tot < (unsigned)SPEC_TOPK;
+    }
+    __syncthreads();
+    int shift;
+    if (!sh.use_fallback) {
+      pick_digit(sh);  // the top digit is 0; this picks the second one
+      shift = BITS - 24;
+    } else {
+      // full top-digit pass (rows whose top 128 spread widely)
+      for (int i = t; i < 256; i += blockDim.x) sh.hist[i] = 0;
+      __syncthreads();
+      for_each_elem<BF16>(row, V, [&](uint32_t bits, int) {
+        atomicAdd(&sh.hist[(kmax - key_of(bits, BF16)) >> (BITS - 8)], 1u);
+      });
+      __syncthreads();
+      pick_digit(sh);
+      shift = BITS - 16;
+    }
+    for (; shift >= 0; shift -= 8) {
+      for (int i = t; i < 256; i += blockDim.x) sh.hist[i] = 0;
+      __syncthreads();
+      const unsigned pre = sh.prefix;
+      for_each_elem<BF16>(row, V, [&](uint32_t bits, int) {
+        const unsigned d = kmax - key_of(bits, BF16);
+        if ((d >> (shift + 8)) == pre) atomicAdd(&sh.hist[(d >> shift) & 0xffu], 1u);
+      });
+      __syncthreads();
+      pick_digit(sh);
+    }
+    // collection: d < thr anywhere; among d == thr the `need` lowest ids
+    const unsigned thr = sh.prefix;
+    const int need = sh.need;
+    const int c_lt = SPEC_TOPK - need;
+    int tie_base = 0;
+    const bool vec_ok = ((uintptr_t)row & 15) == 0;
+    for (int x0t = 0; x0t < V; x0t += TK_TILE) {
+      const int x0 = x0t + t * TK_EPT;
+      uint32_t bits[TK_EPT];
+      if (vec_ok && x0 + TK_EPT <= V) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(row + (long long)x0 * (BF16 ? 2 : 4));
+        if (BF16) {
+#pragma unroll
+          for (int q = 0; q < TK_EPT / 8; ++q) {
+            const uint4 w = __ldg(p + q);
+            bits[8 * q + 0] = w.x & 0xffffu; bits[8 * q + 1] = w.x >> 16;
+            bits[8 * q + 2] = w.y & 0xffffu; bits[8 * q + 3] = w.y >> 16;
+            bits[8 * q + 4] = w.z & 0xffffu; bits[8 * q + 5] = w.z >> 16;
+            bits[8 * q + 6] = w.w & 0xffffu; bits[8 * q + 7] = w.w >> 16;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < TK_EPT / 4; ++q) {
+            const uint4 w = __ldg(p + q);
+            bits[4 * q + 0] = w.x; bits[4 * q + 1] = w.y;
+            bits[4 * q + 2] = w.z; bits[4 * q + 3] = w.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < TK_EPT; ++k) bits[k] = x0 + k < V ? load_bits(row, BF16, x0 + k) : 0u;
+      }
+      int nt = 0;
+#pragma unroll
+      for (int k = 0; k < TK_EPT; ++k) {
+        if (x0 + k >= V) break;
+        const unsigned d = kmax - key_of(bits[k], BF16);
+        if (d < thr) {
+          const int slot = atomicAdd(&sh.lt_count, 1);
+          if (slot < SPEC_TOPK) {
+            sh.sel_idx[slot] = x0 + k;
+            sh.sel_val[slot] = value_of_bits(bits[k], BF16);
+          }
+        } else if (d == thr) {
+          ++nt;
+        }
+      }
+      int tot;
+      const int excl = block_excl_scan_int(nt, sh.scratch, &tot);
+      if (nt > 0) {
+        int rank = tie_base + excl;
+#pragma unroll
+        for (int k = 0; k < TK_EPT; ++k) {
+          if (x0 + k >= V) break;
+          if (kmax - key_of(bits[k], BF16) == thr) {
+            if (rank < need) {
+              sh.sel_idx[c_lt + rank] = x0 + k;
+              sh.sel_val[c_lt + rank] = value_of_bits(bits[k], BF16);
+            }
+            ++rank;
+          }
+        }
+      }
+      tie_base += tot;
+    }
+    __syncthreads();
+  }
+
+  // sort the survivors by id (bitonic over 128 slots; padding sorts last)
+  for (int size = 2; size <= SPEC_TOPK; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (t < SPEC_TOPK) {
+        const int p = t ^ stride;
+        if (p > t) {
+          const bool up = (t & size) == 0;
+          const int ia = sh.sel_idx[t], ib = sh.sel_idx[p];
+          if ((ia > ib) == up) {
+            sh.sel_idx[t] = ib; sh.sel_idx[p] = ia;
+            const float va = sh.sel_val[t];
+            sh.sel_val[t] = sh.sel_val[p]; sh.sel_val[p] = va;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // softmax over the survivors (fixed summation order); greedy: one-hot
+  if (t < 32) {
+    float m = -INFINITY;
+    for (int k = t; k < ksel; k += 32) m = fmaxf(m, sh.sel_val[k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (greedy) {
+      int first = 0x7fffffff;
+      for (int k = t; k < ksel; k += 32)
+        if (sh.sel_val[k] == m) first = min(first, k);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+      for (int k = t; k < SPEC_TOPK; k += 32) sh.sel_e[k] = k == first ? 1.f : 0.f;
+      if (t == 0) sh.S = 1.f;
+    } else {
+      const float c = (float)(1.4426950408889634 / (double)T);
+      float s = 0.f;
+      for (int k = t; k < SPEC_TOPK; k += 32) {
+        const float e = k < ksel ? ex2((sh.sel_val[k] - m) * c) : 0.f;
+        sh.sel_e[k] = e;
+        s += e;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (t == 0) sh.S = s;
+    }
+  }
+  __syncthreads();
+  if (t < SPEC_TOPK) {
+    const bool ok = t < ksel;
+    a.out_idx[(long long)r * SPEC_TOPK + t] = ok ? sh.sel_idx[t] : -1;
+    a.out_prob[(long long)r * SPEC_TOPK + t] = ok ? sh.sel_e[t] / sh.S : 0.f;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(TK_THREADS) k_topk128(const TopkArgs a) {
+  __shared__ TopkSmem sh;
+  if (a.hdr->status != SPEC_OK) return;   // inputs already rejected
+  const int rows = min(a.rows_bound, a.cu[a.B]);
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    if (a.dtype == SPEC_BF16) topk_row<true>(a, sh, r);
+    else topk_row<false>(a, sh, r);
+  }
+}
+
+__global__ void k_topk_validate(const TopkArgs a) {
+  // one block: reset the status word, check offsets and temperatures
+  if (threadIdx.x == 0) {
+    a.hdr->status = SPEC_OK;
+    a.hdr->detail = -1;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+    const int K = a.cu[b + 1] - a.cu[b];
+    const float T = a.temp[b];
+    if ((b == 0 && a.cu[0] != 0) || K < 0 || !(T >= 0.f) || !isfinite(T))
+      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+  }
+  if (threadIdx.x == 0 && a.cu[a.B] > a.rows_bound) set_status(a.hdr, SPEC_ERR_INVALID_ARG, a.B);
+}
+
+int launch_topk128(const void *logits, int dtype, int rows_bound, int V, const int32_t *cu_rows,
+                   const float *temperature, int B, int32_t *out_idx, float *out_prob,
+                   WsHeader *hdr, cudaStream_t stream) {
+  TopkArgs a;
+  a.logits = static_cast<const char *>(logits);
+  a.dtype = dtype;
+  a.row_bytes = (long long)V * (dtype == SPEC_BF16 ? 2 : 4);
+  a.rows_bound = rows_bound;
+  a.V = V;
+  a.cu = cu_rows;
+  a.temp = temperature;
+  a.B = B;
+  a.out_idx = out_idx;
+  a.out_prob = out_prob;
+  a.hdr = hdr;
+  if (rows_bound <= 0) return SPEC_OK;
+  const int sms = num_sms();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  const int grid = min(rows_bound, 4 * sms);
+  k_topk128<<<grid, TK_THREADS, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+constexpr size_t TOPK_WS = 256;
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t draft_topk_softmax_workspace(int rows, int V) {
+  if (rows < 0 || V <= 0 || V > SPEC_MAX_V) return 0;
+  return TOPK_WS;
+}
+
+extern "C" int draft_topk_softmax(const void *draft_logits, int dt, int rows, int V,
+                                  const int32_t *cu_rows, const float *temperature, int B,
+                                  int k, int32_t *out_idx, float *out_prob, void *workspace,
+                                  size_t ws_bytes, spec_stream_t stream) {
+  if (rows < 0 || B < 0 || V <= 0 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  if (k != SPEC_TOPK) return SPEC_ERR_UNSUPPORTED;
+  if (dt != SPEC_F32 && dt != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (cu_rows == nullptr || (B > 0 && temperature == nullptr)) return SPEC_ERR_INVALID_ARG;
+  if (rows > 0 && (draft_logits == nullptr || out_idx == nullptr || out_prob == nullptr))
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(draft_logits, 16) || !aligned(cu_rows, 4) || !aligned(temperature, 4) ||
+      !aligned(out_idx, 4) || !aligned(out_prob, 4))
+    return SPEC_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < TOPK_WS)
+    return SPEC_ERR_WORKSPACE;
+  WsHeader *hdr = static_cast<WsHeader *>(workspace);
+  TopkArgs a{};
+  a.cu = cu_rows;
+  a.temp = temperature;
+  a.B = B;
+  a.rows_bound = rows;
+  a.hdr = hdr;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  k_topk_validate<<<1, 256, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  return launch_topk128(draft_logits, dt, rows, V, cu_rows, temperature, B, out_idx, out_prob,
+                        hdr, st);
+}

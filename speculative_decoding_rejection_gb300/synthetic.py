@@ -35,14 +35,15 @@ VERIFY_SEED_BASE = 0x243F6A8885A308D3
 GREEDY_T = 0.05
 TOPK = 128
 
-# Named workloads. "sigma" / "T" may be a float, a list (per request) or a
-# ("uniform", lo, hi) tuple drawn per request.
+# Named workloads. "sigma" / "T" may be a float, a list (per request), a
+# ("uniform", lo, hi) tuple drawn per request, or ("halves", a, b): the first
+# half of the requests get a, the rest b.
 WORKLOADS = {
     1: dict(name="linear-strict-B4-K4-V1024-f32", kind="linear", B=4, K=4,
             V=1024, dtype="f32", sigma=0.5, T=1.0, top128=False),
     2: dict(name="linear-mixed-B64-K1..5-V32000-bf16", kind="linear", B=64,
             K=(1, 5), V=32000, dtype="bf16", sigma=0.7,
-            T=[0.0] * 32 + [0.7] * 32, top128=False),
+            T=("halves", 0.0, 0.7), top128=False),
     3: dict(name="linear-top128-B256-K7-V151936-bf16", kind="linear", B=256,
             K=7, V=151936, dtype="bf16", sigma=0.5, T=1.0, top128=True),
     4: dict(name="tree-rrsw-B32-N64-D6-W4-V128256-bf16", kind="tree", B=32,
@@ -59,6 +60,9 @@ _DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 def _per_request(spec, B, g, device):
     if isinstance(spec, (int, float)):
         return torch.full((B,), float(spec), dtype=torch.float32)
+    if isinstance(spec, tuple) and spec[0] == "halves":
+        return torch.tensor([spec[1]] * (B // 2) + [spec[2]] * (B - B // 2),
+                            dtype=torch.float32)
     if isinstance(spec, tuple) and spec[0] == "uniform":
         lo, hi = spec[1], spec[2]
         return lo + (hi - lo) * torch.rand(B, generator=g, device=device).cpu()

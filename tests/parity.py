@@ -1,0 +1,86 @@
+"""Helpers comparing the CUDA verifier with the CPU oracle on the same inputs.
+
+Tolerances: committed tokens and accepted counts bit-exact, except from the
+first output slot whose draw the oracle flags as within 1e-6 of a decision
+boundary; probabilities within 1e-5 relative (fp32 GPU vs fp64 oracle).
+"""
+import numpy as np
+import torch
+
+import speculative_decoding_rejection_gb300 as sv
+from oracle import spec_oracle as O
+
+PROB_RTOL = 1e-5
+PROB_ATOL = 1e-30
+
+
+def gpu_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, draft=None,
+               draft_idx=None):
+    draft = lb.draft if draft is None else draft
+    tokens, acc, pq, ws = sv.spec_verify_linear(
+        lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
+        max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx, want_pq=True)
+    status = sv.spec_get_status(ws)
+    return dict(tokens=tokens.cpu().numpy(), accepted=acc.cpu().numpy(),
+                pq=pq.cpu().numpy().astype(np.float64), status=status)
+
+
+def oracle_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, draft=None,
+                  draft_idx=None, requests=None):
+    draft = lb.draft if draft is None else draft
+    host = (lambda t: t.cpu()) if requests is None else (lambda t: t)
+    return O.verify_linear(host(lb.target), host(draft), lb.draft_tokens.cpu().numpy(),
+                           lb.cu_draft.cpu().numpy(), lb.temperature.cpu().numpy(), lb.seed,
+                           rule=rule, draft_kind=draft_kind,
+                           draft_idx=None if draft_idx is None else draft_idx.cpu().numpy(),
+                           max_k=lb.max_k, requests=requests)
+
+
+def assert_probs_close(g, o, what="probabilities"):
+    g = np.asarray(g, np.float64)
+    o = np.asarray(o, np.float64)
+    bad = np.abs(g - o) > PROB_RTOL * np.abs(o) + PROB_ATOL
+    assert not bad.any(), (what, np.argwhere(bad)[:5], g[bad][:5], o[bad][:5])
+
+
+def assert_linear_parity(gpu, ref, cu_draft, min_compared=1):
+    """Token/accepted parity per request, skipping from the first flagged slot;
+    p(d), q(d) parity for every draft position of the compared requests.
+    Returns (n_requests_fully_compared, n_flagged)."""
+    cu = np.asarray(cu_draft)
+    n_full = n_flag = 0
+    rows = []
+    for j, b in enumerate(ref["requests"]):
+        fs = int(ref["flag_slot"][j])
+        gt, rt = gpu["tokens"][b], ref["tokens"][j]
+        if fs < 0:
+            assert np.array_equal(gt, rt), (b, gt, rt)
+            assert gpu["accepted"][b] == ref["accepted"][j], (b, gpu["accepted"][b], ref["accepted"][j])
+            n_full += 1
+        else:
+            assert np.array_equal(gt[:fs], rt[:fs]), (b, fs, gt, rt)
+            n_flag += 1
+        rows.extend(range(int(cu[b]), int(cu[b + 1])))
+    rows = np.asarray(rows, dtype=np.int64)
+    if rows.size:
+        assert_probs_close(gpu["pq"][rows], ref["pq"][rows], "p(d), q(d)")
+    assert n_full >= min_compared
+    return n_full, n_flag
+
+
+def sample_requests(B, n, seed=0):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(B, size=min(n, B), replace=False))
+
+
+def probs_from_logits(draft, cu, temperature):
+    """Draft probabilities softmax(z/T) for the PROBS draft kind (input
+    preparation with torch; T < 0.05 rows get a one-hot on the argmax)."""
+    cu = cu.long().cpu()
+    T = temperature.cpu()
+    req = torch.repeat_interleave(torch.arange(T.numel()), torch.diff(cu)).to(draft.device)
+    Tr = T.to(draft.device)[req]
+    z = draft.float()
+    soft = torch.softmax(z / torch.clamp(Tr, min=0.05)[:, None], dim=1)
+    hard = torch.nn.functional.one_hot(torch.argmax(z, 1), z.shape[1]).float()
+    return torch.where((Tr < 0.05)[:, None], hard, soft).contiguous()

@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function the header declares, sizes its workspaces, and rejects bad
+arguments before launching anything."""
+import ctypes
+
+import pytest
+
+import speculative_decoding_rejection_gb300 as sv
+
+
+@pytest.fixture(scope="module")
+def L():
+    try:
+        return sv.lib()
+    except RuntimeError as e:
+        pytest.fail(f"library not built: {e}")
+
+
+def test_exports_every_declared_function(L):
+    names = sv.header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(sv._SIGS)
+
+
+def test_status_strings(L):
+    for code, name in [(0, "SPEC_OK"), (-1, "SPEC_ERR_INVALID_ARG"), (-3, "SPEC_ERR_WORKSPACE"),
+                       (-5, "SPEC_ERR_TIMEOUT"), (7, "SPEC_ERR_UNKNOWN")]:
+        assert sv.spec_status_string(code) == name
+
+
+def test_workspace_sizes():
+    assert sv.spec_verify_linear_workspace(1024, 4, 201088) > 0
+    assert sv.spec_verify_linear_workspace(4, 4, 1024, sv.SPEC_RULE_STRICT_TOP128) > \
+        sv.spec_verify_linear_workspace(4, 4, 1024, sv.SPEC_RULE_STRICT)
+    assert sv.spec_verify_linear_workspace(-1, 4, 100) == 0
+    assert sv.spec_verify_linear_workspace(4, 4, 0) == 0
+    assert sv.spec_verify_linear_workspace(4, 100000, 100) == 0
+    assert sv.draft_topk_softmax_workspace(10, 1000) > 0
+    assert sv.draft_topk_softmax_workspace(10, 0) == 0
+
+
+FAKE = 1 << 20   # a 256-byte-aligned non-null value; never dereferenced
+
+
+def lin(L, **kw):
+    args = dict(target=FAKE, tdt=1, draft=FAKE, ddt=1, dk=0, draft_idx=None, tokens=FAKE,
+                cu=FAKE, temp=FAKE, B=4, V=1000, max_k=4, seed=1, rule=0, out_tokens=FAKE,
+                out_acc=FAKE, out_pq=None, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    args.update(kw)
+    return L.spec_verify_linear(*args.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=(1 << 24) + 1), sv.SPEC_ERR_INVALID_ARG),
+    (dict(max_k=-1), sv.SPEC_ERR_INVALID_ARG),
+    (dict(max_k=257), sv.SPEC_ERR_UNSUPPORTED),
+    (dict(tdt=5), sv.SPEC_ERR_INVALID_ARG),
+    (dict(dk=3), sv.SPEC_ERR_INVALID_ARG),
+    (dict(rule=9), sv.SPEC_ERR_INVALID_ARG),
+    (dict(rule=2, dk=1), sv.SPEC_ERR_INVALID_ARG),
+    (dict(dk=2, ddt=1, draft_idx=FAKE), sv.SPEC_ERR_INVALID_ARG),
+    (dict(dk=2, ddt=0, draft_idx=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(target=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(tokens=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(target=FAKE + 8), sv.SPEC_ERR_INVALID_ARG),
+    (dict(out_pq=FAKE + 2), sv.SPEC_ERR_INVALID_ARG),
+    (dict(ws=None), sv.SPEC_ERR_WORKSPACE),
+    (dict(ws=FAKE + 128), sv.SPEC_ERR_WORKSPACE),
+    (dict(ws_bytes=100), sv.SPEC_ERR_WORKSPACE),
+])
+def test_linear_rejects_bad_arguments_on_the_host(L, kw, code):
+    assert lin(L, **kw) == code
+
+
+def test_topk_rejects_bad_arguments_on_the_host(L):
+    f = L.draft_topk_softmax
+    ok = dict(logits=FAKE, dt=1, rows=8, V=1000, cu=FAKE, temp=FAKE, B=2, k=128, idx=FAKE,
+              prob=FAKE, ws=FAKE, ws_bytes=256, stream=None)
+    for kw, code in [(dict(k=64), sv.SPEC_ERR_UNSUPPORTED), (dict(V=0), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(dt=4), sv.SPEC_ERR_INVALID_ARG), (dict(cu=None), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(logits=FAKE + 4), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(ws=None), sv.SPEC_ERR_WORKSPACE), (dict(ws_bytes=8), sv.SPEC_ERR_WORKSPACE)]:
+        a = dict(ok)
+        a.update(kw)
+        assert f(*a.values()) == code, kw
+
+
+def test_status_and_uniform_argument_checks(L):
+    v = ctypes.c_int(0)
+    assert L.spec_get_status(None, None, ctypes.byref(v)) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_get_status(FAKE + 4, None, ctypes.byref(v)) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_uniforms(1, None, None, None, -1, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_uniforms(1, None, None, None, 0, None, None) == sv.SPEC_OK
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(sv, "_lib", None)
+    monkeypatch.setattr(sv, "LIB_PATH", tmp_path / "missing.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        sv.lib()

@@ -1,0 +1,207 @@
+"""Parity of the CUDA linear verifier (through the C ABI) with the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_rejection_gb300 as sv
+from oracle import spec_oracle as O
+from speculative_decoding_rejection_gb300 import synthetic as S
+
+from parity import (assert_linear_parity, assert_probs_close, gpu_linear, oracle_linear,
+                    probs_from_logits, sample_requests)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _lib():
+    sv.lib()
+
+
+def test_device_uniforms_equal_the_oracle_hash():
+    rng = np.random.default_rng(0)
+    n = 4096
+    b = rng.integers(0, 1 << 31, n)
+    pos = rng.integers(0, 1 << 24, n)
+    st = rng.integers(0, 3, n)
+    seed = 0x243F6A8885A308D3
+    got = sv.spec_uniforms(seed, *(torch.tensor(x, dtype=torch.int32, device=DEV)
+                                   for x in (b, pos, st))).cpu().numpy()
+    want = np.array([O.uniform(seed, int(x), int(y), int(z)) for x, y, z in zip(b, pos, st)])
+    assert np.array_equal(got.astype(np.float64), want)
+
+
+def test_workload1_full():
+    lb = S.make_linear(1, device=DEV)
+    g = gpu_linear(lb)
+    assert g["status"] == sv.SPEC_OK
+    r = oracle_linear(lb)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=3)
+
+
+def test_workload2_full_mixed_greedy_and_sampling():
+    lb = S.make_linear(2, device=DEV)
+    g = gpu_linear(lb)
+    assert g["status"] == sv.SPEC_OK
+    r = oracle_linear(lb)
+    n_full, n_flag = assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=60)
+    # greedy half: argmax prefix, cross-checked against a direct argmax
+    tgt = lb.target.float()
+    cu = lb.cu_draft.cpu().numpy()
+    for b in range(32):
+        t0, K = cu[b] + b, cu[b + 1] - cu[b]
+        am = torch.argmax(tgt[t0:t0 + K + 1], 1).cpu().numpy()
+        d = lb.draft_tokens[cu[b]:cu[b + 1]].cpu().numpy()
+        n = 0
+        while n < K and d[n] == am[n]:
+            n += 1
+        assert g["accepted"][b] == n and g["tokens"][b][n] == am[n]
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 5003), ("f32", 4099), ("bf16", 100003),
+                                     ("f32", 50001), ("bf16", 7)])
+def test_ragged_batches_unaligned_rows_and_multiple_chunks(dtype, V):
+    T = [0.0, 0.04, 0.05, 0.3, 0.7, 1.0, 1.6, 2.5] * 5
+    lb = S.make_linear(2, device=DEV, B=40, K=(0, 7), V=V, dtype=dtype, sigma=0.8, T=T,
+                       input_seed=1234 + V)
+    assert int(torch.diff(lb.cu_draft).min()) == 0      # includes K = 0
+    g = gpu_linear(lb)
+    assert g["status"] == sv.SPEC_OK
+    r = oracle_linear(lb)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=30)
+
+
+def test_mixed_target_and_draft_dtypes():
+    lb = S.make_linear(1, device=DEV, B=12, K=5, V=3001, dtype="bf16", input_seed=77)
+    draft32 = lb.draft.float().contiguous()
+    g = gpu_linear(lb, draft=draft32)
+    r = oracle_linear(lb, draft=draft32)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=10)
+
+
+def test_draft_given_as_probabilities():
+    lb = S.make_linear(2, device=DEV, B=24, K=(1, 6), V=20000, input_seed=5,
+                       T=[0.0, 0.8, 1.2] * 8)
+    probs = probs_from_logits(lb.draft, lb.cu_draft, lb.temperature)
+    g = gpu_linear(lb, draft_kind=sv.SPEC_DRAFT_PROBS, draft=probs)
+    r = oracle_linear(lb, draft_kind=sv.SPEC_DRAFT_PROBS, draft=probs)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=20)
+
+
+def test_sparse_draft_in_any_order_with_empty_slots():
+    lb = S.make_linear(3, device=DEV, B=20, K=4, V=9000, input_seed=9)
+    R_d = lb.draft.shape[0]
+    gen = torch.Generator(device=DEV).manual_seed(3)
+    top = torch.topk(lb.draft.float(), 128, dim=1).indices
+    perm = torch.argsort(torch.rand(R_d, 128, generator=gen, device=DEV), dim=1)
+    idx = torch.gather(top, 1, perm).to(torch.int32)
+    idx[:, 120:] = -1                                     # some empty slots
+    w = torch.rand(R_d, 128, generator=gen, device=DEV) * (idx >= 0)
+    prob = (w / w.sum(1, keepdim=True)).contiguous()
+    # drafts drawn from the sparse law
+    pick = torch.multinomial(prob, 1, generator=gen).squeeze(1)
+    lb.draft_tokens = torch.gather(idx, 1, pick[:, None]).squeeze(1).contiguous()
+    g = gpu_linear(lb, draft_kind=sv.SPEC_DRAFT_SPARSE128, draft=prob, draft_idx=idx.contiguous())
+    r = oracle_linear(lb, draft_kind=sv.SPEC_DRAFT_SPARSE128, draft=prob, draft_idx=idx)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=15)
+
+
+def test_top128_rule_reduced_workload3():
+    lb = S.make_linear(3, device=DEV, B=24, K=7, V=20011, input_seed=31)
+    g = gpu_linear(lb, rule=sv.SPEC_RULE_STRICT_TOP128)
+    assert g["status"] == sv.SPEC_OK
+    r = oracle_linear(lb, rule=sv.SPEC_RULE_STRICT_TOP128)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=20)
+
+
+def test_greedy_rule_forces_prefix_matching():
+    lb = S.make_linear(1, device=DEV, B=16, K=6, V=2048, input_seed=4)
+    g = gpu_linear(lb, rule=sv.SPEC_RULE_GREEDY)
+    r = oracle_linear(lb, rule=sv.SPEC_RULE_GREEDY)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=16)
+    assert np.all(g["pq"][:, 1] == -1.0)
+
+
+def test_vocabulary_of_one_token():
+    lb = S.make_linear(1, device=DEV, B=3, K=2, V=1, input_seed=2)
+    lb.draft_tokens.zero_()
+    g = gpu_linear(lb)
+    assert np.all(g["accepted"] == 2) and np.all(g["tokens"][:, :3] == 0)
+
+
+def test_repeat_calls_are_bitwise_deterministic():
+    lb = S.make_linear(2, device=DEV, B=32, V=12000, input_seed=8)
+    a, b = gpu_linear(lb), gpu_linear(lb)
+    assert np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["pq"], b["pq"])
+
+
+def test_invalid_device_inputs_set_the_status_word():
+    lb = S.make_linear(1, device=DEV, B=4, K=3, V=512, input_seed=3)
+    bad_cu = lb.cu_draft.clone()
+    bad_cu[2] = bad_cu[1] - 1                             # negative draft count
+    _, acc, _, ws = sv.spec_verify_linear(lb.target, lb.draft, lb.draft_tokens, bad_cu,
+                                          lb.temperature, 1, max_k=lb.max_k)
+    assert sv.spec_get_status(ws) == sv.SPEC_ERR_INVALID_ARG
+    assert torch.all(acc == -1)
+    bad_tok = lb.draft_tokens.clone()
+    bad_tok[1] = 10 ** 6
+    _, _, _, ws = sv.spec_verify_linear(lb.target, lb.draft, bad_tok, lb.cu_draft,
+                                        lb.temperature, 1, max_k=lb.max_k)
+    assert sv.spec_get_status(ws) == sv.SPEC_ERR_INVALID_ARG
+    bad_T = lb.temperature.clone()
+    bad_T[0] = float("nan")
+    _, _, _, ws = sv.spec_verify_linear(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
+                                        bad_T, 1, max_k=lb.max_k)
+    assert sv.spec_get_status(ws) == sv.SPEC_ERR_INVALID_ARG
+    # a good call on the same workspace clears the word
+    _, _, _, ws = sv.spec_verify_linear(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
+                                        lb.temperature, 1, max_k=lb.max_k, workspace=ws)
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+
+
+@pytest.mark.parametrize("cfg,n", [(3, 24), (5, 24)])
+def test_full_size_workloads_on_sampled_requests(cfg, n):
+    lb = S.make_linear(cfg, device=DEV)
+    rule = sv.SPEC_RULE_STRICT_TOP128 if lb.top128 else sv.SPEC_RULE_STRICT
+    g = gpu_linear(lb, rule=rule)
+    assert g["status"] == sv.SPEC_OK
+    req = sample_requests(lb.B, n, seed=cfg)
+    if cfg == 5:   # make sure greedy requests are among the sample
+        greedy = np.nonzero(lb.temperature.cpu().numpy() < 0.05)[0][:4]
+        req = np.unique(np.concatenate([req, greedy]))
+    r = oracle_linear(lb, rule=rule, requests=req)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=n - 3)
+    # whole-batch invariants at full size
+    acc = g["accepted"]
+    K = np.diff(lb.cu_draft.cpu().numpy())
+    assert np.all((acc >= 0) & (acc <= K))
+    tok = g["tokens"]
+    for b in range(lb.B):
+        assert np.all(tok[b, :acc[b] + 1] >= 0) and np.all(tok[b, :acc[b] + 1] < lb.V)
+        assert np.all(tok[b, acc[b] + 1:] == -1)
+
+
+def test_draft_topk_softmax_matches_oracle():
+    lb = S.make_linear(3, device=DEV, B=10, K=7, V=151936, input_seed=12)
+    idx, prob, ws = sv.draft_topk_softmax(lb.draft, lb.cu_draft, lb.temperature)
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    ri, rp = O.draft_topk_softmax(lb.draft.cpu(), lb.cu_draft.cpu().numpy(),
+                                  lb.temperature.cpu().numpy())
+    assert np.array_equal(idx.cpu().numpy(), ri)
+    assert_probs_close(prob.cpu().numpy(), rp, "top-128 probabilities")
+
+
+@pytest.mark.parametrize("dtype,V,T", [("bf16", 100, 1.0), ("f32", 3000, 0.7),
+                                       ("bf16", 777, 0.0), ("f32", 129, 2.0)])
+def test_draft_topk_softmax_edge_cases(dtype, V, T):
+    g = torch.Generator(device=DEV).manual_seed(V)
+    z = torch.randn(9, V, generator=g, device=DEV)
+    z = (torch.round(z * 3) / 3).to(S._DTYPES[dtype])    # many exact ties
+    cu = torch.tensor([0, 4, 9], dtype=torch.int32, device=DEV)
+    temp = torch.tensor([T, T], device=DEV)
+    idx, prob, ws = sv.draft_topk_softmax(z.contiguous(), cu, temp)
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    ri, rp = O.draft_topk_softmax(z.cpu(), cu.cpu().numpy(), temp.cpu().numpy())
+    assert np.array_equal(idx.cpu().numpy(), ri)
+    assert_probs_close(prob.cpu().numpy(), rp, "top-128 probabilities")
