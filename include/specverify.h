@@ -213,6 +213,17 @@ int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos,
                   const int32_t *stream_id, int n, float *out,
                   spec_stream_t stream);
 
+/*
+ * Profiling aid. Registers two CUDA events (cudaEvent_t, created by the
+ * caller) for the next spec_verify_linear / spec_verify_tree call made by
+ * the calling host thread: that call records `before` immediately before it
+ * launches its row-statistics pass and `after` immediately after, on the
+ * call's stream, then forgets them. Pass NULLs to clear. The pass streams
+ * every vocabulary row once and dominates the call's time, so
+ * cudaEventElapsedTime(before, after) is that kernel's duration.
+ */
+int spec_profile_row_pass(void *before, void *after);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,7 @@ __all__ = [
     "spec_verify_linear", "spec_verify_linear_workspace", "spec_verify_tree",
     "spec_verify_tree_workspace", "draft_topk_softmax",
     "draft_topk_softmax_workspace", "spec_get_status", "spec_uniforms",
-    "SpecError",
+    "spec_profile_row_pass", "SpecError",
 ]
 
 SPEC_OK = 0
@@ -52,6 +52,7 @@ _SIGS = {
                                   _sz, _vp]),
     "spec_get_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "spec_uniforms": (_i32, [_u64, _vp, _vp, _vp, _i32, _vp, _vp]),
+    "spec_profile_row_pass": (_i32, [_vp, _vp]),
 }
 
 
@@ -248,3 +249,15 @@ def spec_uniforms(seed: int, b, pos, stream_id, stream=None):
                                _ptr(stream_id), b.numel(), _ptr(out), _stream(stream)),
            "spec_uniforms")
     return out
+
+
+def spec_profile_row_pass(before=None, after=None):
+    """Registers two torch.cuda.Event objects (enable_timing=True) that the
+    next verify call on this thread records around its row-statistics pass."""
+    def ev(e):
+        if e is None:
+            return None
+        if not e.cuda_event:     # torch creates the CUDA event on first record
+            e.record()
+        return ctypes.c_void_p(e.cuda_event)
+    _check(lib().spec_profile_row_pass(ev(before), ev(after)), "spec_profile_row_pass")

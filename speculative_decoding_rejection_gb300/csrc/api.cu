@@ -47,3 +47,8 @@ extern "C" int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos
       seed, b, pos, stream_id, n, out);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
+
+extern "C" int spec_profile_row_pass(void *before, void *after) {
+  set_row_pass_events(reinterpret_cast<cudaEvent_t>(before), reinterpret_cast<cudaEvent_t>(after));
+  return SPEC_OK;
+}

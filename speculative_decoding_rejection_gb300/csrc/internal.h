@@ -28,6 +28,7 @@ struct RowPassArgs {
 };
 
 int num_sms();
+void set_row_pass_events(cudaEvent_t before, cudaEvent_t after);
 int launch_row_pass(const RowPassArgs &a, cudaStream_t stream);
 int nchunks(int V, int dtype);
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -280,6 +280,13 @@ int num_sms() {
   return cached[dev];
 }
 
+static thread_local cudaEvent_t prof_before = nullptr, prof_after = nullptr;
+
+void set_row_pass_events(cudaEvent_t before, cudaEvent_t after) {
+  prof_before = before;
+  prof_after = after;
+}
+
 int launch_row_pass(const RowPassArgs &a, cudaStream_t stream) {
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
@@ -287,8 +294,13 @@ int launch_row_pass(const RowPassArgs &a, cudaStream_t stream) {
   if (cudaFuncSetAttribute(k_row_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return SPEC_ERR_CUDA;
+  cudaEvent_t before = prof_before, after = prof_after;
+  prof_before = prof_after = nullptr;
+  if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   k_row_pass<<<2 * sms, RS_THREADS, smem, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
 }
 
 bool aligned(const void *p, size_t al) { return ((uintptr_t)p % al) == 0; }
