@@ -143,6 +143,37 @@ int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
                        int32_t *out_accepted, float *out_pq, void *workspace,
                        size_t ws_bytes, spec_stream_t stream);
 
+/*
+ * No-allocation variant of spec_verify_linear. The paper has no counterpart:
+ * this exists for callers that cannot supply device scratch, such as serving
+ * engines that reserve nearly all of HBM for their KV cache at start-up (a
+ * later cudaMalloc fails) and decode loops that must not call
+ * cudaMalloc/cudaFree because those calls synchronise the device.
+ *
+ * Same inputs, outputs and semantics as spec_verify_linear; the scratch is a
+ * SPEC_NOALLOC_SCRATCH_BYTES array compiled into the library, which every GPU
+ * that loads the library holds until the process exits. Sizes whose
+ * spec_verify_linear_workspace() exceeds it return SPEC_ERR_UNSUPPORTED.
+ * All calls on a device share that array: calls that overlap on the GPU
+ * race, so order them (one stream, or events). The first call on each device
+ * looks up the array's address (cudaGetSymbolAddress, with that device
+ * current); make it before any stream capture. Nothing is allocated.
+ *
+ *   out_status  optional device int32: receives the call's device status word
+ *               (SPEC_OK or a negative spec_status) once the call's work is
+ *               done on `stream`; NULL to skip.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (16u << 20)
+int spec_verify_linear_noalloc(const void *target, int tdt, const void *draft,
+                               int ddt, int dk, const int32_t *draft_idx,
+                               const int32_t *draft_tokens,
+                               const int32_t *cu_draft,
+                               const float *temperature, int B, int V,
+                               int max_k, uint64_t seed, int rule,
+                               int32_t *out_tokens, int32_t *out_accepted,
+                               float *out_pq, int32_t *out_status,
+                               spec_stream_t stream);
+
 /* Bytes of workspace spec_verify_tree needs (0 on invalid sizes). */
 size_t spec_verify_tree_workspace(int B, int n_nodes, int V, int max_depth,
                                   int max_branch);

@@ -53,6 +53,8 @@ _SIGS = {
     "spec_get_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "spec_uniforms": (_i32, [_u64, _vp, _vp, _vp, _i32, _vp, _vp]),
     "spec_profile_row_pass": (_i32, [_vp, _vp]),
+    "spec_verify_linear_noalloc": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32,
+                                          _i32, _i32, _u64, _i32, _vp, _vp, _vp, _vp, _vp]),
 }
 
 

@@ -1,0 +1,77 @@
+// Linear verification for callers that cannot hand the library any scratch.
+//
+// spec_verify_linear() needs a caller-provided device workspace. Some callers
+// cannot obtain one: serving engines that reserve nearly all of HBM for their
+// KV cache when they start (a later cudaMalloc fails, or has to evict cache),
+// and decode loops that must not call cudaMalloc/cudaFree because those calls
+// synchronise the whole device. This entry point takes the same inputs and
+// outputs but keeps its scratch in a fixed array compiled into the library.
+//
+// Properties of that array:
+//   - SPEC_NOALLOC_SCRATCH_BYTES (16 MiB) per GPU, reserved on every GPU that
+//     loads the library and held until the process exits;
+//   - shared by all calls on a device and left holding the last call's
+//     contents; the words that must start at zero (status, work counter) are
+//     reset by the call's own first kernel, everything else is written before
+//     it is read within the call;
+//   - calls whose work overlaps on the GPU (different streams, or different
+//     host threads, without ordering between them) race on it; order them on
+//     one stream or with events.
+// The first call on each device looks up the array's device address with
+// cudaGetSymbolAddress() (with that device current); make that first call
+// before any stream capture. Nothing here calls cudaMalloc, cudaFree or an
+// allocating library routine.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up once).
+int scratch_address(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return SPEC_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return SPEC_OK;
+}
+}  // namespace
+
+extern "C" int spec_verify_linear_noalloc(const void *target, int tdt, const void *draft,
+                                          int ddt, int dk, const int32_t *draft_idx,
+                                          const int32_t *draft_tokens,
+                                          const int32_t *cu_draft, const float *temperature,
+                                          int B, int V, int max_k, uint64_t seed, int rule,
+                                          int32_t *out_tokens, int32_t *out_accepted,
+                                          float *out_pq, int32_t *out_status,
+                                          spec_stream_t stream) {
+  const size_t need = spec_verify_linear_workspace(B, max_k, V, rule);
+  if (need == 0) return SPEC_ERR_INVALID_ARG;
+  if (need > (size_t)SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_UNSUPPORTED;
+  if (out_status != nullptr && !sv::aligned(out_status, 4)) return SPEC_ERR_INVALID_ARG;
+  void *scratch = nullptr;
+  int rc = scratch_address(&scratch);
+  if (rc != SPEC_OK) return rc;
+  rc = spec_verify_linear(target, tdt, draft, ddt, dk, draft_idx, draft_tokens, cu_draft,
+                          temperature, B, V, max_k, seed, rule, out_tokens, out_accepted, out_pq,
+                          scratch, (size_t)SPEC_NOALLOC_SCRATCH_BYTES, stream);
+  if (rc != SPEC_OK) return rc;
+  if (out_status != nullptr &&
+      cudaMemcpyAsync(out_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
