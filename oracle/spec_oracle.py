@@ -351,13 +351,16 @@ def rrsw_node(p, q, child_tokens, coins):
 
 
 def verify_tree(target, draft, node_token, parent, cu_nodes, temperature,
-                seed, max_depth, rule=RULE_STRICT, requests=None):
+                seed, max_depth, rule=RULE_STRICT, requests=None,
+                draft_kind=DRAFT_LOGITS):
     """Multi-draft tree verification by RRSw.
 
     Request b owns nodes cu_nodes[b] .. cu_nodes[b+1]-1; local node 0 is the
     root. parent[] holds local parent ids (-1 for the root), topologically
     ordered. Target row n is the target law after the path to node n; draft
-    row n is the law node n's children were drawn from.
+    row n is the law node n's children were drawn from: logits (q =
+    softmax(z/T)) or, with draft_kind == DRAFT_PROBS, the probabilities
+    themselves.
 
     Returns tokens [n, max_depth+1], accepted [n], path [n, max_depth+1]
     (local node ids of accepted nodes), flag_slot [n], requests.
@@ -402,7 +405,10 @@ def verify_tree(target, draft, node_token, parent, cu_nodes, temperature,
                     flagged_at = depth
                 tokens[j, depth] = x
                 break
-            q = softmax_T(as_f64(draft[base + v]), T)
+            if draft_kind == DRAFT_PROBS:
+                q = as_f64(draft[base + v])
+            else:
+                q = softmax_T(as_f64(draft[base + v]), T)
             coins = [uniform(seed, b, c, STREAM_COIN) for c in kids]
             acc, law, tested = rrsw_node(p, q, [ntok[base + c] for c in kids],
                                          coins)

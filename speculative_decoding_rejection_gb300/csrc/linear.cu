@@ -245,36 +245,6 @@ struct SampleSmem {
   int xmin, xlast;
 };
 
-// Load SAMPLE_EPT consecutive elements [x0, x0+EPT) of a row; `fill` beyond V.
-__device__ __forceinline__ void load_ept(const char *row, int dt, bool vec_ok, int x0, int V,
-                                         float fill, float *z) {
-  if (vec_ok && x0 + SAMPLE_EPT <= V) {
-    if (dt == SPEC_BF16) {
-      const uint4 *p = reinterpret_cast<const uint4 *>(row + 2LL * x0);
-#pragma unroll
-      for (int q = 0; q < SAMPLE_EPT / 8; ++q) {
-        const uint4 w = __ldg(p + q);
-        z[8 * q + 0] = bf16lo(w.x); z[8 * q + 1] = bf16hi(w.x);
-        z[8 * q + 2] = bf16lo(w.y); z[8 * q + 3] = bf16hi(w.y);
-        z[8 * q + 4] = bf16lo(w.z); z[8 * q + 5] = bf16hi(w.z);
-        z[8 * q + 6] = bf16lo(w.w); z[8 * q + 7] = bf16hi(w.w);
-      }
-    } else {
-      const uint4 *p = reinterpret_cast<const uint4 *>(row + 4LL * x0);
-#pragma unroll
-      for (int q = 0; q < SAMPLE_EPT / 4; ++q) {
-        const uint4 w = __ldg(p + q);
-        z[4 * q + 0] = __uint_as_float(w.x); z[4 * q + 1] = __uint_as_float(w.y);
-        z[4 * q + 2] = __uint_as_float(w.z); z[4 * q + 3] = __uint_as_float(w.w);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < SAMPLE_EPT; ++k)
-      z[k] = x0 + k < V ? load_elem(row, dt, x0 + k) : fill;
-  }
-}
-
 // Weights of this thread's SAMPLE_EPT elements of tile j: the residual
 // max(0, p - q) (kind 1) or p (kind 2).
 template <int DK>

@@ -1,12 +1,534 @@
-// Tree verification (RRSw). Placeholder until the walker lands.
+// Tree verification by recursive rejection sampling without replacement
+// ("RheoSampling 2026", §4 "RheoVerification"): at node v the children are
+// tested in the order they were drawn (node-index order). Child j with token
+// x is accepted with probability min(1, p_j(x)/q_j(x)); on acceptance the
+// walk descends into it. On rejection the target law becomes the normalised
+// residual p_{j+1} = norm(max(0, p_j - q_j)) and the draft law drops x and is
+// renormalised by 1 - q(E) (without replacement). If every child is rejected
+// the final token is drawn from the last residual; at an accepted leaf it is a
+// bonus draw from that leaf's target law. Greedy trees (T < 0.05) accept the
+// first child equal to argmax p_v and otherwise emit argmax p_v.
+//
+// Uniforms: coin of child c at u(seed, b, c, 0); the final draw at node v at
+// u(seed, b, v + 1, 1) (residual) or u(seed, b, v + 1, 2) (bonus), so a chain
+// tree reproduces the linear verifier draw for draw.
+//
+// Pipeline: a one-block setup kernel validates every tree and lists the node
+// rows; the shared row pass computes max / normaliser / argmax of every
+// target row and of the draft rows of internal nodes; then one CTA per tree
+// walks it. The residual laws are never stored: every pass recomputes
+// p_j(y) from p(y) and q(y) through the chain of normalisers, which are
+// scalars. A token rejected at step k has q_k > p_k, so p_{k+1} is exactly 0
+// there and stays 0; the chain can therefore use q(y) s_j for every y without
+// testing membership of the excluded set.
 #include "common.cuh"
 #include "internal.h"
 
-extern "C" size_t spec_verify_tree_workspace(int, int, int, int, int) { return 0; }
+namespace sv {
 
-extern "C" int spec_verify_tree(const void *, int, const void *, int, int, const int32_t *,
-                                const int32_t *, const int32_t *, const float *, int, int, int,
-                                int, int, uint64_t, int32_t *, int32_t *, int32_t *, void *,
-                                size_t, spec_stream_t) {
-  return SPEC_ERR_UNSUPPORTED;
+constexpr int WALK_THREADS = 1024;
+
+struct TreeInfo {
+  int base;   // first node row
+  int N;      // nodes
+  int mode;   // ReqMode
+  float c;    // log2(e)/T
+};
+
+struct TreeArgs {
+  const char *target;
+  const char *draft;
+  int tdt, ddt, dk;
+  const int32_t *node_token;
+  const int32_t *parent;
+  const int32_t *cu;
+  const float *temp;
+  int B, n_nodes, V, max_depth, max_branch;
+  uint64_t seed;
+  int32_t *out_tokens, *out_accepted, *out_path;
+  WsHeader *hdr;
+  TreeInfo *tree;
+  RowTask *list;
+  Part *part;
+  int32_t *node_aux;   // [n_nodes] depth, then child counts
+  long long t_row_bytes, d_row_bytes;
+  int nch_t, nch_d, nch_max;
+  int stream_draft;
+};
+
+struct TreeLayout {
+  size_t hdr, tree, list, part, aux, total;
+  int nch_max;
+};
+
+static TreeLayout tree_layout(int B, int n_nodes, int V) {
+  TreeLayout L;
+  L.nch_max = nchunks(V, SPEC_F32);
+  const size_t rows = 2 * (size_t)n_nodes;
+  size_t o = 0;
+  L.hdr = o;  o += align256(sizeof(WsHeader));
+  L.tree = o; o += align256(sizeof(TreeInfo) * (size_t)B);
+  L.list = o; o += align256(sizeof(RowTask) * rows);
+  L.part = o; o += align256(sizeof(Part) * rows * L.nch_max * RS_CONS_WARPS);
+  L.aux = o;  o += align256(sizeof(int32_t) * 2 * (size_t)n_nodes);
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------------------------ setup
+__global__ void __launch_bounds__(1024) k_setup_tree(const TreeArgs a) {
+  __shared__ int scratch[33];
+  if (threadIdx.x == 0) {
+    a.hdr->status = SPEC_OK;
+    a.hdr->detail = -1;
+    a.hdr->work = 0;
+    a.hdr->n_list = 0;
+  }
+  __syncthreads();
+  const int per = (a.B + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(a.B, (int)threadIdx.x * per), b1 = min(a.B, b0 + per);
+  int32_t *depth = a.node_aux, *nkids = a.node_aux + a.n_nodes;
+  int cnt = 0, bad = 0;
+  const bool cu_ok = a.B == 0 || a.cu[0] == 0;
+  for (int b = b0; b < b1; ++b) {
+    TreeInfo t;
+    t.base = a.cu[b];
+    t.N = a.cu[b + 1] - a.cu[b];
+    const float T = a.temp[b];
+    const bool greedy = T < SPEC_GREEDY_T;
+    bool ok = cu_ok && t.base >= 0 && t.N >= 1 && t.N <= SPEC_MAX_TREE_NODES &&
+              a.cu[b + 1] <= a.n_nodes && T >= 0.f && isfinite(T);
+    if (ok && !greedy && a.draft == nullptr) ok = false;
+    if (ok) {
+      for (int c = 0; c < t.N; ++c) nkids[t.base + c] = 0;
+      for (int c = 0; c < t.N && ok; ++c) {
+        const int p = a.parent[t.base + c];
+        if (c == 0) {
+          ok = p == -1;
+          depth[t.base] = 0;
+          continue;
+        }
+        const int tok = a.node_token[t.base + c];
+        ok = p >= 0 && p < c && tok >= 0 && tok < a.V;
+        if (!ok) break;
+        depth[t.base + c] = depth[t.base + p] + 1;
+        ok = depth[t.base + c] <= a.max_depth && ++nkids[t.base + p] <= a.max_branch;
+      }
+    }
+    t.mode = ok ? (greedy ? MODE_GREEDY : MODE_SAMPLE) : MODE_SKIP;
+    t.c = (ok && !greedy) ? (float)(1.4426950408889634 / (double)T) : 0.f;
+    if (!ok) {
+      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+      bad = 1;
+    } else {
+      cnt += t.N;
+      if (t.mode == MODE_SAMPLE && a.stream_draft)
+        for (int c = 0; c < t.N; ++c) cnt += nkids[t.base + c] > 0;
+    }
+    a.tree[b] = t;
+  }
+  if (__syncthreads_or(bad)) {   // offsets are only trusted when all are sound
+    for (int b = b0; b < b1; ++b) a.tree[b].mode = MODE_SKIP;
+    return;
+  }
+  int total;
+  int off = block_excl_scan_int(cnt, scratch, &total);
+  for (int b = b0; b < b1; ++b) {
+    const TreeInfo t = a.tree[b];
+    for (int c = 0; c < t.N; ++c) a.list[off++] = RowTask{t.base + c, t.base + c, 0, t.c};
+    if (t.mode == MODE_SAMPLE && a.stream_draft)
+      for (int c = 0; c < t.N; ++c)
+        if (nkids[t.base + c] > 0)
+          a.list[off++] = RowTask{a.n_nodes + t.base + c, t.base + c, 1, t.c};
+  }
+  if (threadIdx.x == 0) a.hdr->n_list = total;
+}
+
+// ------------------------------------------------------------------- walk
+struct WalkSmem {
+  float tsum[MAX_SAMPLE_TILES];
+  float scratch[33];
+  int kids[SPEC_MAX_TREE_BRANCH];
+  float s[SPEC_MAX_TREE_BRANCH + 1];     // 1 / (1 - q(E_j))
+  float rinv[SPEC_MAX_TREE_BRANCH + 1];  // 1 / Z_j
+  int skip[SPEC_MAX_TREE_BRANCH + 1];    // Z_j == 0: p_{j+1} = p_j
+  int nk, jstar, xmin, xlast, done, accepted_child;
+  float carry, target, Z;
+};
+
+struct NodeLaw {        // p(y) = 2^((zt - mt) c) / St, q(y) likewise or given
+  const char *trow, *drow;
+  bool tvec, dvec;
+  float mt, invSt, md, invSd;
+};
+
+// p_L(y) and the residual max(0, p_L - q_L) (or p_L itself) from the raw
+// p(y), q(y) through the chain of normalisers.
+__device__ __forceinline__ float chain_weight(float p, float q, int L, bool residual,
+                                              const WalkSmem &sh) {
+  for (int i = 0; i < L; ++i)
+    if (!sh.skip[i]) p = fmaxf(0.f, p - q * sh.s[i]) * sh.rinv[i];
+  return residual ? fmaxf(0.f, p - q * sh.s[L]) : p;
+}
+
+template <int DK>
+__device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkSmem &sh,
+                                                  const NodeLaw &nl, float c, int L,
+                                                  bool residual, int j, float *w) {
+  const int x0 = j * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
+  float zt[SAMPLE_EPT], zd[SAMPLE_EPT];
+  load_ept(nl.trow, a.tdt, nl.tvec, x0, a.V, -INFINITY, zt);
+  if (L > 0 || residual)
+    load_ept(nl.drow, a.ddt, nl.dvec, x0, a.V, DK == SPEC_DRAFT_PROBS ? 0.f : -INFINITY, zd);
+#pragma unroll
+  for (int k = 0; k < SAMPLE_EPT; ++k) {
+    const float p = ex2((zt[k] - nl.mt) * c) * nl.invSt;
+    if (L == 0 && !residual) {
+      w[k] = p;
+      continue;
+    }
+    const float q = DK == SPEC_DRAFT_PROBS ? zd[k] : ex2((zd[k] - nl.md) * c) * nl.invSd;
+    w[k] = chain_weight(p, q, L, residual, sh);
+  }
+}
+
+// One pass over the node's rows: tile totals of the level-L weights into
+// sh.tsum and their sum into sh.Z (thread 0, ascending tile order).
+template <int DK>
+__device__ void weight_pass(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, float c, int L,
+                            bool residual) {
+  const int ntiles = (a.V + SAMPLE_TILE - 1) / SAMPLE_TILE;
+  float w[SAMPLE_EPT];
+  for (int j = 0; j < ntiles; ++j) {
+    tile_weights_tree<DK>(a, sh, nl, c, L, residual, j, w);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
+    float tot;
+    block_excl_scan(s, sh.scratch, &tot);
+    if (threadIdx.x == 0) sh.tsum[j] = tot;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float Z = 0.f;
+    for (int j = 0; j < ntiles; ++j) Z += sh.tsum[j];
+    sh.Z = Z;
+  }
+  __syncthreads();
+}
+
+// Inverse-CDF draw at u from the level-L weights whose tile totals are in
+// sh.tsum (smallest y with u*Z < C_y; the last positive weight if rounding
+// leaves none).
+template <int DK>
+__device__ int weight_draw(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, float c, int L,
+                           bool residual, float u) {
+  const int ntiles = (a.V + SAMPLE_TILE - 1) / SAMPLE_TILE;
+  if (threadIdx.x == 0) {
+    sh.target = u * sh.Z;
+    float carry = 0.f;
+    int js = -1;
+    for (int j = 0; j < ntiles; ++j) {
+      const float nc = carry + sh.tsum[j];
+      if (nc > sh.target) { js = j; break; }
+      carry = nc;
+    }
+    if (js < 0)
+      for (int j = ntiles - 1; j >= 0 && js < 0; --j)
+        if (sh.tsum[j] > 0.f) js = j;
+    sh.jstar = js;
+    sh.carry = carry;
+    sh.xmin = 0x7fffffff;
+    sh.xlast = -1;
+  }
+  __syncthreads();
+  const int js = sh.jstar;
+  if (js >= 0) {
+    float w[SAMPLE_EPT];
+    tile_weights_tree<DK>(a, sh, nl, c, L, residual, js, w);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
+    float tot;
+    const float excl = block_excl_scan(s, sh.scratch, &tot);
+    const int x0 = js * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
+    float pre = 0.f;
+    int cand = 0x7fffffff, lastpos = -1;
+#pragma unroll
+    for (int k = 0; k < SAMPLE_EPT; ++k) {
+      pre += w[k];
+      if (cand == 0x7fffffff && sh.carry + (excl + pre) > sh.target) cand = x0 + k;
+      if (w[k] > 0.f) lastpos = x0 + k;
+    }
+    if (cand != 0x7fffffff) atomicMin(&sh.xmin, cand);
+    if (lastpos >= 0) atomicMax(&sh.xlast, lastpos);
+  }
+  __syncthreads();
+  const int x = sh.xmin != 0x7fffffff ? sh.xmin : sh.xlast;
+  __syncthreads();
+  return x;
+}
+
+__device__ __forceinline__ RowStat node_stat(const TreeArgs &a, int slot, int nch, float c) {
+  return combine_parts(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS, nch * RS_CONS_WARPS,
+                       c);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
+  __shared__ WalkSmem sh;
+  const int b = blockIdx.x;
+  const TreeInfo t = a.tree[b];
+  const int W = a.max_depth + 1;
+  int32_t *out = a.out_tokens + (long long)b * W;
+  int32_t *path = a.out_path ? a.out_path + (long long)b * W : nullptr;
+  for (int j = threadIdx.x; j < W; j += blockDim.x) {
+    out[j] = -1;
+    if (path) path[j] = -1;
+  }
+  if (t.mode == MODE_SKIP) {
+    if (threadIdx.x == 0) a.out_accepted[b] = -1;
+    return;
+  }
+  __syncthreads();
+  const float c = t.c;
+  int v = 0, depth = 0;
+  while (true) {
+    // children of v in node-index order (block-wide ordered compaction)
+    {
+      const int per = (t.N + blockDim.x - 1) / blockDim.x;
+      const int c0 = min(t.N, (int)threadIdx.x * per), c1 = min(t.N, c0 + per);
+      int n = 0;
+      for (int cc = c0; cc < c1; ++cc) n += a.parent[t.base + cc] == v && cc > 0;
+      int tot;
+      int off = block_excl_scan_int(n, reinterpret_cast<int *>(sh.scratch), &tot);
+      for (int cc = c0; cc < c1; ++cc)
+        if (a.parent[t.base + cc] == v && cc > 0) {
+          if (off < SPEC_MAX_TREE_BRANCH) sh.kids[off] = cc;
+          ++off;
+        }
+      if (threadIdx.x == 0) sh.nk = min(tot, SPEC_MAX_TREE_BRANCH);
+      __syncthreads();
+    }
+    const int nk = sh.nk;
+    const int row = t.base + v;
+    const RowStat ts = node_stat(a, row, a.nch_t, c);
+    if (t.mode == MODE_GREEDY) {
+      if (threadIdx.x == 0) {
+        sh.accepted_child = -1;
+        for (int j = 0; j < nk; ++j)
+          if (a.node_token[t.base + sh.kids[j]] == ts.idx) { sh.accepted_child = sh.kids[j]; break; }
+      }
+      __syncthreads();
+      const int ac = sh.accepted_child;
+      __syncthreads();
+      if (ac >= 0 && depth < a.max_depth) {
+        if (threadIdx.x == 0) {
+          out[depth] = a.node_token[t.base + ac];
+          if (path) path[depth] = ac;
+        }
+        v = ac;
+        ++depth;
+        continue;
+      }
+      if (threadIdx.x == 0) {
+        out[depth] = ts.idx;
+        a.out_accepted[b] = depth;
+      }
+      return;
+    }
+    NodeLaw nl;
+    nl.trow = a.target + (long long)row * a.t_row_bytes;
+    nl.tvec = ((uintptr_t)nl.trow & 15) == 0;
+    nl.mt = ts.m;
+    nl.invSt = 1.f / ts.S;
+    nl.drow = nullptr;
+    nl.dvec = false;
+    nl.md = 0.f;
+    nl.invSd = 0.f;
+    if (nk == 0) {  // accepted leaf (or a bare root): bonus draw from p_v
+      weight_pass<DK>(a, sh, nl, c, 0, false);
+      const int x = weight_draw<DK>(a, sh, nl, c, 0, false,
+                                    uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 2));
+      if (threadIdx.x == 0) {
+        out[depth] = x;
+        a.out_accepted[b] = depth;
+      }
+      return;
+    }
+    nl.drow = a.draft + (long long)row * a.d_row_bytes;
+    nl.dvec = ((uintptr_t)nl.drow & 15) == 0;
+    if (DK == SPEC_DRAFT_LOGITS) {
+      const RowStat ds = node_stat(a, a.n_nodes + row, a.nch_d, c);
+      nl.md = ds.m;
+      nl.invSd = 1.f / ds.S;
+    }
+    if (threadIdx.x == 0) {
+      sh.s[0] = 1.f;
+      sh.skip[0] = 0;
+      sh.rinv[0] = 1.f;
+    }
+    __syncthreads();
+    float qE = 0.f;
+    int accepted = -1, L = 0;
+    bool exhausted = false;
+    for (int j = 0; j < nk; ++j) {
+      // coin of child j at its token x, with p_j(x) and q_j(x) from the chain
+      if (threadIdx.x == 0) {
+        const int ch = sh.kids[j];
+        const int x = a.node_token[t.base + ch];
+        const float p = ex2((load_elem(nl.trow, a.tdt, x) - nl.mt) * c) * nl.invSt;
+        const float qx = DK == SPEC_DRAFT_PROBS
+                             ? load_elem(nl.drow, a.ddt, x)
+                             : ex2((load_elem(nl.drow, a.ddt, x) - nl.md) * c) * nl.invSd;
+        const float pj = chain_weight(p, qx, j, false, sh);
+        const float qj = qx * sh.s[j];
+        const float acc = qj <= pj ? 1.f : pj / qj;
+        const bool ok = uniform24(a.seed, (uint32_t)b, (uint32_t)ch, 0) < acc;
+        sh.accepted_child = ok ? ch : -1;
+        sh.carry = qx;   // q(x), for q(E)
+      }
+      __syncthreads();
+      const int ac = sh.accepted_child;
+      const float qx = sh.carry;
+      __syncthreads();
+      if (ac >= 0) {
+        accepted = ac;
+        break;
+      }
+      // rejection: Z_j of the residual at level j (tile totals kept for a
+      // possible final draw), then the next draft normaliser
+      weight_pass<DK>(a, sh, nl, c, j, true);
+      L = j;
+      qE += qx;
+      const float left = 1.f - qE;
+      if (threadIdx.x == 0) {
+        sh.skip[j] = !(sh.Z > 0.f);
+        sh.rinv[j] = sh.Z > 0.f ? 1.f / sh.Z : 1.f;
+        sh.s[j + 1] = left > 0.f ? 1.f / left : 0.f;
+      }
+      __syncthreads();
+      if (!(left > 0.f)) {   // every draft token used up
+        exhausted = true;
+        break;
+      }
+    }
+    if (accepted >= 0 && depth < a.max_depth) {
+      if (threadIdx.x == 0) {
+        out[depth] = a.node_token[t.base + accepted];
+        if (path) path[depth] = accepted;
+      }
+      v = accepted;
+      ++depth;
+      continue;
+    }
+    (void)exhausted;
+    // all tested children rejected: draw from p_{L+1} = norm(residual at L),
+    // or from p_L itself when that residual had no mass
+    bool residual = true;
+    if (sh.skip[L]) {
+      residual = false;
+      weight_pass<DK>(a, sh, nl, c, L, false);
+    }
+    const int x = weight_draw<DK>(a, sh, nl, c, L, residual,
+                                  uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 1));
+    if (threadIdx.x == 0) {
+      out[depth] = x;
+      a.out_accepted[b] = depth;
+    }
+    return;
+  }
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t spec_verify_tree_workspace(int B, int n_nodes, int V, int max_depth,
+                                             int max_branch) {
+  if (B < 0 || n_nodes < B || V <= 0 || V > SPEC_MAX_V) return 0;
+  if (max_depth < 0 || max_depth > SPEC_MAX_TREE_DEPTH) return 0;
+  if (max_branch < 1 || max_branch > SPEC_MAX_TREE_BRANCH) return 0;
+  return tree_layout(B, n_nodes, V).total;
+}
+
+extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, int ddt, int dk,
+                                const int32_t *node_token, const int32_t *parent,
+                                const int32_t *cu_nodes, const float *temperature, int B,
+                                int n_nodes, int V, int max_depth, int max_branch, uint64_t seed,
+                                int32_t *out_tokens, int32_t *out_accepted, int32_t *out_path,
+                                void *workspace, size_t ws_bytes, spec_stream_t stream) {
+  if (B < 0 || n_nodes < B || V <= 0 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  if (max_depth < 0 || max_branch < 1) return SPEC_ERR_INVALID_ARG;
+  if (max_depth > SPEC_MAX_TREE_DEPTH || max_branch > SPEC_MAX_TREE_BRANCH)
+    return SPEC_ERR_UNSUPPORTED;
+  if ((tdt != SPEC_F32 && tdt != SPEC_BF16) || (ddt != SPEC_F32 && ddt != SPEC_BF16))
+    return SPEC_ERR_INVALID_ARG;
+  if (dk != SPEC_DRAFT_LOGITS && dk != SPEC_DRAFT_PROBS) return SPEC_ERR_INVALID_ARG;
+  if (B > 0 && (target == nullptr || node_token == nullptr || parent == nullptr ||
+                cu_nodes == nullptr || temperature == nullptr || out_tokens == nullptr ||
+                out_accepted == nullptr))
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(target, 16) || !aligned(draft, 16) || !aligned(node_token, 4) ||
+      !aligned(parent, 4) || !aligned(cu_nodes, 4) || !aligned(temperature, 4) ||
+      !aligned(out_tokens, 4) || !aligned(out_accepted, 4) || !aligned(out_path, 4))
+    return SPEC_ERR_INVALID_ARG;
+  const TreeLayout L = tree_layout(B, n_nodes, V);
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < L.total)
+    return SPEC_ERR_WORKSPACE;
+  char *ws = static_cast<char *>(workspace);
+  TreeArgs a;
+  a.target = static_cast<const char *>(target);
+  a.draft = static_cast<const char *>(draft);
+  a.tdt = tdt;
+  a.ddt = ddt;
+  a.dk = dk;
+  a.node_token = node_token;
+  a.parent = parent;
+  a.cu = cu_nodes;
+  a.temp = temperature;
+  a.B = B;
+  a.n_nodes = n_nodes;
+  a.V = V;
+  a.max_depth = max_depth;
+  a.max_branch = max_branch;
+  a.seed = seed;
+  a.out_tokens = out_tokens;
+  a.out_accepted = out_accepted;
+  a.out_path = out_path;
+  a.hdr = reinterpret_cast<WsHeader *>(ws + L.hdr);
+  a.tree = reinterpret_cast<TreeInfo *>(ws + L.tree);
+  a.list = reinterpret_cast<RowTask *>(ws + L.list);
+  a.part = reinterpret_cast<Part *>(ws + L.part);
+  a.node_aux = reinterpret_cast<int32_t *>(ws + L.aux);
+  a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
+  a.d_row_bytes = (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
+  a.nch_t = nchunks(V, tdt);
+  a.nch_d = nchunks(V, ddt);
+  a.nch_max = L.nch_max;
+  a.stream_draft = dk == SPEC_DRAFT_LOGITS;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  k_setup_tree<<<1, 1024, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (B == 0) return SPEC_OK;
+  RowPassArgs rp;
+  rp.base[0] = a.target;
+  rp.base[1] = a.draft;
+  rp.row_bytes[0] = a.t_row_bytes;
+  rp.row_bytes[1] = a.d_row_bytes;
+  rp.dtype[0] = tdt;
+  rp.dtype[1] = ddt;
+  rp.nch[0] = a.nch_t;
+  rp.nch[1] = a.nch_d;
+  rp.nch_max = a.nch_max;
+  rp.list = a.list;
+  rp.hdr = a.hdr;
+  rp.part = a.part;
+  const int rc = launch_row_pass(rp, st);
+  if (rc != SPEC_OK) return rc;
+  if (dk == SPEC_DRAFT_PROBS)
+    k_tree_walk<SPEC_DRAFT_PROBS><<<B, WALK_THREADS, 0, st>>>(a);
+  else
+    k_tree_walk<SPEC_DRAFT_LOGITS><<<B, WALK_THREADS, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -1,0 +1,121 @@
+"""Parity of the CUDA tree verifier (RRSw, through the C ABI) with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_rejection_gb300 as sv
+from oracle import spec_oracle as O
+from speculative_decoding_rejection_gb300 import synthetic as S
+
+from parity import probs_from_logits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def gpu_tree(tb, draft=None, draft_kind=sv.SPEC_DRAFT_LOGITS):
+    draft = tb.draft if draft is None else draft
+    tok, acc, path, ws = sv.spec_verify_tree(
+        tb.target, draft, tb.node_token, tb.parent, tb.cu_nodes, tb.temperature, tb.seed,
+        max_depth=tb.max_depth, max_branch=tb.max_branch, draft_kind=draft_kind)
+    return dict(tokens=tok.cpu().numpy(), accepted=acc.cpu().numpy(), path=path.cpu().numpy(),
+                status=sv.spec_get_status(ws))
+
+
+def oracle_tree(tb, draft=None, draft_kind=sv.SPEC_DRAFT_LOGITS, requests=None):
+    draft = tb.draft if draft is None else draft
+    host = (lambda t: t.cpu()) if requests is None else (lambda t: t)
+    return O.verify_tree(host(tb.target), host(draft), tb.node_token.cpu().numpy(),
+                         tb.parent.cpu().numpy(), tb.cu_nodes.cpu().numpy(),
+                         tb.temperature.cpu().numpy(), tb.seed, tb.max_depth,
+                         requests=requests, draft_kind=draft_kind)
+
+
+def assert_tree_parity(g, r, min_compared):
+    n_full = 0
+    for j, b in enumerate(r["requests"]):
+        fs = int(r["flag_slot"][j])
+        if fs < 0:
+            assert np.array_equal(g["tokens"][b], r["tokens"][j]), (b, g["tokens"][b], r["tokens"][j])
+            assert g["accepted"][b] == r["accepted"][j]
+            assert np.array_equal(g["path"][b], r["path"][j])
+            n_full += 1
+        else:
+            assert np.array_equal(g["tokens"][b][:fs], r["tokens"][j][:fs])
+    assert n_full >= min_compared
+    return n_full
+
+
+@pytest.mark.parametrize("T,V,dtype", [(0.8, 5003, "bf16"), (1.3, 4096, "f32"),
+                                       (0.0, 3001, "bf16"), (0.3, 20000, "bf16")])
+def test_random_trees_small_vocab(T, V, dtype):
+    tb = S.make_tree(4, device=DEV, B=12, V=V, dtype=dtype, T=T, input_seed=V)
+    g = gpu_tree(tb)
+    assert g["status"] == sv.SPEC_OK
+    r = oracle_tree(tb)
+    assert_tree_parity(g, r, min_compared=10)
+    assert g["accepted"].max() >= 1
+
+
+def test_wide_shallow_trees_many_rejections():
+    tb = S.make_tree(4, device=DEV, B=16, N=9, depth=1, branch=8, V=64, sigma=2.5, T=1.0,
+                     input_seed=3)
+    g = gpu_tree(tb)
+    r = oracle_tree(tb)
+    assert_tree_parity(g, r, min_compared=14)
+    assert (g["accepted"] == 0).any()        # some nodes reject all 8 children
+
+
+def test_tree_draft_given_as_probabilities():
+    tb = S.make_tree(4, device=DEV, B=10, V=3000, input_seed=17)
+    ones = torch.arange(0, tb.target.shape[0] + 1, dtype=torch.int32, device=DEV)
+    T = tb.temperature.repeat_interleave(torch.diff(tb.cu_nodes.long()))
+    probs = probs_from_logits(tb.draft, ones, T)
+    g = gpu_tree(tb, draft=probs, draft_kind=sv.SPEC_DRAFT_PROBS)
+    r = oracle_tree(tb, draft=probs, draft_kind=sv.SPEC_DRAFT_PROBS)
+    assert_tree_parity(g, r, min_compared=8)
+
+
+@pytest.mark.parametrize("T", [0.9, 0.0])
+def test_chain_tree_equals_linear_verifier_on_the_gpu(T):
+    lb = S.make_linear(1, device=DEV, B=24, K=5, V=4000, dtype="bf16", T=T, input_seed=41)
+    B, K, V = lb.B, lb.max_k, lb.V
+    tgt = lb.target.view(B, K + 1, V)
+    drf = torch.cat([lb.draft.view(B, K, V), torch.zeros(B, 1, V, dtype=lb.draft.dtype,
+                                                         device=DEV)], 1)
+    node_tok = torch.cat([torch.full((B, 1), -1, dtype=torch.int32, device=DEV),
+                          lb.draft_tokens.view(B, K)], 1).reshape(-1).contiguous()
+    parent = torch.arange(-1, K, dtype=torch.int32, device=DEV).repeat(B).contiguous()
+    cu = torch.arange(0, B * (K + 1) + 1, K + 1, dtype=torch.int32, device=DEV)
+    tok_t, acc_t, _, ws = sv.spec_verify_tree(
+        tgt.reshape(-1, V).contiguous(), drf.reshape(-1, V).contiguous(), node_tok, parent, cu,
+        lb.temperature, lb.seed, max_depth=K, max_branch=1)
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    tok_l, acc_l, _, _ = sv.spec_verify_linear(lb.target, lb.draft, lb.draft_tokens,
+                                               lb.cu_draft, lb.temperature, lb.seed, max_k=K)
+    assert torch.equal(acc_t, acc_l)
+    assert torch.equal(tok_t, tok_l)
+
+
+def test_full_size_tree_workload_on_sampled_trees():
+    tb = S.make_tree(4, device=DEV)
+    g = gpu_tree(tb)
+    assert g["status"] == sv.SPEC_OK
+    req = np.arange(0, tb.B, 4)
+    r = oracle_tree(tb, requests=req)
+    assert_tree_parity(g, r, min_compared=len(req) - 2)
+    assert np.all((g["accepted"] >= 0) & (g["accepted"] <= tb.max_depth))
+
+
+def test_malformed_tree_sets_the_status_word():
+    tb = S.make_tree(4, device=DEV, B=3, V=500, input_seed=5)
+    bad = tb.parent.clone()
+    bad[64 + 10] = 12                          # parent after its child
+    tok, acc, _, ws = sv.spec_verify_tree(tb.target, tb.draft, tb.node_token, bad, tb.cu_nodes,
+                                          tb.temperature, 1, max_depth=6, max_branch=4)
+    assert sv.spec_get_status(ws) == sv.SPEC_ERR_INVALID_ARG
+    assert torch.all(acc == -1)
+    tok, acc, _, ws = sv.spec_verify_tree(tb.target, tb.draft, tb.node_token, tb.parent,
+                                          tb.cu_nodes, tb.temperature, 1, max_depth=3,
+                                          max_branch=4)
+    assert sv.spec_get_status(ws) == sv.SPEC_ERR_INVALID_ARG    # deeper than max_depth
