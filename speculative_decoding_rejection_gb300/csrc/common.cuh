@@ -10,9 +10,15 @@ namespace sv {
 
 // ---------------------------------------------------------------- tiling
 constexpr int TILE_BYTES = 16384;   // one TMA bulk copy = one pipeline stage
-constexpr int CHUNK_BYTES = 65536;  // one unit of dynamic work in the row pass
-constexpr int NSTAGE = 6;           // pipeline depth per CTA (96 KB in flight)
-constexpr int RS_CONS_WARPS = 8;    // consumer warps of the row pass
+constexpr int CHUNK_BYTES = 131072; // one unit of dynamic work in the row pass
+// Row pass shape, chosen by measurement on GB300: six CTAs per SM, each one
+// producer lane and four consumer warps over a two-stage ring of 16 KB TMA
+// copies (192 KB of copies in flight per SM); a consumer thread takes eight
+// 16-byte vectors (64 bf16) per stage, enough independent work to keep the
+// exponent pipe fed.
+constexpr int NSTAGE = 2;           // pipeline depth per CTA
+constexpr int RS_CONS_WARPS = 4;    // consumer warps of the row pass
+constexpr int RS_CTAS_PER_SM = 6;   // resident row-pass CTAs per SM
 constexpr int RS_THREADS = 32 * (1 + RS_CONS_WARPS);
 constexpr int SAMPLE_THREADS = 1024;
 constexpr int SAMPLE_EPT = 16;      // contiguous elements per thread per tile
@@ -60,6 +66,11 @@ struct ReqInfo {         // per request, written by the setup kernel
 
 struct RowStat { float m, S; int idx; };
 
+// Running maximum before any element: finite, so (x - m) never forms inf - inf.
+// A row whose statistics keep this value holds no finite logit.
+constexpr float NO_MAX = -3.402823466e38f;
+__device__ __forceinline__ bool row_empty(float m) { return !(m > NO_MAX); }
+
 // --------------------------------------------------------------- status
 __device__ __forceinline__ void set_status(WsHeader *h, int code, int detail) {
   if (atomicCAS(&h->status, 0, code) == 0) atomicExch(&h->detail, detail);
@@ -92,6 +103,39 @@ __device__ __forceinline__ float ex2(float x) {   // MUFU 2^x
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Packed fp32 pairs (Blackwell f32x2 arithmetic) and packed bf16 helpers.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  return ((f32x2)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo2(f32x2 v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// (lo(w) - m, hi(w) - m) for a packed bf16 pair w, exact for bf16 inputs
+// (mixed-precision subtract: the bf16 operand is widened by the instruction).
+__device__ __forceinline__ f32x2 bsub2(uint32_t w, float m) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w), "f"(m));
+  return pk2(lo, hi);
+}
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ float load_elem(const void *row, int dtype, long long i) {
   if (dtype == SPEC_BF16) {
     const uint16_t v = __ldg(reinterpret_cast<const unsigned short *>(row) + i);
@@ -116,7 +160,7 @@ __device__ __forceinline__ void merge_stat(float &m, float &S, int &idx, float m
 }
 
 __device__ __forceinline__ RowStat combine_parts(const Part *p, int n, float c) {
-  RowStat r{-INFINITY, 0.f, 0x7fffffff};
+  RowStat r{NO_MAX, 0.f, 0x7fffffff};
   for (int i = 0; i < n; ++i) merge_stat(r.m, r.S, r.idx, p[i].m, p[i].S, p[i].idx, c);
   return r;
 }

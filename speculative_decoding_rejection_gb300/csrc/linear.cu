@@ -135,17 +135,37 @@ __global__ void __launch_bounds__(1024) k_setup_linear(const LinearArgs a) {
 }
 
 // ------------------------------------------------------------ accept scan
-__device__ __forceinline__ RowStat target_stat(const LinearArgs &a, int row, float c) {
-  return combine_parts(a.part + (long long)row * a.nch_max * RS_CONS_WARPS,
-                       a.nch_t * RS_CONS_WARPS, c);
+// Row statistics combined by the whole warp: lane l merges partials
+// l, l+32, ..., then a butterfly merges the lanes (every lane gets the row's
+// statistics; the merge order is fixed, so the result is deterministic).
+__device__ __forceinline__ RowStat warp_row_stat(const Part *p, int n, float c, int lane) {
+  float m = NO_MAX, S = 0.f;
+  int idx = 0x7fffffff;
+  for (int i = lane; i < n; i += 32) {
+    const Part q = p[i];
+    merge_stat(m, S, idx, q.m, q.S, q.idx, c);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    merge_stat(m, S, idx, m2, S2, i2, c);
+  }
+  return RowStat{m, S, idx};
 }
-__device__ __forceinline__ RowStat draft_stat(const LinearArgs &a, int row, float c) {
-  return combine_parts(a.part + (long long)(a.rt_max + row) * a.nch_max * RS_CONS_WARPS,
-                       a.nch_d * RS_CONS_WARPS, c);
+__device__ __forceinline__ RowStat target_stat(const LinearArgs &a, int row, float c, int lane) {
+  return warp_row_stat(a.part + (long long)row * a.nch_max * RS_CONS_WARPS,
+                       a.nch_t * RS_CONS_WARPS, c, lane);
+}
+__device__ __forceinline__ RowStat draft_stat(const LinearArgs &a, int row, float c, int lane) {
+  return warp_row_stat(a.part + (long long)(a.rt_max + row) * a.nch_max * RS_CONS_WARPS,
+                       a.nch_d * RS_CONS_WARPS, c, lane);
 }
 
-// q(d) for draft row `row` (any order of the sparse ids).
-__device__ float draft_prob_at(const LinearArgs &a, int row, int d, float c) {
+// q(d) for draft row `row` given its statistics ds (dense logits), the
+// probability itself, or a search of the sparse ids (any order).
+__device__ float draft_prob_at(const LinearArgs &a, int row, int d, float c, RowStat ds) {
   if (a.sparse) {
     const int32_t *ids = a.draft_idx + (long long)row * SPEC_TOPK;
     const float *pr = a.sparse_prob + (long long)row * SPEC_TOPK;
@@ -155,8 +175,7 @@ __device__ float draft_prob_at(const LinearArgs &a, int row, int d, float c) {
   }
   const char *drow = a.draft + (long long)row * a.d_row_bytes;
   if (a.dk == SPEC_DRAFT_PROBS) return load_elem(drow, a.ddt, d);
-  const RowStat ds = draft_stat(a, row, c);
-  if (ds.m == -INFINITY) return 0.f;
+  if (row_empty(ds.m)) return 0.f;
   return ex2((load_elem(drow, a.ddt, d) - ds.m) * c) / ds.S;
 }
 
@@ -177,25 +196,36 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
   }
   const int K = r.K;
   const float c = r.c;
+  const bool sample = r.mode == MODE_SAMPLE;
   int n = K;
   for (int base = 0; base < K; base += 32) {
+    const int cnt = min(32, K - base);
+    // statistics of this block of positions: lane i keeps position base + i
+    RowStat ts{NO_MAX, 0.f, 0x7fffffff}, ds{NO_MAX, 0.f, 0x7fffffff};
+    for (int i = 0; i < cnt; ++i) {
+      const RowStat t = target_stat(a, r.t0 + base + i, c, lane);
+      if (lane == i) ts = t;
+      if (sample && a.stream_draft) {
+        const RowStat d = draft_stat(a, r.d0 + base + i, c, lane);
+        if (lane == i) ds = d;
+      }
+    }
     const int i = base + lane;
     bool rej = false;
-    if (i < K) {
+    if (lane < cnt) {
       const int d = a.tokens[r.d0 + i];
       const bool dok = (unsigned)d < (unsigned)a.V;
       if (!dok) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-      const RowStat ts = target_stat(a, r.t0 + i, c);
-      if (ts.m == -INFINITY) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+      if (row_empty(ts.m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
       float pd, qd;
-      if (r.mode == MODE_GREEDY) {
+      if (!sample) {
         rej = !(dok && d == ts.idx);
         pd = rej ? 0.f : 1.f;
         qd = -1.f;
-      } else if (dok && ts.m != -INFINITY) {
+      } else if (dok && !row_empty(ts.m)) {
         const char *trow = a.target + (long long)(r.t0 + i) * a.t_row_bytes;
         pd = ex2((load_elem(trow, a.tdt, d) - ts.m) * c) / ts.S;
-        qd = draft_prob_at(a, r.d0 + i, d, c);
+        qd = draft_prob_at(a, r.d0 + i, d, c, ds);
         const float acc = qd <= pd ? 1.f : pd / qd;
         rej = !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
       } else {
@@ -212,22 +242,21 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
     if (n == K && bal) n = base + __ffs(bal) - 1;
   }
   for (int j = lane; j < W; j += 32) out[j] = j < n ? a.tokens[r.d0 + j] : -1;
+  const RowStat tf = target_stat(a, r.t0 + n, c, lane);
+  RowStat df{NO_MAX, 0.f, 0x7fffffff};
+  if (sample && n < K && a.stream_draft) df = draft_stat(a, r.d0 + n, c, lane);
   __syncwarp();
   if (lane == 0) {
     a.out_accepted[b] = n;
     FinalInfo f{n, 0, 0.f, 0.f, 0.f, 0.f, {0, 0}};
-    const RowStat tf = target_stat(a, r.t0 + n, c);
-    if (r.mode == MODE_GREEDY) {
+    if (!sample) {
       out[n] = tf.idx;
     } else {
       f.kind = n < K ? 1 : 2;
       f.mt = tf.m;
       f.St = tf.S;
-      if (n < K && a.stream_draft) {
-        const RowStat df = draft_stat(a, r.d0 + n, c);
-        f.md = df.m;
-        f.Sd = df.S;
-      }
+      f.md = df.m;
+      f.Sd = df.S;
     }
     a.fin[b] = f;
   }
@@ -289,6 +318,7 @@ __device__ __forceinline__ void tile_weights(const LinearArgs &a, const SampleSm
 template <int DK>
 __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample(const LinearArgs a) {
   __shared__ SampleSmem sh;
+  extern __shared__ float wsum[];   // [tiles][32 warps]
   const int b = blockIdx.x;
   const ReqInfo r = a.req[b];
   if (r.mode != MODE_SAMPLE) return;
@@ -346,16 +376,26 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample(const LinearArgs a) {
   float u = uniform24(a.seed, (uint32_t)b, (uint32_t)(n + 1), kind == 1 ? 1u : 2u);
   float w[SAMPLE_EPT];
   for (int attempt = 0; attempt < 2; ++attempt) {
-    // pass 1: tile totals (same scan as the search pass, so they agree)
+    // pass 1: per-warp sums of every tile, no block-wide sync inside the
+    // streaming loop; then tile totals in a fixed order (warp 0)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll 2
     for (int j = 0; j < ntiles; ++j) {
       tile_weights<DK>(a, sh, trow, tvec, drow, dvec, kind, c, f.mt, invSt, f.md, invSd, j, w);
       float s = 0.f;
 #pragma unroll
       for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
-      float tot;
-      block_excl_scan(s, sh.scratch, &tot);
-      if (threadIdx.x == 0) sh.tsum[j] = tot;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) wsum[j * 32 + warp] = s;
     }
+    __syncthreads();
+    if (warp == 0)
+      for (int j = lane; j < ntiles; j += 32) {
+        float t = 0.f;
+        for (int q = 0; q < SAMPLE_THREADS / 32; ++q) t += wsum[j * 32 + q];
+        sh.tsum[j] = t;
+      }
     __syncthreads();
     if (threadIdx.x == 0) {
       float Z = 0.f;
@@ -519,12 +559,15 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
   if (rc != SPEC_OK) return rc;
   k_accept<<<(B + ACCEPT_WARPS - 1) / ACCEPT_WARPS, ACCEPT_WARPS * 32, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  if (a.sparse)
-    k_sample<SPEC_DRAFT_SPARSE128><<<B, SAMPLE_THREADS, 0, st>>>(a);
-  else if (dk == SPEC_DRAFT_PROBS)
-    k_sample<SPEC_DRAFT_PROBS><<<B, SAMPLE_THREADS, 0, st>>>(a);
-  else
-    k_sample<SPEC_DRAFT_LOGITS><<<B, SAMPLE_THREADS, 0, st>>>(a);
+  const size_t wsum_bytes = sizeof(float) * 32 * ((V + SAMPLE_TILE - 1) / SAMPLE_TILE);
+  void (*sampler)(LinearArgs) = a.sparse ? k_sample<SPEC_DRAFT_SPARSE128>
+                                : dk == SPEC_DRAFT_PROBS ? k_sample<SPEC_DRAFT_PROBS>
+                                                         : k_sample<SPEC_DRAFT_LOGITS>;
+  if (wsum_bytes > 48 * 1024 &&
+      cudaFuncSetAttribute(sampler, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)wsum_bytes) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  sampler<<<B, SAMPLE_THREADS, wsum_bytes, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }

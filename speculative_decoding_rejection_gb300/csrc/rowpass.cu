@@ -21,86 +21,153 @@
 
 namespace sv {
 
-struct StageMeta {
-  int slot;     // -1: no more work
-  int chunk;
-  int last;     // last stage of the chunk
-  int which;    // 0 target, 1 draft
-  int row;
-  int e_first;  // element index of the first vector element in the stage
-  int nvec;     // 16-byte vectors in the stage
-  float c;
-  int head_e, head_n, tail_e, tail_n;  // scalar elements (last stage only)
-  int pad;
-};
-
+// Stage metadata, two 16-byte records read with one shared load each:
+//   m0 = {slot (-1: no more work), chunk, e_first, flags}
+//   m1 = {c (float bits), row, head_e, tail_e}
+// flags: nvec (bits 0-11), last stage of its chunk (bit 12), draft tensor
+// (bit 13), head_n (bits 16-19), tail_n (bits 20-23).
 struct RowPassSmem {
   uint64_t full[NSTAGE];
   uint64_t empty[NSTAGE];
-  StageMeta meta[NSTAGE];
+  int4 m0[NSTAGE];
+  int4 m1[NSTAGE];
   int abort;
 };
 
-__device__ __forceinline__ void scalar_update(float x, int e, float c, float &m, float &S,
-                                              int &idx) {
-  if (x > m) {
-    if (c != 0.f) S *= ex2((m - x) * c);
-    m = x;
-    idx = e;
-  } else if (x == m && e < idx) {
-    idx = e;
-  }
-  if (c != 0.f && m != -INFINITY) S += ex2((x - m) * c);
+constexpr int FULL_NVEC = TILE_BYTES / 16;            // vectors in a full stage
+constexpr int NCT = RS_CONS_WARPS * 32;               // consumer threads
+constexpr int VEC_PER_THREAD = FULL_NVEC / NCT;       // 4
+static_assert(FULL_NVEC % NCT == 0, "full stages split evenly");
+static_assert((VEC_PER_THREAD & (VEC_PER_THREAD - 1)) == 0, "power-of-two vectors per thread");
+
+// Running state of one consumer thread over a chunk: max logit m, the
+// normaliser as a packed pair S2 (its two lanes summed at the chunk end) and
+// the lowest index attaining m.
+struct RunState {
+  float m;
+  f32x2 S2;
+  int idx;
+};
+
+__device__ __forceinline__ void rescale(RunState &st, float m_new, float c) {
+  const float f = ex2((st.m - m_new) * c);
+  st.S2 = mul2(st.S2, pk2(f, f));
+  st.m = m_new;
 }
 
-template <bool SOFTMAX>
-__device__ __forceinline__ void consume_bf16(const uint4 w, int e, float c, float &m, float &S,
-                                             int &idx) {
-  float x[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
-                bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
-  const float vm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
-                         fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
-  if (vm > m) {  // rare after the first few vectors
-    int j = 7;
+__device__ __forceinline__ void scalar_update(float x, int e, float c, RunState &st) {
+  if (x > st.m) {
+    if (c != 0.f) rescale(st, x, c);
+    st.m = x;
+    st.idx = e;
+  } else if (x == st.m && e < st.idx) {
+    st.idx = e;
+  }
+  if (c != 0.f) st.S2 = add2(st.S2, pk2(ex2((x - st.m) * c), 0.f));
+}
+
+// Generic path: one 16-byte vector (partial stages and fp32 rows).
+template <bool SOFTMAX, bool BF16>
+__device__ __forceinline__ void consume_vec(const uint4 w, int e, float c, RunState &st) {
+  constexpr int N = BF16 ? 8 : 4;
+  float x[N];
+  if (BF16) {
+    x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+    x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+  } else {
+    x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+  }
+  float vm = x[0];
 #pragma unroll
-    for (int k = 6; k >= 0; --k)
+  for (int k = 1; k < N; ++k) vm = fmaxf(vm, x[k]);
+  if (vm > st.m) {
+    int j = N - 1;
+#pragma unroll
+    for (int k = N - 2; k >= 0; --k)
       if (x[k] == vm) j = k;
-    if (SOFTMAX) S *= ex2((m - vm) * c);
-    m = vm;
-    idx = e + j;
+    if (SOFTMAX) rescale(st, vm, c);
+    st.m = vm;
+    st.idx = e + j;
   }
-  if (SOFTMAX && m != -INFINITY) {
-    float t[8];
+  if (SOFTMAX) {
+    const f32x2 c2 = pk2(c, c), nm = pk2(-st.m, -st.m);
+    f32x2 acc = pk2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t[k] = ex2((x[k] - m) * c);
-    S += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+    for (int k = 0; k < N; k += 2) {
+      const f32x2 t = mul2(add2(pk2(x[k], x[k + 1]), nm), c2);
+      acc = add2(acc, pk2(ex2(lo2(t)), ex2(hi2(t))));
+    }
+    st.S2 = add2(st.S2, acc);
   }
 }
 
+// Lowest element index holding `vm` among this thread's bf16 vectors of a
+// full stage (vector k sits at element e0 + 8 * NCT * k).
+__device__ __forceinline__ int first_index_of(const uint4 (&v)[VEC_PER_THREAD], float vm, int e0) {
+  int found = e0;
+  bool done = false;
+#pragma unroll
+  for (int k = 0; k < VEC_PER_THREAD; ++k) {
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = e0 + 8 * NCT * k + 2 * q;
+      if (!done && bf16lo(w[q]) == vm) { found = e; done = true; }
+      if (!done && bf16hi(w[q]) == vm) { found = e + 1; done = true; }
+    }
+  }
+  return found;
+}
+
+// Fast path: a full bf16 stage, 32 elements per thread. The max goes through
+// packed bf16 compares and is checked once; exponents are formed with
+// mixed-precision subtracts and packed multiplies, one 2^x per element, and
+// the 32 terms are summed as a packed pairwise tree.
 template <bool SOFTMAX>
-__device__ __forceinline__ void consume_f32(const uint4 w, int e, float c, float &m, float &S,
-                                            int &idx) {
-  float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                __uint_as_float(w.w)};
-  const float vm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-  if (vm > m) {
-    int j = 3;
+__device__ __forceinline__ void consume_full_bf16(const unsigned char *buf, int ctid, int e_first,
+                                                  float c, RunState &st) {
+  uint4 v[VEC_PER_THREAD];
 #pragma unroll
-    for (int k = 2; k >= 0; --k)
-      if (x[k] == vm) j = k;
-    if (SOFTMAX) S *= ex2((m - vm) * c);
-    m = vm;
-    idx = e + j;
+  for (int k = 0; k < VEC_PER_THREAD; ++k) v[k] = lds128(buf + 16 * (ctid + NCT * k));
+  uint32_t a[2 * VEC_PER_THREAD];
+#pragma unroll
+  for (int k = 0; k < VEC_PER_THREAD; ++k) {
+    a[2 * k] = bmax2(v[k].x, v[k].y);
+    a[2 * k + 1] = bmax2(v[k].z, v[k].w);
   }
-  if (SOFTMAX && m != -INFINITY) {
-    float t[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) t[k] = ex2((x[k] - m) * c);
-    S += (t[0] + t[1]) + (t[2] + t[3]);
+  for (int s = VEC_PER_THREAD; s > 0; s >>= 1)
+#pragma unroll
+    for (int i = 0; i < s; ++i) a[i] = bmax2(a[i], a[i + s]);
+  const float vm = fmaxf(bf16lo(a[0]), bf16hi(a[0]));
+  if (vm > st.m) {
+    const int e = first_index_of(v, vm, e_first + 8 * ctid);
+    if (SOFTMAX) rescale(st, vm, c);
+    st.m = vm;
+    st.idx = e;
+  }
+  if (SOFTMAX) {
+    const f32x2 c2 = pk2(c, c);
+    f32x2 e[4 * VEC_PER_THREAD];
+#pragma unroll
+    for (int k = 0; k < VEC_PER_THREAD; ++k) {
+      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const f32x2 t = mul2(bsub2(w[q], st.m), c2);
+        e[4 * k + q] = pk2(ex2(lo2(t)), ex2(hi2(t)));
+      }
+    }
+#pragma unroll
+    for (int s = 2 * VEC_PER_THREAD; s > 0; s >>= 1)
+#pragma unroll
+      for (int i = 0; i < s; ++i) e[i] = add2(e[i], e[i + s]);
+    st.S2 = add2(st.S2, e[0]);
   }
 }
 
-__global__ void __launch_bounds__(RS_THREADS, 2) k_row_pass(const RowPassArgs a) {
+__global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const RowPassArgs a) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ RowPassSmem sh;
   unsigned char *stage_buf = dsmem;
@@ -131,14 +198,16 @@ __global__ void __launch_bounds__(RS_THREADS, 2) k_row_pass(const RowPassArgs a)
       const int chunk = (int)(item % a.nch_max);
       const RowTask t = a.list[entry];
       const int w = t.which;
-      if (chunk < a.nch[w]) {
-        const int esz = dtype_size(a.dtype[w]);
-        const uint64_t row0 = (uint64_t)(a.base[w] + (long long)t.row * a.row_bytes[w]);
+      const long long rbytes = w ? a.row_bytes[1] : a.row_bytes[0];
+      if (chunk < (w ? a.nch[1] : a.nch[0])) {
+        const int esz = dtype_size(w ? a.dtype[1] : a.dtype[0]);
+        const uint64_t row0 = (uint64_t)((w ? a.base[1] : a.base[0]) + (long long)t.row * rbytes);
         const uint64_t cb0 = row0 + (uint64_t)chunk * CHUNK_BYTES;
-        const uint64_t cb1 = min(row0 + (uint64_t)a.row_bytes[w], cb0 + CHUNK_BYTES);
+        const uint64_t cb1 = min(row0 + (uint64_t)rbytes, cb0 + CHUNK_BYTES);
         uint64_t A0 = (cb0 + 15) & ~15ull, A1 = cb1 & ~15ull;
         if (A1 <= A0) A0 = A1 = cb1;  // no aligned interior: all scalar
         const int ntile = A1 > A0 ? (int)((A1 - A0 + TILE_BYTES - 1) / TILE_BYTES) : 1;
+        const int head_n = (int)((A0 - cb0) / esz), tail_n = (int)((cb1 - A1) / esz);
         for (int tl = 0; tl < ntile; ++tl) {
           const int s = (int)(it % NSTAGE);
           const long long use = it / NSTAGE;
@@ -148,19 +217,11 @@ __global__ void __launch_bounds__(RS_THREADS, 2) k_row_pass(const RowPassArgs a)
           }
           const uint64_t off = A0 + (uint64_t)tl * TILE_BYTES;
           const uint32_t nb = (uint32_t)min((uint64_t)TILE_BYTES, A1 - off);
-          StageMeta &md = sh.meta[s];
-          md.slot = t.slot;
-          md.chunk = chunk;
-          md.last = tl == ntile - 1;
-          md.which = w;
-          md.row = t.row;
-          md.e_first = (int)((off - row0) / esz);
-          md.nvec = (int)(nb / 16);
-          md.c = t.c;
-          md.head_e = (int)((cb0 - row0) / esz);
-          md.head_n = (int)((A0 - cb0) / esz);
-          md.tail_e = (int)((A1 - row0) / esz);
-          md.tail_n = (int)((cb1 - A1) / esz);
+          const int flags = (int)(nb / 16) | ((tl == ntile - 1) << 12) | (w << 13) |
+                            (head_n << 16) | (tail_n << 20);
+          sh.m0[s] = make_int4(t.slot, chunk, (int)((off - row0) / esz), flags);
+          sh.m1[s] = make_int4(__float_as_int(t.c), t.row, (int)((cb0 - row0) / esz),
+                               (int)((A1 - row0) / esz));
           if (nb > 0) {
             mbar_arrive_tx(&sh.full[s], nb);
             bulk_g2s(stage_buf + (size_t)s * TILE_BYTES, (const void *)off, nb, &sh.full[s]);
@@ -176,7 +237,7 @@ __global__ void __launch_bounds__(RS_THREADS, 2) k_row_pass(const RowPassArgs a)
       const int s = (int)(it % NSTAGE);
       const long long use = it / NSTAGE;
       if (use == 0 || mbar_wait_bounded(&sh.empty[s], (uint32_t)((use - 1) & 1), abort)) {
-        sh.meta[s].slot = -1;
+        sh.m0[s] = make_int4(-1, 0, 0, 0);
         mbar_arrive(&sh.full[s]);
         return;
       }
@@ -197,9 +258,7 @@ __global__ void __launch_bounds__(RS_THREADS, 2) k_row_pass(const RowPassArgs a)
   // -------------------------------------------------------------- consumers
   const int cw = warp - 1;
   const int ctid = threadIdx.x - 32;
-  constexpr int NCT = RS_CONS_WARPS * 32;
-  float m = -INFINITY, S = 0.f;
-  int idx = 0x7fffffff;
+  RunState st{NO_MAX, pk2(0.f, 0.f), 0x7fffffff};
   for (long long it = 0;; ++it) {
     const int s = (int)(it % NSTAGE);
     if (!mbar_wait_bounded(&sh.full[s], (uint32_t)((it / NSTAGE) & 1), abort)) {
@@ -207,39 +266,44 @@ __global__ void __launch_bounds__(RS_THREADS, 2) k_row_pass(const RowPassArgs a)
       *abort = 1;
       return;
     }
-    const StageMeta md = sh.meta[s];
-    if (md.slot < 0) return;
+    const int4 m0 = sh.m0[s];
+    if (m0.x < 0) return;
+    const int4 m1 = sh.m1[s];
+    const int nvec = m0.w & 0xfff;
+    const bool last = (m0.w >> 12) & 1;
+    const int which = (m0.w >> 13) & 1;
+    const int e_first = m0.z;
+    const float c = __int_as_float(m1.x);
+    const int dt = which ? a.dtype[1] : a.dtype[0];
+    const bool bf16 = dt == SPEC_BF16;
     const unsigned char *buf = stage_buf + (size_t)s * TILE_BYTES;
-    const float c = md.c;
-    if (a.dtype[md.which] == SPEC_BF16) {
-      if (c != 0.f) {
-        for (int v = ctid; v < md.nvec; v += NCT)
-          consume_bf16<true>(lds128(buf + 16 * v), md.e_first + 8 * v, c, m, S, idx);
-      } else {
-        for (int v = ctid; v < md.nvec; v += NCT)
-          consume_bf16<false>(lds128(buf + 16 * v), md.e_first + 8 * v, c, m, S, idx);
+    if (bf16 && nvec == FULL_NVEC) {
+      if (c != 0.f) consume_full_bf16<true>(buf, ctid, e_first, c, st);
+      else consume_full_bf16<false>(buf, ctid, e_first, c, st);
+    } else if (bf16) {
+      for (int v = ctid; v < nvec; v += NCT) {
+        if (c != 0.f) consume_vec<true, true>(lds128(buf + 16 * v), e_first + 8 * v, c, st);
+        else consume_vec<false, true>(lds128(buf + 16 * v), e_first + 8 * v, c, st);
       }
     } else {
-      if (c != 0.f) {
-        for (int v = ctid; v < md.nvec; v += NCT)
-          consume_f32<true>(lds128(buf + 16 * v), md.e_first + 4 * v, c, m, S, idx);
-      } else {
-        for (int v = ctid; v < md.nvec; v += NCT)
-          consume_f32<false>(lds128(buf + 16 * v), md.e_first + 4 * v, c, m, S, idx);
+      for (int v = ctid; v < nvec; v += NCT) {
+        if (c != 0.f) consume_vec<true, false>(lds128(buf + 16 * v), e_first + 4 * v, c, st);
+        else consume_vec<false, false>(lds128(buf + 16 * v), e_first + 4 * v, c, st);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
-    if (md.last) {
+    if (last) {
       if (cw == 0) {  // unaligned head / tail elements of the chunk
-        const char *row = a.base[md.which] + (long long)md.row * a.row_bytes[md.which];
-        const int dt = a.dtype[md.which];
-        if (lane < md.head_n)
-          scalar_update(load_elem(row, dt, md.head_e + lane), md.head_e + lane, c, m, S, idx);
-        if (lane >= 16 && lane - 16 < md.tail_n)
-          scalar_update(load_elem(row, dt, md.tail_e + lane - 16), md.tail_e + lane - 16, c, m,
-                        S, idx);
+        const int head_n = (m0.w >> 16) & 0xf, tail_n = (m0.w >> 20) & 0xf;
+        const char *row = (which ? a.base[1] : a.base[0]) +
+                          (long long)m1.y * (which ? a.row_bytes[1] : a.row_bytes[0]);
+        if (lane < head_n) scalar_update(load_elem(row, dt, m1.z + lane), m1.z + lane, c, st);
+        if (lane >= 16 && lane - 16 < tail_n)
+          scalar_update(load_elem(row, dt, m1.w + lane - 16), m1.w + lane - 16, c, st);
       }
+      float m = st.m, S = lo2(st.S2) + hi2(st.S2);
+      int idx = st.idx;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -253,11 +317,9 @@ __global__ void __launch_bounds__(RS_THREADS, 2) k_row_pass(const RowPassArgs a)
         p.S = S;
         p.idx = idx;
         p.pad = 0;
-        a.part[((long long)md.slot * a.nch_max + md.chunk) * RS_CONS_WARPS + cw] = p;
+        a.part[((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS + cw] = p;
       }
-      m = -INFINITY;
-      S = 0.f;
-      idx = 0x7fffffff;
+      st = RunState{NO_MAX, pk2(0.f, 0.f), 0x7fffffff};
     }
   }
 }
@@ -297,7 +359,7 @@ int launch_row_pass(const RowPassArgs &a, cudaStream_t stream) {
   cudaEvent_t before = prof_before, after = prof_after;
   prof_before = prof_after = nullptr;
   if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  k_row_pass<<<2 * sms, RS_THREADS, smem, stream>>>(a);
+  k_row_pass<<<RS_CTAS_PER_SM * sms, RS_THREADS, smem, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
