@@ -370,7 +370,8 @@ def main():
             else "fallback", "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
             "algorithmic_bytes_per_launch": rp_bytes, "ms_per_launch": rp_ms,
         },
-        "gpu_launches": K * (5 if lb.top128 else 4),
+        # setup, row pass, accept, sampler tiles, sampler final (+ top-128)
+        "gpu_launches": K * (6 if lb.top128 else 5),
         "clocks": clocks.summary(),
         "e2e": e2e,
     }

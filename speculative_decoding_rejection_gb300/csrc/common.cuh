@@ -20,7 +20,7 @@ constexpr int NSTAGE = 2;           // pipeline depth per CTA
 constexpr int RS_CONS_WARPS = 4;    // consumer warps of the row pass
 constexpr int RS_CTAS_PER_SM = 6;   // resident row-pass CTAs per SM
 constexpr int RS_THREADS = 32 * (1 + RS_CONS_WARPS);
-constexpr int SAMPLE_THREADS = 1024;
+constexpr int SAMPLE_THREADS = 256;
 constexpr int SAMPLE_EPT = 16;      // contiguous elements per thread per tile
 constexpr int SAMPLE_TILE = SAMPLE_THREADS * SAMPLE_EPT;
 constexpr int MAX_SAMPLE_TILES = (SPEC_MAX_V + SAMPLE_TILE - 1) / SAMPLE_TILE;
@@ -36,7 +36,10 @@ struct WsHeader {        // first 256 bytes of every workspace
   int detail;            // first offending request / row, -1 if none
   unsigned int work;     // dynamic work counter of the row pass
   int n_list;            // rows in the row-pass list
-  int pad[60];
+  int n_jobs_a;          // final draws over full residual rows (dense drafts)
+  int n_jobs_b;          // final draws located from chunk statistics
+  unsigned int work2;    // dynamic work counter of the residual tile sums
+  int pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -20,12 +20,13 @@ namespace sv {
 
 constexpr int ACCEPT_WARPS = 8;
 
-struct FinalInfo {   // per request, written by the accept kernel
+struct Job {         // one final draw of a sampling request (accept kernel)
+  int b;             // request
   int n;             // accepted drafts
-  int kind;          // 0: final token already written, 1: residual, 2: bonus
+  int kind;          // 1: residual after a rejection, 2: bonus
+  int pad;
   float mt, St;      // statistics of target row n+1
   float md, Sd;      // statistics of draft row n+1 (dense logits only)
-  int pad[2];
 };
 
 struct LinearArgs {
@@ -44,7 +45,11 @@ struct LinearArgs {
   float *out_pq;
   WsHeader *hdr;
   ReqInfo *req;
-  FinalInfo *fin;
+  Job *jobs_a;                // residual draws over dense draft rows
+  Job *jobs_b;                // bonus draws and sparse residual draws
+  float *tsum;                // [B][ntiles] residual tile sums of jobs_a
+  int ntiles;
+  long long rows_max;
   RowTask *list;
   Part *part;
   long long t_row_bytes, d_row_bytes;
@@ -55,7 +60,7 @@ struct LinearArgs {
 };
 
 struct LinearLayout {
-  size_t hdr, req, fin, list, part, tk_idx, tk_prob, total;
+  size_t hdr, req, jobs_a, jobs_b, tsum, list, part, tk_idx, tk_prob, total;
   int nch_max;
   long long rows_max;
 };
@@ -67,7 +72,9 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   size_t o = 0;
   L.hdr = o;  o += align256(sizeof(WsHeader));
   L.req = o;  o += align256(sizeof(ReqInfo) * (size_t)B);
-  L.fin = o;  o += align256(sizeof(FinalInfo) * (size_t)B);
+  L.jobs_a = o; o += align256(sizeof(Job) * (size_t)B);
+  L.jobs_b = o; o += align256(sizeof(Job) * (size_t)B);
+  L.tsum = o; o += align256(sizeof(float) * (size_t)B * ((V + SAMPLE_TILE - 1) / SAMPLE_TILE));
   L.list = o; o += align256(sizeof(RowTask) * (size_t)L.rows_max);
   L.part = o; o += align256(sizeof(Part) * (size_t)L.rows_max * L.nch_max * RS_CONS_WARPS);
   const size_t tk = rule == SPEC_RULE_STRICT_TOP128 ? (size_t)B * max_k * SPEC_TOPK : 0;
@@ -78,60 +85,48 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
 }
 
 // ------------------------------------------------------------------ setup
-__global__ void __launch_bounds__(1024) k_setup_linear(const LinearArgs a) {
-  __shared__ int scratch[33];
-  if (threadIdx.x == 0) {
-    a.hdr->status = SPEC_OK;
-    a.hdr->detail = -1;
-    a.hdr->work = 0;
-    a.hdr->n_list = 0;
-  }
-  __syncthreads();
-  const int per = (a.B + blockDim.x - 1) / blockDim.x;
-  const int b0 = min(a.B, (int)threadIdx.x * per), b1 = min(a.B, b0 + per);
-  const bool cu0_ok = a.B == 0 || a.cu[0] == 0;
-  int cnt = 0;
-  for (int b = b0; b < b1; ++b) {
-    ReqInfo r;
-    const int K = a.cu[b + 1] - a.cu[b];
-    const float T = a.temp[b];
-    r.t0 = a.cu[b] + b;
-    r.d0 = a.cu[b];
-    r.K = K;
-    r.n = 0;
-    r.pad[0] = r.pad[1] = 0;
-    const bool greedy = a.rule == SPEC_RULE_GREEDY || T < SPEC_GREEDY_T;
-    bool ok = cu0_ok && K >= 0 && K <= a.max_k && a.cu[b] >= 0 && T >= 0.f && isfinite(T);
-    if (ok && !greedy && a.draft == nullptr) ok = false;
-    if (!ok) {
-      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-      r.mode = MODE_SKIP;
-      r.c = 0.f;
-    } else {
-      r.mode = greedy ? MODE_GREEDY : MODE_SAMPLE;
-      r.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);
-      cnt += (K + 1) + ((r.mode == MODE_SAMPLE && a.stream_draft) ? K : 0);
-    }
+// One thread per request. The row list is indexed by slot (target row r at
+// position r, draft row r at position rt_max + r), so every thread writes its
+// own entries without a scan; positions no request owns are marked unused.
+// The header was cleared before the launch; an invalid request sets the
+// status word, which makes every later kernel of the call skip its work.
+__global__ void __launch_bounds__(256) k_setup_linear(const LinearArgs a) {
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int gsize = gridDim.x * blockDim.x;
+  if (gtid == 0) a.hdr->n_list = (int)a.rows_max;
+  const long long dmax = a.rows_max - a.rt_max;
+  const long long Rd = a.B > 0 ? min(max((long long)a.cu[a.B], 0LL), dmax) : 0;
+  const long long Rt = min(Rd + a.B, (long long)a.rt_max);
+  for (long long p = Rt + gtid; p < a.rt_max; p += gsize) a.list[p].slot = -1;
+  for (long long p = a.rt_max + Rd + gtid; p < a.rows_max; p += gsize) a.list[p].slot = -1;
+  const int b = gtid;
+  if (b >= a.B) return;
+  ReqInfo r;
+  const int K = a.cu[b + 1] - a.cu[b];
+  const float T = a.temp[b];
+  r.t0 = a.cu[b] + b;
+  r.d0 = a.cu[b];
+  r.K = K;
+  r.n = 0;
+  r.pad[0] = r.pad[1] = 0;
+  const bool greedy = a.rule == SPEC_RULE_GREEDY || T < SPEC_GREEDY_T;
+  bool ok = (b > 0 || a.cu[0] == 0) && K >= 0 && K <= a.max_k && a.cu[b] >= 0 &&
+            (long long)a.cu[b + 1] <= dmax && T >= 0.f && isfinite(T);
+  if (ok && !greedy && a.draft == nullptr) ok = false;
+  if (!ok) {
+    set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+    r.mode = MODE_SKIP;
+    r.c = 0.f;
     a.req[b] = r;
+    return;
   }
-  // Row offsets of one request are only in bounds when all of cu_draft is
-  // well formed, so any invalid request disables the whole call.
-  int local_bad = 0;
-  for (int b = b0; b < b1; ++b) local_bad |= a.req[b].mode == MODE_SKIP;
-  if (__syncthreads_or(local_bad)) {
-    for (int b = b0; b < b1; ++b) a.req[b].mode = MODE_SKIP;
-    return;  // n_list stays 0
-  }
-  int total;
-  int off = block_excl_scan_int(cnt, scratch, &total);
-  for (int b = b0; b < b1; ++b) {
-    const ReqInfo r = a.req[b];
-    if (r.mode == MODE_SKIP) continue;
-    for (int i = 0; i <= r.K; ++i) a.list[off++] = RowTask{r.t0 + i, r.t0 + i, 0, r.c};
-    if (r.mode == MODE_SAMPLE && a.stream_draft)
-      for (int i = 0; i < r.K; ++i) a.list[off++] = RowTask{a.rt_max + r.d0 + i, r.d0 + i, 1, r.c};
-  }
-  if (threadIdx.x == 0) a.hdr->n_list = total;
+  r.mode = greedy ? MODE_GREEDY : MODE_SAMPLE;
+  r.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);
+  a.req[b] = r;
+  for (int i = 0; i <= K; ++i) a.list[r.t0 + i] = RowTask{r.t0 + i, r.t0 + i, 0, r.c};
+  const bool drafts = r.mode == MODE_SAMPLE && a.stream_draft;
+  for (int i = 0; i < K; ++i)
+    a.list[a.rt_max + r.d0 + i] = RowTask{drafts ? a.rt_max + r.d0 + i : -1, r.d0 + i, 1, r.c};
 }
 
 // ------------------------------------------------------------ accept scan
@@ -183,17 +178,15 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
   const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= a.B) return;
-  const ReqInfo r = a.req[b];
   const int W = a.max_k + 1;
   int32_t *out = a.out_tokens + (long long)b * W;
-  if (r.mode == MODE_SKIP) {
+  // inputs rejected by the setup (or an expired wait): no request is verified
+  if (*(volatile int *)&a.hdr->status != SPEC_OK) {
     for (int j = lane; j < W; j += 32) out[j] = -1;
-    if (lane == 0) {
-      a.out_accepted[b] = -1;
-      a.fin[b] = FinalInfo{0, 0, 0.f, 0.f, 0.f, 0.f, {0, 0}};
-    }
+    if (lane == 0) a.out_accepted[b] = -1;
     return;
   }
+  const ReqInfo r = a.req[b];
   const int K = r.K;
   const float c = r.c;
   const bool sample = r.mode == MODE_SAMPLE;
@@ -248,30 +241,31 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
   __syncwarp();
   if (lane == 0) {
     a.out_accepted[b] = n;
-    FinalInfo f{n, 0, 0.f, 0.f, 0.f, 0.f, {0, 0}};
     if (!sample) {
       out[n] = tf.idx;
     } else {
-      f.kind = n < K ? 1 : 2;
-      f.mt = tf.m;
-      f.St = tf.S;
-      f.md = df.m;
-      f.Sd = df.S;
+      const Job j{b, n, n < K ? 1 : 2, 0, tf.m, tf.S, df.m, df.S};
+      if (j.kind == 1 && !a.sparse) a.jobs_a[atomicAdd(&a.hdr->n_jobs_a, 1)] = j;
+      else a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = j;
     }
-    a.fin[b] = f;
   }
 }
 
 // --------------------------------------------------- final-token sampler
+// Tiles of SAMPLE_TILE elements; thread t of a SAMPLE_THREADS block owns
+// elements [tile + 16 t, tile + 16 t + 16).
 struct SampleSmem {
-  float tsum[MAX_SAMPLE_TILES];
   float scratch[33];
+  float wsum[SAMPLE_THREADS / 32];
+  float csum[64];            // per-tile sums inside one chunk (<= 16 tiles)
+  float corr[1024];          // sparse corrections per chunk
   int s_idx[SPEC_TOPK];
   float s_prob[SPEC_TOPK];
   int n_sparse;
   int jstar;
   float carry, target, Z;
   int xmin, xlast;
+  int kind;
 };
 
 // Weights of this thread's SAMPLE_EPT elements of tile j: the residual
@@ -315,33 +309,288 @@ __device__ __forceinline__ void tile_weights(const LinearArgs &a, const SampleSm
   }
 }
 
-template <int DK>
-__global__ void __launch_bounds__(SAMPLE_THREADS) k_sample(const LinearArgs a) {
-  __shared__ SampleSmem sh;
-  extern __shared__ float wsum[];   // [tiles][32 warps]
-  const int b = blockIdx.x;
-  const ReqInfo r = a.req[b];
-  if (r.mode != MODE_SAMPLE) return;
-  const FinalInfo f = a.fin[b];
-  if (f.kind == 0) return;
-  const int n = f.n;
-  const float c = r.c;
-  const char *trow = a.target + (long long)(r.t0 + n) * a.t_row_bytes;
-  const bool tvec = ((uintptr_t)trow & 15) == 0;
-  const char *drow = nullptr;
-  bool dvec = false;
-  if (f.kind == 1 && !a.sparse) {
-    drow = a.draft + (long long)(r.d0 + n) * a.d_row_bytes;
-    dvec = ((uintptr_t)drow & 15) == 0;
+// Block sum of one float per thread in a fixed order (warp butterflies,
+// then warp 0 over the warp sums); the result is returned to every thread.
+__device__ __forceinline__ float block_sum(float v, SampleSmem &sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sh.wsum[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int q = 0; q < SAMPLE_THREADS / 32; ++q) t += sh.wsum[q];
+    sh.scratch[32] = t;
   }
-  if (DK == SPEC_DRAFT_SPARSE128 && f.kind == 1) {
-    // gather this row's sparse law and sort it by id (bitonic, 128 keys)
+  __syncthreads();
+  const float t = sh.scratch[32];
+  __syncthreads();
+  return t;
+}
+
+struct JobRows {
+  const char *trow, *drow;
+  bool tvec, dvec;
+  float c, mt, invSt, md, invSd;
+};
+
+__device__ __forceinline__ JobRows job_rows(const LinearArgs &a, const Job &j) {
+  const ReqInfo r = a.req[j.b];
+  JobRows q;
+  q.trow = a.target + (long long)(r.t0 + j.n) * a.t_row_bytes;
+  q.tvec = ((uintptr_t)q.trow & 15) == 0;
+  q.drow = nullptr;
+  q.dvec = false;
+  if (j.kind == 1 && !a.sparse) {
+    q.drow = a.draft + (long long)(r.d0 + j.n) * a.d_row_bytes;
+    q.dvec = ((uintptr_t)q.drow & 15) == 0;
+  }
+  q.c = r.c;
+  q.mt = j.mt;
+  q.invSt = 1.f / j.St;
+  q.md = j.md;
+  q.invSd = j.Sd > 0.f ? 1.f / j.Sd : 0.f;
+  return q;
+}
+
+// Residual tile sums of the dense-draft residual draws. Persistent blocks
+// take (job, pair of tiles) items from a counter; the loads of both tiles are
+// issued before any arithmetic, so every SM keeps many rows' bytes in flight.
+constexpr int TILES_PER_ITEM = 2;
+
+template <int DK>
+__global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_tiles(const LinearArgs a) {
+  __shared__ SampleSmem sh;
+  __shared__ int s_item;
+  const int na = *(volatile int *)&a.hdr->n_jobs_a;
+  const int ipj = (a.ntiles + TILES_PER_ITEM - 1) / TILES_PER_ITEM;
+  const long long n_items = (long long)na * ipj;
+  while (true) {
+    if (threadIdx.x == 0) s_item = (int)atomicAdd(&a.hdr->work2, 1u);
+    __syncthreads();
+    const long long item = s_item;
+    __syncthreads();
+    if (item >= n_items) return;
+    const int ja = (int)(item / ipj);
+    const int j0 = (int)(item % ipj) * TILES_PER_ITEM;
+    const Job job = a.jobs_a[ja];
+    const JobRows q = job_rows(a, job);
+    const int xa = j0 * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
+    const bool fast = DK == SPEC_DRAFT_LOGITS && a.tdt == SPEC_BF16 && a.ddt == SPEC_BF16 &&
+                      q.tvec && q.dvec && j0 + TILES_PER_ITEM <= a.ntiles &&
+                      (j0 + TILES_PER_ITEM) * SAMPLE_TILE <= a.V;
+    if (fast) {
+      // both tiles' packed bf16 in registers first, arithmetic after
+      uint4 rt[TILES_PER_ITEM][2], rd[TILES_PER_ITEM][2];
+#pragma unroll
+      for (int u = 0; u < TILES_PER_ITEM; ++u) {
+        const uint4 *pt = reinterpret_cast<const uint4 *>(q.trow + 2LL * (xa + u * SAMPLE_TILE));
+        const uint4 *pd = reinterpret_cast<const uint4 *>(q.drow + 2LL * (xa + u * SAMPLE_TILE));
+        rt[u][0] = __ldg(pt); rt[u][1] = __ldg(pt + 1);
+        rd[u][0] = __ldg(pd); rd[u][1] = __ldg(pd + 1);
+      }
+#pragma unroll
+      for (int u = 0; u < TILES_PER_ITEM; ++u) {
+        float s = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t wt[4] = {rt[u][h].x, rt[u][h].y, rt[u][h].z, rt[u][h].w};
+          const uint32_t wd[4] = {rd[u][h].x, rd[u][h].y, rd[u][h].z, rd[u][h].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float p0 = ex2((bf16lo(wt[k]) - q.mt) * q.c) * q.invSt;
+            const float p1 = ex2((bf16hi(wt[k]) - q.mt) * q.c) * q.invSt;
+            const float q0 = ex2((bf16lo(wd[k]) - q.md) * q.c) * q.invSd;
+            const float q1 = ex2((bf16hi(wd[k]) - q.md) * q.c) * q.invSd;
+            s += fmaxf(0.f, p0 - q0) + fmaxf(0.f, p1 - q1);
+          }
+        }
+        const float t = block_sum(s, sh);
+        if (threadIdx.x == 0) a.tsum[(long long)ja * a.ntiles + j0 + u] = t;
+      }
+    } else {
+      for (int u = 0; u < TILES_PER_ITEM && j0 + u < a.ntiles; ++u) {
+        float zt[SAMPLE_EPT], zd[SAMPLE_EPT];
+        const int x0 = xa + u * SAMPLE_TILE;
+        load_ept(q.trow, a.tdt, q.tvec, x0, a.V, -INFINITY, zt);
+        load_ept(q.drow, a.ddt, q.dvec, x0, a.V, DK == SPEC_DRAFT_PROBS ? 0.f : -INFINITY, zd);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < SAMPLE_EPT; ++k) {
+          const float p = ex2((zt[k] - q.mt) * q.c) * q.invSt;
+          const float qq = DK == SPEC_DRAFT_PROBS ? zd[k] : ex2((zd[k] - q.md) * q.c) * q.invSd;
+          s += fmaxf(0.f, p - qq);
+        }
+        const float t = block_sum(s, sh);
+        if (threadIdx.x == 0) a.tsum[(long long)ja * a.ntiles + j0 + u] = t;
+      }
+    }
+  }
+}
+
+// Inverse-CDF step inside tile js: the smallest x with carry + C(x) > target,
+// else the last positive weight of the tile (rounding). Every thread returns x.
+template <int DK>
+__device__ int fine_draw(const LinearArgs &a, SampleSmem &sh, const JobRows &q, int kind, int js) {
+  if (threadIdx.x == 0) {
+    sh.xmin = 0x7fffffff;
+    sh.xlast = -1;
+  }
+  __syncthreads();
+  float w[SAMPLE_EPT];
+  tile_weights<DK>(a, sh, q.trow, q.tvec, q.drow, q.dvec, kind, q.c, q.mt, q.invSt, q.md,
+                   q.invSd, js, w);
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
+  float tot;
+  const float excl = block_excl_scan(s, sh.scratch, &tot);
+  const int x0 = js * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
+  float pre = 0.f;
+  int cand = 0x7fffffff, lastpos = -1;
+#pragma unroll
+  for (int k = 0; k < SAMPLE_EPT; ++k) {
+    pre += w[k];
+    if (cand == 0x7fffffff && sh.carry + (excl + pre) > sh.target) cand = x0 + k;
+    if (w[k] > 0.f) lastpos = x0 + k;
+  }
+  if (cand != 0x7fffffff) atomicMin(&sh.xmin, cand);
+  if (lastpos >= 0) atomicMax(&sh.xlast, lastpos);
+  __syncthreads();
+  const int x = sh.xmin != 0x7fffffff ? sh.xmin : sh.xlast;
+  __syncthreads();
+  return x;
+}
+
+// Bonus draws and sparse residual draws: the chunk holding the target mass
+// is found from the row pass's per-chunk statistics of the target row (minus
+// the sparse corrections min(p, q) at the listed ids), so only that chunk of
+// the row is read again.
+template <int DK>
+__device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, const JobRows &q,
+                          int kind, float u) {
+  const ReqInfo r = a.req[job.b];
+  const int esz = dtype_size(a.tdt);
+  const int chunk_elems = CHUNK_BYTES / esz;
+  const int tpc = chunk_elems / SAMPLE_TILE;  // tiles per chunk
+  const int nch = a.nch_t;
+  const Part *pp = a.part + (long long)(r.t0 + job.n) * a.nch_max * RS_CONS_WARPS;
+  for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
+    float m = 0.f;
+    for (int w = 0; w < RS_CONS_WARPS; ++w) {
+      const Part p = pp[ch * RS_CONS_WARPS + w];
+      m += p.S * ex2((p.m - q.mt) * q.c);
+    }
+    sh.corr[ch] = m * q.invSt;   // chunk mass of p
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (kind == 1 && DK == SPEC_DRAFT_SPARSE128) {
+      for (int k = 0; k < sh.n_sparse; ++k) {
+        const int id = sh.s_idx[k];
+        const float p = ex2((load_elem(q.trow, a.tdt, id) - q.mt) * q.c) * q.invSt;
+        sh.corr[id / chunk_elems] -= fminf(p, sh.s_prob[k]);
+      }
+    }
+    float Z = 0.f;
+    for (int ch = 0; ch < nch; ++ch) Z += fmaxf(sh.corr[ch], 0.f);
+    sh.Z = Z;
+    sh.target = u * Z;
+    float carry = 0.f;
+    int cs = -1;
+    for (int ch = 0; ch < nch; ++ch) {
+      const float nc = carry + fmaxf(sh.corr[ch], 0.f);
+      if (nc > sh.target) { cs = ch; break; }
+      carry = nc;
+    }
+    if (cs < 0)
+      for (int ch = nch - 1; ch >= 0 && cs < 0; --ch)
+        if (sh.corr[ch] > 0.f) cs = ch;
+    sh.jstar = cs;
+    sh.carry = carry;
+  }
+  __syncthreads();
+  const int cs = sh.jstar;
+  if (cs < 0) return -1;
+  // tile sums inside the chunk, then the tile, then the element
+  const int j0 = cs * tpc, j1 = min(a.ntiles, j0 + tpc);
+  float w[SAMPLE_EPT];
+  for (int j = j0; j < j1; ++j) {
+    tile_weights<DK>(a, sh, q.trow, q.tvec, q.drow, q.dvec, kind, q.c, q.mt, q.invSt, q.md,
+                     q.invSd, j, w);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
+    const float t = block_sum(s, sh);
+    if (threadIdx.x == 0) sh.csum[j - j0] = t;
+  }
+  if (threadIdx.x == 0) {
+    float carry = sh.carry;
+    int js = -1;
+    for (int j = j0; j < j1; ++j) {
+      const float nc = carry + sh.csum[j - j0];
+      if (nc > sh.target) { js = j; break; }
+      carry = nc;
+    }
+    if (js < 0)
+      for (int j = j1 - 1; j >= j0 && js < 0; --j)
+        if (sh.csum[j - j0] > 0.f) js = j;
+    sh.jstar = js;
+    sh.carry = carry;
+  }
+  __syncthreads();
+  const int js = sh.jstar;
+  if (js < 0) return -1;
+  return fine_draw<DK>(a, sh, q, kind, js);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArgs a) {
+  __shared__ SampleSmem sh;
+  const int g = blockIdx.x;
+  const int na = *(volatile int *)&a.hdr->n_jobs_a, nb = *(volatile int *)&a.hdr->n_jobs_b;
+  if (g >= na + nb) return;
+  const bool dense = g < na;
+  const Job job = dense ? a.jobs_a[g] : a.jobs_b[g - na];
+  const JobRows q = job_rows(a, job);
+  const float u = uniform24(a.seed, (uint32_t)job.b, (uint32_t)(job.n + 1), job.kind == 1 ? 1u : 2u);
+  int x = -1;
+  bool done = false;
+  if (dense) {
+    if (threadIdx.x == 0) {
+      const float *ts = a.tsum + (long long)g * a.ntiles;
+      float Z = 0.f;
+      for (int j = 0; j < a.ntiles; ++j) Z += ts[j];
+      sh.Z = Z;
+      sh.target = u * Z;
+      float carry = 0.f;
+      int js = -1;
+      for (int j = 0; j < a.ntiles; ++j) {
+        const float nc = carry + ts[j];
+        if (nc > sh.target) { js = j; break; }
+        carry = nc;
+      }
+      if (js < 0)
+        for (int j = a.ntiles - 1; j >= 0 && js < 0; --j)
+          if (ts[j] > 0.f) js = j;
+      sh.jstar = js;
+      sh.carry = carry;
+    }
+    __syncthreads();
+    if (sh.Z > 0.f && sh.jstar >= 0) {
+      x = fine_draw<DK>(a, sh, q, 1, sh.jstar);
+      done = true;
+    }
+    // no residual mass (p == q): the same u draws from p
+  } else if (DK == SPEC_DRAFT_SPARSE128 && job.kind == 1) {
+    const ReqInfo r = a.req[job.b];
     const int t = threadIdx.x;
-    if (t < SPEC_TOPK) {
-      const int id = a.draft_idx[(long long)(r.d0 + n) * SPEC_TOPK + t];
+    if (t < SPEC_TOPK) {   // the row's sparse law, sorted by id (bitonic)
+      const long long row = (long long)(r.d0 + job.n) * SPEC_TOPK + t;
+      const int id = a.draft_idx[row];
       const bool ok = id >= 0 && id < a.V;
       sh.s_idx[t] = ok ? id : 0x7fffffff;
-      sh.s_prob[t] = ok ? a.sparse_prob[(long long)(r.d0 + n) * SPEC_TOPK + t] : 0.f;
+      sh.s_prob[t] = ok ? a.sparse_prob[row] : 0.f;
     }
     __syncthreads();
     for (int size = 2; size <= SPEC_TOPK; size <<= 1) {
@@ -366,89 +615,14 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample(const LinearArgs a) {
       while (cnt < SPEC_TOPK && sh.s_idx[cnt] != 0x7fffffff) ++cnt;
       sh.n_sparse = cnt;
     }
-  }
-  __syncthreads();
-
-  const float invSt = 1.f / f.St;
-  const float invSd = f.Sd > 0.f ? 1.f / f.Sd : 0.f;
-  const int ntiles = (a.V + SAMPLE_TILE - 1) / SAMPLE_TILE;
-  int kind = f.kind;
-  float u = uniform24(a.seed, (uint32_t)b, (uint32_t)(n + 1), kind == 1 ? 1u : 2u);
-  float w[SAMPLE_EPT];
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    // pass 1: per-warp sums of every tile, no block-wide sync inside the
-    // streaming loop; then tile totals in a fixed order (warp 0)
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll 2
-    for (int j = 0; j < ntiles; ++j) {
-      tile_weights<DK>(a, sh, trow, tvec, drow, dvec, kind, c, f.mt, invSt, f.md, invSd, j, w);
-      float s = 0.f;
-#pragma unroll
-      for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) wsum[j * 32 + warp] = s;
-    }
     __syncthreads();
-    if (warp == 0)
-      for (int j = lane; j < ntiles; j += 32) {
-        float t = 0.f;
-        for (int q = 0; q < SAMPLE_THREADS / 32; ++q) t += wsum[j * 32 + q];
-        sh.tsum[j] = t;
-      }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float Z = 0.f;
-      for (int j = 0; j < ntiles; ++j) Z += sh.tsum[j];
-      sh.Z = Z;
-      sh.target = u * Z;
-      float carry = 0.f;
-      int js = -1;
-      for (int j = 0; j < ntiles; ++j) {
-        const float nc = carry + sh.tsum[j];
-        if (nc > sh.target) { js = j; break; }
-        carry = nc;
-      }
-      if (js < 0)  // rounding left u*Z >= Z: the last tile with mass
-        for (int j = ntiles - 1; j >= 0 && js < 0; --j)
-          if (sh.tsum[j] > 0.f) js = j;
-      sh.jstar = js;
-      sh.carry = carry;
-      sh.xmin = 0x7fffffff;
-      sh.xlast = -1;
-    }
-    __syncthreads();
-    if (sh.Z > 0.f || kind == 2) break;
-    kind = 2;  // the residual has no mass (p == q): draw from p instead
+    x = chunk_draw<DK>(a, sh, job, q, 1, u);
+    done = sh.Z > 0.f;
   }
-  const int js = sh.jstar;
-  if (js >= 0) {
-    tile_weights<DK>(a, sh, trow, tvec, drow, dvec, kind, c, f.mt, invSt, f.md, invSd, js, w);
-    float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
-    float tot;
-    const float excl = block_excl_scan(s, sh.scratch, &tot);
-    const int x0 = js * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
-    float pre = 0.f;
-    int cand = 0x7fffffff, lastpos = -1;
-#pragma unroll
-    for (int k = 0; k < SAMPLE_EPT; ++k) {
-      pre += w[k];
-      if (cand == 0x7fffffff && sh.carry + (excl + pre) > sh.target) cand = x0 + k;
-      if (w[k] > 0.f) lastpos = x0 + k;
-    }
-    if (cand != 0x7fffffff) atomicMin(&sh.xmin, cand);
-    if (lastpos >= 0) atomicMax(&sh.xlast, lastpos);
-  }
-  __syncthreads();
+  if (!done) x = chunk_draw<DK>(a, sh, job, q, 2, u);   // bonus, or residual without mass
   if (threadIdx.x == 0) {
-    int x = sh.xmin != 0x7fffffff ? sh.xmin : sh.xlast;
-    if (x < 0) {
-      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);  // a row without mass
-      x = -1;
-    }
-    a.out_tokens[(long long)b * (a.max_k + 1) + n] = x;
+    if (x < 0) set_status(a.hdr, SPEC_ERR_INVALID_ARG, job.b);   // a row without mass
+    a.out_tokens[(long long)job.b * (a.max_k + 1) + job.n] = x;
   }
 }
 
@@ -509,7 +683,11 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
   a.out_pq = out_pq;
   a.hdr = reinterpret_cast<WsHeader *>(ws + L.hdr);
   a.req = reinterpret_cast<ReqInfo *>(ws + L.req);
-  a.fin = reinterpret_cast<FinalInfo *>(ws + L.fin);
+  a.jobs_a = reinterpret_cast<Job *>(ws + L.jobs_a);
+  a.jobs_b = reinterpret_cast<Job *>(ws + L.jobs_b);
+  a.tsum = reinterpret_cast<float *>(ws + L.tsum);
+  a.ntiles = (V + SAMPLE_TILE - 1) / SAMPLE_TILE;
+  a.rows_max = L.rows_max;
   a.list = reinterpret_cast<RowTask *>(ws + L.list);
   a.part = reinterpret_cast<Part *>(ws + L.part);
   a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
@@ -533,9 +711,10 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  k_setup_linear<<<1, 1024, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
+  k_setup_linear<<<(B + 255) / 256, 256, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (rule == SPEC_RULE_STRICT_TOP128) {
     const int rc = launch_topk128(draft, ddt, B * max_k, V, cu_draft, temperature, B,
                                   reinterpret_cast<int32_t *>(ws + L.tk_idx),
@@ -559,15 +738,16 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
   if (rc != SPEC_OK) return rc;
   k_accept<<<(B + ACCEPT_WARPS - 1) / ACCEPT_WARPS, ACCEPT_WARPS * 32, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  const size_t wsum_bytes = sizeof(float) * 32 * ((V + SAMPLE_TILE - 1) / SAMPLE_TILE);
-  void (*sampler)(LinearArgs) = a.sparse ? k_sample<SPEC_DRAFT_SPARSE128>
-                                : dk == SPEC_DRAFT_PROBS ? k_sample<SPEC_DRAFT_PROBS>
-                                                         : k_sample<SPEC_DRAFT_LOGITS>;
-  if (wsum_bytes > 48 * 1024 &&
-      cudaFuncSetAttribute(sampler, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)wsum_bytes) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  sampler<<<B, SAMPLE_THREADS, wsum_bytes, st>>>(a);
+  const int tiles_grid = 8 * num_sms();
+  if (a.sparse) {
+    k_sample_final<SPEC_DRAFT_SPARSE128><<<B, SAMPLE_THREADS, 0, st>>>(a);
+  } else if (dk == SPEC_DRAFT_PROBS) {
+    k_sample_tiles<SPEC_DRAFT_PROBS><<<tiles_grid, SAMPLE_THREADS, 0, st>>>(a);
+    k_sample_final<SPEC_DRAFT_PROBS><<<B, SAMPLE_THREADS, 0, st>>>(a);
+  } else {
+    k_sample_tiles<SPEC_DRAFT_LOGITS><<<tiles_grid, SAMPLE_THREADS, 0, st>>>(a);
+    k_sample_final<SPEC_DRAFT_LOGITS><<<B, SAMPLE_THREADS, 0, st>>>(a);
+  }
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }

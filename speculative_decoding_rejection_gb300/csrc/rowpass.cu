@@ -188,7 +188,9 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
-    const long long n_items = (long long)a.hdr->n_list * a.nch_max;
+    // nothing to stream once the setup rejected the inputs
+    const long long n_items =
+        a.hdr->status != SPEC_OK ? 0 : (long long)a.hdr->n_list * a.nch_max;
     long long it = 0;  // stages issued so far
     bool ok = true;
     long long item = atomicAdd(&a.hdr->work, 1u);
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
       const RowTask t = a.list[entry];
       const int w = t.which;
       const long long rbytes = w ? a.row_bytes[1] : a.row_bytes[0];
-      if (chunk < (w ? a.nch[1] : a.nch[0])) {
+      if (t.slot >= 0 && chunk < (w ? a.nch[1] : a.nch[0])) {
         const int esz = dtype_size(w ? a.dtype[1] : a.dtype[0]);
         const uint64_t row0 = (uint64_t)((w ? a.base[1] : a.base[0]) + (long long)t.row * rbytes);
         const uint64_t cb0 = row0 + (uint64_t)chunk * CHUNK_BYTES;

@@ -27,6 +27,8 @@
 namespace sv {
 
 constexpr int WALK_THREADS = 1024;
+constexpr int WALK_TILE = WALK_THREADS * SAMPLE_EPT;   // elements per tile of a walk pass
+constexpr int MAX_WALK_TILES = (SPEC_MAX_V + WALK_TILE - 1) / WALK_TILE;
 
 struct TreeInfo {
   int base;   // first node row
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(1024) k_setup_tree(const TreeArgs a) {
 
 // ------------------------------------------------------------------- walk
 struct WalkSmem {
-  float tsum[MAX_SAMPLE_TILES];
+  float tsum[MAX_WALK_TILES];
   float scratch[33];
   int kids[SPEC_MAX_TREE_BRANCH];
   float s[SPEC_MAX_TREE_BRANCH + 1];     // 1 / (1 - q(E_j))
@@ -175,7 +177,7 @@ template <int DK>
 __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkSmem &sh,
                                                   const NodeLaw &nl, float c, int L,
                                                   bool residual, int j, float *w) {
-  const int x0 = j * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
+  const int x0 = j * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
   float zt[SAMPLE_EPT], zd[SAMPLE_EPT];
   load_ept(nl.trow, a.tdt, nl.tvec, x0, a.V, -INFINITY, zt);
   if (L > 0 || residual)
@@ -197,7 +199,7 @@ __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkS
 template <int DK>
 __device__ void weight_pass(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, float c, int L,
                             bool residual) {
-  const int ntiles = (a.V + SAMPLE_TILE - 1) / SAMPLE_TILE;
+  const int ntiles = (a.V + WALK_TILE - 1) / WALK_TILE;
   float w[SAMPLE_EPT];
   for (int j = 0; j < ntiles; ++j) {
     tile_weights_tree<DK>(a, sh, nl, c, L, residual, j, w);
@@ -223,7 +225,7 @@ __device__ void weight_pass(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, 
 template <int DK>
 __device__ int weight_draw(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, float c, int L,
                            bool residual, float u) {
-  const int ntiles = (a.V + SAMPLE_TILE - 1) / SAMPLE_TILE;
+  const int ntiles = (a.V + WALK_TILE - 1) / WALK_TILE;
   if (threadIdx.x == 0) {
     sh.target = u * sh.Z;
     float carry = 0.f;
@@ -251,7 +253,7 @@ __device__ int weight_draw(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, f
     for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
     float tot;
     const float excl = block_excl_scan(s, sh.scratch, &tot);
-    const int x0 = js * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
+    const int x0 = js * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
     float pre = 0.f;
     int cand = 0x7fffffff, lastpos = -1;
 #pragma unroll
