@@ -24,6 +24,7 @@ constexpr int SAMPLE_THREADS = 256;
 constexpr int SAMPLE_EPT = 16;      // contiguous elements per thread per tile
 constexpr int SAMPLE_TILE = SAMPLE_THREADS * SAMPLE_EPT;
 constexpr int MAX_SAMPLE_TILES = (SPEC_MAX_V + SAMPLE_TILE - 1) / SAMPLE_TILE;
+constexpr int RES_TILES_PER_ITEM = 4;   // residual tiles per row-pass work item
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr unsigned long long WAIT_NS = 2000000000ull;  // bounded waits: 2 s
@@ -65,6 +66,15 @@ struct ReqInfo {         // per request, written by the setup kernel
   float c;               // log2(e)/T
   int n;                 // accepted drafts (written by the accept kernel)
   int pad[2];
+};
+
+struct Job {         // one final draw of a sampling request (accept kernel)
+  int b;             // request
+  int n;             // accepted drafts
+  int kind;          // 1: residual after a rejection, 2: bonus
+  int pad;
+  float mt, St;      // statistics of target row n+1
+  float md, Sd;      // statistics of draft row n+1 (dense logits only)
 };
 
 struct RowStat { float m, S; int idx; };

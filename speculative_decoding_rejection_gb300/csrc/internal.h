@@ -12,6 +12,8 @@ namespace sv {
 struct WsHeader;
 struct RowTask;
 struct Part;
+struct Job;
+struct ReqInfo;
 
 // Arguments of the row-statistics pass: every listed row is split into
 // CHUNK_BYTES chunks; each consumer warp leaves one Part per chunk at
@@ -25,6 +27,17 @@ struct RowPassArgs {
   const RowTask *list;      // rows to stream (count in hdr->n_list)
   WsHeader *hdr;
   Part *part;
+  // Residual mode: instead of the row list, stream for every job of `jobs`
+  // (count in hdr->n_jobs_a) target row t0+n and draft row d0+n tile by tile
+  // (SAMPLE_TILE elements of each, bf16, 16-byte aligned rows) and leave per
+  // consumer warp the tile sum of max(0, p - q) at
+  // tsum4[(job * ntiles + tile) * RS_CONS_WARPS + warp].
+  int residual;
+  const Job *jobs;
+  const ReqInfo *req;
+  float *tsum4;
+  int ntiles;
+  int V;
 };
 
 int num_sms();

@@ -20,15 +20,6 @@ namespace sv {
 
 constexpr int ACCEPT_WARPS = 8;
 
-struct Job {         // one final draw of a sampling request (accept kernel)
-  int b;             // request
-  int n;             // accepted drafts
-  int kind;          // 1: residual after a rejection, 2: bonus
-  int pad;
-  float mt, St;      // statistics of target row n+1
-  float md, Sd;      // statistics of draft row n+1 (dense logits only)
-};
-
 struct LinearArgs {
   const char *target;
   const char *draft;
@@ -47,7 +38,7 @@ struct LinearArgs {
   ReqInfo *req;
   Job *jobs_a;                // residual draws over dense draft rows
   Job *jobs_b;                // bonus draws and sparse residual draws
-  float *tsum;                // [B][ntiles] residual tile sums of jobs_a
+  float *tsum;                // [B][ntiles][RS_CONS_WARPS] residual tile sums of jobs_a
   int ntiles;
   long long rows_max;
   RowTask *list;
@@ -74,7 +65,8 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   L.req = o;  o += align256(sizeof(ReqInfo) * (size_t)B);
   L.jobs_a = o; o += align256(sizeof(Job) * (size_t)B);
   L.jobs_b = o; o += align256(sizeof(Job) * (size_t)B);
-  L.tsum = o; o += align256(sizeof(float) * (size_t)B * ((V + SAMPLE_TILE - 1) / SAMPLE_TILE));
+  L.tsum = o;
+  o += align256(sizeof(float) * (size_t)B * ((V + SAMPLE_TILE - 1) / SAMPLE_TILE) * RS_CONS_WARPS);
   L.list = o; o += align256(sizeof(RowTask) * (size_t)L.rows_max);
   L.part = o; o += align256(sizeof(Part) * (size_t)L.rows_max * L.nch_max * RS_CONS_WARPS);
   const size_t tk = rule == SPEC_RULE_STRICT_TOP128 ? (size_t)B * max_k * SPEC_TOPK : 0;
@@ -90,7 +82,7 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
 // own entries without a scan; positions no request owns are marked unused.
 // The header was cleared before the launch; an invalid request sets the
 // status word, which makes every later kernel of the call skip its work.
-__global__ void __launch_bounds__(256) k_setup_linear(const LinearArgs a) {
+__global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const int gsize = gridDim.x * blockDim.x;
   if (gtid == 0) a.hdr->n_list = (int)a.rows_max;
@@ -258,7 +250,8 @@ struct SampleSmem {
   float scratch[33];
   float wsum[SAMPLE_THREADS / 32];
   float csum[64];            // per-tile sums inside one chunk (<= 16 tiles)
-  float corr[1024];          // sparse corrections per chunk
+  float cwarp[64 * (SAMPLE_THREADS / 32)];   // per-warp sums of those tiles
+  float corr[MAX_SAMPLE_TILES];  // chunk masses / tile sums of one row
   int s_idx[SPEC_TOPK];
   float s_prob[SPEC_TOPK];
   int n_sparse;
@@ -406,7 +399,9 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_tiles(const LinearArg
           }
         }
         const float t = block_sum(s, sh);
-        if (threadIdx.x == 0) a.tsum[(long long)ja * a.ntiles + j0 + u] = t;
+        if (threadIdx.x < RS_CONS_WARPS)
+          a.tsum[((long long)ja * a.ntiles + j0 + u) * RS_CONS_WARPS + threadIdx.x] =
+              threadIdx.x == 0 ? t : 0.f;
       }
     } else {
       for (int u = 0; u < TILES_PER_ITEM && j0 + u < a.ntiles; ++u) {
@@ -422,7 +417,9 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_tiles(const LinearArg
           s += fmaxf(0.f, p - qq);
         }
         const float t = block_sum(s, sh);
-        if (threadIdx.x == 0) a.tsum[(long long)ja * a.ntiles + j0 + u] = t;
+        if (threadIdx.x < RS_CONS_WARPS)
+          a.tsum[((long long)ja * a.ntiles + j0 + u) * RS_CONS_WARPS + threadIdx.x] =
+              threadIdx.x == 0 ? t : 0.f;
       }
     }
   }
@@ -512,18 +509,30 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
   __syncthreads();
   const int cs = sh.jstar;
   if (cs < 0) return -1;
-  // tile sums inside the chunk, then the tile, then the element
+  // tile sums inside the chunk in one sweep (per-warp sums, one sync), then
+  // the tile, then the element
   const int j0 = cs * tpc, j1 = min(a.ntiles, j0 + tpc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float w[SAMPLE_EPT];
+#pragma unroll 4
   for (int j = j0; j < j1; ++j) {
     tile_weights<DK>(a, sh, q.trow, q.tvec, q.drow, q.dvec, kind, q.c, q.mt, q.invSt, q.md,
                      q.invSd, j, w);
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
-    const float t = block_sum(s, sh);
-    if (threadIdx.x == 0) sh.csum[j - j0] = t;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) sh.cwarp[(j - j0) * (SAMPLE_THREADS / 32) + warp] = s;
   }
+  __syncthreads();
+  if (threadIdx.x < j1 - j0) {
+    float t = 0.f;
+    for (int q2 = 0; q2 < SAMPLE_THREADS / 32; ++q2)
+      t += sh.cwarp[threadIdx.x * (SAMPLE_THREADS / 32) + q2];
+    sh.csum[threadIdx.x] = t;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     float carry = sh.carry;
     int js = -1;
@@ -557,8 +566,16 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArg
   int x = -1;
   bool done = false;
   if (dense) {
+    // tile sums (the consumer warps' partials in a fixed order)
+    const float *ts4 = a.tsum + (long long)g * a.ntiles * RS_CONS_WARPS;
+    for (int j = threadIdx.x; j < a.ntiles; j += blockDim.x) {
+      float t = 0.f;
+      for (int w = 0; w < RS_CONS_WARPS; ++w) t += ts4[j * RS_CONS_WARPS + w];
+      sh.corr[j] = t;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
-      const float *ts = a.tsum + (long long)g * a.ntiles;
+      const float *ts = sh.corr;
       float Z = 0.f;
       for (int j = 0; j < a.ntiles; ++j) Z += ts[j];
       sh.Z = Z;
@@ -713,7 +730,7 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
 
   if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
-  k_setup_linear<<<(B + 255) / 256, 256, 0, st>>>(a);
+  k_setup_linear<<<(B + 63) / 64, 64, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (rule == SPEC_RULE_STRICT_TOP128) {
     const int rc = launch_topk128(draft, ddt, B * max_k, V, cu_draft, temperature, B,
@@ -734,6 +751,12 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
   rp.list = a.list;
   rp.hdr = a.hdr;
   rp.part = a.part;
+  rp.residual = 0;
+  rp.jobs = nullptr;
+  rp.req = nullptr;
+  rp.tsum4 = nullptr;
+  rp.ntiles = 0;
+  rp.V = V;
   int rc = launch_row_pass(rp, st);
   if (rc != SPEC_OK) return rc;
   k_accept<<<(B + ACCEPT_WARPS - 1) / ACCEPT_WARPS, ACCEPT_WARPS * 32, 0, st>>>(a);
@@ -745,7 +768,20 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
     k_sample_tiles<SPEC_DRAFT_PROBS><<<tiles_grid, SAMPLE_THREADS, 0, st>>>(a);
     k_sample_final<SPEC_DRAFT_PROBS><<<B, SAMPLE_THREADS, 0, st>>>(a);
   } else {
-    k_sample_tiles<SPEC_DRAFT_LOGITS><<<tiles_grid, SAMPLE_THREADS, 0, st>>>(a);
+    if (tdt == SPEC_BF16 && ddt == SPEC_BF16 && V % 8 == 0) {
+      // residual tile pairs through the TMA row pass
+      RowPassArgs rr = rp;
+      rr.residual = 1;
+      rr.jobs = a.jobs_a;
+      rr.req = a.req;
+      rr.tsum4 = a.tsum;
+      rr.ntiles = a.ntiles;
+      rr.V = V;
+      rc = launch_row_pass(rr, st);
+      if (rc != SPEC_OK) return rc;
+    } else {
+      k_sample_tiles<SPEC_DRAFT_LOGITS><<<tiles_grid, SAMPLE_THREADS, 0, st>>>(a);
+    }
     k_sample_final<SPEC_DRAFT_LOGITS><<<B, SAMPLE_THREADS, 0, st>>>(a);
   }
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;

@@ -167,6 +167,61 @@ __device__ __forceinline__ void consume_full_bf16(const unsigned char *buf, int 
   }
 }
 
+// Residual mode, full tile: the stage holds SAMPLE_TILE bf16 of the target row
+// (first half) and the same elements of the draft row (second half). Returns
+// this thread's sum of max(0, p - q) over its 32 elements.
+constexpr int RES_VPT = SAMPLE_TILE / 8 / NCT;   // vectors per thread per row
+static_assert(RES_VPT * 8 * NCT == SAMPLE_TILE, "residual tiles split evenly");
+static_assert(2 * SAMPLE_TILE * 2 <= TILE_BYTES, "a residual tile pair fits one stage");
+
+struct ResLaw { float mt, invSt, md, invSd, c; };
+
+__device__ __forceinline__ float consume_res_full(const unsigned char *buf, int ctid,
+                                                  const ResLaw &L) {
+  const f32x2 c2 = pk2(L.c, L.c), it2 = pk2(L.invSt, L.invSt), id2 = pk2(L.invSd, L.invSd);
+  f32x2 e[4 * RES_VPT];
+#pragma unroll
+  for (int k = 0; k < RES_VPT; ++k) {
+    const uint4 vt = lds128(buf + 16 * (ctid + NCT * k));
+    const uint4 vd = lds128(buf + TILE_BYTES / 2 + 16 * (ctid + NCT * k));
+    const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const f32x2 tt = mul2(bsub2(wt[q], L.mt), c2), td = mul2(bsub2(wd[q], L.md), c2);
+      const f32x2 p2 = mul2(pk2(ex2(lo2(tt)), ex2(hi2(tt))), it2);
+      const f32x2 q2 = mul2(pk2(ex2(lo2(td)), ex2(hi2(td))), id2);
+      const f32x2 d2 = add2(p2, q2 ^ 0x8000000080000000ull);
+      e[4 * k + q] = pk2(fmaxf(lo2(d2), 0.f), fmaxf(hi2(d2), 0.f));
+    }
+  }
+#pragma unroll
+  for (int s = 2 * RES_VPT; s > 0; s >>= 1)
+#pragma unroll
+    for (int i = 0; i < s; ++i) e[i] = add2(e[i], e[i + s]);
+  return lo2(e[0]) + hi2(e[0]);
+}
+
+// Residual mode, last (partial) tile of a row: ne < SAMPLE_TILE elements.
+__device__ __forceinline__ float consume_res_partial(const unsigned char *buf, int ctid, int ne,
+                                                     const ResLaw &L) {
+  float s = 0.f;
+  for (int v = ctid; v * 8 < ne; v += NCT) {
+    const uint4 vt = lds128(buf + 16 * v);
+    const uint4 vd = lds128(buf + TILE_BYTES / 2 + 16 * v);
+    const uint32_t wt[4] = {vt.x, vt.y, vt.z, vt.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (8 * v + 2 * q < ne) {
+        s += fmaxf(0.f, ex2((bf16lo(wt[q]) - L.mt) * L.c) * L.invSt -
+                            ex2((bf16lo(wd[q]) - L.md) * L.c) * L.invSd);
+        s += fmaxf(0.f, ex2((bf16hi(wt[q]) - L.mt) * L.c) * L.invSt -
+                            ex2((bf16hi(wd[q]) - L.md) * L.c) * L.invSd);
+      }
+    }
+  }
+  return s;
+}
+
 __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const RowPassArgs a) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ RowPassSmem sh;
@@ -189,13 +244,46 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
     // nothing to stream once the setup rejected the inputs
+    const int ipj = (a.ntiles + RES_TILES_PER_ITEM - 1) / RES_TILES_PER_ITEM;
     const long long n_items =
-        a.hdr->status != SPEC_OK ? 0 : (long long)a.hdr->n_list * a.nch_max;
+        a.hdr->status != SPEC_OK ? 0
+        : a.residual             ? (long long)a.hdr->n_jobs_a * ipj
+                                 : (long long)a.hdr->n_list * a.nch_max;
     long long it = 0;  // stages issued so far
     bool ok = true;
-    long long item = atomicAdd(&a.hdr->work, 1u);
-    while (ok && item < n_items) {
-      const long long next = atomicAdd(&a.hdr->work, 1u);  // one item ahead
+    unsigned int *counter = a.residual ? &a.hdr->work2 : &a.hdr->work;
+    long long item = atomicAdd(counter, 1u);
+    while (ok && a.residual && item < n_items) {
+      const long long next = atomicAdd(counter, 1u);
+      const int ja = (int)(item / ipj);
+      const int g = (int)(item % ipj);
+      const Job job = a.jobs[ja];
+      const ReqInfo r = a.req[job.b];
+      const uint64_t trow = (uint64_t)(a.base[0] + (long long)(r.t0 + job.n) * a.row_bytes[0]);
+      const uint64_t drow = (uint64_t)(a.base[1] + (long long)(r.d0 + job.n) * a.row_bytes[1]);
+      const int j1 = min(a.ntiles, (g + 1) * RES_TILES_PER_ITEM);
+      for (int j = g * RES_TILES_PER_ITEM; j < j1; ++j) {
+        const int s = (int)(it % NSTAGE);
+        const long long use = it / NSTAGE;
+        if (use > 0 && !mbar_wait_bounded(&sh.empty[s], (uint32_t)((use - 1) & 1), abort)) {
+          ok = false;
+          break;
+        }
+        const int e0 = j * SAMPLE_TILE;
+        const int ne = min(SAMPLE_TILE, a.V - e0);
+        const uint32_t nb = (uint32_t)ne * 2;
+        sh.m0[s] = make_int4(ja, j, e0, ne | (1 << 14));
+        sh.m1[s] = make_int4(__float_as_int(r.c), 0, 0, 0);
+        mbar_arrive_tx(&sh.full[s], 2 * nb);
+        unsigned char *dst = stage_buf + (size_t)s * TILE_BYTES;
+        bulk_g2s(dst, (const void *)(trow + 2ull * e0), nb, &sh.full[s]);
+        bulk_g2s(dst + TILE_BYTES / 2, (const void *)(drow + 2ull * e0), nb, &sh.full[s]);
+        ++it;
+      }
+      item = next;
+    }
+    while (ok && !a.residual && item < n_items) {
+      const long long next = atomicAdd(counter, 1u);  // one item ahead
       const int entry = (int)(item / a.nch_max);
       const int chunk = (int)(item % a.nch_max);
       const RowTask t = a.list[entry];
@@ -261,6 +349,8 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
   const int cw = warp - 1;
   const int ctid = threadIdx.x - 32;
   RunState st{NO_MAX, pk2(0.f, 0.f), 0x7fffffff};
+  int res_job = -1;
+  ResLaw res_law{0.f, 0.f, 0.f, 0.f, 0.f};
   for (long long it = 0;; ++it) {
     const int s = (int)(it % NSTAGE);
     if (!mbar_wait_bounded(&sh.full[s], (uint32_t)((it / NSTAGE) & 1), abort)) {
@@ -271,6 +361,24 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
     const int4 m0 = sh.m0[s];
     if (m0.x < 0) return;
     const int4 m1 = sh.m1[s];
+    if (m0.w & (1 << 14)) {   // residual tile pair
+      const int ja = m0.x, j = m0.y, ne = m0.w & 0x3fff;
+      if (ja != res_job) {
+        const Job job = a.jobs[ja];
+        res_law = ResLaw{job.mt, 1.f / job.St, job.md, job.Sd > 0.f ? 1.f / job.Sd : 0.f,
+                         __int_as_float(m1.x)};
+        res_job = ja;
+      }
+      const unsigned char *rbuf = stage_buf + (size_t)s * TILE_BYTES;
+      float rs = ne == SAMPLE_TILE ? consume_res_full(rbuf, ctid, res_law)
+                                   : consume_res_partial(rbuf, ctid, ne, res_law);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[s]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+      if (lane == 0) a.tsum4[((long long)ja * a.ntiles + j) * RS_CONS_WARPS + cw] = rs;
+      continue;
+    }
     const int nvec = m0.w & 0xfff;
     const bool last = (m0.w >> 12) & 1;
     const int which = (m0.w >> 13) & 1;

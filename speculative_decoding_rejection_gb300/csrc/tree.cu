@@ -526,6 +526,12 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   rp.list = a.list;
   rp.hdr = a.hdr;
   rp.part = a.part;
+  rp.residual = 0;
+  rp.jobs = nullptr;
+  rp.req = nullptr;
+  rp.tsum4 = nullptr;
+  rp.ntiles = 0;
+  rp.V = V;
   const int rc = launch_row_pass(rp, st);
   if (rc != SPEC_OK) return rc;
   if (dk == SPEC_DRAFT_PROBS)
