@@ -1,20 +1,23 @@
 #!/usr/bin/env python
 """Throughput of the batched speculative-decoding verifier on GB300.
 
-A step is one spec_verify_linear call over one batch of synthetic requests
-(default: B=1024 requests x K=4 drafts, V=201088, bf16 target and draft
-logits, per-request T ~ U[0, 1.2], greedy below 0.05). The headline value is
-verified draft positions per second (sum of K over the batch / step time);
-the JSON line also carries the achieved HBM bandwidth of the dominant kernel
-(the row-statistics pass) against the measured copy peak, an end-to-end
-number through the same C ABI with host buffers, and the CPU oracle timed on
-a bounded sample.
+A step is one verification call over one batch of synthetic requests. The
+default workload is B=1024 requests x K=4 drafts, V=201088, bf16 target and
+draft logits, per-request T ~ U[0, 1.2] (greedy below 0.05): one
+spec_verify_linear call per step. The headline value is verified draft
+positions per second (draft positions in the batch / step time); the JSON
+line also carries the achieved HBM bandwidth of the dominant kernel (the
+row-statistics pass) against the measured copy peak, an end-to-end number
+through the same C ABI with host buffers, and the CPU oracle timed on a
+bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--config 1..5]
+                  [--config 1|2|3|4|5]
 
-Under torchrun each rank verifies its own batch (weak scaling, no data-path
-collective); rank 0 prints the line.
+--config 3 is the top-128 truncation workload, --config 4 the tree (RRSw)
+workload (spec_verify_tree; positions = draft nodes). Under torchrun each rank
+verifies its own batch (weak scaling, no data-path collective); rank 0 prints
+the line.
 """
 from __future__ import annotations
 
@@ -47,12 +50,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 5])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--B", type=int, default=None,
                     help="override the number of requests (small profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--cpu-requests", type=int, default=1024,
-                    help="requests in the oracle's timed sample")
+                    help="requests (or trees) in the oracle's timed sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -78,8 +81,8 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
+    def __init__(self, gpu_id):
+        self.gpu = gpu_id
         self.proc = None
         self.lines = []
 
@@ -121,7 +124,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup():
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -154,69 +157,171 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
-def workload_bytes(lb):
-    """Algorithmic bytes of one call: every target row once, plus the dense
-    draft rows of sampling requests (read by the row pass, or by the top-128
-    select under the truncation rule)."""
-    import torch
-    K = torch.diff(lb.cu_draft.cpu().long())
-    T = lb.temperature.cpu()
-    samp = T >= 0.05
-    tgt = int((K + 1).sum()) * lb.V * lb.target.element_size()
-    drf = int(K[samp].sum()) * lb.V * lb.draft.element_size()
-    return tgt, drf, int(K.sum())
+# ---------------------------------------------------------------- workloads
+class LinearWork:
+    """spec_verify_linear on a linear workload (configs 1, 2, 3, 5)."""
+    unit_name = "requests"
+
+    def __init__(self, cfg, dev, input_seed=None, B=None):
+        import torch
+        import speculative_decoding_rejection_gb300 as sv
+        from speculative_decoding_rejection_gb300 import synthetic as S
+        self.sv = sv
+        over = {} if B is None else {"B": B}
+        self.lb = lb = S.make_linear(cfg, device=dev, input_seed=input_seed, **over)
+        self.rule = sv.SPEC_RULE_STRICT_TOP128 if lb.top128 else sv.SPEC_RULE_STRICT
+        K = torch.diff(lb.cu_draft.cpu().long())
+        samp = lb.temperature.cpu() >= 0.05
+        self.positions = int(K.sum())
+        self.tgt_bytes = int((K + 1).sum()) * lb.V * lb.target.element_size()
+        self.drf_bytes = int(K[samp].sum()) * lb.V * lb.draft.element_size()
+        # the row pass reads the target rows and the dense draft rows of
+        # sampling requests; under truncation the top-128 kernel reads the latter
+        self.rowpass_bytes = self.tgt_bytes + (0 if lb.top128 else self.drf_bytes)
+        # setup, row pass, accept, final draw, + residual sums (dense drafts)
+        # or the top-128 select (truncation); the header memset is not ours
+        self.launches = 5
+        self.outs = (torch.empty(lb.B, lb.max_k + 1, dtype=torch.int32, device=dev),
+                     torch.empty(lb.B, dtype=torch.int32, device=dev), None)
+        self.ws = torch.empty(sv.spec_verify_linear_workspace(lb.B, lb.max_k, lb.V, self.rule),
+                              dtype=torch.uint8, device=dev)
+        self.config = {"workload": lb.meta["workload"], "B": lb.B, "K": lb.max_k, "V": lb.V,
+                       "logits": "bf16" if lb.target.element_size() == 2 else "f32",
+                       "rule": "strict_top128" if lb.top128 else "strict"}
+
+    def input_tensors(self):
+        lb = self.lb
+        return {"target": lb.target, "draft": lb.draft, "draft_tokens": lb.draft_tokens,
+                "cu_draft": lb.cu_draft, "temperature": lb.temperature}
+
+    def call(self, inputs=None):
+        lb = self.lb
+        t = inputs or self.input_tensors()
+        self.sv.spec_verify_linear(t["target"], t["draft"], t["draft_tokens"], t["cu_draft"],
+                                   t["temperature"], lb.seed, max_k=lb.max_k, rule=self.rule,
+                                   workspace=self.ws, out=self.outs)
+
+    def result_tensors(self):
+        return [self.outs[0], self.outs[1]]
+
+    def mean_accepted(self):
+        return float(self.outs[1].float().mean())
+
+    def oracle_sample(self, units, offset=0):
+        """Runs the oracle on `units` requests; returns the draft positions done."""
+        import numpy as np
+        from oracle import spec_oracle as O
+        lb = self.lb
+        if not hasattr(self, "_host"):
+            self._host = (lb.target.cpu(), lb.draft.cpu(), lb.draft_tokens.cpu().numpy(),
+                          lb.cu_draft.cpu().numpy(), lb.temperature.cpu().numpy())
+            self._order = np.random.default_rng(1).permutation(lb.B)
+        tgt, drf, toks, cu, T = self._host
+        req = np.sort(np.roll(self._order, -offset)[:min(units, lb.B)])
+        O.verify_linear(tgt, drf, toks, cu, T, lb.seed, rule=self.rule, max_k=lb.max_k,
+                        requests=req)
+        return int(sum(cu[b + 1] - cu[b] for b in req))
 
 
-def cpu_baseline(lb, n_req, rule):
+class TreeWork:
+    """spec_verify_tree on the tree workload (config 4)."""
+    unit_name = "trees"
+
+    def __init__(self, cfg, dev, input_seed=None, B=None):
+        import torch
+        import speculative_decoding_rejection_gb300 as sv
+        from speculative_decoding_rejection_gb300 import synthetic as S
+        self.sv = sv
+        over = {} if B is None else {"B": B}
+        self.tb = tb = S.make_tree(cfg, device=dev, input_seed=input_seed, **over)
+        cu = tb.cu_nodes.cpu().long()
+        par = tb.parent.cpu().long()
+        base = torch.repeat_interleave(cu[:-1], torch.diff(cu))
+        n = tb.target.shape[0]
+        internal = torch.zeros(n, dtype=torch.bool)
+        has_parent = par >= 0
+        internal[(par + base)[has_parent]] = True
+        samp = (tb.temperature.cpu() >= 0.05).repeat_interleave(torch.diff(cu))
+        self.positions = n - tb.B
+        self.tgt_bytes = n * tb.V * tb.target.element_size()
+        self.drf_bytes = int((internal & samp).sum()) * tb.V * tb.draft.element_size()
+        self.rowpass_bytes = self.tgt_bytes + self.drf_bytes
+        self.launches = 3   # setup, row pass, walk
+        W = tb.max_depth + 1
+        self.outs = (torch.empty(tb.B, W, dtype=torch.int32, device=dev),
+                     torch.empty(tb.B, dtype=torch.int32, device=dev),
+                     torch.empty(tb.B, W, dtype=torch.int32, device=dev))
+        self.ws = torch.empty(sv.spec_verify_tree_workspace(tb.B, n, tb.V, tb.max_depth,
+                                                            tb.max_branch),
+                              dtype=torch.uint8, device=dev)
+        self.config = {"workload": tb.meta["workload"], "B": tb.B, "nodes": n, "V": tb.V,
+                       "logits": "bf16" if tb.target.element_size() == 2 else "f32",
+                       "rule": "rrsw_tree"}
+
+    def input_tensors(self):
+        tb = self.tb
+        return {"target": tb.target, "draft": tb.draft, "node_token": tb.node_token,
+                "parent": tb.parent, "cu_nodes": tb.cu_nodes, "temperature": tb.temperature}
+
+    def call(self, inputs=None):
+        tb = self.tb
+        t = inputs or self.input_tensors()
+        self.sv.spec_verify_tree(t["target"], t["draft"], t["node_token"], t["parent"],
+                                 t["cu_nodes"], t["temperature"], tb.seed,
+                                 max_depth=tb.max_depth, max_branch=tb.max_branch,
+                                 workspace=self.ws, out=self.outs)
+
+    def result_tensors(self):
+        return list(self.outs)
+
+    def mean_accepted(self):
+        return float(self.outs[1].float().mean())
+
+    def oracle_sample(self, units, offset=0):
+        import numpy as np
+        from oracle import spec_oracle as O
+        tb = self.tb
+        if not hasattr(self, "_host"):
+            self._host = (tb.target.cpu(), tb.draft.cpu(), tb.node_token.cpu().numpy(),
+                          tb.parent.cpu().numpy(), tb.cu_nodes.cpu().numpy(),
+                          tb.temperature.cpu().numpy())
+        tgt, drf, tok, par, cu, T = self._host
+        req = np.sort((np.arange(min(units, tb.B)) + offset) % tb.B)
+        O.verify_tree(tgt, drf, tok, par, cu, T, tb.seed, tb.max_depth, requests=req)
+        return int(sum(cu[b + 1] - cu[b] - 1 for b in req))
+
+
+def make_work(cfg, dev, input_seed=None, B=None):
+    return (TreeWork if cfg == 4 else LinearWork)(cfg, dev, input_seed, B)
+
+
+def cpu_baseline(work, n_units):
     """The oracle, as it stands, on a bounded sample of the same workload."""
-    import numpy as np
-    from oracle import spec_oracle as O
-    tgt = lb.target.cpu()
-    drf = lb.draft.cpu()
-    toks = lb.draft_tokens.cpu().numpy()
-    cu = lb.cu_draft.cpu().numpy()
-    T = lb.temperature.cpu().numpy()
-    req = np.sort(np.random.default_rng(0).choice(lb.B, size=min(n_req, lb.B), replace=False))
     t0 = time.perf_counter()
-    O.verify_linear(tgt, drf, toks, cu, T, lb.seed, rule=rule, max_k=lb.max_k, requests=req)
+    pos = work.oracle_sample(n_units)
     dt = time.perf_counter() - t0
-    pos = int(sum(cu[b + 1] - cu[b] for b in req))
+    n = min(n_units, work.config["B"])
     return {"value": pos / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{len(req)} of {lb.B} requests ({pos} draft positions) of the same "
-                      f"workload, fp64 numpy, one thread, {dt:.1f} s"}
+            "sample": f"{n} of {work.config['B']} {work.unit_name} ({pos} draft positions) of "
+                      f"the same workload, fp64 numpy, one thread, {dt:.1f} s"}
 
 
 def run_reference(args):
     """Reference arm: the CPU oracle timed as it stands (rank 0 only)."""
-    world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import numpy as np
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     import torch
-    from oracle import spec_oracle as O
-    from speculative_decoding_rejection_gb300 import synthetic as S
     dev = "cuda:0" if torch.cuda.is_available() else "cpu"
-    lb = S.make_linear(args.config, device=dev)
-    rule = 2 if lb.top128 else 0
-    tgt, drf = lb.target.cpu(), lb.draft.cpu()
-    toks = lb.draft_tokens.cpu().numpy()
-    cu = lb.cu_draft.cpu().numpy()
-    T = lb.temperature.cpu().numpy()
-    per_step = 2
-    order = np.random.default_rng(1).permutation(lb.B)
-
-    def step(k):
-        req = np.sort(order[(k * per_step) % lb.B:][:per_step])
-        O.verify_linear(tgt, drf, toks, cu, T, lb.seed, rule=rule, max_k=lb.max_k, requests=req)
-        return int(sum(cu[b + 1] - cu[b] for b in req))
-
+    work = make_work(args.config, dev, B=args.B)
+    per_step = 1 if args.config == 4 else 2
     for k in range(args.warmup):
-        step(k)
+        work.oracle_sample(per_step, offset=k * per_step)
     pos = 0
     t0 = time.perf_counter()
     for k in range(args.steps):
-        pos += step(args.warmup + k)
+        pos += work.oracle_sample(per_step, offset=(args.warmup + k) * per_step)
     dt = time.perf_counter() - t0
     value = pos / dt
     line = {
@@ -224,10 +329,9 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": lb.meta["workload"], "B": lb.B, "V": lb.V,
-                   "step": f"{per_step} requests of the batch per step"},
+        "config": dict(work.config, step=f"{per_step} {work.unit_name} of the batch per step"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step} requests per step, {args.steps} steps, "
+                         "sample": f"{per_step} {work.unit_name} per step, {args.steps} steps, "
                                    "fp64 numpy, one thread"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -243,29 +347,16 @@ def main():
     import speculative_decoding_rejection_gb300 as sv
     from speculative_decoding_rejection_gb300 import synthetic as S
 
-    world, rank, local = dist_setup(args.gpus)
+    world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     sv.lib()
-    over = {} if args.B is None else {"B": args.B}
-    lb = S.make_linear(args.config, device=dev,
-                       input_seed=S.INPUT_SEED_BASE + args.config + 7919 * rank, **over)
-    rule = sv.SPEC_RULE_STRICT_TOP128 if lb.top128 else sv.SPEC_RULE_STRICT
-    tgt_bytes, drf_bytes, positions = workload_bytes(lb)
-    B = lb.B
-    outs = (torch.empty(B, lb.max_k + 1, dtype=torch.int32, device=dev),
-            torch.empty(B, dtype=torch.int32, device=dev), None)
-    ws = torch.empty(sv.spec_verify_linear_workspace(B, lb.max_k, lb.V, rule),
-                     dtype=torch.uint8, device=dev)
-
-    def call():
-        sv.spec_verify_linear(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
-                              lb.temperature, lb.seed, max_k=lb.max_k, rule=rule,
-                              workspace=ws, out=outs)
+    work = make_work(args.config, dev, input_seed=S.INPUT_SEED_BASE + args.config + 7919 * rank,
+                     B=args.B)
 
     for _ in range(max(3, args.warmup)):
-        call()
+        work.call()
     torch.cuda.synchronize()
-    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    assert sv.spec_get_status(work.ws) == sv.SPEC_OK
     K = args.steps
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -280,52 +371,44 @@ def main():
     e0.record()
     for k in range(K):
         sv.spec_profile_row_pass(ev_b[k], ev_a[k])
-        call()
+        work.call()
     e1.record()
     torch.cuda.synchronize()
     barrier(world)
     clocks.stop()
     ms_step = max_over_ranks(e0.elapsed_time(e1) / K, world)
     rp_ms = statistics.mean(b.elapsed_time(a) for b, a in zip(ev_b, ev_a))
-    mean_acc = float(outs[1].float().mean())
 
-    # dominant kernel: the row pass streams the target rows and the dense
-    # draft rows of sampling requests (not under the top-128 rule)
-    rp_bytes = tgt_bytes + (0 if lb.top128 else drf_bytes)
     peaks, peak_src = measured_peaks()
     peak = float(peaks["hbm_gbs"])
-    achieved = rp_bytes / (rp_ms * 1e-3) / 1e9
+    achieved = work.rowpass_bytes / (rp_ms * 1e-3) / 1e9
     traffic = None
     src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "rowpass.cu")
     if ROWPASS_TRAFFIC["source_sha1"] == sha1(src):
-        traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * rp_bytes
+        traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
 
     # end to end through the same API: pinned host inputs copied in, the
-    # result read back, every step
+    # results read back, every step
     e2e = None
     if not args.no_e2e:
-        host = {n: getattr(lb, n).cpu().pin_memory()
-                for n in ("target", "draft", "draft_tokens", "cu_draft", "temperature")}
-        dev_in = {n: torch.empty_like(getattr(lb, n)) for n in host}
-        h_tok = torch.empty(outs[0].shape, dtype=torch.int32).pin_memory()
-        h_acc = torch.empty(outs[1].shape, dtype=torch.int32).pin_memory()
+        host = {n: t.cpu().pin_memory() for n, t in work.input_tensors().items()}
+        dev_in = {n: torch.empty_like(t) for n, t in work.input_tensors().items()}
+        res = work.result_tensors()
+        host_out = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in res]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = h_tok.numel() * 4 + h_acc.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
 
         def e2e_step():
             for n, t in host.items():
                 dev_in[n].copy_(t, non_blocking=True)
-            sv.spec_verify_linear(dev_in["target"], dev_in["draft"], dev_in["draft_tokens"],
-                                  dev_in["cu_draft"], dev_in["temperature"], lb.seed,
-                                  max_k=lb.max_k, rule=rule, workspace=ws, out=outs)
-            h_tok.copy_(outs[0], non_blocking=True)
-            h_acc.copy_(outs[1], non_blocking=True)
+            work.call(dev_in)
+            for h, r in zip(host_out, res):
+                h.copy_(r, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
         barrier(world)
-        t0 = time.perf_counter()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record()
@@ -335,14 +418,14 @@ def main():
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.e2e_steps, world)
-        e2e = {"value": world * positions / (e2e_ms * 1e-3), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms}
+        e2e = {"value": world * work.positions / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         del host, dev_in
 
+    algo = work.tgt_bytes + work.drf_bytes
     line = {
         "metric": METRIC,
-        "value": world * positions / (ms_step * 1e-3),
+        "value": world * work.positions / (ms_step * 1e-3),
         "unit": UNIT,
         "n_gpus": world,
         "steps": K,
@@ -354,29 +437,25 @@ def main():
         "dtype": "f32",
         "data": "synthetic",
         "impl": "gb300",
-        "config": {
-            "workload": lb.meta["workload"], "B": B, "K": lb.max_k, "V": lb.V,
-            "logits": "bf16" if lb.target.element_size() == 2 else "f32",
-            "rule": {0: "strict", 2: "strict_top128"}[rule],
-            "l2": f"inputs {(tgt_bytes + drf_bytes) / 1e9:.2f} GB per step, larger than L2",
-            "parallelism": f"replicas x{world} (independent request batches)",
-        },
-        "hbm_gbs_whole_call": (tgt_bytes + drf_bytes) / (ms_step * 1e-3) / 1e9,
-        "algorithmic_bytes_per_step": tgt_bytes + drf_bytes,
-        "mean_accepted": mean_acc,
+        "config": dict(work.config,
+                       l2=f"inputs {algo / 1e9:.2f} GB per step"
+                          + (", larger than L2" if algo > 200e6 else ", L2 not flushed"),
+                       parallelism=f"replicas x{world} (independent request batches)"),
+        "hbm_gbs_whole_call": algo / (ms_step * 1e-3) / 1e9,
+        "algorithmic_bytes_per_step": algo,
+        "mean_accepted": work.mean_accepted(),
         "roofline": {
             "kernel": "k_row_pass", "bound": "hbm", "achieved": achieved, "peak": peak,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback", "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-            "algorithmic_bytes_per_launch": rp_bytes, "ms_per_launch": rp_ms,
+            "algorithmic_bytes_per_launch": work.rowpass_bytes, "ms_per_launch": rp_ms,
         },
-        # setup, row pass, accept, sampler tiles, sampler final (+ top-128)
-        "gpu_launches": K * (6 if lb.top128 else 5),
+        "gpu_launches": K * work.launches,
         "clocks": clocks.summary(),
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(lb, args.cpu_requests, rule)
+        line["cpu_baseline"] = cpu_baseline(work, args.cpu_requests if args.config != 4 else 8)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -254,6 +254,7 @@ struct SampleSmem {
   float corr[MAX_SAMPLE_TILES];  // chunk masses / tile sums of one row
   int s_idx[SPEC_TOPK];
   float s_prob[SPEC_TOPK];
+  float pmin[SPEC_TOPK];
   int n_sparse;
   int jstar;
   float carry, target, Z;
@@ -480,15 +481,16 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
     }
     sh.corr[ch] = m * q.invSt;   // chunk mass of p
   }
+  const bool sparse_res = kind == 1 && DK == SPEC_DRAFT_SPARSE128;
+  if (sparse_res && threadIdx.x < sh.n_sparse) {   // min(p, q) at every listed id
+    const int id = sh.s_idx[threadIdx.x];
+    const float p = ex2((load_elem(q.trow, a.tdt, id) - q.mt) * q.c) * q.invSt;
+    sh.pmin[threadIdx.x] = fminf(p, sh.s_prob[threadIdx.x]);
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (kind == 1 && DK == SPEC_DRAFT_SPARSE128) {
-      for (int k = 0; k < sh.n_sparse; ++k) {
-        const int id = sh.s_idx[k];
-        const float p = ex2((load_elem(q.trow, a.tdt, id) - q.mt) * q.c) * q.invSt;
-        sh.corr[id / chunk_elems] -= fminf(p, sh.s_prob[k]);
-      }
-    }
+    if (sparse_res)
+      for (int k = 0; k < sh.n_sparse; ++k) sh.corr[sh.s_idx[k] / chunk_elems] -= sh.pmin[k];
     float Z = 0.f;
     for (int ch = 0; ch < nch; ++ch) Z += fmaxf(sh.corr[ch], 0.f);
     sh.Z = Z;

@@ -36,7 +36,15 @@ struct TopkArgs {
   WsHeader *hdr;
 };
 
+constexpr int TK_WARPS = TK_THREADS / 32;
+constexpr int CAND_CAP = 1024;
+static_assert(SPEC_TOPK % TK_WARPS == 0 && SPEC_TOPK / TK_WARPS <= 32, "bound needs k per warp");
+
 struct TopkSmem {
+  unsigned long long cand[CAND_CAP];   // (key << 32) | ~id of the candidates
+  float tmax[TK_WARPS];                // per-warp 4th-largest thread maxima
+  int cand_n;
+  float m128;
   unsigned hist[256];
   int scratch[33];
   int sel_idx[SPEC_TOPK];
@@ -48,6 +56,7 @@ struct TopkSmem {
   int lt_count;
   int use_fallback;
   float S;
+  float T;
 };
 
 __device__ __forceinline__ unsigned key_of(uint32_t bits, bool bf16) {
@@ -110,6 +119,80 @@ __device__ __forceinline__ void pick_digit(TopkSmem &sh) {
   __syncthreads();
 }
 
+
+// bf16 keys back to values (inverse of key_of for 16-bit keys).
+__device__ __forceinline__ float value_of_key16(unsigned key) {
+  const unsigned bits = (key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu);
+  return __uint_as_float(bits << 16);
+}
+
+// Fast selection for bf16 rows with V % 8 == 0 and V >= 8 * TK_THREADS
+// (every row 16-byte aligned, every thread holds elements). A packed max pass
+// leaves each thread's maximum; every warp sorts its 32 maxima with a
+// shuffle bitonic network, and the smallest of the warps' 4th-largest
+// maxima is a lower bound on the 128-th largest element (32 warps x 4
+// threads each hold an element at least that large). A second pass, read
+// back from L2 (one row per CTA, one CTA per SM, keeps the rows in flight
+// far below L2), gathers the elements at or above the bound — a few hundred
+// on logit rows — and the exact top 128 (ties to the lower id) is ranked
+// among them in shared memory. Returns false, having written no selection,
+// when the candidates overflow CAND_CAP.
+__device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const uint4 *vp = reinterpret_cast<const uint4 *>(row);
+  const int nvec = V / 8;
+  uint32_t pm = 0xff80ff80u;   // (-inf, -inf)
+#pragma unroll 8
+  for (int v = t; v < nvec; v += TK_THREADS) {
+    const uint4 w = __ldg(vp + v);
+    pm = bmax2(pm, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+  }
+  float m = fmaxf(bf16lo(pm), bf16hi(pm));
+  // descending bitonic sort of the warp's 32 maxima
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, m, j);
+      m = (((lane & k) == 0) == ((lane & j) == 0)) ? fmaxf(m, o) : fminf(m, o);
+    }
+  if (lane == SPEC_TOPK / TK_WARPS - 1) sh.tmax[warp] = m;
+  if (t == 0) sh.cand_n = 0;
+  __syncthreads();
+  float bound = sh.tmax[0];
+  for (int w = 1; w < TK_WARPS; ++w) bound = fminf(bound, sh.tmax[w]);
+#pragma unroll 4
+  for (int v = t; v < nvec; v += TK_THREADS) {
+    const uint4 w = __ldg(vp + v);
+    const uint32_t m8 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+    if (fmaxf(bf16lo(m8), bf16hi(m8)) < bound) continue;
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t b = (k & 1) ? (ww[k >> 1] >> 16) : (ww[k >> 1] & 0xffffu);
+      if (__uint_as_float(b << 16) >= bound) {
+        const int slot = atomicAdd(&sh.cand_n, 1);
+        if (slot < CAND_CAP)
+          sh.cand[slot] = ((unsigned long long)key_of(b, true) << 32) | (~(unsigned)(8 * v + k));
+      }
+    }
+  }
+  __syncthreads();
+  const int n = sh.cand_n;
+  if (n > CAND_CAP) return false;
+  for (int i = t; i < n; i += TK_THREADS) {
+    const unsigned long long ci = sh.cand[i];
+    int r = 0;
+    for (int j = 0; j < n; ++j) r += sh.cand[j] > ci;
+    if (r < SPEC_TOPK) {
+      sh.sel_idx[r] = (int)~(unsigned)(ci & 0xffffffffull);
+      sh.sel_val[r] = value_of_key16((unsigned)(ci >> 32));
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
 template <bool BF16>
 __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
   constexpr int BITS = BF16 ? 16 : 32;
@@ -117,13 +200,23 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
   const int V = a.V;
   const int t = threadIdx.x;
 
-  // request of this row -> temperature
-  int lo = 0, hi = a.B;  // largest b with cu[b] <= r
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (a.cu[mid] <= r) lo = mid; else hi = mid;
+  // request of this row (largest b with cu[b] <= r) -> temperature: warp 0
+  // narrows the range 32-fold per step with one load per lane
+  if (t < 32) {
+    int lo = 0, hi = a.B;
+    while (hi - lo > 1) {
+      const int step = (hi - lo + 31) / 32;
+      const int probe = lo + t * step;
+      const bool le = probe < hi && a.cu[probe] <= r;
+      const unsigned m = __ballot_sync(0xffffffffu, le);
+      const int last = 31 - __clz(m);        // lane 0 always qualifies (cu[lo] <= r)
+      lo = lo + last * step;
+      hi = min(hi, lo + step);
+    }
+    if (t == 0) sh.T = a.temp[lo];
   }
-  const float T = a.temp[lo];
+  __syncthreads();
+  const float T = sh.T;
   const bool greedy = !(T >= SPEC_GREEDY_T);
 
   const int ksel = min(SPEC_TOPK, V);
@@ -133,8 +226,12 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
       sh.sel_val[t] = t < V ? value_of_bits(load_bits(row, BF16, t), BF16) : -INFINITY;
     }
     __syncthreads();
+  } else if (BF16 && V % 8 == 0 && V >= 8 * TK_THREADS && ((uintptr_t)row & 15) == 0 &&
+             select_bf16_fast(row, V, sh)) {
+    // selected by the fast path
   } else {
     // pass 1: the maximum key
+    __syncthreads();
     if (t == 0) { sh.kmax = 0; sh.lt_count = 0; sh.prefix = 0; sh.need = SPEC_TOPK; }
     for (int i = t; i < 256; i += blockDim.x) sh.hist[i] = 0;
     __syncthreads();
@@ -249,23 +346,23 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
     __syncthreads();
   }
 
-  // sort the survivors by id (bitonic over 128 slots; padding sorts last)
-  for (int size = 2; size <= SPEC_TOPK; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (t < SPEC_TOPK) {
-        const int p = t ^ stride;
-        if (p > t) {
-          const bool up = (t & size) == 0;
-          const int ia = sh.sel_idx[t], ib = sh.sel_idx[p];
-          if ((ia > ib) == up) {
-            sh.sel_idx[t] = ib; sh.sel_idx[p] = ia;
-            const float va = sh.sel_val[t];
-            sh.sel_val[t] = sh.sel_val[p]; sh.sel_val[p] = va;
-          }
-        }
-      }
-      __syncthreads();
+  // order the survivors by id: each finds its place by counting smaller ids
+  // (ids are distinct; padding slots carry INT_MAX and stay at the end)
+  {
+    int id = 0x7fffffff, place = SPEC_TOPK;
+    float val = -INFINITY;
+    if (t < SPEC_TOPK) {
+      id = sh.sel_idx[t];
+      val = sh.sel_val[t];
+      place = 0;
+      for (int j = 0; j < SPEC_TOPK; ++j) place += sh.sel_idx[j] < id || (sh.sel_idx[j] == id && j < t);
     }
+    __syncthreads();
+    if (t < SPEC_TOPK) {
+      sh.sel_idx[place] = id;
+      sh.sel_val[place] = val;
+    }
+    __syncthreads();
   }
   // softmax over the survivors (fixed summation order); greedy: one-hot
   if (t < 32) {
@@ -303,7 +400,7 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(TK_THREADS) k_topk128(const TopkArgs a) {
+__global__ void __launch_bounds__(TK_THREADS, 2) k_topk128(const TopkArgs a) {
   __shared__ TopkSmem sh;
   if (a.hdr->status != SPEC_OK) return;   // inputs already rejected
   const int rows = min(a.rows_bound, a.cu[a.B]);
@@ -347,7 +444,7 @@ int launch_topk128(const void *logits, int dtype, int rows_bound, int V, const i
   if (rows_bound <= 0) return SPEC_OK;
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
-  const int grid = min(rows_bound, 4 * sms);
+  const int grid = min(rows_bound, 2 * sms);   // two 512-thread CTAs per SM
   k_topk128<<<grid, TK_THREADS, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -52,14 +52,13 @@ struct TreeArgs {
   TreeInfo *tree;
   RowTask *list;
   Part *part;
-  int32_t *node_aux;   // [n_nodes] depth, then child counts
   long long t_row_bytes, d_row_bytes;
   int nch_t, nch_d, nch_max;
   int stream_draft;
 };
 
 struct TreeLayout {
-  size_t hdr, tree, list, part, aux, total;
+  size_t hdr, tree, list, part, total;
   int nch_max;
 };
 
@@ -72,83 +71,92 @@ static TreeLayout tree_layout(int B, int n_nodes, int V) {
   L.tree = o; o += align256(sizeof(TreeInfo) * (size_t)B);
   L.list = o; o += align256(sizeof(RowTask) * rows);
   L.part = o; o += align256(sizeof(Part) * rows * L.nch_max * RS_CONS_WARPS);
-  L.aux = o;  o += align256(sizeof(int32_t) * 2 * (size_t)n_nodes);
   L.total = o;
   return L;
 }
 
 // ------------------------------------------------------------------ setup
-__global__ void __launch_bounds__(1024) k_setup_tree(const TreeArgs a) {
-  __shared__ int scratch[33];
-  if (threadIdx.x == 0) {
-    a.hdr->status = SPEC_OK;
-    a.hdr->detail = -1;
-    a.hdr->work = 0;
-    a.hdr->n_list = 0;
+// One block per tree. The tree's parent ids are staged in shared memory; one
+// thread derives depths in topological order, the block counts children and
+// checks tokens. The row list is indexed by slot (target row n at position
+// n, draft row n at position n_nodes + n), so trees write their entries
+// without a scan. The header was cleared before the launch; an invalid tree
+// sets the status word and every later kernel of the call skips its work.
+constexpr int SETUP_THREADS = 256;
+
+__global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) {
+  __shared__ int s_par[SPEC_MAX_TREE_NODES];
+  __shared__ unsigned short s_depth[SPEC_MAX_TREE_NODES];   // depths <= 4095
+  __shared__ int s_kids[SPEC_MAX_TREE_NODES];
+  __shared__ int s_bad;
+  const int b = blockIdx.x, t = threadIdx.x;
+  if (b == 0 && t == 0) a.hdr->n_list = 2 * a.n_nodes;
+  {   // rows past the last tree (n_nodes > cu[B]) are not streamed
+    const int used = min(max(a.cu[a.B], 0), a.n_nodes);
+    for (int n = used + b * SETUP_THREADS + t; n < a.n_nodes; n += gridDim.x * SETUP_THREADS) {
+      a.list[n].slot = -1;
+      a.list[a.n_nodes + n].slot = -1;
+    }
+  }
+  TreeInfo ti;
+  ti.base = a.cu[b];
+  ti.N = a.cu[b + 1] - a.cu[b];
+  const float T = a.temp[b];
+  const bool greedy = T < SPEC_GREEDY_T;
+  bool ok = (b > 0 || a.cu[0] == 0) && ti.base >= 0 && ti.N >= 1 &&
+            ti.N <= SPEC_MAX_TREE_NODES && a.cu[b + 1] <= a.n_nodes && T >= 0.f && isfinite(T);
+  if (ok && !greedy && a.draft == nullptr) ok = false;
+  if (t == 0) s_bad = !ok;
+  __syncthreads();
+  if (ok) {
+    for (int c = t; c < ti.N; c += SETUP_THREADS) {
+      const int p = a.parent[ti.base + c];
+      s_par[c] = p;
+      s_kids[c] = 0;
+      const bool good = c == 0 ? p == -1
+                               : (p >= 0 && p < c && (unsigned)a.node_token[ti.base + c] <
+                                                          (unsigned)a.V);
+      if (!good) s_bad = 1;
+    }
   }
   __syncthreads();
-  const int per = (a.B + blockDim.x - 1) / blockDim.x;
-  const int b0 = min(a.B, (int)threadIdx.x * per), b1 = min(a.B, b0 + per);
-  int32_t *depth = a.node_aux, *nkids = a.node_aux + a.n_nodes;
-  int cnt = 0, bad = 0;
-  const bool cu_ok = a.B == 0 || a.cu[0] == 0;
-  for (int b = b0; b < b1; ++b) {
-    TreeInfo t;
-    t.base = a.cu[b];
-    t.N = a.cu[b + 1] - a.cu[b];
-    const float T = a.temp[b];
-    const bool greedy = T < SPEC_GREEDY_T;
-    bool ok = cu_ok && t.base >= 0 && t.N >= 1 && t.N <= SPEC_MAX_TREE_NODES &&
-              a.cu[b + 1] <= a.n_nodes && T >= 0.f && isfinite(T);
-    if (ok && !greedy && a.draft == nullptr) ok = false;
-    if (ok) {
-      for (int c = 0; c < t.N; ++c) nkids[t.base + c] = 0;
-      for (int c = 0; c < t.N && ok; ++c) {
-        const int p = a.parent[t.base + c];
-        if (c == 0) {
-          ok = p == -1;
-          depth[t.base] = 0;
-          continue;
-        }
-        const int tok = a.node_token[t.base + c];
-        ok = p >= 0 && p < c && tok >= 0 && tok < a.V;
-        if (!ok) break;
-        depth[t.base + c] = depth[t.base + p] + 1;
-        ok = depth[t.base + c] <= a.max_depth && ++nkids[t.base + p] <= a.max_branch;
+  if (ok && !s_bad) {
+    for (int c = t + 1; c < ti.N; c += SETUP_THREADS) atomicAdd(&s_kids[s_par[c]], 1);
+    if (t == 0) {   // depths in topological order (parent[c] < c)
+      s_depth[0] = 0;
+      int worst = 0;
+      for (int c = 1; c < ti.N; ++c) {
+        s_depth[c] = (unsigned short)(s_depth[s_par[c]] + 1);
+        worst = max(worst, (int)s_depth[c]);
       }
+      if (worst > a.max_depth) s_bad = 1;
     }
-    t.mode = ok ? (greedy ? MODE_GREEDY : MODE_SAMPLE) : MODE_SKIP;
-    t.c = (ok && !greedy) ? (float)(1.4426950408889634 / (double)T) : 0.f;
-    if (!ok) {
-      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-      bad = 1;
-    } else {
-      cnt += t.N;
-      if (t.mode == MODE_SAMPLE && a.stream_draft)
-        for (int c = 0; c < t.N; ++c) cnt += nkids[t.base + c] > 0;
-    }
-    a.tree[b] = t;
   }
-  if (__syncthreads_or(bad)) {   // offsets are only trusted when all are sound
-    for (int b = b0; b < b1; ++b) a.tree[b].mode = MODE_SKIP;
-    return;
+  __syncthreads();
+  if (ok && !s_bad)
+    for (int c = t; c < ti.N; c += SETUP_THREADS)
+      if (s_kids[c] > a.max_branch) s_bad = 1;
+  __syncthreads();
+  ok = ok && !s_bad;
+  ti.mode = ok ? (greedy ? MODE_GREEDY : MODE_SAMPLE) : MODE_SKIP;
+  ti.c = (ok && !greedy) ? (float)(1.4426950408889634 / (double)T) : 0.f;
+  if (t == 0) {
+    a.tree[b] = ti;
+    if (!ok) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
   }
-  int total;
-  int off = block_excl_scan_int(cnt, scratch, &total);
-  for (int b = b0; b < b1; ++b) {
-    const TreeInfo t = a.tree[b];
-    for (int c = 0; c < t.N; ++c) a.list[off++] = RowTask{t.base + c, t.base + c, 0, t.c};
-    if (t.mode == MODE_SAMPLE && a.stream_draft)
-      for (int c = 0; c < t.N; ++c)
-        if (nkids[t.base + c] > 0)
-          a.list[off++] = RowTask{a.n_nodes + t.base + c, t.base + c, 1, t.c};
+  if (!ok) return;
+  const bool drafts = ti.mode == MODE_SAMPLE && a.stream_draft;
+  for (int c = t; c < ti.N; c += SETUP_THREADS) {
+    const int n = ti.base + c;
+    a.list[n] = RowTask{n, n, 0, ti.c};
+    a.list[a.n_nodes + n] = RowTask{drafts && s_kids[c] > 0 ? a.n_nodes + n : -1, n, 1, ti.c};
   }
-  if (threadIdx.x == 0) a.hdr->n_list = total;
 }
 
 // ------------------------------------------------------------------- walk
 struct WalkSmem {
   float tsum[MAX_WALK_TILES];
+  float wsum[64 * 32];                   // per-warp tile sums of one batch
   float scratch[33];
   int kids[SPEC_MAX_TREE_BRANCH];
   float s[SPEC_MAX_TREE_BRANCH + 1];     // 1 / (1 - q(E_j))
@@ -195,22 +203,34 @@ __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkS
 }
 
 // One pass over the node's rows: tile totals of the level-L weights into
-// sh.tsum and their sum into sh.Z (thread 0, ascending tile order).
+// sh.tsum and their sum into sh.Z (ascending tile order). Tiles are summed
+// per warp and combined once per batch of up to 64 tiles.
 template <int DK>
 __device__ void weight_pass(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, float c, int L,
                             bool residual) {
   const int ntiles = (a.V + WALK_TILE - 1) / WALK_TILE;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float w[SAMPLE_EPT];
-  for (int j = 0; j < ntiles; ++j) {
-    tile_weights_tree<DK>(a, sh, nl, c, L, residual, j, w);
-    float s = 0.f;
+  for (int j0 = 0; j0 < ntiles; j0 += 64) {
+    const int j1 = min(ntiles, j0 + 64);
+#pragma unroll 2
+    for (int j = j0; j < j1; ++j) {
+      tile_weights_tree<DK>(a, sh, nl, c, L, residual, j, w);
+      float s = 0.f;
 #pragma unroll
-    for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
-    float tot;
-    block_excl_scan(s, sh.scratch, &tot);
-    if (threadIdx.x == 0) sh.tsum[j] = tot;
+      for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) sh.wsum[(j - j0) * 32 + warp] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < j1 - j0) {
+      float t = 0.f;
+      for (int q = 0; q < WALK_THREADS / 32; ++q) t += sh.wsum[threadIdx.x * 32 + q];
+      sh.tsum[j0 + threadIdx.x] = t;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   if (threadIdx.x == 0) {
     float Z = 0.f;
     for (int j = 0; j < ntiles; ++j) Z += sh.tsum[j];
@@ -288,7 +308,7 @@ __global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
     out[j] = -1;
     if (path) path[j] = -1;
   }
-  if (t.mode == MODE_SKIP) {
+  if (t.mode == MODE_SKIP || *(volatile int *)&a.hdr->status != SPEC_OK) {
     if (threadIdx.x == 0) a.out_accepted[b] = -1;
     return;
   }
@@ -502,7 +522,6 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   a.tree = reinterpret_cast<TreeInfo *>(ws + L.tree);
   a.list = reinterpret_cast<RowTask *>(ws + L.list);
   a.part = reinterpret_cast<Part *>(ws + L.part);
-  a.node_aux = reinterpret_cast<int32_t *>(ws + L.aux);
   a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
   a.d_row_bytes = (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
   a.nch_t = nchunks(V, tdt);
@@ -510,9 +529,10 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   a.nch_max = L.nch_max;
   a.stream_draft = dk == SPEC_DRAFT_LOGITS;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  k_setup_tree<<<1, 1024, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
+  k_setup_tree<<<B, SETUP_THREADS, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   RowPassArgs rp;
   rp.base[0] = a.target;
   rp.base[1] = a.draft;

@@ -193,11 +193,16 @@ def test_draft_topk_softmax_matches_oracle():
 
 
 @pytest.mark.parametrize("dtype,V,T", [("bf16", 100, 1.0), ("f32", 3000, 0.7),
-                                       ("bf16", 777, 0.0), ("f32", 129, 2.0)])
+                                       ("bf16", 777, 0.0), ("f32", 129, 2.0),
+                                       ("bf16", 4096, 1.0), ("bf16", 65536, 0.5)])
 def test_draft_topk_softmax_edge_cases(dtype, V, T):
     g = torch.Generator(device=DEV).manual_seed(V)
     z = torch.randn(9, V, generator=g, device=DEV)
     z = (torch.round(z * 3) / 3).to(S._DTYPES[dtype])    # many exact ties
+    if V == 65536:   # one row of a logit shape (few ties), one constant row
+        z[0] = (2.0 * torch.randn(V, generator=g, device=DEV)
+                - 1.1 * torch.log(torch.randperm(V, generator=g, device=DEV).float() + 1)).to(z.dtype)
+        z[1] = 0.25
     cu = torch.tensor([0, 4, 9], dtype=torch.int32, device=DEV)
     temp = torch.tensor([T, T], device=DEV)
     idx, prob, ws = sv.draft_topk_softmax(z.contiguous(), cu, temp)
