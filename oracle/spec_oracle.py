@@ -21,6 +21,12 @@ Sources (web pages; cited by title and section):
   (accept with min(1, p/q~); on rejection use the normalised residual
   norm(max(0, p - q~)) and test the remaining drafts against it; descend into
   the subtree on acceptance), §6 "Teorema 1" (the output law equals p).
+* "Acceptance Is Not Speed (arXiv:2610.23818)", §2 "Taksonomi 5 Aturan Lossy
+  Speculative Decoding" (relaxed rules replace the target law in the
+  acceptance test), §6 RULE 1-3 of the reference harness (the low-support
+  guard on target rank and p(x), then the strict test, then the CACTUS test
+  gamma(x) = min(p(x) + sqrt(2 alpha p(x) (1 - p(x))), 1) against q(x)) and §7
+  item 3 (the guard with p(x) < 0.10 or outside the top k = 10).
 * "Speculative decoding: memverifikasi token draft sebelum diterima"
   (nalar.dev), sections "Draft mengubah tebakan serial menjadi batch
   verifikasi" (one target pass scores positions 1..K+1, each conditioned on
@@ -53,8 +59,19 @@ R7  Tree: children of a node are tested in node-index order (the order they
     argmax p_v.
 R8  A draw is *flagged* when the exact value sits within 1e-6 of a decision
     boundary (|u - a| <= 1e-6 for a coin, |u*Z - C| <= 1e-6*Z for either
-    cumulative bracketing the chosen token). Tokens from that output slot on
-    are not compared bit for bit against a fp32 implementation.
+    cumulative bracketing the chosen token, |p(d) - min_prob| <= 1e-6 for the
+    low-support guard). Tokens from that output slot on are not compared bit
+    for bit against a fp32 implementation.
+R9  Target rank of d: 1 + the number of tokens whose target logit is strictly
+    larger than d's (tied tokens share the better rank; temperature does not
+    change it).
+R10 CACTUS rule: accept d iff u < min(1, gamma(d) / q(d)) (accepted outright
+    when q(d) <= gamma(d), which covers q <= p); the guard, when on, rejects
+    first, without a coin, when rank(d) > max_rank (max_rank > 0) or
+    p(d) < min_prob. Greedy requests (R2) keep the greedy rule.
+R11 The CACTUS residual is not given (its table is lost): after a rejection
+    the final token is drawn from norm(max(0, p - q)) as in the lossless rule
+    (p itself when that has no mass), the bonus from p_{K+1}.
 """
 from __future__ import annotations
 
@@ -73,6 +90,7 @@ STREAM_BONUS = 2
 RULE_STRICT = 0
 RULE_GREEDY = 1
 RULE_STRICT_TOP128 = 2
+RULE_CACTUS = 3
 
 DRAFT_LOGITS = 0
 DRAFT_PROBS = 1
@@ -180,6 +198,25 @@ def coin_flagged(u: float, a: float) -> bool:
     return abs(u - a) <= FLAG_EPS
 
 
+def target_rank(zt: np.ndarray, d: int) -> int:
+    """R9: 1 + #{y : z_y > z_d} over the target logits of the position."""
+    zt = np.asarray(zt, dtype=np.float64)
+    return 1 + int(np.count_nonzero(zt > zt[d]))
+
+
+def cactus_gamma(p_d: float, alpha: float) -> float:
+    """Relaxed target mass of the CACTUS rule ("Acceptance Is Not Speed", §6
+    RULE 3): min(p + sqrt(2 alpha p (1 - p)), 1)."""
+    return min(p_d + float(np.sqrt(2.0 * alpha * p_d * (1.0 - p_d))), 1.0)
+
+
+def low_support(p_d: float, rank: int, max_rank: int, min_prob: float) -> bool:
+    """Low-support guard ("Acceptance Is Not Speed", §6 RULE 1 and §7 item
+    3): reject outright a draft whose target rank exceeds max_rank (when
+    max_rank > 0) or whose target probability is below min_prob."""
+    return (max_rank > 0 and rank > max_rank) or p_d < min_prob
+
+
 def residual(p: np.ndarray, q: np.ndarray) -> np.ndarray:
     """Unnormalised residual max(0, p - q) (RheoSampling 2026, §4 step 3)."""
     return np.maximum(0.0, p - q)
@@ -229,7 +266,8 @@ def _draft_law(draft, draft_kind, draft_idx, row, T, V, rule):
 
 def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
                   rule=RULE_STRICT, draft_kind=DRAFT_LOGITS, draft_idx=None,
-                  max_k=None, requests=None):
+                  max_k=None, requests=None, alpha=0.0, max_rank=0,
+                  min_prob=0.0):
     """One verification round for a batch of requests.
 
     Request b owns drafts d_1..d_K (K = cu_draft[b+1] - cu_draft[b]), target
@@ -244,7 +282,9 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
     (1 or 0, -1)), ``flag_slot`` [n] (first output slot decided by a flagged
     draw, -1 if none) and ``requests`` (the request ids processed).
     ``requests`` restricts the work to a subset (the hash still uses the
-    global request id).
+    global request id). ``rank`` [R_d] is the target rank of every draft
+    token (R9). Under ``RULE_CACTUS`` the acceptance test is R10 with
+    ``alpha``, ``max_rank`` and ``min_prob``; the final token follows R11.
     """
     cu = np.asarray(cu_draft, dtype=np.int64)
     B = cu.size - 1
@@ -257,6 +297,7 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
     flag_slot = np.full(len(req), -1, dtype=np.int64)
     R_d = int(cu[-1])
     pq = np.full((R_d, 2), np.nan)
+    rank = np.full(R_d, -1, dtype=np.int64)
     toks = np.asarray(draft_tokens, dtype=np.int64)
     temps = np.asarray(temperature, dtype=np.float64)
 
@@ -271,19 +312,28 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
         for i in range(K):
             d = int(toks[d0 + i])
             zt = as_f64(target[t0 + i])
+            rank[d0 + i] = target_rank(zt, d)
             if greedy:
                 ok = d == argmax_lowest(zt)          # "Semantik penerimaan"
                 pq[d0 + i] = (1.0 if ok else 0.0, -1.0)
             else:
                 p = softmax_T(zt, T)
                 q = _draft_law(draft, draft_kind, draft_idx, d0 + i, T, V, rule)
-                a = acceptance_prob(p[d], q[d])
                 pq[d0 + i] = (p[d], q[d])
+                if rule == RULE_CACTUS:
+                    a = acceptance_prob(cactus_gamma(p[d], alpha), q[d])
+                    guard = low_support(p[d], rank[d0 + i], max_rank, min_prob)
+                else:
+                    a = acceptance_prob(p[d], q[d])
+                    guard = False
                 if n == K:   # still scanning: draw this position's coin
                     u = uniform(seed, b, i + 1, STREAM_COIN)
-                    if coin_flagged(u, a) and flagged_at < 0:
+                    if rule == RULE_CACTUS and min_prob > 0.0 \
+                            and abs(p[d] - min_prob) <= FLAG_EPS and flagged_at < 0:
                         flagged_at = i
-                    ok = coin_accepts(u, a)
+                    if not guard and coin_flagged(u, a) and flagged_at < 0:
+                        flagged_at = i
+                    ok = not guard and coin_accepts(u, a)
             if n == K and not ok:
                 n = i      # first rejection stops the scan ("Penolakan")
         # the final token, from target row n+1
@@ -305,7 +355,7 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
         tokens[j, n] = final
         accepted[j] = n
         flag_slot[j] = flagged_at
-    return dict(tokens=tokens, accepted=accepted, pq=pq,
+    return dict(tokens=tokens, accepted=accepted, pq=pq, rank=rank,
                 flag_slot=flag_slot, requests=np.asarray(req))
 
 
