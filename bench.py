@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--cpu-requests", type=int, default=1024,
                     help="requests (or trees) in the oracle's timed sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rule", default="default", choices=["default", "cactus"],
+                    help="linear workloads: the workload's lossless rule, or the relaxed "
+                         "CACTUS rule with the recommended low-support guard")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
 
@@ -165,7 +168,10 @@ class LinearWork:
     """spec_verify_linear on a linear workload (configs 1, 2, 3, 5)."""
     unit_name = "requests"
 
-    def __init__(self, cfg, dev, input_seed=None, B=None):
+    # relaxed rule options: the guard the page recommends (p >= 0.10, top 10)
+    CACTUS = {"alpha": 0.5, "max_rank": 10, "min_prob": 0.10}
+
+    def __init__(self, cfg, dev, input_seed=None, B=None, rule=None):
         import torch
         import speculative_decoding_rejection_gb300 as sv
         from speculative_decoding_rejection_gb300 import synthetic as S
@@ -173,6 +179,9 @@ class LinearWork:
         over = {} if B is None else {"B": B}
         self.lb = lb = S.make_linear(cfg, device=dev, input_seed=input_seed, **over)
         self.rule = sv.SPEC_RULE_STRICT_TOP128 if lb.top128 else sv.SPEC_RULE_STRICT
+        self.ext = None
+        if rule == "cactus":
+            self.rule, self.ext = sv.SPEC_RULE_CACTUS, dict(self.CACTUS)
         K = torch.diff(lb.cu_draft.cpu().long())
         samp = lb.temperature.cpu() >= 0.05
         self.positions = int(K.sum())
@@ -191,6 +200,9 @@ class LinearWork:
         self.config = {"workload": lb.meta["workload"], "B": lb.B, "K": lb.max_k, "V": lb.V,
                        "logits": "bf16" if lb.target.element_size() == 2 else "f32",
                        "rule": "strict_top128" if lb.top128 else "strict"}
+        if self.ext is not None:
+            self.config["rule"] = ("cactus(alpha={alpha},max_rank={max_rank},"
+                                   "min_prob={min_prob})".format(**self.ext))
 
     def input_tensors(self):
         lb = self.lb
@@ -200,6 +212,12 @@ class LinearWork:
     def call(self, inputs=None):
         lb = self.lb
         t = inputs or self.input_tensors()
+        if self.ext is not None:
+            self.sv.spec_verify_linear_ext(t["target"], t["draft"], t["draft_tokens"],
+                                           t["cu_draft"], t["temperature"], lb.seed,
+                                           max_k=lb.max_k, rule=self.rule, workspace=self.ws,
+                                           out=self.outs + (None,), **self.ext)
+            return
         self.sv.spec_verify_linear(t["target"], t["draft"], t["draft_tokens"], t["cu_draft"],
                                    t["temperature"], lb.seed, max_k=lb.max_k, rule=self.rule,
                                    workspace=self.ws, out=self.outs)
@@ -222,7 +240,7 @@ class LinearWork:
         tgt, drf, toks, cu, T = self._host
         req = np.sort(np.roll(self._order, -offset)[:min(units, lb.B)])
         O.verify_linear(tgt, drf, toks, cu, T, lb.seed, rule=self.rule, max_k=lb.max_k,
-                        requests=req)
+                        requests=req, **(self.ext or {}))
         return int(sum(cu[b + 1] - cu[b] for b in req))
 
 
@@ -294,8 +312,10 @@ class TreeWork:
         return int(sum(cu[b + 1] - cu[b] - 1 for b in req))
 
 
-def make_work(cfg, dev, input_seed=None, B=None):
-    return (TreeWork if cfg == 4 else LinearWork)(cfg, dev, input_seed, B)
+def make_work(cfg, dev, input_seed=None, B=None, rule=None):
+    if cfg == 4:
+        return TreeWork(cfg, dev, input_seed, B)
+    return LinearWork(cfg, dev, input_seed, B, rule)
 
 
 def cpu_baseline(work, n_units):
@@ -317,7 +337,7 @@ def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     import torch
     dev = "cuda:0" if torch.cuda.is_available() else "cpu"
-    work = make_work(args.config, dev, B=args.B)
+    work = make_work(args.config, dev, B=args.B, rule=args.rule)
     per_step = 1 if args.config == 4 else 2
     for k in range(args.warmup):
         work.oracle_sample(per_step, offset=k * per_step)
@@ -354,7 +374,7 @@ def main():
     dev = torch.device("cuda", local)
     sv.lib()
     work = make_work(args.config, dev, input_seed=S.INPUT_SEED_BASE + args.config + 7919 * rank,
-                     B=args.B)
+                     B=args.B, rule=args.rule)
 
     for _ in range(max(3, args.warmup)):
         work.call()

@@ -28,6 +28,13 @@
  *     ("RheoSampling 2026", §3).
  *   - tree verification by recursive rejection sampling without replacement
  *     over siblings ("RheoSampling 2026", §4).
+ *   - relaxed (lossy) CACTUS rule: accept d_i with probability
+ *     min(1, gamma/q_i(d_i)), gamma = min(p + sqrt(2 alpha p (1 - p)), 1) at
+ *     p = p_i(d_i), after a low-support guard that rejects outright a draft
+ *     whose target rank exceeds k or whose p is below a floor ("Acceptance
+ *     Is Not Speed (arXiv:2610.23818)", §2, §6 rules 1-3 and §7 item 3). The
+ *     page's residual for this rule is lost; the library draws the
+ *     replacement from norm(max(0, p - q)) as in the lossless rule.
  *
  * Random numbers. Every uniform is u = (splitmix64(seed ^ splitmix64(key))
  * >> 40) * 2^-24 with key = (b << 32) | (pos << 8) | stream, where
@@ -91,7 +98,8 @@ typedef enum {
 typedef enum {
   SPEC_RULE_STRICT = 0,       /* lossless; requests with T < 0.05 greedy     */
   SPEC_RULE_GREEDY = 1,       /* every request greedy                        */
-  SPEC_RULE_STRICT_TOP128 = 2 /* lossless, dense draft logits cut to top-128 */
+  SPEC_RULE_STRICT_TOP128 = 2, /* lossless, dense draft logits cut to top-128 */
+  SPEC_RULE_CACTUS = 3         /* relaxed rule + guard; needs spec_linear_ext */
 } spec_rule;
 
 #define SPEC_TOPK 128
@@ -142,6 +150,46 @@ int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
                        uint64_t seed, int rule, int32_t *out_tokens,
                        int32_t *out_accepted, float *out_pq, void *workspace,
                        size_t ws_bytes, spec_stream_t stream);
+
+/*
+ * Options of spec_verify_linear_ext (host memory, read during the call).
+ *   alpha     SPEC_RULE_CACTUS divergence budget, finite and >= 0; 0 makes
+ *             gamma = p, the lossless test.
+ *   max_rank  guard: reject d_i when its target rank (1 + the number of
+ *             tokens whose target logit is strictly larger than d_i's; ties
+ *             share the better rank) exceeds max_rank; 0 = off. Used by
+ *             SPEC_RULE_CACTUS only.
+ *   min_prob  guard: reject d_i when p_i(d_i) < min_prob; 0 = off.
+ *             SPEC_RULE_CACTUS only.
+ *   out_rank  optional device [R_d] int32: the target rank of every draft
+ *             token (every request and rule; also after the first
+ *             rejection). NULL to skip.
+ * The guard and the relaxed coin apply to sampling requests; greedy
+ * requests (T < 0.05) keep the greedy rule.
+ */
+typedef struct {
+  float alpha;
+  int32_t max_rank;
+  float min_prob;
+  int32_t reserved;   /* must be 0 */
+  int32_t *out_rank;
+} spec_linear_ext;
+
+/*
+ * spec_verify_linear with options: the same arguments and semantics, plus
+ * `ext` (NULL = no options, then identical to spec_verify_linear).
+ * SPEC_RULE_CACTUS requires ext. Needs spec_verify_linear_workspace(B,
+ * max_k, V, rule) bytes of workspace.
+ */
+int spec_verify_linear_ext(const void *target, int tdt, const void *draft,
+                           int ddt, int dk, const int32_t *draft_idx,
+                           const int32_t *draft_tokens,
+                           const int32_t *cu_draft, const float *temperature,
+                           int B, int V, int max_k, uint64_t seed, int rule,
+                           const spec_linear_ext *ext, int32_t *out_tokens,
+                           int32_t *out_accepted, float *out_pq,
+                           void *workspace, size_t ws_bytes,
+                           spec_stream_t stream);
 
 /*
  * No-allocation variant of spec_verify_linear. The paper has no counterpart:

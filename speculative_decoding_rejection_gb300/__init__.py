@@ -16,8 +16,8 @@ from pathlib import Path
 __all__ = [
     "SPEC_OK", "SPEC_F32", "SPEC_BF16", "SPEC_DRAFT_LOGITS", "SPEC_DRAFT_PROBS",
     "SPEC_DRAFT_SPARSE128", "SPEC_RULE_STRICT", "SPEC_RULE_GREEDY",
-    "SPEC_RULE_STRICT_TOP128", "SPEC_TOPK", "lib", "spec_status_string",
-    "spec_verify_linear", "spec_verify_linear_workspace", "spec_verify_tree",
+    "SPEC_RULE_STRICT_TOP128", "SPEC_RULE_CACTUS", "SPEC_TOPK", "lib", "spec_status_string",
+    "spec_verify_linear", "spec_verify_linear_ext", "spec_verify_linear_workspace", "spec_verify_tree",
     "spec_verify_tree_workspace", "draft_topk_softmax",
     "draft_topk_softmax_workspace", "spec_get_status", "spec_uniforms",
     "spec_profile_row_pass", "SpecError",
@@ -31,7 +31,7 @@ SPEC_ERR_CUDA = -4
 SPEC_ERR_TIMEOUT = -5
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS, SPEC_DRAFT_SPARSE128 = 0, 1, 2
-SPEC_RULE_STRICT, SPEC_RULE_GREEDY, SPEC_RULE_STRICT_TOP128 = 0, 1, 2
+SPEC_RULE_STRICT, SPEC_RULE_GREEDY, SPEC_RULE_STRICT_TOP128, SPEC_RULE_CACTUS = 0, 1, 2, 3
 SPEC_TOPK = 128
 
 LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
@@ -39,11 +39,21 @@ HEADER = Path(__file__).resolve().parent.parent / "include" / "specverify.h"
 
 _lib = None
 _vp, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+class SpecLinearExt(ctypes.Structure):
+    """spec_linear_ext of include/specverify.h."""
+    _fields_ = [("alpha", ctypes.c_float), ("max_rank", ctypes.c_int32),
+                ("min_prob", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("out_rank", ctypes.c_void_p)]
+
+
 _SIGS = {
     "spec_status_string": (ctypes.c_char_p, [_i32]),
     "spec_verify_linear_workspace": (_sz, [_i32, _i32, _i32, _i32]),
     "spec_verify_linear": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                   _i32, _u64, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify_linear_ext": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32,
+                                      _i32, _i32, _u64, _i32, ctypes.POINTER(SpecLinearExt),
+                                      _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_verify_tree_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "spec_verify_tree": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                 _i32, _i32, _i32, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -171,6 +181,43 @@ def spec_verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed:
         _ptr(pq), _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
     _check(code, "spec_verify_linear")
     return tokens, accepted, pq, ws
+
+
+def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, seed: int, *,
+                           max_k: int, rule: int = SPEC_RULE_STRICT,
+                           draft_kind: int = SPEC_DRAFT_LOGITS, draft_idx=None, alpha=0.0,
+                           max_rank=0, min_prob=0.0, want_pq=False, want_rank=False,
+                           workspace=None, out=None, stream=None):
+    """spec_verify_linear with the relaxed CACTUS rule's options and target
+    ranks.
+
+    Returns (tokens, accepted, pq or None, rank [R_d] int32 or None,
+    workspace).
+    """
+    torch = _torch()
+    B = cu_draft.numel() - 1
+    V = target.shape[1]
+    dev = target.device
+    ws_bytes = spec_verify_linear_workspace(B, max_k, V, rule)
+    if ws_bytes == 0:
+        raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_linear_workspace")
+    ws = _workspace(ws_bytes, dev, workspace)
+    if out is None:
+        tokens = torch.empty(B, max_k + 1, dtype=torch.int32, device=dev)
+        accepted = torch.empty(B, dtype=torch.int32, device=dev)
+        pq = torch.empty(draft_tokens.numel(), 2, dtype=torch.float32, device=dev) if want_pq else None
+        rank = torch.empty(draft_tokens.numel(), dtype=torch.int32, device=dev) if want_rank else None
+    else:
+        tokens, accepted, pq, rank = out
+    ext = SpecLinearExt(float(alpha), int(max_rank), float(min_prob), 0, _ptr(rank))
+    ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
+    code = lib().spec_verify_linear_ext(
+        _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(draft_idx),
+        _ptr(draft_tokens), _ptr(cu_draft), _ptr(temperature), B, V, max_k,
+        ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), rule, ctypes.byref(ext), _ptr(tokens),
+        _ptr(accepted), _ptr(pq), _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check(code, "spec_verify_linear_ext")
+    return tokens, accepted, pq, rank, ws
 
 
 def spec_verify_tree_workspace(B: int, n_nodes: int, V: int, max_depth: int, max_branch: int) -> int:

@@ -55,7 +55,7 @@ struct Part {            // statistics of one chunk of one row
   float m;               // max logit
   float S;               // sum of 2^((z - m) c)
   int idx;               // lowest index attaining m
-  int pad;
+  int cnt;               // logits above the rank threshold (rank count only)
 };
 
 struct ReqInfo {         // per request, written by the setup kernel
@@ -146,6 +146,12 @@ __device__ __forceinline__ f32x2 bsub2(uint32_t w, float m) {
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Packed a > b on two bf16 lanes: each 16-bit half is 0xffff where true.
+__device__ __forceinline__ uint32_t bgt2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 

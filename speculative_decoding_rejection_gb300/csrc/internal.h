@@ -27,6 +27,10 @@ struct RowPassArgs {
   const RowTask *list;      // rows to stream (count in hdr->n_list)
   WsHeader *hdr;
   Part *part;
+  // Optional rank count: for a target row of list slot s, rank_thr[s] is the
+  // draft token's logit (+inf: no count) and every Part's `cnt` receives the
+  // number of the chunk's logits strictly above it. NULL: no counting.
+  const float *rank_thr;
   // Residual mode: instead of the row list, stream for every job of `jobs`
   // (count in hdr->n_jobs_a) target row t0+n and draft row d0+n tile by tile
   // (SAMPLE_TILE elements of each, bf16, 16-byte aligned rows) and leave per

@@ -13,6 +13,13 @@
 //                 itself when Z == 0); n == K: bonus draw from p_{K+1} at
 //                 u(seed, b, K+1, 2); greedy: argmax p_{n+1}.
 //                 Draw = smallest x (ascending id) with u*Z < C_x.
+//   CACTUS rule   a_i = min(1, gamma/q_i(d_i)) with gamma = min(p + sqrt(2
+//                 alpha p (1 - p)), 1), p = p_i(d_i), after the low-support
+//                 guard (reject outright when rank(d_i) > max_rank or
+//                 p < min_prob) ("Acceptance Is Not Speed", §6 rules 1-3 and
+//                 §7 item 3); the rank is counted by the row pass. The
+//                 replacement after a rejection is the lossless residual
+//                 draw (the page's residual for the rule is lost).
 #include "common.cuh"
 #include "internal.h"
 
@@ -48,10 +55,16 @@ struct LinearArgs {
   int rt_max;                 // slot offset of draft rows
   int sparse;                 // the draft law is sparse (given or top-128)
   int stream_draft;           // the row pass reads dense draft logits
+  // relaxed rule and target ranks
+  float alpha, min_prob;
+  int max_rank;
+  int want_rank;              // the row pass counts ranks
+  float *rank_thr;            // [rt_max] draft token's target logit per slot
+  int32_t *out_rank;
 };
 
 struct LinearLayout {
-  size_t hdr, req, jobs_a, jobs_b, tsum, list, part, tk_idx, tk_prob, total;
+  size_t hdr, req, jobs_a, jobs_b, tsum, list, part, tk_idx, tk_prob, rank_thr, total;
   int nch_max;
   long long rows_max;
 };
@@ -72,6 +85,7 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   const size_t tk = rule == SPEC_RULE_STRICT_TOP128 ? (size_t)B * max_k * SPEC_TOPK : 0;
   L.tk_idx = o;  o += align256(sizeof(int32_t) * tk);
   L.tk_prob = o; o += align256(sizeof(float) * tk);
+  L.rank_thr = o; o += align256(sizeof(float) * (size_t)B * (max_k + 1));
   L.total = o;
   return L;
 }
@@ -116,6 +130,16 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
   r.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);
   a.req[b] = r;
   for (int i = 0; i <= K; ++i) a.list[r.t0 + i] = RowTask{r.t0 + i, r.t0 + i, 0, r.c};
+  if (a.want_rank) {   // threshold of the rank count: the draft token's target logit
+    for (int i = 0; i < K; ++i) {
+      const int d = a.tokens[r.d0 + i];
+      a.rank_thr[r.t0 + i] =
+          (unsigned)d < (unsigned)a.V
+              ? load_elem(a.target + (long long)(r.t0 + i) * a.t_row_bytes, a.tdt, d)
+              : INFINITY;   // reported by the accept scan
+    }
+    a.rank_thr[r.t0 + K] = INFINITY;
+  }
   const bool drafts = r.mode == MODE_SAMPLE && a.stream_draft;
   for (int i = 0; i < K; ++i)
     a.list[a.rt_max + r.d0 + i] = RowTask{drafts ? a.rt_max + r.d0 + i : -1, r.d0 + i, 1, r.c};
@@ -140,6 +164,16 @@ __device__ __forceinline__ RowStat warp_row_stat(const Part *p, int n, float c, 
     merge_stat(m, S, idx, m2, S2, i2, c);
   }
   return RowStat{m, S, idx};
+}
+// Rank count of a target row: the sum of the chunk partials' counts.
+__device__ __forceinline__ int warp_row_count(const LinearArgs &a, int row, int lane) {
+  const Part *p = a.part + (long long)row * a.nch_max * RS_CONS_WARPS;
+  const int n = a.nch_t * RS_CONS_WARPS;
+  int c = 0;
+  for (int i = lane; i < n; i += 32) c += p[i].cnt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  return c;
 }
 __device__ __forceinline__ RowStat target_stat(const LinearArgs &a, int row, float c, int lane) {
   return warp_row_stat(a.part + (long long)row * a.nch_max * RS_CONS_WARPS,
@@ -187,9 +221,14 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
     const int cnt = min(32, K - base);
     // statistics of this block of positions: lane i keeps position base + i
     RowStat ts{NO_MAX, 0.f, 0x7fffffff}, ds{NO_MAX, 0.f, 0x7fffffff};
+    int rank = 0;
     for (int i = 0; i < cnt; ++i) {
       const RowStat t = target_stat(a, r.t0 + base + i, c, lane);
       if (lane == i) ts = t;
+      if (a.want_rank) {
+        const int rk = 1 + warp_row_count(a, r.t0 + base + i, lane);
+        if (lane == i) rank = rk;
+      }
       if (sample && a.stream_draft) {
         const RowStat d = draft_stat(a, r.d0 + base + i, c, lane);
         if (lane == i) ds = d;
@@ -211,8 +250,15 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
         const char *trow = a.target + (long long)(r.t0 + i) * a.t_row_bytes;
         pd = ex2((load_elem(trow, a.tdt, d) - ts.m) * c) / ts.S;
         qd = draft_prob_at(a, r.d0 + i, d, c, ds);
-        const float acc = qd <= pd ? 1.f : pd / qd;
-        rej = !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
+        if (a.rule == SPEC_RULE_CACTUS) {
+          const float g = fminf(pd + sqrtf(2.f * a.alpha * pd * (1.f - pd)), 1.f);
+          const float acc = qd <= g ? 1.f : g / qd;
+          const bool guard = (a.max_rank > 0 && rank > a.max_rank) || pd < a.min_prob;
+          rej = guard || !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
+        } else {
+          const float acc = qd <= pd ? 1.f : pd / qd;
+          rej = !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
+        }
       } else {
         pd = 0.f;
         qd = 0.f;
@@ -222,6 +268,7 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
         a.out_pq[2LL * (r.d0 + i)] = pd;
         a.out_pq[2LL * (r.d0 + i) + 1] = qd;
       }
+      if (a.out_rank) a.out_rank[r.d0 + i] = rank;
     }
     const unsigned bal = __ballot_sync(0xffffffffu, rej);
     if (n == K && bal) n = base + __ffs(bal) - 1;
@@ -651,7 +698,7 @@ using namespace sv;
 
 extern "C" size_t spec_verify_linear_workspace(int B, int max_k, int V, int rule) {
   if (B < 0 || max_k < 0 || max_k > SPEC_MAX_K || V <= 0 || V > SPEC_MAX_V) return 0;
-  if (rule < 0 || rule > 2) return 0;
+  if (rule < SPEC_RULE_STRICT || rule > SPEC_RULE_CACTUS) return 0;
   return linear_layout(B, max_k, V, rule).total;
 }
 
@@ -662,13 +709,32 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
                                   uint64_t seed, int rule, int32_t *out_tokens,
                                   int32_t *out_accepted, float *out_pq, void *workspace,
                                   size_t ws_bytes, spec_stream_t stream) {
+  return spec_verify_linear_ext(target, tdt, draft, ddt, dk, draft_idx, draft_tokens, cu_draft,
+                                temperature, B, V, max_k, seed, rule, nullptr, out_tokens,
+                                out_accepted, out_pq, workspace, ws_bytes, stream);
+}
+
+extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *draft, int ddt,
+                                      int dk, const int32_t *draft_idx,
+                                      const int32_t *draft_tokens, const int32_t *cu_draft,
+                                      const float *temperature, int B, int V, int max_k,
+                                      uint64_t seed, int rule, const spec_linear_ext *ext,
+                                      int32_t *out_tokens, int32_t *out_accepted,
+                                      float *out_pq, void *workspace, size_t ws_bytes,
+                                      spec_stream_t stream) {
   if (B < 0 || V <= 0 || V > SPEC_MAX_V || max_k < 0) return SPEC_ERR_INVALID_ARG;
   if (max_k > SPEC_MAX_K) return SPEC_ERR_UNSUPPORTED;
   if ((tdt != SPEC_F32 && tdt != SPEC_BF16) || (ddt != SPEC_F32 && ddt != SPEC_BF16))
     return SPEC_ERR_INVALID_ARG;
   if (dk < SPEC_DRAFT_LOGITS || dk > SPEC_DRAFT_SPARSE128) return SPEC_ERR_INVALID_ARG;
-  if (rule < SPEC_RULE_STRICT || rule > SPEC_RULE_STRICT_TOP128) return SPEC_ERR_INVALID_ARG;
+  if (rule < SPEC_RULE_STRICT || rule > SPEC_RULE_CACTUS) return SPEC_ERR_INVALID_ARG;
   if (rule == SPEC_RULE_STRICT_TOP128 && dk != SPEC_DRAFT_LOGITS) return SPEC_ERR_INVALID_ARG;
+  if (rule == SPEC_RULE_CACTUS && ext == nullptr) return SPEC_ERR_INVALID_ARG;
+  if (ext != nullptr &&
+      (!(ext->alpha >= 0.f) || !isfinite(ext->alpha) || ext->max_rank < 0 ||
+       !(ext->min_prob >= 0.f) || !isfinite(ext->min_prob) || ext->reserved != 0 ||
+       !aligned(ext->out_rank, 4)))
+    return SPEC_ERR_INVALID_ARG;
   if (dk == SPEC_DRAFT_SPARSE128 && (ddt != SPEC_F32 || draft_idx == nullptr || draft == nullptr))
     return SPEC_ERR_INVALID_ARG;
   if (B > 0 && (target == nullptr || draft_tokens == nullptr || cu_draft == nullptr ||
@@ -718,6 +784,12 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
   a.rt_max = B * (max_k + 1);
   a.sparse = dk == SPEC_DRAFT_SPARSE128 || rule == SPEC_RULE_STRICT_TOP128;
   a.stream_draft = dk == SPEC_DRAFT_LOGITS && rule != SPEC_RULE_STRICT_TOP128;
+  a.alpha = ext ? ext->alpha : 0.f;
+  a.min_prob = ext ? ext->min_prob : 0.f;
+  a.max_rank = ext ? ext->max_rank : 0;
+  a.out_rank = ext ? ext->out_rank : nullptr;
+  a.want_rank = a.out_rank != nullptr || (rule == SPEC_RULE_CACTUS && a.max_rank > 0);
+  a.rank_thr = reinterpret_cast<float *>(ws + L.rank_thr);
   if (dk == SPEC_DRAFT_SPARSE128) {
     a.draft_idx = draft_idx;
     a.sparse_prob = static_cast<const float *>(draft);
@@ -753,6 +825,7 @@ extern "C" int spec_verify_linear(const void *target, int tdt, const void *draft
   rp.list = a.list;
   rp.hdr = a.hdr;
   rp.part = a.part;
+  rp.rank_thr = a.want_rank ? a.rank_thr : nullptr;
   rp.residual = 0;
   rp.jobs = nullptr;
   rp.req = nullptr;

@@ -21,6 +21,12 @@
 
 namespace sv {
 
+// With RANK, the consumers of a target row also count the logits strictly
+// above the row's threshold (the draft token's own logit): the draft token's
+// target rank minus one ("Acceptance Is Not Speed", §6 rule 1, the
+// low-support guard on target rank), one packed bf16 compare per two
+// elements.
+//
 // Stage metadata, two 16-byte records read with one shared load each:
 //   m0 = {slot (-1: no more work), chunk, e_first, flags}
 //   m1 = {c (float bits), row, head_e, tail_e}
@@ -31,6 +37,7 @@ struct RowPassSmem {
   uint64_t empty[NSTAGE];
   int4 m0[NSTAGE];
   int4 m1[NSTAGE];
+  float thr[NSTAGE];   // rank threshold of the stage's row (+inf: none)
   int abort;
 };
 
@@ -47,6 +54,8 @@ struct RunState {
   float m;
   f32x2 S2;
   int idx;
+  int cnt;        // rank count (generic path)
+  uint32_t cnt2;  // rank count, two 16-bit lanes (packed bf16 path)
 };
 
 __device__ __forceinline__ void rescale(RunState &st, float m_new, float c) {
@@ -55,7 +64,9 @@ __device__ __forceinline__ void rescale(RunState &st, float m_new, float c) {
   st.m = m_new;
 }
 
-__device__ __forceinline__ void scalar_update(float x, int e, float c, RunState &st) {
+__device__ __forceinline__ void scalar_update(float x, int e, float c, RunState &st,
+                                              float thr) {
+  st.cnt += x > thr;
   if (x > st.m) {
     if (c != 0.f) rescale(st, x, c);
     st.m = x;
@@ -68,7 +79,8 @@ __device__ __forceinline__ void scalar_update(float x, int e, float c, RunState 
 
 // Generic path: one 16-byte vector (partial stages and fp32 rows).
 template <bool SOFTMAX, bool BF16>
-__device__ __forceinline__ void consume_vec(const uint4 w, int e, float c, RunState &st) {
+__device__ __forceinline__ void consume_vec(const uint4 w, int e, float c, RunState &st,
+                                            float thr) {
   constexpr int N = BF16 ? 8 : 4;
   float x[N];
   if (BF16) {
@@ -81,6 +93,8 @@ __device__ __forceinline__ void consume_vec(const uint4 w, int e, float c, RunSt
   float vm = x[0];
 #pragma unroll
   for (int k = 1; k < N; ++k) vm = fmaxf(vm, x[k]);
+#pragma unroll
+  for (int k = 0; k < N; ++k) st.cnt += x[k] > thr;
   if (vm > st.m) {
     int j = N - 1;
 #pragma unroll
@@ -124,12 +138,18 @@ __device__ __forceinline__ int first_index_of(const uint4 (&v)[VEC_PER_THREAD], 
 // packed bf16 compares and is checked once; exponents are formed with
 // mixed-precision subtracts and packed multiplies, one 2^x per element, and
 // the 32 terms are summed as a packed pairwise tree.
-template <bool SOFTMAX>
+template <bool SOFTMAX, bool RANK>
 __device__ __forceinline__ void consume_full_bf16(const unsigned char *buf, int ctid, int e_first,
-                                                  float c, RunState &st) {
+                                                  float c, RunState &st, uint32_t thr2) {
   uint4 v[VEC_PER_THREAD];
 #pragma unroll
   for (int k = 0; k < VEC_PER_THREAD; ++k) v[k] = lds128(buf + 16 * (ctid + NCT * k));
+  if (RANK) {
+#pragma unroll
+    for (int k = 0; k < VEC_PER_THREAD; ++k)
+      st.cnt2 += (bgt2(v[k].x, thr2) & 0x00010001u) + (bgt2(v[k].y, thr2) & 0x00010001u) +
+                 (bgt2(v[k].z, thr2) & 0x00010001u) + (bgt2(v[k].w, thr2) & 0x00010001u);
+  }
   uint32_t a[2 * VEC_PER_THREAD];
 #pragma unroll
   for (int k = 0; k < VEC_PER_THREAD; ++k) {
@@ -222,7 +242,12 @@ __device__ __forceinline__ float consume_res_partial(const unsigned char *buf, i
   return s;
 }
 
-__global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const RowPassArgs a) {
+// The rank count needs a few more registers than 6 CTAs per SM leave.
+constexpr int RS_RANK_CTAS_PER_SM = 4;
+
+template <bool RANK>
+__global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM)
+    k_row_pass(const RowPassArgs a) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ RowPassSmem sh;
   unsigned char *stage_buf = dsmem;
@@ -288,6 +313,7 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
       const int chunk = (int)(item % a.nch_max);
       const RowTask t = a.list[entry];
       const int w = t.which;
+      const float thr = RANK && w == 0 && t.slot >= 0 ? a.rank_thr[t.slot] : INFINITY;
       const long long rbytes = w ? a.row_bytes[1] : a.row_bytes[0];
       if (t.slot >= 0 && chunk < (w ? a.nch[1] : a.nch[0])) {
         const int esz = dtype_size(w ? a.dtype[1] : a.dtype[0]);
@@ -312,6 +338,7 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
           sh.m0[s] = make_int4(t.slot, chunk, (int)((off - row0) / esz), flags);
           sh.m1[s] = make_int4(__float_as_int(t.c), t.row, (int)((cb0 - row0) / esz),
                                (int)((A1 - row0) / esz));
+          if (RANK) sh.thr[s] = thr;
           if (nb > 0) {
             mbar_arrive_tx(&sh.full[s], nb);
             bulk_g2s(stage_buf + (size_t)s * TILE_BYTES, (const void *)off, nb, &sh.full[s]);
@@ -348,7 +375,7 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
   // -------------------------------------------------------------- consumers
   const int cw = warp - 1;
   const int ctid = threadIdx.x - 32;
-  RunState st{NO_MAX, pk2(0.f, 0.f), 0x7fffffff};
+  RunState st{NO_MAX, pk2(0.f, 0.f), 0x7fffffff, 0, 0u};
   int res_job = -1;
   ResLaw res_law{0.f, 0.f, 0.f, 0.f, 0.f};
   for (long long it = 0;; ++it) {
@@ -387,18 +414,27 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
     const int dt = which ? a.dtype[1] : a.dtype[0];
     const bool bf16 = dt == SPEC_BF16;
     const unsigned char *buf = stage_buf + (size_t)s * TILE_BYTES;
+    // rank threshold; +inf counts nothing (logits are finite or -inf)
+    const float thr = RANK ? sh.thr[s] : INFINITY;
     if (bf16 && nvec == FULL_NVEC) {
-      if (c != 0.f) consume_full_bf16<true>(buf, ctid, e_first, c, st);
-      else consume_full_bf16<false>(buf, ctid, e_first, c, st);
+      if (RANK && thr != INFINITY) {
+        const uint32_t h = __float_as_uint(thr) >> 16;   // exact: a bf16 logit
+        const uint32_t thr2 = h | (h << 16);
+        if (c != 0.f) consume_full_bf16<true, true>(buf, ctid, e_first, c, st, thr2);
+        else consume_full_bf16<false, true>(buf, ctid, e_first, c, st, thr2);
+      } else {
+        if (c != 0.f) consume_full_bf16<true, false>(buf, ctid, e_first, c, st, 0u);
+        else consume_full_bf16<false, false>(buf, ctid, e_first, c, st, 0u);
+      }
     } else if (bf16) {
       for (int v = ctid; v < nvec; v += NCT) {
-        if (c != 0.f) consume_vec<true, true>(lds128(buf + 16 * v), e_first + 8 * v, c, st);
-        else consume_vec<false, true>(lds128(buf + 16 * v), e_first + 8 * v, c, st);
+        if (c != 0.f) consume_vec<true, true>(lds128(buf + 16 * v), e_first + 8 * v, c, st, thr);
+        else consume_vec<false, true>(lds128(buf + 16 * v), e_first + 8 * v, c, st, thr);
       }
     } else {
       for (int v = ctid; v < nvec; v += NCT) {
-        if (c != 0.f) consume_vec<true, false>(lds128(buf + 16 * v), e_first + 4 * v, c, st);
-        else consume_vec<false, false>(lds128(buf + 16 * v), e_first + 4 * v, c, st);
+        if (c != 0.f) consume_vec<true, false>(lds128(buf + 16 * v), e_first + 4 * v, c, st, thr);
+        else consume_vec<false, false>(lds128(buf + 16 * v), e_first + 4 * v, c, st, thr);
       }
     }
     __syncwarp();
@@ -408,12 +444,18 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
         const int head_n = (m0.w >> 16) & 0xf, tail_n = (m0.w >> 20) & 0xf;
         const char *row = (which ? a.base[1] : a.base[0]) +
                           (long long)m1.y * (which ? a.row_bytes[1] : a.row_bytes[0]);
-        if (lane < head_n) scalar_update(load_elem(row, dt, m1.z + lane), m1.z + lane, c, st);
+        if (lane < head_n)
+          scalar_update(load_elem(row, dt, m1.z + lane), m1.z + lane, c, st, thr);
         if (lane >= 16 && lane - 16 < tail_n)
-          scalar_update(load_elem(row, dt, m1.w + lane - 16), m1.w + lane - 16, c, st);
+          scalar_update(load_elem(row, dt, m1.w + lane - 16), m1.w + lane - 16, c, st, thr);
       }
       float m = st.m, S = lo2(st.S2) + hi2(st.S2);
       int idx = st.idx;
+      int cnt = RANK ? st.cnt + (int)(st.cnt2 & 0xffffu) + (int)(st.cnt2 >> 16) : 0;
+      if (RANK) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -426,10 +468,10 @@ __global__ void __launch_bounds__(RS_THREADS, RS_CTAS_PER_SM) k_row_pass(const R
         p.m = m;
         p.S = S;
         p.idx = idx;
-        p.pad = 0;
+        p.cnt = cnt;
         a.part[((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS + cw] = p;
       }
-      st = RunState{NO_MAX, pk2(0.f, 0.f), 0x7fffffff};
+      st = RunState{NO_MAX, pk2(0.f, 0.f), 0x7fffffff, 0, 0u};
     }
   }
 }
@@ -463,13 +505,15 @@ int launch_row_pass(const RowPassArgs &a, cudaStream_t stream) {
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
   const size_t smem = (size_t)NSTAGE * TILE_BYTES;
-  if (cudaFuncSetAttribute(k_row_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const bool rank = a.rank_thr != nullptr && !a.residual;
+  auto kern = rank ? k_row_pass<true> : k_row_pass<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
     return SPEC_ERR_CUDA;
   cudaEvent_t before = prof_before, after = prof_after;
   prof_before = prof_after = nullptr;
   if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  k_row_pass<<<RS_CTAS_PER_SM * sms, RS_THREADS, smem, stream>>>(a);
+  kern<<<(rank ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM) * sms, RS_THREADS, smem, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;

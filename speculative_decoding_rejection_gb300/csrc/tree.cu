@@ -21,14 +21,25 @@
 // scalars. A token rejected at step k has q_k > p_k, so p_{k+1} is exactly 0
 // there and stays 0; the chain can therefore use q(y) s_j for every y without
 // testing membership of the excluded set.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
+namespace cg = cooperative_groups;
+
 namespace sv {
 
-constexpr int WALK_THREADS = 1024;
+// The walk of one tree runs on a cluster of WALK_CLUSTER CTAs. Every CTA
+// repeats the walk's scalar decisions (children, node statistics, coins) on
+// identical data; each full-row pass is split into contiguous vocabulary
+// slices, one per CTA, whose totals are exchanged through distributed shared
+// memory. Only the CTA whose slice holds the drawn mass searches it.
+constexpr int WALK_THREADS = 256;
+constexpr int WALK_CLUSTER = 8;
 constexpr int WALK_TILE = WALK_THREADS * SAMPLE_EPT;   // elements per tile of a walk pass
 constexpr int MAX_WALK_TILES = (SPEC_MAX_V + WALK_TILE - 1) / WALK_TILE;
+constexpr int MAX_SLICE_TILES = (MAX_WALK_TILES + WALK_CLUSTER - 1) / WALK_CLUSTER;
 
 struct TreeInfo {
   int base;   // first node row
@@ -155,14 +166,16 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
 
 // ------------------------------------------------------------------- walk
 struct WalkSmem {
-  float tsum[MAX_WALK_TILES];
-  float wsum[64 * 32];                   // per-warp tile sums of one batch
+  float tsum[MAX_SLICE_TILES];           // tile totals of this CTA's slice
+  float wsum[64 * (WALK_THREADS / 32)];  // per-warp tile sums of one batch
+  float zr[2];                           // this slice's total, by pass parity
+  float zall[WALK_CLUSTER];              // every slice's total of the last pass
   float scratch[33];
   int kids[SPEC_MAX_TREE_BRANCH];
   float s[SPEC_MAX_TREE_BRANCH + 1];     // 1 / (1 - q(E_j))
   float rinv[SPEC_MAX_TREE_BRANCH + 1];  // 1 / Z_j
   int skip[SPEC_MAX_TREE_BRANCH + 1];    // Z_j == 0: p_{j+1} = p_j
-  int nk, jstar, xmin, xlast, done, accepted_child;
+  int nk, jstar, xmin, xlast, rstar, accepted_child, par, ok, go;
   float carry, target, Z;
 };
 
@@ -171,6 +184,13 @@ struct NodeLaw {        // p(y) = 2^((zt - mt) c) / St, q(y) likewise or given
   bool tvec, dvec;
   float mt, invSt, md, invSd;
 };
+
+struct Slice { int j0, j1; };   // tiles [j0, j1) of this CTA
+
+__device__ __forceinline__ Slice my_slice(int V, int rank) {
+  const int nt = (V + WALK_TILE - 1) / WALK_TILE;
+  return Slice{rank * nt / WALK_CLUSTER, (rank + 1) * nt / WALK_CLUSTER};
+}
 
 // p_L(y) and the residual max(0, p_L - q_L) (or p_L itself) from the raw
 // p(y), q(y) through the chain of normalisers.
@@ -202,17 +222,16 @@ __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkS
   }
 }
 
-// One pass over the node's rows: tile totals of the level-L weights into
-// sh.tsum and their sum into sh.Z (ascending tile order). Tiles are summed
-// per warp and combined once per batch of up to 64 tiles.
+// One pass over the node's rows: this CTA's tile totals of the level-L
+// weights into sh.tsum, the slice totals of the whole cluster into sh.zall
+// and their sum (ascending slice order, the same in every CTA) into sh.Z.
 template <int DK>
 __device__ void weight_pass(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, float c, int L,
-                            bool residual) {
-  const int ntiles = (a.V + WALK_TILE - 1) / WALK_TILE;
+                            bool residual, const Slice sl, cg::cluster_group &cluster) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float w[SAMPLE_EPT];
-  for (int j0 = 0; j0 < ntiles; j0 += 64) {
-    const int j1 = min(ntiles, j0 + 64);
+  for (int j0 = sl.j0; j0 < sl.j1; j0 += 64) {
+    const int j1 = min(sl.j1, j0 + 64);
 #pragma unroll 2
     for (int j = j0; j < j1; ++j) {
       tile_weights_tree<DK>(a, sh, nl, c, L, residual, j, w);
@@ -221,43 +240,79 @@ __device__ void weight_pass(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, 
       for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) sh.wsum[(j - j0) * 32 + warp] = s;
+      if (lane == 0) sh.wsum[(j - j0) * (WALK_THREADS / 32) + warp] = s;
     }
     __syncthreads();
     if (threadIdx.x < j1 - j0) {
       float t = 0.f;
-      for (int q = 0; q < WALK_THREADS / 32; ++q) t += sh.wsum[threadIdx.x * 32 + q];
-      sh.tsum[j0 + threadIdx.x] = t;
+      for (int q = 0; q < WALK_THREADS / 32; ++q)
+        t += sh.wsum[threadIdx.x * (WALK_THREADS / 32) + q];
+      sh.tsum[j0 + threadIdx.x - sl.j0] = t;
     }
     __syncthreads();
   }
+  const int par = sh.par;
+  if (threadIdx.x == 0) {
+    float Zr = 0.f;
+    for (int j = sl.j0; j < sl.j1; ++j) Zr += sh.tsum[j - sl.j0];
+    sh.zr[par] = Zr;
+  }
+  cluster.sync();   // every slice total written (slots alternate by parity)
   if (threadIdx.x == 0) {
     float Z = 0.f;
-    for (int j = 0; j < ntiles; ++j) Z += sh.tsum[j];
+    for (int r = 0; r < WALK_CLUSTER; ++r) {
+      const float zr = *cluster.map_shared_rank(&sh.zr[par], r);
+      sh.zall[r] = zr;
+      Z += zr;
+    }
     sh.Z = Z;
+    sh.par = par ^ 1;
   }
   __syncthreads();
 }
 
-// Inverse-CDF draw at u from the level-L weights whose tile totals are in
-// sh.tsum (smallest y with u*Z < C_y; the last positive weight if rounding
-// leaves none).
+// Inverse-CDF draw at u from the level-L weights of the last pass: the slice
+// holding u*Z is found from the slice totals, then its tile, then the element
+// (smallest y with u*Z < C_y; the last positive weight if rounding leaves
+// none). Returns the token in the CTA that owns it, -1 in the others.
 template <int DK>
 __device__ int weight_draw(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, float c, int L,
-                           bool residual, float u) {
-  const int ntiles = (a.V + WALK_TILE - 1) / WALK_TILE;
+                           bool residual, float u, const Slice sl, int rank) {
   if (threadIdx.x == 0) {
     sh.target = u * sh.Z;
     float carry = 0.f;
+    int rs = -1;
+    for (int r = 0; r < WALK_CLUSTER; ++r) {
+      const float nc = carry + sh.zall[r];
+      if (nc > sh.target) { rs = r; break; }
+      carry = nc;
+    }
+    if (rs < 0) {
+      carry = 0.f;
+      for (int r = 0; r < WALK_CLUSTER; ++r)
+        if (sh.zall[r] > 0.f) rs = r;
+      for (int r = 0; r < rs; ++r) carry += sh.zall[r];
+    }
+    sh.rstar = rs;
+    sh.carry = carry;
+  }
+  __syncthreads();
+  // with no mass anywhere, rank 0 reports it
+  if (sh.rstar != rank && !(sh.rstar < 0 && rank == 0)) return -1;
+  if (threadIdx.x == 0) {
+    float carry = sh.carry;
     int js = -1;
-    for (int j = 0; j < ntiles; ++j) {
-      const float nc = carry + sh.tsum[j];
+    for (int j = sl.j0; j < sl.j1; ++j) {
+      const float nc = carry + sh.tsum[j - sl.j0];
       if (nc > sh.target) { js = j; break; }
       carry = nc;
     }
-    if (js < 0)
-      for (int j = ntiles - 1; j >= 0 && js < 0; --j)
-        if (sh.tsum[j] > 0.f) js = j;
+    if (js < 0) {
+      carry = sh.carry;
+      for (int j = sl.j0; j < sl.j1; ++j)
+        if (sh.tsum[j - sl.j0] > 0.f) js = j;
+      for (int j = sl.j0; j < js; ++j) carry += sh.tsum[j - sl.j0];
+    }
     sh.jstar = js;
     sh.carry = carry;
     sh.xmin = 0x7fffffff;
@@ -286,7 +341,8 @@ __device__ int weight_draw(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, f
     if (lastpos >= 0) atomicMax(&sh.xlast, lastpos);
   }
   __syncthreads();
-  const int x = sh.xmin != 0x7fffffff ? sh.xmin : sh.xlast;
+  int x = sh.xmin != 0x7fffffff ? sh.xmin : sh.xlast;
+  if (x < 0) x = 0x7fffffff;   // owner found no mass: reported as invalid below
   __syncthreads();
   return x;
 }
@@ -296,23 +352,24 @@ __device__ __forceinline__ RowStat node_stat(const TreeArgs &a, int slot, int nc
                        c);
 }
 
+__device__ __forceinline__ void write_final(const TreeArgs &a, int b, int depth, int x) {
+  if (x == 0x7fffffff) {
+    set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);   // a row without mass
+    x = -1;
+  }
+  a.out_tokens[(long long)b * (a.max_depth + 1) + depth] = x;
+}
+
+// The walk of tree b on the CTA of cluster rank `rank`. Every exit of this
+// function is followed by the kernel's closing cluster barrier, so no CTA
+// leaves while another may still read its slice totals.
 template <int DK>
-__global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
-  __shared__ WalkSmem sh;
-  const int b = blockIdx.x;
-  const TreeInfo t = a.tree[b];
+__device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const TreeInfo &t,
+                                          int b, int rank, cg::cluster_group &cluster) {
   const int W = a.max_depth + 1;
+  const Slice sl = my_slice(a.V, rank);
   int32_t *out = a.out_tokens + (long long)b * W;
   int32_t *path = a.out_path ? a.out_path + (long long)b * W : nullptr;
-  for (int j = threadIdx.x; j < W; j += blockDim.x) {
-    out[j] = -1;
-    if (path) path[j] = -1;
-  }
-  if (t.mode == MODE_SKIP || *(volatile int *)&a.hdr->status != SPEC_OK) {
-    if (threadIdx.x == 0) a.out_accepted[b] = -1;
-    return;
-  }
-  __syncthreads();
   const float c = t.c;
   int v = 0, depth = 0;
   while (true) {
@@ -345,7 +402,7 @@ __global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
       const int ac = sh.accepted_child;
       __syncthreads();
       if (ac >= 0 && depth < a.max_depth) {
-        if (threadIdx.x == 0) {
+        if (rank == 0 && threadIdx.x == 0) {
           out[depth] = a.node_token[t.base + ac];
           if (path) path[depth] = ac;
         }
@@ -353,7 +410,7 @@ __global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
         ++depth;
         continue;
       }
-      if (threadIdx.x == 0) {
+      if (rank == 0 && threadIdx.x == 0) {
         out[depth] = ts.idx;
         a.out_accepted[b] = depth;
       }
@@ -369,13 +426,12 @@ __global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
     nl.md = 0.f;
     nl.invSd = 0.f;
     if (nk == 0) {  // accepted leaf (or a bare root): bonus draw from p_v
-      weight_pass<DK>(a, sh, nl, c, 0, false);
+      weight_pass<DK>(a, sh, nl, c, 0, false, sl, cluster);
       const int x = weight_draw<DK>(a, sh, nl, c, 0, false,
-                                    uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 2));
-      if (threadIdx.x == 0) {
-        out[depth] = x;
-        a.out_accepted[b] = depth;
-      }
+                                    uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 2), sl,
+                                    rank);
+      if (x != -1 && threadIdx.x == 0) write_final(a, b, depth, x);
+      if (rank == 0 && threadIdx.x == 0) a.out_accepted[b] = depth;
       return;
     }
     nl.drow = a.draft + (long long)row * a.d_row_bytes;
@@ -393,7 +449,6 @@ __global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
     __syncthreads();
     float qE = 0.f;
     int accepted = -1, L = 0;
-    bool exhausted = false;
     for (int j = 0; j < nk; ++j) {
       // coin of child j at its token x, with p_j(x) and q_j(x) from the chain
       if (threadIdx.x == 0) {
@@ -420,7 +475,7 @@ __global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
       }
       // rejection: Z_j of the residual at level j (tile totals kept for a
       // possible final draw), then the next draft normaliser
-      weight_pass<DK>(a, sh, nl, c, j, true);
+      weight_pass<DK>(a, sh, nl, c, j, true, sl, cluster);
       L = j;
       qE += qx;
       const float left = 1.f - qE;
@@ -430,13 +485,10 @@ __global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
         sh.s[j + 1] = left > 0.f ? 1.f / left : 0.f;
       }
       __syncthreads();
-      if (!(left > 0.f)) {   // every draft token used up
-        exhausted = true;
-        break;
-      }
+      if (!(left > 0.f)) break;   // every draft token used up
     }
     if (accepted >= 0 && depth < a.max_depth) {
-      if (threadIdx.x == 0) {
+      if (rank == 0 && threadIdx.x == 0) {
         out[depth] = a.node_token[t.base + accepted];
         if (path) path[depth] = accepted;
       }
@@ -444,22 +496,54 @@ __global__ void __launch_bounds__(WALK_THREADS) k_tree_walk(const TreeArgs a) {
       ++depth;
       continue;
     }
-    (void)exhausted;
     // all tested children rejected: draw from p_{L+1} = norm(residual at L),
     // or from p_L itself when that residual had no mass
     bool residual = true;
     if (sh.skip[L]) {
       residual = false;
-      weight_pass<DK>(a, sh, nl, c, L, false);
+      weight_pass<DK>(a, sh, nl, c, L, false, sl, cluster);
     }
     const int x = weight_draw<DK>(a, sh, nl, c, L, residual,
-                                  uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 1));
-    if (threadIdx.x == 0) {
-      out[depth] = x;
-      a.out_accepted[b] = depth;
-    }
+                                  uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 1), sl, rank);
+    if (x != -1 && threadIdx.x == 0) write_final(a, b, depth, x);
+    if (rank == 0 && threadIdx.x == 0) a.out_accepted[b] = depth;
     return;
   }
+}
+
+template <int DK>
+__global__ void __cluster_dims__(WALK_CLUSTER, 1, 1) __launch_bounds__(WALK_THREADS, 2)
+    k_tree_walk(const TreeArgs a) {
+  __shared__ WalkSmem sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / WALK_CLUSTER;
+  const TreeInfo t = a.tree[b];
+  const int W = a.max_depth + 1;
+  if (rank == 0)
+    for (int j = threadIdx.x; j < W; j += blockDim.x) {
+      a.out_tokens[(long long)b * W + j] = -1;
+      if (a.out_path) a.out_path[(long long)b * W + j] = -1;
+    }
+  // Whether to walk is decided once for the whole cluster: the status word
+  // can change under a running walk (another tree without mass), so each CTA
+  // reads it and the CTAs agree on the conjunction.
+  if (threadIdx.x == 0) {
+    sh.ok = t.mode != MODE_SKIP && *(volatile int *)&a.hdr->status == SPEC_OK;
+    sh.par = 0;
+  }
+  cluster.sync();   // also orders the -1 fill before every later token write
+  if (threadIdx.x == 0) {
+    int all = 1;
+    for (int r = 0; r < WALK_CLUSTER; ++r) all &= *cluster.map_shared_rank(&sh.ok, r);
+    sh.go = all;
+  }
+  __syncthreads();
+  if (sh.go)
+    walk_tree<DK>(a, sh, t, b, rank, cluster);
+  else if (rank == 0 && threadIdx.x == 0)
+    a.out_accepted[b] = -1;
+  cluster.sync();
 }
 
 }  // namespace sv
@@ -534,6 +618,7 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   k_setup_tree<<<B, SETUP_THREADS, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   RowPassArgs rp;
+  rp.rank_thr = nullptr;
   rp.base[0] = a.target;
   rp.base[1] = a.draft;
   rp.row_bytes[0] = a.t_row_bytes;
@@ -555,8 +640,8 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   const int rc = launch_row_pass(rp, st);
   if (rc != SPEC_OK) return rc;
   if (dk == SPEC_DRAFT_PROBS)
-    k_tree_walk<SPEC_DRAFT_PROBS><<<B, WALK_THREADS, 0, st>>>(a);
+    k_tree_walk<SPEC_DRAFT_PROBS><<<B * WALK_CLUSTER, WALK_THREADS, 0, st>>>(a);
   else
-    k_tree_walk<SPEC_DRAFT_LOGITS><<<B, WALK_THREADS, 0, st>>>(a);
+    k_tree_walk<SPEC_DRAFT_LOGITS><<<B * WALK_CLUSTER, WALK_THREADS, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -15,25 +15,37 @@ PROB_ATOL = 1e-30
 
 
 def gpu_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, draft=None,
-               draft_idx=None):
+               draft_idx=None, ext=None):
+    """Runs the CUDA verifier; `ext` (a dict of alpha / max_rank / min_prob)
+    goes through spec_verify_linear_ext, which also returns target ranks."""
     draft = lb.draft if draft is None else draft
-    tokens, acc, pq, ws = sv.spec_verify_linear(
-        lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
-        max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx, want_pq=True)
+    if ext is None:
+        tokens, acc, pq, ws = sv.spec_verify_linear(
+            lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
+            max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx, want_pq=True)
+        rank = None
+    else:
+        tokens, acc, pq, rank, ws = sv.spec_verify_linear_ext(
+            lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
+            max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx,
+            want_pq=True, want_rank=True, **ext)
     status = sv.spec_get_status(ws)
-    return dict(tokens=tokens.cpu().numpy(), accepted=acc.cpu().numpy(),
-                pq=pq.cpu().numpy().astype(np.float64), status=status)
+    out = dict(tokens=tokens.cpu().numpy(), accepted=acc.cpu().numpy(),
+               pq=pq.cpu().numpy().astype(np.float64), status=status)
+    if rank is not None:
+        out["rank"] = rank.cpu().numpy().astype(np.int64)
+    return out
 
 
 def oracle_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, draft=None,
-                  draft_idx=None, requests=None):
+                  draft_idx=None, requests=None, ext=None):
     draft = lb.draft if draft is None else draft
     host = (lambda t: t.cpu()) if requests is None else (lambda t: t)
     return O.verify_linear(host(lb.target), host(draft), lb.draft_tokens.cpu().numpy(),
                            lb.cu_draft.cpu().numpy(), lb.temperature.cpu().numpy(), lb.seed,
                            rule=rule, draft_kind=draft_kind,
                            draft_idx=None if draft_idx is None else draft_idx.cpu().numpy(),
-                           max_k=lb.max_k, requests=requests)
+                           max_k=lb.max_k, requests=requests, **(ext or {}))
 
 
 def assert_probs_close(g, o, what="probabilities"):
@@ -64,6 +76,10 @@ def assert_linear_parity(gpu, ref, cu_draft, min_compared=1):
     rows = np.asarray(rows, dtype=np.int64)
     if rows.size:
         assert_probs_close(gpu["pq"][rows], ref["pq"][rows], "p(d), q(d)")
+        if "rank" in gpu:   # integer counts: bit-exact
+            bad = gpu["rank"][rows] != ref["rank"][rows]
+            assert not bad.any(), ("rank", rows[bad][:5], gpu["rank"][rows][bad][:5],
+                                   ref["rank"][rows][bad][:5])
     assert n_full >= min_compared
     return n_full, n_flag
 

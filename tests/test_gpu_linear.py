@@ -210,3 +210,63 @@ def test_draft_topk_softmax_edge_cases(dtype, V, T):
     ri, rp = O.draft_topk_softmax(z.cpu(), cu.cpu().numpy(), temp.cpu().numpy())
     assert np.array_equal(idx.cpu().numpy(), ri)
     assert_probs_close(prob.cpu().numpy(), rp, "top-128 probabilities")
+
+
+# ------------------------------------------- relaxed CACTUS rule and ranks
+CACTUS_CASES = [
+    dict(alpha=0.0, max_rank=0, min_prob=0.0),     # the lossless test
+    dict(alpha=0.05, max_rank=0, min_prob=0.0),
+    dict(alpha=0.5, max_rank=10, min_prob=0.10),   # the recommended guard
+    dict(alpha=2.0, max_rank=3, min_prob=0.0),
+    dict(alpha=0.2, max_rank=0, min_prob=0.02),
+]
+
+
+@pytest.mark.parametrize("ext", CACTUS_CASES)
+@pytest.mark.parametrize("dtype,V", [("bf16", 50021), ("f32", 3001), ("bf16", 262144)])
+def test_cactus_rule_and_target_ranks(ext, dtype, V):
+    T = [0.0, 0.3, 0.7, 1.0, 1.4] * 6
+    lb = S.make_linear(2, device=DEV, B=30, K=(0, 6), V=V, dtype=dtype, sigma=0.6, T=T,
+                       input_seed=900 + V)
+    g = gpu_linear(lb, rule=sv.SPEC_RULE_CACTUS, ext=ext)
+    assert g["status"] == sv.SPEC_OK
+    r = oracle_linear(lb, rule=sv.SPEC_RULE_CACTUS, ext=ext)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=20)
+    if ext["alpha"] == 0.0:   # alpha 0, guard off: the strict rule bit for bit
+        s = gpu_linear(lb)
+        assert np.array_equal(s["tokens"], g["tokens"])
+
+
+def test_target_ranks_under_the_strict_rule_with_ties():
+    """Ranks through the extended entry point with the lossless rule; logits
+    rounded to a coarse grid so many tokens tie with the draft token."""
+    lb = S.make_linear(1, device=DEV, B=16, K=5, V=70001, input_seed=21)
+    lb.target = (torch.round(lb.target.float() * 4) / 4).to(lb.target.dtype).contiguous()
+    g = gpu_linear(lb, ext=dict(alpha=0.0, max_rank=0, min_prob=0.0))
+    r = oracle_linear(lb)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=12)
+    s = gpu_linear(lb)
+    assert np.array_equal(s["tokens"], g["tokens"])
+
+
+def test_cactus_full_size_workload5_sampled():
+    lb = S.make_linear(5, device=DEV)
+    ext = dict(alpha=0.5, max_rank=10, min_prob=0.10)
+    g = gpu_linear(lb, rule=sv.SPEC_RULE_CACTUS, ext=ext)
+    assert g["status"] == sv.SPEC_OK
+    req = sample_requests(lb.B, 16, seed=55)
+    r = oracle_linear(lb, rule=sv.SPEC_RULE_CACTUS, requests=req, ext=ext)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=13)
+
+
+def test_cactus_argument_errors():
+    lb = S.make_linear(1, device=DEV, B=2, K=2, V=64, input_seed=3)
+    with pytest.raises(sv.SpecError):   # the relaxed rule needs its options
+        sv.spec_verify_linear(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
+                              lb.temperature, 1, max_k=lb.max_k, rule=sv.SPEC_RULE_CACTUS)
+    for bad in (dict(alpha=-1.0), dict(alpha=float("nan")), dict(max_rank=-2),
+                dict(min_prob=float("inf"))):
+        with pytest.raises(sv.SpecError):
+            sv.spec_verify_linear_ext(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
+                                      lb.temperature, 1, max_k=lb.max_k,
+                                      rule=sv.SPEC_RULE_CACTUS, **bad)
