@@ -72,6 +72,10 @@ R10 CACTUS rule: accept d iff u < min(1, gamma(d) / q(d)) (accepted outright
 R11 The CACTUS residual is not given (its table is lost): after a rejection
     the final token is drawn from norm(max(0, p - q)) as in the lossless rule
     (p itself when that has no mass), the bonus from p_{K+1}.
+R12 Position-lazy verification reads, per request, target rows 1..n+1 and
+    the draft rows 1..min(n+1, K) a sampling request with dense draft rows
+    needs; it returns the same tokens and counts, and p(d), q(d) and the rank
+    only for the positions it read (NaN and -1 after them).
 """
 from __future__ import annotations
 
@@ -357,6 +361,34 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
         flag_slot[j] = flagged_at
     return dict(tokens=tokens, accepted=accepted, pq=pq, rank=rank,
                 flag_slot=flag_slot, requests=np.asarray(req))
+
+
+def lazy_positions(cu_draft, accepted, requests=None):
+    """R12: for each request, the number of draft positions whose target and
+    draft rows a position-lazy verifier reads: min(n + 1, K). Rows after the
+    first rejection are never used ("Penolakan memendekkan pekerjaan
+    speculative": the proposals after a rejected one are not continuations
+    of the committed prefix)."""
+    cu = np.asarray(cu_draft, dtype=np.int64)
+    req = range(cu.size - 1) if requests is None else requests
+    return np.array([min(int(n) + 1, int(cu[b + 1] - cu[b]))
+                     for b, n in zip(req, accepted)], dtype=np.int64)
+
+
+def lazy_view(result, cu_draft):
+    """The eager result as a position-lazy verifier reports it (R12): p(d),
+    q(d) become NaN and the rank -1 on the draft positions it never read."""
+    cu = np.asarray(cu_draft, dtype=np.int64)
+    out = dict(result)
+    pq = np.array(result["pq"], dtype=np.float64, copy=True)
+    rank = np.array(result["rank"], copy=True)
+    req = result["requests"]
+    for b, m in zip(req, lazy_positions(cu, result["accepted"], req)):
+        d0, d1 = int(cu[b]), int(cu[b + 1])
+        pq[d0 + m:d1] = np.nan
+        rank[d0 + m:d1] = -1
+    out["pq"], out["rank"] = pq, rank
+    return out
 
 
 # --------------------------------------------------------------------------
