@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--cpu-requests", type=int, default=1024,
                     help="requests (or trees) in the oracle's timed sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lazy", action="store_true",
+                    help="linear workloads: position-lazy verification (rows 1..n+1 only)")
     ap.add_argument("--rule", default="default", choices=["default", "cactus"],
                     help="linear workloads: the workload's lossless rule, or the relaxed "
                          "CACTUS rule with the recommended low-support guard")
@@ -171,7 +173,7 @@ class LinearWork:
     # relaxed rule options: the guard the page recommends (p >= 0.10, top 10)
     CACTUS = {"alpha": 0.5, "max_rank": 10, "min_prob": 0.10}
 
-    def __init__(self, cfg, dev, input_seed=None, B=None, rule=None):
+    def __init__(self, cfg, dev, input_seed=None, B=None, rule=None, lazy=False):
         import torch
         import speculative_decoding_rejection_gb300 as sv
         from speculative_decoding_rejection_gb300 import synthetic as S
@@ -182,6 +184,7 @@ class LinearWork:
         self.ext = None
         if rule == "cactus":
             self.rule, self.ext = sv.SPEC_RULE_CACTUS, dict(self.CACTUS)
+        self.lazy = lazy
         K = torch.diff(lb.cu_draft.cpu().long())
         samp = lb.temperature.cpu() >= 0.05
         self.positions = int(K.sum())
@@ -203,6 +206,9 @@ class LinearWork:
         if self.ext is not None:
             self.config["rule"] = ("cactus(alpha={alpha},max_rank={max_rank},"
                                    "min_prob={min_prob})".format(**self.ext))
+        if lazy:
+            self.config["schedule"] = "position-lazy (rows 1..n+1 per request)"
+            self.launches = 2 + 2 * (lb.max_k + 1) + (0 if lb.top128 else 1) + 1
 
     def input_tensors(self):
         lb = self.lb
@@ -212,11 +218,12 @@ class LinearWork:
     def call(self, inputs=None):
         lb = self.lb
         t = inputs or self.input_tensors()
-        if self.ext is not None:
+        if self.ext is not None or self.lazy:
             self.sv.spec_verify_linear_ext(t["target"], t["draft"], t["draft_tokens"],
                                            t["cu_draft"], t["temperature"], lb.seed,
                                            max_k=lb.max_k, rule=self.rule, workspace=self.ws,
-                                           out=self.outs + (None,), **self.ext)
+                                           out=self.outs + (None,), lazy=self.lazy,
+                                           **(self.ext or {}))
             return
         self.sv.spec_verify_linear(t["target"], t["draft"], t["draft_tokens"], t["cu_draft"],
                                    t["temperature"], lb.seed, max_k=lb.max_k, rule=self.rule,
@@ -224,6 +231,21 @@ class LinearWork:
 
     def result_tensors(self):
         return [self.outs[0], self.outs[1]]
+
+    def settle(self):
+        """Position-lazy: the bytes a call reads follow from its outcome
+        (target rows 1..n+1, dense draft rows 1..min(n+1, K) of sampling
+        requests), fixed for fixed inputs and seed."""
+        if not self.lazy:
+            return
+        import torch
+        lb = self.lb
+        n = self.outs[1].cpu().long()
+        K = torch.diff(lb.cu_draft.cpu().long())
+        samp = lb.temperature.cpu() >= 0.05
+        self.tgt_bytes = int((n + 1).sum()) * lb.V * lb.target.element_size()
+        self.drf_bytes = int(torch.minimum(n + 1, K)[samp].sum()) * lb.V * lb.draft.element_size()
+        self.rowpass_bytes = self.tgt_bytes + (0 if lb.top128 else self.drf_bytes)
 
     def mean_accepted(self):
         return float(self.outs[1].float().mean())
@@ -312,10 +334,10 @@ class TreeWork:
         return int(sum(cu[b + 1] - cu[b] - 1 for b in req))
 
 
-def make_work(cfg, dev, input_seed=None, B=None, rule=None):
+def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False):
     if cfg == 4:
         return TreeWork(cfg, dev, input_seed, B)
-    return LinearWork(cfg, dev, input_seed, B, rule)
+    return LinearWork(cfg, dev, input_seed, B, rule, lazy)
 
 
 def cpu_baseline(work, n_units):
@@ -374,11 +396,13 @@ def main():
     dev = torch.device("cuda", local)
     sv.lib()
     work = make_work(args.config, dev, input_seed=S.INPUT_SEED_BASE + args.config + 7919 * rank,
-                     B=args.B, rule=args.rule)
+                     B=args.B, rule=args.rule, lazy=args.lazy)
 
     for _ in range(max(3, args.warmup)):
         work.call()
     torch.cuda.synchronize()
+    if hasattr(work, "settle"):
+        work.settle()
     assert sv.spec_get_status(work.ws) == sv.SPEC_OK
     K = args.steps
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -407,7 +431,8 @@ def main():
     achieved = work.rowpass_bytes / (rp_ms * 1e-3) / 1e9
     traffic = None
     src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "rowpass.cu")
-    if ROWPASS_TRAFFIC["source_sha1"] == sha1(src):
+    lazy = getattr(work, "lazy", False)
+    if ROWPASS_TRAFFIC["source_sha1"] == sha1(src) and not lazy:
         traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
 
     # end to end through the same API: pinned host inputs copied in, the
@@ -468,7 +493,9 @@ def main():
         "algorithmic_bytes_per_step": algo,
         "mean_accepted": work.mean_accepted(),
         "roofline": {
-            "kernel": "k_row_pass", "bound": "hbm", "achieved": achieved, "peak": peak,
+            "kernel": ("k_row_pass rounds with k_lazy_decide (one span)" if lazy
+                       else "k_row_pass"),
+            "bound": "hbm", "achieved": achieved, "peak": peak,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback", "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
             "algorithmic_bytes_per_launch": work.rowpass_bytes, "ms_per_launch": rp_ms,

@@ -161,17 +161,27 @@ int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
  *             SPEC_RULE_CACTUS only.
  *   min_prob  guard: reject d_i when p_i(d_i) < min_prob; 0 = off.
  *             SPEC_RULE_CACTUS only.
+ *   flags     0 or SPEC_EXT_LAZY: position-lazy verification. Position
+ *             i's rows are read only when drafts 1..i-1 were accepted (one
+ *             row pass and one decision per position, max_k + 1 rounds), so a
+ *             request reads rows 1..n+1 only (nalar.dev "Penolakan
+ *             memendekkan pekerjaan speculative": proposals after a rejected
+ *             one are discarded). Same tokens and counts as the eager call;
+ *             out_pq is NaN and out_rank -1 on the positions after n+1, and
+ *             those positions' tokens are not validated. The top-128 rule
+ *             still cuts every draft row.
  *   out_rank  optional device [R_d] int32: the target rank of every draft
  *             token (every request and rule; also after the first
- *             rejection). NULL to skip.
+ *             rejection unless lazy). NULL to skip.
  * The guard and the relaxed coin apply to sampling requests; greedy
  * requests (T < 0.05) keep the greedy rule.
  */
+#define SPEC_EXT_LAZY 1
 typedef struct {
   float alpha;
   int32_t max_rank;
   float min_prob;
-  int32_t reserved;   /* must be 0 */
+  int32_t flags;
   int32_t *out_rank;
 } spec_linear_ext;
 
@@ -299,7 +309,9 @@ int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos,
  * launches its row-statistics pass and `after` immediately after, on the
  * call's stream, then forgets them. Pass NULLs to clear. The pass streams
  * every vocabulary row once and dominates the call's time, so
- * cudaEventElapsedTime(before, after) is that kernel's duration.
+ * cudaEventElapsedTime(before, after) is that kernel's duration. A
+ * position-lazy call (SPEC_EXT_LAZY) records them around all its rounds:
+ * every row pass and every per-round decision.
  */
 int spec_profile_row_pass(void *before, void *after);
 

@@ -33,6 +33,7 @@ SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS, SPEC_DRAFT_SPARSE128 = 0, 1, 2
 SPEC_RULE_STRICT, SPEC_RULE_GREEDY, SPEC_RULE_STRICT_TOP128, SPEC_RULE_CACTUS = 0, 1, 2, 3
 SPEC_TOPK = 128
+SPEC_EXT_LAZY = 1
 
 LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
 HEADER = Path(__file__).resolve().parent.parent / "include" / "specverify.h"
@@ -42,7 +43,7 @@ _vp, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_
 class SpecLinearExt(ctypes.Structure):
     """spec_linear_ext of include/specverify.h."""
     _fields_ = [("alpha", ctypes.c_float), ("max_rank", ctypes.c_int32),
-                ("min_prob", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("min_prob", ctypes.c_float), ("flags", ctypes.c_int32),
                 ("out_rank", ctypes.c_void_p)]
 
 
@@ -186,8 +187,8 @@ def spec_verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed:
 def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, seed: int, *,
                            max_k: int, rule: int = SPEC_RULE_STRICT,
                            draft_kind: int = SPEC_DRAFT_LOGITS, draft_idx=None, alpha=0.0,
-                           max_rank=0, min_prob=0.0, want_pq=False, want_rank=False,
-                           workspace=None, out=None, stream=None):
+                           max_rank=0, min_prob=0.0, lazy=False, want_pq=False,
+                           want_rank=False, workspace=None, out=None, stream=None):
     """spec_verify_linear with the relaxed CACTUS rule's options and target
     ranks.
 
@@ -209,7 +210,8 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
         rank = torch.empty(draft_tokens.numel(), dtype=torch.int32, device=dev) if want_rank else None
     else:
         tokens, accepted, pq, rank = out
-    ext = SpecLinearExt(float(alpha), int(max_rank), float(min_prob), 0, _ptr(rank))
+    ext = SpecLinearExt(float(alpha), int(max_rank), float(min_prob),
+                        SPEC_EXT_LAZY if lazy else 0, _ptr(rank))
     ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
     code = lib().spec_verify_linear_ext(
         _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(draft_idx),

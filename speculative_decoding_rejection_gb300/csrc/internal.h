@@ -46,6 +46,9 @@ struct RowPassArgs {
 
 int num_sms();
 void set_row_pass_events(cudaEvent_t before, cudaEvent_t after);
+// Hands the registered events to a caller that brackets several launches
+// itself (and unregisters them).
+void take_row_pass_events(cudaEvent_t *before, cudaEvent_t *after);
 int launch_row_pass(const RowPassArgs &a, cudaStream_t stream);
 int nchunks(int V, int dtype);
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -20,6 +20,8 @@
 //                 §7 item 3); the rank is counted by the row pass. The
 //                 replacement after a rejection is the lossless residual
 //                 draw (the page's residual for the rule is lost).
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -61,6 +63,8 @@ struct LinearArgs {
   int want_rank;              // the row pass counts ranks
   float *rank_thr;            // [rt_max] draft token's target logit per slot
   int32_t *out_rank;
+  // position-lazy schedule: one row pass + decide per position (round)
+  int lazy, round;
 };
 
 struct LinearLayout {
@@ -80,7 +84,7 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   L.jobs_b = o; o += align256(sizeof(Job) * (size_t)B);
   L.tsum = o;
   o += align256(sizeof(float) * (size_t)B * ((V + SAMPLE_TILE - 1) / SAMPLE_TILE) * RS_CONS_WARPS);
-  L.list = o; o += align256(sizeof(RowTask) * (size_t)L.rows_max);
+  L.list = o; o += align256(sizeof(RowTask) * (size_t)std::max(L.rows_max, 2LL * B));
   L.part = o; o += align256(sizeof(Part) * (size_t)L.rows_max * L.nch_max * RS_CONS_WARPS);
   const size_t tk = rule == SPEC_RULE_STRICT_TOP128 ? (size_t)B * max_k * SPEC_TOPK : 0;
   L.tk_idx = o;  o += align256(sizeof(int32_t) * tk);
@@ -96,17 +100,25 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
 // own entries without a scan; positions no request owns are marked unused.
 // The header was cleared before the launch; an invalid request sets the
 // status word, which makes every later kernel of the call skip its work.
+// Position-lazy: the list holds, per request b, entry b (target row) and
+// entry B + b (draft row) of the first position only.
 __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const int gsize = gridDim.x * blockDim.x;
-  if (gtid == 0) a.hdr->n_list = (int)a.rows_max;
+  if (gtid == 0) a.hdr->n_list = a.lazy ? 2 * a.B : (int)a.rows_max;
   const long long dmax = a.rows_max - a.rt_max;
-  const long long Rd = a.B > 0 ? min(max((long long)a.cu[a.B], 0LL), dmax) : 0;
-  const long long Rt = min(Rd + a.B, (long long)a.rt_max);
-  for (long long p = Rt + gtid; p < a.rt_max; p += gsize) a.list[p].slot = -1;
-  for (long long p = a.rt_max + Rd + gtid; p < a.rows_max; p += gsize) a.list[p].slot = -1;
+  if (!a.lazy) {
+    const long long Rd = a.B > 0 ? min(max((long long)a.cu[a.B], 0LL), dmax) : 0;
+    const long long Rt = min(Rd + a.B, (long long)a.rt_max);
+    for (long long p = Rt + gtid; p < a.rt_max; p += gsize) a.list[p].slot = -1;
+    for (long long p = a.rt_max + Rd + gtid; p < a.rows_max; p += gsize) a.list[p].slot = -1;
+  }
   const int b = gtid;
   if (b >= a.B) return;
+  if (a.lazy) {   // idle until the request validates
+    a.list[b].slot = -1;
+    a.list[a.B + b].slot = -1;
+  }
   ReqInfo r;
   const int K = a.cu[b + 1] - a.cu[b];
   const float T = a.temp[b];
@@ -129,7 +141,15 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
   r.mode = greedy ? MODE_GREEDY : MODE_SAMPLE;
   r.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);
   a.req[b] = r;
-  for (int i = 0; i <= K; ++i) a.list[r.t0 + i] = RowTask{r.t0 + i, r.t0 + i, 0, r.c};
+  const bool drafts = r.mode == MODE_SAMPLE && a.stream_draft;
+  if (a.lazy) {
+    a.list[b] = RowTask{r.t0, r.t0, 0, r.c};
+    a.list[a.B + b] = RowTask{drafts && K > 0 ? a.rt_max + r.d0 : -1, r.d0, 1, r.c};
+  } else {
+    for (int i = 0; i <= K; ++i) a.list[r.t0 + i] = RowTask{r.t0 + i, r.t0 + i, 0, r.c};
+    for (int i = 0; i < K; ++i)
+      a.list[a.rt_max + r.d0 + i] = RowTask{drafts ? a.rt_max + r.d0 + i : -1, r.d0 + i, 1, r.c};
+  }
   if (a.want_rank) {   // threshold of the rank count: the draft token's target logit
     for (int i = 0; i < K; ++i) {
       const int d = a.tokens[r.d0 + i];
@@ -140,9 +160,6 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
     }
     a.rank_thr[r.t0 + K] = INFINITY;
   }
-  const bool drafts = r.mode == MODE_SAMPLE && a.stream_draft;
-  for (int i = 0; i < K; ++i)
-    a.list[a.rt_max + r.d0 + i] = RowTask{drafts ? a.rt_max + r.d0 + i : -1, r.d0 + i, 1, r.c};
 }
 
 // ------------------------------------------------------------ accept scan
@@ -200,6 +217,70 @@ __device__ float draft_prob_at(const LinearArgs &a, int row, int d, float c, Row
   return ex2((load_elem(drow, a.ddt, d) - ds.m) * c) / ds.S;
 }
 
+// Decision on draft position i (0-based) of request b from the statistics of
+// its target row (ts) and dense draft row (ds) and its target rank: greedy
+// prefix match, the lossless coin, or the CACTUS guard and coin. Writes
+// p(d), q(d) and the rank. Returns true when the draft is rejected.
+__device__ bool position_rejects(const LinearArgs &a, int b, const ReqInfo &r, int i, bool sample,
+                                 const RowStat &ts, const RowStat &ds, int rank) {
+  const float c = r.c;
+  const int d = a.tokens[r.d0 + i];
+  const bool dok = (unsigned)d < (unsigned)a.V;
+  if (!dok) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+  if (row_empty(ts.m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+  float pd, qd;
+  bool rej;
+  if (!sample) {
+    rej = !(dok && d == ts.idx);
+    pd = rej ? 0.f : 1.f;
+    qd = -1.f;
+  } else if (dok && !row_empty(ts.m)) {
+    const char *trow = a.target + (long long)(r.t0 + i) * a.t_row_bytes;
+    pd = ex2((load_elem(trow, a.tdt, d) - ts.m) * c) / ts.S;
+    qd = draft_prob_at(a, r.d0 + i, d, c, ds);
+    if (a.rule == SPEC_RULE_CACTUS) {
+      const float g = fminf(pd + sqrtf(2.f * a.alpha * pd * (1.f - pd)), 1.f);
+      const float acc = qd <= g ? 1.f : g / qd;
+      const bool guard = (a.max_rank > 0 && rank > a.max_rank) || pd < a.min_prob;
+      rej = guard || !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
+    } else {
+      const float acc = qd <= pd ? 1.f : pd / qd;
+      rej = !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
+    }
+  } else {
+    pd = 0.f;
+    qd = 0.f;
+    rej = true;
+  }
+  if (a.out_pq) {
+    a.out_pq[2LL * (r.d0 + i)] = pd;
+    a.out_pq[2LL * (r.d0 + i) + 1] = qd;
+  }
+  if (a.out_rank) a.out_rank[r.d0 + i] = rank;
+  return rej;
+}
+
+// n drafts accepted: write them and queue the final token (greedy: the
+// argmax of p_{n+1}; sampling: a residual job when n < K, else a bonus job).
+// tf / df are the statistics of target row n+1 and dense draft row n+1.
+__device__ void finish_request(const LinearArgs &a, int b, const ReqInfo &r, int n, bool sample,
+                               const RowStat &tf, const RowStat &df, int lane) {
+  const int W = a.max_k + 1;
+  int32_t *out = a.out_tokens + (long long)b * W;
+  for (int j = lane; j < W; j += 32) out[j] = j < n ? a.tokens[r.d0 + j] : -1;
+  __syncwarp();
+  if (lane == 0) {
+    a.out_accepted[b] = n;
+    if (!sample) {
+      out[n] = tf.idx;
+    } else {
+      const Job j{b, n, n < r.K ? 1 : 2, 0, tf.m, tf.S, df.m, df.S};
+      if (j.kind == 1 && !a.sparse) a.jobs_a[atomicAdd(&a.hdr->n_jobs_a, 1)] = j;
+      else a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = j;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a) {
   const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -235,58 +316,77 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
       }
     }
     const int i = base + lane;
-    bool rej = false;
-    if (lane < cnt) {
-      const int d = a.tokens[r.d0 + i];
-      const bool dok = (unsigned)d < (unsigned)a.V;
-      if (!dok) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-      if (row_empty(ts.m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-      float pd, qd;
-      if (!sample) {
-        rej = !(dok && d == ts.idx);
-        pd = rej ? 0.f : 1.f;
-        qd = -1.f;
-      } else if (dok && !row_empty(ts.m)) {
-        const char *trow = a.target + (long long)(r.t0 + i) * a.t_row_bytes;
-        pd = ex2((load_elem(trow, a.tdt, d) - ts.m) * c) / ts.S;
-        qd = draft_prob_at(a, r.d0 + i, d, c, ds);
-        if (a.rule == SPEC_RULE_CACTUS) {
-          const float g = fminf(pd + sqrtf(2.f * a.alpha * pd * (1.f - pd)), 1.f);
-          const float acc = qd <= g ? 1.f : g / qd;
-          const bool guard = (a.max_rank > 0 && rank > a.max_rank) || pd < a.min_prob;
-          rej = guard || !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
-        } else {
-          const float acc = qd <= pd ? 1.f : pd / qd;
-          rej = !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
-        }
-      } else {
-        pd = 0.f;
-        qd = 0.f;
-        rej = true;
-      }
-      if (a.out_pq) {
-        a.out_pq[2LL * (r.d0 + i)] = pd;
-        a.out_pq[2LL * (r.d0 + i) + 1] = qd;
-      }
-      if (a.out_rank) a.out_rank[r.d0 + i] = rank;
-    }
+    const bool rej = lane < cnt && position_rejects(a, b, r, i, sample, ts, ds, rank);
     const unsigned bal = __ballot_sync(0xffffffffu, rej);
     if (n == K && bal) n = base + __ffs(bal) - 1;
   }
-  for (int j = lane; j < W; j += 32) out[j] = j < n ? a.tokens[r.d0 + j] : -1;
   const RowStat tf = target_stat(a, r.t0 + n, c, lane);
   RowStat df{NO_MAX, 0.f, 0x7fffffff};
   if (sample && n < K && a.stream_draft) df = draft_stat(a, r.d0 + n, c, lane);
-  __syncwarp();
-  if (lane == 0) {
-    a.out_accepted[b] = n;
-    if (!sample) {
-      out[n] = tf.idx;
-    } else {
-      const Job j{b, n, n < K ? 1 : 2, 0, tf.m, tf.S, df.m, df.S};
-      if (j.kind == 1 && !a.sparse) a.jobs_a[atomicAdd(&a.hdr->n_jobs_a, 1)] = j;
-      else a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = j;
+  finish_request(a, b, r, n, sample, tf, df, lane);
+}
+
+// ------------------------------------------------ position-lazy rounds
+// Round `a.round` = j: the row pass has just streamed, for every request
+// still active, target row p_{j+1} and (sampling, dense draft) draft row
+// q_{j+1}. One warp per request decides draft j+1 (or, at j == K, takes the
+// bonus row), then either lists the next position's rows or finishes the
+// request. The row list is indexed by request: entry b the target row,
+// entry B + b the draft row, slot -1 when idle. Rows after the first
+// rejection are never streamed (nalar.dev, "Penolakan memendekkan pekerjaan
+// speculative").
+__global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearArgs a) {
+  const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.hdr->work = 0;   // the next round's counter
+  if (b >= a.B) return;
+  const int W = a.max_k + 1;
+  int32_t *out = a.out_tokens + (long long)b * W;
+  if (*(volatile int *)&a.hdr->status != SPEC_OK) {
+    for (int j = lane; j < W; j += 32) out[j] = -1;
+    if (lane == 0) {
+      a.out_accepted[b] = -1;
+      a.list[b].slot = -1;
+      a.list[a.B + b].slot = -1;
     }
+    return;
+  }
+  if (a.list[b].slot < 0) return;   // finished in an earlier round
+  const ReqInfo r = a.req[b];
+  const int K = r.K, j = a.round;
+  const float c = r.c;
+  const bool sample = r.mode == MODE_SAMPLE;
+  const RowStat ts = target_stat(a, r.t0 + j, c, lane);
+  RowStat ds{NO_MAX, 0.f, 0x7fffffff};
+  int n = K;
+  if (j < K) {
+    const int rank = a.want_rank ? 1 + warp_row_count(a, r.t0 + j, lane) : 0;
+    if (sample && a.stream_draft) ds = draft_stat(a, r.d0 + j, c, lane);
+    const bool rej = __shfl_sync(0xffffffffu,
+                                 lane == 0 && position_rejects(a, b, r, j, sample, ts, ds, rank),
+                                 0);
+    if (!rej) {   // accepted: list the next position's rows
+      if (lane == 0) {
+        a.list[b] = RowTask{r.t0 + j + 1, r.t0 + j + 1, 0, c};
+        const bool drow = sample && a.stream_draft && j + 1 < K;
+        a.list[a.B + b] = RowTask{drow ? a.rt_max + r.d0 + j + 1 : -1, r.d0 + j + 1, 1, c};
+      }
+      return;
+    }
+    n = j;
+  }
+  finish_request(a, b, r, n, sample, ts, ds, lane);
+  // positions after n+1 were never read
+  for (int i = n + 1 + lane; i < K; i += 32) {
+    if (a.out_pq) {
+      a.out_pq[2LL * (r.d0 + i)] = __int_as_float(0x7fc00000);
+      a.out_pq[2LL * (r.d0 + i) + 1] = __int_as_float(0x7fc00000);
+    }
+    if (a.out_rank) a.out_rank[r.d0 + i] = -1;
+  }
+  if (lane == 0) {
+    a.list[b].slot = -1;
+    a.list[a.B + b].slot = -1;
   }
 }
 
@@ -732,7 +832,8 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   if (rule == SPEC_RULE_CACTUS && ext == nullptr) return SPEC_ERR_INVALID_ARG;
   if (ext != nullptr &&
       (!(ext->alpha >= 0.f) || !isfinite(ext->alpha) || ext->max_rank < 0 ||
-       !(ext->min_prob >= 0.f) || !isfinite(ext->min_prob) || ext->reserved != 0 ||
+       !(ext->min_prob >= 0.f) || !isfinite(ext->min_prob) ||
+       (ext->flags & ~SPEC_EXT_LAZY) != 0 ||
        !aligned(ext->out_rank, 4)))
     return SPEC_ERR_INVALID_ARG;
   if (dk == SPEC_DRAFT_SPARSE128 && (ddt != SPEC_F32 || draft_idx == nullptr || draft == nullptr))
@@ -789,6 +890,8 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.max_rank = ext ? ext->max_rank : 0;
   a.out_rank = ext ? ext->out_rank : nullptr;
   a.want_rank = a.out_rank != nullptr || (rule == SPEC_RULE_CACTUS && a.max_rank > 0);
+  a.lazy = ext && (ext->flags & SPEC_EXT_LAZY) ? 1 : 0;
+  a.round = 0;
   a.rank_thr = reinterpret_cast<float *>(ws + L.rank_thr);
   if (dk == SPEC_DRAFT_SPARSE128) {
     a.draft_idx = draft_idx;
@@ -832,10 +935,26 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   rp.tsum4 = nullptr;
   rp.ntiles = 0;
   rp.V = V;
-  int rc = launch_row_pass(rp, st);
-  if (rc != SPEC_OK) return rc;
-  k_accept<<<(B + ACCEPT_WARPS - 1) / ACCEPT_WARPS, ACCEPT_WARPS * 32, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  int rc;
+  if (a.lazy) {
+    // profiling events, if any, bracket all rounds (row passes and decisions)
+    cudaEvent_t before, after;
+    take_row_pass_events(&before, &after);
+    if (before && cudaEventRecord(before, st) != cudaSuccess) return SPEC_ERR_CUDA;
+    for (int j = 0; j <= max_k; ++j) {
+      rc = launch_row_pass(rp, st);
+      if (rc != SPEC_OK) return rc;
+      a.round = j;
+      k_lazy_decide<<<(B + ACCEPT_WARPS - 1) / ACCEPT_WARPS, ACCEPT_WARPS * 32, 0, st>>>(a);
+      if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    }
+    if (after && cudaEventRecord(after, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  } else {
+    rc = launch_row_pass(rp, st);
+    if (rc != SPEC_OK) return rc;
+    k_accept<<<(B + ACCEPT_WARPS - 1) / ACCEPT_WARPS, ACCEPT_WARPS * 32, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  }
   const int tiles_grid = 8 * num_sms();
   if (a.sparse) {
     k_sample_final<SPEC_DRAFT_SPARSE128><<<B, SAMPLE_THREADS, 0, st>>>(a);

@@ -501,6 +501,12 @@ void set_row_pass_events(cudaEvent_t before, cudaEvent_t after) {
   prof_after = after;
 }
 
+void take_row_pass_events(cudaEvent_t *before, cudaEvent_t *after) {
+  *before = prof_before;
+  *after = prof_after;
+  prof_before = prof_after = nullptr;
+}
+
 int launch_row_pass(const RowPassArgs &a, cudaStream_t stream) {
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;

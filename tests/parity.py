@@ -15,11 +15,12 @@ PROB_ATOL = 1e-30
 
 
 def gpu_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, draft=None,
-               draft_idx=None, ext=None):
+               draft_idx=None, ext=None, lazy=False):
     """Runs the CUDA verifier; `ext` (a dict of alpha / max_rank / min_prob)
-    goes through spec_verify_linear_ext, which also returns target ranks."""
+    or `lazy` goes through spec_verify_linear_ext, which also returns target
+    ranks."""
     draft = lb.draft if draft is None else draft
-    if ext is None:
+    if ext is None and not lazy:
         tokens, acc, pq, ws = sv.spec_verify_linear(
             lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
             max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx, want_pq=True)
@@ -28,7 +29,7 @@ def gpu_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, dr
         tokens, acc, pq, rank, ws = sv.spec_verify_linear_ext(
             lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
             max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx,
-            want_pq=True, want_rank=True, **ext)
+            want_pq=True, want_rank=True, lazy=lazy, **(ext or {}))
     status = sv.spec_get_status(ws)
     out = dict(tokens=tokens.cpu().numpy(), accepted=acc.cpu().numpy(),
                pq=pq.cpu().numpy().astype(np.float64), status=status)

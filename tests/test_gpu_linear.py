@@ -270,3 +270,71 @@ def test_cactus_argument_errors():
             sv.spec_verify_linear_ext(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
                                       lb.temperature, 1, max_k=lb.max_k,
                                       rule=sv.SPEC_RULE_CACTUS, **bad)
+
+
+# ---------------------------------------------- position-lazy verification
+def assert_lazy_matches(g, ref, lb):
+    """Tokens and counts as the oracle; p(d), q(d) and ranks on the read
+    positions, NaN / -1 exactly on the unread ones."""
+    lz = O.lazy_view(ref, lb.cu_draft.cpu().numpy())
+    assert np.array_equal(np.isnan(g["pq"][:, 0]), np.isnan(lz["pq"][:, 0]))
+    assert np.array_equal(g["rank"] == -1, lz["rank"] == -1)
+    assert_linear_parity(g, lz, lb.cu_draft.cpu(), min_compared=10)
+
+
+LAZY_CASES = [
+    dict(cfg=2, over=dict(B=40, K=(0, 7), V=30011, dtype="bf16", sigma=0.9,
+                          T=[0.0, 0.6, 1.0, 1.3] * 10), kw={}),
+    dict(cfg=2, over=dict(B=24, K=(1, 6), V=4099, dtype="f32", sigma=1.2,
+                          T=[0.7, 1.0] * 12), kw={}),
+    dict(cfg=1, over=dict(B=16, K=8, V=100003, dtype="bf16", sigma=1.0, T=1.0),
+         kw=dict(rule=sv.SPEC_RULE_CACTUS, ext=dict(alpha=0.2, max_rank=10, min_prob=0.05))),
+]
+
+
+@pytest.mark.parametrize("case", LAZY_CASES)
+def test_lazy_equals_eager_and_the_oracle(case):
+    lb = S.make_linear(case["cfg"], device=DEV, input_seed=4242, **case["over"])
+    kw = dict(case["kw"])
+    g = gpu_linear(lb, lazy=True, **kw)
+    assert g["status"] == sv.SPEC_OK
+    e = gpu_linear(lb, **kw)
+    assert np.array_equal(g["tokens"], e["tokens"]) and np.array_equal(g["accepted"], e["accepted"])
+    ref = oracle_linear(lb, rule=kw.get("rule", sv.SPEC_RULE_STRICT), ext=kw.get("ext"))
+    assert_lazy_matches(g, ref, lb)
+    assert 0 < g["accepted"].mean() < lb.max_k
+
+
+def test_lazy_with_probability_and_sparse_drafts():
+    lb = S.make_linear(2, device=DEV, B=20, K=(1, 6), V=20000, input_seed=515,
+                       T=[0.0, 0.8, 1.2, 1.0] * 5)
+    probs = probs_from_logits(lb.draft, lb.cu_draft, lb.temperature)
+    g = gpu_linear(lb, draft_kind=sv.SPEC_DRAFT_PROBS, draft=probs, lazy=True)
+    ref = oracle_linear(lb, draft_kind=sv.SPEC_DRAFT_PROBS, draft=probs)
+    assert_lazy_matches(g, ref, lb)
+    idx, prob, _ = sv.draft_topk_softmax(lb.draft, lb.cu_draft, lb.temperature)
+    g = gpu_linear(lb, draft_kind=sv.SPEC_DRAFT_SPARSE128, draft=prob, draft_idx=idx, lazy=True)
+    ref = oracle_linear(lb, draft_kind=sv.SPEC_DRAFT_SPARSE128, draft=prob, draft_idx=idx)
+    assert_lazy_matches(g, ref, lb)
+
+
+def test_lazy_never_reads_rows_after_the_first_rejection():
+    """Rows after position n+1 are set to -inf everywhere (no mass): the
+    eager call reports them, the lazy call never touches them."""
+    lb = S.make_linear(2, device=DEV, B=32, K=(2, 6), V=8192, input_seed=99, sigma=1.5,
+                       T=[0.0, 1.0] * 16)
+    ref = oracle_linear(lb)
+    cu = lb.cu_draft.cpu().numpy()
+    t2, d2 = lb.target.clone(), lb.draft.clone()
+    for j, b in enumerate(ref["requests"]):
+        n, K = int(ref["accepted"][j]), int(cu[b + 1] - cu[b])
+        t0, d0 = int(cu[b]) + int(b), int(cu[b])
+        t2[t0 + n + 1:t0 + K + 1] = float("-inf")
+        d2[d0 + min(n + 1, K):d0 + K] = float("-inf")
+    assert (t2 == float("-inf")).all(1).sum() > 10
+    lb2 = S.LinearBatch(**{**lb.__dict__, "target": t2, "draft": d2})
+    g = gpu_linear(lb2, lazy=True)
+    assert g["status"] == sv.SPEC_OK
+    assert_lazy_matches(g, ref, lb)
+    e = gpu_linear(lb2)
+    assert e["status"] == sv.SPEC_ERR_INVALID_ARG
