@@ -10,6 +10,9 @@ namespace sv {
 
 // ---------------------------------------------------------------- tiling
 constexpr int TILE_BYTES = 16384;   // one TMA bulk copy = one pipeline stage
+// Position-lazy rounds stream few rows each: finer chunks spread them over
+// more CTAs.
+constexpr int LAZY_CHUNK_BYTES = 32768;
 constexpr int CHUNK_BYTES = 131072; // one unit of dynamic work in the row pass
 // Row pass shape, chosen by measurement on GB300: six CTAs per SM, each one
 // producer lane and four consumer warps over a two-stage ring of 16 KB TMA

@@ -24,10 +24,11 @@ struct RowPassArgs {
   int dtype[2];
   int nch[2];               // chunks per row of each tensor
   int nch_max;
+  int chunk_bytes;          // chunk size, a multiple of TILE_BYTES
   const RowTask *list;      // rows to stream (count in hdr->n_list)
   WsHeader *hdr;
   Part *part;
-  // Optional rank count: for a target row of list slot s, rank_thr[s] is the
+  // Optional rank count: for a listed target row r, rank_thr[r] is the
   // draft token's logit (+inf: no count) and every Part's `cnt` receives the
   // number of the chunk's logits strictly above it. NULL: no counting.
   const float *rank_thr;
@@ -50,7 +51,7 @@ void set_row_pass_events(cudaEvent_t before, cudaEvent_t after);
 // itself (and unregisters them).
 void take_row_pass_events(cudaEvent_t *before, cudaEvent_t *after);
 int launch_row_pass(const RowPassArgs &a, cudaStream_t stream);
-int nchunks(int V, int dtype);
+int nchunks(int V, int dtype, int chunk_bytes);
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Top-128 select + softmax over draft rows. Row r belongs to the request b

@@ -53,7 +53,8 @@ struct LinearArgs {
   RowTask *list;
   Part *part;
   long long t_row_bytes, d_row_bytes;
-  int nch_t, nch_d, nch_max;
+  int nch_t, nch_d, nch_max;   // chunks of the mode's chunk size
+  int chunk_bytes;
   int rt_max;                 // slot offset of draft rows
   int sparse;                 // the draft law is sparse (given or top-128)
   int stream_draft;           // the row pass reads dense draft logits
@@ -69,13 +70,14 @@ struct LinearArgs {
 
 struct LinearLayout {
   size_t hdr, req, jobs_a, jobs_b, tsum, list, part, tk_idx, tk_prob, rank_thr, total;
-  int nch_max;
+  int nch_max, nch_max_lazy;
   long long rows_max;
 };
 
 static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   LinearLayout L;
-  L.nch_max = nchunks(V, SPEC_F32);
+  L.nch_max = nchunks(V, SPEC_F32, CHUNK_BYTES);
+  L.nch_max_lazy = nchunks(V, SPEC_F32, LAZY_CHUNK_BYTES);
   L.rows_max = (long long)B * (2LL * max_k + 1);
   size_t o = 0;
   L.hdr = o;  o += align256(sizeof(WsHeader));
@@ -85,7 +87,11 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   L.tsum = o;
   o += align256(sizeof(float) * (size_t)B * ((V + SAMPLE_TILE - 1) / SAMPLE_TILE) * RS_CONS_WARPS);
   L.list = o; o += align256(sizeof(RowTask) * (size_t)std::max(L.rows_max, 2LL * B));
-  L.part = o; o += align256(sizeof(Part) * (size_t)L.rows_max * L.nch_max * RS_CONS_WARPS);
+  // eager: one slot per listed row; lazy: two per request (its rows of the
+  // current round), in finer chunks
+  L.part = o;
+  o += align256(sizeof(Part) * RS_CONS_WARPS *
+                std::max((size_t)L.rows_max * L.nch_max, (size_t)2 * B * L.nch_max_lazy));
   const size_t tk = rule == SPEC_RULE_STRICT_TOP128 ? (size_t)B * max_k * SPEC_TOPK : 0;
   L.tk_idx = o;  o += align256(sizeof(int32_t) * tk);
   L.tk_prob = o; o += align256(sizeof(float) * tk);
@@ -143,8 +149,8 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
   a.req[b] = r;
   const bool drafts = r.mode == MODE_SAMPLE && a.stream_draft;
   if (a.lazy) {
-    a.list[b] = RowTask{r.t0, r.t0, 0, r.c};
-    a.list[a.B + b] = RowTask{drafts && K > 0 ? a.rt_max + r.d0 : -1, r.d0, 1, r.c};
+    a.list[b] = RowTask{b, r.t0, 0, r.c};
+    a.list[a.B + b] = RowTask{drafts && K > 0 ? a.B + b : -1, r.d0, 1, r.c};
   } else {
     for (int i = 0; i <= K; ++i) a.list[r.t0 + i] = RowTask{r.t0 + i, r.t0 + i, 0, r.c};
     for (int i = 0; i < K; ++i)
@@ -182,9 +188,18 @@ __device__ __forceinline__ RowStat warp_row_stat(const Part *p, int n, float c, 
   }
   return RowStat{m, S, idx};
 }
+// Part slots of position i's rows of request b: eager, one per listed row;
+// lazy, entries b and B + b of the current round.
+__device__ __forceinline__ int tslot(const LinearArgs &a, const ReqInfo &r, int b, int i) {
+  return a.lazy ? b : r.t0 + i;
+}
+__device__ __forceinline__ int dslot(const LinearArgs &a, const ReqInfo &r, int b, int i) {
+  return a.lazy ? a.B + b : a.rt_max + r.d0 + i;
+}
+
 // Rank count of a target row: the sum of the chunk partials' counts.
-__device__ __forceinline__ int warp_row_count(const LinearArgs &a, int row, int lane) {
-  const Part *p = a.part + (long long)row * a.nch_max * RS_CONS_WARPS;
+__device__ __forceinline__ int warp_row_count(const LinearArgs &a, int slot, int lane) {
+  const Part *p = a.part + (long long)slot * a.nch_max * RS_CONS_WARPS;
   const int n = a.nch_t * RS_CONS_WARPS;
   int c = 0;
   for (int i = lane; i < n; i += 32) c += p[i].cnt;
@@ -192,12 +207,12 @@ __device__ __forceinline__ int warp_row_count(const LinearArgs &a, int row, int 
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
   return c;
 }
-__device__ __forceinline__ RowStat target_stat(const LinearArgs &a, int row, float c, int lane) {
-  return warp_row_stat(a.part + (long long)row * a.nch_max * RS_CONS_WARPS,
+__device__ __forceinline__ RowStat target_stat(const LinearArgs &a, int slot, float c, int lane) {
+  return warp_row_stat(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS,
                        a.nch_t * RS_CONS_WARPS, c, lane);
 }
-__device__ __forceinline__ RowStat draft_stat(const LinearArgs &a, int row, float c, int lane) {
-  return warp_row_stat(a.part + (long long)(a.rt_max + row) * a.nch_max * RS_CONS_WARPS,
+__device__ __forceinline__ RowStat draft_stat(const LinearArgs &a, int slot, float c, int lane) {
+  return warp_row_stat(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS,
                        a.nch_d * RS_CONS_WARPS, c, lane);
 }
 
@@ -222,7 +237,8 @@ __device__ float draft_prob_at(const LinearArgs &a, int row, int d, float c, Row
 // prefix match, the lossless coin, or the CACTUS guard and coin. Writes
 // p(d), q(d) and the rank. Returns true when the draft is rejected.
 __device__ bool position_rejects(const LinearArgs &a, int b, const ReqInfo &r, int i, bool sample,
-                                 const RowStat &ts, const RowStat &ds, int rank) {
+                                 const RowStat &ts, const RowStat &ds, int rank,
+                                 float q_given = -1.f) {
   const float c = r.c;
   const int d = a.tokens[r.d0 + i];
   const bool dok = (unsigned)d < (unsigned)a.V;
@@ -237,7 +253,7 @@ __device__ bool position_rejects(const LinearArgs &a, int b, const ReqInfo &r, i
   } else if (dok && !row_empty(ts.m)) {
     const char *trow = a.target + (long long)(r.t0 + i) * a.t_row_bytes;
     pd = ex2((load_elem(trow, a.tdt, d) - ts.m) * c) / ts.S;
-    qd = draft_prob_at(a, r.d0 + i, d, c, ds);
+    qd = q_given >= 0.f ? q_given : draft_prob_at(a, r.d0 + i, d, c, ds);
     if (a.rule == SPEC_RULE_CACTUS) {
       const float g = fminf(pd + sqrtf(2.f * a.alpha * pd * (1.f - pd)), 1.f);
       const float acc = qd <= g ? 1.f : g / qd;
@@ -304,14 +320,14 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
     RowStat ts{NO_MAX, 0.f, 0x7fffffff}, ds{NO_MAX, 0.f, 0x7fffffff};
     int rank = 0;
     for (int i = 0; i < cnt; ++i) {
-      const RowStat t = target_stat(a, r.t0 + base + i, c, lane);
+      const RowStat t = target_stat(a, tslot(a, r, b, base + i), c, lane);
       if (lane == i) ts = t;
       if (a.want_rank) {
-        const int rk = 1 + warp_row_count(a, r.t0 + base + i, lane);
+        const int rk = 1 + warp_row_count(a, tslot(a, r, b, base + i), lane);
         if (lane == i) rank = rk;
       }
       if (sample && a.stream_draft) {
-        const RowStat d = draft_stat(a, r.d0 + base + i, c, lane);
+        const RowStat d = draft_stat(a, dslot(a, r, b, base + i), c, lane);
         if (lane == i) ds = d;
       }
     }
@@ -320,9 +336,9 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
     const unsigned bal = __ballot_sync(0xffffffffu, rej);
     if (n == K && bal) n = base + __ffs(bal) - 1;
   }
-  const RowStat tf = target_stat(a, r.t0 + n, c, lane);
+  const RowStat tf = target_stat(a, tslot(a, r, b, n), c, lane);
   RowStat df{NO_MAX, 0.f, 0x7fffffff};
-  if (sample && n < K && a.stream_draft) df = draft_stat(a, r.d0 + n, c, lane);
+  if (sample && n < K && a.stream_draft) df = draft_stat(a, dslot(a, r, b, n), c, lane);
   finish_request(a, b, r, n, sample, tf, df, lane);
 }
 
@@ -356,20 +372,32 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
   const int K = r.K, j = a.round;
   const float c = r.c;
   const bool sample = r.mode == MODE_SAMPLE;
-  const RowStat ts = target_stat(a, r.t0 + j, c, lane);
+  const RowStat ts = target_stat(a, tslot(a, r, b, j), c, lane);
   RowStat ds{NO_MAX, 0.f, 0x7fffffff};
   int n = K;
   if (j < K) {
-    const int rank = a.want_rank ? 1 + warp_row_count(a, r.t0 + j, lane) : 0;
-    if (sample && a.stream_draft) ds = draft_stat(a, r.d0 + j, c, lane);
-    const bool rej = __shfl_sync(0xffffffffu,
-                                 lane == 0 && position_rejects(a, b, r, j, sample, ts, ds, rank),
-                                 0);
+    const int rank = a.want_rank ? 1 + warp_row_count(a, tslot(a, r, b, j), lane) : 0;
+    if (sample && a.stream_draft) ds = draft_stat(a, dslot(a, r, b, j), c, lane);
+    // a sparse draft's q(d): the warp searches the row's 128 ids together
+    float qs = -1.f;
+    if (sample && a.sparse) {
+      const int d = a.tokens[r.d0 + j];
+      const long long row = (long long)(r.d0 + j) * SPEC_TOPK;
+      unsigned hit = 0;
+      int k_hit = 0;
+      for (int k = lane; k < SPEC_TOPK; k += 32) {
+        const unsigned m = __ballot_sync(0xffffffffu, a.draft_idx[row + k] == d);
+        if (m && !hit) { hit = m; k_hit = k - lane + __ffs(m) - 1; }
+      }
+      qs = hit ? a.sparse_prob[row + k_hit] : 0.f;
+    }
+    const bool rej = __shfl_sync(
+        0xffffffffu, lane == 0 && position_rejects(a, b, r, j, sample, ts, ds, rank, qs), 0);
     if (!rej) {   // accepted: list the next position's rows
       if (lane == 0) {
-        a.list[b] = RowTask{r.t0 + j + 1, r.t0 + j + 1, 0, c};
+        a.list[b] = RowTask{b, r.t0 + j + 1, 0, c};
         const bool drow = sample && a.stream_draft && j + 1 < K;
-        a.list[a.B + b] = RowTask{drow ? a.rt_max + r.d0 + j + 1 : -1, r.d0 + j + 1, 1, c};
+        a.list[a.B + b] = RowTask{drow ? a.B + b : -1, r.d0 + j + 1, 1, c};
       }
       return;
     }
@@ -616,10 +644,10 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
                           int kind, float u) {
   const ReqInfo r = a.req[job.b];
   const int esz = dtype_size(a.tdt);
-  const int chunk_elems = CHUNK_BYTES / esz;
+  const int chunk_elems = a.chunk_bytes / esz;
   const int tpc = chunk_elems / SAMPLE_TILE;  // tiles per chunk
   const int nch = a.nch_t;
-  const Part *pp = a.part + (long long)(r.t0 + job.n) * a.nch_max * RS_CONS_WARPS;
+  const Part *pp = a.part + (long long)tslot(a, r, job.b, job.n) * a.nch_max * RS_CONS_WARPS;
   for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
     float m = 0.f;
     for (int w = 0; w < RS_CONS_WARPS; ++w) {
@@ -879,9 +907,11 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
   a.d_row_bytes = dk == SPEC_DRAFT_SPARSE128 ? (long long)SPEC_TOPK * 4
                                              : (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
-  a.nch_t = nchunks(V, tdt);
-  a.nch_d = nchunks(V, ddt);
-  a.nch_max = L.nch_max;
+  const bool lazy = ext && (ext->flags & SPEC_EXT_LAZY);
+  a.chunk_bytes = lazy ? LAZY_CHUNK_BYTES : CHUNK_BYTES;
+  a.nch_t = nchunks(V, tdt, a.chunk_bytes);
+  a.nch_d = nchunks(V, ddt, a.chunk_bytes);
+  a.nch_max = lazy ? L.nch_max_lazy : L.nch_max;
   a.rt_max = B * (max_k + 1);
   a.sparse = dk == SPEC_DRAFT_SPARSE128 || rule == SPEC_RULE_STRICT_TOP128;
   a.stream_draft = dk == SPEC_DRAFT_LOGITS && rule != SPEC_RULE_STRICT_TOP128;
@@ -925,6 +955,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   rp.nch[0] = a.nch_t;
   rp.nch[1] = a.nch_d;
   rp.nch_max = a.nch_max;
+  rp.chunk_bytes = a.chunk_bytes;
   rp.list = a.list;
   rp.hdr = a.hdr;
   rp.part = a.part;

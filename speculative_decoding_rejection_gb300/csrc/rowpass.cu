@@ -313,13 +313,13 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
       const int chunk = (int)(item % a.nch_max);
       const RowTask t = a.list[entry];
       const int w = t.which;
-      const float thr = RANK && w == 0 && t.slot >= 0 ? a.rank_thr[t.slot] : INFINITY;
+      const float thr = RANK && w == 0 && t.slot >= 0 ? a.rank_thr[t.row] : INFINITY;
       const long long rbytes = w ? a.row_bytes[1] : a.row_bytes[0];
       if (t.slot >= 0 && chunk < (w ? a.nch[1] : a.nch[0])) {
         const int esz = dtype_size(w ? a.dtype[1] : a.dtype[0]);
         const uint64_t row0 = (uint64_t)((w ? a.base[1] : a.base[0]) + (long long)t.row * rbytes);
-        const uint64_t cb0 = row0 + (uint64_t)chunk * CHUNK_BYTES;
-        const uint64_t cb1 = min(row0 + (uint64_t)rbytes, cb0 + CHUNK_BYTES);
+        const uint64_t cb0 = row0 + (uint64_t)chunk * a.chunk_bytes;
+        const uint64_t cb1 = min(row0 + (uint64_t)rbytes, cb0 + (uint64_t)a.chunk_bytes);
         uint64_t A0 = (cb0 + 15) & ~15ull, A1 = cb1 & ~15ull;
         if (A1 <= A0) A0 = A1 = cb1;  // no aligned interior: all scalar
         const int ntile = A1 > A0 ? (int)((A1 - A0 + TILE_BYTES - 1) / TILE_BYTES) : 1;
@@ -476,9 +476,9 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
   }
 }
 
-int nchunks(int V, int dtype) {
+int nchunks(int V, int dtype, int chunk_bytes) {
   const long long bytes = (long long)V * (dtype == SPEC_BF16 ? 2 : 4);
-  return (int)((bytes + CHUNK_BYTES - 1) / CHUNK_BYTES);
+  return (int)((bytes + chunk_bytes - 1) / chunk_bytes);
 }
 
 int num_sms() {

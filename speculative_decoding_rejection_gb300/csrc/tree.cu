@@ -75,7 +75,7 @@ struct TreeLayout {
 
 static TreeLayout tree_layout(int B, int n_nodes, int V) {
   TreeLayout L;
-  L.nch_max = nchunks(V, SPEC_F32);
+  L.nch_max = nchunks(V, SPEC_F32, CHUNK_BYTES);
   const size_t rows = 2 * (size_t)n_nodes;
   size_t o = 0;
   L.hdr = o;  o += align256(sizeof(WsHeader));
@@ -608,8 +608,8 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   a.part = reinterpret_cast<Part *>(ws + L.part);
   a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
   a.d_row_bytes = (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
-  a.nch_t = nchunks(V, tdt);
-  a.nch_d = nchunks(V, ddt);
+  a.nch_t = nchunks(V, tdt, CHUNK_BYTES);
+  a.nch_d = nchunks(V, ddt, CHUNK_BYTES);
   a.nch_max = L.nch_max;
   a.stream_draft = dk == SPEC_DRAFT_LOGITS;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -628,6 +628,7 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   rp.nch[0] = a.nch_t;
   rp.nch[1] = a.nch_d;
   rp.nch_max = a.nch_max;
+  rp.chunk_bytes = CHUNK_BYTES;
   rp.list = a.list;
   rp.hdr = a.hdr;
   rp.part = a.part;
