@@ -187,6 +187,26 @@ __device__ __forceinline__ RowStat combine_parts(const Part *p, int n, float c) 
   return r;
 }
 
+// Row statistics combined by the whole warp: lane l merges partials
+// l, l+32, ..., then a butterfly merges the lanes (every lane gets the row's
+// statistics; the merge order is fixed, so the result is deterministic).
+__device__ __forceinline__ RowStat warp_row_stat(const Part *p, int n, float c, int lane) {
+  float m = NO_MAX, S = 0.f;
+  int idx = 0x7fffffff;
+  for (int i = lane; i < n; i += 32) {
+    const Part q = p[i];
+    merge_stat(m, S, idx, q.m, q.S, q.idx, c);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    merge_stat(m, S, idx, m2, S2, i2, c);
+  }
+  return RowStat{m, S, idx};
+}
+
 // Load SAMPLE_EPT consecutive elements [x0, x0+EPT) of a row; `fill` beyond V.
 __device__ __forceinline__ void load_ept(const char *row, int dt, bool vec_ok, int x0, int V,
                                          float fill, float *z) {

@@ -172,6 +172,9 @@ struct WalkSmem {
   float zall[WALK_CLUSTER];              // every slice's total of the last pass
   float scratch[33];
   int kids[SPEC_MAX_TREE_BRANCH];
+  int kx[SPEC_MAX_TREE_BRANCH];          // children's tokens
+  float kzt[SPEC_MAX_TREE_BRANCH];       // target logit at each child's token
+  float kzd[SPEC_MAX_TREE_BRANCH];       // draft logit (or probability) there
   float s[SPEC_MAX_TREE_BRANCH + 1];     // 1 / (1 - q(E_j))
   float rinv[SPEC_MAX_TREE_BRANCH + 1];  // 1 / Z_j
   int skip[SPEC_MAX_TREE_BRANCH + 1];    // Z_j == 0: p_{j+1} = p_j
@@ -208,17 +211,26 @@ __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkS
   const int x0 = j * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
   float zt[SAMPLE_EPT], zd[SAMPLE_EPT];
   load_ept(nl.trow, a.tdt, nl.tvec, x0, a.V, -INFINITY, zt);
-  if (L > 0 || residual)
-    load_ept(nl.drow, a.ddt, nl.dvec, x0, a.V, DK == SPEC_DRAFT_PROBS ? 0.f : -INFINITY, zd);
 #pragma unroll
-  for (int k = 0; k < SAMPLE_EPT; ++k) {
-    const float p = ex2((zt[k] - nl.mt) * c) * nl.invSt;
-    if (L == 0 && !residual) {
-      w[k] = p;
-      continue;
-    }
-    const float q = DK == SPEC_DRAFT_PROBS ? zd[k] : ex2((zd[k] - nl.md) * c) * nl.invSd;
-    w[k] = chain_weight(p, q, L, residual, sh);
+  for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = ex2((zt[k] - nl.mt) * c) * nl.invSt;
+  if (L == 0 && !residual) return;
+  load_ept(nl.drow, a.ddt, nl.dvec, x0, a.V, DK == SPEC_DRAFT_PROBS ? 0.f : -INFINITY, zd);
+  float q[SAMPLE_EPT];
+#pragma unroll
+  for (int k = 0; k < SAMPLE_EPT; ++k)
+    q[k] = DK == SPEC_DRAFT_PROBS ? zd[k] : ex2((zd[k] - nl.md) * c) * nl.invSd;
+  // the chain level by level over all elements (the same operations per
+  // element as chain_weight, so the same bits)
+  for (int i = 0; i < L; ++i) {
+    if (sh.skip[i]) continue;
+    const float si = sh.s[i], ri = sh.rinv[i];
+#pragma unroll
+    for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = fmaxf(0.f, w[k] - q[k] * si) * ri;
+  }
+  if (residual) {
+    const float sL = sh.s[L];
+#pragma unroll
+    for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = fmaxf(0.f, w[k] - q[k] * sL);
   }
 }
 
@@ -258,13 +270,12 @@ __device__ void weight_pass(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, 
     sh.zr[par] = Zr;
   }
   cluster.sync();   // every slice total written (slots alternate by parity)
+  if (threadIdx.x < WALK_CLUSTER)   // one remote read per thread, in parallel
+    sh.zall[threadIdx.x] = *cluster.map_shared_rank(&sh.zr[par], (int)threadIdx.x);
+  __syncthreads();
   if (threadIdx.x == 0) {
     float Z = 0.f;
-    for (int r = 0; r < WALK_CLUSTER; ++r) {
-      const float zr = *cluster.map_shared_rank(&sh.zr[par], r);
-      sh.zall[r] = zr;
-      Z += zr;
-    }
+    for (int r = 0; r < WALK_CLUSTER; ++r) Z += sh.zall[r];
     sh.Z = Z;
     sh.par = par ^ 1;
   }
@@ -347,9 +358,11 @@ __device__ int weight_draw(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, f
   return x;
 }
 
+// Row statistics from the row pass's partials; every warp merges them the
+// same fixed way, so all threads of the cluster get identical values.
 __device__ __forceinline__ RowStat node_stat(const TreeArgs &a, int slot, int nch, float c) {
-  return combine_parts(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS, nch * RS_CONS_WARPS,
-                       c);
+  return warp_row_stat(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS, nch * RS_CONS_WARPS,
+                       c, (int)threadIdx.x & 31);
 }
 
 __device__ __forceinline__ void write_final(const TreeArgs &a, int b, int depth, int x) {
@@ -388,6 +401,18 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
         }
       if (threadIdx.x == 0) sh.nk = min(tot, SPEC_MAX_TREE_BRANCH);
       __syncthreads();
+      // the children's tokens and the logits the coins need, one thread each
+      const int j = threadIdx.x;
+      if (j < sh.nk) {
+        const long long rv = t.base + v;
+        const int x = a.node_token[t.base + sh.kids[j]];
+        sh.kx[j] = x;
+        if (t.mode != MODE_GREEDY && (unsigned)x < (unsigned)a.V) {
+          sh.kzt[j] = load_elem(a.target + rv * a.t_row_bytes, a.tdt, x);
+          sh.kzd[j] = load_elem(a.draft + rv * a.d_row_bytes, a.ddt, x);
+        }
+      }
+      __syncthreads();
     }
     const int nk = sh.nk;
     const int row = t.base + v;
@@ -396,14 +421,14 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       if (threadIdx.x == 0) {
         sh.accepted_child = -1;
         for (int j = 0; j < nk; ++j)
-          if (a.node_token[t.base + sh.kids[j]] == ts.idx) { sh.accepted_child = sh.kids[j]; break; }
+          if (sh.kx[j] == ts.idx) { sh.accepted_child = sh.kids[j]; break; }
       }
       __syncthreads();
       const int ac = sh.accepted_child;
       __syncthreads();
       if (ac >= 0 && depth < a.max_depth) {
         if (rank == 0 && threadIdx.x == 0) {
-          out[depth] = a.node_token[t.base + ac];
+          out[depth] = ts.idx;   // the accepted child's token is the argmax
           if (path) path[depth] = ac;
         }
         v = ac;
@@ -453,11 +478,9 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       // coin of child j at its token x, with p_j(x) and q_j(x) from the chain
       if (threadIdx.x == 0) {
         const int ch = sh.kids[j];
-        const int x = a.node_token[t.base + ch];
-        const float p = ex2((load_elem(nl.trow, a.tdt, x) - nl.mt) * c) * nl.invSt;
-        const float qx = DK == SPEC_DRAFT_PROBS
-                             ? load_elem(nl.drow, a.ddt, x)
-                             : ex2((load_elem(nl.drow, a.ddt, x) - nl.md) * c) * nl.invSd;
+        const float p = ex2((sh.kzt[j] - nl.mt) * c) * nl.invSt;
+        const float qx = DK == SPEC_DRAFT_PROBS ? sh.kzd[j]
+                                                : ex2((sh.kzd[j] - nl.md) * c) * nl.invSd;
         const float pj = chain_weight(p, qx, j, false, sh);
         const float qj = qx * sh.s[j];
         const float acc = qj <= pj ? 1.f : pj / qj;
