@@ -349,6 +349,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 // 1-D TMA bulk copy global -> shared, completion counted on `bar`.
+// Asks L2 to fetch [p, p + bytes) ahead of use (a hint: the range is
+// trimmed to 16-byte boundaries inside it; nothing is copied anywhere).
+__device__ __forceinline__ void prefetch_l2(const void *p, long long bytes) {
+  const uintptr_t a0 = ((uintptr_t)p + 15) & ~(uintptr_t)15;
+  const uintptr_t a1 = ((uintptr_t)p + (uintptr_t)bytes) & ~(uintptr_t)15;
+  if (a1 > a0)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"((uint32_t)(a1 - a0))
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
                                         uint64_t *bar) {
   asm volatile(

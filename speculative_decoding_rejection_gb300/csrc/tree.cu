@@ -385,7 +385,16 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
   int32_t *path = a.out_path ? a.out_path + (long long)b * W : nullptr;
   const float c = t.c;
   int v = 0, depth = 0;
+  const int esz_t = dtype_size(a.tdt), esz_d = dtype_size(a.ddt);
   while (true) {
+    // this CTA's slice of node v's rows into L2 while the node is set up
+    if (threadIdx.x == 0 && t.mode != MODE_GREEDY && sl.j1 > sl.j0) {
+      const long long e0 = (long long)sl.j0 * WALK_TILE;
+      const long long e1 = min((long long)sl.j1 * WALK_TILE, (long long)a.V);
+      const long long rv = t.base + v;
+      prefetch_l2(a.target + rv * a.t_row_bytes + e0 * esz_t, (e1 - e0) * esz_t);
+      prefetch_l2(a.draft + rv * a.d_row_bytes + e0 * esz_d, (e1 - e0) * esz_d);
+    }
     // children of v in node-index order (block-wide ordered compaction)
     {
       const int per = (t.N + blockDim.x - 1) / blockDim.x;
