@@ -2,17 +2,19 @@
 // Top-128": the draft logits keep their 128 largest entries, the rest is set
 // to -inf, and the softmax runs over the survivors).
 //
-// One CTA per row. Logits map to order-preserving unsigned keys (-0 folded
-// onto +0, so equal floats give equal keys); d = key(max) - key counts down
-// from the row maximum. The 128-th smallest d is found by an 8-bit radix
-// select. Its first pass only histograms elements with d below one digit
-// (the few hundred keys just under the max), which is where the threshold of
-// a real logit row lies, so almost no shared-memory atomics are contended;
-// rows whose top 128 spread further fall back to a full top-digit pass. The
-// collection pass keeps every d below the threshold and the lowest ids among
-// the ties (a block scan over id-ordered tiles). The 128 survivors are sorted
-// by id (bitonic) and softmaxed at temperature T; T < 0.05 gives a one-hot on
-// the argmax. Rows are re-read from L2 after the first pass.
+// One 512-thread CTA per row at a time, two CTAs per SM, rows taken in grid
+// strides. bf16 rows (V a multiple of 8, V >= 4096) take a two-pass fast
+// path: a packed bf16 max pass leaves each thread's maximum; each warp sorts
+// its 32 maxima, and the smallest of the warps' (128/16 = 8)-th largest
+// maxima bounds the 128-th largest logit from below (16 warps x 8 threads
+// hold an element at least that large). The second pass, served from L2, gathers the few hundred
+// elements at or above the bound, and each candidate's rank under the order
+// (logit descending, id ascending) keeps the top 128. Other rows, and rows
+// whose candidates overflow, use an exact radix select on order-preserving
+// keys (-0 folded onto +0): the maximum, then 8-bit digits of the distance
+// from it, and a collection pass that keeps the lowest ids among ties. The
+// survivors are put in id order by counting smaller ids and softmaxed at
+// temperature T; T < 0.05 gives a one-hot on the argmax.
 #include "common.cuh"
 #include "internal.h"
 
@@ -42,7 +44,7 @@ static_assert(SPEC_TOPK % TK_WARPS == 0 && SPEC_TOPK / TK_WARPS <= 32, "bound ne
 
 struct TopkSmem {
   unsigned long long cand[CAND_CAP];   // (key << 32) | ~id of the candidates
-  float tmax[TK_WARPS];                // per-warp 4th-largest thread maxima
+  float tmax[TK_WARPS];                // per-warp (128 / warps)-th largest thread maxima
   int cand_n;
   float m128;
   unsigned hist[256];
@@ -129,10 +131,10 @@ __device__ __forceinline__ float value_of_key16(unsigned key) {
 // Fast selection for bf16 rows with V % 8 == 0 and V >= 8 * TK_THREADS
 // (every row 16-byte aligned, every thread holds elements). A packed max pass
 // leaves each thread's maximum; every warp sorts its 32 maxima with a
-// shuffle bitonic network, and the smallest of the warps' 4th-largest
-// maxima is a lower bound on the 128-th largest element (32 warps x 4
+// shuffle bitonic network, and the smallest of the warps' 8th-largest
+// maxima is a lower bound on the 128-th largest element (16 warps x 8
 // threads each hold an element at least that large). A second pass, read
-// back from L2 (one row per CTA, one CTA per SM, keeps the rows in flight
+// back from L2 (one row per CTA, two CTAs per SM, keeps the rows in flight
 // far below L2), gathers the elements at or above the bound — a few hundred
 // on logit rows — and the exact top 128 (ties to the lower id) is ranked
 // among them in shared memory. Returns false, having written no selection,
