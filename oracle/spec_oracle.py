@@ -27,6 +27,9 @@ Sources (web pages; cited by title and section):
   guard on target rank and p(x), then the strict test, then the CACTUS test
   gamma(x) = min(p(x) + sqrt(2 alpha p(x) (1 - p(x))), 1) against q(x)) and §7
   item 3 (the guard with p(x) < 0.10 or outside the top k = 10).
+* "Test-Time Speculation" (gist.science summary of arXiv 2605.09329), §2
+  "Methodik" step 3: the verification step's target law p and draft law q
+  over the drafted canvas give the distillation signal KL(p || q).
 * "Speculative decoding: memverifikasi token draft sebelum diterima"
   (nalar.dev), sections "Draft mengubah tebakan serial menjadi batch
   verifikasi" (one target pass scores positions 1..K+1, each conditioned on
@@ -76,6 +79,13 @@ R12 Position-lazy verification reads, per request, target rows 1..n+1 and
     the draft rows 1..min(n+1, K) a sampling request with dense draft rows
     needs; it returns the same tokens and counts, and p(d), q(d) and the rank
     only for the positions it read (NaN and -1 after them).
+R13 Per-position KL(p_i || q_i) = sum_y p(y) ln(p(y) / q(y)), natural log,
+    for every draft position of a sampling request, with p and q the laws the
+    verifier uses (softmax at the request's temperature; the given or sparse
+    draft law): +inf where q has no mass under p's, NaN for greedy requests.
+    The second TTS term, KL(q_t || q), compares the drafter before and after
+    an update; a verifier sees one draft law, so it is 0 here and not
+    reported.
 """
 from __future__ import annotations
 
@@ -221,6 +231,17 @@ def low_support(p_d: float, rank: int, max_rank: int, min_prob: float) -> bool:
     return (max_rank > 0 and rank > max_rank) or p_d < min_prob
 
 
+def kl_divergence(p: np.ndarray, q: np.ndarray) -> float:
+    """KL(p || q) in nats over the support of p (R13): terms with p = 0 are
+    0; a token with p > 0 and q = 0 makes it +inf."""
+    p = np.asarray(p, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    on = p > 0.0
+    if np.any(q[on] <= 0.0):
+        return float("inf")
+    return float(np.sum(p[on] * (np.log(p[on]) - np.log(q[on]))))
+
+
 def residual(p: np.ndarray, q: np.ndarray) -> np.ndarray:
     """Unnormalised residual max(0, p - q) (RheoSampling 2026, §4 step 3)."""
     return np.maximum(0.0, p - q)
@@ -287,7 +308,7 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
     draw, -1 if none) and ``requests`` (the request ids processed).
     ``requests`` restricts the work to a subset (the hash still uses the
     global request id). ``rank`` [R_d] is the target rank of every draft
-    token (R9). Under ``RULE_CACTUS`` the acceptance test is R10 with
+    token (R9), ``kl`` [R_d] the per-position KL(p || q) (R13). Under ``RULE_CACTUS`` the acceptance test is R10 with
     ``alpha``, ``max_rank`` and ``min_prob``; the final token follows R11.
     """
     cu = np.asarray(cu_draft, dtype=np.int64)
@@ -302,6 +323,7 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
     R_d = int(cu[-1])
     pq = np.full((R_d, 2), np.nan)
     rank = np.full(R_d, -1, dtype=np.int64)
+    kl = np.full(R_d, np.nan)
     toks = np.asarray(draft_tokens, dtype=np.int64)
     temps = np.asarray(temperature, dtype=np.float64)
 
@@ -324,6 +346,7 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
                 p = softmax_T(zt, T)
                 q = _draft_law(draft, draft_kind, draft_idx, d0 + i, T, V, rule)
                 pq[d0 + i] = (p[d], q[d])
+                kl[d0 + i] = kl_divergence(p, q)
                 if rule == RULE_CACTUS:
                     a = acceptance_prob(cactus_gamma(p[d], alpha), q[d])
                     guard = low_support(p[d], rank[d0 + i], max_rank, min_prob)
@@ -359,7 +382,7 @@ def verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed,
         tokens[j, n] = final
         accepted[j] = n
         flag_slot[j] = flagged_at
-    return dict(tokens=tokens, accepted=accepted, pq=pq, rank=rank,
+    return dict(tokens=tokens, accepted=accepted, pq=pq, rank=rank, kl=kl,
                 flag_slot=flag_slot, requests=np.asarray(req))
 
 
@@ -382,12 +405,14 @@ def lazy_view(result, cu_draft):
     out = dict(result)
     pq = np.array(result["pq"], dtype=np.float64, copy=True)
     rank = np.array(result["rank"], copy=True)
+    kl = np.array(result["kl"], dtype=np.float64, copy=True)
     req = result["requests"]
     for b, m in zip(req, lazy_positions(cu, result["accepted"], req)):
         d0, d1 = int(cu[b]), int(cu[b + 1])
         pq[d0 + m:d1] = np.nan
         rank[d0 + m:d1] = -1
-    out["pq"], out["rank"] = pq, rank
+        kl[d0 + m:d1] = np.nan
+    out["pq"], out["rank"], out["kl"] = pq, rank, kl
     return out
 
 
