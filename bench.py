@@ -43,8 +43,8 @@ FALLBACK_HBM_GBS = 6800.0
 # the row-pass source it was taken on.
 # Captured on B=128, K=4, V=201088 bf16 (460.09 MB streamed by the launch):
 # 460.17 MB read + 3.81 MB written (the per-chunk partial statistics).
-ROWPASS_TRAFFIC = {"source_sha1": "baca931f4da2dffc8f200381ae6dcf8ba1355a77",
-                   "dram_per_algorithmic_byte": (460165888 + 3813376) / 460089344}
+ROWPASS_TRAFFIC = {"source_sha1": "4bb57b7f0287ffb15ec5c3d818ba995f8235f3e6",
+                   "dram_per_algorithmic_byte": (460191232 + 3402240) / 460089344}
 
 
 def parse():
@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--cpu-requests", type=int, default=1024,
                     help="requests (or trees) in the oracle's timed sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kl", action="store_true",
+                    help="linear workloads: also emit the per-position KL(p || q)")
     ap.add_argument("--lazy", action="store_true",
                     help="linear workloads: position-lazy verification (rows 1..n+1 only)")
     ap.add_argument("--rule", default="default", choices=["default", "cactus"],
@@ -173,7 +175,7 @@ class LinearWork:
     # relaxed rule options: the guard the page recommends (p >= 0.10, top 10)
     CACTUS = {"alpha": 0.5, "max_rank": 10, "min_prob": 0.10}
 
-    def __init__(self, cfg, dev, input_seed=None, B=None, rule=None, lazy=False):
+    def __init__(self, cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False):
         import torch
         import speculative_decoding_rejection_gb300 as sv
         from speculative_decoding_rejection_gb300 import synthetic as S
@@ -185,6 +187,8 @@ class LinearWork:
         if rule == "cactus":
             self.rule, self.ext = sv.SPEC_RULE_CACTUS, dict(self.CACTUS)
         self.lazy = lazy
+        self.kl = (torch.empty(lb.draft_tokens.numel(), dtype=torch.float32, device=dev)
+                   if kl else None)
         K = torch.diff(lb.cu_draft.cpu().long())
         samp = lb.temperature.cpu() >= 0.05
         self.positions = int(K.sum())
@@ -206,6 +210,8 @@ class LinearWork:
         if self.ext is not None:
             self.config["rule"] = ("cactus(alpha={alpha},max_rank={max_rank},"
                                    "min_prob={min_prob})".format(**self.ext))
+        if kl:
+            self.config["outputs"] = "tokens, counts and per-position KL(p || q)"
         if lazy:
             self.config["schedule"] = "position-lazy (rows 1..n+1 per request)"
             self.launches = 2 + 2 * (lb.max_k + 1) + (0 if lb.top128 else 1) + 1
@@ -218,11 +224,11 @@ class LinearWork:
     def call(self, inputs=None):
         lb = self.lb
         t = inputs or self.input_tensors()
-        if self.ext is not None or self.lazy:
+        if self.ext is not None or self.lazy or self.kl is not None:
             self.sv.spec_verify_linear_ext(t["target"], t["draft"], t["draft_tokens"],
                                            t["cu_draft"], t["temperature"], lb.seed,
                                            max_k=lb.max_k, rule=self.rule, workspace=self.ws,
-                                           out=self.outs + (None,), lazy=self.lazy,
+                                           out=self.outs + (None, self.kl), lazy=self.lazy,
                                            **(self.ext or {}))
             return
         self.sv.spec_verify_linear(t["target"], t["draft"], t["draft_tokens"], t["cu_draft"],
@@ -334,10 +340,10 @@ class TreeWork:
         return int(sum(cu[b + 1] - cu[b] - 1 for b in req))
 
 
-def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False):
+def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False):
     if cfg == 4:
         return TreeWork(cfg, dev, input_seed, B)
-    return LinearWork(cfg, dev, input_seed, B, rule, lazy)
+    return LinearWork(cfg, dev, input_seed, B, rule, lazy, kl)
 
 
 def cpu_baseline(work, n_units):
@@ -396,7 +402,7 @@ def main():
     dev = torch.device("cuda", local)
     sv.lib()
     work = make_work(args.config, dev, input_seed=S.INPUT_SEED_BASE + args.config + 7919 * rank,
-                     B=args.B, rule=args.rule, lazy=args.lazy)
+                     B=args.B, rule=args.rule, lazy=args.lazy, kl=args.kl)
 
     for _ in range(max(3, args.warmup)):
         work.call()
@@ -432,7 +438,8 @@ def main():
     traffic = None
     src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "rowpass.cu")
     lazy = getattr(work, "lazy", False)
-    if ROWPASS_TRAFFIC["source_sha1"] == sha1(src) and not lazy:
+    plain = not lazy and getattr(work, "kl", None) is None and getattr(work, "ext", None) is None
+    if ROWPASS_TRAFFIC["source_sha1"] == sha1(src) and plain:
         traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
 
     # end to end through the same API: pinned host inputs copied in, the

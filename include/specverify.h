@@ -173,6 +173,16 @@ int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
  *   out_rank  optional device [R_d] int32: the target rank of every draft
  *             token (every request and rule; also after the first
  *             rejection unless lazy). NULL to skip.
+ *   out_kl    optional device [R_d] f32: KL(p_i || q_i) in nats for every
+ *             draft position of a sampling request, with p and q the laws
+ *             the verifier uses; NaN for greedy requests (and, lazy, after
+ *             position n+1). The distillation signal of "Test-Time
+ *             Speculation" §2 step 3, taken from the same single read: each
+ *             target row is streamed together with its draft row. Needs
+ *             draft logits (SPEC_DRAFT_LOGITS) of the target's dtype, rows
+ *             whose byte length is a multiple of 16, and a rule other than
+ *             SPEC_RULE_STRICT_TOP128 (whose truncated q makes it +inf).
+ *             NULL to skip.
  * The guard and the relaxed coin apply to sampling requests; greedy
  * requests (T < 0.05) keep the greedy rule.
  */
@@ -183,6 +193,7 @@ typedef struct {
   float min_prob;
   int32_t flags;
   int32_t *out_rank;
+  float *out_kl;
 } spec_linear_ext;
 
 /*

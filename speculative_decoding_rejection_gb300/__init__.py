@@ -44,7 +44,7 @@ class SpecLinearExt(ctypes.Structure):
     """spec_linear_ext of include/specverify.h."""
     _fields_ = [("alpha", ctypes.c_float), ("max_rank", ctypes.c_int32),
                 ("min_prob", ctypes.c_float), ("flags", ctypes.c_int32),
-                ("out_rank", ctypes.c_void_p)]
+                ("out_rank", ctypes.c_void_p), ("out_kl", ctypes.c_void_p)]
 
 
 _SIGS = {
@@ -188,12 +188,13 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
                            max_k: int, rule: int = SPEC_RULE_STRICT,
                            draft_kind: int = SPEC_DRAFT_LOGITS, draft_idx=None, alpha=0.0,
                            max_rank=0, min_prob=0.0, lazy=False, want_pq=False,
-                           want_rank=False, workspace=None, out=None, stream=None):
+                           want_rank=False, want_kl=False, workspace=None, out=None,
+                           stream=None):
     """spec_verify_linear with the relaxed CACTUS rule's options and target
     ranks.
 
     Returns (tokens, accepted, pq or None, rank [R_d] int32 or None,
-    workspace).
+    kl [R_d] f32 or None, workspace).
     """
     torch = _torch()
     B = cu_draft.numel() - 1
@@ -208,10 +209,11 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
         accepted = torch.empty(B, dtype=torch.int32, device=dev)
         pq = torch.empty(draft_tokens.numel(), 2, dtype=torch.float32, device=dev) if want_pq else None
         rank = torch.empty(draft_tokens.numel(), dtype=torch.int32, device=dev) if want_rank else None
+        kl = torch.empty(draft_tokens.numel(), dtype=torch.float32, device=dev) if want_kl else None
     else:
-        tokens, accepted, pq, rank = out
+        tokens, accepted, pq, rank, kl = out
     ext = SpecLinearExt(float(alpha), int(max_rank), float(min_prob),
-                        SPEC_EXT_LAZY if lazy else 0, _ptr(rank))
+                        SPEC_EXT_LAZY if lazy else 0, _ptr(rank), _ptr(kl))
     ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
     code = lib().spec_verify_linear_ext(
         _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(draft_idx),
@@ -219,7 +221,7 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
         ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), rule, ctypes.byref(ext), _ptr(tokens),
         _ptr(accepted), _ptr(pq), _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
     _check(code, "spec_verify_linear_ext")
-    return tokens, accepted, pq, rank, ws
+    return tokens, accepted, pq, rank, kl, ws
 
 
 def spec_verify_tree_workspace(B: int, n_nodes: int, V: int, max_depth: int, max_branch: int) -> int:

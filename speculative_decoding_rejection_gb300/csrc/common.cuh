@@ -47,12 +47,16 @@ struct WsHeader {        // first 256 bytes of every workspace
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
-struct RowTask {         // one row streamed by the row pass
+struct RowTask {         // one row (or row pair) streamed by the row pass
   int slot;              // index into the partial-statistics array
   int row;               // row index within its tensor
-  int which;             // 0 = target tensor, 1 = draft tensor
+  int which;             // 0 = target tensor, 1 = draft tensor, 2 = target
+                         // row paired with draft row `drow`
   float c;               // log2(e)/T, 0 for argmax-only rows
+  int dslot, drow;       // pairs: the draft row's slot and index
+  int pad[2];
 };
+constexpr int ROW_PAIR = 2;
 
 struct Part {            // statistics of one chunk of one row
   float m;               // max logit
@@ -179,6 +183,19 @@ __device__ __forceinline__ void merge_stat(float &m, float &S, int &idx, float m
   if (m2 > m || (m2 == m && i2 < idx)) idx = i2;
   m = M;
   S = s;
+}
+
+// merge_stat that also carries A = sum 2^((z - m) c) * w, rescaled with S
+// (an infinite A stays infinite).
+__device__ __forceinline__ void merge_stat_a(float &m, float &S, int &idx, float &A, float m2,
+                                             float S2, int i2, float A2, float c) {
+  const float M = fmaxf(m, m2);
+  const float f1 = ex2((m - M) * c), f2 = ex2((m2 - M) * c);
+  const float a1 = isinf(A) ? A : A * f1, a2 = isinf(A2) ? A2 : A2 * f2;
+  S = S * f1 + S2 * f2;
+  A = a1 + a2;
+  if (m2 > m || (m2 == m && i2 < idx)) idx = i2;
+  m = M;
 }
 
 __device__ __forceinline__ RowStat combine_parts(const Part *p, int n, float c) {

@@ -32,6 +32,10 @@ struct RowPassArgs {
   // draft token's logit (+inf: no count) and every Part's `cnt` receives the
   // number of the chunk's logits strictly above it. NULL: no counting.
   const float *rank_thr;
+  // Optional row pairs (RowTask::which == ROW_PAIR): a target row and its
+  // draft row streamed together; kl_part receives, per target part, A = the
+  // sum of 2^((zt - m) c) (zt - zd) over the chunk. NULL: no pairs.
+  float *kl_part;
   // Residual mode: instead of the row list, stream for every job of `jobs`
   // (count in hdr->n_jobs_a) target row t0+n and draft row d0+n tile by tile
   // (SAMPLE_TILE elements of each, bf16, 16-byte aligned rows) and leave per

@@ -66,10 +66,14 @@ struct LinearArgs {
   int32_t *out_rank;
   // position-lazy schedule: one row pass + decide per position (round)
   int lazy, round;
+  // per-position KL(p || q): target and draft rows streamed as pairs
+  int want_kl;
+  float *kl_part;             // A partials of the pair rows' target slots
+  float *out_kl;
 };
 
 struct LinearLayout {
-  size_t hdr, req, jobs_a, jobs_b, tsum, list, part, tk_idx, tk_prob, rank_thr, total;
+  size_t hdr, req, jobs_a, jobs_b, tsum, list, part, kl_part, tk_idx, tk_prob, rank_thr, total;
   int nch_max, nch_max_lazy;
   long long rows_max;
 };
@@ -93,6 +97,9 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   o += align256(sizeof(Part) * RS_CONS_WARPS *
                 std::max((size_t)L.rows_max * L.nch_max, (size_t)2 * B * L.nch_max_lazy));
   const size_t tk = rule == SPEC_RULE_STRICT_TOP128 ? (size_t)B * max_k * SPEC_TOPK : 0;
+  L.kl_part = o;
+  o += align256(sizeof(float) * RS_CONS_WARPS *
+                std::max((size_t)B * (max_k + 1) * L.nch_max, (size_t)B * L.nch_max_lazy));
   L.tk_idx = o;  o += align256(sizeof(int32_t) * tk);
   L.tk_prob = o; o += align256(sizeof(float) * tk);
   L.rank_thr = o; o += align256(sizeof(float) * (size_t)B * (max_k + 1));
@@ -148,13 +155,24 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
   r.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);
   a.req[b] = r;
   const bool drafts = r.mode == MODE_SAMPLE && a.stream_draft;
+  // with KL, a draft row travels with its target row as one pair entry
+  const bool pairs = drafts && a.want_kl;
   if (a.lazy) {
-    a.list[b] = RowTask{b, r.t0, 0, r.c};
-    a.list[a.B + b] = RowTask{drafts && K > 0 ? a.B + b : -1, r.d0, 1, r.c};
+    if (pairs && K > 0) {
+      a.list[b] = RowTask{b, r.t0, ROW_PAIR, r.c, a.B + b, r.d0};
+      a.list[a.B + b].slot = -1;
+    } else {
+      a.list[b] = RowTask{b, r.t0, 0, r.c};
+      a.list[a.B + b] = RowTask{drafts && K > 0 ? a.B + b : -1, r.d0, 1, r.c};
+    }
   } else {
-    for (int i = 0; i <= K; ++i) a.list[r.t0 + i] = RowTask{r.t0 + i, r.t0 + i, 0, r.c};
+    for (int i = 0; i <= K; ++i)
+      a.list[r.t0 + i] = pairs && i < K
+                             ? RowTask{r.t0 + i, r.t0 + i, ROW_PAIR, r.c, a.rt_max + r.d0 + i, r.d0 + i}
+                             : RowTask{r.t0 + i, r.t0 + i, 0, r.c};
     for (int i = 0; i < K; ++i)
-      a.list[a.rt_max + r.d0 + i] = RowTask{drafts ? a.rt_max + r.d0 + i : -1, r.d0 + i, 1, r.c};
+      a.list[a.rt_max + r.d0 + i] =
+          RowTask{drafts && !pairs ? a.rt_max + r.d0 + i : -1, r.d0 + i, 1, r.c};
   }
   if (a.want_rank) {   // threshold of the rank count: the draft token's target logit
     for (int i = 0; i < K; ++i) {
@@ -195,6 +213,30 @@ __device__ __forceinline__ RowStat target_stat(const LinearArgs &a, int slot, fl
 __device__ __forceinline__ RowStat draft_stat(const LinearArgs &a, int slot, float c, int lane) {
   return warp_row_stat(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS,
                        a.nch_d * RS_CONS_WARPS, c, lane);
+}
+
+// KL(p || q) of a pair row: the target partials merged with their A sums
+// (warp-wide, fixed order), then KL = (A/S - (m_t - m_d))/T - ln S + ln S_d.
+__device__ __forceinline__ float warp_pair_kl(const LinearArgs &a, int tslot_, const RowStat &ds,
+                                              float c, int lane) {
+  const long long base = (long long)tslot_ * a.nch_max * RS_CONS_WARPS;
+  const int n = a.nch_t * RS_CONS_WARPS;
+  float m = NO_MAX, S = 0.f, A = 0.f;
+  int idx = 0x7fffffff;
+  for (int i = lane; i < n; i += 32) {
+    const Part q = a.part[base + i];
+    merge_stat_a(m, S, idx, A, q.m, q.S, q.idx, a.kl_part[base + i], c);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const float A2 = __shfl_xor_sync(0xffffffffu, A, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    merge_stat_a(m, S, idx, A, m2, S2, i2, A2, c);
+  }
+  const float inv_t = c * 0.6931471805599453f;   // 1/T = ln 2 * log2(e)/T
+  return inv_t * (A / S - (m - ds.m)) + logf(ds.S / S);
 }
 
 // q(d) for draft row `row` given its statistics ds (dense logits), the
@@ -300,6 +342,7 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
     // statistics of this block of positions: lane i keeps position base + i
     RowStat ts{NO_MAX, 0.f, 0x7fffffff}, ds{NO_MAX, 0.f, 0x7fffffff};
     int rank = 0;
+    float kl = __int_as_float(0x7fc00000);   // NaN: greedy requests
     for (int i = 0; i < cnt; ++i) {
       const RowStat t = target_stat(a, tslot(a, r, b, base + i), c, lane);
       if (lane == i) ts = t;
@@ -310,8 +353,13 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
       if (sample && a.stream_draft) {
         const RowStat d = draft_stat(a, dslot(a, r, b, base + i), c, lane);
         if (lane == i) ds = d;
+        if (a.want_kl) {
+          const float k = warp_pair_kl(a, tslot(a, r, b, base + i), d, c, lane);
+          if (lane == i) kl = k;
+        }
       }
     }
+    if (a.out_kl && lane < cnt) a.out_kl[r.d0 + base + lane] = kl;
     const int i = base + lane;
     const bool rej = lane < cnt && position_rejects(a, b, r, i, sample, ts, ds, rank);
     const unsigned bal = __ballot_sync(0xffffffffu, rej);
@@ -359,6 +407,11 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
   if (j < K) {
     const int rank = a.want_rank ? 1 + warp_row_count(a, tslot(a, r, b, j), lane) : 0;
     if (sample && a.stream_draft) ds = draft_stat(a, dslot(a, r, b, j), c, lane);
+    if (a.out_kl) {
+      const float kl = sample && a.stream_draft ? warp_pair_kl(a, tslot(a, r, b, j), ds, c, lane)
+                                                : __int_as_float(0x7fc00000);
+      if (lane == 0) a.out_kl[r.d0 + j] = kl;
+    }
     // a sparse draft's q(d): the warp searches the row's 128 ids together
     float qs = -1.f;
     if (sample && a.sparse) {
@@ -376,9 +429,14 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
         0xffffffffu, lane == 0 && position_rejects(a, b, r, j, sample, ts, ds, rank, qs), 0);
     if (!rej) {   // accepted: list the next position's rows
       if (lane == 0) {
-        a.list[b] = RowTask{b, r.t0 + j + 1, 0, c};
         const bool drow = sample && a.stream_draft && j + 1 < K;
-        a.list[a.B + b] = RowTask{drow ? a.B + b : -1, r.d0 + j + 1, 1, c};
+        if (drow && a.want_kl) {
+          a.list[b] = RowTask{b, r.t0 + j + 1, ROW_PAIR, c, a.B + b, r.d0 + j + 1};
+          a.list[a.B + b].slot = -1;
+        } else {
+          a.list[b] = RowTask{b, r.t0 + j + 1, 0, c};
+          a.list[a.B + b] = RowTask{drow ? a.B + b : -1, r.d0 + j + 1, 1, c};
+        }
       }
       return;
     }
@@ -392,6 +450,7 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
       a.out_pq[2LL * (r.d0 + i) + 1] = __int_as_float(0x7fc00000);
     }
     if (a.out_rank) a.out_rank[r.d0 + i] = -1;
+    if (a.out_kl) a.out_kl[r.d0 + i] = __int_as_float(0x7fc00000);
   }
   if (lane == 0) {
     a.list[b].slot = -1;
@@ -842,7 +901,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   if (ext != nullptr &&
       (!(ext->alpha >= 0.f) || !isfinite(ext->alpha) || ext->max_rank < 0 ||
        !(ext->min_prob >= 0.f) || !isfinite(ext->min_prob) ||
-       (ext->flags & ~SPEC_EXT_LAZY) != 0 ||
+       (ext->flags & ~SPEC_EXT_LAZY) != 0 || !aligned(ext->out_kl, 4) ||
        !aligned(ext->out_rank, 4)))
     return SPEC_ERR_INVALID_ARG;
   if (dk == SPEC_DRAFT_SPARSE128 && (ddt != SPEC_F32 || draft_idx == nullptr || draft == nullptr))
@@ -889,7 +948,14 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.d_row_bytes = dk == SPEC_DRAFT_SPARSE128 ? (long long)SPEC_TOPK * 4
                                              : (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
   const bool lazy = ext && (ext->flags & SPEC_EXT_LAZY);
-  a.chunk_bytes = lazy ? LAZY_CHUNK_BYTES : CHUNK_BYTES;
+  const bool want_kl = ext && ext->out_kl != nullptr;
+  if (want_kl && (dk != SPEC_DRAFT_LOGITS || rule == SPEC_RULE_STRICT_TOP128 || tdt != ddt ||
+                  ((long long)V * (tdt == SPEC_BF16 ? 2 : 4)) % 16 != 0))
+    return SPEC_ERR_INVALID_ARG;
+  // pairs split each row into chunks of 32768 elements (the slots' chunk
+  // capacity); lazy rounds keep their finer chunks
+  a.chunk_bytes = lazy ? LAZY_CHUNK_BYTES
+                       : want_kl ? 32768 * (tdt == SPEC_BF16 ? 2 : 4) : CHUNK_BYTES;
   a.nch_t = nchunks(V, tdt, a.chunk_bytes);
   a.nch_d = nchunks(V, ddt, a.chunk_bytes);
   a.nch_max = lazy ? L.nch_max_lazy : L.nch_max;
@@ -902,6 +968,9 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.out_rank = ext ? ext->out_rank : nullptr;
   a.want_rank = a.out_rank != nullptr || (rule == SPEC_RULE_CACTUS && a.max_rank > 0);
   a.lazy = ext && (ext->flags & SPEC_EXT_LAZY) ? 1 : 0;
+  a.want_kl = want_kl ? 1 : 0;
+  a.out_kl = want_kl ? ext->out_kl : nullptr;
+  a.kl_part = reinterpret_cast<float *>(ws + L.kl_part);
   a.round = 0;
   a.rank_thr = reinterpret_cast<float *>(ws + L.rank_thr);
   if (dk == SPEC_DRAFT_SPARSE128) {
@@ -941,6 +1010,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   rp.hdr = a.hdr;
   rp.part = a.part;
   rp.rank_thr = a.want_rank ? a.rank_thr : nullptr;
+  rp.kl_part = a.want_kl ? a.kl_part : nullptr;
   rp.residual = 0;
   rp.jobs = nullptr;
   rp.req = nullptr;

@@ -242,11 +242,73 @@ __device__ __forceinline__ float consume_res_partial(const unsigned char *buf, i
   return s;
 }
 
+// Row pairs (KL mode): running statistics of a target row and its draft row
+// over the same elements, plus A = sum 2^((zt - mt) c) (zt - zd) relative to
+// the running target max: with the row totals it gives KL(p || q) ("Test-Time
+// Speculation", §2 step 3) without a second read.
+struct PairState {
+  float mt, St, A;
+  int idx, cnt;
+  float md, Sd;
+};
+
+template <bool BF16, bool RANK>
+__device__ __forceinline__ void consume_pair_vec(const uint4 wt, const uint4 wd, int e, float c,
+                                                 PairState &ps, float thr) {
+  constexpr int N = BF16 ? 8 : 4;
+  float xt[N], xd[N];
+  const uint32_t ut[4] = {wt.x, wt.y, wt.z, wt.w}, ud[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (BF16) {
+      xt[2 * q] = bf16lo(ut[q]); xt[2 * q + 1] = bf16hi(ut[q]);
+      xd[2 * q] = bf16lo(ud[q]); xd[2 * q + 1] = bf16hi(ud[q]);
+    } else {
+      xt[q] = __uint_as_float(ut[q]);
+      xd[q] = __uint_as_float(ud[q]);
+    }
+  }
+  float vmt = xt[0], vmd = xd[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) {
+    vmt = fmaxf(vmt, xt[k]);
+    vmd = fmaxf(vmd, xd[k]);
+  }
+  if (RANK) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) ps.cnt += xt[k] > thr;
+  }
+  if (vmt > ps.mt) {
+    int j = N - 1;
+#pragma unroll
+    for (int k = N - 2; k >= 0; --k)
+      if (xt[k] == vmt) j = k;
+    const float f = ex2((ps.mt - vmt) * c);
+    ps.St *= f;
+    if (!isinf(ps.A)) ps.A *= f;
+    ps.mt = vmt;
+    ps.idx = e + j;
+  }
+  if (vmd > ps.md) {
+    ps.Sd *= ex2((ps.md - vmd) * c);
+    ps.md = vmd;
+  }
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const float et = ex2((xt[k] - ps.mt) * c);
+    ps.St += et;
+    ps.Sd += ex2((xd[k] - ps.md) * c);
+    // zt - zd; -inf on both sides (NaN) or on the target side weighs 0
+    if (et > 0.f) ps.A += et * fmaxf(xt[k] - xd[k], NO_MAX);
+  }
+}
+
 // The rank count needs a few more registers than 6 CTAs per SM leave.
 constexpr int RS_RANK_CTAS_PER_SM = 4;
 
-template <bool RANK>
-__global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM)
+template <bool RANK, bool PAIR>
+__global__ void __launch_bounds__(RS_THREADS,
+                                  RANK || PAIR ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM)
     k_row_pass(const RowPassArgs a) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ RowPassSmem sh;
@@ -313,7 +375,41 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
       const int chunk = (int)(item % a.nch_max);
       const RowTask t = a.list[entry];
       const int w = t.which;
-      const float thr = RANK && w == 0 && t.slot >= 0 ? a.rank_thr[t.row] : INFINITY;
+      const float thr = RANK && w != 1 && t.slot >= 0 ? a.rank_thr[t.row] : INFINITY;
+      if (PAIR && w == ROW_PAIR) {
+        // target row and draft row side by side: each stage holds up to
+        // TILE_BYTES/2 of both (same dtype, 16-byte aligned rows)
+        if (t.slot >= 0 && chunk < a.nch[0]) {
+          const long long rbytes = a.row_bytes[0];
+          const int esz = dtype_size(a.dtype[0]);
+          const uint64_t trow = (uint64_t)(a.base[0] + (long long)t.row * rbytes);
+          const uint64_t drow = (uint64_t)(a.base[1] + (long long)t.drow * rbytes);
+          const uint64_t off0 = (uint64_t)chunk * a.chunk_bytes;
+          const uint64_t off1 = min((uint64_t)rbytes, off0 + (uint64_t)a.chunk_bytes);
+          const int ntile = (int)((off1 - off0 + TILE_BYTES / 2 - 1) / (TILE_BYTES / 2));
+          for (int tl = 0; tl < ntile && ok; ++tl) {
+            const int s = (int)(it % NSTAGE);
+            const long long use = it / NSTAGE;
+            if (use > 0 && !mbar_wait_bounded(&sh.empty[s], (uint32_t)((use - 1) & 1), abort)) {
+              ok = false;
+              break;
+            }
+            const uint64_t off = off0 + (uint64_t)tl * (TILE_BYTES / 2);
+            const uint32_t nb = (uint32_t)min((uint64_t)(TILE_BYTES / 2), off1 - off);
+            sh.m0[s] = make_int4(t.slot, chunk, (int)(off / esz),
+                                 (int)(nb / 16) | ((tl == ntile - 1) << 12) | (1 << 15));
+            sh.m1[s] = make_int4(__float_as_int(t.c), t.row, t.dslot, 0);
+            if (RANK) sh.thr[s] = thr;
+            mbar_arrive_tx(&sh.full[s], 2 * nb);
+            unsigned char *dst = stage_buf + (size_t)s * TILE_BYTES;
+            bulk_g2s(dst, (const void *)(trow + off), nb, &sh.full[s]);
+            bulk_g2s(dst + TILE_BYTES / 2, (const void *)(drow + off), nb, &sh.full[s]);
+            ++it;
+          }
+        }
+        item = next;
+        continue;
+      }
       const long long rbytes = w ? a.row_bytes[1] : a.row_bytes[0];
       if (t.slot >= 0 && chunk < (w ? a.nch[1] : a.nch[0])) {
         const int esz = dtype_size(w ? a.dtype[1] : a.dtype[0]);
@@ -376,6 +472,7 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
   const int cw = warp - 1;
   const int ctid = threadIdx.x - 32;
   RunState st{NO_MAX, pk2(0.f, 0.f), 0x7fffffff, 0, 0u};
+  PairState ps{NO_MAX, 0.f, 0.f, 0x7fffffff, 0, NO_MAX, 0.f};
   int res_job = -1;
   ResLaw res_law{0.f, 0.f, 0.f, 0.f, 0.f};
   for (long long it = 0;; ++it) {
@@ -404,6 +501,48 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
       if (lane == 0) a.tsum4[((long long)ja * a.ntiles + j) * RS_CONS_WARPS + cw] = rs;
+      continue;
+    }
+    if (PAIR && (m0.w & (1 << 15))) {   // target row + draft row
+      const int nvp = m0.w & 0xfff;
+      const float c = __int_as_float(m1.x);
+      const float thr = RANK ? sh.thr[s] : INFINITY;
+      const unsigned char *buf = stage_buf + (size_t)s * TILE_BYTES;
+      if (a.dtype[0] == SPEC_BF16) {
+        for (int v = ctid; v < nvp; v += NCT)
+          consume_pair_vec<true, RANK>(lds128(buf + 16 * v), lds128(buf + TILE_BYTES / 2 + 16 * v),
+                                       m0.z + 8 * v, c, ps, thr);
+      } else {
+        for (int v = ctid; v < nvp; v += NCT)
+          consume_pair_vec<false, RANK>(lds128(buf + 16 * v), lds128(buf + TILE_BYTES / 2 + 16 * v),
+                                        m0.z + 4 * v, c, ps, thr);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[s]);
+      if ((m0.w >> 12) & 1) {   // end of the chunk: merge the warp, write both rows
+        float m = ps.mt, S = ps.St, A = ps.A, md = ps.md, Sd = ps.Sd;
+        int idx = ps.idx, cnt = ps.cnt, nid = 0x7fffffff;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+          const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+          const float A2 = __shfl_xor_sync(0xffffffffu, A, o);
+          const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+          merge_stat_a(m, S, idx, A, m2, S2, i2, A2, c);
+          const float md2 = __shfl_xor_sync(0xffffffffu, md, o);
+          const float Sd2 = __shfl_xor_sync(0xffffffffu, Sd, o);
+          merge_stat(md, Sd, nid, md2, Sd2, 0x7fffffff, c);
+          cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        }
+        if (lane == 0) {
+          const long long k = ((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS + cw;
+          a.part[k] = Part{m, S, idx, cnt};
+          a.part[((long long)m1.z * a.nch_max + m0.y) * RS_CONS_WARPS + cw] =
+              Part{md, Sd, 0x7fffffff, 0};
+          a.kl_part[k] = A;
+        }
+        ps = PairState{NO_MAX, 0.f, 0.f, 0x7fffffff, 0, NO_MAX, 0.f};
+      }
       continue;
     }
     const int nvec = m0.w & 0xfff;
@@ -512,14 +651,17 @@ int launch_row_pass(const RowPassArgs &a, cudaStream_t stream) {
   if (sms <= 0) return SPEC_ERR_CUDA;
   const size_t smem = (size_t)NSTAGE * TILE_BYTES;
   const bool rank = a.rank_thr != nullptr && !a.residual;
-  auto kern = rank ? k_row_pass<true> : k_row_pass<false>;
+  const bool pair = a.kl_part != nullptr && !a.residual;
+  auto kern = rank ? (pair ? k_row_pass<true, true> : k_row_pass<true, false>)
+                   : (pair ? k_row_pass<false, true> : k_row_pass<false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;
   cudaEvent_t before = prof_before, after = prof_after;
   prof_before = prof_after = nullptr;
   if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  kern<<<(rank ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM) * sms, RS_THREADS, smem, stream>>>(a);
+  kern<<<(rank || pair ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM) * sms, RS_THREADS, smem,
+         stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;

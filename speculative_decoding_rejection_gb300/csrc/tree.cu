@@ -651,6 +651,7 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   RowPassArgs rp;
   rp.rank_thr = nullptr;
+  rp.kl_part = nullptr;
   rp.base[0] = a.target;
   rp.base[1] = a.draft;
   rp.row_bytes[0] = a.t_row_bytes;

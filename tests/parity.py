@@ -4,6 +4,8 @@ Tolerances: committed tokens and accepted counts bit-exact, except from the
 first output slot whose draw the oracle flags as within 1e-6 of a decision
 boundary; probabilities within 1e-5 relative (fp32 GPU vs fp64 oracle).
 """
+import math
+
 import numpy as np
 import torch
 
@@ -15,26 +17,28 @@ PROB_ATOL = 1e-30
 
 
 def gpu_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, draft=None,
-               draft_idx=None, ext=None, lazy=False):
+               draft_idx=None, ext=None, lazy=False, kl=False):
     """Runs the CUDA verifier; `ext` (a dict of alpha / max_rank / min_prob)
     or `lazy` goes through spec_verify_linear_ext, which also returns target
     ranks."""
     draft = lb.draft if draft is None else draft
-    if ext is None and not lazy:
+    if ext is None and not lazy and not kl:
         tokens, acc, pq, ws = sv.spec_verify_linear(
             lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
             max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx, want_pq=True)
         rank = None
     else:
-        tokens, acc, pq, rank, ws = sv.spec_verify_linear_ext(
+        tokens, acc, pq, rank, klv, ws = sv.spec_verify_linear_ext(
             lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
             max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx,
-            want_pq=True, want_rank=True, lazy=lazy, **(ext or {}))
+            want_pq=True, want_rank=True, want_kl=kl, lazy=lazy, **(ext or {}))
     status = sv.spec_get_status(ws)
     out = dict(tokens=tokens.cpu().numpy(), accepted=acc.cpu().numpy(),
                pq=pq.cpu().numpy().astype(np.float64), status=status)
     if rank is not None:
         out["rank"] = rank.cpu().numpy().astype(np.int64)
+    if kl:
+        out["kl"] = klv.cpu().numpy().astype(np.float64)
     return out
 
 
@@ -83,6 +87,36 @@ def assert_linear_parity(gpu, ref, cu_draft, min_compared=1):
                                    ref["rank"][rows][bad][:5])
     assert n_full >= min_compared
     return n_full, n_flag
+
+
+# KL(p || q) = (A/S - (m_t - m_d))/T - ln S_t + ln S_d from fp32 sums: each
+# term is bounded by (max|z_t| + max|z_d|)/T or by ln V, and fp32 sums over a
+# row carry ~1e-7 relative error (measured: at most 4e-8 of the scale), so
+# the bound is KL_RTOL of that scale.
+KL_RTOL = 1e-6
+
+
+def assert_kl_close(g_kl, ref, lb, rows):
+    """KL per draft row `rows`: NaN exactly where the oracle has NaN, +inf
+    where it has +inf, else within KL_RTOL * (1 + R/T + ln V)."""
+    o = ref["kl"][rows]
+    g = g_kl[rows]
+    assert np.array_equal(np.isnan(g), np.isnan(o)), ("kl NaN pattern", rows[np.isnan(g) != np.isnan(o)][:5])
+    assert np.array_equal(np.isinf(g), np.isinf(o))
+    ok = np.isfinite(o)
+    if not ok.any():
+        return 0.0
+    cu = lb.cu_draft.cpu().numpy()
+    req = np.searchsorted(cu, rows, side="right") - 1
+    t_rows = rows + req
+    T = lb.temperature.cpu().numpy()[req]
+    zt = lb.target.float()[torch.as_tensor(t_rows, device=lb.target.device)]
+    zd = lb.draft.float()[torch.as_tensor(rows, device=lb.draft.device)]
+    R = (zt.abs().amax(1) + zd.abs().amax(1)).cpu().numpy().astype(np.float64)
+    scale = 1.0 + R / np.maximum(T, 1e-30) + math.log(lb.V)
+    err = np.abs(g[ok] - o[ok]) / scale[ok]
+    assert err.max() <= KL_RTOL, ("kl", float(err.max()), rows[ok][np.argmax(err)])
+    return float(err.max())
 
 
 def sample_requests(B, n, seed=0):

@@ -338,3 +338,66 @@ def test_lazy_never_reads_rows_after_the_first_rejection():
     assert_lazy_matches(g, ref, lb)
     e = gpu_linear(lb2)
     assert e["status"] == sv.SPEC_ERR_INVALID_ARG
+
+
+# ------------------------------------------------- per-position KL(p || q)
+from parity import assert_kl_close  # noqa: E402
+
+
+@pytest.mark.parametrize("dtype,V,over", [
+    ("bf16", 32000, dict(cfg=2, B=40, K=(0, 6), T=[0.0, 0.4, 0.8, 1.0, 1.7] * 8)),
+    ("f32", 1024, dict(cfg=1, B=12, K=5, T=1.0)),
+    ("bf16", 200000, dict(cfg=2, B=10, K=(1, 4), T=[0.6, 1.2] * 5)),
+])
+def test_kl_per_position_eager(dtype, V, over):
+    cfg = over.pop("cfg")
+    lb = S.make_linear(cfg, device=DEV, V=V, dtype=dtype, sigma=0.8, input_seed=77 + V, **over)
+    g = gpu_linear(lb, kl=True)
+    assert g["status"] == sv.SPEC_OK
+    r = oracle_linear(lb)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=8)
+    rows = np.arange(int(lb.cu_draft[-1]))
+    print("kl err / scale", assert_kl_close(g["kl"], r, lb, rows))
+
+
+def test_kl_with_cactus_rank_and_lazy_rounds():
+    lb = S.make_linear(2, device=DEV, B=24, K=(1, 6), V=65536, sigma=1.0,
+                       T=[0.0, 0.7, 1.0, 1.3] * 6, input_seed=321)
+    ext = dict(alpha=0.3, max_rank=5, min_prob=0.01)
+    g = gpu_linear(lb, rule=sv.SPEC_RULE_CACTUS, ext=ext, kl=True)
+    r = oracle_linear(lb, rule=sv.SPEC_RULE_CACTUS, ext=ext)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=18)
+    assert_kl_close(g["kl"], r, lb, np.arange(int(lb.cu_draft[-1])))
+    gl = gpu_linear(lb, rule=sv.SPEC_RULE_CACTUS, ext=ext, kl=True, lazy=True)
+    lz = O.lazy_view(r, lb.cu_draft.cpu().numpy())
+    assert_linear_parity(gl, lz, lb.cu_draft.cpu(), min_compared=18)
+    assert_kl_close(gl["kl"], lz, lb, np.arange(int(lb.cu_draft[-1])))
+
+
+def test_kl_full_size_workload5_sampled():
+    lb = S.make_linear(5, device=DEV)
+    g = gpu_linear(lb, kl=True)
+    assert g["status"] == sv.SPEC_OK
+    req = sample_requests(lb.B, 12, seed=8)
+    r = oracle_linear(lb, requests=req)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=9)
+    cu = lb.cu_draft.cpu().numpy()
+    rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in req])
+    assert_kl_close(g["kl"], r, lb, rows)
+
+
+def test_kl_argument_errors():
+    lb = S.make_linear(1, device=DEV, B=2, K=2, V=64, input_seed=3)
+    probs = probs_from_logits(lb.draft, lb.cu_draft, lb.temperature)
+    with pytest.raises(sv.SpecError):   # q given as probabilities
+        sv.spec_verify_linear_ext(lb.target, probs, lb.draft_tokens, lb.cu_draft,
+                                  lb.temperature, 1, max_k=lb.max_k,
+                                  draft_kind=sv.SPEC_DRAFT_PROBS, want_kl=True)
+    with pytest.raises(sv.SpecError):   # truncated draft law
+        sv.spec_verify_linear_ext(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
+                                  lb.temperature, 1, max_k=lb.max_k,
+                                  rule=sv.SPEC_RULE_STRICT_TOP128, want_kl=True)
+    odd = S.make_linear(1, device=DEV, B=2, K=2, V=5003, dtype="bf16", input_seed=3)
+    with pytest.raises(sv.SpecError):   # rows not 16-byte multiples
+        sv.spec_verify_linear_ext(odd.target, odd.draft, odd.draft_tokens, odd.cu_draft,
+                                  odd.temperature, 1, max_k=odd.max_k, want_kl=True)
