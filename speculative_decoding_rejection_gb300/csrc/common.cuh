@@ -14,6 +14,9 @@ constexpr int TILE_BYTES = 16384;   // one TMA bulk copy = one pipeline stage
 // more CTAs.
 constexpr int LAZY_CHUNK_BYTES = 32768;
 constexpr int CHUNK_BYTES = 131072; // one unit of dynamic work in the row pass
+// The streaming verifier's unit of work: one completion count per chunk, and
+// a position's rows still spread over a dozen CTAs.
+constexpr int STREAM_CHUNK_BYTES = 65536;
 // Row pass shape, chosen by measurement on GB300: six CTAs per SM, each one
 // producer lane and four consumer warps over a two-stage ring of 16 KB TMA
 // copies (192 KB of copies in flight per SM); a consumer thread takes eight
@@ -43,7 +46,12 @@ struct WsHeader {        // first 256 bytes of every workspace
   int n_jobs_a;          // final draws over full residual rows (dense drafts)
   int n_jobs_b;          // final draws located from chunk statistics
   unsigned int work2;    // dynamic work counter of the residual tile sums
-  int pad[57];
+  int n_done;            // streaming verifier: requests whose final token is written
+  unsigned long long work_s;   // streaming verifier: tickets of the static entries
+  unsigned long long work_d;   // streaming verifier: tickets of the dynamic entries
+  int n_alloc_d;         // streaming verifier: dynamic entries allocated
+  int setup_bad;         // streaming verifier: the setup rejected a request
+  int pad[50];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -85,6 +93,13 @@ struct Job {         // one final draw of a sampling request (accept kernel)
 };
 
 struct RowStat { float m, S; int idx; };
+
+// A chunk partial read through L2 only: in the streaming verifier it was
+// written by another CTA of the same running kernel.
+__device__ __forceinline__ Part ldcg_part(const Part *p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
+  return Part{__int_as_float(v.x), __int_as_float(v.y), v.z, v.w};
+}
 
 // Running maximum before any element: finite, so (x - m) never forms inf - inf.
 // A row whose statistics keep this value holds no finite logit.
@@ -211,7 +226,7 @@ __device__ __forceinline__ RowStat warp_row_stat(const Part *p, int n, float c, 
   float m = NO_MAX, S = 0.f;
   int idx = 0x7fffffff;
   for (int i = lane; i < n; i += 32) {
-    const Part q = p[i];
+    const Part q = ldcg_part(p + i);
     merge_stat(m, S, idx, q.m, q.S, q.idx, c);
   }
 #pragma unroll

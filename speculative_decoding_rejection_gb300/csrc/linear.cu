@@ -24,56 +24,13 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "linear.cuh"
 
 namespace sv {
 
-constexpr int ACCEPT_WARPS = 8;
-
-struct LinearArgs {
-  const char *target;
-  const char *draft;
-  int tdt, ddt, dk, rule;
-  const int32_t *draft_idx;   // sparse ids (caller's, or the top-128 scratch)
-  const float *sparse_prob;   // sparse probabilities (caller's or scratch)
-  const int32_t *tokens;
-  const int32_t *cu;
-  const float *temp;
-  int B, V, max_k;
-  uint64_t seed;
-  int32_t *out_tokens;
-  int32_t *out_accepted;
-  float *out_pq;
-  WsHeader *hdr;
-  ReqInfo *req;
-  Job *jobs_a;                // residual draws over dense draft rows
-  Job *jobs_b;                // bonus draws and sparse residual draws
-  float *tsum;                // [B][ntiles][RS_CONS_WARPS] residual tile sums of jobs_a
-  int ntiles;
-  long long rows_max;
-  RowTask *list;
-  Part *part;
-  long long t_row_bytes, d_row_bytes;
-  int nch_t, nch_d, nch_max;   // chunks of the mode's chunk size
-  int chunk_bytes;
-  int rt_max;                 // slot offset of draft rows
-  int sparse;                 // the draft law is sparse (given or top-128)
-  int stream_draft;           // the row pass reads dense draft logits
-  // relaxed rule and target ranks
-  float alpha, min_prob;
-  int max_rank;
-  int want_rank;              // the row pass counts ranks
-  float *rank_thr;            // [rt_max] draft token's target logit per slot
-  int32_t *out_rank;
-  // position-lazy schedule: one row pass + decide per position (round)
-  int lazy, round;
-  // per-position KL(p || q): target and draft rows streamed as pairs
-  int want_kl;
-  float *kl_part;             // A partials of the pair rows' target slots
-  float *out_kl;
-};
-
 struct LinearLayout {
-  size_t hdr, req, jobs_a, jobs_b, tsum, list, part, kl_part, tk_idx, tk_prob, rank_thr, total;
+  size_t hdr, err, req, jobs_a, jobs_b, tsum, list, part, kl_part, tk_idx, tk_prob, rank_thr;
+  size_t ent_s, ent_d, ready_d, rs, zd_at, total;
   int nch_max, nch_max_lazy;
   long long rows_max;
 };
@@ -85,6 +42,7 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   L.rows_max = (long long)B * (2LL * max_k + 1);
   size_t o = 0;
   L.hdr = o;  o += align256(sizeof(WsHeader));
+  L.err = o;  o += align256(sizeof(WsHeader));   // errors found by the streaming verifier
   L.req = o;  o += align256(sizeof(ReqInfo) * (size_t)B);
   L.jobs_a = o; o += align256(sizeof(Job) * (size_t)B);
   L.jobs_b = o; o += align256(sizeof(Job) * (size_t)B);
@@ -103,6 +61,14 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   L.tk_idx = o;  o += align256(sizeof(int32_t) * tk);
   L.tk_prob = o; o += align256(sizeof(float) * tk);
   L.rank_thr = o; o += align256(sizeof(float) * (size_t)B * (max_k + 1));
+  // streaming verifier: static and dynamic entries (32 B), ready flags,
+  // per-request progress (16 B)
+  const size_t cap_d = (size_t)B * (max_k + 1);
+  L.ent_s = o; o += align256(32 * (size_t)B);
+  L.ent_d = o; o += align256(32 * cap_d);
+  L.ready_d = o; o += align256(sizeof(int) * cap_d);
+  L.rs = o; o += align256(16 * (size_t)B);
+  L.zd_at = o; o += align256(sizeof(float) * (size_t)B * max_k);
   L.total = o;
   return L;
 }
@@ -133,26 +99,11 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
     a.list[a.B + b].slot = -1;
   }
   ReqInfo r;
-  const int K = a.cu[b + 1] - a.cu[b];
-  const float T = a.temp[b];
-  r.t0 = a.cu[b] + b;
-  r.d0 = a.cu[b];
-  r.K = K;
-  r.n = 0;
-  r.pad[0] = r.pad[1] = 0;
-  const bool greedy = a.rule == SPEC_RULE_GREEDY || T < SPEC_GREEDY_T;
-  bool ok = (b > 0 || a.cu[0] == 0) && K >= 0 && K <= a.max_k && a.cu[b] >= 0 &&
-            (long long)a.cu[b + 1] <= dmax && T >= 0.f && isfinite(T);
-  if (ok && !greedy && a.draft == nullptr) ok = false;
-  if (!ok) {
-    set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-    r.mode = MODE_SKIP;
-    r.c = 0.f;
+  if (!load_request(a, b, r)) {
     a.req[b] = r;
     return;
   }
-  r.mode = greedy ? MODE_GREEDY : MODE_SAMPLE;
-  r.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);
+  const int K = r.K;
   a.req[b] = r;
   const bool drafts = r.mode == MODE_SAMPLE && a.stream_draft;
   // with KL, a draft row travels with its target row as one pair entry
@@ -183,140 +134,6 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
               : INFINITY;   // reported by the accept scan
     }
     a.rank_thr[r.t0 + K] = INFINITY;
-  }
-}
-
-// ------------------------------------------------------------ accept scan
-// Part slots of position i's rows of request b: eager, one per listed row;
-// lazy, entries b and B + b of the current round.
-__device__ __forceinline__ int tslot(const LinearArgs &a, const ReqInfo &r, int b, int i) {
-  return a.lazy ? b : r.t0 + i;
-}
-__device__ __forceinline__ int dslot(const LinearArgs &a, const ReqInfo &r, int b, int i) {
-  return a.lazy ? a.B + b : a.rt_max + r.d0 + i;
-}
-
-// Rank count of a target row: the sum of the chunk partials' counts.
-__device__ __forceinline__ int warp_row_count(const LinearArgs &a, int slot, int lane) {
-  const Part *p = a.part + (long long)slot * a.nch_max * RS_CONS_WARPS;
-  const int n = a.nch_t * RS_CONS_WARPS;
-  int c = 0;
-  for (int i = lane; i < n; i += 32) c += p[i].cnt;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  return c;
-}
-__device__ __forceinline__ RowStat target_stat(const LinearArgs &a, int slot, float c, int lane) {
-  return warp_row_stat(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS,
-                       a.nch_t * RS_CONS_WARPS, c, lane);
-}
-__device__ __forceinline__ RowStat draft_stat(const LinearArgs &a, int slot, float c, int lane) {
-  return warp_row_stat(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS,
-                       a.nch_d * RS_CONS_WARPS, c, lane);
-}
-
-// KL(p || q) of a pair row: the target partials merged with their A sums
-// (warp-wide, fixed order), then KL = (A/S - (m_t - m_d))/T - ln S + ln S_d.
-__device__ __forceinline__ float warp_pair_kl(const LinearArgs &a, int tslot_, const RowStat &ds,
-                                              float c, int lane) {
-  const long long base = (long long)tslot_ * a.nch_max * RS_CONS_WARPS;
-  const int n = a.nch_t * RS_CONS_WARPS;
-  float m = NO_MAX, S = 0.f, A = 0.f;
-  int idx = 0x7fffffff;
-  for (int i = lane; i < n; i += 32) {
-    const Part q = a.part[base + i];
-    merge_stat_a(m, S, idx, A, q.m, q.S, q.idx, a.kl_part[base + i], c);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
-    const float A2 = __shfl_xor_sync(0xffffffffu, A, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-    merge_stat_a(m, S, idx, A, m2, S2, i2, A2, c);
-  }
-  const float inv_t = c * 0.6931471805599453f;   // 1/T = ln 2 * log2(e)/T
-  return inv_t * (A / S - (m - ds.m)) + logf(ds.S / S);
-}
-
-// q(d) for draft row `row` given its statistics ds (dense logits), the
-// probability itself, or a search of the sparse ids (any order).
-__device__ float draft_prob_at(const LinearArgs &a, int row, int d, float c, RowStat ds) {
-  if (a.sparse) {
-    const int32_t *ids = a.draft_idx + (long long)row * SPEC_TOPK;
-    const float *pr = a.sparse_prob + (long long)row * SPEC_TOPK;
-    for (int k = 0; k < SPEC_TOPK; ++k)
-      if (ids[k] == d) return pr[k];
-    return 0.f;
-  }
-  const char *drow = a.draft + (long long)row * a.d_row_bytes;
-  if (a.dk == SPEC_DRAFT_PROBS) return load_elem(drow, a.ddt, d);
-  if (row_empty(ds.m)) return 0.f;
-  return ex2((load_elem(drow, a.ddt, d) - ds.m) * c) / ds.S;
-}
-
-// Decision on draft position i (0-based) of request b from the statistics of
-// its target row (ts) and dense draft row (ds) and its target rank: greedy
-// prefix match, the lossless coin, or the CACTUS guard and coin. Writes
-// p(d), q(d) and the rank. Returns true when the draft is rejected.
-__device__ bool position_rejects(const LinearArgs &a, int b, const ReqInfo &r, int i, bool sample,
-                                 const RowStat &ts, const RowStat &ds, int rank,
-                                 float q_given = -1.f) {
-  const float c = r.c;
-  const int d = a.tokens[r.d0 + i];
-  const bool dok = (unsigned)d < (unsigned)a.V;
-  if (!dok) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-  if (row_empty(ts.m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-  float pd, qd;
-  bool rej;
-  if (!sample) {
-    rej = !(dok && d == ts.idx);
-    pd = rej ? 0.f : 1.f;
-    qd = -1.f;
-  } else if (dok && !row_empty(ts.m)) {
-    const char *trow = a.target + (long long)(r.t0 + i) * a.t_row_bytes;
-    pd = ex2((load_elem(trow, a.tdt, d) - ts.m) * c) / ts.S;
-    qd = q_given >= 0.f ? q_given : draft_prob_at(a, r.d0 + i, d, c, ds);
-    if (a.rule == SPEC_RULE_CACTUS) {
-      const float g = fminf(pd + sqrtf(2.f * a.alpha * pd * (1.f - pd)), 1.f);
-      const float acc = qd <= g ? 1.f : g / qd;
-      const bool guard = (a.max_rank > 0 && rank > a.max_rank) || pd < a.min_prob;
-      rej = guard || !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
-    } else {
-      const float acc = qd <= pd ? 1.f : pd / qd;
-      rej = !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
-    }
-  } else {
-    pd = 0.f;
-    qd = 0.f;
-    rej = true;
-  }
-  if (a.out_pq) {
-    a.out_pq[2LL * (r.d0 + i)] = pd;
-    a.out_pq[2LL * (r.d0 + i) + 1] = qd;
-  }
-  if (a.out_rank) a.out_rank[r.d0 + i] = rank;
-  return rej;
-}
-
-// n drafts accepted: write them and queue the final token (greedy: the
-// argmax of p_{n+1}; sampling: a residual job when n < K, else a bonus job).
-// tf / df are the statistics of target row n+1 and dense draft row n+1.
-__device__ void finish_request(const LinearArgs &a, int b, const ReqInfo &r, int n, bool sample,
-                               const RowStat &tf, const RowStat &df, int lane) {
-  const int W = a.max_k + 1;
-  int32_t *out = a.out_tokens + (long long)b * W;
-  for (int j = lane; j < W; j += 32) out[j] = j < n ? a.tokens[r.d0 + j] : -1;
-  __syncwarp();
-  if (lane == 0) {
-    a.out_accepted[b] = n;
-    if (!sample) {
-      out[n] = tf.idx;
-    } else {
-      const Job j{b, n, n < r.K ? 1 : 2, 0, tf.m, tf.S, df.m, df.S};
-      if (j.kind == 1 && !a.sparse) a.jobs_a[atomicAdd(&a.hdr->n_jobs_a, 1)] = j;
-      else a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = j;
-    }
   }
 }
 
@@ -535,31 +352,6 @@ __device__ __forceinline__ float block_sum(float v, SampleSmem &sh) {
   const float t = sh.scratch[32];
   __syncthreads();
   return t;
-}
-
-struct JobRows {
-  const char *trow, *drow;
-  bool tvec, dvec;
-  float c, mt, invSt, md, invSd;
-};
-
-__device__ __forceinline__ JobRows job_rows(const LinearArgs &a, const Job &j) {
-  const ReqInfo r = a.req[j.b];
-  JobRows q;
-  q.trow = a.target + (long long)(r.t0 + j.n) * a.t_row_bytes;
-  q.tvec = ((uintptr_t)q.trow & 15) == 0;
-  q.drow = nullptr;
-  q.dvec = false;
-  if (j.kind == 1 && !a.sparse) {
-    q.drow = a.draft + (long long)(r.d0 + j.n) * a.d_row_bytes;
-    q.dvec = ((uintptr_t)q.drow & 15) == 0;
-  }
-  q.c = r.c;
-  q.mt = j.mt;
-  q.invSt = 1.f / j.St;
-  q.md = j.md;
-  q.invSd = j.Sd > 0.f ? 1.f / j.Sd : 0.f;
-  return q;
 }
 
 // Residual tile sums of the dense-draft residual draws. Persistent blocks
@@ -936,6 +728,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.out_accepted = out_accepted;
   a.out_pq = out_pq;
   a.hdr = reinterpret_cast<WsHeader *>(ws + L.hdr);
+  a.err = a.hdr;
   a.req = reinterpret_cast<ReqInfo *>(ws + L.req);
   a.jobs_a = reinterpret_cast<Job *>(ws + L.jobs_a);
   a.jobs_b = reinterpret_cast<Job *>(ws + L.jobs_b);
@@ -987,6 +780,27 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
 
   if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
+  a.ent_s = reinterpret_cast<StreamEntry *>(ws + L.ent_s);
+  a.ent_d = reinterpret_cast<StreamEntry *>(ws + L.ent_d);
+  a.ready_d = reinterpret_cast<int *>(ws + L.ready_d);
+  a.rs = reinterpret_cast<ReqStream *>(ws + L.rs);
+  a.zd_at = reinterpret_cast<float *>(ws + L.zd_at);
+  a.cap_d = B * (max_k + 1);
+  a.n_res_items = (a.ntiles + RES_TILES_PER_ITEM - 1) / RES_TILES_PER_ITEM;
+  if (stream_supported(a)) {
+    a.chunk_bytes = STREAM_CHUNK_BYTES;   // within the lazy slots' chunk capacity
+    a.nch_t = nchunks(V, tdt, a.chunk_bytes);
+    a.nch_d = nchunks(V, ddt, a.chunk_bytes);
+    a.stride = std::max(a.nch_t + a.nch_d, a.n_res_items);
+    // position-lazy schedule in one persistent kernel; decisions report
+    // invalid inputs through a second header, merged at the end
+    a.err = reinterpret_cast<WsHeader *>(ws + L.err);
+    if (cudaMemsetAsync(a.err, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
+    const int rc = launch_verify_stream(a, st);
+    if (rc != SPEC_OK) return rc;
+    k_sample_final<SPEC_DRAFT_LOGITS><<<B, SAMPLE_THREADS, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  }
   k_setup_linear<<<(B + 63) / 64, 64, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (rule == SPEC_RULE_STRICT_TOP128) {

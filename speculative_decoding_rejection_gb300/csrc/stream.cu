@@ -1,0 +1,637 @@
+// Streaming verifier: position-lazy linear verification in one persistent
+// kernel.
+//
+// What it computes is the position-lazy schedule of the linear verifier
+// (nalar.dev "Penolakan memendekkan pekerjaan speculative": proposals after
+// a rejected one do not continue the committed prefix, so their rows are
+// never read). Request b reads target row p_1 and, when it samples, draft
+// row q_1; the decision on d_1 (the lossless coin of "Acceptance Is Not
+// Speed", §6 and "RheoSampling 2026", §4 step 1; the CACTUS rule and its
+// low-support guard; the greedy prefix match of nalar.dev "Semantik
+// penerimaan") either lists position 2's rows or ends the request: with the
+// draw from norm(max(0, p - q)) after a rejection ("RheoSampling 2026", §4
+// step 3), with the bonus draw from p_{K+1} after K acceptances, or with the
+// target argmax for greedy requests.
+//
+// How (GB300): the CTA shape of the TMA row pass (one producer lane and four
+// consumer warps over a two-stage ring of 16 KB bulk copies, six CTAs per
+// SM), fed by two work queues instead of one fixed list.
+//   - Static entries, position 1 of every request, are written by the setup.
+//   - Dynamic entries, a later position's rows or the residual tile pairs of
+//     a rejection, are appended while the kernel runs by the consumer warp
+//     whose partial completes the previous entry of the same request: that
+//     warp decides the position in place.
+//   - Each producer holds one ticket of the dynamic queue and serves it as
+//     soon as its entry exists, taking static work meanwhile. A request's
+//     next position and its residual rows are therefore read right after its
+//     decision; the residual pass re-reads the two rows just streamed, from
+//     L2.
+//   - A rejected sampling request's residual entry streams the two rows
+//     just decided on once more, as tile pairs whose sums of max(0, p - q)
+//     land in the job's tile-sum slots; the finishing warp queues the final
+//     draws (those residual draws and the bonus draws) as jobs, and the
+//     final-draw kernel runs them after this kernel, as in the multi-launch
+//     schedule.
+// Partials written by other CTAs are read through L2 (ld.global.cg) after an
+// acquire on the completion counter; entries are published with a release
+// store of their ready flag. Every wait is bounded (2 s of %globaltimer): on
+// expiry the status word gets SPEC_ERR_TIMEOUT, producers stop issuing, and
+// each CTA drains its own copies and returns.
+#include "common.cuh"
+#include "internal.h"
+#include "linear.cuh"
+#include "rowpass.cuh"
+
+namespace sv {
+
+enum EntryKind : int { ENT_ROWS = 0, ENT_RES = 1 };
+
+struct StreamEntry {   // one position's rows of a request, or its residual tile pairs
+  int b;               // request; -1: nothing to stream
+  int kind;            // EntryKind
+  int trow;            // target row
+  int drow;            // draft row; -1: none is streamed
+  float c;             // log2(e)/T; 0 for argmax-only rows
+  int expect;          // completions that end the entry (one per work item)
+  int aux;             // rows: position j | K << 16; residual: index of the final-draw job
+  int pad;
+};
+static_assert(sizeof(StreamEntry) == 32, "entries are two 16-byte words");
+
+struct ReqStream {     // progress of one request
+  int round;           // position being read (0-based)
+  int count;           // completions of its current entry
+  int pad[2];
+};
+
+// Stage flags (m0.w).
+constexpr int F_NVEC = 0xfff;       // 16-byte vectors in the stage (row stages)
+constexpr int F_LAST = 1 << 12;     // last stage of its chunk / residual item
+constexpr int F_DRAFT = 1 << 13;    // the draft tensor
+constexpr int F_RES = 1 << 14;      // a residual tile pair
+// bits 16-19 / 20-23: unaligned head / tail elements of the chunk
+
+struct StreamSmem {
+  uint64_t full[NSTAGE];
+  uint64_t empty[NSTAGE];
+  int4 m0[NSTAGE];     // {part slot (-1: end of work), chunk or tile, first element, flags}
+  int4 m1[NSTAGE];     // {c bits, row (residual: elements), head element, tail element}
+  int4 m2[NSTAGE];     // {request, completions that end its entry, entry aux, target row
+                       //  (residual: first tile of the item)}
+  float4 law[NSTAGE];  // residual stages: m_t, 1/S_t, m_d, 1/S_d
+  float thr[NSTAGE];   // rank threshold of a target row (+inf: none)
+  // chunk ends: each consumer warp leaves its partial (row chunks) or its tile
+  // sums (residual items) in the slot of the chunk's last stage, double
+  // buffered by the parity of that stage's chunk-end count; the last of the
+  // four warps to arrive (counted in cend) publishes them
+  Part cp[NSTAGE][2][RS_CONS_WARPS];
+  float ct[NSTAGE][2][RS_CONS_WARPS][RES_TILES_PER_ITEM];
+  unsigned cend[NSTAGE];
+  int abort;
+  int skip;            // the setup rejected the inputs: no work
+};
+
+// ---------------------------------------------------------- memory order
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ StreamEntry ldcg_entry(const StreamEntry *e) {
+  const int4 *p = reinterpret_cast<const int4 *>(e);
+  const int4 x = __ldcg(p), y = __ldcg(p + 1);
+  return StreamEntry{x.x, x.y, x.z, x.w, __int_as_float(y.x), y.y, y.z, 0};
+}
+__device__ __forceinline__ void st_entry(StreamEntry *e, const StreamEntry &v) {
+  int4 *p = reinterpret_cast<int4 *>(e);
+  p[0] = make_int4(v.b, v.kind, v.trow, v.drow);
+  p[1] = make_int4(__float_as_int(v.c), v.expect, v.aux, 0);
+}
+__device__ __forceinline__ Job ldcg_job(const Job *j) {
+  const int4 *p = reinterpret_cast<const int4 *>(j);
+  const int4 x = __ldcg(p), y = __ldcg(p + 1);
+  return Job{x.x, x.y, x.z, x.w, __int_as_float(y.x), __int_as_float(y.y), __int_as_float(y.z),
+             __int_as_float(y.w)};
+}
+
+__device__ __forceinline__ int entry_expect(const LinearArgs &a, bool drow) {
+  return a.nch_t + (drow ? a.nch_d : 0);
+}
+
+// ------------------------------------------------------------------ setup
+// One thread per request: its record, its first-position entry, the rank
+// thresholds, and a check that every draft token is a vocabulary id (the
+// eager schedule checks them all, so this one does too). The dynamic ready
+// flags are cleared in grid strides.
+__global__ void __launch_bounds__(64) k_setup_stream(const LinearArgs a) {
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int gsize = gridDim.x * blockDim.x;
+  for (int e = gtid; e < a.cap_d; e += gsize) a.ready_d[e] = 0;
+  const int b = gtid;
+  if (b >= a.B) return;
+  ReqInfo r;
+  const bool ok = load_request(a, b, r);
+  a.req[b] = r;
+  a.rs[b] = ReqStream{0, 0, {0, 0}};
+  if (!ok) {
+    a.hdr->setup_bad = 1;
+    st_entry(a.ent_s + b, StreamEntry{-1, ENT_ROWS, 0, -1, 0.f, 0, -1, 0});
+    return;
+  }
+  for (int i = 0; i < r.K; ++i)
+    if ((unsigned)a.tokens[r.d0 + i] >= (unsigned)a.V) {
+      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+      a.hdr->setup_bad = 1;
+      break;
+    }
+  const bool drow = r.mode == MODE_SAMPLE && a.stream_draft && r.K > 0;
+  st_entry(a.ent_s + b,
+           StreamEntry{b, ENT_ROWS, r.t0, drow ? r.d0 : -1, r.c, entry_expect(a, drow), r.K << 16, 0});
+  // the draft tokens' logits, gathered once so a decision needs no dependent
+  // load: z_t(d_i) (also the rank count's threshold) and z_d(d_i)
+  for (int i = 0; i < r.K; ++i) {
+    const int d = a.tokens[r.d0 + i];
+    const bool dok = (unsigned)d < (unsigned)a.V;
+    a.rank_thr[r.t0 + i] =
+        dok ? load_elem(a.target + (long long)(r.t0 + i) * a.t_row_bytes, a.tdt, d) : INFINITY;
+    if (drow)
+      a.zd_at[r.d0 + i] = dok ? load_elem(a.draft + (long long)(r.d0 + i) * a.d_row_bytes, a.ddt, d)
+                              : 0.f;
+  }
+  a.rank_thr[r.t0 + r.K] = INFINITY;
+}
+
+// --------------------------------------------------------------- producer
+__device__ __forceinline__ bool acquire_stage(StreamSmem &sh, long long it, volatile int *abort) {
+  const int s = (int)(it % NSTAGE);
+  const long long use = it / NSTAGE;
+  return use == 0 || mbar_wait_bounded(&sh.empty[s], (uint32_t)((use - 1) & 1), abort);
+}
+
+// Streams chunk `chunk` of one row into the ring: its 16-byte aligned
+// interior in TMA bulk copies of up to 16 KB, the unaligned head and tail
+// left to the consumers' scalar loads.
+template <bool RANK>
+__device__ bool issue_row_chunk(const LinearArgs &a, StreamSmem &sh, unsigned char *stage_buf,
+                                long long &it, volatile int *abort, int slot, bool draft,
+                                int row, int chunk, const StreamEntry &E) {
+  const float c = E.c;
+  const long long rbytes = draft ? a.d_row_bytes : a.t_row_bytes;
+  const int esz = dtype_size(draft ? a.ddt : a.tdt);
+  const uint64_t row0 = (uint64_t)((draft ? a.draft : a.target) + (long long)row * rbytes);
+  const uint64_t cb0 = row0 + (uint64_t)chunk * a.chunk_bytes;
+  const uint64_t cb1 = min(row0 + (uint64_t)rbytes, cb0 + (uint64_t)a.chunk_bytes);
+  uint64_t A0 = (cb0 + 15) & ~15ull, A1 = cb1 & ~15ull;
+  if (A1 <= A0) A0 = A1 = cb1;   // no aligned interior: all scalar
+  const int ntile = A1 > A0 ? (int)((A1 - A0 + TILE_BYTES - 1) / TILE_BYTES) : 1;
+  const int head_n = (int)((A0 - cb0) / esz), tail_n = (int)((cb1 - A1) / esz);
+  const float thr = RANK && !draft ? a.rank_thr[row] : INFINITY;
+  for (int tl = 0; tl < ntile; ++tl) {
+    if (!acquire_stage(sh, it, abort)) return false;
+    const int s = (int)(it % NSTAGE);
+    const uint64_t off = A0 + (uint64_t)tl * TILE_BYTES;
+    const uint32_t nb = (uint32_t)min((uint64_t)TILE_BYTES, A1 - off);
+    sh.m0[s] = make_int4(slot, chunk, (int)((off - row0) / esz),
+                         (int)(nb / 16) | (tl == ntile - 1 ? F_LAST : 0) | (draft ? F_DRAFT : 0) |
+                             (head_n << 16) | (tail_n << 20));
+    sh.m1[s] = make_int4(__float_as_int(c), row, (int)((cb0 - row0) / esz),
+                         (int)((A1 - row0) / esz));
+    sh.m2[s] = make_int4(E.b, E.expect, E.aux, E.trow);
+    if (RANK) sh.thr[s] = thr;
+    if (nb > 0) {
+      mbar_arrive_tx(&sh.full[s], nb);
+      bulk_g2s(stage_buf + (size_t)s * TILE_BYTES, (const void *)off, nb, &sh.full[s]);
+    } else {
+      mbar_arrive(&sh.full[s]);
+    }
+    ++it;
+  }
+  return true;
+}
+
+// Streams residual item g of entry E: up to RES_TILES_PER_ITEM tiles, each
+// SAMPLE_TILE bf16 of the target row and the same elements of the draft row
+// side by side in one stage.
+__device__ bool issue_res_item(const LinearArgs &a, StreamSmem &sh, unsigned char *stage_buf,
+                               long long &it, volatile int *abort, const StreamEntry &E, int g) {
+  const Job job = ldcg_job(a.jobs_a + E.aux);
+  const float4 law = make_float4(job.mt, 1.f / job.St, job.md, job.Sd > 0.f ? 1.f / job.Sd : 0.f);
+  const uint64_t trow = (uint64_t)(a.target + (long long)E.trow * a.t_row_bytes);
+  const uint64_t drow = (uint64_t)(a.draft + (long long)E.drow * a.d_row_bytes);
+  const int j0 = g * RES_TILES_PER_ITEM, j1 = min(a.ntiles, j0 + RES_TILES_PER_ITEM);
+  for (int j = j0; j < j1; ++j) {
+    if (!acquire_stage(sh, it, abort)) return false;
+    const int s = (int)(it % NSTAGE);
+    const int e0 = j * SAMPLE_TILE;
+    const int ne = min(SAMPLE_TILE, a.V - e0);
+    const uint32_t nb = (uint32_t)ne * 2;
+    sh.m0[s] = make_int4(E.b, j, e0, F_RES | (j == j1 - 1 ? F_LAST : 0));
+    sh.m1[s] = make_int4(__float_as_int(E.c), ne, j0, j1 - j0);
+    sh.m2[s] = make_int4(E.b, E.expect, E.aux, j0);
+    sh.law[s] = law;
+    mbar_arrive_tx(&sh.full[s], 2 * nb);
+    unsigned char *dst = stage_buf + (size_t)s * TILE_BYTES;
+    bulk_g2s(dst, (const void *)(trow + 2ull * e0), nb, &sh.full[s]);
+    bulk_g2s(dst + TILE_BYTES / 2, (const void *)(drow + 2ull * e0), nb, &sh.full[s]);
+    ++it;
+  }
+  return true;
+}
+
+// Work item k of entry E: target chunks first, then draft chunks, or a
+// residual item; tickets past the entry's items carry nothing.
+template <bool RANK>
+__device__ bool issue_item(const LinearArgs &a, StreamSmem &sh, unsigned char *stage_buf,
+                           long long &it, volatile int *abort, const StreamEntry &E, int k) {
+  if (E.b < 0) return true;
+  if (E.kind == ENT_RES)
+    return k < a.n_res_items ? issue_res_item(a, sh, stage_buf, it, abort, E, k) : true;
+  if (k < a.nch_t)
+    return issue_row_chunk<RANK>(a, sh, stage_buf, it, abort, E.b, false, E.trow, k, E);
+  k -= a.nch_t;
+  if (E.drow >= 0 && k < a.nch_d)
+    return issue_row_chunk<RANK>(a, sh, stage_buf, it, abort, a.B + E.b, true, E.drow, k, E);
+  return true;
+}
+
+// --------------------------------------------------- completions, entries
+// Appends a dynamic entry and publishes it (release store of its flag).
+__device__ void push_entry(const LinearArgs &a, const StreamEntry &E) {
+  const int e = atomicAdd(&a.hdr->n_alloc_d, 1);
+  if (e >= a.cap_d) {   // cannot happen: a request appends at most K + 1 entries
+    set_status(a.hdr, SPEC_ERR_TIMEOUT, -4);
+    return;
+  }
+  st_entry(a.ent_d + e, E);
+  __threadfence();
+  st_release(a.ready_d + e, 1);
+}
+
+// Request b's final token is written (or queued as a final-draw job). The
+// last request to finish moves the errors the decisions reported (empty
+// rows) into the status word.
+__device__ void finish_one(const LinearArgs &a, int lane) {
+  if (lane == 0) {
+    __threadfence();
+    const int old = atomicAdd(&a.hdr->n_done, 1);
+    if (old + 1 == a.B) {
+      const int st = *(volatile int *)&a.err->status;
+      if (st != SPEC_OK) set_status(a.hdr, st, *(volatile int *)&a.err->detail);
+    }
+  }
+  __syncwarp();
+}
+
+// Row statistics of `n` (<= 32) chunk partials held one per lane, merged
+// in the order of warp_row_stat (the same bits).
+__device__ __forceinline__ RowStat lane_parts_stat(const Part &p, bool have, float c) {
+  float m = NO_MAX, S = 0.f;
+  int idx = 0x7fffffff;
+  if (have) merge_stat(m, S, idx, p.m, p.S, p.idx, c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    merge_stat(m, S, idx, m2, S2, i2, c);
+  }
+  return RowStat{m, S, idx};
+}
+
+// Decision on position j of request b (target row trow, K drafts, c =
+// log2(e)/T, 0 for greedy), once both of its rows are complete: accept and
+// list the next position, or finish the request. Every input comes from one
+// round of independent loads: the chunk partials, the token and the
+// gathered logits z_t(d), z_d(d).
+__device__ __noinline__ void stream_decide(const LinearArgs &a, int b, int j, int K, int trow,
+                                           float c, int lane) {
+  ReqInfo r;
+  r.t0 = trow - j;
+  r.d0 = r.t0 - b;
+  r.K = K;
+  r.mode = c != 0.f ? MODE_SAMPLE : MODE_GREEDY;
+  r.c = c;
+  const bool sample = r.mode == MODE_SAMPLE;
+  const bool drow = sample && a.stream_draft && j < K;
+  const bool fast = a.nch_t * RS_CONS_WARPS <= 32 && a.nch_d * RS_CONS_WARPS <= 32;
+  const long long tb = (long long)b * a.nch_max * RS_CONS_WARPS;
+  const long long db = (long long)(a.B + b) * a.nch_max * RS_CONS_WARPS;
+  const bool th = lane < a.nch_t * RS_CONS_WARPS, dh = drow && lane < a.nch_d * RS_CONS_WARPS;
+  Part tp{}, dp{};
+  int d = -1;
+  float zt = 0.f, zd = 0.f;
+  if (fast && th) tp = ldcg_part(a.part + tb + lane);
+  if (fast && dh) dp = ldcg_part(a.part + db + lane);
+  if (j < K) {
+    d = a.tokens[r.d0 + j];
+    zt = __ldcg(a.rank_thr + trow);
+    if (drow) zd = __ldcg(a.zd_at + r.d0 + j);
+  }
+  const RowStat ts = fast ? lane_parts_stat(tp, th, c) : target_stat(a, b, c, lane);
+  RowStat ds{NO_MAX, 0.f, 0x7fffffff};
+  int n = K;
+  if (j < K) {
+    int rank = 0;
+    if (a.want_rank) {
+      if (fast) {
+        rank = th ? tp.cnt : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        rank += 1;
+      } else {
+        rank = 1 + warp_row_count(a, b, lane);
+      }
+    }
+    if (drow) ds = fast ? lane_parts_stat(dp, dh, c) : draft_stat(a, a.B + b, c, lane);
+    const bool rej = __shfl_sync(
+        0xffffffffu,
+        lane == 0 && position_rejects_z(a, b, r, j, sample, ts, ds, rank, d, zt, zd, false), 0);
+    if (!rej) {   // accepted: the next position's rows
+      if (lane == 0) {
+        const bool next_drow = sample && a.stream_draft && j + 1 < K;
+        push_entry(a, StreamEntry{b, ENT_ROWS, trow + 1, next_drow ? r.d0 + j + 1 : -1, c,
+                                  entry_expect(a, next_drow), (j + 1) | (K << 16), 0});
+      }
+      return;
+    }
+    n = j;
+  }
+  // positions after n+1 were never read
+  for (int i = n + 1 + lane; i < K; i += 32) {
+    if (a.out_pq) {
+      a.out_pq[2LL * (r.d0 + i)] = __int_as_float(0x7fc00000);
+      a.out_pq[2LL * (r.d0 + i) + 1] = __int_as_float(0x7fc00000);
+    }
+    if (a.out_rank) a.out_rank[r.d0 + i] = -1;
+  }
+  const int W = a.max_k + 1;
+  int32_t *out = a.out_tokens + (long long)b * W;
+  for (int jj = lane; jj < W; jj += 32) out[jj] = jj < n ? a.tokens[r.d0 + jj] : -1;
+  if (lane == 0) a.out_accepted[b] = n;
+  __syncwarp();
+  if (!sample) {   // greedy: the target's argmax replaces the rejected draft
+    if (lane == 0) out[n] = ts.idx;
+    finish_one(a, lane);
+    return;
+  }
+  const bool residual = n < K && a.stream_draft;
+  if (lane == 0) {
+    if (residual) {
+      // the residual's tile sums are summed here, the draw after this kernel
+      const int ja = atomicAdd(&a.hdr->n_jobs_a, 1);
+      a.jobs_a[ja] = Job{b, n, 1, 0, ts.m, ts.S, ds.m, ds.S};
+      push_entry(a, StreamEntry{b, ENT_RES, trow, r.d0 + n, c, a.n_res_items, ja, 0});
+    } else {   // bonus draw from p_{K+1}, after this kernel
+      a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = Job{b, n, 2, 0, ts.m, ts.S, 0.f, 0.f};
+    }
+  }
+  if (!residual) finish_one(a, lane);
+  __syncwarp();
+}
+
+// A consumer warp at the end of a chunk (row partial p) or a residual item
+// (tile sums rs) on stage slot s, before it releases the stage: it leaves its
+// result in the slot's buffer of parity `par` and counts itself in cend[s].
+// Counting before the release keeps the slot from being refilled, and so from
+// reaching its next chunk end, until all four warps have counted. Returns
+// true in every lane of the last warp to count: the closer.
+__device__ __forceinline__ bool chunk_end_count(StreamSmem &sh, int s, int par, int cw, int lane,
+                                                bool res, const Part &p,
+                                                const float (&rs)[RES_TILES_PER_ITEM]) {
+  unsigned old = 0;
+  if (lane == 0) {
+    if (res) {
+#pragma unroll
+      for (int t = 0; t < RES_TILES_PER_ITEM; ++t) sh.ct[s][par][cw][t] = rs[t];
+    } else {
+      sh.cp[s][par][cw] = p;
+    }
+    __threadfence_block();
+    old = atomicAdd(&sh.cend[s], 1u);
+  }
+  return (__shfl_sync(0xffffffffu, old, 0) & 3u) == 3u;
+}
+
+// The closer, after releasing the stage: the four warps' results to global
+// memory, one completion of the request's entry, and, for the entry's last
+// completion, the decision on the position (rows) or the end of the request
+// (residual). Only this warp waits on global memory.
+__device__ __forceinline__ void chunk_close(const LinearArgs &a, StreamSmem &sh, int s, int par,
+                                            int lane, bool res, const int4 m0, const int4 m1,
+                                            const int4 m2) {
+  int last = 0;
+  if (lane == 0) {
+    __threadfence_block();
+    if (res) {   // m2.z: job, m2.w: first tile, m1.w: tiles in the item
+      for (int t = 0; t < m1.w; ++t)
+        reinterpret_cast<float4 *>(a.tsum)[(long long)m2.z * a.ntiles + m2.w + t] =
+            make_float4(sh.ct[s][par][0][t], sh.ct[s][par][1][t], sh.ct[s][par][2][t],
+                        sh.ct[s][par][3][t]);
+    } else {
+      Part *dst = a.part + ((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS;
+#pragma unroll
+      for (int w = 0; w < RS_CONS_WARPS; ++w) dst[w] = sh.cp[s][par][w];
+    }
+    __threadfence();
+    last = atomicAdd(&a.rs[m2.x].count, 1) + 1 == m2.y;
+    if (last) {
+      a.rs[m2.x].count = 0;   // the request's next entry starts a new count
+      __threadfence();
+    }
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  if (res) finish_one(a, lane);
+  else stream_decide(a, m2.x, m2.z & 0xffff, m2.z >> 16, m2.w, __int_as_float(m1.x), lane);
+}
+
+// ------------------------------------------------------------------ kernel
+template <bool RANK>
+__global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM)
+    k_verify_stream(const LinearArgs a) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ StreamSmem sh;
+  unsigned char *stage_buf = dsmem;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], RS_CONS_WARPS);
+    }
+    sh.abort = 0;
+    for (int q = 0; q < NSTAGE; ++q) sh.cend[q] = 0;
+    // the setup's verdict (fixed before this kernel starts); errors found
+    // while it runs go to the status word without stopping the other requests
+    sh.skip = *(volatile int *)&a.hdr->setup_bad;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (sh.skip) {   // inputs rejected by the setup: nothing is verified
+    const int W = a.max_k + 1;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)a.B * W;
+         i += (long long)gridDim.x * blockDim.x) {
+      a.out_tokens[i] = -1;
+      if (i < a.B) a.out_accepted[i] = -1;
+    }
+    return;
+  }
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int *abort = &sh.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    long long it = 0;
+    bool ok = true;
+    const unsigned long long n_static = (unsigned long long)a.B * a.stride;
+    const unsigned long long n_dyn = (unsigned long long)a.cap_d * a.stride;
+    unsigned long long st_t = atomicAdd(&a.hdr->work_s, 1ull);
+    unsigned long long dy_t = atomicAdd(&a.hdr->work_d, 1ull);
+    while (true) {
+      // 1. the held dynamic ticket, once its entry exists
+      const int e = (int)(dy_t / a.stride);
+      if (dy_t < n_dyn && ld_acquire(a.ready_d + e)) {
+        const StreamEntry E = ldcg_entry(a.ent_d + e);
+        if (!issue_item<RANK>(a, sh, stage_buf, it, abort, E, (int)(dy_t % a.stride))) {
+          ok = false;
+          break;
+        }
+        dy_t = atomicAdd(&a.hdr->work_d, 1ull);
+        continue;
+      }
+      // 2. static work meanwhile
+      if (st_t < n_static) {
+        const unsigned long long next = atomicAdd(&a.hdr->work_s, 1ull);
+        const StreamEntry E = ldcg_entry(a.ent_s + st_t / a.stride);
+        if (!issue_item<RANK>(a, sh, stage_buf, it, abort, E, (int)(st_t % a.stride))) {
+          ok = false;
+          break;
+        }
+        st_t = next;
+        continue;
+      }
+      // 3. nothing else: wait for the ticket's entry, the last request or an error
+      const unsigned long long t0 = global_ns();
+      int outcome = 0;   // 1: entry ready, 2: every request finished, 3: give up
+      while (outcome == 0) {
+        if (dy_t < n_dyn && ld_acquire(a.ready_d + e)) outcome = 1;
+        else if (*(volatile int *)&a.hdr->n_done >= a.B) outcome = 2;
+        else if (*(volatile int *)&a.hdr->status == SPEC_ERR_TIMEOUT || *abort) outcome = 3;
+        else if (global_ns() - t0 > WAIT_NS) outcome = 3;
+        else __nanosleep(256);
+      }
+      if (outcome == 1) continue;
+      ok = outcome == 2;
+      break;
+    }
+    if (ok && acquire_stage(sh, it, abort)) {   // end marker
+      const int s = (int)(it % NSTAGE);
+      sh.m0[s] = make_int4(-1, 0, 0, 0);
+      mbar_arrive(&sh.full[s]);
+      return;
+    }
+    // gave up: record it, tell the consumers, then wait (bounded) for this
+    // CTA's copies in flight
+    set_status(a.hdr, SPEC_ERR_TIMEOUT, -2);
+    *abort = 1;
+    for (int s = 0; s < NSTAGE; ++s) {
+      const long long issued = (it - s + NSTAGE - 1) / NSTAGE;   // uses of stage s
+      if (issued > 0) {
+        volatile int never = 0;
+        mbar_wait_bounded(&sh.full[s], (uint32_t)((issued - 1) & 1), &never);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  static_assert(NSTAGE == 2, "chunk-end counters are kept per stage slot");
+  const int cw = warp - 1;
+  const int ctid = threadIdx.x - 32;
+  RunState st{NO_MAX, pk2(0.f, 0.f), 0x7fffffff, 0, 0u};
+  float rsum[RES_TILES_PER_ITEM] = {};
+  unsigned ends0 = 0, ends1 = 0;   // chunk ends seen on each stage slot
+  for (long long it = 0;; ++it) {
+    const int s = (int)(it % NSTAGE);
+    if (!mbar_wait_bounded(&sh.full[s], (uint32_t)((it / NSTAGE) & 1), abort)) {
+      if (!*abort) set_status(a.hdr, SPEC_ERR_TIMEOUT, -3);
+      *abort = 1;
+      return;
+    }
+    const int4 m0 = sh.m0[s];
+    if (m0.x < 0) return;
+    const int4 m1 = sh.m1[s];
+    const int4 m2 = sh.m2[s];
+    const unsigned char *buf = stage_buf + (size_t)s * TILE_BYTES;
+    const bool res = (m0.w & F_RES) != 0;
+    const bool last = (m0.w & F_LAST) != 0;
+    Part p{};
+    if (res) {   // residual tile pair: tile m0.y, the item's tiles start at m1.z
+      const float4 lw = sh.law[s];
+      const ResLaw L{lw.x, lw.y, lw.z, lw.w, __int_as_float(m1.x)};
+      const int ne = m1.y;
+      float r = ne == SAMPLE_TILE ? consume_res_full(buf, ctid, L)
+                                  : consume_res_partial(buf, ctid, ne, L);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+#pragma unroll
+      for (int q = 0; q < RES_TILES_PER_ITEM; ++q)
+        if (q == m0.y - m1.z) rsum[q] = r;
+    } else {
+      const int nvec = m0.w & F_NVEC;
+      const bool draft = (m0.w & F_DRAFT) != 0;
+      const int dt = draft ? a.ddt : a.tdt;
+      const float c = __int_as_float(m1.x);
+      const float thr = RANK ? sh.thr[s] : INFINITY;
+      consume_row_stage<RANK>(buf, nvec, m0.z, c, dt == SPEC_BF16, thr, ctid, st);
+      if (last) {
+        if (cw == 0) {
+          const char *row = (draft ? a.draft : a.target) +
+                            (long long)m1.y * (draft ? a.d_row_bytes : a.t_row_bytes);
+          consume_head_tail(row, dt, m0.w, m1.z, m1.w, c, thr, lane, st);
+        }
+        p = finish_row_chunk<RANK>(st, c);
+      }
+    }
+    bool closer = false;
+    int par = 0;
+    if (last) {
+      unsigned &e = s ? ends1 : ends0;
+      par = (int)(e & 1u);
+      ++e;
+      closer = chunk_end_count(sh, s, par, cw, lane, res, p, rsum);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);
+    if (closer) chunk_close(a, sh, s, par, lane, res, m0, m1, m2);
+  }
+}
+
+bool stream_supported(const LinearArgs &a) {
+  return a.lazy && a.dk == SPEC_DRAFT_LOGITS && a.rule != SPEC_RULE_STRICT_TOP128 && !a.want_kl &&
+         a.tdt == SPEC_BF16 && a.ddt == SPEC_BF16 && a.V % 8 == 0;
+}
+
+int launch_verify_stream(const LinearArgs &a, cudaStream_t stream) {
+  const int sms = num_sms();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  k_setup_stream<<<(a.B + 63) / 64, 64, 0, stream>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  const size_t smem = (size_t)NSTAGE * TILE_BYTES;
+  auto kern = a.want_rank ? k_verify_stream<true> : k_verify_stream<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  cudaEvent_t before, after;
+  take_row_pass_events(&before, &after);
+  if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  kern<<<(a.want_rank ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM) * sms, RS_THREADS, smem, stream>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+}  // namespace sv

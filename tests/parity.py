@@ -17,10 +17,10 @@ PROB_ATOL = 1e-30
 
 
 def gpu_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, draft=None,
-               draft_idx=None, ext=None, lazy=False, kl=False):
+               draft_idx=None, ext=None, lazy=False, kl=False, rank=True):
     """Runs the CUDA verifier; `ext` (a dict of alpha / max_rank / min_prob)
     or `lazy` goes through spec_verify_linear_ext, which also returns target
-    ranks."""
+    ranks unless `rank` is False."""
     draft = lb.draft if draft is None else draft
     if ext is None and not lazy and not kl:
         tokens, acc, pq, ws = sv.spec_verify_linear(
@@ -31,7 +31,7 @@ def gpu_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, dr
         tokens, acc, pq, rank, klv, ws = sv.spec_verify_linear_ext(
             lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
             max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx,
-            want_pq=True, want_rank=True, want_kl=kl, lazy=lazy, **(ext or {}))
+            want_pq=True, want_rank=rank, want_kl=kl, lazy=lazy, **(ext or {}))
     status = sv.spec_get_status(ws)
     out = dict(tokens=tokens.cpu().numpy(), accepted=acc.cpu().numpy(),
                pq=pq.cpu().numpy().astype(np.float64), status=status)
