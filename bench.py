@@ -42,9 +42,18 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum over the algorithmic bytes it streams). Valid only for
 # the row-pass source it was taken on.
 # Captured on B=128, K=4, V=201088 bf16 (460.09 MB streamed by the launch):
-# 460.17 MB read + 3.81 MB written (the per-chunk partial statistics).
-ROWPASS_TRAFFIC = {"source_sha1": "4bb57b7f0287ffb15ec5c3d818ba995f8235f3e6",
-                   "dram_per_algorithmic_byte": (460191232 + 3402240) / 460089344}
+# 460.19 MB read + 3.49 MB written (the per-chunk partial statistics).
+ROWPASS_TRAFFIC = {"source_sha1": "7fb47217e418563d0e3bfdcba1c829cfc8eb4206",
+                   "dram_per_algorithmic_byte": (460191744 + 3492352) / 460089344}
+# The same for the streaming verifier (position-lazy schedule), per byte of
+# the rows the schedule must read (target rows 1..n+1, dense draft rows
+# 1..min(n+1, K) of sampling requests). Captured on the full B=1024, K=4,
+# V=201088 workload (one pass): 2711.8 MB read + 23.5 MB written for
+# 1975.1 MB; the excess is the residual rows read a second time and rows
+# read before a rejection made them unneeded, so the ratio holds for this
+# workload and source only.
+STREAM_TRAFFIC = {"source_sha1": "de41eca4c0b1ee2cb156d518af6b89da32d6a706",
+                  "dram_per_algorithmic_byte": (2711803136 + 23505920) / 1975086336}
 
 
 def parse():
@@ -212,9 +221,14 @@ class LinearWork:
                                    "min_prob={min_prob})".format(**self.ext))
         if kl:
             self.config["outputs"] = "tokens, counts and per-position KL(p || q)"
+        # the position-lazy schedule of dense bf16 logits (V % 8 == 0, no KL)
+        # runs as one persistent kernel: setup, streaming verifier, final draws
+        self.stream = (lazy and not lb.top128 and not kl and lb.V % 8 == 0
+                       and lb.target.dtype == torch.bfloat16)
         if lazy:
             self.config["schedule"] = "position-lazy (rows 1..n+1 per request)"
-            self.launches = 2 + 2 * (lb.max_k + 1) + (0 if lb.top128 else 1) + 1
+            self.launches = (3 if self.stream
+                             else 2 + 2 * (lb.max_k + 1) + (0 if lb.top128 else 1) + 1)
 
     def input_tensors(self):
         lb = self.lb
@@ -438,9 +452,14 @@ def main():
     traffic = None
     src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "rowpass.cu")
     lazy = getattr(work, "lazy", False)
+    stream = getattr(work, "stream", False)
     plain = not lazy and getattr(work, "kl", None) is None and getattr(work, "ext", None) is None
     if ROWPASS_TRAFFIC["source_sha1"] == sha1(src) and plain:
         traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    stream_src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "stream.cu")
+    if (stream and getattr(work, "ext", None) is None and args.B is None and args.config == 5
+            and STREAM_TRAFFIC["source_sha1"] == sha1(stream_src)):
+        traffic = STREAM_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
 
     # end to end through the same API: pinned host inputs copied in, the
     # results read back, every step
@@ -500,7 +519,8 @@ def main():
         "algorithmic_bytes_per_step": algo,
         "mean_accepted": work.mean_accepted(),
         "roofline": {
-            "kernel": ("k_row_pass rounds with k_lazy_decide (one span)" if lazy
+            "kernel": ("k_verify_stream" if stream
+                       else "k_row_pass rounds with k_lazy_decide (one span)" if lazy
                        else "k_row_pass"),
             "bound": "hbm", "achieved": achieved, "peak": peak,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"

@@ -30,8 +30,8 @@ namespace sv {
 
 struct LinearLayout {
   size_t hdr, err, req, jobs_a, jobs_b, tsum, list, part, kl_part, tk_idx, tk_prob, rank_thr;
-  size_t ent_s, ent_d, ready_d, rs, zd_at, total;
-  int nch_max, nch_max_lazy;
+  size_t ent_d, ready_d, pos_done, pos_join, rej_at, zd_at, total;
+  int nch_max, nch_max_lazy, nch_max_stream;
   long long rows_max;
 };
 
@@ -51,9 +51,11 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   L.list = o; o += align256(sizeof(RowTask) * (size_t)std::max(L.rows_max, 2LL * B));
   // eager: one slot per listed row; lazy: two per request (its rows of the
   // current round), in finer chunks
+  L.nch_max_stream = nchunks(V, SPEC_F32, STREAM_CHUNK_BYTES);
   L.part = o;
   o += align256(sizeof(Part) * RS_CONS_WARPS *
-                std::max((size_t)L.rows_max * L.nch_max, (size_t)2 * B * L.nch_max_lazy));
+                std::max({(size_t)L.rows_max * L.nch_max, (size_t)2 * B * L.nch_max_lazy,
+                          (size_t)L.rows_max * L.nch_max_stream}));
   const size_t tk = rule == SPEC_RULE_STRICT_TOP128 ? (size_t)B * max_k * SPEC_TOPK : 0;
   L.kl_part = o;
   o += align256(sizeof(float) * RS_CONS_WARPS *
@@ -61,13 +63,14 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   L.tk_idx = o;  o += align256(sizeof(int32_t) * tk);
   L.tk_prob = o; o += align256(sizeof(float) * tk);
   L.rank_thr = o; o += align256(sizeof(float) * (size_t)B * (max_k + 1));
-  // streaming verifier: static and dynamic entries (32 B), ready flags,
-  // per-request progress (16 B)
-  const size_t cap_d = (size_t)B * (max_k + 1);
-  L.ent_s = o; o += align256(32 * (size_t)B);
-  L.ent_d = o; o += align256(32 * cap_d);
-  L.ready_d = o; o += align256(sizeof(int) * cap_d);
-  L.rs = o; o += align256(16 * (size_t)B);
+  // streaming verifier: residual entries (32 B) and their ready flags,
+  // per-position counters, first rejections
+  const size_t npos = (size_t)B * (max_k + 1);
+  L.ent_d = o; o += align256(32 * (size_t)B);
+  L.ready_d = o; o += align256(sizeof(int) * 2 * (size_t)B);   // flags, then counts
+  L.pos_done = o; o += align256(sizeof(int) * npos);
+  L.pos_join = o; o += align256(sizeof(int) * npos);
+  L.rej_at = o; o += align256(sizeof(int) * (size_t)B);
   L.zd_at = o; o += align256(sizeof(float) * (size_t)B * max_k);
   L.total = o;
   return L;
@@ -780,18 +783,22 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
 
   if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
-  a.ent_s = reinterpret_cast<StreamEntry *>(ws + L.ent_s);
   a.ent_d = reinterpret_cast<StreamEntry *>(ws + L.ent_d);
   a.ready_d = reinterpret_cast<int *>(ws + L.ready_d);
-  a.rs = reinterpret_cast<ReqStream *>(ws + L.rs);
+  a.pos_done = reinterpret_cast<int *>(ws + L.pos_done);
+  a.pos_join = reinterpret_cast<int *>(ws + L.pos_join);
+  a.rej_at = reinterpret_cast<int *>(ws + L.rej_at);
   a.zd_at = reinterpret_cast<float *>(ws + L.zd_at);
-  a.cap_d = B * (max_k + 1);
+  a.cap_d = B;
   a.n_res_items = (a.ntiles + RES_TILES_PER_ITEM - 1) / RES_TILES_PER_ITEM;
   if (stream_supported(a)) {
-    a.chunk_bytes = STREAM_CHUNK_BYTES;   // within the lazy slots' chunk capacity
+    // partial slots by absolute row (as the eager schedule), 64 KB chunks
+    a.lazy = 0;
+    a.chunk_bytes = STREAM_CHUNK_BYTES;
     a.nch_t = nchunks(V, tdt, a.chunk_bytes);
     a.nch_d = nchunks(V, ddt, a.chunk_bytes);
-    a.stride = std::max(a.nch_t + a.nch_d, a.n_res_items);
+    a.nch_max = L.nch_max_stream;
+    a.stride = a.nch_t + a.nch_d;
     // position-lazy schedule in one persistent kernel; decisions report
     // invalid inputs through a second header, merged at the end
     a.err = reinterpret_cast<WsHeader *>(ws + L.err);

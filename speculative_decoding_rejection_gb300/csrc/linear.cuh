@@ -11,7 +11,6 @@ namespace sv {
 constexpr int ACCEPT_WARPS = 8;
 
 struct StreamEntry;
-struct ReqStream;
 
 struct LinearArgs {
   const char *target;
@@ -55,14 +54,17 @@ struct LinearArgs {
   int want_kl;
   float *kl_part;             // A partials of the pair rows' target slots
   float *out_kl;
-  // streaming verifier: work entries and per-request progress
-  StreamEntry *ent_s;  // [B] first-position entries, written by the setup
-  StreamEntry *ent_d;  // [cap_d] entries allocated while the kernel runs
-  int *ready_d;               // [cap_d] 1 once ent_d[e] is written
+  // streaming verifier: per-position progress and residual entries
+  StreamEntry *ent_d;         // [cap_d] residual entries allocated while the kernel runs
+  int *ready_d;               // [2 cap_d] 1 once ent_d[e] is written; then, per
+                              // request, the completed items of its residual entry
+  int *pos_done;              // [B * (max_k + 1)] completed work items of a position's rows
+  int *pos_join;              // [B * (max_k + 1)] events of a position: its rows are
+                              // complete, the previous position was accepted
+  int *rej_at;                // [B] position of the first rejection (INT_MAX: none yet)
   float *zd_at;               // [R_d] z_d(d_i), gathered by the setup
-  ReqStream *rs;       // [B]
-  int cap_d;                  // B * (max_k + 1)
-  int stride;                 // tickets per entry
+  int cap_d;                  // B
+  int stride;                 // tickets per position of a request
   int n_res_items;            // residual work items per final draw
 };
 

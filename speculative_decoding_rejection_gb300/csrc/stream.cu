@@ -3,40 +3,45 @@
 //
 // What it computes is the position-lazy schedule of the linear verifier
 // (nalar.dev "Penolakan memendekkan pekerjaan speculative": proposals after
-// a rejected one do not continue the committed prefix, so their rows are
-// never read). Request b reads target row p_1 and, when it samples, draft
-// row q_1; the decision on d_1 (the lossless coin of "Acceptance Is Not
-// Speed", §6 and "RheoSampling 2026", §4 step 1; the CACTUS rule and its
-// low-support guard; the greedy prefix match of nalar.dev "Semantik
-// penerimaan") either lists position 2's rows or ends the request: with the
-// draw from norm(max(0, p - q)) after a rejection ("RheoSampling 2026", §4
-// step 3), with the bonus draw from p_{K+1} after K acceptances, or with the
-// target argmax for greedy requests.
+// a rejected one do not continue the committed prefix, so their rows are not
+// needed). Position j of request b is decided once its target row p_{j+1}
+// and, when the request samples, its draft row q_{j+1} are reduced and
+// position j-1 was accepted: the lossless coin ("Acceptance Is Not Speed",
+// §6; "RheoSampling 2026", §4 step 1), the CACTUS rule with its low-support
+// guard, or the greedy prefix match (nalar.dev "Semantik penerimaan"). A
+// rejection ends the request with the draw from norm(max(0, p - q))
+// ("RheoSampling 2026", §4 step 3), K acceptances with the bonus draw from
+// p_{K+1}, a greedy request with the target argmax.
 //
 // How (GB300): the CTA shape of the TMA row pass (one producer lane and four
 // consumer warps over a two-stage ring of 16 KB bulk copies, six CTAs per
-// SM), fed by two work queues instead of one fixed list.
-//   - Static entries, position 1 of every request, are written by the setup.
-//   - Dynamic entries, a later position's rows or the residual tile pairs of
-//     a rejection, are appended while the kernel runs by the consumer warp
-//     whose partial completes the previous entry of the same request: that
-//     warp decides the position in place.
-//   - Each producer holds one ticket of the dynamic queue and serves it as
-//     soon as its entry exists, taking static work meanwhile. A request's
-//     next position and its residual rows are therefore read right after its
-//     decision; the residual pass re-reads the two rows just streamed, from
-//     L2.
-//   - A rejected sampling request's residual entry streams the two rows
-//     just decided on once more, as tile pairs whose sums of max(0, p - q)
-//     land in the job's tile-sum slots; the finishing warp queues the final
-//     draws (those residual draws and the bonus draws) as jobs, and the
-//     final-draw kernel runs them after this kernel, as in the multi-launch
-//     schedule.
+// SM) over two work sources.
+//   - The static list holds every position's rows in layer order: position 1
+//     of every request, then position 2, and so on, each row split into
+//     256 KB chunks. A producer skips a chunk of request b at position j once
+//     b is known to have rejected an earlier position; by the time a layer
+//     comes up the previous layer's decisions are mostly known, so the rows
+//     after a rejection are mostly never read.
+//   - Chunk ends are aggregated per CTA: each consumer warp leaves its
+//     partial in shared memory, and the last of the four publishes them and
+//     counts one completion of the position with a release atomic.
+//   - A position is decided by whichever of two events comes second: its
+//     rows complete, or the previous position accepted (an atomic join). An
+//     acceptance whose next position is already complete decides that one
+//     too, in the same warp.
+//   - A rejection of a sampling request appends its residual entry: the two
+//     rows just decided on, streamed once more as tile pairs whose sums of
+//     max(0, p - q) land in the job's tile-sum slots. Producers serve these
+//     entries first, so the re-read mostly hits L2. The final draws (these
+//     and the bonus draws) are queued as jobs for the final-draw kernel,
+//     which runs after this kernel as in the multi-launch schedule.
 // Partials written by other CTAs are read through L2 (ld.global.cg) after an
-// acquire on the completion counter; entries are published with a release
-// store of their ready flag. Every wait is bounded (2 s of %globaltimer): on
-// expiry the status word gets SPEC_ERR_TIMEOUT, producers stop issuing, and
-// each CTA drains its own copies and returns.
+// acquire; entries are published with a release store of their ready flag.
+// Every wait is bounded (2 s of %globaltimer): on expiry the status word
+// gets SPEC_ERR_TIMEOUT, producers stop issuing, and each CTA drains its own
+// copies and returns.
+#include <limits.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "linear.cuh"
@@ -44,25 +49,14 @@
 
 namespace sv {
 
-enum EntryKind : int { ENT_ROWS = 0, ENT_RES = 1 };
-
-struct StreamEntry {   // one position's rows of a request, or its residual tile pairs
-  int b;               // request; -1: nothing to stream
-  int kind;            // EntryKind
-  int trow;            // target row
-  int drow;            // draft row; -1: none is streamed
-  float c;             // log2(e)/T; 0 for argmax-only rows
-  int expect;          // completions that end the entry (one per work item)
-  int aux;             // rows: position j | K << 16; residual: index of the final-draw job
-  int pad;
+struct StreamEntry {   // the residual tile pairs of a rejected position
+  int b;               // request
+  int trow, drow;      // the rejected position's target and draft rows
+  int job;             // index of the final-draw job (its tile-sum slots)
+  float c;             // log2(e)/T
+  int pad[3];
 };
 static_assert(sizeof(StreamEntry) == 32, "entries are two 16-byte words");
-
-struct ReqStream {     // progress of one request
-  int round;           // position being read (0-based)
-  int count;           // completions of its current entry
-  int pad[2];
-};
 
 // Stage flags (m0.w).
 constexpr int F_NVEC = 0xfff;       // 16-byte vectors in the stage (row stages)
@@ -75,15 +69,16 @@ struct StreamSmem {
   uint64_t full[NSTAGE];
   uint64_t empty[NSTAGE];
   int4 m0[NSTAGE];     // {part slot (-1: end of work), chunk or tile, first element, flags}
-  int4 m1[NSTAGE];     // {c bits, row (residual: elements), head element, tail element}
-  int4 m2[NSTAGE];     // {request, completions that end its entry, entry aux, target row
-                       //  (residual: first tile of the item)}
+  int4 m1[NSTAGE];     // {c bits, row (residual: elements), head element (residual: first
+                       //  tile of the item), tail element (residual: tiles in the item)}
+  int4 m2[NSTAGE];     // rows: {request, items of the position, j | K << 16, target row};
+                       // residual: {request, items of the entry, job, first tile}
   float4 law[NSTAGE];  // residual stages: m_t, 1/S_t, m_d, 1/S_d
   float thr[NSTAGE];   // rank threshold of a target row (+inf: none)
   // chunk ends: each consumer warp leaves its partial (row chunks) or its tile
   // sums (residual items) in the slot of the chunk's last stage, double
   // buffered by the parity of that stage's chunk-end count; the last of the
-  // four warps to arrive (counted in cend) publishes them
+  // four warps to count (in cend) publishes them
   Part cp[NSTAGE][2][RS_CONS_WARPS];
   float ct[NSTAGE][2][RS_CONS_WARPS][RES_TILES_PER_ITEM];
   unsigned cend[NSTAGE];
@@ -92,23 +87,36 @@ struct StreamSmem {
 };
 
 // ---------------------------------------------------------- memory order
+// Returns the old value; this thread's earlier writes are visible to any
+// thread that acquires the new one.
+__device__ __forceinline__ int atom_add_release(int *p, int v) {
+  int old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acquire() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void st_release(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release(int *p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ StreamEntry ldcg_entry(const StreamEntry *e) {
   const int4 *p = reinterpret_cast<const int4 *>(e);
   const int4 x = __ldcg(p), y = __ldcg(p + 1);
-  return StreamEntry{x.x, x.y, x.z, x.w, __int_as_float(y.x), y.y, y.z, 0};
+  return StreamEntry{x.x, x.y, x.z, x.w, __int_as_float(y.x), {0, 0, 0}};
 }
 __device__ __forceinline__ void st_entry(StreamEntry *e, const StreamEntry &v) {
   int4 *p = reinterpret_cast<int4 *>(e);
-  p[0] = make_int4(v.b, v.kind, v.trow, v.drow);
-  p[1] = make_int4(__float_as_int(v.c), v.expect, v.aux, 0);
+  p[0] = make_int4(v.b, v.trow, v.drow, v.job);
+  p[1] = make_int4(__float_as_int(v.c), 0, 0, 0);
 }
 __device__ __forceinline__ Job ldcg_job(const Job *j) {
   const int4 *p = reinterpret_cast<const int4 *>(j);
@@ -117,49 +125,44 @@ __device__ __forceinline__ Job ldcg_job(const Job *j) {
              __int_as_float(y.w)};
 }
 
-__device__ __forceinline__ int entry_expect(const LinearArgs &a, bool drow) {
-  return a.nch_t + (drow ? a.nch_d : 0);
-}
-
 // ------------------------------------------------------------------ setup
-// One thread per request: its record, its first-position entry, the rank
-// thresholds, and a check that every draft token is a vocabulary id (the
-// eager schedule checks them all, so this one does too). The dynamic ready
-// flags are cleared in grid strides.
+// One thread per request: its record, its first rejection (none), its
+// position counters (position 0 needs no acceptance), its residual entry's
+// flag and count, and the draft tokens' logits z_t(d_i) (also the rank
+// count's threshold) and z_d(d_i), gathered once so a decision needs no
+// dependent load. Every draft token must be a vocabulary id (the eager
+// schedule checks them all, so this one does too).
 __global__ void __launch_bounds__(64) k_setup_stream(const LinearArgs a) {
-  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
-  const int gsize = gridDim.x * blockDim.x;
-  for (int e = gtid; e < a.cap_d; e += gsize) a.ready_d[e] = 0;
-  const int b = gtid;
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= a.B) return;
+  const int W = a.max_k + 1;
+  a.ready_d[b] = 0;
+  a.ready_d[a.cap_d + b] = 0;
+  a.rej_at[b] = INT_MAX;
+  for (int j = 0; j < W; ++j) {
+    a.pos_done[b * W + j] = 0;
+    a.pos_join[b * W + j] = j == 0;
+  }
   ReqInfo r;
   const bool ok = load_request(a, b, r);
   a.req[b] = r;
-  a.rs[b] = ReqStream{0, 0, {0, 0}};
   if (!ok) {
     a.hdr->setup_bad = 1;
-    st_entry(a.ent_s + b, StreamEntry{-1, ENT_ROWS, 0, -1, 0.f, 0, -1, 0});
     return;
   }
-  for (int i = 0; i < r.K; ++i)
-    if ((unsigned)a.tokens[r.d0 + i] >= (unsigned)a.V) {
-      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-      a.hdr->setup_bad = 1;
-      break;
-    }
-  const bool drow = r.mode == MODE_SAMPLE && a.stream_draft && r.K > 0;
-  st_entry(a.ent_s + b,
-           StreamEntry{b, ENT_ROWS, r.t0, drow ? r.d0 : -1, r.c, entry_expect(a, drow), r.K << 16, 0});
-  // the draft tokens' logits, gathered once so a decision needs no dependent
-  // load: z_t(d_i) (also the rank count's threshold) and z_d(d_i)
+  const bool drow = r.mode == MODE_SAMPLE && a.stream_draft;
   for (int i = 0; i < r.K; ++i) {
     const int d = a.tokens[r.d0 + i];
     const bool dok = (unsigned)d < (unsigned)a.V;
+    if (!dok) {
+      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+      a.hdr->setup_bad = 1;
+    }
     a.rank_thr[r.t0 + i] =
         dok ? load_elem(a.target + (long long)(r.t0 + i) * a.t_row_bytes, a.tdt, d) : INFINITY;
     if (drow)
-      a.zd_at[r.d0 + i] = dok ? load_elem(a.draft + (long long)(r.d0 + i) * a.d_row_bytes, a.ddt, d)
-                              : 0.f;
+      a.zd_at[r.d0 + i] =
+          dok ? load_elem(a.draft + (long long)(r.d0 + i) * a.d_row_bytes, a.ddt, d) : 0.f;
   }
   a.rank_thr[r.t0 + r.K] = INFINITY;
 }
@@ -173,12 +176,11 @@ __device__ __forceinline__ bool acquire_stage(StreamSmem &sh, long long it, vola
 
 // Streams chunk `chunk` of one row into the ring: its 16-byte aligned
 // interior in TMA bulk copies of up to 16 KB, the unaligned head and tail
-// left to the consumers' scalar loads.
+// left to the consumers' scalar loads. m2 travels with every stage.
 template <bool RANK>
 __device__ bool issue_row_chunk(const LinearArgs &a, StreamSmem &sh, unsigned char *stage_buf,
                                 long long &it, volatile int *abort, int slot, bool draft,
-                                int row, int chunk, const StreamEntry &E) {
-  const float c = E.c;
+                                int row, int chunk, float c, int4 m2) {
   const long long rbytes = draft ? a.d_row_bytes : a.t_row_bytes;
   const int esz = dtype_size(draft ? a.ddt : a.tdt);
   const uint64_t row0 = (uint64_t)((draft ? a.draft : a.target) + (long long)row * rbytes);
@@ -199,7 +201,7 @@ __device__ bool issue_row_chunk(const LinearArgs &a, StreamSmem &sh, unsigned ch
                              (head_n << 16) | (tail_n << 20));
     sh.m1[s] = make_int4(__float_as_int(c), row, (int)((cb0 - row0) / esz),
                          (int)((A1 - row0) / esz));
-    sh.m2[s] = make_int4(E.b, E.expect, E.aux, E.trow);
+    sh.m2[s] = m2;
     if (RANK) sh.thr[s] = thr;
     if (nb > 0) {
       mbar_arrive_tx(&sh.full[s], nb);
@@ -212,12 +214,39 @@ __device__ bool issue_row_chunk(const LinearArgs &a, StreamSmem &sh, unsigned ch
   return true;
 }
 
-// Streams residual item g of entry E: up to RES_TILES_PER_ITEM tiles, each
+// Static ticket t: position j of request b (layer order), chunk k of its
+// target row, then of its draft row. Skipped when the position does not
+// exist, when b already rejected an earlier position (a stale view only
+// costs a read that turns out unneeded), or when k names no chunk. Partial
+// slots are by absolute row: target row r at slot r, draft row r at slot
+// rt_max + r.
+template <bool RANK>
+__device__ bool issue_static(const LinearArgs &a, StreamSmem &sh, unsigned char *stage_buf,
+                             long long &it, volatile int *abort, unsigned long long t) {
+  const unsigned long long e = t / (unsigned)a.stride;
+  const int k = (int)(t % (unsigned)a.stride);
+  const int j = (int)(e / (unsigned)a.B), b = (int)(e % (unsigned)a.B);
+  const ReqInfo r = a.req[b];
+  const int rej = __ldcg(a.rej_at + b);
+  if (r.mode == MODE_SKIP || j > r.K || j > rej) return true;
+  const bool drow = r.mode == MODE_SAMPLE && a.stream_draft && j < r.K;
+  const int4 m2 = make_int4(b, a.nch_t + (drow ? a.nch_d : 0), j | (r.K << 16), r.t0 + j);
+  if (k < a.nch_t)
+    return issue_row_chunk<RANK>(a, sh, stage_buf, it, abort, r.t0 + j, false, r.t0 + j, k, r.c,
+                                 m2);
+  if (drow && k - a.nch_t < a.nch_d)
+    return issue_row_chunk<RANK>(a, sh, stage_buf, it, abort, a.rt_max + r.d0 + j, true,
+                                 r.d0 + j, k - a.nch_t, r.c, m2);
+  return true;
+}
+
+// Residual item g of entry E: up to RES_TILES_PER_ITEM tiles, each
 // SAMPLE_TILE bf16 of the target row and the same elements of the draft row
 // side by side in one stage.
 __device__ bool issue_res_item(const LinearArgs &a, StreamSmem &sh, unsigned char *stage_buf,
                                long long &it, volatile int *abort, const StreamEntry &E, int g) {
-  const Job job = ldcg_job(a.jobs_a + E.aux);
+  if (g >= a.n_res_items) return true;
+  const Job job = ldcg_job(a.jobs_a + E.job);
   const float4 law = make_float4(job.mt, 1.f / job.St, job.md, job.Sd > 0.f ? 1.f / job.Sd : 0.f);
   const uint64_t trow = (uint64_t)(a.target + (long long)E.trow * a.t_row_bytes);
   const uint64_t drow = (uint64_t)(a.draft + (long long)E.drow * a.d_row_bytes);
@@ -230,7 +259,7 @@ __device__ bool issue_res_item(const LinearArgs &a, StreamSmem &sh, unsigned cha
     const uint32_t nb = (uint32_t)ne * 2;
     sh.m0[s] = make_int4(E.b, j, e0, F_RES | (j == j1 - 1 ? F_LAST : 0));
     sh.m1[s] = make_int4(__float_as_int(E.c), ne, j0, j1 - j0);
-    sh.m2[s] = make_int4(E.b, E.expect, E.aux, j0);
+    sh.m2[s] = make_int4(E.b, a.n_res_items, E.job, j0);
     sh.law[s] = law;
     mbar_arrive_tx(&sh.full[s], 2 * nb);
     unsigned char *dst = stage_buf + (size_t)s * TILE_BYTES;
@@ -241,35 +270,7 @@ __device__ bool issue_res_item(const LinearArgs &a, StreamSmem &sh, unsigned cha
   return true;
 }
 
-// Work item k of entry E: target chunks first, then draft chunks, or a
-// residual item; tickets past the entry's items carry nothing.
-template <bool RANK>
-__device__ bool issue_item(const LinearArgs &a, StreamSmem &sh, unsigned char *stage_buf,
-                           long long &it, volatile int *abort, const StreamEntry &E, int k) {
-  if (E.b < 0) return true;
-  if (E.kind == ENT_RES)
-    return k < a.n_res_items ? issue_res_item(a, sh, stage_buf, it, abort, E, k) : true;
-  if (k < a.nch_t)
-    return issue_row_chunk<RANK>(a, sh, stage_buf, it, abort, E.b, false, E.trow, k, E);
-  k -= a.nch_t;
-  if (E.drow >= 0 && k < a.nch_d)
-    return issue_row_chunk<RANK>(a, sh, stage_buf, it, abort, a.B + E.b, true, E.drow, k, E);
-  return true;
-}
-
-// --------------------------------------------------- completions, entries
-// Appends a dynamic entry and publishes it (release store of its flag).
-__device__ void push_entry(const LinearArgs &a, const StreamEntry &E) {
-  const int e = atomicAdd(&a.hdr->n_alloc_d, 1);
-  if (e >= a.cap_d) {   // cannot happen: a request appends at most K + 1 entries
-    set_status(a.hdr, SPEC_ERR_TIMEOUT, -4);
-    return;
-  }
-  st_entry(a.ent_d + e, E);
-  __threadfence();
-  st_release(a.ready_d + e, 1);
-}
-
+// ------------------------------------------------------- request progress
 // Request b's final token is written (or queued as a final-draw job). The
 // last request to finish moves the errors the decisions reported (empty
 // rows) into the status word.
@@ -285,8 +286,8 @@ __device__ void finish_one(const LinearArgs &a, int lane) {
   __syncwarp();
 }
 
-// Row statistics of `n` (<= 32) chunk partials held one per lane, merged
-// in the order of warp_row_stat (the same bits).
+// Row statistics of at most 32 chunk partials held one per lane, merged in
+// the order of warp_row_stat (the same bits).
 __device__ __forceinline__ RowStat lane_parts_stat(const Part &p, bool have, float c) {
   float m = NO_MAX, S = 0.f;
   int idx = 0x7fffffff;
@@ -301,95 +302,110 @@ __device__ __forceinline__ RowStat lane_parts_stat(const Part &p, bool have, flo
   return RowStat{m, S, idx};
 }
 
-// Decision on position j of request b (target row trow, K drafts, c =
-// log2(e)/T, 0 for greedy), once both of its rows are complete: accept and
-// list the next position, or finish the request. Every input comes from one
-// round of independent loads: the chunk partials, the token and the
-// gathered logits z_t(d), z_d(d).
-__device__ __noinline__ void stream_decide(const LinearArgs &a, int b, int j, int K, int trow,
+// Adds one event to position j's join (rows complete, previous position
+// accepted); true for the second of the two.
+__device__ __forceinline__ bool join_second(const LinearArgs &a, int b, int j) {
+  const bool second = atomicAdd(a.pos_join + b * (a.max_k + 1) + j, 1) == 1;
+  if (second) __threadfence();
+  return second;
+}
+
+// Decisions on request b from position j on (target rows from t0, K
+// drafts, c = log2(e)/T, 0 for greedy): both of position j's events are in.
+// Every input of a decision comes from one round of independent loads: the
+// chunk partials, the token and the gathered logits z_t(d), z_d(d). An
+// accepted position whose successor's rows are already complete goes on to
+// decide the successor.
+__device__ __noinline__ void stream_decide(const LinearArgs &a, int b, int j, int K, int t0,
                                            float c, int lane) {
   ReqInfo r;
-  r.t0 = trow - j;
-  r.d0 = r.t0 - b;
+  r.t0 = t0;
+  r.d0 = t0 - b;
   r.K = K;
   r.mode = c != 0.f ? MODE_SAMPLE : MODE_GREEDY;
   r.c = c;
+  r.n = 0;
+  r.pad[0] = r.pad[1] = 0;
   const bool sample = r.mode == MODE_SAMPLE;
-  const bool drow = sample && a.stream_draft && j < K;
   const bool fast = a.nch_t * RS_CONS_WARPS <= 32 && a.nch_d * RS_CONS_WARPS <= 32;
-  const long long tb = (long long)b * a.nch_max * RS_CONS_WARPS;
-  const long long db = (long long)(a.B + b) * a.nch_max * RS_CONS_WARPS;
-  const bool th = lane < a.nch_t * RS_CONS_WARPS, dh = drow && lane < a.nch_d * RS_CONS_WARPS;
-  Part tp{}, dp{};
-  int d = -1;
-  float zt = 0.f, zd = 0.f;
-  if (fast && th) tp = ldcg_part(a.part + tb + lane);
-  if (fast && dh) dp = ldcg_part(a.part + db + lane);
-  if (j < K) {
-    d = a.tokens[r.d0 + j];
-    zt = __ldcg(a.rank_thr + trow);
-    if (drow) zd = __ldcg(a.zd_at + r.d0 + j);
-  }
-  const RowStat ts = fast ? lane_parts_stat(tp, th, c) : target_stat(a, b, c, lane);
-  RowStat ds{NO_MAX, 0.f, 0x7fffffff};
-  int n = K;
-  if (j < K) {
-    int rank = 0;
-    if (a.want_rank) {
-      if (fast) {
-        rank = th ? tp.cnt : 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-        rank += 1;
-      } else {
-        rank = 1 + warp_row_count(a, b, lane);
-      }
+  while (true) {
+    const bool drow = sample && a.stream_draft && j < K;
+    const int tslot = r.t0 + j, dslot = a.rt_max + r.d0 + j;
+    const bool th = lane < a.nch_t * RS_CONS_WARPS, dh = drow && lane < a.nch_d * RS_CONS_WARPS;
+    Part tp{}, dp{};
+    int d = -1;
+    float zt = 0.f, zd = 0.f;
+    if (fast && th) tp = ldcg_part(a.part + (long long)tslot * a.nch_max * RS_CONS_WARPS + lane);
+    if (fast && dh) dp = ldcg_part(a.part + (long long)dslot * a.nch_max * RS_CONS_WARPS + lane);
+    if (j < K) {
+      d = a.tokens[r.d0 + j];
+      zt = __ldcg(a.rank_thr + r.t0 + j);
+      if (drow) zd = __ldcg(a.zd_at + r.d0 + j);
     }
-    if (drow) ds = fast ? lane_parts_stat(dp, dh, c) : draft_stat(a, a.B + b, c, lane);
-    const bool rej = __shfl_sync(
-        0xffffffffu,
-        lane == 0 && position_rejects_z(a, b, r, j, sample, ts, ds, rank, d, zt, zd, false), 0);
-    if (!rej) {   // accepted: the next position's rows
-      if (lane == 0) {
-        const bool next_drow = sample && a.stream_draft && j + 1 < K;
-        push_entry(a, StreamEntry{b, ENT_ROWS, trow + 1, next_drow ? r.d0 + j + 1 : -1, c,
-                                  entry_expect(a, next_drow), (j + 1) | (K << 16), 0});
+    const RowStat ts = fast ? lane_parts_stat(tp, th, c) : target_stat(a, tslot, c, lane);
+    RowStat ds{NO_MAX, 0.f, 0x7fffffff};
+    int n = K;
+    if (j < K) {
+      int rank = 0;
+      if (a.want_rank) {
+        if (fast) {
+          rank = th ? tp.cnt : 0;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+          rank += 1;
+        } else {
+          rank = 1 + warp_row_count(a, tslot, lane);
+        }
       }
+      if (drow) ds = fast ? lane_parts_stat(dp, dh, c) : draft_stat(a, dslot, c, lane);
+      const bool rej = __shfl_sync(
+          0xffffffffu,
+          lane == 0 && position_rejects_z(a, b, r, j, sample, ts, ds, rank, d, zt, zd, false), 0);
+      if (!rej) {   // accepted: position j + 1 is decided once its rows are complete
+        const bool go = __shfl_sync(0xffffffffu, lane == 0 && join_second(a, b, j + 1), 0);
+        if (!go) return;
+        ++j;
+        continue;
+      }
+      n = j;
+      if (lane == 0) a.rej_at[b] = j;   // later positions' rows are no longer read
+    }
+    // positions after n+1 are not reported
+    for (int i = n + 1 + lane; i < K; i += 32) {
+      if (a.out_pq) {
+        a.out_pq[2LL * (r.d0 + i)] = __int_as_float(0x7fc00000);
+        a.out_pq[2LL * (r.d0 + i) + 1] = __int_as_float(0x7fc00000);
+      }
+      if (a.out_rank) a.out_rank[r.d0 + i] = -1;
+    }
+    const int W = a.max_k + 1;
+    int32_t *out = a.out_tokens + (long long)b * W;
+    for (int jj = lane; jj < W; jj += 32) out[jj] = jj < n ? a.tokens[r.d0 + jj] : -1;
+    if (lane == 0) a.out_accepted[b] = n;
+    __syncwarp();
+    if (!sample) {   // greedy: the target's argmax replaces the rejected draft
+      if (lane == 0) out[n] = ts.idx;
+      finish_one(a, lane);
       return;
     }
-    n = j;
-  }
-  // positions after n+1 were never read
-  for (int i = n + 1 + lane; i < K; i += 32) {
-    if (a.out_pq) {
-      a.out_pq[2LL * (r.d0 + i)] = __int_as_float(0x7fc00000);
-      a.out_pq[2LL * (r.d0 + i) + 1] = __int_as_float(0x7fc00000);
+    const bool residual = n < K && a.stream_draft;
+    if (lane == 0) {
+      if (residual) {
+        // the residual's tile sums are summed in this kernel, the draw after it
+        const int ja = atomicAdd(&a.hdr->n_jobs_a, 1);
+        a.jobs_a[ja] = Job{b, n, 1, 0, ts.m, ts.S, ds.m, ds.S};
+        const int e = atomicAdd(&a.hdr->n_alloc_d, 1);   // < B: one per request
+        st_entry(a.ent_d + e, StreamEntry{b, r.t0 + n, r.d0 + n, ja, c, {0, 0, 0}});
+        __threadfence();
+        st_release(a.ready_d + e, 1);
+      } else {   // bonus draw from p_{K+1}, after this kernel
+        a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = Job{b, n, 2, 0, ts.m, ts.S, 0.f, 0.f};
+      }
     }
-    if (a.out_rank) a.out_rank[r.d0 + i] = -1;
-  }
-  const int W = a.max_k + 1;
-  int32_t *out = a.out_tokens + (long long)b * W;
-  for (int jj = lane; jj < W; jj += 32) out[jj] = jj < n ? a.tokens[r.d0 + jj] : -1;
-  if (lane == 0) a.out_accepted[b] = n;
-  __syncwarp();
-  if (!sample) {   // greedy: the target's argmax replaces the rejected draft
-    if (lane == 0) out[n] = ts.idx;
-    finish_one(a, lane);
+    if (!residual) finish_one(a, lane);
+    __syncwarp();
     return;
   }
-  const bool residual = n < K && a.stream_draft;
-  if (lane == 0) {
-    if (residual) {
-      // the residual's tile sums are summed here, the draw after this kernel
-      const int ja = atomicAdd(&a.hdr->n_jobs_a, 1);
-      a.jobs_a[ja] = Job{b, n, 1, 0, ts.m, ts.S, ds.m, ds.S};
-      push_entry(a, StreamEntry{b, ENT_RES, trow, r.d0 + n, c, a.n_res_items, ja, 0});
-    } else {   // bonus draw from p_{K+1}, after this kernel
-      a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = Job{b, n, 2, 0, ts.m, ts.S, 0.f, 0.f};
-    }
-  }
-  if (!residual) finish_one(a, lane);
-  __syncwarp();
 }
 
 // A consumer warp at the end of a chunk (row partial p) or a residual item
@@ -416,35 +432,38 @@ __device__ __forceinline__ bool chunk_end_count(StreamSmem &sh, int s, int par, 
 }
 
 // The closer, after releasing the stage: the four warps' results to global
-// memory, one completion of the request's entry, and, for the entry's last
-// completion, the decision on the position (rows) or the end of the request
-// (residual). Only this warp waits on global memory.
+// memory, one completion of the position's rows (or of the residual entry),
+// and, for the last completion, the position's join (its decision when the
+// previous position was accepted) or the end of the request. Only this warp
+// waits on global memory.
 __device__ __forceinline__ void chunk_close(const LinearArgs &a, StreamSmem &sh, int s, int par,
                                             int lane, bool res, const int4 m0, const int4 m1,
                                             const int4 m2) {
-  int last = 0;
+  int go = 0;
   if (lane == 0) {
     __threadfence_block();
+    int *count;
     if (res) {   // m2.z: job, m2.w: first tile, m1.w: tiles in the item
       for (int t = 0; t < m1.w; ++t)
         reinterpret_cast<float4 *>(a.tsum)[(long long)m2.z * a.ntiles + m2.w + t] =
             make_float4(sh.ct[s][par][0][t], sh.ct[s][par][1][t], sh.ct[s][par][2][t],
                         sh.ct[s][par][3][t]);
+      count = a.ready_d + a.cap_d + m2.x;   // the residual entry's own count
     } else {
       Part *dst = a.part + ((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS;
 #pragma unroll
       for (int w = 0; w < RS_CONS_WARPS; ++w) dst[w] = sh.cp[s][par][w];
+      count = a.pos_done + m2.x * (a.max_k + 1) + (m2.z & 0xffff);
     }
-    __threadfence();
-    last = atomicAdd(&a.rs[m2.x].count, 1) + 1 == m2.y;
-    if (last) {
-      a.rs[m2.x].count = 0;   // the request's next entry starts a new count
-      __threadfence();
+    if (atom_add_release(count, 1) + 1 == m2.y) {
+      fence_acquire();
+      go = res ? 1 : join_second(a, m2.x, m2.z & 0xffff);
     }
   }
-  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  if (!__shfl_sync(0xffffffffu, go, 0)) return;
   if (res) finish_one(a, lane);
-  else stream_decide(a, m2.x, m2.z & 0xffff, m2.z >> 16, m2.w, __int_as_float(m1.x), lane);
+  else stream_decide(a, m2.x, m2.z & 0xffff, m2.z >> 16, m2.w - (m2.z & 0xffff),
+                     __int_as_float(m1.x), lane);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -486,27 +505,28 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
     if (lane != 0) return;
     long long it = 0;
     bool ok = true;
-    const unsigned long long n_static = (unsigned long long)a.B * a.stride;
-    const unsigned long long n_dyn = (unsigned long long)a.cap_d * a.stride;
+    const unsigned long long n_static =
+        (unsigned long long)(a.max_k + 1) * (unsigned)a.B * (unsigned)a.stride;
+    const unsigned long long n_dyn = (unsigned long long)a.cap_d * a.n_res_items;
     unsigned long long st_t = atomicAdd(&a.hdr->work_s, 1ull);
     unsigned long long dy_t = atomicAdd(&a.hdr->work_d, 1ull);
     while (true) {
-      // 1. the held dynamic ticket, once its entry exists
-      const int e = (int)(dy_t / a.stride);
+      // 1. the held residual ticket, once its entry exists
+      const int e = (int)(dy_t / (unsigned)a.n_res_items);
       if (dy_t < n_dyn && ld_acquire(a.ready_d + e)) {
         const StreamEntry E = ldcg_entry(a.ent_d + e);
-        if (!issue_item<RANK>(a, sh, stage_buf, it, abort, E, (int)(dy_t % a.stride))) {
+        if (!issue_res_item(a, sh, stage_buf, it, abort, E,
+                            (int)(dy_t % (unsigned)a.n_res_items))) {
           ok = false;
           break;
         }
         dy_t = atomicAdd(&a.hdr->work_d, 1ull);
         continue;
       }
-      // 2. static work meanwhile
+      // 2. the static list meanwhile
       if (st_t < n_static) {
         const unsigned long long next = atomicAdd(&a.hdr->work_s, 1ull);
-        const StreamEntry E = ldcg_entry(a.ent_s + st_t / a.stride);
-        if (!issue_item<RANK>(a, sh, stage_buf, it, abort, E, (int)(st_t % a.stride))) {
+        if (!issue_static<RANK>(a, sh, stage_buf, it, abort, st_t)) {
           ok = false;
           break;
         }
