@@ -162,14 +162,19 @@ int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
  *   min_prob  guard: reject d_i when p_i(d_i) < min_prob; 0 = off.
  *             SPEC_RULE_CACTUS only.
  *   flags     0 or SPEC_EXT_LAZY: position-lazy verification. Position
- *             i's rows are read only when drafts 1..i-1 were accepted (one
- *             row pass and one decision per position, max_k + 1 rounds), so a
- *             request reads rows 1..n+1 only (nalar.dev "Penolakan
+ *             i is decided only when drafts 1..i-1 were accepted, so a
+ *             request's decisions use rows 1..n+1 only (nalar.dev "Penolakan
  *             memendekkan pekerjaan speculative": proposals after a rejected
  *             one are discarded). Same tokens and counts as the eager call;
- *             out_pq is NaN and out_rank -1 on the positions after n+1, and
- *             those positions' tokens are not validated. The top-128 rule
- *             still cuts every draft row.
+ *             out_pq is NaN and out_rank -1 on the positions after n+1.
+ *             Dense bf16 logits with V a multiple of 8 and no out_kl run as
+ *             one persistent kernel that scans every position's rows in
+ *             layer order, skips a request's rows once it has rejected, and
+ *             checks every draft token; it may still read some rows after a
+ *             rejection (never used, so they are not checked). Other inputs
+ *             run one row pass and one decision per position (max_k + 1
+ *             rounds), read rows 1..n+1 only and do not check the tokens
+ *             after n+1. The top-128 rule still cuts every draft row.
  *   out_rank  optional device [R_d] int32: the target rank of every draft
  *             token (every request and rule; also after the first
  *             rejection unless lazy). NULL to skip.
@@ -321,8 +326,9 @@ int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos,
  * call's stream, then forgets them. Pass NULLs to clear. The pass streams
  * every vocabulary row once and dominates the call's time, so
  * cudaEventElapsedTime(before, after) is that kernel's duration. A
- * position-lazy call (SPEC_EXT_LAZY) records them around all its rounds:
- * every row pass and every per-round decision.
+ * position-lazy call (SPEC_EXT_LAZY) records them around its streaming
+ * kernel, or, on the multi-launch schedule, around all its rounds: every row
+ * pass and every per-round decision.
  */
 int spec_profile_row_pass(void *before, void *after);
 

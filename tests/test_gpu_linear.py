@@ -410,9 +410,10 @@ def test_lazy_with_probability_and_sparse_drafts():
     assert_lazy_matches(g, ref, lb)
 
 
-def test_lazy_never_reads_rows_after_the_first_rejection():
+def test_lazy_never_uses_rows_after_the_first_rejection():
     """Rows after position n+1 are set to -inf everywhere (no mass): the
-    eager call reports them, the lazy call never touches them."""
+    eager call reports them, the lazy call never uses them (the streaming
+    kernel may read some of them before the rejection is known)."""
     lb = S.make_linear(2, device=DEV, B=32, K=(2, 6), V=8192, input_seed=99, sigma=1.5,
                        T=[0.0, 1.0] * 16)
     ref = oracle_linear(lb)
