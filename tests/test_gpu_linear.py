@@ -212,6 +212,30 @@ def test_draft_topk_softmax_edge_cases(dtype, V, T):
     assert_probs_close(prob.cpu().numpy(), rp, "top-128 probabilities")
 
 
+def test_draft_topk_softmax_row_orders():
+    """Rows that defeat a bound taken from the leading logits (ascending
+    ramps, whose leading block holds the smallest logits), rows whose top 128
+    sit inside it (descending ramps), a block of ties straddling the 128th
+    logit, and logit-shaped rows: the one-pass selection, its overflow
+    fallback and the tie rule against the oracle."""
+    g = torch.Generator(device=DEV).manual_seed(17)
+    V = 20480
+    ramp = torch.arange(V, device=DEV, dtype=torch.float32) / 64
+    rows = [ramp, ramp.flip(0), torch.zeros(V, device=DEV), ramp.clone(), ramp.clone()]
+    rows[2][5000:5300] = 3.0                       # 300 ties: 128 lowest ids win
+    rows[3][100:400] = 1000.0                      # ties inside the leading block
+    rows[4] = (2.0 * torch.randn(V, generator=g, device=DEV)
+               - 1.1 * torch.log(torch.randperm(V, generator=g, device=DEV).float() + 1))
+    z = torch.stack(rows).to(torch.bfloat16).contiguous()
+    cu = torch.tensor([0, 5], dtype=torch.int32, device=DEV)
+    temp = torch.tensor([1.0], device=DEV)
+    idx, prob, ws = sv.draft_topk_softmax(z, cu, temp)
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    ri, rp = O.draft_topk_softmax(z.cpu(), cu.cpu().numpy(), temp.cpu().numpy())
+    assert np.array_equal(idx.cpu().numpy(), ri)
+    assert_probs_close(prob.cpu().numpy(), rp, "top-128 probabilities")
+
+
 # ------------------------------------------- relaxed CACTUS rule and ranks
 CACTUS_CASES = [
     dict(alpha=0.0, max_rank=0, min_prob=0.0),     # the lossless test
