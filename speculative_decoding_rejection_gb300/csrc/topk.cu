@@ -3,8 +3,11 @@
 // to -inf, and the softmax runs over the survivors).
 //
 // One 512-thread CTA per row at a time, two CTAs per SM, rows taken in grid
-// strides. bf16 rows (V a multiple of 8, V >= 4096) take a two-pass fast
-// path: a packed bf16 max pass leaves each thread's maximum; each warp sorts
+// strides (measured faster than 3 or 4 CTAs of 256 threads, whose rows in
+// flight outgrow L2 between the passes). bf16 rows (V a multiple of 8,
+// V >= 4096) take a two-pass fast path, each pass keeping eight 16-byte
+// loads in flight per thread: a packed bf16 max pass leaves each thread's
+// maximum; each warp sorts
 // its 32 maxima, and the smallest of the warps' (128/16 = 8)-th largest
 // maxima bounds the 128-th largest logit from below (16 warps x 8 threads
 // hold an element at least that large). The second pass, served from L2, gathers the few hundred
@@ -144,10 +147,17 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
   const uint4 *vp = reinterpret_cast<const uint4 *>(row);
   const int nvec = V / 8;
   uint32_t pm = 0xff80ff80u;   // (-inf, -inf)
-#pragma unroll 8
-  for (int v = t; v < nvec; v += TK_THREADS) {
-    const uint4 w = __ldg(vp + v);
-    pm = bmax2(pm, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+  constexpr uint32_t NINF2 = 0xff80ff80u;
+  // eight 16-byte loads in flight per thread before any is used
+  for (int v0 = t; v0 < nvec; v0 += 8 * TK_THREADS) {
+    uint4 w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int v = v0 + u * TK_THREADS;
+      w[u] = v < nvec ? __ldg(vp + v) : make_uint4(NINF2, NINF2, NINF2, NINF2);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) pm = bmax2(pm, bmax2(bmax2(w[u].x, w[u].y), bmax2(w[u].z, w[u].w)));
   }
   float m = fmaxf(bf16lo(pm), bf16hi(pm));
   // descending bitonic sort of the warp's 32 maxima
@@ -163,19 +173,30 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
   __syncthreads();
   float bound = sh.tmax[0];
   for (int w = 1; w < TK_WARPS; ++w) bound = fminf(bound, sh.tmax[w]);
-#pragma unroll 4
-  for (int v = t; v < nvec; v += TK_THREADS) {
-    const uint4 w = __ldg(vp + v);
-    const uint32_t m8 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
-    if (fmaxf(bf16lo(m8), bf16hi(m8)) < bound) continue;
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  // the second pass (from L2), eight loads in flight again; a group of 8
+  // logits is looked at only when its packed maximum reaches the bound
+  for (int v0 = t; v0 < nvec; v0 += 8 * TK_THREADS) {
+    uint4 wv[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t b = (k & 1) ? (ww[k >> 1] >> 16) : (ww[k >> 1] & 0xffffu);
-      if (__uint_as_float(b << 16) >= bound) {
-        const int slot = atomicAdd(&sh.cand_n, 1);
-        if (slot < CAND_CAP)
-          sh.cand[slot] = ((unsigned long long)key_of(b, true) << 32) | (~(unsigned)(8 * v + k));
+    for (int u = 0; u < 8; ++u) {
+      const int v = v0 + u * TK_THREADS;
+      wv[u] = v < nvec ? __ldg(vp + v) : make_uint4(NINF2, NINF2, NINF2, NINF2);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int v = v0 + u * TK_THREADS;
+      const uint4 w = wv[u];
+      const uint32_t m8 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+      if (v >= nvec || fmaxf(bf16lo(m8), bf16hi(m8)) < bound) continue;
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t b = (k & 1) ? (ww[k >> 1] >> 16) : (ww[k >> 1] & 0xffffu);
+        if (__uint_as_float(b << 16) >= bound) {
+          const int slot = atomicAdd(&sh.cand_n, 1);
+          if (slot < CAND_CAP)
+            sh.cand[slot] = ((unsigned long long)key_of(b, true) << 32) | (~(unsigned)(8 * v + k));
+        }
       }
     }
   }
