@@ -274,6 +274,9 @@ size_t spec_verify_tree_workspace(int B, int n_nodes, int V, int max_depth,
  *   out_accepted [B] int32: number of accepted nodes.
  *   out_path    [B, max_depth+1] int32: local ids of the accepted nodes, -1
  *               padded. May be NULL.
+ * Only the rows of the nodes the walk visits (the root and the accepted
+ * path) are read: a node's statistics are computed when the walk reaches it,
+ * so rows of other nodes are neither read nor checked.
  */
 int spec_verify_tree(const void *target, int tdt, const void *draft, int ddt,
                      int dk, const int32_t *node_token, const int32_t *parent,
@@ -322,13 +325,14 @@ int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos,
  * Profiling aid. Registers two CUDA events (cudaEvent_t, created by the
  * caller) for the next spec_verify_linear / spec_verify_tree call made by
  * the calling host thread: that call records `before` immediately before it
- * launches its row-statistics pass and `after` immediately after, on the
- * call's stream, then forgets them. Pass NULLs to clear. The pass streams
- * every vocabulary row once and dominates the call's time, so
- * cudaEventElapsedTime(before, after) is that kernel's duration. A
- * position-lazy call (SPEC_EXT_LAZY) records them around its streaming
- * kernel, or, on the multi-launch schedule, around all its rounds: every row
- * pass and every per-round decision.
+ * launches its dominant kernel and `after` immediately after, on the call's
+ * stream, then forgets them. Pass NULLs to clear. The dominant kernel is the
+ * row-statistics pass of an eager linear call (it streams every vocabulary
+ * row once), the top-128 select under SPEC_RULE_STRICT_TOP128, the streaming
+ * kernel of a position-lazy call (SPEC_EXT_LAZY) or,
+ * on its multi-launch schedule, all its rounds (every row pass and every
+ * per-round decision), and the walk of a tree call. So
+ * cudaEventElapsedTime(before, after) is that kernel's duration.
  */
 int spec_profile_row_pass(void *before, void *after);
 

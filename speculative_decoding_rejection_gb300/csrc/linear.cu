@@ -811,10 +811,16 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   k_setup_linear<<<(B + 63) / 64, 64, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (rule == SPEC_RULE_STRICT_TOP128) {
+    // the top-128 select reads every draft row and dominates this rule's
+    // call: profiling events, if registered, bracket it
+    cudaEvent_t before, after;
+    take_row_pass_events(&before, &after);
+    if (before && cudaEventRecord(before, st) != cudaSuccess) return SPEC_ERR_CUDA;
     const int rc = launch_topk128(draft, ddt, B * max_k, V, cu_draft, temperature, B,
                                   reinterpret_cast<int32_t *>(ws + L.tk_idx),
                                   reinterpret_cast<float *>(ws + L.tk_prob), a.hdr, st);
     if (rc != SPEC_OK) return rc;
+    if (after && cudaEventRecord(after, st) != cudaSuccess) return SPEC_ERR_CUDA;
   }
   RowPassArgs rp;
   rp.base[0] = a.target;

@@ -13,10 +13,13 @@
 // u(seed, b, v + 1, 1) (residual) or u(seed, b, v + 1, 2) (bonus), so a chain
 // tree reproduces the linear verifier draw for draw.
 //
-// Pipeline: a one-block setup kernel validates every tree and lists the node
-// rows; the shared row pass computes max / normaliser / argmax of every
-// target row and of the draft rows of internal nodes; then one CTA per tree
-// walks it. The residual laws are never stored: every pass recomputes
+// Pipeline: a one-block-per-tree setup kernel validates every tree; then a
+// cluster of CTAs per tree walks it. The walk reads only the rows of the
+// nodes it visits (the others never enter the decision): at each visited
+// node the cluster first reduces the node's target row (and, for a sampling
+// node with children, its draft row) to max / normaliser / argmax, each CTA
+// over its vocabulary slice, then tests the children. The residual laws are
+// never stored: every pass recomputes
 // p_j(y) from p(y) and q(y) through the chain of normalisers, which are
 // scalars. A token rejected at step k has q_k > p_k, so p_{k+1} is exactly 0
 // there and stays 0; the chain can therefore use q(y) s_j for every y without
@@ -61,27 +64,18 @@ struct TreeArgs {
   int32_t *out_tokens, *out_accepted, *out_path;
   WsHeader *hdr;
   TreeInfo *tree;
-  RowTask *list;
-  Part *part;
   long long t_row_bytes, d_row_bytes;
-  int nch_t, nch_d, nch_max;
-  int stream_draft;
 };
 
 struct TreeLayout {
-  size_t hdr, tree, list, part, total;
-  int nch_max;
+  size_t hdr, tree, total;
 };
 
-static TreeLayout tree_layout(int B, int n_nodes, int V) {
+static TreeLayout tree_layout(int B) {
   TreeLayout L;
-  L.nch_max = nchunks(V, SPEC_F32, CHUNK_BYTES);
-  const size_t rows = 2 * (size_t)n_nodes;
   size_t o = 0;
   L.hdr = o;  o += align256(sizeof(WsHeader));
   L.tree = o; o += align256(sizeof(TreeInfo) * (size_t)B);
-  L.list = o; o += align256(sizeof(RowTask) * rows);
-  L.part = o; o += align256(sizeof(Part) * rows * L.nch_max * RS_CONS_WARPS);
   L.total = o;
   return L;
 }
@@ -89,10 +83,8 @@ static TreeLayout tree_layout(int B, int n_nodes, int V) {
 // ------------------------------------------------------------------ setup
 // One block per tree. The tree's parent ids are staged in shared memory; one
 // thread derives depths in topological order, the block counts children and
-// checks tokens. The row list is indexed by slot (target row n at position
-// n, draft row n at position n_nodes + n), so trees write their entries
-// without a scan. The header was cleared before the launch; an invalid tree
-// sets the status word and every later kernel of the call skips its work.
+// checks tokens. The header was cleared before the launch; an invalid tree
+// sets the status word and the walk of every tree is skipped.
 constexpr int SETUP_THREADS = 256;
 
 __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) {
@@ -101,14 +93,6 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
   __shared__ int s_kids[SPEC_MAX_TREE_NODES];
   __shared__ int s_bad;
   const int b = blockIdx.x, t = threadIdx.x;
-  if (b == 0 && t == 0) a.hdr->n_list = 2 * a.n_nodes;
-  {   // rows past the last tree (n_nodes > cu[B]) are not streamed
-    const int used = min(max(a.cu[a.B], 0), a.n_nodes);
-    for (int n = used + b * SETUP_THREADS + t; n < a.n_nodes; n += gridDim.x * SETUP_THREADS) {
-      a.list[n].slot = -1;
-      a.list[a.n_nodes + n].slot = -1;
-    }
-  }
   TreeInfo ti;
   ti.base = a.cu[b];
   ti.N = a.cu[b + 1] - a.cu[b];
@@ -155,13 +139,6 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
     a.tree[b] = ti;
     if (!ok) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
   }
-  if (!ok) return;
-  const bool drafts = ti.mode == MODE_SAMPLE && a.stream_draft;
-  for (int c = t; c < ti.N; c += SETUP_THREADS) {
-    const int n = ti.base + c;
-    a.list[n] = RowTask{n, n, 0, ti.c};
-    a.list[a.n_nodes + n] = RowTask{drafts && s_kids[c] > 0 ? a.n_nodes + n : -1, n, 1, ti.c};
-  }
 }
 
 // ------------------------------------------------------------------- walk
@@ -178,6 +155,9 @@ struct WalkSmem {
   float s[SPEC_MAX_TREE_BRANCH + 1];     // 1 / (1 - q(E_j))
   float rinv[SPEC_MAX_TREE_BRANCH + 1];  // 1 / Z_j
   int skip[SPEC_MAX_TREE_BRANCH + 1];    // Z_j == 0: p_{j+1} = p_j
+  RowStat wst[WALK_THREADS / 32][2];     // per-warp statistics of a node pass (target, draft)
+  RowStat st[2][2];                      // this slice's statistics, by pass parity (target, draft)
+  RowStat node[2];                       // the node's statistics (target, draft)
   int nk, jstar, xmin, xlast, rstar, accepted_child, par, ok, go;
   float carry, target, Z;
 };
@@ -358,11 +338,90 @@ __device__ int weight_draw(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, f
   return x;
 }
 
-// Row statistics from the row pass's partials; every warp merges them the
-// same fixed way, so all threads of the cluster get identical values.
-__device__ __forceinline__ RowStat node_stat(const TreeArgs &a, int slot, int nch, float c) {
-  return warp_row_stat(a.part + (long long)slot * a.nch_max * RS_CONS_WARPS, nch * RS_CONS_WARPS,
-                       c, (int)threadIdx.x & 31);
+// Running statistics of SAMPLE_EPT consecutive logits into (m, S, idx):
+// max, sum of 2^((z - m) c) (none when c is 0), lowest index of the max.
+__device__ __forceinline__ void stat_update(const float *z, int x0, float c, float &m, float &S,
+                                            int &idx) {
+  float vm = z[0];
+  int j = 0;
+#pragma unroll
+  for (int k = 1; k < SAMPLE_EPT; ++k)
+    if (z[k] > vm) { vm = z[k]; j = k; }
+  if (vm > m) {
+    if (c != 0.f) S *= ex2((m - vm) * c);
+    m = vm;
+    idx = x0 + j;
+  }
+  if (c != 0.f) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < SAMPLE_EPT; ++k) t += ex2((z[k] - m) * c);
+    S += t;
+  }
+}
+
+// Statistics of node rows computed by the cluster: every CTA reduces its
+// vocabulary slice of the target row (and, when `drow` is set, of the draft
+// row), the slices are exchanged through distributed shared memory and merged
+// in rank order, so every CTA gets the same bits. Only the rows of nodes the
+// walk visits are read.
+__device__ void node_stats(const TreeArgs &a, WalkSmem &sh, const char *trow, const char *drow,
+                           float c, const Slice sl, cg::cluster_group &cluster, RowStat &ts,
+                           RowStat &ds) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool tvec = ((uintptr_t)trow & 15) == 0, dvec = drow && ((uintptr_t)drow & 15) == 0;
+  float m = NO_MAX, S = 0.f, md = NO_MAX, Sd = 0.f;
+  int idx = 0x7fffffff, idd = 0x7fffffff;
+  float z[SAMPLE_EPT];
+#pragma unroll 2
+  for (int j = sl.j0; j < sl.j1; ++j) {
+    const int x0 = j * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
+    load_ept(trow, a.tdt, tvec, x0, a.V, -INFINITY, z);
+    stat_update(z, x0, c, m, S, idx);
+    if (drow) {
+      load_ept(drow, a.ddt, dvec, x0, a.V, -INFINITY, z);
+      stat_update(z, x0, c, md, Sd, idd);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    merge_stat(m, S, idx, m2, S2, i2, c);
+    const float md2 = __shfl_xor_sync(0xffffffffu, md, o);
+    const float Sd2 = __shfl_xor_sync(0xffffffffu, Sd, o);
+    const int id2 = __shfl_xor_sync(0xffffffffu, idd, o);
+    merge_stat(md, Sd, idd, md2, Sd2, id2, c);
+  }
+  if (lane == 0) {
+    sh.wst[warp][0] = RowStat{m, S, idx};
+    sh.wst[warp][1] = RowStat{md, Sd, idd};
+  }
+  __syncthreads();
+  const int par = sh.par;
+  if (threadIdx.x < 2) {   // thread 0: the target row, thread 1: the draft row
+    const int r = threadIdx.x;
+    RowStat q{NO_MAX, 0.f, 0x7fffffff};
+    for (int w = 0; w < WALK_THREADS / 32; ++w)
+      merge_stat(q.m, q.S, q.idx, sh.wst[w][r].m, sh.wst[w][r].S, sh.wst[w][r].idx, c);
+    sh.st[par][r] = q;
+  }
+  cluster.sync();   // every slice's statistics written (slots alternate by parity)
+  if (threadIdx.x < 2) {
+    const int r = threadIdx.x;
+    RowStat q{NO_MAX, 0.f, 0x7fffffff};
+    for (int k = 0; k < WALK_CLUSTER; ++k) {
+      const RowStat *o = cluster.map_shared_rank(&sh.st[par][r], k);
+      merge_stat(q.m, q.S, q.idx, o->m, o->S, o->idx, c);
+    }
+    sh.node[r] = q;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sh.par = par ^ 1;
+  ts = sh.node[0];
+  ds = sh.node[1];
+  __syncthreads();
 }
 
 __device__ __forceinline__ void write_final(const TreeArgs &a, int b, int depth, int x) {
@@ -388,12 +447,13 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
   const int esz_t = dtype_size(a.tdt), esz_d = dtype_size(a.ddt);
   while (true) {
     // this CTA's slice of node v's rows into L2 while the node is set up
-    if (threadIdx.x == 0 && t.mode != MODE_GREEDY && sl.j1 > sl.j0) {
+    if (threadIdx.x == 0 && sl.j1 > sl.j0) {
       const long long e0 = (long long)sl.j0 * WALK_TILE;
       const long long e1 = min((long long)sl.j1 * WALK_TILE, (long long)a.V);
       const long long rv = t.base + v;
       prefetch_l2(a.target + rv * a.t_row_bytes + e0 * esz_t, (e1 - e0) * esz_t);
-      prefetch_l2(a.draft + rv * a.d_row_bytes + e0 * esz_d, (e1 - e0) * esz_d);
+      if (t.mode != MODE_GREEDY && a.draft != nullptr)
+        prefetch_l2(a.draft + rv * a.d_row_bytes + e0 * esz_d, (e1 - e0) * esz_d);
     }
     // children of v in node-index order (block-wide ordered compaction)
     {
@@ -425,7 +485,13 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     }
     const int nk = sh.nk;
     const int row = t.base + v;
-    const RowStat ts = node_stat(a, row, a.nch_t, c);
+    // the node's statistics: its target row, and its draft row when a
+    // sampling node has children to test
+    const char *trow = a.target + (long long)row * a.t_row_bytes;
+    const bool want_d = t.mode != MODE_GREEDY && nk > 0 && DK == SPEC_DRAFT_LOGITS;
+    RowStat ts, dstat;
+    node_stats(a, sh, trow, want_d ? a.draft + (long long)row * a.d_row_bytes : nullptr, c, sl,
+               cluster, ts, dstat);
     if (t.mode == MODE_GREEDY) {
       if (threadIdx.x == 0) {
         sh.accepted_child = -1;
@@ -451,7 +517,7 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       return;
     }
     NodeLaw nl;
-    nl.trow = a.target + (long long)row * a.t_row_bytes;
+    nl.trow = trow;
     nl.tvec = ((uintptr_t)nl.trow & 15) == 0;
     nl.mt = ts.m;
     nl.invSt = 1.f / ts.S;
@@ -471,9 +537,8 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     nl.drow = a.draft + (long long)row * a.d_row_bytes;
     nl.dvec = ((uintptr_t)nl.drow & 15) == 0;
     if (DK == SPEC_DRAFT_LOGITS) {
-      const RowStat ds = node_stat(a, a.n_nodes + row, a.nch_d, c);
-      nl.md = ds.m;
-      nl.invSd = 1.f / ds.S;
+      nl.md = dstat.m;
+      nl.invSd = 1.f / dstat.S;
     }
     if (threadIdx.x == 0) {
       sh.s[0] = 1.f;
@@ -587,7 +652,7 @@ extern "C" size_t spec_verify_tree_workspace(int B, int n_nodes, int V, int max_
   if (B < 0 || n_nodes < B || V <= 0 || V > SPEC_MAX_V) return 0;
   if (max_depth < 0 || max_depth > SPEC_MAX_TREE_DEPTH) return 0;
   if (max_branch < 1 || max_branch > SPEC_MAX_TREE_BRANCH) return 0;
-  return tree_layout(B, n_nodes, V).total;
+  return tree_layout(B).total;
 }
 
 extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, int ddt, int dk,
@@ -611,7 +676,7 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
       !aligned(parent, 4) || !aligned(cu_nodes, 4) || !aligned(temperature, 4) ||
       !aligned(out_tokens, 4) || !aligned(out_accepted, 4) || !aligned(out_path, 4))
     return SPEC_ERR_INVALID_ARG;
-  const TreeLayout L = tree_layout(B, n_nodes, V);
+  const TreeLayout L = tree_layout(B);
   if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < L.total)
     return SPEC_ERR_WORKSPACE;
   char *ws = static_cast<char *>(workspace);
@@ -636,46 +701,22 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   a.out_path = out_path;
   a.hdr = reinterpret_cast<WsHeader *>(ws + L.hdr);
   a.tree = reinterpret_cast<TreeInfo *>(ws + L.tree);
-  a.list = reinterpret_cast<RowTask *>(ws + L.list);
-  a.part = reinterpret_cast<Part *>(ws + L.part);
   a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
   a.d_row_bytes = (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
-  a.nch_t = nchunks(V, tdt, CHUNK_BYTES);
-  a.nch_d = nchunks(V, ddt, CHUNK_BYTES);
-  a.nch_max = L.nch_max;
-  a.stream_draft = dk == SPEC_DRAFT_LOGITS;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
   k_setup_tree<<<B, SETUP_THREADS, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  RowPassArgs rp;
-  rp.rank_thr = nullptr;
-  rp.kl_part = nullptr;
-  rp.base[0] = a.target;
-  rp.base[1] = a.draft;
-  rp.row_bytes[0] = a.t_row_bytes;
-  rp.row_bytes[1] = a.d_row_bytes;
-  rp.dtype[0] = tdt;
-  rp.dtype[1] = ddt;
-  rp.nch[0] = a.nch_t;
-  rp.nch[1] = a.nch_d;
-  rp.nch_max = a.nch_max;
-  rp.chunk_bytes = CHUNK_BYTES;
-  rp.list = a.list;
-  rp.hdr = a.hdr;
-  rp.part = a.part;
-  rp.residual = 0;
-  rp.jobs = nullptr;
-  rp.req = nullptr;
-  rp.tsum4 = nullptr;
-  rp.ntiles = 0;
-  rp.V = V;
-  const int rc = launch_row_pass(rp, st);
-  if (rc != SPEC_OK) return rc;
+  // profiling events, if registered, bracket the walk
+  cudaEvent_t before, after;
+  take_row_pass_events(&before, &after);
+  if (before && cudaEventRecord(before, st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (dk == SPEC_DRAFT_PROBS)
     k_tree_walk<SPEC_DRAFT_PROBS><<<B * WALK_CLUSTER, WALK_THREADS, 0, st>>>(a);
   else
     k_tree_walk<SPEC_DRAFT_LOGITS><<<B * WALK_CLUSTER, WALK_THREADS, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (after && cudaEventRecord(after, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
 }

@@ -119,3 +119,28 @@ def test_malformed_tree_sets_the_status_word():
                                           tb.cu_nodes, tb.temperature, 1, max_depth=3,
                                           max_branch=4)
     assert sv.spec_get_status(ws) == sv.SPEC_ERR_INVALID_ARG    # deeper than max_depth
+
+
+def test_walk_reads_only_the_rows_of_visited_nodes():
+    """The rows of every node off the walked path are set to -inf (no mass):
+    the outputs stay those of the clean call and no error is reported, since
+    the walk reads only the root's and the accepted path's rows."""
+    tb = S.make_tree(4, device=DEV, B=12, V=8192, input_seed=44)
+    clean = gpu_tree(tb)
+    assert clean["status"] == sv.SPEC_OK
+    cu = tb.cu_nodes.cpu().numpy()
+    keep = torch.zeros(tb.target.shape[0], dtype=torch.bool)
+    for b in range(tb.B):
+        nodes = [0] + [int(x) for x in clean["path"][b][:clean["accepted"][b]]]
+        keep[[int(cu[b]) + v for v in nodes]] = True
+    assert int((~keep).sum()) > tb.B * 30
+    t2, d2 = tb.target.clone(), tb.draft.clone()
+    gone = (~keep).nonzero().squeeze(1).to(DEV)
+    t2[gone] = float("-inf")
+    d2[gone] = float("-inf")
+    tb2 = S.TreeBatch(**{**tb.__dict__, "target": t2, "draft": d2})
+    g = gpu_tree(tb2)
+    assert g["status"] == sv.SPEC_OK
+    assert np.array_equal(g["tokens"], clean["tokens"])
+    assert np.array_equal(g["accepted"], clean["accepted"])
+    assert np.array_equal(g["path"], clean["path"])
