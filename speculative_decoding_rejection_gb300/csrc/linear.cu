@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
     }
     if (a.out_kl && lane < cnt) a.out_kl[r.d0 + base + lane] = kl;
     const int i = base + lane;
+    // (a sparse law's q(d) is searched by each lane for its own position: the
+    // positions' searches run side by side)
     const bool rej = lane < cnt && position_rejects(a, b, r, i, sample, ts, ds, rank);
     const unsigned bal = __ballot_sync(0xffffffffu, rej);
     if (n == K && bal) n = base + __ffs(bal) - 1;
@@ -233,18 +235,8 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
       if (lane == 0) a.out_kl[r.d0 + j] = kl;
     }
     // a sparse draft's q(d): the warp searches the row's 128 ids together
-    float qs = -1.f;
-    if (sample && a.sparse) {
-      const int d = a.tokens[r.d0 + j];
-      const long long row = (long long)(r.d0 + j) * SPEC_TOPK;
-      unsigned hit = 0;
-      int k_hit = 0;
-      for (int k = lane; k < SPEC_TOPK; k += 32) {
-        const unsigned m = __ballot_sync(0xffffffffu, a.draft_idx[row + k] == d);
-        if (m && !hit) { hit = m; k_hit = k - lane + __ffs(m) - 1; }
-      }
-      qs = hit ? a.sparse_prob[row + k_hit] : 0.f;
-    }
+    const float qs = sample && a.sparse ? warp_sparse_q(a, r.d0 + j, a.tokens[r.d0 + j], lane)
+                                        : -1.f;
     const bool rej = __shfl_sync(
         0xffffffffu, lane == 0 && position_rejects(a, b, r, j, sample, ts, ds, rank, qs), 0);
     if (!rej) {   // accepted: list the next position's rows
@@ -622,7 +614,9 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArg
       sh.s_prob[t] = ok ? a.sparse_prob[row] : 0.f;
     }
     __syncthreads();
-    for (int size = 2; size <= SPEC_TOPK; size <<= 1) {
+    // the internal top-128 returns its ids ascending (-1 padding last); a
+    // caller's sparse law may list them in any order
+    for (int size = 2; size <= SPEC_TOPK && a.rule != SPEC_RULE_STRICT_TOP128; size <<= 1) {
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
         if (t < SPEC_TOPK) {
           const int p = t ^ stride;

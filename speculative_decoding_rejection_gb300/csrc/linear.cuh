@@ -165,6 +165,18 @@ static __device__ float draft_prob_at(const LinearArgs &a, int row, int d, float
   return ex2((load_elem(drow, a.ddt, d) - ds.m) * c) / ds.S;
 }
 
+// q(d) of sparse draft row `row` (up to SPEC_TOPK (id, prob) pairs, any
+// order, -1 for an empty slot): the warp searches the ids together; 0 when d
+// is not listed. Every lane returns the value.
+__device__ __forceinline__ float warp_sparse_q(const LinearArgs &a, int row, int d, int lane) {
+  const long long base = (long long)row * SPEC_TOPK;
+  for (int k0 = 0; k0 < SPEC_TOPK; k0 += 32) {
+    const unsigned m = __ballot_sync(0xffffffffu, a.draft_idx[base + k0 + lane] == d);
+    if (m) return a.sparse_prob[base + k0 + __ffs(m) - 1];
+  }
+  return 0.f;
+}
+
 // Decision on draft position i (0-based) of request b from the statistics of
 // its target row (ts) and dense draft row (ds), its target rank, its token d
 // and, for a valid d, the target logit zt = z_t(d) and either the draft
