@@ -322,6 +322,22 @@ int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos,
                   spec_stream_t stream);
 
 /*
+ * Self-test of the device-side bounded waits (failure detection without a
+ * GPU fault). Launches one small kernel that waits, with the verifier
+ * kernels' own waiting code, on something nothing completes: kind 0 a
+ * shared-memory mbarrier phase (the waits of the TMA rings), kind 1 a global
+ * word (the streaming verifier's producers). After limit_ns (1 ns .. 10 s)
+ * of the GPU's global timer the wait gives up and the kernel records
+ * SPEC_ERR_TIMEOUT in the status word of `workspace` (256 bytes, 256-byte
+ * aligned) and returns; the context stays usable. Asynchronous on `stream`;
+ * read the result with spec_get_status. Returns SPEC_ERR_INVALID_ARG for
+ * another kind or limit, SPEC_ERR_WORKSPACE for a missing or misaligned
+ * workspace.
+ */
+int spec_wait_selftest(int kind, unsigned long long limit_ns, void *workspace,
+                       spec_stream_t stream);
+
+/*
  * Profiling aid. Registers two CUDA events (cudaEvent_t, created by the
  * caller) for the next spec_verify_linear / spec_verify_tree call made by
  * the calling host thread: that call records `before` immediately before it

@@ -64,6 +64,7 @@ _SIGS = {
     "spec_get_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "spec_uniforms": (_i32, [_u64, _vp, _vp, _vp, _i32, _vp, _vp]),
     "spec_profile_row_pass": (_i32, [_vp, _vp]),
+    "spec_wait_selftest": (_i32, [_i32, ctypes.c_ulonglong, _vp, _vp]),
     "spec_verify_linear_noalloc": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32,
                                           _i32, _i32, _u64, _i32, _vp, _vp, _vp, _vp, _vp]),
 }
@@ -302,6 +303,16 @@ def spec_uniforms(seed: int, b, pos, stream_id, stream=None):
                                _ptr(stream_id), b.numel(), _ptr(out), _stream(stream)),
            "spec_uniforms")
     return out
+
+
+def spec_wait_selftest(kind: int, limit_ns: int, workspace=None, stream=None):
+    """Runs the bounded-wait self-test (kind 0: mbarrier, 1: global word);
+    returns the workspace, whose status word then reads SPEC_ERR_TIMEOUT."""
+    torch = _torch()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda") if workspace is None else workspace
+    _check(lib().spec_wait_selftest(int(kind), ctypes.c_ulonglong(limit_ns), _ptr(ws),
+                                    _stream(stream)), "spec_wait_selftest")
+    return ws
 
 
 def spec_profile_row_pass(before=None, after=None):

@@ -4,6 +4,27 @@
 
 namespace sv {
 
+// A bounded wait on something nothing completes, with the waiting code of
+// the verifier kernels: kind 0 waits on a shared-memory mbarrier phase (the
+// TMA rings' waits), kind 1 polls a global word (the streaming verifier's
+// producers). The wait gives up after limit_ns and records SPEC_ERR_TIMEOUT.
+__global__ void k_wait_selftest(WsHeader *hdr, int kind, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x != 0) return;
+  bool done;
+  if (kind == 0) {
+    mbar_init(&bar, 1);   // one arrival completes phase 0; none comes
+    abort = 0;
+    fence_mbar_init();
+    done = mbar_wait_bounded(&bar, 0, &abort, limit_ns);
+  } else {
+    const volatile int *word = &hdr->pad[0];   // zero, and nothing writes it
+    done = poll_bounded([&]() -> int { return *word != 0; }, 0, limit_ns) != 0;
+  }
+  if (!done) set_status(hdr, SPEC_ERR_TIMEOUT, kind);
+}
+
 __global__ void k_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos,
                            const int32_t *stream_id, int n, float *out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -45,6 +66,18 @@ extern "C" int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos
   if (!b || !pos || !stream_id || !out) return SPEC_ERR_INVALID_ARG;
   k_uniforms<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       seed, b, pos, stream_id, n, out);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+extern "C" int spec_wait_selftest(int kind, unsigned long long limit_ns, void *workspace,
+                                  spec_stream_t stream) {
+  if (kind != 0 && kind != 1) return SPEC_ERR_INVALID_ARG;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return SPEC_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256)) return SPEC_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  WsHeader *hdr = static_cast<WsHeader *>(workspace);
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
+  k_wait_selftest<<<1, 32, 0, st>>>(hdr, kind, limit_ns);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -368,15 +368,31 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 // Waits for the phase of `bar` with `parity` to complete, giving up after
-// WAIT_NS or once *abort is set. Returns false when it gave up.
+// limit_ns of %globaltimer or once *abort is set. Returns false when it gave
+// up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  volatile int *abort) {
+                                                  volatile int *abort,
+                                                  unsigned long long limit_ns = WAIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > WAIT_NS) return false;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Polls check() until it reports an outcome (nonzero) and returns it, or
+// returns `timeout` once limit_ns of %globaltimer have passed; sleeps 256 ns
+// between polls. The streaming verifier's producers wait for work this way.
+template <class Check>
+__device__ __forceinline__ int poll_bounded(Check check, int timeout, unsigned long long limit_ns) {
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    const int o = check();
+    if (o) return o;
+    if (global_ns() - t0 > limit_ns) return timeout;
+    __nanosleep(256);
   }
 }
 // 1-D TMA bulk copy global -> shared, completion counted on `bar`.

@@ -534,15 +534,15 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
         continue;
       }
       // 3. nothing else: wait for the ticket's entry, the last request or an error
-      const unsigned long long t0 = global_ns();
-      int outcome = 0;   // 1: entry ready, 2: every request finished, 3: give up
-      while (outcome == 0) {
-        if (dy_t < n_dyn && ld_acquire(a.ready_d + e)) outcome = 1;
-        else if (*(volatile int *)&a.hdr->n_done >= a.B) outcome = 2;
-        else if (*(volatile int *)&a.hdr->status == SPEC_ERR_TIMEOUT || *abort) outcome = 3;
-        else if (global_ns() - t0 > WAIT_NS) outcome = 3;
-        else __nanosleep(256);
-      }
+      // (1: entry ready, 2: every request finished, 3: give up)
+      const int outcome = poll_bounded(
+          [&]() -> int {
+            if (dy_t < n_dyn && ld_acquire(a.ready_d + e)) return 1;
+            if (*(volatile int *)&a.hdr->n_done >= a.B) return 2;
+            if (*(volatile int *)&a.hdr->status == SPEC_ERR_TIMEOUT || *abort) return 3;
+            return 0;
+          },
+          3, WAIT_NS);
       if (outcome == 1) continue;
       ok = outcome == 2;
       break;

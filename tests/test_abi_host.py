@@ -102,3 +102,11 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sv, "LIB_PATH", tmp_path / "missing.so")
     with pytest.raises(RuntimeError, match="not built"):
         sv.lib()
+
+
+def test_wait_selftest_rejects_bad_arguments(L):
+    assert L.spec_wait_selftest(2, 1000, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_wait_selftest(0, 0, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_wait_selftest(0, 20 * 10 ** 9, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_wait_selftest(1, 1000, None, None) == sv.SPEC_ERR_WORKSPACE
+    assert L.spec_wait_selftest(1, 1000, FAKE + 16, None) == sv.SPEC_ERR_WORKSPACE
