@@ -41,32 +41,32 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic of the row pass per algorithmic byte, from an ncu capture of
 # a smaller case of the same kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum over the algorithmic bytes it streams). Valid only for
-# the row-pass source it was taken on.
+# dram__bytes_write.sum over the algorithmic bytes it streams). Each figure
+# below is valid only for the sources it was taken on (KERNEL_SOURCES).
 # Captured on B=128, K=4, V=201088 bf16 (460.09 MB streamed by the launch):
-# 460.19 MB read + 3.49 MB written (the per-chunk partial statistics).
-ROWPASS_TRAFFIC = {"source_sha1": "7fb47217e418563d0e3bfdcba1c829cfc8eb4206",
-                   "dram_per_algorithmic_byte": (460191744 + 3492352) / 460089344}
+# 460.19 MB read + 3.43 MB written (the per-chunk partial statistics).
+ROWPASS_TRAFFIC = {"source_sha1": "bf1d3cf8733d92f398f6bf1bab7874841186e6a8",
+                   "dram_per_algorithmic_byte": (460189952 + 3429376) / 460089344}
 # The same for the streaming verifier (position-lazy schedule), per byte of
 # the rows the schedule must read (target rows 1..n+1, dense draft rows
 # 1..min(n+1, K) of sampling requests). Captured on the full B=1024, K=4,
-# V=201088 workload (one pass): 2711.8 MB read + 23.5 MB written for
+# V=201088 workload (one pass): 2708.4 MB read + 23.3 MB written for
 # 1975.1 MB; the excess is the residual rows read a second time and rows
 # read before a rejection made them unneeded, so the ratio holds for this
 # workload and source only.
-STREAM_TRAFFIC = {"source_sha1": "de41eca4c0b1ee2cb156d518af6b89da32d6a706",
-                  "dram_per_algorithmic_byte": (2711803136 + 23505920) / 1975086336}
+STREAM_TRAFFIC = {"source_sha1": "af2841c6d6ad0bdf2548c33a8a1429e759b11cdd",
+                  "dram_per_algorithmic_byte": (2708409856 + 23307264) / 1975086336}
 # The top-128 select (two passes, the second mostly from L2), per byte of
 # the draft rows; captured on the full B=256, K=7, V=151936 workload (one
-# pass): 581.84 MB read + 4.56 MB written for 544.54 MB. Valid for this
-# topk.cu and workload.
-TOPK_TRAFFIC = {"source_sha1": "8bdc84bb3376229ee37c47816fffcdd26f5025f4",
-                "dram_per_algorithmic_byte": (581836544 + 4556288) / 544538624}
+# pass): 570.80 MB read + 4.65 MB written for 544.54 MB. Valid for these
+# sources and this workload.
+TOPK_TRAFFIC = {"source_sha1": "44b6662ddd4906c33d1f831ded049874cb49f908",
+                "dram_per_algorithmic_byte": (570798080 + 4648192) / 544538624}
 # The tree walk (no row pass: only visited nodes' rows), per byte of those
 # rows' first read; captured on the full 32-tree workload (one pass): 63.27 MB
-# read + 0.60 MB written for 59.25 MB. Valid for this tree.cu and workload.
-TREE_TRAFFIC = {"source_sha1": "5ea13c5cc5f15985a80e7766f7fbe59b91aaa544",
-                "dram_per_algorithmic_byte": (63272192 + 597248) / 59254272}
+# read + 0.58 MB written for 59.25 MB. Valid for these sources and workload.
+TREE_TRAFFIC = {"source_sha1": "145469fd96e6eb60a5f8619c846d9ce972acf001",
+                "dram_per_algorithmic_byte": (63270144 + 579072) / 59254272}
 
 
 def parse():
@@ -93,9 +93,25 @@ def parse():
     return ap.parse_args()
 
 
-def sha1(path):
-    with open(path, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+# Every source a kernel is compiled from: a traffic figure holds only while
+# all of them are unchanged.
+KERNEL_SOURCES = {
+    "rowpass": ("rowpass.cu", "rowpass.cuh", "common.cuh", "internal.h"),
+    "stream": ("stream.cu", "linear.cuh", "rowpass.cuh", "common.cuh", "internal.h"),
+    "topk": ("topk.cu", "common.cuh", "internal.h"),
+    "tree": ("tree.cu", "common.cuh", "internal.h"),
+}
+
+
+def source_sha1(kernel):
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc")
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    with open(os.path.join(ROOT, "include", "specverify.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
 
 
 def measured_peaks():
@@ -267,7 +283,7 @@ class LinearWork:
                                    workspace=self.ws, out=self.outs)
 
     def result_tensors(self):
-        return [self.outs[0], self.outs[1]]
+        return [self.outs[0], self.outs[1]] + ([self.kl] if self.kl is not None else [])
 
     def settle(self):
         """Position-lazy: the bytes a call reads follow from its outcome
@@ -510,24 +526,20 @@ def main():
     peak = float(peaks["hbm_gbs"])
     achieved = work.rowpass_bytes / (rp_ms * 1e-3) / 1e9
     traffic = None
-    src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "rowpass.cu")
     lazy = getattr(work, "lazy", False)
     stream = getattr(work, "stream", False)
     plain = (not lazy and getattr(work, "kl", None) is None and getattr(work, "ext", None) is None
              and getattr(work, "kernel", None) is None)
-    if ROWPASS_TRAFFIC["source_sha1"] == sha1(src) and plain:
+    if ROWPASS_TRAFFIC["source_sha1"] == source_sha1("rowpass") and plain:
         traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    topk_src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "topk.cu")
     if (getattr(work, "kernel", None) == "k_topk128" and args.B is None and args.config == 3
-            and TOPK_TRAFFIC["source_sha1"] == sha1(topk_src)):
+            and TOPK_TRAFFIC["source_sha1"] == source_sha1("topk")):
         traffic = TOPK_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    tree_src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "tree.cu")
     if (getattr(work, "kernel", None) == "k_tree_walk" and args.B is None and args.config == 4
-            and TREE_TRAFFIC["source_sha1"] == sha1(tree_src)):
+            and TREE_TRAFFIC["source_sha1"] == source_sha1("tree")):
         traffic = TREE_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    stream_src = os.path.join(ROOT, "speculative_decoding_rejection_gb300", "csrc", "stream.cu")
     if (stream and getattr(work, "ext", None) is None and args.B is None and args.config == 5
-            and STREAM_TRAFFIC["source_sha1"] == sha1(stream_src)):
+            and STREAM_TRAFFIC["source_sha1"] == source_sha1("stream")):
         traffic = STREAM_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
 
     # end to end through the same API: pinned host inputs copied in, the
