@@ -86,6 +86,34 @@ R13 Per-position KL(p_i || q_i) = sum_y p(y) ln(p(y) / q(y)), natural log,
     The second TTS term, KL(q_t || q), compares the drafter before and after
     an update; a verifier sees one draft law, so it is 0 here and not
     reported.
+
+RheoSampling tree construction ("RheoSampling 2026", §2 "Dual-Identity
+Decoupling", §3 "Parameter Kendali Rheostat", §7 "Rekomendasi"), one
+expansion level of a batch of dynamic trees:
+
+R14 Every frontier row keeps its top-128 logits (R6). Ranking, expansion and
+    pruning use q = softmax(z) over them with no temperature (§7, first
+    item); the probe is drawn from q~ = softmax(z / T) over the same 128
+    (greedy T: one-hot on the argmax), its true sampling law (§2).
+R15 Rheostat m: the children of a frontier node, in slot order, are the m
+    best tokens by q (the deterministic lead), the probe, then the next best
+    tokens up to K children. The deterministic children skip the probe's
+    token, so siblings are distinct. The probe's proxy probability is
+    q(x_{m+1}) + eps, x_j the j-th best token of the row (ties to the lower
+    id): for m = 0 this is the page's q(x_1) + eps, and for every m it ranks
+    the probe in slot m+1. eps is the caller's (the page names no value).
+    Deterministic children rank by their own q.
+R16 A child's path score is ln of the product of proxy probabilities along
+    its path: the frontier node's score + ln q_proxy(child). Pruning keeps,
+    per tree, the n_keep candidates with the largest scores (ties to the
+    lower candidate index f * K + slot), in descending score order.
+R17 The probe's uniform is u(seed, f, level, 3): key b = the global frontier
+    row f, pos = the expansion level, stream 3; the draw is the inverse CDF
+    over q~ in ascending token id (R4).
+R18 The deterministic children depend on the probe's token (R15), so a
+    verifier of these trees tests the probe first, as "RheoSampling 2026" §4
+    step 1 does, and the deterministic children after it as point masses.
+    Only construction is computed here.
 """
 from __future__ import annotations
 
@@ -100,6 +128,7 @@ TOPK = 128               # R6
 STREAM_COIN = 0
 STREAM_RESIDUAL = 1
 STREAM_BONUS = 2
+STREAM_PROBE = 3         # R17
 
 RULE_STRICT = 0
 RULE_GREEDY = 1
@@ -559,3 +588,98 @@ def draft_topk_softmax(draft_logits, cu_rows, temperature, k=TOPK):
             idx[r, :ids.size] = ids
             prob[r, :ids.size] = probs
     return idx, prob
+
+
+# --------------------------------------------------------------------------
+# RheoSampling tree construction, one expansion level (R14-R18)
+# --------------------------------------------------------------------------
+def rheo_ranking_order(z: np.ndarray, k: int = TOPK) -> np.ndarray:
+    """The row's top-k token ids from best to worst: logit descending, ties
+    to the lower id ("RheoSampling 2026", §3; R6, R15)."""
+    z = np.asarray(z, dtype=np.float64)
+    order = np.lexsort((np.arange(z.size), -z))
+    return order[: min(k, z.size)]
+
+
+def rheo_ranking_law(z: np.ndarray, ids: np.ndarray) -> np.ndarray:
+    """q over the surviving ids with no temperature ("RheoSampling 2026", §7:
+    tree expansion and ranking run on the unscaled draft law; R14)."""
+    zs = np.asarray(z, dtype=np.float64)[ids]
+    e = np.exp(zs - np.max(zs))
+    return e / np.sum(e)
+
+
+def rheo_slots(order: np.ndarray, probe: int, K: int, m: int) -> list:
+    """Children in slot order: the m best tokens other than the probe, the
+    probe, then the next best up to K children (§3 rheostat; R15)."""
+    det = [int(x) for x in order if int(x) != probe][: K - 1]
+    return det[:m] + [probe] + det[m:]
+
+
+def rheo_probe_proxy(q_by_rank: np.ndarray, m: int, eps: float) -> float:
+    """q_proxy of the probe: q(x_{m+1}) + eps, x ranked best first (§3: m = 0
+    gives q(x_1) + eps; R15). Beyond the last survivor it is eps."""
+    return (float(q_by_rank[m]) if m < q_by_rank.size else 0.0) + eps
+
+
+def rheo_select(scores: np.ndarray, n_keep: int) -> np.ndarray:
+    """Pruning: indices of the n_keep largest scores, descending, ties to the
+    lower index, -1 padded (§2 global pruning; R16)."""
+    scores = np.asarray(scores, dtype=np.float64)
+    order = np.lexsort((np.arange(scores.size), -scores))
+    out = np.full(n_keep, -1, dtype=np.int64)
+    take = order[:n_keep]
+    out[: take.size] = take
+    return out
+
+
+def rheo_expand(draft, cu_frontier, frontier_score, temperature, seed, level,
+                K, m, eps, n_keep):
+    """One level of RheoSampling dynamic-tree expansion for a batch of trees.
+
+    draft [F, V] logits: row f is the draft model's output at frontier node
+    f; tree b owns rows cu_frontier[b] .. cu_frontier[b+1]-1.
+    frontier_score [F]: ln of each frontier node's path score (0 at a root).
+    Returns child_token, child_qproxy, child_qtrue, child_score (each
+    [F, K], slot order of R15), keep [B, n_keep] (candidate ids f * K +
+    slot, R16) and probe_flag [F] (the probe draw sat within R8's margin of
+    a CDF boundary).
+    """
+    cu = np.asarray(cu_frontier, dtype=np.int64)
+    B, F = cu.size - 1, int(cu[-1])
+    temps = np.asarray(temperature, dtype=np.float64)
+    fscore = np.asarray(frontier_score, dtype=np.float64)
+    token = np.full((F, K), -1, dtype=np.int64)
+    qproxy = np.zeros((F, K))
+    qtrue = np.zeros((F, K))
+    score = np.full((F, K), -np.inf)
+    flag = np.zeros(F, dtype=bool)
+    for b in range(B):
+        T = float(temps[b])
+        for f in range(int(cu[b]), int(cu[b + 1])):
+            z = as_f64(draft[f])
+            order = rheo_ranking_order(z)                # R14: top-128, best first
+            ids = np.sort(order)                         # ascending id
+            q = rheo_ranking_law(z, ids)                 # unscaled, by ascending id
+            q_of = dict(zip(ids.tolist(), q.tolist()))
+            _, qt = top128_softmax(z, T)                 # q~, by ascending id
+            qt_of = dict(zip(ids.tolist(), qt.tolist()))
+            u = uniform(seed, f, level, STREAM_PROBE)    # R17
+            j, fl = inverse_cdf(qt, u)
+            probe = int(ids[j])
+            flag[f] = fl
+            slots = rheo_slots(order, probe, K, m)       # R15
+            q_rank = np.array([q_of[int(x)] for x in order])
+            for s, x in enumerate(slots):
+                pr = rheo_probe_proxy(q_rank, m, eps) if x == probe else q_of[x]
+                token[f, s] = x
+                qproxy[f, s] = pr
+                qtrue[f, s] = qt_of[x]
+                score[f, s] = fscore[f] + np.log(pr)     # R16
+    keep = np.full((B, n_keep), -1, dtype=np.int64)
+    for b in range(B):
+        lo, hi = int(cu[b]) * K, int(cu[b + 1]) * K
+        sel = rheo_select(score.reshape(-1)[lo:hi], n_keep)
+        keep[b] = np.where(sel >= 0, sel + lo, -1)
+    return dict(child_token=token, child_qproxy=qproxy, child_qtrue=qtrue,
+                child_score=score, keep=keep, probe_flag=flag)
