@@ -89,6 +89,9 @@ def parse():
     ap.add_argument("--rule", default="default", choices=["default", "cactus"],
                     help="linear workloads: the workload's lossless rule, or the relaxed "
                          "CACTUS rule with the recommended low-support guard")
+    ap.add_argument("--rheo", action="store_true",
+                    help="time one level of RheoSampling tree construction (spec_rheo_expand) "
+                         "on its own workload instead of a verify workload")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
 
@@ -411,7 +414,77 @@ class TreeWork:
         return int(sum(cu[b + 1] - cu[b] - 1 for b in req))
 
 
-def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False):
+class RheoWork:
+    """spec_rheo_expand: one expansion level of RheoSampling dynamic trees
+    (64 trees x 10 frontier nodes, V = 128256 bf16, K = 10, m = 1)."""
+    unit_name = "trees"
+    metric = ("expanded frontier nodes/sec (RheoSampling tree construction, one level) and "
+              "achieved HBM GB/s (% of GB300 peak), 1 GPU")
+    unit = "frontier nodes/s"
+
+    def __init__(self, dev, input_seed=None, B=None):
+        import torch
+        import speculative_decoding_rejection_gb300 as sv
+        from speculative_decoding_rejection_gb300 import synthetic as S
+        self.sv = sv
+        rb = S.make_rheo(device=dev, input_seed=input_seed, **({"B": B} if B else {}))
+        self.rb = rb
+        F, V = rb.draft.shape
+        self.positions = F
+        self.tgt_bytes = 0
+        self.drf_bytes = F * V * rb.draft.element_size()
+        self.rowpass_bytes = self.drf_bytes       # the top-128 select reads every row once
+        self.launches = 4   # validate, top-128 select, children, selection
+        self.kernel = "k_topk128"
+        self.outs = (torch.empty(F, rb.K, dtype=torch.int32, device=dev),
+                     torch.empty(F, rb.K, dtype=torch.float32, device=dev),
+                     torch.empty(F, rb.K, dtype=torch.float32, device=dev),
+                     torch.empty(F, rb.K, dtype=torch.float32, device=dev),
+                     torch.empty(rb.B, rb.n_keep, dtype=torch.int32, device=dev))
+        self.ws = torch.empty(sv.spec_rheo_expand_workspace(F, V), dtype=torch.uint8,
+                              device=dev)
+        self.config = {"workload": rb.meta["workload"], "B": rb.B, "frontier": F, "K": rb.K,
+                       "m": rb.m, "n_keep": rb.n_keep, "V": V,
+                       "logits": "bf16" if rb.draft.element_size() == 2 else "f32",
+                       "rule": "rheo_expand"}
+
+    def input_tensors(self):
+        rb = self.rb
+        return {"draft": rb.draft, "cu_frontier": rb.cu_frontier,
+                "frontier_score": rb.frontier_score, "temperature": rb.temperature}
+
+    def call(self, inputs=None):
+        rb = self.rb
+        t = inputs or self.input_tensors()
+        self.sv.spec_rheo_expand(t["draft"], t["cu_frontier"], t["frontier_score"],
+                                 t["temperature"], rb.seed, rb.level, K=rb.K, m=rb.m, eps=rb.eps,
+                                 n_keep=rb.n_keep, workspace=self.ws, out=self.outs)
+
+    def result_tensors(self):
+        return [self.outs[0], self.outs[3], self.outs[4]]   # tokens, scores, kept ids
+
+    def mean_accepted(self):
+        return None
+
+    def oracle_sample(self, units, offset=0):
+        import numpy as np
+        from oracle import spec_oracle as O
+        rb = self.rb
+        if not hasattr(self, "_host"):
+            self._host = (rb.draft.cpu(), rb.cu_frontier.cpu().numpy(),
+                          rb.frontier_score.cpu().numpy(), rb.temperature.cpu().numpy())
+        drf, cu, fs, T = self._host
+        b0 = offset % rb.B
+        b1 = min(rb.B, b0 + units)
+        lo, hi = int(cu[b0]), int(cu[b1])
+        O.rheo_expand(drf[lo:hi], cu[b0:b1 + 1] - lo, fs[lo:hi], T[b0:b1], rb.seed, rb.level,
+                      rb.K, rb.m, rb.eps, rb.n_keep)
+        return hi - lo
+
+
+def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False, rheo=False):
+    if rheo:
+        return RheoWork(dev, input_seed, B)
     if cfg == 4:
         return TreeWork(cfg, dev, input_seed, B)
     return LinearWork(cfg, dev, input_seed, B, rule, lazy, kl)
@@ -423,9 +496,11 @@ def cpu_baseline(work, n_units):
     pos = work.oracle_sample(n_units)
     dt = time.perf_counter() - t0
     n = min(n_units, work.config["B"])
-    return {"value": pos / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} of {work.config['B']} {work.unit_name} ({pos} draft positions) of "
-                      f"the same workload, fp64 numpy, one thread, {dt:.1f} s"}
+    unit = getattr(work, "unit", UNIT)
+    return {"value": pos / dt, "unit": unit, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {work.config['B']} {work.unit_name} ({pos} "
+                      f"{unit.split('/')[0]}) of the same workload, fp64 numpy, one thread, "
+                      f"{dt:.1f} s"}
 
 
 def run_reference(args):
@@ -436,8 +511,9 @@ def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     import torch
     dev = "cuda:0" if torch.cuda.is_available() else "cpu"
-    work = make_work(args.config, dev, B=args.B, rule=args.rule)
-    per_step = 1 if args.config == 4 else 2
+    work = make_work(args.config, dev, B=args.B, rule=args.rule, rheo=args.rheo)
+    per_step = 1 if args.config == 4 and not args.rheo else 2
+    metric, unit = getattr(work, "metric", METRIC), getattr(work, "unit", UNIT)
     for k in range(args.warmup):
         work.oracle_sample(per_step, offset=k * per_step)
     pos = 0
@@ -447,15 +523,15 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     value = pos / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": metric, "value": value, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(work.config, step=f"{per_step} {work.unit_name} of the batch per step"),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": f"{per_step} {work.unit_name} per step, {args.steps} steps, "
                                    "fp64 numpy, one thread"},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -472,8 +548,10 @@ def main():
     world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     sv.lib()
-    work = make_work(args.config, dev, input_seed=S.INPUT_SEED_BASE + args.config + 7919 * rank,
-                     B=args.B, rule=args.rule, lazy=args.lazy, kl=args.kl)
+    seed_base = S.INPUT_SEED_BASE + (0x100 if args.rheo else args.config)
+    work = make_work(args.config, dev, input_seed=seed_base + 7919 * rank, B=args.B,
+                     rule=args.rule, lazy=args.lazy, kl=args.kl, rheo=args.rheo)
+    unit = getattr(work, "unit", UNIT)
 
     for _ in range(max(3, args.warmup)):
         work.call()
@@ -533,6 +611,7 @@ def main():
     if ROWPASS_TRAFFIC["source_sha1"] == source_sha1("rowpass") and plain:
         traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
     if (getattr(work, "kernel", None) == "k_topk128" and args.B is None and args.config == 3
+            and not args.rheo
             and TOPK_TRAFFIC["source_sha1"] == source_sha1("topk")):
         traffic = TOPK_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
     if (getattr(work, "kernel", None) == "k_tree_walk" and args.B is None and args.config == 4
@@ -573,15 +652,15 @@ def main():
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.e2e_steps, world)
-        e2e = {"value": world * work.positions / (e2e_ms * 1e-3), "unit": UNIT,
+        e2e = {"value": world * work.positions / (e2e_ms * 1e-3), "unit": unit,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         del host, dev_in
 
     algo = work.tgt_bytes + work.drf_bytes
     line = {
-        "metric": METRIC,
+        "metric": getattr(work, "metric", METRIC),
         "value": world * work.positions / (ms_step * 1e-3),
-        "unit": UNIT,
+        "unit": unit,
         "n_gpus": world,
         "steps": K,
         "warmup": max(3, args.warmup),
@@ -616,7 +695,9 @@ def main():
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(work, args.cpu_requests if args.config != 4 else 8)
+        line["cpu_baseline"] = cpu_baseline(
+            work, 8 if args.config == 4 and not args.rheo else 16 if args.rheo
+            else args.cpu_requests)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

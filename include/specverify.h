@@ -305,6 +305,66 @@ int draft_topk_softmax(const void *draft_logits, int dt, int rows, int V,
                        void *workspace, size_t ws_bytes, spec_stream_t stream);
 
 /*
+ * RheoSampling dynamic-tree construction, one expansion level for B trees
+ * ("RheoSampling 2026": §2 "Dual-Identity Decoupling", §3 "Parameter
+ * Kendali Rheostat & Optimasi Sparse Top-128", §7 "Rekomendasi"). Every
+ * frontier node f of tree b gets K children in slot order:
+ *   - slots 0..m-1: the m best tokens of its draft row other than the probe
+ *     (the deterministic lead);
+ *   - slot m: the probe, a token drawn from q~ = softmax(z/T_b) over the
+ *     row's 128 largest logits (ties to the lower id; T < 0.05: the argmax)
+ *     by inverse CDF in ascending id at u(seed, b = f, pos = level,
+ *     stream 3) as defined above;
+ *   - slots m+1..K-1: the next best tokens other than the probe.
+ * "Best" ranks by the logit, descending, ties to the lower id, among the
+ * row's top 128; siblings are distinct. Ranking uses q = softmax(z) over
+ * the same 128 logits, with no temperature (§7). q_proxy of a deterministic
+ * child is its q; the probe's is q(x_{m+1}) + eps, x_j the row's j-th best
+ * token (0 + eps when m+1 exceeds the survivors), which at m = 0 is the
+ * page's q(x_1) + eps. score = frontier_score[f] + ln q_proxy. Each tree
+ * then keeps the n_keep candidates with the largest scores (ties to the
+ * lower candidate index f*K + slot), best first (§2, global pruning). The
+ * children depend on the probe, so a verifier of the resulting trees should
+ * test the probe first ("RheoSampling 2026", §4 step 1), then the
+ * deterministic children as point masses.
+ *
+ *   draft          [F, V] draft logits (ddt), 16-byte aligned: row f is the
+ *                  draft model's output at frontier node f.
+ *   cu_frontier    [B+1] int32: tree b owns frontier rows cu_frontier[b] ..
+ *                  cu_frontier[b+1]-1; cu_frontier[0] = 0,
+ *                  cu_frontier[B] = F; at most SPEC_RHEO_MAX_CANDIDATES
+ *                  candidates (rows x K) per tree.
+ *   frontier_score [F] f32: ln of each frontier node's path score (0 at a
+ *                  root), finite or -inf.
+ *   temperature    [B] f32 >= 0, finite.
+ *   K              children per frontier node, 1 <= K <= min(V, 128).
+ *   m              rheostat, 0 <= m < K (the page recommends m = 1).
+ *   eps            >= 0, finite: the probe's proxy margin.
+ *   n_keep         candidates kept per tree, 0 .. SPEC_RHEO_MAX_CANDIDATES.
+ *   level          0 <= level < 2^24, keys the probe draws of this level.
+ *   child_token    [F, K] int32 out.   child_score [F, K] f32 out.
+ *   child_qproxy   [F, K] f32 out, or NULL.
+ *   child_qtrue    [F, K] f32 out, or NULL: q~ of each child's token (the
+ *                  probe's true sampling probability in slot m).
+ *   keep           [B, n_keep] int32 out: candidate ids f*K + slot, -1 when
+ *                  a tree has fewer candidates. NULL only when n_keep == 0.
+ *   workspace      >= spec_rheo_expand_workspace(F, V) bytes, 256-byte
+ *                  aligned.
+ * A device-side status (read with spec_get_status) reports bad offsets,
+ * temperatures or scores (SPEC_ERR_INVALID_ARG) and trees over the
+ * candidate limit (SPEC_ERR_UNSUPPORTED); outputs are then unspecified.
+ */
+#define SPEC_RHEO_MAX_CANDIDATES 8192
+size_t spec_rheo_expand_workspace(int F, int V);
+int spec_rheo_expand(const void *draft, int ddt, const int32_t *cu_frontier,
+                     const float *frontier_score, const float *temperature,
+                     int B, int F, int V, int K, int m, float eps, int n_keep,
+                     uint64_t seed, int level, int32_t *child_token,
+                     float *child_qproxy, float *child_qtrue,
+                     float *child_score, int32_t *keep, void *workspace,
+                     size_t ws_bytes, spec_stream_t stream);
+
+/*
  * Synchronises `stream` and reads the device status word that the last call
  * using `workspace` left: *device_status = SPEC_OK or a negative spec_status.
  * Returns SPEC_OK or SPEC_ERR_CUDA / SPEC_ERR_INVALID_ARG.
@@ -347,7 +407,8 @@ int spec_wait_selftest(int kind, unsigned long long limit_ns, void *workspace,
  * row once), the top-128 select under SPEC_RULE_STRICT_TOP128, the streaming
  * kernel of a position-lazy call (SPEC_EXT_LAZY) or,
  * on its multi-launch schedule, all its rounds (every row pass and every
- * per-round decision), and the walk of a tree call. So
+ * per-round decision), the walk of a tree call, and the top-128 select of
+ * spec_rheo_expand. So
  * cudaEventElapsedTime(before, after) is that kernel's duration.
  */
 int spec_profile_row_pass(void *before, void *after);

@@ -20,7 +20,7 @@ __all__ = [
     "spec_verify_linear", "spec_verify_linear_ext", "spec_verify_linear_workspace", "spec_verify_tree",
     "spec_verify_tree_workspace", "draft_topk_softmax",
     "draft_topk_softmax_workspace", "spec_get_status", "spec_uniforms",
-    "spec_profile_row_pass", "SpecError",
+    "spec_profile_row_pass", "spec_rheo_expand", "spec_rheo_expand_workspace", "SpecError",
 ]
 
 SPEC_OK = 0
@@ -34,6 +34,7 @@ SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS, SPEC_DRAFT_SPARSE128 = 0, 1, 2
 SPEC_RULE_STRICT, SPEC_RULE_GREEDY, SPEC_RULE_STRICT_TOP128, SPEC_RULE_CACTUS = 0, 1, 2, 3
 SPEC_TOPK = 128
 SPEC_EXT_LAZY = 1
+SPEC_RHEO_MAX_CANDIDATES = 8192
 
 LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
 HEADER = Path(__file__).resolve().parent.parent / "include" / "specverify.h"
@@ -61,6 +62,10 @@ _SIGS = {
     "draft_topk_softmax_workspace": (_sz, [_i32, _i32]),
     "draft_topk_softmax": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp,
                                   _sz, _vp]),
+    "spec_rheo_expand_workspace": (_sz, [_i32, _i32]),
+    "spec_rheo_expand": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                ctypes.c_float, _i32, _u64, _i32, _vp, _vp, _vp, _vp, _vp,
+                                _vp, _sz, _vp]),
     "spec_get_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "spec_uniforms": (_i32, [_u64, _vp, _vp, _vp, _i32, _vp, _vp]),
     "spec_profile_row_pass": (_i32, [_vp, _vp]),
@@ -285,6 +290,41 @@ def draft_topk_softmax(draft_logits, cu_rows, temperature, *, workspace=None, ou
         ctypes.c_size_t(ws.numel()), _stream(stream))
     _check(code, "draft_topk_softmax")
     return idx, prob, ws
+
+
+def spec_rheo_expand_workspace(F: int, V: int) -> int:
+    return int(lib().spec_rheo_expand_workspace(F, V))
+
+
+def spec_rheo_expand(draft, cu_frontier, frontier_score, temperature, seed: int, level: int,
+                     *, K: int, m: int = 1, eps: float = 1e-6, n_keep: int = 0,
+                     want_qproxy=True, want_qtrue=True, workspace=None, out=None,
+                     stream=None):
+    """One level of RheoSampling tree expansion (see spec_rheo_expand in
+    include/specverify.h). Returns (child_token [F, K] int32, child_qproxy
+    [F, K] f32 or None, child_qtrue [F, K] f32 or None, child_score [F, K] f32,
+    keep [B, n_keep] int32, workspace)."""
+    torch = _torch()
+    F, V = draft.shape
+    B = cu_frontier.numel() - 1
+    dev = draft.device
+    ws = _workspace(spec_rheo_expand_workspace(F, V), dev, workspace)
+    if out is None:
+        token = torch.empty(F, K, dtype=torch.int32, device=dev)
+        qproxy = torch.empty(F, K, dtype=torch.float32, device=dev) if want_qproxy else None
+        qtrue = torch.empty(F, K, dtype=torch.float32, device=dev) if want_qtrue else None
+        score = torch.empty(F, K, dtype=torch.float32, device=dev)
+        keep = torch.empty(B, n_keep, dtype=torch.int32, device=dev)
+    else:
+        token, qproxy, qtrue, score, keep = out
+    code = lib().spec_rheo_expand(
+        _ptr(draft), _dtype_code(draft), _ptr(cu_frontier), _ptr(frontier_score),
+        _ptr(temperature), B, F, V, K, m, ctypes.c_float(eps), n_keep, ctypes.c_uint64(seed),
+        level, _ptr(token), _ptr(qproxy), _ptr(qtrue), _ptr(score),
+        _ptr(keep) if n_keep > 0 else None, _ptr(ws), ctypes.c_size_t(ws.numel()),
+        _stream(stream))
+    _check(code, "spec_rheo_expand")
+    return token, qproxy, qtrue, score, keep, ws
 
 
 def spec_get_status(workspace, stream=None) -> int:

@@ -20,7 +20,10 @@ rows stand in for them):
 * trees: node 0 is the root; each new node picks its parent uniformly among
   nodes of depth < max_depth with fewer than max_branch children; the
   children of a node carry tokens drawn without replacement from that node's
-  draft law, in node-index order (Gumbel-top-k).
+  draft law, in node-index order (Gumbel-top-k);
+* tree-expansion frontiers: W draft rows per tree with the draft logit
+  recipe above (one Zipf permutation per tree), and ln path scores uniform
+  in [-3 * level, 0] (0 at level 0, where each tree's frontier is its root).
 """
 from __future__ import annotations
 
@@ -262,3 +265,72 @@ def make_tree(cfg: int = 4, device="cpu", input_seed=None, **overrides) -> TreeB
                      max_branch=w["branch"], seed=VERIFY_SEED_BASE + cfg,
                      meta=dict(workload=w["name"], cfg=cfg, B=B, V=V,
                                dtype=w["dtype"]))
+
+
+# One level of dynamic-tree expansion on the setting "RheoSampling 2026" §5
+# measures on (EAGLE-3 trees, temperature 1.0, Llama-3.1's 128256-token
+# vocabulary): 64 trees, 10 frontier nodes each, 10 children per node,
+# rheostat m = 1 (the page's recommended value), 10 nodes kept per tree.
+RHEO_WORKLOAD = dict(name="rheo-expand-B64-W10-K10-m1-V128256-bf16", B=64, W=10, K=10, m=1,
+                     n_keep=10, V=128256, dtype="bf16", T=1.0, level=3, eps=1e-6)
+
+
+@dataclass
+class RheoBatch:
+    draft: torch.Tensor           # [F, V] draft logits of the frontier nodes
+    cu_frontier: torch.Tensor     # [B+1] int32
+    frontier_score: torch.Tensor  # [F] float32, ln path score
+    temperature: torch.Tensor     # [B] float32
+    K: int
+    m: int
+    n_keep: int
+    eps: float
+    level: int
+    seed: int
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def B(self):
+        return self.cu_frontier.numel() - 1
+
+    @property
+    def V(self):
+        return self.draft.shape[1]
+
+
+def make_rheo(device="cpu", input_seed=None, **overrides) -> RheoBatch:
+    """Frontier rows for one expansion level (fields overridable: B, W (an
+    int or a (lo, hi) range per tree), K, m, n_keep, V, dtype, T, level,
+    eps)."""
+    w = dict(RHEO_WORKLOAD)
+    w.update(overrides)
+    device = torch.device(device)
+    seed = INPUT_SEED_BASE + 0x100 if input_seed is None else input_seed
+    gcpu = torch.Generator().manual_seed(seed)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed + 1)
+    B, V = w["B"], w["V"]
+    if isinstance(w["W"], tuple):
+        lo, hi = w["W"]
+        W = torch.randint(lo, hi + 1, (B,), generator=gcpu)
+    else:
+        W = torch.full((B,), int(w["W"]), dtype=torch.int64)
+    cu = torch.zeros(B + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(W, 0)
+    F = int(cu[-1])
+    T = _per_request(w["T"], B, gcpu, "cpu")
+    bias = _zipf_bias(B, V, g, device)
+    req = torch.repeat_interleave(torch.arange(B), W).to(device)
+    z = 2.0 * torch.randn(F, V, generator=g, device=device) + bias[req]
+    draft = z.to(_DTYPES[w["dtype"]])
+    del z, bias
+    level = int(w["level"])
+    score = -3.0 * level * torch.rand(F, generator=gcpu)
+    return RheoBatch(draft=draft, cu_frontier=cu.to(torch.int32).to(device),
+                     frontier_score=score.to(torch.float32).to(device),
+                     temperature=T.to(device), K=int(w["K"]), m=int(w["m"]),
+                     n_keep=int(w["n_keep"]), eps=float(w["eps"]), level=level,
+                     seed=VERIFY_SEED_BASE + 0x100,
+                     meta=dict(workload=w["name"] if not overrides else
+                               f"{w['name']}+{sorted(overrides.items())}",
+                               B=B, V=V, dtype=w["dtype"]))

@@ -110,3 +110,32 @@ def test_wait_selftest_rejects_bad_arguments(L):
     assert L.spec_wait_selftest(0, 20 * 10 ** 9, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
     assert L.spec_wait_selftest(1, 1000, None, None) == sv.SPEC_ERR_WORKSPACE
     assert L.spec_wait_selftest(1, 1000, FAKE + 16, None) == sv.SPEC_ERR_WORKSPACE
+
+
+def test_rheo_expand_rejects_bad_arguments_on_the_host(L):
+    f = L.spec_rheo_expand
+    ws = sv.spec_rheo_expand_workspace(8, 1000)
+    assert ws >= 256 + 8 * 128 * 8
+    assert sv.spec_rheo_expand_workspace(-1, 1000) == 0
+    assert sv.spec_rheo_expand_workspace(8, 0) == 0
+    ok = dict(draft=FAKE, ddt=1, cu=FAKE, fscore=FAKE, temp=FAKE, B=2, F=8, V=1000, K=10, m=1,
+              eps=1e-6, n_keep=10, seed=1, level=0, token=FAKE, qproxy=None, qtrue=None,
+              score=FAKE, keep=FAKE, ws=FAKE, ws_bytes=ws, stream=None)
+    for kw, code in [(dict(K=0), sv.SPEC_ERR_INVALID_ARG), (dict(K=129), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(V=5, K=6), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(m=10), sv.SPEC_ERR_INVALID_ARG), (dict(m=-1), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(eps=-1.0), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(eps=float("inf")), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(level=1 << 24), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(n_keep=-1), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(n_keep=sv.SPEC_RHEO_MAX_CANDIDATES + 1), sv.SPEC_ERR_UNSUPPORTED),
+                     (dict(ddt=3), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(draft=FAKE + 8), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(keep=None), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(score=None), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(cu=None), sv.SPEC_ERR_INVALID_ARG),
+                     (dict(ws=None), sv.SPEC_ERR_WORKSPACE),
+                     (dict(ws_bytes=ws - 1), sv.SPEC_ERR_WORKSPACE)]:
+        a = dict(ok)
+        a.update(kw)
+        assert f(*a.values()) == code, kw
