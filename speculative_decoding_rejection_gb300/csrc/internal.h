@@ -58,14 +58,31 @@ int launch_row_pass(const RowPassArgs &a, cudaStream_t stream);
 int nchunks(int V, int dtype, int chunk_bytes);
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Optional epilogue of the top-128 select for RheoSampling tree expansion:
+// for every row f, the K children in rheostat slot order (the m best tokens
+// other than the probe, the probe drawn from the row's top-128 law at
+// u(seed, f, level, 3), the next best), their proxy probabilities under the
+// unscaled top-128 law (the probe's: q(x_{m+1}) + eps), the probe law of
+// each child's token, and path scores fscore[f] + ln q_proxy, written to
+// [rows, K] arrays (qproxy and qtrue may be NULL).
+struct RheoEpi {
+  const float *fscore;
+  int K, m;
+  float eps;
+  uint64_t seed;
+  int level;
+  int32_t *token;
+  float *qproxy, *qtrue, *score;
+};
+
 // Top-128 select + softmax over draft rows. Row r belongs to the request b
 // with cu_rows[b] <= r < cu_rows[b+1]; rows >= cu_rows[B] are skipped.
-// When `req_mode` is non-NULL, rows of requests whose mode is not
-// sampling are skipped.
+// out_idx / out_prob may be NULL when `rh` is given: the rows then feed the
+// RheoSampling epilogue instead.
 int launch_topk128(const void *logits, int dtype, int rows_bound, int V,
                    const int32_t *cu_rows, const float *temperature, int B,
                    int32_t *out_idx, float *out_prob, WsHeader *hdr,
-                   cudaStream_t stream);
+                   cudaStream_t stream, const RheoEpi *rh = nullptr);
 
 bool aligned(const void *p, size_t a);
 

@@ -18,8 +18,14 @@
 // from it, and a collection pass that keeps the lowest ids among ties. The
 // survivors are put in id order by counting smaller ids and softmaxed at
 // temperature T; T < 0.05 gives a one-hot on the argmax.
+//
+// With a RheoSampling epilogue (spec_rheo_expand) the block then expands the
+// row into its tree children from the survivors still in shared memory, so
+// the 128 logits are neither written out nor gathered again.
 #include "common.cuh"
 #include "internal.h"
+
+#include <climits>
 
 namespace sv {
 
@@ -39,6 +45,8 @@ struct TopkArgs {
   int32_t *out_idx;
   float *out_prob;
   WsHeader *hdr;
+  int has_rh;
+  RheoEpi rh;
 };
 
 constexpr int TK_WARPS = TK_THREADS / 32;
@@ -62,7 +70,13 @@ struct TopkSmem {
   int use_fallback;
   float S;
   float T;
+  float zmax;            // largest survivor logit
+  float red[8];          // epilogue: per-warp sums and scan totals
+  float Zc, qm;
+  int probe_lo, probe_hi;
 };
+static_assert(TK_THREADS == 4 * SPEC_TOPK, "the epilogue counts with four threads per survivor");
+static_assert(CAND_CAP * 2 >= 5 * SPEC_TOPK, "the epilogue's counters fit in the candidate area");
 
 __device__ __forceinline__ unsigned key_of(uint32_t bits, bool bf16) {
   if (bf16) {
@@ -214,6 +228,104 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
   }
   __syncthreads();
   return true;
+}
+
+// RheoSampling expansion of row r ("RheoSampling 2026": §2 true sampling law
+// and proxy, §3 rheostat m, §7 no temperature in construction), run by the
+// whole block after the select. sh.sel_idx / sel_val hold the survivors in
+// ascending id, sh.sel_e / sh.S their law at the tree's temperature (the
+// probe's true sampling law) and sh.zmax their largest logit.
+__device__ void rheo_epilogue(const TopkArgs &a, TopkSmem &sh, int r, int ksel) {
+  const RheoEpi &h = a.rh;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  int *cnt = reinterpret_cast<int *>(sh.cand);   // free once the select is done
+  int *rank_of = cnt + 4 * SPEC_TOPK;
+  {
+    // rank best first (logit descending, ties and -inf to the lower id,
+    // padding last): four threads per survivor count 32 entries each
+    const int e = t & (SPEC_TOPK - 1), part = t / SPEC_TOPK;
+    const float ze = e < ksel ? sh.sel_val[e] : -INFINITY;
+    const int ke = e < ksel ? sh.sel_idx[e] : INT_MAX;
+    int c = 0;
+#pragma unroll 8
+    for (int j = part * 32; j < part * 32 + 32; ++j) {
+      const float zj = j < ksel ? sh.sel_val[j] : -INFINITY;
+      const int kj = j < ksel ? sh.sel_idx[j] : INT_MAX;
+      c += (zj > ze || (zj == ze && kj < ke)) ? 1 : 0;
+    }
+    cnt[part * SPEC_TOPK + e] = c;
+  }
+  if (t == 0) {
+    sh.probe_lo = SPEC_TOPK;
+    sh.probe_hi = -1;
+    sh.qm = 0.f;
+  }
+  __syncthreads();
+  // survivors (threads t < 128): rank, unscaled weight, probe-law prefix sum
+  const bool surv = t < SPEC_TOPK;
+  const bool valid = t < ksel;
+  int rk = SPEC_TOPK;
+  float eu = 0.f, qt = 0.f, C = 0.f;
+  if (surv) {
+    rk = cnt[t] + cnt[SPEC_TOPK + t] + cnt[2 * SPEC_TOPK + t] + cnt[3 * SPEC_TOPK + t];
+    rank_of[t] = rk;
+    eu = valid && sh.sel_val[t] > -INFINITY ? expf(sh.sel_val[t] - sh.zmax) : 0.f;
+    qt = valid ? sh.sel_e[t] / sh.S : 0.f;
+    float su = eu;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
+    C = qt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, C, o);
+      if (lane >= o) C += y;
+    }
+    if (lane == 31) {
+      sh.red[warp] = su;
+      sh.red[4 + warp] = C;
+    }
+  }
+  __syncthreads();
+  float qu = 0.f;
+  if (surv) {
+    float off = 0.f;
+    for (int k = 0; k < warp; ++k) off += sh.red[4 + k];
+    C += off;
+    if (t == SPEC_TOPK - 1) sh.Zc = C;
+    qu = eu / (sh.red[0] + sh.red[1] + sh.red[2] + sh.red[3]);
+    if (valid && rk == h.m) sh.qm = qu;        // q(x_{m+1})
+  }
+  __syncthreads();
+  if (surv) {
+    // the probe: the smallest id (ascending slot) with u * Z < C; if rounding
+    // leaves none, the last slot with weight
+    const float tu = uniform24(h.seed, (uint32_t)r, (uint32_t)h.level, 3u) * sh.Zc;
+    if (tu < C) atomicMin(&sh.probe_lo, t);
+    if (qt > 0.f) atomicMax(&sh.probe_hi, t);
+  }
+  __syncthreads();
+  if (valid) {
+    const int ps = sh.probe_lo < SPEC_TOPK ? sh.probe_lo : max(sh.probe_hi, 0);
+    const int prk = rank_of[ps];
+    const size_t out0 = (size_t)r * h.K;
+    const float fs = h.fscore[r];
+    int slot = -1;
+    float pr = qu;
+    if (t == ps) {
+      slot = h.m;
+      pr = sh.qm + h.eps;
+    } else {
+      const int rr = rk - (prk < rk ? 1 : 0);
+      if (rr < h.K - 1) slot = rr < h.m ? rr : rr + 1;
+    }
+    if (slot >= 0) {
+      h.token[out0 + slot] = sh.sel_idx[t];
+      if (h.qproxy) h.qproxy[out0 + slot] = pr;
+      if (h.qtrue) h.qtrue[out0 + slot] = qt;
+      h.score[out0 + slot] = fs + logf(pr);
+    }
+  }
+  __syncthreads();
 }
 
 template <bool BF16>
@@ -393,6 +505,7 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
     for (int k = t; k < ksel; k += 32) m = fmaxf(m, sh.sel_val[k]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (t == 0) sh.zmax = m;
     if (greedy) {
       int first = 0x7fffffff;
       for (int k = t; k < ksel; k += 32)
@@ -415,11 +528,12 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
     }
   }
   __syncthreads();
-  if (t < SPEC_TOPK) {
+  if (t < SPEC_TOPK && a.out_idx != nullptr) {
     const bool ok = t < ksel;
     a.out_idx[(long long)r * SPEC_TOPK + t] = ok ? sh.sel_idx[t] : -1;
     a.out_prob[(long long)r * SPEC_TOPK + t] = ok ? sh.sel_e[t] / sh.S : 0.f;
   }
+  if (a.has_rh) rheo_epilogue(a, sh, r, ksel);
   __syncthreads();
 }
 
@@ -451,8 +565,10 @@ __global__ void k_topk_validate(const TopkArgs a) {
 
 int launch_topk128(const void *logits, int dtype, int rows_bound, int V, const int32_t *cu_rows,
                    const float *temperature, int B, int32_t *out_idx, float *out_prob,
-                   WsHeader *hdr, cudaStream_t stream) {
-  TopkArgs a;
+                   WsHeader *hdr, cudaStream_t stream, const RheoEpi *rh) {
+  TopkArgs a{};
+  a.has_rh = rh != nullptr;
+  if (rh) a.rh = *rh;
   a.logits = static_cast<const char *>(logits);
   a.dtype = dtype;
   a.row_bytes = (long long)V * (dtype == SPEC_BF16 ? 2 : 4);
