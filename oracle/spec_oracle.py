@@ -113,7 +113,15 @@ R17 The probe's uniform is u(seed, f, level, 3): key b = the global frontier
 R18 The deterministic children depend on the probe's token (R15), so a
     verifier of these trees tests the probe first, as "RheoSampling 2026" §4
     step 1 does, and the deterministic children after it as point masses.
-    Only construction is computed here.
+R19 Point-mass children ("RheoSampling 2026" §4 steps 1-3 with deterministic
+    candidates): a child flagged fixed was not drawn from its parent's draft
+    law, so its draft law is the point mass on its token. It is accepted with
+    probability min(1, p_j(x) / 1) = p_j(x). On rejection the target law
+    becomes norm(max(0, p_j - delta_x)), i.e. p_j without x, renormalised,
+    and the draft law of the drawn children is unchanged (without replacement
+    runs over drawn children only). Children are still tested in node-index
+    order; a tree whose fixed children depend on a drawn sibling's token must
+    list that sibling first.
 """
 from __future__ import annotations
 
@@ -453,14 +461,16 @@ def children_of(parent: np.ndarray, v: int):
     return [int(c) for c in np.nonzero(np.asarray(parent) == v)[0]]
 
 
-def rrsw_node(p, q, child_tokens, coins):
+def rrsw_node(p, q, child_tokens, coins, fixed=None):
     """Recursive rejection sampling without replacement at one node
-    (RheoSampling 2026, §4; R7).
+    (RheoSampling 2026, §4; R7, R19).
 
     p, q: the node's target and draft laws. child_tokens: the children's
     tokens in the order they were drawn. coins: one uniform per child.
-    Returns (index of the accepted child or -1, the law to sample when all
-    are rejected (unnormalised), list of (u, a) pairs that were tested).
+    fixed: optional flags, one per child; a fixed child is a point mass on
+    its token (R19). Returns (index of the accepted child or -1, the law to
+    sample when all are rejected (unnormalised), list of (u, a) pairs that
+    were tested).
     """
     p_j = np.asarray(p, dtype=np.float64)
     q = np.asarray(q, dtype=np.float64)
@@ -468,6 +478,18 @@ def rrsw_node(p, q, child_tokens, coins):
     q_j = q.copy()
     tested = []
     for j, x in enumerate(child_tokens):
+        if fixed is not None and fixed[j]:
+            # point mass: accept with min(1, p_j(x) / 1); on rejection the
+            # residual max(0, p_j - delta_x) is p_j without x
+            a = acceptance_prob(p_j[x], 1.0)
+            tested.append((coins[j], a))
+            if coin_accepts(coins[j], a):
+                return j, None, tested
+            r = np.maximum(0.0, p_j - (np.arange(p_j.size) == x))
+            Z = np.sum(r)
+            if Z > 0.0:
+                p_j = r / Z
+            continue
         a = acceptance_prob(p_j[x], q_j[x])
         tested.append((coins[j], a))
         if coin_accepts(coins[j], a):
@@ -488,7 +510,7 @@ def rrsw_node(p, q, child_tokens, coins):
 
 def verify_tree(target, draft, node_token, parent, cu_nodes, temperature,
                 seed, max_depth, rule=RULE_STRICT, requests=None,
-                draft_kind=DRAFT_LOGITS):
+                draft_kind=DRAFT_LOGITS, node_fixed=None):
     """Multi-draft tree verification by RRSw.
 
     Request b owns nodes cu_nodes[b] .. cu_nodes[b+1]-1; local node 0 is the
@@ -496,7 +518,7 @@ def verify_tree(target, draft, node_token, parent, cu_nodes, temperature,
     ordered. Target row n is the target law after the path to node n; draft
     row n is the law node n's children were drawn from: logits (q =
     softmax(z/T)) or, with draft_kind == DRAFT_PROBS, the probabilities
-    themselves.
+    themselves. node_fixed[n] != 0 marks node n as a point-mass child (R19).
 
     Returns tokens [n, max_depth+1], accepted [n], path [n, max_depth+1]
     (local node ids of accepted nodes), flag_slot [n], requests.
@@ -546,8 +568,9 @@ def verify_tree(target, draft, node_token, parent, cu_nodes, temperature,
             else:
                 q = softmax_T(as_f64(draft[base + v]), T)
             coins = [uniform(seed, b, c, STREAM_COIN) for c in kids]
+            fx = None if node_fixed is None else [bool(node_fixed[base + c]) for c in kids]
             acc, law, tested = rrsw_node(p, q, [ntok[base + c] for c in kids],
-                                         coins)
+                                         coins, fx)
             if flagged_at < 0 and any(coin_flagged(u, a) for u, a in tested):
                 flagged_at = depth
             if acc >= 0:

@@ -261,3 +261,123 @@ def test_pins_catch_ascending_selection(monkeypatch):
     monkeypatch.setattr(O, "rheo_select", worst_first)
     with pytest.raises(AssertionError):
         _run_pins()
+
+
+# ------------------------- verifying built trees: point-mass children (R19)
+def _node_output_law(p, qt, kids, fixed):
+    """Exact law of the token one node emits: every accept / reject branch
+    of the oracle's rrsw_node, weighted by its acceptance probabilities
+    (coin 0 accepts whenever a > 0; a coin just below 1 rejects unless
+    a = 1), plus the final draw's law when every child is rejected."""
+    V = p.size
+    out = np.zeros(V)
+    for k in range(len(kids) + 1):            # children 0..k-1 rejected, k accepted
+        coins = [1.0 - 2.0 ** -40] * k + ([0.0] if k < len(kids) else [])
+        coins += [0.0] * (len(kids) - len(coins))
+        acc, law, tested = O.rrsw_node(p, qt, kids, coins, fixed)
+        if acc != (k if k < len(kids) else -1):
+            continue                          # this branch has probability 0
+        w = 1.0
+        for j in range(min(k, len(tested))):
+            w *= 1.0 - tested[j][1]
+        if k < len(kids):
+            out[kids[k]] += w * tested[k][1]
+        elif w > 0.0:
+            out += w * law / law.sum()
+    return out
+
+
+def _rheo_node_law(zd, zt, T, K, m, probe_first=True):
+    """Output law of one node built by construction and verified with the
+    probe drawn from q~ (enumerated exactly) and point-mass leads."""
+    ids = np.arange(zd.size)
+    qt = special.softmax(zd / T)               # V <= 128: the top-128 law is dense
+    p = special.softmax(zt / T)
+    order = sorted(ids.tolist(), key=lambda x: (-zd[x], x))
+    out = np.zeros(zd.size)
+    for u in ids:
+        slots = O.rheo_slots(np.array(order), int(u), K, m)
+        det = [x for x in slots if x != u]
+        if probe_first:
+            kids, fixed = [int(u)] + det, [False] + [True] * len(det)
+        else:
+            kids, fixed = slots, [x != u for x in slots]
+        out += qt[u] * _node_output_law(p, qt, kids, fixed)
+    return out, p
+
+
+@pytest.mark.parametrize("K,m,T,seed", [(3, 1, 1.0, 0), (4, 0, 0.7, 1), (5, 2, 1.3, 2),
+                                        (6, 5, 0.9, 3), (2, 1, 2.0, 4)])
+def test_built_node_verified_probe_first_is_lossless(K, m, T, seed):
+    """"RheoSampling 2026" §6 Teorema 1 for one built node: the emitted
+    token's law equals p exactly."""
+    rng = np.random.default_rng(seed)
+    zd = rng.standard_normal(6) * 1.5
+    zt = zd + rng.standard_normal(6)
+    law, p = _rheo_node_law(zd, zt, T, K, m)
+    np.testing.assert_allclose(law, p, atol=1e-12)
+
+
+def test_leads_tested_before_the_probe_are_not_lossless():
+    """The reading behind R18: the leads depend on the probe's token, so
+    testing them first distorts the law; probe first restores it."""
+    rng = np.random.default_rng(7)
+    zd = rng.standard_normal(6) * 1.5
+    zt = zd + rng.standard_normal(6) * 1.5
+    bad, p = _rheo_node_law(zd, zt, 1.0, 3, 2, probe_first=False)
+    good, _ = _rheo_node_law(zd, zt, 1.0, 3, 2)
+    assert np.abs(bad - p).max() > 1e-3
+    np.testing.assert_allclose(good, p, atol=1e-12)
+
+
+def test_fixed_children_alone_are_lossless():
+    rng = np.random.default_rng(8)
+    zt = rng.standard_normal(5)
+    p = special.softmax(zt)
+    qt = special.softmax(rng.standard_normal(5))
+    law = _node_output_law(p, qt, [3, 0, 4], [True, True, True])
+    np.testing.assert_allclose(law, p, atol=1e-12)
+    # a single fixed child x is accepted with probability p(x)
+    _, _, tested = O.rrsw_node(p, qt, [2], [0.5], [True])
+    assert tested[0][1] == pytest.approx(p[2], rel=1e-14)
+
+
+def test_verify_tree_with_point_mass_children_chain_and_greedy():
+    """Through verify_tree: a chain tree of fixed children emits the token
+    of each accepted node; greedy trees ignore the flags."""
+    rng = np.random.default_rng(9)
+    V = 7
+    zt = rng.standard_normal((3, V))
+    zd = rng.standard_normal((3, V))
+    parent = [-1, 0, 1]
+    tokens = [-1, int(np.argmax(zt[0])), int(np.argmax(zt[1]))]
+    for T in (0.01, 1.0):
+        r = O.verify_tree(zt, zd, tokens, parent, [0, 3], [T], 5, 2, node_fixed=[0, 1, 1])
+        assert 0 <= r["accepted"][0] <= 2
+        n = int(r["accepted"][0])
+        assert r["tokens"][0, :n].tolist() == tokens[1:1 + n]
+        if T < 0.05:
+            assert n == 2                      # argmax children are accepted greedily
+
+
+def _pins_rheo_verify():
+    test_built_node_verified_probe_first_is_lossless(3, 1, 1.0, 0)
+    test_built_node_verified_probe_first_is_lossless(5, 2, 1.3, 2)
+    test_fixed_children_alone_are_lossless()
+
+
+def test_pins_catch_fixed_child_tested_against_q(monkeypatch):
+    real = O.rrsw_node
+    monkeypatch.setattr(O, "rrsw_node",
+                        lambda p, q, kids, coins, fixed=None: real(p, q, kids, coins, None))
+    with pytest.raises(AssertionError):
+        _pins_rheo_verify()
+
+
+def test_pins_catch_fixed_child_accepted_with_its_draft_ratio(monkeypatch):
+    real_acc = O.acceptance_prob
+    # a point mass mistaken for a draw from q: min(1, p / q(x)) instead of p
+    monkeypatch.setattr(O, "acceptance_prob",
+                        lambda p_d, q_d: real_acc(p_d, 0.5 if q_d == 1.0 else q_d))
+    with pytest.raises(AssertionError):
+        _pins_rheo_verify()
