@@ -286,6 +286,33 @@ int spec_verify_tree(const void *target, int tdt, const void *draft, int ddt,
                      int32_t *out_path, void *workspace, size_t ws_bytes,
                      spec_stream_t stream);
 
+/*
+ * spec_verify_tree with point-mass children ("RheoSampling 2026", §4 with
+ * deterministic candidates, such as the leads spec_rheo_expand builds).
+ * Same arguments and semantics, plus
+ *   node_fixed  [n_nodes] int32 or NULL (= spec_verify_tree): nonzero marks
+ *               a node that was not drawn from its parent's draft law. Such
+ *               a child x is accepted with probability p_j(x), p_j the
+ *               parent's current target law; on rejection p_{j+1} is p_j
+ *               without x, renormalised, and the draft law of the drawn
+ *               siblings is unchanged (without replacement runs over drawn
+ *               children only). Roots' flags are ignored.
+ * Children are still tested in node-index order. The test is lossless when
+ * a fixed child's token does not depend on the draws of the siblings tested
+ * after it: for a RheoSampling node list the probe (slot m of
+ * spec_rheo_expand) first, then the other slots in order. Drawn siblings
+ * carry distinct tokens; a fixed child may repeat a sibling's token.
+ */
+int spec_verify_tree_ext(const void *target, int tdt, const void *draft,
+                         int ddt, int dk, const int32_t *node_token,
+                         const int32_t *parent, const int32_t *node_fixed,
+                         const int32_t *cu_nodes, const float *temperature,
+                         int B, int n_nodes, int V, int max_depth,
+                         int max_branch, uint64_t seed, int32_t *out_tokens,
+                         int32_t *out_accepted, int32_t *out_path,
+                         void *workspace, size_t ws_bytes,
+                         spec_stream_t stream);
+
 /* Bytes of workspace draft_topk_softmax needs (0 on invalid sizes). */
 size_t draft_topk_softmax_workspace(int rows, int V);
 

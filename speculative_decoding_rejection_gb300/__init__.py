@@ -18,7 +18,7 @@ __all__ = [
     "SPEC_DRAFT_SPARSE128", "SPEC_RULE_STRICT", "SPEC_RULE_GREEDY",
     "SPEC_RULE_STRICT_TOP128", "SPEC_RULE_CACTUS", "SPEC_TOPK", "lib", "spec_status_string",
     "spec_verify_linear", "spec_verify_linear_ext", "spec_verify_linear_workspace", "spec_verify_tree",
-    "spec_verify_tree_workspace", "draft_topk_softmax",
+    "spec_verify_tree_workspace", "spec_verify_tree_ext", "draft_topk_softmax",
     "draft_topk_softmax_workspace", "spec_get_status", "spec_uniforms",
     "spec_profile_row_pass", "spec_rheo_expand", "spec_rheo_expand_workspace", "SpecError",
 ]
@@ -59,6 +59,8 @@ _SIGS = {
     "spec_verify_tree_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "spec_verify_tree": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                 _i32, _i32, _i32, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify_tree_ext": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32,
+                                    _i32, _i32, _i32, _i32, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "draft_topk_softmax_workspace": (_sz, [_i32, _i32]),
     "draft_topk_softmax": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp,
                                   _sz, _vp]),
@@ -236,8 +238,10 @@ def spec_verify_tree_workspace(B: int, n_nodes: int, V: int, max_depth: int, max
 
 def spec_verify_tree(target, draft, node_token, parent, cu_nodes, temperature, seed: int, *,
                      max_depth: int, max_branch: int, draft_kind: int = SPEC_DRAFT_LOGITS,
-                     workspace=None, out=None, stream=None):
-    """Verifies a batch of draft trees (RRSw) on the GPU.
+                     node_fixed=None, workspace=None, out=None, stream=None):
+    """Verifies a batch of draft trees (RRSw) on the GPU. With `node_fixed`
+    ([n_nodes] int32, nonzero = a point-mass child) the call goes through
+    spec_verify_tree_ext.
 
     Returns (tokens [B, max_depth+1], accepted [B], path [B, max_depth+1],
     workspace).
@@ -257,12 +261,17 @@ def spec_verify_tree(target, draft, node_token, parent, cu_nodes, temperature, s
     else:
         tokens, accepted, path = out
     ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
-    code = lib().spec_verify_tree(
-        _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(node_token),
-        _ptr(parent), _ptr(cu_nodes), _ptr(temperature), B, n_nodes, V, max_depth, max_branch,
-        ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), _ptr(tokens), _ptr(accepted), _ptr(path),
-        _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
-    _check(code, "spec_verify_tree")
+    head = (_ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(node_token),
+            _ptr(parent))
+    tail = (_ptr(cu_nodes), _ptr(temperature), B, n_nodes, V, max_depth, max_branch,
+            ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), _ptr(tokens), _ptr(accepted), _ptr(path),
+            _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    if node_fixed is None:
+        code = lib().spec_verify_tree(*head, *tail)
+        _check(code, "spec_verify_tree")
+    else:
+        code = lib().spec_verify_tree_ext(*head, _ptr(node_fixed), *tail)
+        _check(code, "spec_verify_tree_ext")
     return tokens, accepted, path, ws
 
 

@@ -9,6 +9,13 @@
 // bonus draw from that leaf's target law. Greedy trees (T < 0.05) accept the
 // first child equal to argmax p_v and otherwise emit argmax p_v.
 //
+// Point-mass children (spec_verify_tree_ext): a child flagged fixed was not
+// drawn from the draft law (a deterministic lead of a RheoSampling tree,
+// §3), so its draft law is the point mass on its token. It is accepted with
+// probability p_j(x); on rejection p_{j+1} is p_j without x, renormalised by
+// 1 - p_j(x) (a scalar: no pass over the rows), and the draft law of the
+// drawn children is unchanged.
+//
 // Uniforms: coin of child c at u(seed, b, c, 0); the final draw at node v at
 // u(seed, b, v + 1, 1) (residual) or u(seed, b, v + 1, 2) (bonus), so a chain
 // tree reproduces the linear verifier draw for draw.
@@ -57,6 +64,7 @@ struct TreeArgs {
   int tdt, ddt, dk;
   const int32_t *node_token;
   const int32_t *parent;
+  const int32_t *node_fixed;   // optional point-mass flags
   const int32_t *cu;
   const float *temp;
   int B, n_nodes, V, max_depth, max_branch;
@@ -150,6 +158,7 @@ struct WalkSmem {
   float scratch[33];
   int kids[SPEC_MAX_TREE_BRANCH];
   int kx[SPEC_MAX_TREE_BRANCH];          // children's tokens
+  int kfix[SPEC_MAX_TREE_BRANCH + 1];    // point-mass child (its level of the chain)
   float kzt[SPEC_MAX_TREE_BRANCH];       // target logit at each child's token
   float kzd[SPEC_MAX_TREE_BRANCH];       // draft logit (or probability) there
   float s[SPEC_MAX_TREE_BRANCH + 1];     // 1 / (1 - q(E_j))
@@ -159,7 +168,7 @@ struct WalkSmem {
   RowStat st[2][2];                      // this slice's statistics, by pass parity (target, draft)
   RowStat node[2];                       // the node's statistics (target, draft)
   int nk, jstar, xmin, xlast, rstar, accepted_child, par, ok, go;
-  float carry, target, Z;
+  float carry, target, Z, pfix;
 };
 
 struct NodeLaw {        // p(y) = 2^((zt - mt) c) / St, q(y) likewise or given
@@ -176,12 +185,17 @@ __device__ __forceinline__ Slice my_slice(int V, int rank) {
 }
 
 // p_L(y) and the residual max(0, p_L - q_L) (or p_L itself) from the raw
-// p(y), q(y) through the chain of normalisers.
-__device__ __forceinline__ float chain_weight(float p, float q, int L, bool residual,
+// p(y), q(y) of token y through the chain of normalisers. A point-mass level
+// removes its own token and rescales the rest.
+__device__ __forceinline__ float chain_weight(float p, float q, int y, int L, bool residual,
                                               const WalkSmem &sh) {
-  for (int i = 0; i < L; ++i)
-    if (!sh.skip[i]) p = fmaxf(0.f, p - q * sh.s[i]) * sh.rinv[i];
-  return residual ? fmaxf(0.f, p - q * sh.s[L]) : p;
+  for (int i = 0; i < L; ++i) {
+    if (sh.skip[i]) continue;
+    p = sh.kfix[i] ? (y == sh.kx[i] ? 0.f : p * sh.rinv[i])
+                   : fmaxf(0.f, p - q * sh.s[i]) * sh.rinv[i];
+  }
+  if (!residual) return p;
+  return sh.kfix[L] ? (y == sh.kx[L] ? 0.f : p) : fmaxf(0.f, p - q * sh.s[L]);
 }
 
 template <int DK>
@@ -204,13 +218,25 @@ __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkS
   for (int i = 0; i < L; ++i) {
     if (sh.skip[i]) continue;
     const float si = sh.s[i], ri = sh.rinv[i];
+    if (sh.kfix[i]) {
+      const int xi = sh.kx[i];
 #pragma unroll
-    for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = fmaxf(0.f, w[k] - q[k] * si) * ri;
+      for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = x0 + k == xi ? 0.f : w[k] * ri;
+    } else {
+#pragma unroll
+      for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = fmaxf(0.f, w[k] - q[k] * si) * ri;
+    }
   }
   if (residual) {
-    const float sL = sh.s[L];
+    if (sh.kfix[L]) {
+      const int xL = sh.kx[L];
 #pragma unroll
-    for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = fmaxf(0.f, w[k] - q[k] * sL);
+      for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = x0 + k == xL ? 0.f : w[k];
+    } else {
+      const float sL = sh.s[L];
+#pragma unroll
+      for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = fmaxf(0.f, w[k] - q[k] * sL);
+    }
   }
 }
 
@@ -476,6 +502,7 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
         const long long rv = t.base + v;
         const int x = a.node_token[t.base + sh.kids[j]];
         sh.kx[j] = x;
+        sh.kfix[j] = a.node_fixed != nullptr && a.node_fixed[t.base + sh.kids[j]] != 0;
         if (t.mode != MODE_GREEDY && (unsigned)x < (unsigned)a.V) {
           sh.kzt[j] = load_elem(a.target + rv * a.t_row_bytes, a.tdt, x);
           sh.kzd[j] = load_elem(a.draft + rv * a.d_row_bytes, a.ddt, x);
@@ -548,32 +575,50 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     __syncthreads();
     float qE = 0.f;
     int accepted = -1, L = 0;
+    bool passed = false;   // the tile totals of level L's residual are in sh
     for (int j = 0; j < nk; ++j) {
       // coin of child j at its token x, with p_j(x) and q_j(x) from the chain
+      // (a point mass has q_j(x) = 1)
       if (threadIdx.x == 0) {
         const int ch = sh.kids[j];
         const float p = ex2((sh.kzt[j] - nl.mt) * c) * nl.invSt;
         const float qx = DK == SPEC_DRAFT_PROBS ? sh.kzd[j]
                                                 : ex2((sh.kzd[j] - nl.md) * c) * nl.invSd;
-        const float pj = chain_weight(p, qx, j, false, sh);
-        const float qj = qx * sh.s[j];
+        const float pj = chain_weight(p, qx, sh.kx[j], j, false, sh);
+        const float qj = sh.kfix[j] ? 1.f : qx * sh.s[j];
         const float acc = qj <= pj ? 1.f : pj / qj;
         const bool ok = uniform24(a.seed, (uint32_t)b, (uint32_t)ch, 0) < acc;
         sh.accepted_child = ok ? ch : -1;
         sh.carry = qx;   // q(x), for q(E)
+        sh.pfix = pj;
       }
       __syncthreads();
       const int ac = sh.accepted_child;
       const float qx = sh.carry;
+      const float pj = sh.pfix;
       __syncthreads();
       if (ac >= 0) {
         accepted = ac;
         break;
       }
+      if (sh.kfix[j]) {
+        // point-mass rejection: p_{j+1} = p_j without x over Z_j = 1 - p_j(x)
+        L = j;
+        passed = false;
+        if (threadIdx.x == 0) {
+          const float Zf = 1.f - pj;
+          sh.skip[j] = !(Zf > 0.f);
+          sh.rinv[j] = Zf > 0.f ? 1.f / Zf : 1.f;
+          sh.s[j + 1] = sh.s[j];
+        }
+        __syncthreads();
+        continue;
+      }
       // rejection: Z_j of the residual at level j (tile totals kept for a
       // possible final draw), then the next draft normaliser
       weight_pass<DK>(a, sh, nl, c, j, true, sl, cluster);
       L = j;
+      passed = true;
       qE += qx;
       const float left = 1.f - qE;
       if (threadIdx.x == 0) {
@@ -599,6 +644,8 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     if (sh.skip[L]) {
       residual = false;
       weight_pass<DK>(a, sh, nl, c, L, false, sl, cluster);
+    } else if (!passed) {   // the last rejection was a point mass: no pass yet
+      weight_pass<DK>(a, sh, nl, c, L, true, sl, cluster);
     }
     const int x = weight_draw<DK>(a, sh, nl, c, L, residual,
                                   uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 1), sl, rank);
@@ -655,12 +702,13 @@ extern "C" size_t spec_verify_tree_workspace(int B, int n_nodes, int V, int max_
   return tree_layout(B).total;
 }
 
-extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, int ddt, int dk,
-                                const int32_t *node_token, const int32_t *parent,
-                                const int32_t *cu_nodes, const float *temperature, int B,
-                                int n_nodes, int V, int max_depth, int max_branch, uint64_t seed,
-                                int32_t *out_tokens, int32_t *out_accepted, int32_t *out_path,
-                                void *workspace, size_t ws_bytes, spec_stream_t stream) {
+static int verify_tree(const void *target, int tdt, const void *draft, int ddt, int dk,
+                       const int32_t *node_token, const int32_t *parent,
+                       const int32_t *node_fixed, const int32_t *cu_nodes,
+                       const float *temperature, int B, int n_nodes, int V, int max_depth,
+                       int max_branch, uint64_t seed, int32_t *out_tokens,
+                       int32_t *out_accepted, int32_t *out_path, void *workspace, size_t ws_bytes,
+                       spec_stream_t stream) {
   if (B < 0 || n_nodes < B || V <= 0 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
   if (max_depth < 0 || max_branch < 1) return SPEC_ERR_INVALID_ARG;
   if (max_depth > SPEC_MAX_TREE_DEPTH || max_branch > SPEC_MAX_TREE_BRANCH)
@@ -674,7 +722,8 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
     return SPEC_ERR_INVALID_ARG;
   if (!aligned(target, 16) || !aligned(draft, 16) || !aligned(node_token, 4) ||
       !aligned(parent, 4) || !aligned(cu_nodes, 4) || !aligned(temperature, 4) ||
-      !aligned(out_tokens, 4) || !aligned(out_accepted, 4) || !aligned(out_path, 4))
+      !aligned(out_tokens, 4) || !aligned(out_accepted, 4) || !aligned(out_path, 4) ||
+      !aligned(node_fixed, 4))
     return SPEC_ERR_INVALID_ARG;
   const TreeLayout L = tree_layout(B);
   if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < L.total)
@@ -688,6 +737,7 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   a.dk = dk;
   a.node_token = node_token;
   a.parent = parent;
+  a.node_fixed = node_fixed;
   a.cu = cu_nodes;
   a.temp = temperature;
   a.B = B;
@@ -719,4 +769,28 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (after && cudaEventRecord(after, st) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
+}
+
+extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, int ddt, int dk,
+                                const int32_t *node_token, const int32_t *parent,
+                                const int32_t *cu_nodes, const float *temperature, int B,
+                                int n_nodes, int V, int max_depth, int max_branch, uint64_t seed,
+                                int32_t *out_tokens, int32_t *out_accepted, int32_t *out_path,
+                                void *workspace, size_t ws_bytes, spec_stream_t stream) {
+  return verify_tree(target, tdt, draft, ddt, dk, node_token, parent, nullptr, cu_nodes,
+                     temperature, B, n_nodes, V, max_depth, max_branch, seed, out_tokens,
+                     out_accepted, out_path, workspace, ws_bytes, stream);
+}
+
+extern "C" int spec_verify_tree_ext(const void *target, int tdt, const void *draft, int ddt,
+                                    int dk, const int32_t *node_token, const int32_t *parent,
+                                    const int32_t *node_fixed, const int32_t *cu_nodes,
+                                    const float *temperature, int B, int n_nodes, int V,
+                                    int max_depth, int max_branch, uint64_t seed,
+                                    int32_t *out_tokens, int32_t *out_accepted,
+                                    int32_t *out_path, void *workspace, size_t ws_bytes,
+                                    spec_stream_t stream) {
+  return verify_tree(target, tdt, draft, ddt, dk, node_token, parent, node_fixed, cu_nodes,
+                     temperature, B, n_nodes, V, max_depth, max_branch, seed, out_tokens,
+                     out_accepted, out_path, workspace, ws_bytes, stream);
 }

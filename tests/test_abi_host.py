@@ -139,3 +139,9 @@ def test_rheo_expand_rejects_bad_arguments_on_the_host(L):
         a = dict(ok)
         a.update(kw)
         assert f(*a.values()) == code, kw
+
+
+def test_tree_ext_rejects_a_misaligned_flag_array(L):
+    args = [FAKE, 1, FAKE, 1, 0, FAKE, FAKE, FAKE + 2, FAKE, FAKE, 2, 128, 1000, 6, 4, 1,
+            FAKE, FAKE, None, FAKE, 1 << 20, None]
+    assert L.spec_verify_tree_ext(*args) == sv.SPEC_ERR_INVALID_ARG

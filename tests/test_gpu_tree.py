@@ -13,22 +13,25 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def gpu_tree(tb, draft=None, draft_kind=sv.SPEC_DRAFT_LOGITS):
+def gpu_tree(tb, draft=None, draft_kind=sv.SPEC_DRAFT_LOGITS, node_fixed=None):
     draft = tb.draft if draft is None else draft
     tok, acc, path, ws = sv.spec_verify_tree(
         tb.target, draft, tb.node_token, tb.parent, tb.cu_nodes, tb.temperature, tb.seed,
-        max_depth=tb.max_depth, max_branch=tb.max_branch, draft_kind=draft_kind)
+        max_depth=tb.max_depth, max_branch=tb.max_branch, draft_kind=draft_kind,
+        node_fixed=node_fixed)
     return dict(tokens=tok.cpu().numpy(), accepted=acc.cpu().numpy(), path=path.cpu().numpy(),
                 status=sv.spec_get_status(ws))
 
 
-def oracle_tree(tb, draft=None, draft_kind=sv.SPEC_DRAFT_LOGITS, requests=None):
+def oracle_tree(tb, draft=None, draft_kind=sv.SPEC_DRAFT_LOGITS, requests=None,
+                node_fixed=None):
     draft = tb.draft if draft is None else draft
     host = (lambda t: t.cpu()) if requests is None else (lambda t: t)
     return O.verify_tree(host(tb.target), host(draft), tb.node_token.cpu().numpy(),
                          tb.parent.cpu().numpy(), tb.cu_nodes.cpu().numpy(),
                          tb.temperature.cpu().numpy(), tb.seed, tb.max_depth,
-                         requests=requests, draft_kind=draft_kind)
+                         requests=requests, draft_kind=draft_kind,
+                         node_fixed=None if node_fixed is None else node_fixed.cpu().numpy())
 
 
 def assert_tree_parity(g, r, min_compared):
@@ -144,3 +147,53 @@ def test_walk_reads_only_the_rows_of_visited_nodes():
     assert np.array_equal(g["tokens"], clean["tokens"])
     assert np.array_equal(g["accepted"], clean["accepted"])
     assert np.array_equal(g["path"], clean["path"])
+
+
+# ------------------------------------------- point-mass children (ext entry)
+def random_fixed(tb, frac, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.rand(tb.node_token.numel(), generator=g) < frac).to(torch.int32).to(DEV)
+
+
+@pytest.mark.parametrize("T,V,frac", [(0.8, 5003, 0.3), (1.2, 4096, 0.6), (0.0, 3001, 0.5),
+                                      (0.9, 64, 0.5), (0.7, 20000, 1.0)])
+def test_point_mass_children_match_oracle(T, V, frac):
+    tb = S.make_tree(4, device=DEV, B=12, V=V, dtype="bf16", T=T, input_seed=V + 1)
+    nf = random_fixed(tb, frac, V)
+    g = gpu_tree(tb, node_fixed=nf)
+    assert g["status"] == sv.SPEC_OK
+    assert_tree_parity(g, oracle_tree(tb, node_fixed=nf), min_compared=10)
+
+
+def test_rheosampling_shaped_nodes_probe_first():
+    """Depth-1 trees shaped like a built RheoSampling node: child 1 is drawn
+    (the probe), children 2..K are the best draft tokens other than it,
+    flagged as point masses; many rejections and final draws."""
+    K = 6
+    tb = S.make_tree(4, device=DEV, B=16, N=K + 1, depth=1, branch=K, V=2048, sigma=1.5,
+                     T=1.0, input_seed=91)
+    tok = tb.node_token.cpu().clone()
+    drf = tb.draft.float().cpu()
+    fixed = torch.zeros_like(tok)
+    for b in range(tb.B):
+        base = b * (K + 1)
+        probe = int(tok[base + 1])
+        order = torch.argsort(-drf[base], stable=True).tolist()   # ties to the lower id
+        best = [x for x in order if x != probe][:K - 1]
+        tok[base + 2:base + K + 1] = torch.tensor(best, dtype=tok.dtype)
+        fixed[base + 2:base + K + 1] = 1
+    tb2 = S.TreeBatch(**{**tb.__dict__, "node_token": tok.to(DEV).contiguous()})
+    nf = fixed.to(torch.int32).to(DEV)
+    g = gpu_tree(tb2, node_fixed=nf)
+    assert g["status"] == sv.SPEC_OK
+    assert_tree_parity(g, oracle_tree(tb2, node_fixed=nf), min_compared=14)
+
+
+def test_full_size_tree_workload_with_point_mass_children():
+    tb = S.make_tree(4, device=DEV)
+    nf = random_fixed(tb, 0.5, 4)
+    g = gpu_tree(tb, node_fixed=nf)
+    assert g["status"] == sv.SPEC_OK
+    req = np.arange(1, tb.B, 4)
+    assert_tree_parity(g, oracle_tree(tb, requests=req, node_fixed=nf),
+                       min_compared=len(req) - 2)
