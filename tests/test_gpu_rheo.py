@@ -187,3 +187,88 @@ def test_rheo_invalid_inputs_set_the_status():
     # the workspace stays usable: a valid call afterwards is clean
     g = gpu_rheo(rb)
     assert g["status"] == sv.SPEC_OK
+
+
+# ------------------------------ construction, then verification of the trees
+def built_trees(tokens, K, m):
+    """Depth-1 trees from one frontier row per tree: the probe (slot m)
+    first, then the other slots in order, those flagged as point masses."""
+    B = tokens.shape[0]
+    order = [m] + [s for s in range(K) if s != m]
+    node_token = np.full((B, K + 1), -1, dtype=np.int32)
+    node_token[:, 1:] = tokens[:, order]
+    parent = np.tile(np.array([-1] + [0] * K, dtype=np.int32), B)
+    fixed = np.tile(np.array([0, 0] + [1] * (K - 1), dtype=np.int32), B)
+    return node_token.reshape(-1), parent, fixed
+
+
+def test_built_trees_verify_like_the_oracle():
+    """Construction then verification, each side on its own outputs: the
+    GPU verifies the trees the GPU built, the oracle the trees the oracle
+    built; trees whose probe draw the oracle flags are skipped."""
+    K, m, V, B = 5, 1, 3000, 12
+    rb = S.make_rheo(device=DEV, input_seed=7301, B=B, W=1, V=V, K=K, m=m, n_keep=K,
+                     dtype="bf16", T=0.9, level=0)
+    g, r = gpu_rheo(rb), oracle_rheo(rb)
+    gen = torch.Generator(device=DEV).manual_seed(7302)
+    target = (2.0 * torch.randn(B * (K + 1), V, generator=gen, device=DEV)).to(torch.bfloat16)
+    # each tree's root draft row is its frontier row; leaves' draft rows are unused
+    draft = torch.zeros(B * (K + 1), V, dtype=torch.bfloat16, device=DEV)
+    draft[0::K + 1] = rb.draft
+    cu = np.arange(0, B * (K + 1) + 1, K + 1, dtype=np.int32)
+    nt_g, par, fx = built_trees(g["child_token"], K, m)
+    nt_o, _, _ = built_trees(r["child_token"].astype(np.int32), K, m)
+    seed = 0x5EED
+    tok, acc, path, ws = sv.spec_verify_tree(
+        target, draft, torch.from_numpy(nt_g).to(DEV), torch.from_numpy(par).to(DEV),
+        torch.from_numpy(cu).to(DEV), rb.temperature, seed, max_depth=1, max_branch=K,
+        node_fixed=torch.from_numpy(fx).to(DEV))
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    ro = O.verify_tree(target.cpu(), draft.cpu(), nt_o, par, cu, rb.temperature.cpu().numpy(),
+                       seed, 1, node_fixed=fx)
+    tok, acc = tok.cpu().numpy(), acc.cpu().numpy()
+    compared = 0
+    for b in range(B):
+        if r["probe_flag"][b] or ro["flag_slot"][b] >= 0:
+            continue
+        assert np.array_equal(tok[b], ro["tokens"][b]) and acc[b] == ro["accepted"][b], b
+        compared += 1
+    assert compared >= B - 2
+
+
+def test_built_and_verified_node_emits_the_target_law():
+    """"RheoSampling 2026" §6 on the GPU: 8192 copies of one built node
+    (probe drawn from q~, three point-mass leads, probe verified first);
+    the first emitted token follows p = softmax(z_t / T) (chi-square)."""
+    from scipy import special, stats
+    B, V, K, m, T = 8192, 48, 4, 1, 0.9
+    rng = np.random.default_rng(5)
+    zd = rng.standard_normal(V) * 1.5
+    zt = zd + rng.standard_normal(V)
+    draft_rows = torch.tensor(np.tile(zd, (B, 1)), dtype=torch.float32, device=DEV)
+    cu_f = torch.arange(0, B + 1, dtype=torch.int32, device=DEV)
+    temp = torch.full((B,), T, dtype=torch.float32, device=DEV)
+    tok, _, _, _, _, ws = sv.spec_rheo_expand(draft_rows, cu_f, torch.zeros(B, device=DEV), temp,
+                                              11, 0, K=K, m=m, n_keep=0)
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    nt, par, fx = built_trees(tok.cpu().numpy(), K, m)
+    target = torch.tensor(np.tile(zt, (B * (K + 1), 1)), dtype=torch.float32, device=DEV)
+    draft = torch.tensor(np.tile(zd, (B * (K + 1), 1)), dtype=torch.float32, device=DEV)
+    cu = torch.arange(0, B * (K + 1) + 1, K + 1, dtype=torch.int32, device=DEV)
+    out, acc, _, ws2 = sv.spec_verify_tree(
+        target, draft, torch.from_numpy(nt).to(DEV), torch.from_numpy(par).to(DEV), cu, temp, 12,
+        max_depth=1, max_branch=K, node_fixed=torch.from_numpy(fx).to(DEV))
+    assert sv.spec_get_status(ws2) == sv.SPEC_OK
+    first = out[:, 0].cpu().numpy()
+    p = special.softmax(zt / T)
+    obs = np.bincount(first, minlength=V).astype(np.float64)
+    exp = p * B
+    big = exp >= 5
+    chi = np.sum((obs[big] - exp[big]) ** 2 / exp[big])
+    rest_o, rest_e = obs[~big].sum(), exp[~big].sum()
+    dof = int(big.sum()) - 1
+    if rest_e > 0:
+        chi += (rest_o - rest_e) ** 2 / rest_e
+        dof += 1
+    assert stats.chi2.sf(chi, dof) > 1e-4, (chi, dof)
+    assert (acc.cpu().numpy() == 1).mean() > 0.3      # the built children are accepted often
