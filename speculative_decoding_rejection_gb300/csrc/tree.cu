@@ -25,7 +25,11 @@
 // nodes it visits (the others never enter the decision): at each visited
 // node the cluster first reduces the node's target row (and, for a sampling
 // node with children, its draft row) to max / normaliser / argmax, each CTA
-// over its vocabulary slice, then tests the children. The residual laws are
+// over its vocabulary slice, then tests the children. When the slices fit,
+// each CTA copies its slice of the node's rows into shared memory with one
+// TMA bulk copy per row as it reaches the node (the target row at once, the
+// draft row once the node's children are known), and every pass over the
+// node (statistics, residuals, the final draw) reads shared memory. The residual laws are
 // never stored: every pass recomputes
 // p_j(y) from p(y) and q(y) through the chain of normalisers, which are
 // scalars. A token rejected at step k has q_k > p_k, so p_{k+1} is exactly 0
@@ -50,6 +54,9 @@ constexpr int WALK_CLUSTER = 8;
 constexpr int WALK_TILE = WALK_THREADS * SAMPLE_EPT;   // elements per tile of a walk pass
 constexpr int MAX_WALK_TILES = (SPEC_MAX_V + WALK_TILE - 1) / WALK_TILE;
 constexpr int MAX_SLICE_TILES = (MAX_WALK_TILES + WALK_CLUSTER - 1) / WALK_CLUSTER;
+// Largest staged slices (target + draft) per CTA: two walk CTAs per SM keep
+// room for their static shared memory.
+constexpr size_t WALK_STAGE_MAX = 96 * 1024;
 
 struct TreeInfo {
   int base;   // first node row
@@ -73,6 +80,8 @@ struct TreeArgs {
   WsHeader *hdr;
   TreeInfo *tree;
   long long t_row_bytes, d_row_bytes;
+  int staged;    // row slices are copied to shared memory
+  int dsm_off;   // byte offset of the draft slice in the dynamic shared memory
 };
 
 struct TreeLayout {
@@ -167,15 +176,81 @@ struct WalkSmem {
   RowStat wst[WALK_THREADS / 32][2];     // per-warp statistics of a node pass (target, draft)
   RowStat st[2][2];                      // this slice's statistics, by pass parity (target, draft)
   RowStat node[2];                       // the node's statistics (target, draft)
-  int nk, jstar, xmin, xlast, rstar, accepted_child, par, ok, go;
+  uint64_t bar_t, bar_d;                 // completion of the staged target / draft slice
+  int nk, jstar, xmin, xlast, rstar, accepted_child, par, ok, go, never;
   float carry, target, Z, pfix;
 };
 
 struct NodeLaw {        // p(y) = 2^((zt - mt) c) / St, q(y) likewise or given
   const char *trow, *drow;
+  const unsigned char *tsm, *dsm;   // this CTA's staged slices, or null
+  long long e0;                     // first element of the slice
   bool tvec, dvec;
   float mt, invSt, md, invSd;
 };
+
+// SAMPLE_EPT elements x0.. of a row (fill beyond V): from this CTA's staged
+// slice, starting at element e0, when `sm` is set, else from global memory.
+__device__ __forceinline__ void load_row_ept(const char *row, const unsigned char *sm,
+                                             long long e0, int dt, bool vec_ok, int x0, int V,
+                                             float fill, float *z) {
+  if (sm == nullptr) {
+    load_ept(row, dt, vec_ok, x0, V, fill, z);
+    return;
+  }
+  const int esz = dt == SPEC_BF16 ? 2 : 4;
+  const unsigned char *p = sm + ((long long)x0 - e0) * esz;
+  if (x0 + SAMPLE_EPT <= V) {
+    if (dt == SPEC_BF16) {
+#pragma unroll
+      for (int q = 0; q < SAMPLE_EPT / 8; ++q) {
+        const uint4 w = lds128(p + 16 * q);
+        z[8 * q + 0] = bf16lo(w.x); z[8 * q + 1] = bf16hi(w.x);
+        z[8 * q + 2] = bf16lo(w.y); z[8 * q + 3] = bf16hi(w.y);
+        z[8 * q + 4] = bf16lo(w.z); z[8 * q + 5] = bf16hi(w.z);
+        z[8 * q + 6] = bf16lo(w.w); z[8 * q + 7] = bf16hi(w.w);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < SAMPLE_EPT / 4; ++q) {
+        const uint4 w = lds128(p + 16 * q);
+        z[4 * q + 0] = __uint_as_float(w.x); z[4 * q + 1] = __uint_as_float(w.y);
+        z[4 * q + 2] = __uint_as_float(w.z); z[4 * q + 3] = __uint_as_float(w.w);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < SAMPLE_EPT; ++k) {
+      if (x0 + k >= V) {
+        z[k] = fill;
+      } else if (dt == SPEC_BF16) {
+        z[k] = __uint_as_float((uint32_t)reinterpret_cast<const unsigned short *>(p)[k] << 16);
+      } else {
+        z[k] = reinterpret_cast<const float *>(p)[k];
+      }
+    }
+  }
+}
+
+// Waits for a staged slice; on running out of time records SPEC_ERR_TIMEOUT
+// and waits once more (bounded) for the copy in flight before going on.
+__device__ __forceinline__ void wait_slice(const TreeArgs &a, WalkSmem &sh, uint64_t *bar,
+                                           uint32_t parity) {
+  if (!mbar_wait_bounded(bar, parity, &sh.never)) {
+    set_status(a.hdr, SPEC_ERR_TIMEOUT, -3);
+    mbar_wait_bounded(bar, parity, &sh.never);
+  }
+}
+
+// Thread 0 copies this CTA's slice [e0, e1) of `row` into `dst`, completion
+// on `bar`.
+__device__ __forceinline__ void stage_slice(uint64_t *bar, unsigned char *dst, const char *row,
+                                            int esz, long long e0, long long e1) {
+  const uint32_t bytes = (uint32_t)((e1 - e0) * esz);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive_tx(bar, bytes);
+  bulk_g2s(dst, row + e0 * esz, bytes, bar);
+}
 
 struct Slice { int j0, j1; };   // tiles [j0, j1) of this CTA
 
@@ -204,11 +279,12 @@ __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkS
                                                   bool residual, int j, float *w) {
   const int x0 = j * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
   float zt[SAMPLE_EPT], zd[SAMPLE_EPT];
-  load_ept(nl.trow, a.tdt, nl.tvec, x0, a.V, -INFINITY, zt);
+  load_row_ept(nl.trow, nl.tsm, nl.e0, a.tdt, nl.tvec, x0, a.V, -INFINITY, zt);
 #pragma unroll
   for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = ex2((zt[k] - nl.mt) * c) * nl.invSt;
   if (L == 0 && !residual) return;
-  load_ept(nl.drow, a.ddt, nl.dvec, x0, a.V, DK == SPEC_DRAFT_PROBS ? 0.f : -INFINITY, zd);
+  load_row_ept(nl.drow, nl.dsm, nl.e0, a.ddt, nl.dvec, x0, a.V,
+               DK == SPEC_DRAFT_PROBS ? 0.f : -INFINITY, zd);
   float q[SAMPLE_EPT];
 #pragma unroll
   for (int k = 0; k < SAMPLE_EPT; ++k)
@@ -392,20 +468,24 @@ __device__ __forceinline__ void stat_update(const float *z, int x0, float c, flo
 // in rank order, so every CTA gets the same bits. Only the rows of nodes the
 // walk visits are read.
 __device__ void node_stats(const TreeArgs &a, WalkSmem &sh, const char *trow, const char *drow,
-                           float c, const Slice sl, cg::cluster_group &cluster, RowStat &ts,
-                           RowStat &ds) {
+                           const unsigned char *tsm, const unsigned char *dsm, uint32_t pt,
+                           uint32_t pd, float c, const Slice sl, cg::cluster_group &cluster,
+                           RowStat &ts, RowStat &ds) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool tvec = ((uintptr_t)trow & 15) == 0, dvec = drow && ((uintptr_t)drow & 15) == 0;
+  const long long e0 = (long long)sl.j0 * WALK_TILE;
+  if (tsm != nullptr) wait_slice(a, sh, &sh.bar_t, pt);
+  if (drow && dsm != nullptr) wait_slice(a, sh, &sh.bar_d, pd);
   float m = NO_MAX, S = 0.f, md = NO_MAX, Sd = 0.f;
   int idx = 0x7fffffff, idd = 0x7fffffff;
   float z[SAMPLE_EPT];
 #pragma unroll 2
   for (int j = sl.j0; j < sl.j1; ++j) {
     const int x0 = j * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
-    load_ept(trow, a.tdt, tvec, x0, a.V, -INFINITY, z);
+    load_row_ept(trow, tsm, e0, a.tdt, tvec, x0, a.V, -INFINITY, z);
     stat_update(z, x0, c, m, S, idx);
     if (drow) {
-      load_ept(drow, a.ddt, dvec, x0, a.V, -INFINITY, z);
+      load_row_ept(drow, dsm, e0, a.ddt, dvec, x0, a.V, -INFINITY, z);
       stat_update(z, x0, c, md, Sd, idd);
     }
   }
@@ -463,7 +543,8 @@ __device__ __forceinline__ void write_final(const TreeArgs &a, int b, int depth,
 // leaves while another may still read its slice totals.
 template <int DK>
 __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const TreeInfo &t,
-                                          int b, int rank, cg::cluster_group &cluster) {
+                                          int b, int rank, cg::cluster_group &cluster,
+                                          unsigned char *tsm, unsigned char *dsm) {
   const int W = a.max_depth + 1;
   const Slice sl = my_slice(a.V, rank);
   int32_t *out = a.out_tokens + (long long)b * W;
@@ -471,15 +552,22 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
   const float c = t.c;
   int v = 0, depth = 0;
   const int esz_t = dtype_size(a.tdt), esz_d = dtype_size(a.ddt);
+  const long long se0 = (long long)sl.j0 * WALK_TILE;
+  const long long se1 = min((long long)sl.j1 * WALK_TILE, (long long)a.V);
+  const bool has_slice = sl.j1 > sl.j0;
+  if (!has_slice) tsm = dsm = nullptr;
+  uint32_t pt = 0, pd = 0;   // phases of the staged-slice barriers
   while (true) {
-    // this CTA's slice of node v's rows into L2 while the node is set up
-    if (threadIdx.x == 0 && sl.j1 > sl.j0) {
-      const long long e0 = (long long)sl.j0 * WALK_TILE;
-      const long long e1 = min((long long)sl.j1 * WALK_TILE, (long long)a.V);
+    // this CTA's slice of node v's target row into shared memory (or L2),
+    // and of its draft row into L2, while the node is set up
+    if (threadIdx.x == 0 && has_slice) {
       const long long rv = t.base + v;
-      prefetch_l2(a.target + rv * a.t_row_bytes + e0 * esz_t, (e1 - e0) * esz_t);
+      if (tsm != nullptr)
+        stage_slice(&sh.bar_t, tsm, a.target + rv * a.t_row_bytes, esz_t, se0, se1);
+      else
+        prefetch_l2(a.target + rv * a.t_row_bytes + se0 * esz_t, (se1 - se0) * esz_t);
       if (t.mode != MODE_GREEDY && a.draft != nullptr)
-        prefetch_l2(a.draft + rv * a.d_row_bytes + e0 * esz_d, (e1 - e0) * esz_d);
+        prefetch_l2(a.draft + rv * a.d_row_bytes + se0 * esz_d, (se1 - se0) * esz_d);
     }
     // children of v in node-index order (block-wide ordered compaction)
     {
@@ -516,9 +604,17 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     // sampling node has children to test
     const char *trow = a.target + (long long)row * a.t_row_bytes;
     const bool want_d = t.mode != MODE_GREEDY && nk > 0 && DK == SPEC_DRAFT_LOGITS;
+    // a sampling node with children tests them against its draft row: stage
+    // this CTA's slice of it too
+    const bool stage_d = dsm != nullptr && t.mode != MODE_GREEDY && nk > 0;
+    if (stage_d && threadIdx.x == 0)
+      stage_slice(&sh.bar_d, dsm, a.draft + (long long)row * a.d_row_bytes, esz_d, se0, se1);
     RowStat ts, dstat;
-    node_stats(a, sh, trow, want_d ? a.draft + (long long)row * a.d_row_bytes : nullptr, c, sl,
-               cluster, ts, dstat);
+    node_stats(a, sh, trow, want_d ? a.draft + (long long)row * a.d_row_bytes : nullptr, tsm,
+               want_d ? dsm : nullptr, pt, pd, c, sl, cluster, ts, dstat);
+    if (tsm != nullptr) pt ^= 1;
+    if (stage_d && !want_d) wait_slice(a, sh, &sh.bar_d, pd);   // draft probabilities
+    if (stage_d) pd ^= 1;
     if (t.mode == MODE_GREEDY) {
       if (threadIdx.x == 0) {
         sh.accepted_child = -1;
@@ -545,6 +641,9 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     }
     NodeLaw nl;
     nl.trow = trow;
+    nl.tsm = tsm;
+    nl.dsm = stage_d ? dsm : nullptr;
+    nl.e0 = se0;
     nl.tvec = ((uintptr_t)nl.trow & 15) == 0;
     nl.mt = ts.m;
     nl.invSt = 1.f / ts.S;
@@ -659,6 +758,7 @@ template <int DK>
 __global__ void __cluster_dims__(WALK_CLUSTER, 1, 1) __launch_bounds__(WALK_THREADS, 2)
     k_tree_walk(const TreeArgs a) {
   __shared__ WalkSmem sh;
+  extern __shared__ __align__(16) unsigned char rows_sm[];
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / WALK_CLUSTER;
@@ -675,6 +775,10 @@ __global__ void __cluster_dims__(WALK_CLUSTER, 1, 1) __launch_bounds__(WALK_THRE
   if (threadIdx.x == 0) {
     sh.ok = t.mode != MODE_SKIP && *(volatile int *)&a.hdr->status == SPEC_OK;
     sh.par = 0;
+    sh.never = 0;
+    mbar_init(&sh.bar_t, 1);
+    mbar_init(&sh.bar_d, 1);
+    fence_mbar_init();
   }
   cluster.sync();   // also orders the -1 fill before every later token write
   if (threadIdx.x == 0) {
@@ -684,7 +788,8 @@ __global__ void __cluster_dims__(WALK_CLUSTER, 1, 1) __launch_bounds__(WALK_THRE
   }
   __syncthreads();
   if (sh.go)
-    walk_tree<DK>(a, sh, t, b, rank, cluster);
+    walk_tree<DK>(a, sh, t, b, rank, cluster, a.staged ? rows_sm : nullptr,
+                  a.staged ? rows_sm + a.dsm_off : nullptr);
   else if (rank == 0 && threadIdx.x == 0)
     a.out_accepted[b] = -1;
   cluster.sync();
@@ -753,6 +858,16 @@ static int verify_tree(const void *target, int tdt, const void *draft, int ddt, 
   a.tree = reinterpret_cast<TreeInfo *>(ws + L.tree);
   a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
   a.d_row_bytes = (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
+  // stage the row slices in shared memory when they fit and every slice
+  // copy starts and ends on 16-byte boundaries
+  const long long slice_elems =
+      (long long)((V + WALK_TILE - 1) / WALK_TILE + WALK_CLUSTER - 1) / WALK_CLUSTER * WALK_TILE;
+  const size_t t_stage = ((size_t)slice_elems * (tdt == SPEC_BF16 ? 2 : 4) + 15) & ~(size_t)15;
+  const size_t d_stage = draft ? (size_t)slice_elems * (ddt == SPEC_BF16 ? 2 : 4) : 0;
+  a.staged = t_stage + d_stage <= WALK_STAGE_MAX && a.t_row_bytes % 16 == 0 &&
+             (draft == nullptr || a.d_row_bytes % 16 == 0);
+  a.dsm_off = (int)t_stage;
+  const size_t smem = a.staged ? t_stage + d_stage : 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
@@ -762,10 +877,19 @@ static int verify_tree(const void *target, int tdt, const void *draft, int ddt, 
   cudaEvent_t before, after;
   take_row_pass_events(&before, &after);
   if (before && cudaEventRecord(before, st) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (dk == SPEC_DRAFT_PROBS)
-    k_tree_walk<SPEC_DRAFT_PROBS><<<B * WALK_CLUSTER, WALK_THREADS, 0, st>>>(a);
-  else
-    k_tree_walk<SPEC_DRAFT_LOGITS><<<B * WALK_CLUSTER, WALK_THREADS, 0, st>>>(a);
+  if (dk == SPEC_DRAFT_PROBS) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(k_tree_walk<SPEC_DRAFT_PROBS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    k_tree_walk<SPEC_DRAFT_PROBS><<<B * WALK_CLUSTER, WALK_THREADS, smem, st>>>(a);
+  } else {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(k_tree_walk<SPEC_DRAFT_LOGITS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    k_tree_walk<SPEC_DRAFT_LOGITS><<<B * WALK_CLUSTER, WALK_THREADS, smem, st>>>(a);
+  }
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (after && cudaEventRecord(after, st) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
