@@ -71,6 +71,8 @@ struct TopkSmem {
   float S;
   float T;
   float zmax;            // largest survivor logit
+  float prev128;         // the 128th largest logit of this block's previous fast-path row
+  float delta;           // margin below it for the next row's predicted bound
   float red[8];          // epilogue: per-warp sums and scan totals
   float Zc, qm;
   int probe_lo, probe_hi;
@@ -156,12 +158,35 @@ __device__ __forceinline__ float value_of_key16(unsigned key) {
 // on logit rows — and the exact top 128 (ties to the lower id) is ranked
 // among them in shared memory. Returns false, having written no selection,
 // when the candidates overflow CAND_CAP.
-__device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
+//
+// With a predicted bound `pred` (finite: the block's previous row's 128th
+// largest logit minus a margin), the max pass also gathers the elements at or
+// above pred. When at least 128 are found, every element of the top 128 is
+// among them (the 128th largest is then >= pred), so the second pass is
+// skipped; otherwise (too few, or an overflow) the second pass runs as above.
+__device__ __forceinline__ void gather_candidates(const uint4 &w, int v, float bound,
+                                                  TopkSmem &sh) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t b = (k & 1) ? (ww[k >> 1] >> 16) : (ww[k >> 1] & 0xffffu);
+    if (__uint_as_float(b << 16) >= bound) {
+      const int slot = atomicAdd(&sh.cand_n, 1);
+      if (slot < CAND_CAP)
+        sh.cand[slot] = ((unsigned long long)key_of(b, true) << 32) | (~(unsigned)(8 * v + k));
+    }
+  }
+}
+
+__device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh, float pred) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const uint4 *vp = reinterpret_cast<const uint4 *>(row);
   const int nvec = V / 8;
   uint32_t pm = 0xff80ff80u;   // (-inf, -inf)
   constexpr uint32_t NINF2 = 0xff80ff80u;
+  const bool predicted = pred > -INFINITY;
+  if (t == 0) sh.cand_n = 0;
+  __syncthreads();
   // eight 16-byte loads in flight per thread before any is used
   for (int v0 = t; v0 < nvec; v0 += 8 * TK_THREADS) {
     uint4 w[8];
@@ -171,7 +196,12 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
       w[u] = v < nvec ? __ldg(vp + v) : make_uint4(NINF2, NINF2, NINF2, NINF2);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) pm = bmax2(pm, bmax2(bmax2(w[u].x, w[u].y), bmax2(w[u].z, w[u].w)));
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t m8 = bmax2(bmax2(w[u].x, w[u].y), bmax2(w[u].z, w[u].w));
+      pm = bmax2(pm, m8);
+      if (predicted && v0 + u * TK_THREADS < nvec && fmaxf(bf16lo(m8), bf16hi(m8)) >= pred)
+        gather_candidates(w[u], v0 + u * TK_THREADS, pred, sh);
+    }
   }
   float m = fmaxf(bf16lo(pm), bf16hi(pm));
   // descending bitonic sort of the warp's 32 maxima
@@ -183,13 +213,17 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
       m = (((lane & k) == 0) == ((lane & j) == 0)) ? fmaxf(m, o) : fminf(m, o);
     }
   if (lane == SPEC_TOPK / TK_WARPS - 1) sh.tmax[warp] = m;
-  if (t == 0) sh.cand_n = 0;
+  __syncthreads();
+  const int n1 = sh.cand_n;
+  const bool held = predicted && n1 >= SPEC_TOPK && n1 <= CAND_CAP;
+  __syncthreads();   // every thread has read the count before it is reset
+  if (!held && t == 0) sh.cand_n = 0;
   __syncthreads();
   float bound = sh.tmax[0];
   for (int w = 1; w < TK_WARPS; ++w) bound = fminf(bound, sh.tmax[w]);
   // the second pass (from L2), eight loads in flight again; a group of 8
   // logits is looked at only when its packed maximum reaches the bound
-  for (int v0 = t; v0 < nvec; v0 += 8 * TK_THREADS) {
+  for (int v0 = t; v0 < nvec && !held; v0 += 8 * TK_THREADS) {
     uint4 wv[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -202,16 +236,7 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
       const uint4 w = wv[u];
       const uint32_t m8 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
       if (v >= nvec || fmaxf(bf16lo(m8), bf16hi(m8)) < bound) continue;
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t b = (k & 1) ? (ww[k >> 1] >> 16) : (ww[k >> 1] & 0xffffu);
-        if (__uint_as_float(b << 16) >= bound) {
-          const int slot = atomicAdd(&sh.cand_n, 1);
-          if (slot < CAND_CAP)
-            sh.cand[slot] = ((unsigned long long)key_of(b, true) << 32) | (~(unsigned)(8 * v + k));
-        }
-      }
+      gather_candidates(w, v, bound, sh);
     }
   }
   __syncthreads();
@@ -227,6 +252,13 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh) {
     }
   }
   __syncthreads();
+  // the next row's prediction: this row's 128th largest logit, and a margin
+  // that widens after a miss and narrows when the candidates were many
+  if (t == 0) {
+    sh.prev128 = sh.sel_val[SPEC_TOPK - 1];
+    if (predicted && !held) sh.delta = fminf(sh.delta * 2.f, 64.f);
+    else if (held && n1 > 4 * SPEC_TOPK) sh.delta = fmaxf(sh.delta * 0.5f, 1.f / 64.f);
+  }
   return true;
 }
 
@@ -362,7 +394,7 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
     }
     __syncthreads();
   } else if (BF16 && V % 8 == 0 && V >= 8 * TK_THREADS && ((uintptr_t)row & 15) == 0 &&
-             select_bf16_fast(row, V, sh)) {
+             select_bf16_fast(row, V, sh, sh.prev128 - sh.delta)) {
     // selected by the fast path
   } else {
     // pass 1: the maximum key
@@ -540,6 +572,11 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
 __global__ void __launch_bounds__(TK_THREADS, 2) k_topk128(const TopkArgs a) {
   __shared__ TopkSmem sh;
   if (a.hdr->status != SPEC_OK) return;   // inputs already rejected
+  if (threadIdx.x == 0) {
+    sh.prev128 = -INFINITY;   // no prediction for the first row
+    sh.delta = 0.5f;
+  }
+  __syncthreads();
   const int rows = min(a.rows_bound, a.cu[a.B]);
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     if (a.dtype == SPEC_BF16) topk_row<true>(a, sh, r);

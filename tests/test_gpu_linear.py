@@ -236,6 +236,33 @@ def test_draft_topk_softmax_row_orders():
     assert_probs_close(prob.cpu().numpy(), rp, "top-128 probabilities")
 
 
+def test_draft_topk_softmax_predicted_bound_misses():
+    """Each block predicts a row's bound from its previous row. Rows whose
+    scale and offset change from row to row make that prediction too high
+    (too few candidates), too low (an overflow) or right, so all three
+    outcomes and the second pass they fall back to are compared with the
+    oracle. 1400 rows put several rows on every block."""
+    g = torch.Generator(device=DEV).manual_seed(23)
+    R, V = 1400, 4096
+    base = (2.0 * torch.randn(R, V, generator=g, device=DEV)
+            - 1.1 * torch.log(torch.rand(R, V, generator=g, device=DEV) * V + 1))
+    scale = torch.tensor([1.0, 8.0, 0.05, 1.0, 3.0, 0.5, 20.0], device=DEV)
+    shift = torch.tensor([0.0, -30.0, 20.0, 5.0, -2.0, 60.0, 0.0], device=DEV)
+    k = torch.arange(R, device=DEV) % 7
+    z = base * scale[k, None] + shift[k, None]
+    z[5::11] = torch.round(z[5::11])                  # ties at the 128th logit
+    z = z.to(torch.bfloat16).contiguous()
+    cu = torch.tensor([0, R], dtype=torch.int32, device=DEV)
+    temp = torch.tensor([0.8], device=DEV)
+    idx, prob, ws = sv.draft_topk_softmax(z, cu, temp)
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    rows = np.r_[0:40, 300:340, 600:640, 1300:1400]
+    cu_s = np.array([0, rows.size], dtype=np.int32)
+    ri, rp = O.draft_topk_softmax(z[rows].cpu(), cu_s, temp.cpu().numpy())
+    assert np.array_equal(idx[rows].cpu().numpy(), ri)
+    assert_probs_close(prob[rows].cpu().numpy(), rp, "top-128 probabilities")
+
+
 # ------------------------------------------- relaxed CACTUS rule and ranks
 CACTUS_CASES = [
     dict(alpha=0.0, max_rank=0, min_prob=0.0),     # the lossless test
