@@ -30,6 +30,7 @@
 namespace sv {
 
 constexpr int TK_THREADS = 512;
+constexpr int TK_CTAS_PER_SM = 2;
 constexpr int TK_EPT = 16;
 constexpr int TK_TILE = TK_THREADS * TK_EPT;
 
@@ -77,8 +78,9 @@ struct TopkSmem {
   float Zc, qm;
   int probe_lo, probe_hi;
 };
-static_assert(TK_THREADS == 4 * SPEC_TOPK, "the epilogue counts with four threads per survivor");
-static_assert(CAND_CAP * 2 >= 5 * SPEC_TOPK, "the epilogue's counters fit in the candidate area");
+constexpr int TK_PARTS = TK_THREADS / SPEC_TOPK;   // epilogue threads per survivor
+static_assert(TK_PARTS * SPEC_TOPK == TK_THREADS && TK_PARTS >= 1, "whole parts per survivor");
+static_assert(CAND_CAP * 2 >= (TK_PARTS + 1) * SPEC_TOPK, "the epilogue's counters fit");
 
 __device__ __forceinline__ unsigned key_of(uint32_t bits, bool bf16) {
   if (bf16) {
@@ -271,16 +273,17 @@ __device__ void rheo_epilogue(const TopkArgs &a, TopkSmem &sh, int r, int ksel) 
   const RheoEpi &h = a.rh;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   int *cnt = reinterpret_cast<int *>(sh.cand);   // free once the select is done
-  int *rank_of = cnt + 4 * SPEC_TOPK;
+  int *rank_of = cnt + TK_PARTS * SPEC_TOPK;
   {
     // rank best first (logit descending, ties and -inf to the lower id,
-    // padding last): four threads per survivor count 32 entries each
+    // padding last): TK_PARTS threads per survivor count a share each
+    constexpr int SHARE = SPEC_TOPK / TK_PARTS;
     const int e = t & (SPEC_TOPK - 1), part = t / SPEC_TOPK;
     const float ze = e < ksel ? sh.sel_val[e] : -INFINITY;
     const int ke = e < ksel ? sh.sel_idx[e] : INT_MAX;
     int c = 0;
 #pragma unroll 8
-    for (int j = part * 32; j < part * 32 + 32; ++j) {
+    for (int j = part * SHARE; j < part * SHARE + SHARE; ++j) {
       const float zj = j < ksel ? sh.sel_val[j] : -INFINITY;
       const int kj = j < ksel ? sh.sel_idx[j] : INT_MAX;
       c += (zj > ze || (zj == ze && kj < ke)) ? 1 : 0;
@@ -299,7 +302,9 @@ __device__ void rheo_epilogue(const TopkArgs &a, TopkSmem &sh, int r, int ksel) 
   int rk = SPEC_TOPK;
   float eu = 0.f, qt = 0.f, C = 0.f;
   if (surv) {
-    rk = cnt[t] + cnt[SPEC_TOPK + t] + cnt[2 * SPEC_TOPK + t] + cnt[3 * SPEC_TOPK + t];
+    rk = 0;
+#pragma unroll
+    for (int q = 0; q < TK_PARTS; ++q) rk += cnt[q * SPEC_TOPK + t];
     rank_of[t] = rk;
     eu = valid && sh.sel_val[t] > -INFINITY ? expf(sh.sel_val[t] - sh.zmax) : 0.f;
     qt = valid ? sh.sel_e[t] / sh.S : 0.f;
@@ -569,7 +574,7 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(TK_THREADS, 2) k_topk128(const TopkArgs a) {
+__global__ void __launch_bounds__(TK_THREADS, TK_CTAS_PER_SM) k_topk128(const TopkArgs a) {
   __shared__ TopkSmem sh;
   if (a.hdr->status != SPEC_OK) return;   // inputs already rejected
   if (threadIdx.x == 0) {
@@ -620,7 +625,7 @@ int launch_topk128(const void *logits, int dtype, int rows_bound, int V, const i
   if (rows_bound <= 0) return SPEC_OK;
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
-  const int grid = min(rows_bound, 2 * sms);   // two 512-thread CTAs per SM
+  const int grid = min(rows_bound, TK_CTAS_PER_SM * sms);
   k_topk128<<<grid, TK_THREADS, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
