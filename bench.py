@@ -83,6 +83,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--V", type=int, default=None,
+                    help="linear workloads: override the vocabulary size (size sweeps)")
     ap.add_argument("--B", type=int, default=None,
                     help="override the number of requests (small profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=6)
@@ -99,6 +101,9 @@ def parse():
     ap.add_argument("--rheo", action="store_true",
                     help="time one level of RheoSampling tree construction (spec_rheo_expand) "
                          "on its own workload instead of a verify workload")
+    ap.add_argument("--fused-limit", type=int, default=None,
+                    help="linear workloads: largest call (bytes of rows) the fused small-batch "
+                         "kernel takes; 0 forces the multi-kernel schedule")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
 
@@ -223,12 +228,15 @@ class LinearWork:
     # relaxed rule options: the guard the page recommends (p >= 0.10, top 10)
     CACTUS = {"alpha": 0.5, "max_rank": 10, "min_prob": 0.10}
 
-    def __init__(self, cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False):
+    def __init__(self, cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False,
+                 V=None):
         import torch
         import speculative_decoding_rejection_gb300 as sv
         from speculative_decoding_rejection_gb300 import synthetic as S
         self.sv = sv
         over = {} if B is None else {"B": B}
+        if V is not None:
+            over["V"] = V
         self.lb = lb = S.make_linear(cfg, device=dev, input_seed=input_seed, **over)
         self.rule = sv.SPEC_RULE_STRICT_TOP128 if lb.top128 else sv.SPEC_RULE_STRICT
         self.ext = None
@@ -489,12 +497,13 @@ class RheoWork:
         return hi - lo
 
 
-def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False, rheo=False):
+def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False, rheo=False,
+              V=None):
     if rheo:
         return RheoWork(dev, input_seed, B)
     if cfg == 4:
         return TreeWork(cfg, dev, input_seed, B)
-    return LinearWork(cfg, dev, input_seed, B, rule, lazy, kl)
+    return LinearWork(cfg, dev, input_seed, B, rule, lazy, kl, V)
 
 
 def cpu_baseline(work, n_units):
@@ -555,8 +564,10 @@ def main():
     world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     sv.lib()
+    if args.fused_limit is not None:
+        sv.spec_set_fused_limit(args.fused_limit)
     seed_base = S.INPUT_SEED_BASE + (0x100 if args.rheo else args.config)
-    work = make_work(args.config, dev, input_seed=seed_base + 7919 * rank, B=args.B,
+    work = make_work(args.config, dev, input_seed=seed_base + 7919 * rank, B=args.B, V=args.V,
                      rule=args.rule, lazy=args.lazy, kl=args.kl, rheo=args.rheo)
     unit = getattr(work, "unit", UNIT)
 
@@ -617,17 +628,17 @@ def main():
              and getattr(work, "kernel", None) is None)
     if ROWPASS_TRAFFIC["source_sha1"] == source_sha1("rowpass") and plain:
         traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if (getattr(work, "kernel", None) == "k_topk128" and args.B is None and args.rheo
+    if (getattr(work, "kernel", None) == "k_topk128" and args.B is None and args.V is None and args.rheo
             and RHEO_TRAFFIC["source_sha1"] == source_sha1("topk")):
         traffic = RHEO_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if (getattr(work, "kernel", None) == "k_topk128" and args.B is None and args.config == 3
+    if (getattr(work, "kernel", None) == "k_topk128" and args.B is None and args.V is None and args.config == 3
             and not args.rheo
             and TOPK_TRAFFIC["source_sha1"] == source_sha1("topk")):
         traffic = TOPK_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if (getattr(work, "kernel", None) == "k_tree_walk" and args.B is None and args.config == 4
+    if (getattr(work, "kernel", None) == "k_tree_walk" and args.B is None and args.V is None and args.config == 4
             and TREE_TRAFFIC["source_sha1"] == source_sha1("tree")):
         traffic = TREE_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if (stream and getattr(work, "ext", None) is None and args.B is None and args.config == 5
+    if (stream and getattr(work, "ext", None) is None and args.B is None and args.V is None and args.config == 5
             and STREAM_TRAFFIC["source_sha1"] == source_sha1("stream")):
         traffic = STREAM_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
 

@@ -152,6 +152,20 @@ int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
                        size_t ws_bytes, spec_stream_t stream);
 
 /*
+ * Tuning of the linear verifier's schedule. A call with rule
+ * SPEC_RULE_STRICT or SPEC_RULE_GREEDY, draft logits or probabilities and
+ * no options runs as one fused kernel, one block per request, when V is at
+ * most 8192, a request's rows ((max_k + 1) target rows and max_k draft rows)
+ * total at most 1 MiB and all B requests' rows at most `bytes`. Such calls
+ * are decode steps over short rows, where one launch costs less than the
+ * multi-kernel schedule. Same results either way, up to the rounding of the row sums.
+ * `bytes` = 0 turns the fused kernel off; the default is 32 MiB. A
+ * process-wide setting, read when a call is made. Returns the previous
+ * value.
+ */
+size_t spec_set_fused_limit(size_t bytes);
+
+/*
  * Options of spec_verify_linear_ext (host memory, read during the call).
  *   alpha     SPEC_RULE_CACTUS divergence budget, finite and >= 0; 0 makes
  *             gamma = p, the lossless test.

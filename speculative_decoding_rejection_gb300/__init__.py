@@ -20,7 +20,8 @@ __all__ = [
     "spec_verify_linear", "spec_verify_linear_ext", "spec_verify_linear_workspace", "spec_verify_tree",
     "spec_verify_tree_workspace", "spec_verify_tree_ext", "draft_topk_softmax",
     "draft_topk_softmax_workspace", "spec_get_status", "spec_uniforms",
-    "spec_profile_row_pass", "spec_rheo_expand", "spec_rheo_expand_workspace", "SpecError",
+    "spec_profile_row_pass", "spec_rheo_expand", "spec_rheo_expand_workspace",
+    "spec_set_fused_limit", "SpecError",
 ]
 
 SPEC_OK = 0
@@ -69,6 +70,7 @@ _SIGS = {
                                 ctypes.c_float, _i32, _u64, _i32, _vp, _vp, _vp, _vp, _vp,
                                 _vp, _sz, _vp]),
     "spec_get_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+    "spec_set_fused_limit": (_sz, [_sz]),
     "spec_uniforms": (_i32, [_u64, _vp, _vp, _vp, _i32, _vp, _vp]),
     "spec_profile_row_pass": (_i32, [_vp, _vp]),
     "spec_wait_selftest": (_i32, [_i32, ctypes.c_ulonglong, _vp, _vp]),
@@ -334,6 +336,12 @@ def spec_rheo_expand(draft, cu_frontier, frontier_score, temperature, seed: int,
         _stream(stream))
     _check(code, "spec_rheo_expand")
     return token, qproxy, qtrue, score, keep, ws
+
+
+def spec_set_fused_limit(nbytes: int) -> int:
+    """Sets the largest call (bytes of rows) the fused small-batch kernel
+    takes (0: never); returns the previous limit."""
+    return int(lib().spec_set_fused_limit(ctypes.c_size_t(nbytes)))
 
 
 def spec_get_status(workspace, stream=None) -> int:

@@ -271,6 +271,11 @@ static __device__ void finish_request(const LinearArgs &a, int b, const ReqInfo 
 bool stream_supported(const LinearArgs &a);
 int launch_verify_stream(const LinearArgs &a, cudaStream_t stream);
 
+// The fused small-batch verifier (one kernel, one block per request) and the
+// calls it takes.
+bool small_supported(const LinearArgs &a, const spec_linear_ext *ext);
+int launch_verify_small(const LinearArgs &a, cudaStream_t stream);
+
 // Rows and laws of a final draw.
 struct JobRows {
   const char *trow, *drow;

@@ -11,6 +11,16 @@ from parity import (assert_linear_parity, assert_probs_close, gpu_linear, oracle
                     probs_from_logits, sample_requests)
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["fused", "multi"])
+def schedule(request):
+    """Runs a test under both schedules of the linear verifier: the fused
+    small-batch kernel (taken by calls under its size limit) and the
+    multi-kernel path (limit 0)."""
+    old = sv.spec_set_fused_limit((32 << 20) if request.param == "fused" else 0)
+    yield request.param
+    sv.spec_set_fused_limit(old)
 DEV = "cuda:0"
 
 
@@ -32,6 +42,7 @@ def test_device_uniforms_equal_the_oracle_hash():
     assert np.array_equal(got.astype(np.float64), want)
 
 
+@pytest.mark.usefixtures("schedule")
 def test_workload1_full():
     lb = S.make_linear(1, device=DEV)
     g = gpu_linear(lb)
@@ -40,6 +51,7 @@ def test_workload1_full():
     assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=3)
 
 
+@pytest.mark.usefixtures("schedule")
 def test_workload2_full_mixed_greedy_and_sampling():
     lb = S.make_linear(2, device=DEV)
     g = gpu_linear(lb)
@@ -61,6 +73,7 @@ def test_workload2_full_mixed_greedy_and_sampling():
 
 @pytest.mark.parametrize("dtype,V", [("bf16", 5003), ("f32", 4099), ("bf16", 100003),
                                      ("f32", 50001), ("bf16", 7)])
+@pytest.mark.usefixtures("schedule")
 def test_ragged_batches_unaligned_rows_and_multiple_chunks(dtype, V):
     T = [0.0, 0.04, 0.05, 0.3, 0.7, 1.0, 1.6, 2.5] * 5
     lb = S.make_linear(2, device=DEV, B=40, K=(0, 7), V=V, dtype=dtype, sigma=0.8, T=T,
@@ -72,6 +85,7 @@ def test_ragged_batches_unaligned_rows_and_multiple_chunks(dtype, V):
     assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=30)
 
 
+@pytest.mark.usefixtures("schedule")
 def test_mixed_target_and_draft_dtypes():
     lb = S.make_linear(1, device=DEV, B=12, K=5, V=3001, dtype="bf16", input_seed=77)
     draft32 = lb.draft.float().contiguous()
@@ -80,8 +94,10 @@ def test_mixed_target_and_draft_dtypes():
     assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=10)
 
 
-def test_draft_given_as_probabilities():
-    lb = S.make_linear(2, device=DEV, B=24, K=(1, 6), V=20000, input_seed=5,
+@pytest.mark.parametrize("V", [20000, 6000])
+@pytest.mark.usefixtures("schedule")
+def test_draft_given_as_probabilities(V):
+    lb = S.make_linear(2, device=DEV, B=24, K=(1, 6), V=V, input_seed=5,
                        T=[0.0, 0.8, 1.2] * 8)
     probs = probs_from_logits(lb.draft, lb.cu_draft, lb.temperature)
     g = gpu_linear(lb, draft_kind=sv.SPEC_DRAFT_PROBS, draft=probs)
@@ -115,6 +131,7 @@ def test_top128_rule_reduced_workload3():
     assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=20)
 
 
+@pytest.mark.usefixtures("schedule")
 def test_greedy_rule_forces_prefix_matching():
     lb = S.make_linear(1, device=DEV, B=16, K=6, V=2048, input_seed=4)
     g = gpu_linear(lb, rule=sv.SPEC_RULE_GREEDY)
@@ -123,6 +140,7 @@ def test_greedy_rule_forces_prefix_matching():
     assert np.all(g["pq"][:, 1] == -1.0)
 
 
+@pytest.mark.usefixtures("schedule")
 def test_vocabulary_of_one_token():
     lb = S.make_linear(1, device=DEV, B=3, K=2, V=1, input_seed=2)
     lb.draft_tokens.zero_()
@@ -130,12 +148,14 @@ def test_vocabulary_of_one_token():
     assert np.all(g["accepted"] == 2) and np.all(g["tokens"][:, :3] == 0)
 
 
+@pytest.mark.usefixtures("schedule")
 def test_repeat_calls_are_bitwise_deterministic():
     lb = S.make_linear(2, device=DEV, B=32, V=12000, input_seed=8)
     a, b = gpu_linear(lb), gpu_linear(lb)
     assert np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["pq"], b["pq"])
 
 
+@pytest.mark.usefixtures("schedule")
 def test_invalid_device_inputs_set_the_status_word():
     lb = S.make_linear(1, device=DEV, B=4, K=3, V=512, input_seed=3)
     bad_cu = lb.cu_draft.clone()
