@@ -202,6 +202,11 @@ size_t spec_set_fused_limit(size_t bytes);
  *             whose byte length is a multiple of 16, and a rule other than
  *             SPEC_RULE_STRICT_TOP128 (whose truncated q makes it +inf).
  *             NULL to skip.
+ *   seed_dev  optional device uint64, 8-byte aligned: when set, the kernels
+ *             read the seed from it as they run and the `seed` argument is
+ *             ignored. A call captured in a CUDA graph then draws new
+ *             uniforms on every replay after the caller writes a new seed
+ *             there. NULL to use `seed`.
  * The guard and the relaxed coin apply to sampling requests; greedy
  * requests (T < 0.05) keep the greedy rule.
  */
@@ -213,6 +218,7 @@ typedef struct {
   int32_t flags;
   int32_t *out_rank;
   float *out_kl;
+  const uint64_t *seed_dev;
 } spec_linear_ext;
 
 /*
@@ -316,13 +322,17 @@ int spec_verify_tree(const void *target, int tdt, const void *draft, int ddt,
  * after it: for a RheoSampling node list the probe (slot m of
  * spec_rheo_expand) first, then the other slots in order. Drawn siblings
  * carry distinct tokens; a fixed child may repeat a sibling's token.
+ *   seed_dev    optional device uint64, 8-byte aligned: when set, the walk
+ *               reads the seed from it as it runs and `seed` is ignored (for
+ *               calls replayed from a CUDA graph). NULL to use `seed`.
  */
 int spec_verify_tree_ext(const void *target, int tdt, const void *draft,
                          int ddt, int dk, const int32_t *node_token,
                          const int32_t *parent, const int32_t *node_fixed,
                          const int32_t *cu_nodes, const float *temperature,
                          int B, int n_nodes, int V, int max_depth,
-                         int max_branch, uint64_t seed, int32_t *out_tokens,
+                         int max_branch, uint64_t seed,
+                         const uint64_t *seed_dev, int32_t *out_tokens,
                          int32_t *out_accepted, int32_t *out_path,
                          void *workspace, size_t ws_bytes,
                          spec_stream_t stream);

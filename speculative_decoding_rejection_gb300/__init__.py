@@ -46,7 +46,8 @@ class SpecLinearExt(ctypes.Structure):
     """spec_linear_ext of include/specverify.h."""
     _fields_ = [("alpha", ctypes.c_float), ("max_rank", ctypes.c_int32),
                 ("min_prob", ctypes.c_float), ("flags", ctypes.c_int32),
-                ("out_rank", ctypes.c_void_p), ("out_kl", ctypes.c_void_p)]
+                ("out_rank", ctypes.c_void_p), ("out_kl", ctypes.c_void_p),
+                ("seed_dev", ctypes.c_void_p)]
 
 
 _SIGS = {
@@ -61,7 +62,8 @@ _SIGS = {
     "spec_verify_tree": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32,
                                 _i32, _i32, _i32, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_verify_tree_ext": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32,
-                                    _i32, _i32, _i32, _i32, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
+                                    _i32, _i32, _i32, _i32, _u64, _vp, _vp, _vp, _vp, _vp, _sz,
+                                    _vp]),
     "draft_topk_softmax_workspace": (_sz, [_i32, _i32]),
     "draft_topk_softmax": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp,
                                   _sz, _vp]),
@@ -198,7 +200,7 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
                            max_k: int, rule: int = SPEC_RULE_STRICT,
                            draft_kind: int = SPEC_DRAFT_LOGITS, draft_idx=None, alpha=0.0,
                            max_rank=0, min_prob=0.0, lazy=False, want_pq=False,
-                           want_rank=False, want_kl=False, workspace=None, out=None,
+                           want_rank=False, want_kl=False, seed_dev=None, workspace=None, out=None,
                            stream=None):
     """spec_verify_linear with the relaxed CACTUS rule's options and target
     ranks.
@@ -223,7 +225,7 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
     else:
         tokens, accepted, pq, rank, kl = out
     ext = SpecLinearExt(float(alpha), int(max_rank), float(min_prob),
-                        SPEC_EXT_LAZY if lazy else 0, _ptr(rank), _ptr(kl))
+                        SPEC_EXT_LAZY if lazy else 0, _ptr(rank), _ptr(kl), _ptr(seed_dev))
     ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
     code = lib().spec_verify_linear_ext(
         _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(draft_idx),
@@ -240,9 +242,10 @@ def spec_verify_tree_workspace(B: int, n_nodes: int, V: int, max_depth: int, max
 
 def spec_verify_tree(target, draft, node_token, parent, cu_nodes, temperature, seed: int, *,
                      max_depth: int, max_branch: int, draft_kind: int = SPEC_DRAFT_LOGITS,
-                     node_fixed=None, workspace=None, out=None, stream=None):
+                     node_fixed=None, seed_dev=None, workspace=None, out=None, stream=None):
     """Verifies a batch of draft trees (RRSw) on the GPU. With `node_fixed`
-    ([n_nodes] int32, nonzero = a point-mass child) the call goes through
+    ([n_nodes] int32, nonzero = a point-mass child) or `seed_dev` (a device
+    uint64 tensor read as the seed when the walk runs) the call goes through
     spec_verify_tree_ext.
 
     Returns (tokens [B, max_depth+1], accepted [B], path [B, max_depth+1],
@@ -265,14 +268,15 @@ def spec_verify_tree(target, draft, node_token, parent, cu_nodes, temperature, s
     ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
     head = (_ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(node_token),
             _ptr(parent))
-    tail = (_ptr(cu_nodes), _ptr(temperature), B, n_nodes, V, max_depth, max_branch,
-            ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), _ptr(tokens), _ptr(accepted), _ptr(path),
-            _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
-    if node_fixed is None:
-        code = lib().spec_verify_tree(*head, *tail)
+    mid = (_ptr(cu_nodes), _ptr(temperature), B, n_nodes, V, max_depth, max_branch,
+           ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF))
+    tail = (_ptr(tokens), _ptr(accepted), _ptr(path), _ptr(ws), ctypes.c_size_t(ws.numel()),
+            _stream(stream))
+    if node_fixed is None and seed_dev is None:
+        code = lib().spec_verify_tree(*head, *mid, *tail)
         _check(code, "spec_verify_tree")
     else:
-        code = lib().spec_verify_tree_ext(*head, _ptr(node_fixed), *tail)
+        code = lib().spec_verify_tree_ext(*head, _ptr(node_fixed), *mid, _ptr(seed_dev), *tail)
         _check(code, "spec_verify_tree_ext")
     return tokens, accepted, path, ws
 

@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArg
   const bool dense = g < na;
   const Job job = dense ? a.jobs_a[g] : a.jobs_b[g - na];
   const JobRows q = job_rows(a, job);
-  const float u = uniform24(a.seed, (uint32_t)job.b, (uint32_t)(job.n + 1), job.kind == 1 ? 1u : 2u);
+  const float u = uniform24(seed_of(a), (uint32_t)job.b, (uint32_t)(job.n + 1), job.kind == 1 ? 1u : 2u);
   int x = -1;
   bool done = false;
   if (dense) {
@@ -718,7 +718,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
       (!(ext->alpha >= 0.f) || !isfinite(ext->alpha) || ext->max_rank < 0 ||
        !(ext->min_prob >= 0.f) || !isfinite(ext->min_prob) ||
        (ext->flags & ~SPEC_EXT_LAZY) != 0 || !aligned(ext->out_kl, 4) ||
-       !aligned(ext->out_rank, 4)))
+       !aligned(ext->out_rank, 4) || !aligned(ext->seed_dev, 8)))
     return SPEC_ERR_INVALID_ARG;
   if (dk == SPEC_DRAFT_SPARSE128 && (ddt != SPEC_F32 || draft_idx == nullptr || draft == nullptr))
     return SPEC_ERR_INVALID_ARG;
@@ -748,6 +748,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.V = V;
   a.max_k = max_k;
   a.seed = seed;
+  a.seed_dev = ext ? ext->seed_dev : nullptr;
   a.out_tokens = out_tokens;
   a.out_accepted = out_accepted;
   a.out_pq = out_pq;

@@ -23,6 +23,7 @@ struct LinearArgs {
   const float *temp;
   int B, V, max_k;
   uint64_t seed;
+  const uint64_t *seed_dev;   // optional: the seed read on the device at run time
   int32_t *out_tokens;
   int32_t *out_accepted;
   float *out_pq;
@@ -72,6 +73,12 @@ struct LinearArgs {
 // c = log2(e)/T). Returns false, with the status word set, on an invalid
 // request: a bad offset, a draft count outside [0, max_k], a negative or
 // non-finite temperature, or a sampling request without a draft tensor.
+// The call's seed: from device memory when the caller gave a pointer (so a
+// captured CUDA graph draws new uniforms after the caller writes a new seed).
+__device__ __forceinline__ uint64_t seed_of(const LinearArgs &a) {
+  return a.seed_dev != nullptr ? __ldg(a.seed_dev) : a.seed;
+}
+
 __device__ __forceinline__ bool load_request(const LinearArgs &a, int b, ReqInfo &r) {
   const int K = a.cu[b + 1] - a.cu[b];
   const float T = a.temp[b];
@@ -204,10 +211,10 @@ static __device__ bool position_rejects_z(const LinearArgs &a, int b, const ReqI
       const float g = fminf(pd + sqrtf(2.f * a.alpha * pd * (1.f - pd)), 1.f);
       const float acc = qd <= g ? 1.f : g / qd;
       const bool guard = (a.max_rank > 0 && rank > a.max_rank) || pd < a.min_prob;
-      rej = guard || !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
+      rej = guard || !(uniform24(seed_of(a), (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
     } else {
       const float acc = qd <= pd ? 1.f : pd / qd;
-      rej = !(uniform24(a.seed, (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
+      rej = !(uniform24(seed_of(a), (uint32_t)b, (uint32_t)(i + 1), 0) < acc);
     }
   } else {
     pd = 0.f;

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(SMALL_THREADS) k_verify_small(const LinearArgs
     x = sh.ts[n].idx;
   } else {
     const char *trow = a.target + (long long)(r.t0 + n) * a.t_row_bytes;
-    const float u = uniform24(a.seed, (uint32_t)b, (uint32_t)(n + 1), n < K ? 1u : 2u);
+    const float u = uniform24(seed_of(a), (uint32_t)b, (uint32_t)(n + 1), n < K ? 1u : 2u);
     x = -1;
     if (n < K) {   // residual of the rejected position
       const RowStat dn = dense_draft ? sh.ds[n] : RowStat{NO_MAX, 0.f, 0x7fffffff};

@@ -76,6 +76,7 @@ struct TreeArgs {
   const float *temp;
   int B, n_nodes, V, max_depth, max_branch;
   uint64_t seed;
+  const uint64_t *seed_dev;   // optional: the seed read on the device at run time
   int32_t *out_tokens, *out_accepted, *out_path;
   WsHeader *hdr;
   TreeInfo *tree;
@@ -83,6 +84,11 @@ struct TreeArgs {
   int staged;    // row slices are copied to shared memory
   int dsm_off;   // byte offset of the draft slice in the dynamic shared memory
 };
+
+// The call's seed: from device memory when the caller gave a pointer.
+__device__ __forceinline__ uint64_t tree_seed(const TreeArgs &a) {
+  return a.seed_dev != nullptr ? __ldg(a.seed_dev) : a.seed;
+}
 
 struct TreeLayout {
   size_t hdr, tree, total;
@@ -654,7 +660,7 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     if (nk == 0) {  // accepted leaf (or a bare root): bonus draw from p_v
       weight_pass<DK>(a, sh, nl, c, 0, false, sl, cluster);
       const int x = weight_draw<DK>(a, sh, nl, c, 0, false,
-                                    uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 2), sl,
+                                    uniform24(tree_seed(a), (uint32_t)b, (uint32_t)(v + 1), 2), sl,
                                     rank);
       if (x != -1 && threadIdx.x == 0) write_final(a, b, depth, x);
       if (rank == 0 && threadIdx.x == 0) a.out_accepted[b] = depth;
@@ -686,7 +692,7 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
         const float pj = chain_weight(p, qx, sh.kx[j], j, false, sh);
         const float qj = sh.kfix[j] ? 1.f : qx * sh.s[j];
         const float acc = qj <= pj ? 1.f : pj / qj;
-        const bool ok = uniform24(a.seed, (uint32_t)b, (uint32_t)ch, 0) < acc;
+        const bool ok = uniform24(tree_seed(a), (uint32_t)b, (uint32_t)ch, 0) < acc;
         sh.accepted_child = ok ? ch : -1;
         sh.carry = qx;   // q(x), for q(E)
         sh.pfix = pj;
@@ -747,7 +753,7 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       weight_pass<DK>(a, sh, nl, c, L, true, sl, cluster);
     }
     const int x = weight_draw<DK>(a, sh, nl, c, L, residual,
-                                  uniform24(a.seed, (uint32_t)b, (uint32_t)(v + 1), 1), sl, rank);
+                                  uniform24(tree_seed(a), (uint32_t)b, (uint32_t)(v + 1), 1), sl, rank);
     if (x != -1 && threadIdx.x == 0) write_final(a, b, depth, x);
     if (rank == 0 && threadIdx.x == 0) a.out_accepted[b] = depth;
     return;
@@ -811,9 +817,9 @@ static int verify_tree(const void *target, int tdt, const void *draft, int ddt, 
                        const int32_t *node_token, const int32_t *parent,
                        const int32_t *node_fixed, const int32_t *cu_nodes,
                        const float *temperature, int B, int n_nodes, int V, int max_depth,
-                       int max_branch, uint64_t seed, int32_t *out_tokens,
-                       int32_t *out_accepted, int32_t *out_path, void *workspace, size_t ws_bytes,
-                       spec_stream_t stream) {
+                       int max_branch, uint64_t seed, const uint64_t *seed_dev,
+                       int32_t *out_tokens, int32_t *out_accepted, int32_t *out_path,
+                       void *workspace, size_t ws_bytes, spec_stream_t stream) {
   if (B < 0 || n_nodes < B || V <= 0 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
   if (max_depth < 0 || max_branch < 1) return SPEC_ERR_INVALID_ARG;
   if (max_depth > SPEC_MAX_TREE_DEPTH || max_branch > SPEC_MAX_TREE_BRANCH)
@@ -828,7 +834,7 @@ static int verify_tree(const void *target, int tdt, const void *draft, int ddt, 
   if (!aligned(target, 16) || !aligned(draft, 16) || !aligned(node_token, 4) ||
       !aligned(parent, 4) || !aligned(cu_nodes, 4) || !aligned(temperature, 4) ||
       !aligned(out_tokens, 4) || !aligned(out_accepted, 4) || !aligned(out_path, 4) ||
-      !aligned(node_fixed, 4))
+      !aligned(node_fixed, 4) || !aligned(seed_dev, 8))
     return SPEC_ERR_INVALID_ARG;
   const TreeLayout L = tree_layout(B);
   if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < L.total)
@@ -851,6 +857,7 @@ static int verify_tree(const void *target, int tdt, const void *draft, int ddt, 
   a.max_depth = max_depth;
   a.max_branch = max_branch;
   a.seed = seed;
+  a.seed_dev = seed_dev;
   a.out_tokens = out_tokens;
   a.out_accepted = out_accepted;
   a.out_path = out_path;
@@ -902,7 +909,7 @@ extern "C" int spec_verify_tree(const void *target, int tdt, const void *draft, 
                                 int32_t *out_tokens, int32_t *out_accepted, int32_t *out_path,
                                 void *workspace, size_t ws_bytes, spec_stream_t stream) {
   return verify_tree(target, tdt, draft, ddt, dk, node_token, parent, nullptr, cu_nodes,
-                     temperature, B, n_nodes, V, max_depth, max_branch, seed, out_tokens,
+                     temperature, B, n_nodes, V, max_depth, max_branch, seed, nullptr, out_tokens,
                      out_accepted, out_path, workspace, ws_bytes, stream);
 }
 
@@ -911,10 +918,10 @@ extern "C" int spec_verify_tree_ext(const void *target, int tdt, const void *dra
                                     const int32_t *node_fixed, const int32_t *cu_nodes,
                                     const float *temperature, int B, int n_nodes, int V,
                                     int max_depth, int max_branch, uint64_t seed,
-                                    int32_t *out_tokens, int32_t *out_accepted,
-                                    int32_t *out_path, void *workspace, size_t ws_bytes,
-                                    spec_stream_t stream) {
+                                    const uint64_t *seed_dev, int32_t *out_tokens,
+                                    int32_t *out_accepted, int32_t *out_path, void *workspace,
+                                    size_t ws_bytes, spec_stream_t stream) {
   return verify_tree(target, tdt, draft, ddt, dk, node_token, parent, node_fixed, cu_nodes,
-                     temperature, B, n_nodes, V, max_depth, max_branch, seed, out_tokens,
-                     out_accepted, out_path, workspace, ws_bytes, stream);
+                     temperature, B, n_nodes, V, max_depth, max_branch, seed, seed_dev,
+                     out_tokens, out_accepted, out_path, workspace, ws_bytes, stream);
 }

@@ -143,5 +143,7 @@ def test_rheo_expand_rejects_bad_arguments_on_the_host(L):
 
 def test_tree_ext_rejects_a_misaligned_flag_array(L):
     args = [FAKE, 1, FAKE, 1, 0, FAKE, FAKE, FAKE + 2, FAKE, FAKE, 2, 128, 1000, 6, 4, 1,
-            FAKE, FAKE, None, FAKE, 1 << 20, None]
+            None, FAKE, FAKE, None, FAKE, 1 << 20, None]
+    assert L.spec_verify_tree_ext(*args) == sv.SPEC_ERR_INVALID_ARG
+    args[7], args[16] = FAKE, FAKE + 4                     # a misaligned seed pointer
     assert L.spec_verify_tree_ext(*args) == sv.SPEC_ERR_INVALID_ARG

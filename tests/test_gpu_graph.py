@@ -112,3 +112,50 @@ def test_tree_and_construction_calls_replay_in_a_cuda_graph():
     assert sv.spec_get_status(wst) == sv.SPEC_OK and sv.spec_get_status(wsr) == sv.SPEC_OK
     for a, b in zip(eager, tout + rout):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("cfg,over", [(1, {}), (2, dict(B=16))])
+def test_device_seed_gives_new_draws_on_each_replay(cfg, over):
+    """With the seed in device memory, one captured call replays with the
+    draws of whatever seed was last written there, equal to eager calls
+    with that seed."""
+    lb, ws, out = _linear_graph_case(cfg, **over)
+    seed_dev = torch.zeros(1, dtype=torch.int64, device=DEV)
+
+    def call():
+        sv.spec_verify_linear_ext(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
+                                  lb.temperature, 0, max_k=lb.max_k, want_pq=True,
+                                  seed_dev=seed_dev, workspace=ws, out=out + (None, None))
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    outs = []
+    for seed in (11, 12345, 2 ** 40 + 7):
+        seed_dev.fill_(seed)
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in out]
+        ref = sv.spec_verify_linear(lb.target, lb.draft, lb.draft_tokens, lb.cu_draft,
+                                    lb.temperature, seed, max_k=lb.max_k, want_pq=True)
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1]), seed
+        outs.append(got[0])
+    assert not (torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2]))
+
+
+def test_tree_device_seed():
+    tb = S.make_tree(4, device=DEV, B=8, V=3000, input_seed=31)
+    seed_dev = torch.tensor([tb.seed + 5], dtype=torch.int64, device=DEV)
+    a = sv.spec_verify_tree(tb.target, tb.draft, tb.node_token, tb.parent, tb.cu_nodes,
+                            tb.temperature, 0, max_depth=tb.max_depth,
+                            max_branch=tb.max_branch, seed_dev=seed_dev)
+    b = sv.spec_verify_tree(tb.target, tb.draft, tb.node_token, tb.parent, tb.cu_nodes,
+                            tb.temperature, tb.seed + 5, max_depth=tb.max_depth,
+                            max_branch=tb.max_branch)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
