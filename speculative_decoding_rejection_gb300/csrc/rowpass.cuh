@@ -111,12 +111,6 @@ __device__ __forceinline__ void consume_full_bf16(const unsigned char *buf, int 
   uint4 v[VEC_PER_THREAD];
 #pragma unroll
   for (int k = 0; k < VEC_PER_THREAD; ++k) v[k] = lds128(buf + 16 * (ctid + NCT * k));
-  if (RANK) {
-#pragma unroll
-    for (int k = 0; k < VEC_PER_THREAD; ++k)
-      st.cnt2 += (bgt2(v[k].x, thr2) & 0x00010001u) + (bgt2(v[k].y, thr2) & 0x00010001u) +
-                 (bgt2(v[k].z, thr2) & 0x00010001u) + (bgt2(v[k].w, thr2) & 0x00010001u);
-  }
   uint32_t a[2 * VEC_PER_THREAD];
 #pragma unroll
   for (int k = 0; k < VEC_PER_THREAD; ++k) {
@@ -128,6 +122,14 @@ __device__ __forceinline__ void consume_full_bf16(const unsigned char *buf, int 
 #pragma unroll
     for (int i = 0; i < s; ++i) a[i] = bmax2(a[i], a[i + s]);
   const float vm = fmaxf(bf16lo(a[0]), bf16hi(a[0]));
+  // rank count: only a thread holding a logit above the threshold compares
+  // its 32 (the draft token is usually among the largest logits)
+  if (RANK && vm > __uint_as_float(thr2 << 16)) {
+#pragma unroll
+    for (int k = 0; k < VEC_PER_THREAD; ++k)
+      st.cnt2 += (bgt2(v[k].x, thr2) & 0x00010001u) + (bgt2(v[k].y, thr2) & 0x00010001u) +
+                 (bgt2(v[k].z, thr2) & 0x00010001u) + (bgt2(v[k].w, thr2) & 0x00010001u);
+  }
   if (vm > st.m) {
     const int e = first_index_of(v, vm, e_first + 8 * ctid);
     if (SOFTMAX) rescale(st, vm, c);
