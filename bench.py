@@ -44,36 +44,36 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum over the algorithmic bytes it streams). Each figure
 # below is valid only for the sources it was taken on (KERNEL_SOURCES).
 # Captured on B=128, K=4, V=201088 bf16 (460.09 MB streamed by the launch):
-# 460.19 MB read + 3.50 MB written (the per-chunk partial statistics).
-ROWPASS_TRAFFIC = {"source_sha1": "9d2684d2cffbaddc38d8d0747329cd3af68574a4",
-                   "dram_per_algorithmic_byte": (460191744 + 3496960) / 460089344}
+# 460.19 MB read + 3.48 MB written (the per-chunk partial statistics).
+ROWPASS_TRAFFIC = {"source_sha1": "6f64b6019569898dcbfb786b84f81e6a98e4f7e3",
+                   "dram_per_algorithmic_byte": (460194816 + 3479040) / 460089344}
 # The same for the streaming verifier (position-lazy schedule), per byte of
 # the rows the schedule must read (target rows 1..n+1, dense draft rows
 # 1..min(n+1, K) of sampling requests). Captured on the full B=1024, K=4,
-# V=201088 workload (one pass): 2700.7 MB read + 23.1 MB written for
+# V=201088 workload (one pass): 2706.0 MB read + 23.2 MB written for
 # 1975.1 MB; the excess is the residual rows read a second time and rows
 # read before a rejection made them unneeded, so the ratio holds for this
 # workload and source only.
-STREAM_TRAFFIC = {"source_sha1": "5ba4d9981504141e0e13400b131132f2972837a5",
-                  "dram_per_algorithmic_byte": (2700709632 + 23086592) / 1975086336}
+STREAM_TRAFFIC = {"source_sha1": "c93836928a74d1fffc4847464cc572ff109c064d",
+                  "dram_per_algorithmic_byte": (2705958144 + 23199744) / 1975086336}
 # The top-128 select (two passes, the second mostly from L2), per byte of
 # the draft rows; captured on the full B=256, K=7, V=151936 workload (one
-# pass): 557.20 MB read + 4.50 MB written for 544.54 MB. Valid for these
+# pass): 556.91 MB read + 4.47 MB written for 544.54 MB. Valid for these
 # sources and this workload.
-TOPK_TRAFFIC = {"source_sha1": "7958358e0712c242ff242ef3155723de24da483b",
-                "dram_per_algorithmic_byte": (557195008 + 4502272) / 544538624}
+TOPK_TRAFFIC = {"source_sha1": "4f5a787da0ac621e138d1f4864d88364a51b4c30",
+                "dram_per_algorithmic_byte": (556910592 + 4467456) / 544538624}
 # The top-128 select with its construction epilogue on the construction
 # workload (640 frontier rows, V = 128256 bf16; L2 flushed before the call):
-# 164.54 MB read + 3.29 MB written for 164.17 MB (most of the write is
+# 164.60 MB read + 3.17 MB written for 164.17 MB (most of the write is
 # dirty lines of the L2 flush buffer, written back as the rows evict them).
 # Valid for these sources and workload.
-RHEO_TRAFFIC = {"source_sha1": "7958358e0712c242ff242ef3155723de24da483b",
-                "dram_per_algorithmic_byte": (164539392 + 3294208) / 164167680}
+RHEO_TRAFFIC = {"source_sha1": "4f5a787da0ac621e138d1f4864d88364a51b4c30",
+                "dram_per_algorithmic_byte": (164600064 + 3171328) / 164167680}
 # The tree walk (no row pass: only visited nodes' rows), per byte of those
 # rows' first read; captured on the full 32-tree workload (one pass): 63.30 MB
-# read + 0.52 MB written for 59.25 MB. Valid for these sources and workload.
-TREE_TRAFFIC = {"source_sha1": "5cbf2870df4bbe58ca5ef9c8c9fc11a15a5dc20a",
-                "dram_per_algorithmic_byte": (63298816 + 523264) / 59254272}
+# read + 0.48 MB written for 59.25 MB. Valid for these sources and workload.
+TREE_TRAFFIC = {"source_sha1": "0a249bdc0ac97606bbfcbb25420fbb6d07129a26",
+                "dram_per_algorithmic_byte": (63298560 + 480256) / 59254272}
 
 
 def parse():
