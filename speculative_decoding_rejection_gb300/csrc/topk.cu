@@ -3,21 +3,25 @@
 // to -inf, and the softmax runs over the survivors).
 //
 // One 512-thread CTA per row at a time, two CTAs per SM, rows taken in grid
-// strides (measured faster than 3 or 4 CTAs of 256 threads, whose rows in
-// flight outgrow L2 between the passes). bf16 rows (V a multiple of 8,
-// V >= 4096) take a two-pass fast path, each pass keeping eight 16-byte
-// loads in flight per thread: a packed bf16 max pass leaves each thread's
-// maximum; each warp sorts
-// its 32 maxima, and the smallest of the warps' (128/16 = 8)-th largest
-// maxima bounds the 128-th largest logit from below (16 warps x 8 threads
-// hold an element at least that large). The second pass, served from L2, gathers the few hundred
-// elements at or above the bound, and each candidate's rank under the order
-// (logit descending, id ascending) keeps the top 128. Other rows, and rows
-// whose candidates overflow, use an exact radix select on order-preserving
-// keys (-0 folded onto +0): the maximum, then 8-bit digits of the distance
-// from it, and a collection pass that keeps the lowest ids among ties. The
-// survivors are put in id order by counting smaller ids and softmaxed at
-// temperature T; T < 0.05 gives a one-hot on the argmax.
+// strides (measured faster than 4 x 256 or 8 x 128 threads per SM). bf16 rows
+// (V a multiple of 8, V >= 4096) take the fast path, each pass keeping eight
+// 16-byte loads in flight per thread:
+//   - a packed bf16 max pass leaves each thread's maximum. It also gathers the
+//     elements at or above a bound predicted from the block's previous row
+//     (that row's 128th largest logit minus a margin). When at least 128 reach
+//     it, the top 128 are among them and the row needs no second pass;
+//   - otherwise each warp sorts its 32 maxima, and the smallest of the warps'
+//     (128/16 = 8)-th largest maxima bounds the 128th largest logit from
+//     below (16 warps x 8 threads hold an element at least that large). A
+//     second pass, served from L2, gathers the few hundred elements at or
+//     above that bound;
+//   - each candidate's rank under the order (logit descending, id ascending)
+//     keeps the top 128.
+// Other rows, and rows whose candidates overflow, use an exact radix select on
+// order-preserving keys (-0 folded onto +0): the maximum, then 8-bit digits of
+// the distance from it, and a collection pass that keeps the lowest ids among
+// ties. The survivors are put in id order by counting smaller ids and
+// softmaxed at temperature T; T < 0.05 gives a one-hot on the argmax.
 //
 // With a RheoSampling epilogue (spec_rheo_expand) the block then expands the
 // row into its tree children from the survivors still in shared memory, so
