@@ -30,7 +30,7 @@
 namespace sv {
 namespace {
 
-constexpr int RH_SELECT_THREADS = 1024;
+constexpr int RH_SELECT_THREADS = 256;
 
 struct RheoArgs {
   const int32_t *cu;
