@@ -44,36 +44,36 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum over the algorithmic bytes it streams). Each figure
 # below is valid only for the sources it was taken on (KERNEL_SOURCES).
 # Captured on B=128, K=4, V=201088 bf16 (460.09 MB streamed by the launch):
-# 460.19 MB read + 3.48 MB written (the per-chunk partial statistics).
+# 460.19 MB read + 3.43 MB written (the per-chunk partial statistics).
 ROWPASS_TRAFFIC = {"source_sha1": "6f64b6019569898dcbfb786b84f81e6a98e4f7e3",
-                   "dram_per_algorithmic_byte": (460194816 + 3479040) / 460089344}
+                   "dram_per_algorithmic_byte": (460192768 + 3425280) / 460089344}
 # The same for the streaming verifier (position-lazy schedule), per byte of
 # the rows the schedule must read (target rows 1..n+1, dense draft rows
 # 1..min(n+1, K) of sampling requests). Captured on the full B=1024, K=4,
-# V=201088 workload (one pass): 2706.0 MB read + 23.2 MB written for
+# V=201088 workload (one pass): 2707.6 MB read + 22.8 MB written for
 # 1975.1 MB; the excess is the residual rows read a second time and rows
 # read before a rejection made them unneeded, so the ratio holds for this
 # workload and source only.
 STREAM_TRAFFIC = {"source_sha1": "c93836928a74d1fffc4847464cc572ff109c064d",
-                  "dram_per_algorithmic_byte": (2705958144 + 23199744) / 1975086336}
+                  "dram_per_algorithmic_byte": (2707580672 + 22810880) / 1975086336}
 # The top-128 select (two passes, the second mostly from L2), per byte of
 # the draft rows; captured on the full B=256, K=7, V=151936 workload (one
-# pass): 556.91 MB read + 4.47 MB written for 544.54 MB. Valid for these
+# pass): 556.56 MB read + 4.54 MB written for 544.54 MB. Valid for these
 # sources and this workload.
-TOPK_TRAFFIC = {"source_sha1": "4f5a787da0ac621e138d1f4864d88364a51b4c30",
-                "dram_per_algorithmic_byte": (556910592 + 4467456) / 544538624}
+TOPK_TRAFFIC = {"source_sha1": "e8249b1d1907a23dfa3f849dc81e33617e583623",
+                "dram_per_algorithmic_byte": (556563456 + 4540928) / 544538624}
 # The top-128 select with its construction epilogue on the construction
 # workload (640 frontier rows, V = 128256 bf16; L2 flushed before the call):
-# 164.60 MB read + 3.17 MB written for 164.17 MB (most of the write is
+# 164.55 MB read + 3.21 MB written for 164.17 MB (most of the write is
 # dirty lines of the L2 flush buffer, written back as the rows evict them).
 # Valid for these sources and workload.
-RHEO_TRAFFIC = {"source_sha1": "4f5a787da0ac621e138d1f4864d88364a51b4c30",
-                "dram_per_algorithmic_byte": (164600064 + 3171328) / 164167680}
+RHEO_TRAFFIC = {"source_sha1": "e8249b1d1907a23dfa3f849dc81e33617e583623",
+                "dram_per_algorithmic_byte": (164545024 + 3206912) / 164167680}
 # The tree walk (no row pass: only visited nodes' rows), per byte of those
 # rows' first read; captured on the full 32-tree workload (one pass): 63.30 MB
-# read + 0.48 MB written for 59.25 MB. Valid for these sources and workload.
+# read + 0.49 MB written for 59.25 MB. Valid for these sources and workload.
 TREE_TRAFFIC = {"source_sha1": "0a249bdc0ac97606bbfcbb25420fbb6d07129a26",
-                "dram_per_algorithmic_byte": (63298560 + 480256) / 59254272}
+                "dram_per_algorithmic_byte": (63298560 + 493056) / 59254272}
 
 
 def parse():
