@@ -283,6 +283,31 @@ def test_draft_topk_softmax_predicted_bound_misses():
     assert_probs_close(prob[rows].cpu().numpy(), rp, "top-128 probabilities")
 
 
+@pytest.mark.parametrize("B", [20, 700])
+def test_draft_topk_softmax_request_lookup(B):
+    """Each row's temperature is its request's: rows map to requests through
+    cu (the largest b with cu[b] <= r), with empty requests among them, and
+    the search narrows in one (20) or two (700) 32-way steps. Every
+    request has its own temperature, greedy ones among them, so a row given
+    a neighbour's temperature fails the comparison."""
+    g = torch.Generator(device="cpu").manual_seed(B)
+    V = 4096
+    K = torch.randint(0, 4, (B,), generator=g)
+    K[0], K[-1] = 0, 2                                  # an empty first request
+    cu = torch.zeros(B + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(K, 0)
+    R = int(cu[-1])
+    temp = 0.3 + 0.004 * torch.arange(B, dtype=torch.float32)
+    temp[::9] = 0.0                                      # greedy requests
+    z = (2.0 * torch.randn(R, V, generator=g)
+         - 1.1 * torch.log(torch.rand(R, V, generator=g) * V + 1)).to(torch.bfloat16)
+    idx, prob, ws = sv.draft_topk_softmax(z.to(DEV), cu.to(DEV), temp.to(DEV))
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    ri, rp = O.draft_topk_softmax(z, cu.numpy(), temp.numpy())
+    assert np.array_equal(idx.cpu().numpy(), ri)
+    assert_probs_close(prob.cpu().numpy(), rp, "top-128 probabilities")
+
+
 # ------------------------------------------- relaxed CACTUS rule and ranks
 CACTUS_CASES = [
     dict(alpha=0.0, max_rank=0, min_prob=0.0),     # the lossless test
