@@ -140,6 +140,64 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
   }
 }
 
+// warp_row_stat of up to ACC_ROWS rows at once. Each row keeps that
+// function's merge order exactly (lane l merges partials l, l+32, ..., then
+// the butterfly), so the statistics are bit for bit the same; only the rows'
+// partial loads are issued together, and the warp waits one memory latency
+// per group of rows instead of one per row. With `cnt`, the first rows'
+// rank counts (the sum of their partials' counts) come from the same loads.
+constexpr int ACC_G = 4;               // positions per group
+constexpr int ACC_ROWS = 2 * ACC_G;    // their target rows, then their draft rows
+__device__ __forceinline__ void warp_row_stats_group(const Part *const (&rows)[ACC_ROWS],
+                                                     const int (&nparts)[ACC_ROWS], float c,
+                                                     int lane, RowStat (&out)[ACC_ROWS],
+                                                     int (&cnt)[ACC_G]) {
+  float m[ACC_ROWS], S[ACC_ROWS];
+  int idx[ACC_ROWS];
+  int nmax = 0;
+#pragma unroll
+  for (int k = 0; k < ACC_ROWS; ++k) {
+    m[k] = NO_MAX;
+    S[k] = 0.f;
+    idx[k] = 0x7fffffff;
+    nmax = max(nmax, nparts[k]);
+  }
+#pragma unroll
+  for (int k = 0; k < ACC_G; ++k) cnt[k] = 0;
+  for (int i = lane; i < nmax; i += 32) {
+    Part q[ACC_ROWS];
+#pragma unroll
+    for (int k = 0; k < ACC_ROWS; ++k)
+      if (i < nparts[k]) q[k] = ldcg_part(rows[k] + i);
+#pragma unroll
+    for (int k = 0; k < ACC_ROWS; ++k)
+      if (i < nparts[k]) {
+        merge_stat(m[k], S[k], idx[k], q[k].m, q[k].S, q[k].idx, c);
+        if (k < ACC_G) cnt[k] += q[k].cnt;
+      }
+  }
+#pragma unroll
+  for (int k = 0; k < ACC_ROWS; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m[k], o);
+      const float S2 = __shfl_xor_sync(0xffffffffu, S[k], o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, idx[k], o);
+      merge_stat(m[k], S[k], idx[k], m2, S2, i2, c);
+    }
+    out[k] = RowStat{m[k], S[k], idx[k]};
+  }
+#pragma unroll
+  for (int k = 0; k < ACC_G; ++k)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt[k] += __shfl_xor_sync(0xffffffffu, cnt[k], o);
+}
+
+__device__ __forceinline__ RowStat shfl_stat(const RowStat &s, int src) {
+  return RowStat{__shfl_sync(0xffffffffu, s.m, src), __shfl_sync(0xffffffffu, s.S, src),
+                 __shfl_sync(0xffffffffu, s.idx, src)};
+}
+
 __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a) {
   const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -156,40 +214,80 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
   const int K = r.K;
   const float c = r.c;
   const bool sample = r.mode == MODE_SAMPLE;
+  const bool dense = sample && a.stream_draft;   // dense draft logits, reduced by the row pass
+  const long long rstride = (long long)a.nch_max * RS_CONS_WARPS;
   int n = K;
+  // lane 0's statistics of target row n+1 and draft row n+1 (the final
+  // draw's law), taken when the first rejection is found
+  RowStat tf{NO_MAX, 0.f, 0x7fffffff}, df{NO_MAX, 0.f, 0x7fffffff};
   for (int base = 0; base < K; base += 32) {
     const int cnt = min(32, K - base);
+    // lane i decides position base + i; its token and, for dense drafts, the
+    // two logits at it are loaded first so their latency overlaps the
+    // statistics below
+    const int i = base + lane;
+    int d = -1;
+    float zt = 0.f, zq = 0.f;
+    if (lane < cnt) {
+      d = a.tokens[r.d0 + i];
+      if (dense && (unsigned)d < (unsigned)a.V) {
+        zt = load_elem(a.target + (long long)(r.t0 + i) * a.t_row_bytes, a.tdt, d);
+        zq = load_elem(a.draft + (long long)(r.d0 + i) * a.d_row_bytes, a.ddt, d);
+      }
+    }
     // statistics of this block of positions: lane i keeps position base + i
+    // as reduced on lane i (its decision) and as reduced on lane 0 (the
+    // final draw's law, as the job records it)
     RowStat ts{NO_MAX, 0.f, 0x7fffffff}, ds{NO_MAX, 0.f, 0x7fffffff};
+    RowStat ts0 = ts, ds0 = ds;
     int rank = 0;
     float kl = __int_as_float(0x7fc00000);   // NaN: greedy requests
-    for (int i = 0; i < cnt; ++i) {
-      const RowStat t = target_stat(a, tslot(a, r, b, base + i), c, lane);
-      if (lane == i) ts = t;
-      if (a.want_rank) {
-        const int rk = 1 + warp_row_count(a, tslot(a, r, b, base + i), lane);
-        if (lane == i) rank = rk;
+    for (int g0 = 0; g0 < cnt; g0 += ACC_G) {
+      const Part *rows[ACC_ROWS];
+      int np[ACC_ROWS];
+#pragma unroll
+      for (int k = 0; k < ACC_G; ++k) {
+        const bool on = g0 + k < cnt;
+        rows[k] = a.part + (long long)tslot(a, r, b, base + g0 + k) * rstride;
+        np[k] = on ? a.nch_t * RS_CONS_WARPS : 0;
+        rows[ACC_G + k] = a.part + (long long)dslot(a, r, b, base + g0 + k) * rstride;
+        np[ACC_G + k] = on && dense ? a.nch_d * RS_CONS_WARPS : 0;
       }
-      if (sample && a.stream_draft) {
-        const RowStat d = draft_stat(a, dslot(a, r, b, base + i), c, lane);
-        if (lane == i) ds = d;
-        if (a.want_kl) {
-          const float k = warp_pair_kl(a, tslot(a, r, b, base + i), d, c, lane);
-          if (lane == i) kl = k;
+      RowStat st[ACC_ROWS];
+      int rc[ACC_G];
+      warp_row_stats_group(rows, np, c, lane, st, rc);
+#pragma unroll
+      for (int k = 0; k < ACC_G; ++k) {
+        if (g0 + k >= cnt) break;
+        const RowStat t0 = shfl_stat(st[k], 0), d0 = shfl_stat(st[ACC_G + k], 0);
+        if (lane == g0 + k) {
+          ts = st[k];
+          ds = st[ACC_G + k];
+          ts0 = t0;
+          ds0 = d0;
+          rank = a.want_rank ? 1 + rc[k] : 0;
+        }
+        if (dense && a.want_kl) {
+          const float kk = warp_pair_kl(a, tslot(a, r, b, base + g0 + k), st[ACC_G + k], c, lane);
+          if (lane == g0 + k) kl = kk;
         }
       }
     }
     if (a.out_kl && lane < cnt) a.out_kl[r.d0 + base + lane] = kl;
-    const int i = base + lane;
     // (a sparse law's q(d) is searched by each lane for its own position: the
     // positions' searches run side by side)
-    const bool rej = lane < cnt && position_rejects(a, b, r, i, sample, ts, ds, rank);
+    const bool rej =
+        lane < cnt && (dense ? position_rejects_z(a, b, r, i, sample, ts, ds, rank, d, zt, zq,
+                                                  false)
+                             : position_rejects(a, b, r, i, sample, ts, ds, rank));
     const unsigned bal = __ballot_sync(0xffffffffu, rej);
-    if (n == K && bal) n = base + __ffs(bal) - 1;
+    if (n == K && bal) {
+      n = base + __ffs(bal) - 1;
+      tf = shfl_stat(ts0, n - base);
+      df = shfl_stat(ds0, n - base);
+    }
   }
-  const RowStat tf = target_stat(a, tslot(a, r, b, n), c, lane);
-  RowStat df{NO_MAX, 0.f, 0x7fffffff};
-  if (sample && n < K && a.stream_draft) df = draft_stat(a, dslot(a, r, b, n), c, lane);
+  if (n == K) tf = target_stat(a, tslot(a, r, b, n), c, lane);
   finish_request(a, b, r, n, sample, tf, df, lane);
 }
 

@@ -32,7 +32,9 @@
 //   - A rejection of a sampling request appends its residual entry: the two
 //     rows just decided on, streamed once more as tile pairs whose sums of
 //     max(0, p - q) land in the job's tile-sum slots. Producers serve these
-//     entries first, so the re-read mostly hits L2. The final draws (these
+//     entries first, so the re-read follows the first read as closely as the
+//     ring allows (on a batch of a thousand requests most of it still comes
+//     from HBM, as the row traffic shows). The final draws (these
 //     and the bonus draws) are queued as jobs for the final-draw kernel,
 //     which runs after this kernel as in the multi-launch schedule.
 // Partials written by other CTAs are read through L2 (ld.global.cg) after an
