@@ -50,12 +50,12 @@ ROWPASS_TRAFFIC = {"source_sha1": "6f64b6019569898dcbfb786b84f81e6a98e4f7e3",
 # The same for the streaming verifier (position-lazy schedule), per byte of
 # the rows the schedule must read (target rows 1..n+1, dense draft rows
 # 1..min(n+1, K) of sampling requests). Captured on the full B=1024, K=4,
-# V=201088 workload (one pass): 2707.6 MB read + 22.8 MB written for
+# V=201088 workload (one pass): 2708.1 MB read + 23.3 MB written for
 # 1975.1 MB; the excess is the residual rows read a second time and rows
 # read before a rejection made them unneeded, so the ratio holds for this
 # workload and source only.
-STREAM_TRAFFIC = {"source_sha1": "c93836928a74d1fffc4847464cc572ff109c064d",
-                  "dram_per_algorithmic_byte": (2707580672 + 22810880) / 1975086336}
+STREAM_TRAFFIC = {"source_sha1": "5017700c1d26c56531cf5112684a963d1e4d8325",
+                  "dram_per_algorithmic_byte": (2708053248 + 23286528) / 1975086336}
 # The top-128 select (two passes, the second mostly from L2), per byte of
 # the draft rows; captured on the full B=256, K=7, V=151936 workload (one
 # pass): 556.56 MB read + 4.54 MB written for 544.54 MB. Valid for these
@@ -257,8 +257,9 @@ class LinearWork:
                               else self.tgt_bytes + self.drf_bytes)
         if lb.top128:
             self.kernel = "k_topk128"
-        # setup, row pass, accept, final draw, + residual sums (dense drafts)
-        # or the top-128 select (truncation); the header memset is not ours
+        # setup, row pass, accept, final draws, + the residual sums (dense
+        # drafts) or the top-128 select (truncation); the header memset is
+        # not ours
         self.launches = 5
         self.outs = (torch.empty(lb.B, lb.max_k + 1, dtype=torch.int32, device=dev),
                      torch.empty(lb.B, dtype=torch.int32, device=dev), None)
@@ -279,7 +280,21 @@ class LinearWork:
         if lazy:
             self.config["schedule"] = "position-lazy (rows 1..n+1 per request)"
             self.launches = (3 if self.stream
-                             else 2 + 2 * (lb.max_k + 1) + (0 if lb.top128 else 1) + 1)
+                             else 2 + 2 * (lb.max_k + 1) + (1 if lb.top128 else 2))
+        # small calls of the strict or greedy rule on dense logits or
+        # probabilities run as one fused kernel (the library's own test:
+        # rows of at most 8192 logits, at most 1 MiB of rows per request and
+        # the fused limit in all)
+        limit = sv.spec_set_fused_limit(0)
+        sv.spec_set_fused_limit(limit)
+        esz = lb.target.element_size()
+        per_req = (lb.max_k + 1) * lb.V * esz + lb.max_k * lb.V * lb.draft.element_size()
+        self.fused = (not lazy and not kl and self.ext is None and not lb.top128
+                      and lb.V <= 8192 and per_req <= 1 << 20 and lb.B * per_req <= limit)
+        if self.fused:
+            self.launches = 1
+            self.kernel = "k_verify_small"
+            self.config["schedule"] = "fused (one block per request)"
 
     def input_tensors(self):
         lb = self.lb

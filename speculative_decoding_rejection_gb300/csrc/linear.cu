@@ -389,15 +389,13 @@ struct SampleSmem {
 
 // Weights of this thread's SAMPLE_EPT elements of tile j: the residual
 // max(0, p - q) (kind 1) or p (kind 2).
+// (tile_weights_z: the same from target logits z already loaded; x0 is the
+// thread's first element.)
 template <int DK>
-__device__ __forceinline__ void tile_weights(const LinearArgs &a, const SampleSmem &sh,
-                                             const char *trow, bool tvec, const char *drow,
-                                             bool dvec, int kind, float c, float mt,
-                                             float invSt, float md, float invSd, int j,
-                                             float *w) {
-  const int x0 = j * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
-  float z[SAMPLE_EPT];
-  load_ept(trow, a.tdt, tvec, x0, a.V, -INFINITY, z);
+__device__ __forceinline__ void tile_weights_z(const LinearArgs &a, const SampleSmem &sh,
+                                               const float *z, int x0, const char *drow,
+                                               bool dvec, int kind, float c, float mt,
+                                               float invSt, float md, float invSd, float *w) {
 #pragma unroll
   for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = ex2((z[k] - mt) * c) * invSt;
   if (kind != 1) return;
@@ -425,6 +423,62 @@ __device__ __forceinline__ void tile_weights(const LinearArgs &a, const SampleSm
     load_ept(drow, a.ddt, dvec, x0, a.V, -INFINITY, y);
 #pragma unroll
     for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = fmaxf(0.f, w[k] - ex2((y[k] - md) * c) * invSd);
+  }
+}
+
+template <int DK>
+__device__ __forceinline__ void tile_weights(const LinearArgs &a, const SampleSmem &sh,
+                                             const char *trow, bool tvec, const char *drow,
+                                             bool dvec, int kind, float c, float mt,
+                                             float invSt, float md, float invSd, int j,
+                                             float *w) {
+  const int x0 = j * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
+  float z[SAMPLE_EPT];
+  load_ept(trow, a.tdt, tvec, x0, a.V, -INFINITY, z);
+  tile_weights_z<DK>(a, sh, z, x0, drow, dvec, kind, c, mt, invSt, md, invSd, w);
+}
+
+// A thread's SAMPLE_EPT target logits of tile j as raw 16-byte vectors
+// (bf16: two, f32: four), loaded without being used, so that several tiles'
+// loads are in flight at once; `full` is false for a tile the vectors do not
+// cover (a ragged end, an unaligned row), whose logits load_ept reads later.
+struct RawEpt {
+  uint4 v[SAMPLE_EPT / 4];
+  bool full;
+};
+__device__ __forceinline__ void load_raw_ept(const char *row, int dt, bool vec_ok, int x0, int V,
+                                             RawEpt &r) {
+  r.full = vec_ok && x0 + SAMPLE_EPT <= V;
+  if (!r.full) return;
+  const int esz = dt == SPEC_BF16 ? 2 : 4;
+  const uint4 *p = reinterpret_cast<const uint4 *>(row + (long long)esz * x0);
+#pragma unroll
+  for (int k = 0; k < SAMPLE_EPT / 4; ++k)
+    if (k < SAMPLE_EPT * esz / 16) r.v[k] = __ldg(p + k);
+}
+// The logits of a RawEpt, as load_ept gives them.
+__device__ __forceinline__ void raw_to_z(const RawEpt &r, const char *row, int dt, bool vec_ok,
+                                         int x0, int V, float *z) {
+  if (!r.full) {
+    load_ept(row, dt, vec_ok, x0, V, -INFINITY, z);
+    return;
+  }
+  if (dt == SPEC_BF16) {
+#pragma unroll
+    for (int q = 0; q < SAMPLE_EPT / 8; ++q) {
+      const uint4 w = r.v[q];
+      z[8 * q + 0] = bf16lo(w.x); z[8 * q + 1] = bf16hi(w.x);
+      z[8 * q + 2] = bf16lo(w.y); z[8 * q + 3] = bf16hi(w.y);
+      z[8 * q + 4] = bf16lo(w.z); z[8 * q + 5] = bf16hi(w.z);
+      z[8 * q + 6] = bf16lo(w.w); z[8 * q + 7] = bf16hi(w.w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < SAMPLE_EPT / 4; ++q) {
+      const uint4 w = r.v[q];
+      z[4 * q + 0] = __uint_as_float(w.x); z[4 * q + 1] = __uint_as_float(w.y);
+      z[4 * q + 2] = __uint_as_float(w.z); z[4 * q + 3] = __uint_as_float(w.w);
+    }
   }
 }
 
@@ -564,7 +618,7 @@ __device__ int fine_draw(const LinearArgs &a, SampleSmem &sh, const JobRows &q, 
 // is found from the row pass's per-chunk statistics of the target row (minus
 // the sparse corrections min(p, q) at the listed ids), so only that chunk of
 // the row is read again.
-template <int DK>
+template <int DK, bool BATCH>
 __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, const JobRows &q,
                           int kind, float u) {
   const ReqInfo r = a.req[job.b];
@@ -616,16 +670,48 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
   const int j0 = cs * tpc, j1 = min(a.ntiles, j0 + tpc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float w[SAMPLE_EPT];
+  if constexpr (BATCH) {
+    // the weights read only the target row here (the bonus law, or a
+    // residual against a sparse law held in shared memory): the target loads
+    // of SWEEP_BATCH tiles are issued before the first of them is used (more
+    // registers per thread, fewer blocks per SM)
+    constexpr int SWEEP_BATCH = 4;
+    for (int jb = j0; jb < j1; jb += SWEEP_BATCH) {
+      RawEpt raw[SWEEP_BATCH];
+#pragma unroll
+      for (int u = 0; u < SWEEP_BATCH; ++u)
+        if (jb + u < j1)
+          load_raw_ept(q.trow, a.tdt, q.tvec,
+                       (jb + u) * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT, a.V, raw[u]);
+#pragma unroll
+      for (int u = 0; u < SWEEP_BATCH; ++u) {
+        const int j = jb + u;
+        if (j >= j1) break;
+        const int x0 = j * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
+        float z[SAMPLE_EPT];
+        raw_to_z(raw[u], q.trow, a.tdt, q.tvec, x0, a.V, z);
+        tile_weights_z<DK>(a, sh, z, x0, q.drow, q.dvec, kind, q.c, q.mt, q.invSt, q.md,
+                           q.invSd, w);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) sh.cwarp[(j - j0) * (SAMPLE_THREADS / 32) + warp] = s;
+      }
+    }
+  } else {
 #pragma unroll 4
-  for (int j = j0; j < j1; ++j) {
-    tile_weights<DK>(a, sh, q.trow, q.tvec, q.drow, q.dvec, kind, q.c, q.mt, q.invSt, q.md,
-                     q.invSd, j, w);
-    float s = 0.f;
+    for (int j = j0; j < j1; ++j) {
+      tile_weights<DK>(a, sh, q.trow, q.tvec, q.drow, q.dvec, kind, q.c, q.mt, q.invSt, q.md,
+                       q.invSd, j, w);
+      float s = 0.f;
 #pragma unroll
-    for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
+      for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) sh.cwarp[(j - j0) * (SAMPLE_THREADS / 32) + warp] = s;
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) sh.cwarp[(j - j0) * (SAMPLE_THREADS / 32) + warp] = s;
+    }
   }
   __syncthreads();
   if (threadIdx.x < j1 - j0) {
@@ -655,11 +741,20 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
   return fine_draw<DK>(a, sh, q, kind, js);
 }
 
-template <int DK>
+// JOBS: the queues the launch serves. The first queue holds the dense
+// residual draws (tile sums already made; one tile is read), the second the
+// bonus draws and the residual draws against sparse laws (a chunk of the
+// target row is swept first). SAMPLE_JOBS_ALL serves both in one launch;
+// SAMPLE_JOBS_B only the second, with the sweep's loads batched, for calls
+// whose draws are all there (sparse laws). Measured: a second launch for the
+// dense calls' bonus draws costs more than the batched sweep saves.
+constexpr int SAMPLE_JOBS_ALL = 0, SAMPLE_JOBS_B = 2;
+template <int DK, int JOBS>
 __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArgs a) {
   __shared__ SampleSmem sh;
   const int g = blockIdx.x;
-  const int na = *(volatile int *)&a.hdr->n_jobs_a, nb = *(volatile int *)&a.hdr->n_jobs_b;
+  const int na = JOBS == SAMPLE_JOBS_B ? 0 : *(volatile int *)&a.hdr->n_jobs_a;
+  const int nb = *(volatile int *)&a.hdr->n_jobs_b;
   if (g >= na + nb) return;
   const bool dense = g < na;
   const Job job = dense ? a.jobs_a[g] : a.jobs_b[g - na];
@@ -737,10 +832,11 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArg
       sh.n_sparse = cnt;
     }
     __syncthreads();
-    x = chunk_draw<DK>(a, sh, job, q, 1, u);
+    x = chunk_draw<DK, JOBS == SAMPLE_JOBS_B>(a, sh, job, q, 1, u);
     done = sh.Z > 0.f;
   }
-  if (!done) x = chunk_draw<DK>(a, sh, job, q, 2, u);   // bonus, or residual without mass
+  if (!done)   // bonus, or residual without mass
+    x = chunk_draw<DK, JOBS == SAMPLE_JOBS_B>(a, sh, job, q, 2, u);
   if (threadIdx.x == 0) {
     if (x < 0) set_status(a.hdr, SPEC_ERR_INVALID_ARG, job.b);   // a row without mass
     a.out_tokens[(long long)job.b * (a.max_k + 1) + job.n] = x;
@@ -926,7 +1022,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
     if (cudaMemsetAsync(a.err, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
     const int rc = launch_verify_stream(a, st);
     if (rc != SPEC_OK) return rc;
-    k_sample_final<SPEC_DRAFT_LOGITS><<<B, SAMPLE_THREADS, 0, st>>>(a);
+    k_sample_final<SPEC_DRAFT_LOGITS, SAMPLE_JOBS_ALL><<<B, SAMPLE_THREADS, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
   k_setup_linear<<<(B + 63) / 64, 64, 0, st>>>(a);
@@ -986,11 +1082,11 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
     if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   }
   const int tiles_grid = 8 * num_sms();
-  if (a.sparse) {
-    k_sample_final<SPEC_DRAFT_SPARSE128><<<B, SAMPLE_THREADS, 0, st>>>(a);
+  if (a.sparse) {   // every draw is in the second queue
+    k_sample_final<SPEC_DRAFT_SPARSE128, SAMPLE_JOBS_B><<<B, SAMPLE_THREADS, 0, st>>>(a);
   } else if (dk == SPEC_DRAFT_PROBS) {
     k_sample_tiles<SPEC_DRAFT_PROBS><<<tiles_grid, SAMPLE_THREADS, 0, st>>>(a);
-    k_sample_final<SPEC_DRAFT_PROBS><<<B, SAMPLE_THREADS, 0, st>>>(a);
+    k_sample_final<SPEC_DRAFT_PROBS, SAMPLE_JOBS_ALL><<<B, SAMPLE_THREADS, 0, st>>>(a);
   } else {
     if (tdt == SPEC_BF16 && ddt == SPEC_BF16 && V % 8 == 0) {
       // residual tile pairs through the TMA row pass
@@ -1006,7 +1102,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
     } else {
       k_sample_tiles<SPEC_DRAFT_LOGITS><<<tiles_grid, SAMPLE_THREADS, 0, st>>>(a);
     }
-    k_sample_final<SPEC_DRAFT_LOGITS><<<B, SAMPLE_THREADS, 0, st>>>(a);
+    k_sample_final<SPEC_DRAFT_LOGITS, SAMPLE_JOBS_ALL><<<B, SAMPLE_THREADS, 0, st>>>(a);
   }
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;

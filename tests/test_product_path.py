@@ -64,3 +64,25 @@ def test_reference_arm_prints_the_contract_keys():
         assert key in d, key
     assert d["impl"] == "reference" and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["value"] > 0
+
+
+def test_bench_counts_the_fused_schedule_as_one_launch():
+    """Small strict calls run as one fused kernel; the bench's launch claim
+    and dominant kernel follow the library's own size test."""
+    import bench
+    import speculative_decoding_rejection_gb300 as sv
+    try:
+        sv.lib()
+    except RuntimeError:
+        pytest.skip("library not built")
+    cpu = torch.device("cpu")
+    w = bench.make_work(1, cpu)
+    assert w.fused and w.launches == 1 and w.kernel == "k_verify_small"
+    old = sv.spec_set_fused_limit(0)
+    try:
+        w = bench.make_work(1, cpu)
+        assert not w.fused and w.launches == 5
+    finally:
+        sv.spec_set_fused_limit(old)
+    assert not bench.make_work(2, cpu, B=4).fused          # rows above 8192 logits
+    assert not bench.make_work(1, cpu, lazy=True).fused
