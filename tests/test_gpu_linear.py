@@ -123,6 +123,20 @@ def test_sparse_draft_in_any_order_with_empty_slots():
     assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=15)
 
 
+@pytest.mark.parametrize("V", [12288, 10001])
+def test_top128_rule_with_f32_logits(V):
+    """The top-128 rule on f32 logits: the final draws sweep a chunk of the
+    target row four tiles of loads at a time, as 16-byte vectors (V = 12288:
+    aligned rows, whole tiles) or element by element (V = 10001: rows off
+    16-byte alignment, a ragged last tile)."""
+    lb = S.make_linear(3, device=DEV, B=16, K=5, V=V, dtype="f32", input_seed=V)
+    g = gpu_linear(lb, rule=sv.SPEC_RULE_STRICT_TOP128)
+    assert g["status"] == sv.SPEC_OK
+    r = oracle_linear(lb, rule=sv.SPEC_RULE_STRICT_TOP128)
+    assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=12)
+    assert (g["accepted"] == 5).any() and (g["accepted"] < 5).any()   # bonus and residual draws
+
+
 def test_top128_rule_reduced_workload3():
     lb = S.make_linear(3, device=DEV, B=24, K=7, V=20011, input_seed=31)
     g = gpu_linear(lb, rule=sv.SPEC_RULE_STRICT_TOP128)
