@@ -279,8 +279,10 @@ class LinearWork:
                        and lb.target.dtype == torch.bfloat16)
         if lazy:
             self.config["schedule"] = "position-lazy (rows 1..n+1 per request)"
-            self.launches = (3 if self.stream
-                             else 2 + 2 * (lb.max_k + 1) + (1 if lb.top128 else 2))
+            # rounds: a row pass and a decision launch per position; around
+            # them the setup, the top-128 select or the residual sums, and
+            # the final draws
+            self.launches = 3 if self.stream else 3 + 2 * (lb.max_k + 1)
         # small calls of the strict or greedy rule on dense logits or
         # probabilities run as one fused kernel (the library's own test:
         # rows of at most 8192 logits, at most 1 MiB of rows per request and
@@ -464,7 +466,7 @@ class RheoWork:
         self.tgt_bytes = 0
         self.drf_bytes = F * V * rb.draft.element_size()
         self.rowpass_bytes = self.drf_bytes       # the top-128 select reads every row once
-        self.launches = 4   # validate, top-128 select, children, selection
+        self.launches = 3   # validate, top-128 select with the expansion epilogue, selection
         self.kernel = "k_topk128"
         self.outs = (torch.empty(F, rb.K, dtype=torch.int32, device=dev),
                      torch.empty(F, rb.K, dtype=torch.float32, device=dev),
