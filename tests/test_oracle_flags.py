@@ -78,3 +78,22 @@ def test_greedy_requests_are_never_flagged():
     r = O.verify_linear(target, draft, np.array([0]), np.array([0, 1]), np.array([0.0]),
                         SEED, max_k=1)
     assert r["flag_slot"][0] == -1
+
+
+def _one_child_tree(p0, q0):
+    """A root with one child (token 0): target rows of the root and the
+    child, the root's draft row; V = 2, T = 1."""
+    target = np.log(np.array([[p0, 1 - p0], [0.5, 0.5]]))
+    draft = np.log(np.array([[q0, 1 - q0], [0.5, 0.5]]))
+    return O.verify_tree(target, draft, np.array([-1, 0]), np.array([-1, 0]),
+                         np.array([0, 2]), np.array([1.0]), SEED, 1)
+
+
+def test_tree_coin_on_the_acceptance_ratio_flags_depth_zero():
+    """The child's coin is keyed by its node index (1); with a = p(x)/q(x)
+    equal to it, the root's decision is flagged."""
+    u = O.uniform(SEED, 0, 1, O.STREAM_COIN)
+    q0 = 0.9
+    assert _one_child_tree(u * q0, q0)["flag_slot"][0] == 0
+    a = u + 0.01 if u < 0.5 else u - 0.01
+    assert _one_child_tree(a * q0, q0)["flag_slot"][0] != 0
