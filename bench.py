@@ -6,20 +6,23 @@ default workload is B=1024 requests x K=4 drafts, V=201088, bf16 target and
 draft logits, per-request T ~ U[0, 1.2] (greedy below 0.05): one
 spec_verify_linear call per step. The headline value is verified draft
 positions per second (draft positions in the batch / step time); the JSON
-line also carries the achieved HBM bandwidth of the dominant kernel (the
-row-statistics pass) against the measured copy peak, an end-to-end number
-through the same C ABI with host buffers, and the CPU oracle timed on a
-bounded sample.
+line also carries the achieved HBM bandwidth of the dominant kernel against
+the measured copy peak, an end-to-end number through the same C ABI with
+host buffers, the CPU oracle timed on the whole batch, and the parity of the
+timed call's outputs with the oracle's (requests compared, mismatched, and
+flagged: draws the oracle finds within 1e-6 of a decision boundary).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--config 1|2|3|4|5]
 
---config 3 is the top-128 truncation workload, --config 4 the tree (RRSw)
-workload (spec_verify_tree; positions = draft nodes). Workloads whose call
-reads less than twice the L2 (configs 1, 2 and 4) write twice the L2 before
-every call, outside the call's timing. Under torchrun each rank
-verifies its own batch (weak scaling, no data-path collective); rank 0 prints
-the line.
+Without --config, the line also carries `per_config`: workloads 1-4 timed
+the same way in the same run, each with its dominant kernel's roofline, its
+clocks and its whole-batch parity. --config 3 is the top-128 truncation
+workload, --config 4 the tree (RRSw) workload (spec_verify_tree; positions =
+draft nodes). Workloads whose call reads less than twice the L2 (configs 1,
+2 and 4) write twice the L2 before every call, outside the call's timing.
+Under torchrun each rank verifies its own batch (weak scaling, no data-path
+collective); rank 0 prints the line.
 """
 from __future__ import annotations
 
@@ -76,21 +79,27 @@ TREE_TRAFFIC = {"source_sha1": "0a249bdc0ac97606bbfcbb25420fbb6d07129a26",
                 "dram_per_algorithmic_byte": (63298560 + 493056) / 59254272}
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="time this workload alone (default: workload 5, with workloads 1-4 "
+                         "in per_config)")
     ap.add_argument("--V", type=int, default=None,
                     help="linear workloads: override the vocabulary size (size sweeps)")
     ap.add_argument("--B", type=int, default=None,
                     help="override the number of requests (small profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=6)
-    ap.add_argument("--cpu-requests", type=int, default=1024,
-                    help="requests (or trees) in the oracle's timed sample")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-requests", type=int, default=None,
+                    help="requests (or trees) in the oracle's timed sample (default: the "
+                         "whole batch, 16 trees for the construction workload)")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle (and so the parity check)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time workload 5 alone")
     ap.add_argument("--kl", action="store_true",
                     help="linear workloads: also emit the per-position KL(p || q)")
     ap.add_argument("--lazy", action="store_true",
@@ -105,7 +114,11 @@ def parse():
                     help="linear workloads: largest call (bytes of rows) the fused small-batch "
                          "kernel takes; 0 forces the multi-kernel schedule")
     ap.add_argument("--no-e2e", action="store_true")
-    return ap.parse_args()
+    args = ap.parse_args(argv)
+    args.headline_only = args.config is not None or args.no_per_config
+    if args.config is None:
+        args.config = 5
+    return args
 
 
 # Every source a kernel is compiled from: a traffic figure holds only while
@@ -221,6 +234,71 @@ def max_over_ranks(x, world):
 
 
 # ---------------------------------------------------------------- workloads
+def _overrides(B=None, V=None):
+    over = {}
+    if B is not None:
+        over["B"] = B
+    if V is not None:
+        over["V"] = V
+    return over
+
+
+def shape_config(cfg, rheo=False, B=None, V=None):
+    """The workload's name and sizes, from its definition alone (no inputs
+    are built and the library is not loaded)."""
+    from speculative_decoding_rejection_gb300 import synthetic as S
+    over = _overrides(B, V)
+    if rheo:
+        w = dict(S.RHEO_WORKLOAD)
+        w.update(over)
+        name = w["name"] if not over else f"{w['name']}+{sorted(over.items())}"
+        return {"workload": name, "B": w["B"], "frontier": w["B"] * w["W"], "K": w["K"],
+                "m": w["m"], "n_keep": w["n_keep"], "V": w["V"], "logits": w["dtype"],
+                "rule": "rheo_expand"}
+    w = S.workload(cfg, **over)
+    if w["kind"] == "tree":
+        return {"workload": w["name"], "B": w["B"], "nodes": w["B"] * w["N"], "V": w["V"],
+                "logits": w["dtype"], "rule": "rrsw_tree"}
+    name = w["name"] if not over else f"{w['name']}+{sorted(over.items())}"
+    K = w["K"][1] if isinstance(w["K"], tuple) else int(w["K"])
+    return {"workload": name, "B": w["B"], "K": K, "V": w["V"], "logits": w["dtype"],
+            "rule": "strict_top128" if w.get("top128") else "strict"}
+
+
+def linear_variant(config, rule, lazy, kl, ext):
+    """The rule, schedule and output keys a linear call adds to its config."""
+    c = dict(config)
+    if ext is not None:
+        c["rule"] = "cactus(alpha={alpha},max_rank={max_rank},min_prob={min_prob})".format(**ext)
+    if kl:
+        c["outputs"] = "tokens, counts and per-position KL(p || q)"
+    if lazy:
+        c["schedule"] = "position-lazy (rows 1..n+1 per request)"
+    return c
+
+
+def compare_outputs(ref, tokens, accepted, path=None):
+    """Whole-batch parity of one call's outputs with the oracle's on the
+    same inputs. A request compares bit for bit (tokens, accepted count,
+    tree path) unless the oracle flags one of its draws as within 1e-6 of a
+    decision boundary; a flagged request compares the output slots before
+    the flagged one."""
+    import numpy as np
+    mism = flagged = 0
+    for j, b in enumerate(ref["requests"]):
+        fs = int(ref["flag_slot"][j])
+        if fs < 0:
+            ok = (np.array_equal(tokens[b], ref["tokens"][j])
+                  and int(accepted[b]) == int(ref["accepted"][j])
+                  and (path is None or np.array_equal(path[b], ref["path"][j])))
+        else:
+            flagged += 1
+            ok = np.array_equal(tokens[b][:fs], ref["tokens"][j][:fs])
+        mism += 0 if ok else 1
+    return {"requests": int(len(tokens)), "compared": int(len(ref["requests"])),
+            "mismatched": mism, "flagged": flagged}
+
+
 class LinearWork:
     """spec_verify_linear on a linear workload (configs 1, 2, 3, 5)."""
     unit_name = "requests"
@@ -234,10 +312,8 @@ class LinearWork:
         import speculative_decoding_rejection_gb300 as sv
         from speculative_decoding_rejection_gb300 import synthetic as S
         self.sv = sv
-        over = {} if B is None else {"B": B}
-        if V is not None:
-            over["V"] = V
-        self.lb = lb = S.make_linear(cfg, device=dev, input_seed=input_seed, **over)
+        self.cfg = cfg
+        self.lb = lb = S.make_linear(cfg, device=dev, input_seed=input_seed, **_overrides(B, V))
         self.rule = sv.SPEC_RULE_STRICT_TOP128 if lb.top128 else sv.SPEC_RULE_STRICT
         self.ext = None
         if rule == "cactus":
@@ -255,8 +331,7 @@ class LinearWork:
         # top-128 select, which then dominates, reads every draft row
         self.rowpass_bytes = (lb.draft.numel() * lb.draft.element_size() if lb.top128
                               else self.tgt_bytes + self.drf_bytes)
-        if lb.top128:
-            self.kernel = "k_topk128"
+        self.kernel = "k_topk128" if lb.top128 else None
         # setup, row pass, accept, final draws, + the residual sums (dense
         # drafts) or the top-128 select (truncation); the header memset is
         # not ours
@@ -265,20 +340,12 @@ class LinearWork:
                      torch.empty(lb.B, dtype=torch.int32, device=dev), None)
         self.ws = torch.empty(sv.spec_verify_linear_workspace(lb.B, lb.max_k, lb.V, self.rule),
                               dtype=torch.uint8, device=dev)
-        self.config = {"workload": lb.meta["workload"], "B": lb.B, "K": lb.max_k, "V": lb.V,
-                       "logits": "bf16" if lb.target.element_size() == 2 else "f32",
-                       "rule": "strict_top128" if lb.top128 else "strict"}
-        if self.ext is not None:
-            self.config["rule"] = ("cactus(alpha={alpha},max_rank={max_rank},"
-                                   "min_prob={min_prob})".format(**self.ext))
-        if kl:
-            self.config["outputs"] = "tokens, counts and per-position KL(p || q)"
+        self.config = linear_variant(shape_config(cfg, B=B, V=V), rule, lazy, kl, self.ext)
         # the position-lazy schedule of dense bf16 logits (V % 8 == 0, no KL)
         # runs as one persistent kernel: setup, streaming verifier, final draws
         self.stream = (lazy and not lb.top128 and not kl and lb.V % 8 == 0
                        and lb.target.dtype == torch.bfloat16)
         if lazy:
-            self.config["schedule"] = "position-lazy (rows 1..n+1 per request)"
             # rounds: a row pass and a decision launch per position; around
             # them the setup, the top-128 select or the residual sums, and
             # the final draws
@@ -297,6 +364,10 @@ class LinearWork:
             self.launches = 1
             self.kernel = "k_verify_small"
             self.config["schedule"] = "fused (one block per request)"
+        if self.kernel is None:
+            self.kernel = ("k_verify_stream" if self.stream
+                           else "k_row_pass rounds with k_lazy_decide (one span)" if lazy
+                           else "k_row_pass")
 
     def input_tensors(self):
         lb = self.lb
@@ -339,20 +410,29 @@ class LinearWork:
     def mean_accepted(self):
         return float(self.outs[1].float().mean())
 
-    def oracle_sample(self, units, offset=0):
-        """Runs the oracle on `units` requests; returns the draft positions done."""
+    def host_inputs(self):
         import numpy as np
-        from oracle import spec_oracle as O
-        lb = self.lb
         if not hasattr(self, "_host"):
+            lb = self.lb
             self._host = (lb.target.cpu(), lb.draft.cpu(), lb.draft_tokens.cpu().numpy(),
                           lb.cu_draft.cpu().numpy(), lb.temperature.cpu().numpy())
             self._order = np.random.default_rng(1).permutation(lb.B)
-        tgt, drf, toks, cu, T = self._host
+        return self._host
+
+    def oracle_sample(self, units, offset=0):
+        """Runs the oracle on `units` requests; returns the draft positions
+        done and the oracle's result."""
+        import numpy as np
+        from oracle import spec_oracle as O
+        lb = self.lb
+        tgt, drf, toks, cu, T = self.host_inputs()
         req = np.sort(np.roll(self._order, -offset)[:min(units, lb.B)])
-        O.verify_linear(tgt, drf, toks, cu, T, lb.seed, rule=self.rule, max_k=lb.max_k,
-                        requests=req, **(self.ext or {}))
-        return int(sum(cu[b + 1] - cu[b] for b in req))
+        ref = O.verify_linear(tgt, drf, toks, cu, T, lb.seed, rule=self.rule, max_k=lb.max_k,
+                              requests=req, **(self.ext or {}))
+        return int(sum(cu[b + 1] - cu[b] for b in req)), ref
+
+    def compare(self, ref):
+        return compare_outputs(ref, self.outs[0].cpu().numpy(), self.outs[1].cpu().numpy())
 
 
 class TreeWork:
@@ -364,8 +444,8 @@ class TreeWork:
         import speculative_decoding_rejection_gb300 as sv
         from speculative_decoding_rejection_gb300 import synthetic as S
         self.sv = sv
-        over = {} if B is None else {"B": B}
-        self.tb = tb = S.make_tree(cfg, device=dev, input_seed=input_seed, **over)
+        self.cfg = cfg
+        self.tb = tb = S.make_tree(cfg, device=dev, input_seed=input_seed, **_overrides(B))
         cu = tb.cu_nodes.cpu().long()
         par = tb.parent.cpu().long()
         base = torch.repeat_interleave(cu[:-1], torch.diff(cu))
@@ -390,9 +470,7 @@ class TreeWork:
         self.ws = torch.empty(sv.spec_verify_tree_workspace(tb.B, n, tb.V, tb.max_depth,
                                                             tb.max_branch),
                               dtype=torch.uint8, device=dev)
-        self.config = {"workload": tb.meta["workload"], "B": tb.B, "nodes": n, "V": tb.V,
-                       "logits": "bf16" if tb.target.element_size() == 2 else "f32",
-                       "rule": "rrsw_tree"}
+        self.config = shape_config(cfg, B=B)
 
     def input_tensors(self):
         tb = self.tb
@@ -432,18 +510,26 @@ class TreeWork:
     def mean_accepted(self):
         return float(self.outs[1].float().mean())
 
+    def host_inputs(self):
+        if not hasattr(self, "_host"):
+            tb = self.tb
+            self._host = (tb.target.cpu(), tb.draft.cpu(), tb.node_token.cpu().numpy(),
+                          tb.parent.cpu().numpy(), tb.cu_nodes.cpu().numpy(),
+                          tb.temperature.cpu().numpy())
+        return self._host
+
     def oracle_sample(self, units, offset=0):
         import numpy as np
         from oracle import spec_oracle as O
         tb = self.tb
-        if not hasattr(self, "_host"):
-            self._host = (tb.target.cpu(), tb.draft.cpu(), tb.node_token.cpu().numpy(),
-                          tb.parent.cpu().numpy(), tb.cu_nodes.cpu().numpy(),
-                          tb.temperature.cpu().numpy())
-        tgt, drf, tok, par, cu, T = self._host
+        tgt, drf, tok, par, cu, T = self.host_inputs()
         req = np.sort((np.arange(min(units, tb.B)) + offset) % tb.B)
-        O.verify_tree(tgt, drf, tok, par, cu, T, tb.seed, tb.max_depth, requests=req)
-        return int(sum(cu[b + 1] - cu[b] - 1 for b in req))
+        ref = O.verify_tree(tgt, drf, tok, par, cu, T, tb.seed, tb.max_depth, requests=req)
+        return int(sum(cu[b + 1] - cu[b] - 1 for b in req)), ref
+
+    def compare(self, ref):
+        return compare_outputs(ref, self.outs[0].cpu().numpy(), self.outs[1].cpu().numpy(),
+                               self.outs[2].cpu().numpy())
 
 
 class RheoWork:
@@ -459,7 +545,8 @@ class RheoWork:
         import speculative_decoding_rejection_gb300 as sv
         from speculative_decoding_rejection_gb300 import synthetic as S
         self.sv = sv
-        rb = S.make_rheo(device=dev, input_seed=input_seed, **({"B": B} if B else {}))
+        self.cfg = None
+        rb = S.make_rheo(device=dev, input_seed=input_seed, **_overrides(B))
         self.rb = rb
         F, V = rb.draft.shape
         self.positions = F
@@ -475,10 +562,7 @@ class RheoWork:
                      torch.empty(rb.B, rb.n_keep, dtype=torch.int32, device=dev))
         self.ws = torch.empty(sv.spec_rheo_expand_workspace(F, V), dtype=torch.uint8,
                               device=dev)
-        self.config = {"workload": rb.meta["workload"], "B": rb.B, "frontier": F, "K": rb.K,
-                       "m": rb.m, "n_keep": rb.n_keep, "V": V,
-                       "logits": "bf16" if rb.draft.element_size() == 2 else "f32",
-                       "rule": "rheo_expand"}
+        self.config = shape_config(None, rheo=True, B=B)
 
     def input_tensors(self):
         rb = self.rb
@@ -499,7 +583,6 @@ class RheoWork:
         return None
 
     def oracle_sample(self, units, offset=0):
-        import numpy as np
         from oracle import spec_oracle as O
         rb = self.rb
         if not hasattr(self, "_host"):
@@ -509,9 +592,12 @@ class RheoWork:
         b0 = offset % rb.B
         b1 = min(rb.B, b0 + units)
         lo, hi = int(cu[b0]), int(cu[b1])
-        O.rheo_expand(drf[lo:hi], cu[b0:b1 + 1] - lo, fs[lo:hi], T[b0:b1], rb.seed, rb.level,
-                      rb.K, rb.m, rb.eps, rb.n_keep)
-        return hi - lo
+        ref = O.rheo_expand(drf[lo:hi], cu[b0:b1 + 1] - lo, fs[lo:hi], T[b0:b1], rb.seed,
+                            rb.level, rb.K, rb.m, rb.eps, rb.n_keep)
+        return hi - lo, None
+
+    def compare(self, ref):
+        return None
 
 
 def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False, rheo=False,
@@ -524,16 +610,82 @@ def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False
 
 
 def cpu_baseline(work, n_units):
-    """The oracle, as it stands, on a bounded sample of the same workload."""
+    """The oracle, as it stands, on a bounded sample of the same workload (the
+    whole batch by default). Returns the baseline record and the oracle's
+    result on that sample."""
     t0 = time.perf_counter()
-    pos = work.oracle_sample(n_units)
+    pos, ref = work.oracle_sample(n_units)
     dt = time.perf_counter() - t0
     n = min(n_units, work.config["B"])
     unit = getattr(work, "unit", UNIT)
     return {"value": pos / dt, "unit": unit, "cores": 1, "kind": "oracle",
             "sample": f"{n} of {work.config['B']} {work.unit_name} ({pos} "
                       f"{unit.split('/')[0]}) of the same workload, fp64 numpy, one thread, "
-                      f"{dt:.1f} s"}
+                      f"{dt:.1f} s"}, ref
+
+
+# --------------------------------------------------------- reference arm
+class ReferenceSample:
+    """The reference arm's inputs: a batch of `n` requests (trees) drawn on
+    the CPU from the workload's own recipe. The arm times the oracle alone,
+    so it builds nothing on the GPU and never loads the verifier library."""
+
+    def __init__(self, args, n):
+        from speculative_decoding_rejection_gb300 import synthetic as S
+        self.rheo = args.rheo
+        self.cfg = args.config
+        self.ext = LinearWork.CACTUS if args.rule == "cactus" else None
+        if args.rheo:
+            self.config = shape_config(None, rheo=True, B=args.B)
+            self.unit_name = "trees"
+            self.rb = S.make_rheo(device="cpu", B=n)
+        elif args.config == 4:
+            self.config = shape_config(4, B=args.B)
+            self.unit_name = "trees"
+            self.tb = S.make_tree(4, device="cpu", B=n)
+        else:
+            self.config = linear_variant(shape_config(args.config, B=args.B, V=args.V),
+                                         args.rule, args.lazy, args.kl, self.ext)
+            self.unit_name = "requests"
+            over = {"B": n}
+            if args.V is not None:
+                over["V"] = args.V
+            self.lb = S.make_linear(args.config, device="cpu", **over)
+            # rule ids as include/specverify.h numbers them
+            self.rule = 3 if self.ext else 2 if self.lb.top128 else 0
+        self.n = n
+
+    def oracle_sample(self, units, offset=0):
+        import numpy as np
+        from oracle import spec_oracle as O
+        if self.rheo:
+            rb = self.rb
+            b0 = offset % rb.B
+            b1 = min(rb.B, b0 + units)
+            cu = rb.cu_frontier.numpy()
+            lo, hi = int(cu[b0]), int(cu[b1])
+            O.rheo_expand(rb.draft[lo:hi], cu[b0:b1 + 1] - lo, rb.frontier_score.numpy()[lo:hi],
+                          rb.temperature.numpy()[b0:b1], rb.seed, rb.level, rb.K, rb.m, rb.eps,
+                          rb.n_keep)
+            return hi - lo
+        if self.cfg == 4:
+            tb = self.tb
+            req = np.sort((np.arange(min(units, tb.B)) + offset) % tb.B)
+            cu = tb.cu_nodes.numpy()
+            O.verify_tree(tb.target, tb.draft, tb.node_token.numpy(), tb.parent.numpy(), cu,
+                          tb.temperature.numpy(), tb.seed, tb.max_depth, requests=req)
+            return int(sum(cu[b + 1] - cu[b] - 1 for b in req))
+        lb = self.lb
+        req = np.sort((np.arange(min(units, lb.B)) + offset) % lb.B)
+        cu = lb.cu_draft.numpy()
+        O.verify_linear(lb.target, lb.draft, lb.draft_tokens.numpy(), cu, lb.temperature.numpy(),
+                        lb.seed, rule=self.rule, max_k=lb.max_k, requests=req, **(self.ext or {}))
+        return int(sum(cu[b + 1] - cu[b] for b in req))
+
+
+# requests (trees) the reference arm draws on the CPU: enough for the steps it
+# cycles over, few enough to build in seconds
+REFERENCE_SAMPLE = {1: 4, 2: 64, 3: 16, 4: 8, 5: 32, "rheo": 16}
 
 
 def run_reference(args):
@@ -542,11 +694,11 @@ def run_reference(args):
     if rank != 0:
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    import torch
-    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
-    work = make_work(args.config, dev, B=args.B, rule=args.rule, rheo=args.rheo)
+    full_B = shape_config(args.config, rheo=args.rheo, B=args.B)["B"]
+    n = min(full_B, REFERENCE_SAMPLE["rheo" if args.rheo else args.config])
+    work = ReferenceSample(args, n)
     per_step = 1 if args.config == 4 and not args.rheo else 2
-    metric, unit = getattr(work, "metric", METRIC), getattr(work, "unit", UNIT)
+    metric, unit = (RheoWork.metric, RheoWork.unit) if args.rheo else (METRIC, UNIT)
     for k in range(args.warmup):
         work.oracle_sample(per_step, offset=k * per_step)
     pos = 0
@@ -563,45 +715,40 @@ def run_reference(args):
         "config": dict(work.config, step=f"{per_step} {work.unit_name} of the batch per step"),
         "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": f"{per_step} {work.unit_name} per step, {args.steps} steps, "
-                                   "fp64 numpy, one thread"},
+                                   f"cycling over {n} {work.unit_name} drawn on the CPU from "
+                                   "the workload's recipe; fp64 numpy, one thread"},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def main():
-    args = parse()
-    if args.impl == "reference":
-        run_reference(args)
-        return
+# ------------------------------------------------------------- measurement
+def l2_size(dev):
     import torch
-    import speculative_decoding_rejection_gb300 as sv
-    from speculative_decoding_rejection_gb300 import synthetic as S
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 128 << 20
 
-    world, rank, local = dist_setup()
-    dev = torch.device("cuda", local)
-    sv.lib()
-    if args.fused_limit is not None:
-        sv.spec_set_fused_limit(args.fused_limit)
-    seed_base = S.INPUT_SEED_BASE + (0x100 if args.rheo else args.config)
-    work = make_work(args.config, dev, input_seed=seed_base + 7919 * rank, B=args.B, V=args.V,
-                     rule=args.rule, lazy=args.lazy, kl=args.kl, rheo=args.rheo)
-    unit = getattr(work, "unit", UNIT)
 
-    for _ in range(max(3, args.warmup)):
+def timed_calls(work, sv, dev, steps, warmup, world):
+    """W warm-up calls, then `steps` calls bracketed by a barrier and a
+    device synchronisation, timed with CUDA events on the calling stream;
+    the library records two more events around the dominant kernel of each
+    call. Returns the step time (max over ranks), that kernel's mean time,
+    whether L2 was flushed, and the clocks sampled meanwhile."""
+    import torch
+    for _ in range(max(3, warmup)):
         work.call()
     torch.cuda.synchronize()
     if hasattr(work, "settle"):
         work.settle()
     assert sv.spec_get_status(work.ws) == sv.SPEC_OK
-    K = args.steps
+    K = steps
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # a call that touches less than twice the L2 would find its rows there
     # on the next call: such workloads write a buffer of twice the L2 before
     # every call, outside the call's own timing
-    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 128 << 20
+    l2_bytes = l2_size(dev)
     touched = work.tgt_bytes + work.drf_bytes
     flush = touched < 2 * l2_bytes
     if flush:
@@ -628,51 +775,124 @@ def main():
     torch.cuda.synchronize()
     barrier(world)
     clocks.stop()
+    sv.spec_profile_row_pass(None, None)
     if flush:
         ms_step = max_over_ranks(statistics.mean(s_.elapsed_time(e_) for s_, e_ in
                                                  zip(ev_s, ev_e)), world)
     else:
         ms_step = max_over_ranks(e0.elapsed_time(e1) / K, world)
     rp_ms = statistics.mean(b.elapsed_time(a) for b, a in zip(ev_b, ev_a))
+    assert sv.spec_get_status(work.ws) == sv.SPEC_OK
+    return {"ms_step": ms_step, "rp_ms": rp_ms, "flush": flush, "l2_bytes": l2_bytes,
+            "clocks": clocks.summary()}
 
+
+def traffic_for(work, args):
+    """DRAM bytes per launch of the dominant kernel from its committed ncu
+    capture, scaled by the algorithmic bytes; None where the capture does not
+    hold (other sources, sizes or kernel variants)."""
+    kernel = getattr(work, "kernel", None)
+    full = args.B is None and args.V is None
+    ext = getattr(work, "ext", None)
+    if kernel == "k_row_pass" and getattr(work, "kl", None) is None and ext is None:
+        if ROWPASS_TRAFFIC["source_sha1"] == source_sha1("rowpass"):
+            return ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    if kernel == "k_topk128" and full:
+        if isinstance(work, RheoWork):
+            if RHEO_TRAFFIC["source_sha1"] == source_sha1("topk"):
+                return RHEO_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+        elif work.cfg == 3 and TOPK_TRAFFIC["source_sha1"] == source_sha1("topk"):
+            return TOPK_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    if (kernel == "k_tree_walk" and full and work.cfg == 4
+            and TREE_TRAFFIC["source_sha1"] == source_sha1("tree")):
+        return TREE_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    if (kernel == "k_verify_stream" and ext is None and full and work.cfg == 5
+            and STREAM_TRAFFIC["source_sha1"] == source_sha1("stream")):
+        return STREAM_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    return None
+
+
+def roofline(work, t, args):
     peaks, peak_src = measured_peaks()
     peak = float(peaks["hbm_gbs"])
-    achieved = work.rowpass_bytes / (rp_ms * 1e-3) / 1e9
-    traffic = None
-    lazy = getattr(work, "lazy", False)
-    stream = getattr(work, "stream", False)
-    plain = (not lazy and getattr(work, "kl", None) is None and getattr(work, "ext", None) is None
-             and getattr(work, "kernel", None) is None)
-    if ROWPASS_TRAFFIC["source_sha1"] == source_sha1("rowpass") and plain:
-        traffic = ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if (getattr(work, "kernel", None) == "k_topk128" and args.B is None and args.V is None and args.rheo
-            and RHEO_TRAFFIC["source_sha1"] == source_sha1("topk")):
-        traffic = RHEO_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if (getattr(work, "kernel", None) == "k_topk128" and args.B is None and args.V is None and args.config == 3
-            and not args.rheo
-            and TOPK_TRAFFIC["source_sha1"] == source_sha1("topk")):
-        traffic = TOPK_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if (getattr(work, "kernel", None) == "k_tree_walk" and args.B is None and args.V is None and args.config == 4
-            and TREE_TRAFFIC["source_sha1"] == source_sha1("tree")):
-        traffic = TREE_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if (stream and getattr(work, "ext", None) is None and args.B is None and args.V is None and args.config == 5
-            and STREAM_TRAFFIC["source_sha1"] == source_sha1("stream")):
-        traffic = STREAM_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    achieved = work.rowpass_bytes / (t["rp_ms"] * 1e-3) / 1e9
+    return {"kernel": work.kernel, "bound": "hbm", "achieved": achieved, "peak": peak,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback", "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic_for(work, args),
+            "algorithmic_bytes_per_launch": work.rowpass_bytes, "ms_per_launch": t["rp_ms"]}
+
+
+def l2_note(work, t):
+    algo = work.tgt_bytes + work.drf_bytes
+    if t["flush"]:
+        return (f"{algo / 1e9:.3f} GB read per step; L2 ({t['l2_bytes'] >> 20} MiB) "
+                "flushed before every call by writing twice its size, untimed")
+    return f"inputs {algo / 1e9:.2f} GB per step, larger than L2"
+
+
+def parity_leg(work, n_units):
+    """The oracle on `n_units` of the batch (timed: the CPU baseline) and the
+    last timed call's outputs compared with it."""
+    base, ref = cpu_baseline(work, n_units)
+    return base, (work.compare(ref) if ref is not None else None)
+
+
+def per_config_entry(cfg, dev, args, world, sv):
+    """One workload of per_config: timed as the headline, with its roofline,
+    clocks and whole-batch parity."""
+    import torch
+    from speculative_decoding_rejection_gb300 import synthetic as S
+    work = make_work(cfg, dev, input_seed=S.INPUT_SEED_BASE + cfg)
+    t = timed_calls(work, sv, dev, args.steps, args.warmup, world)
+    entry = {"workload": work.config["workload"], "config": dict(work.config, l2=l2_note(work, t)),
+             "value": work.positions / (t["ms_step"] * 1e-3),
+             "unit": getattr(work, "unit", UNIT), "ms_per_step": t["ms_step"],
+             "mean_accepted": work.mean_accepted(),
+             "roofline": roofline(work, t, args), "gpu_launches": args.steps * work.launches,
+             "clocks": t["clocks"]}
+    if not args.no_cpu_baseline:
+        entry["cpu_baseline"], entry["parity"] = parity_leg(work, work.config["B"])
+    del work
+    torch.cuda.empty_cache()
+    return entry
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import speculative_decoding_rejection_gb300 as sv
+    from speculative_decoding_rejection_gb300 import synthetic as S
+
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    sv.lib()
+    if args.fused_limit is not None:
+        sv.spec_set_fused_limit(args.fused_limit)
+    seed_base = S.INPUT_SEED_BASE + (0x100 if args.rheo else args.config)
+    work = make_work(args.config, dev, input_seed=seed_base + 7919 * rank, B=args.B, V=args.V,
+                     rule=args.rule, lazy=args.lazy, kl=args.kl, rheo=args.rheo)
+    unit = getattr(work, "unit", UNIT)
+    t = timed_calls(work, sv, dev, args.steps, args.warmup, world)
+    ms_step = t["ms_step"]
 
     # end to end through the same API: pinned host inputs copied in, the
     # results read back, every step
     e2e = None
     if not args.no_e2e:
-        host = {n: t.cpu().pin_memory() for n, t in work.input_tensors().items()}
-        dev_in = {n: torch.empty_like(t) for n, t in work.input_tensors().items()}
+        host = {n: t_.cpu().pin_memory() for n, t_ in work.input_tensors().items()}
+        dev_in = {n: torch.empty_like(t_) for n, t_ in work.input_tensors().items()}
         res = work.result_tensors()
         host_out = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in res]
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        h2d = sum(t_.numel() * t_.element_size() for t_ in host.values())
+        d2h = sum(t_.numel() * t_.element_size() for t_ in host_out)
 
         def e2e_step():
-            for n, t in host.items():
-                dev_in[n].copy_(t, non_blocking=True)
+            for n, t_ in host.items():
+                dev_in[n].copy_(t_, non_blocking=True)
             work.call(dev_in)
             for h, r in zip(host_out, res):
                 h.copy_(r, non_blocking=True)
@@ -700,7 +920,7 @@ def main():
         "value": world * work.positions / (ms_step * 1e-3),
         "unit": unit,
         "n_gpus": world,
-        "steps": K,
+        "steps": args.steps,
         "warmup": max(3, args.warmup),
         "ms_per_step": ms_step,
         "higher_is_better": True,
@@ -709,33 +929,26 @@ def main():
         "dtype": "f32",
         "data": "synthetic",
         "impl": "gb300",
-        "config": dict(work.config,
-                       l2=(f"{algo / 1e9:.3f} GB read per step; L2 ({l2_bytes >> 20} MiB) "
-                           "flushed before every call by writing twice its size, untimed"
-                           if flush else
-                           f"inputs {algo / 1e9:.2f} GB per step, larger than L2"),
+        "config": dict(work.config, l2=l2_note(work, t),
                        parallelism=f"replicas x{world} (independent request batches)"),
         "hbm_gbs_whole_call": algo / (ms_step * 1e-3) / 1e9,
         "algorithmic_bytes_per_step": algo,
         "mean_accepted": work.mean_accepted(),
-        "roofline": {
-            "kernel": (getattr(work, "kernel", None) or
-                       ("k_verify_stream" if stream
-                        else "k_row_pass rounds with k_lazy_decide (one span)" if lazy
-                        else "k_row_pass")),
-            "bound": "hbm", "achieved": achieved, "peak": peak,
-            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-            else "fallback", "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-            "algorithmic_bytes_per_launch": work.rowpass_bytes, "ms_per_launch": rp_ms,
-        },
-        "gpu_launches": K * work.launches,
-        "clocks": clocks.summary(),
+        "roofline": roofline(work, t, args),
+        "gpu_launches": args.steps * work.launches,
+        "clocks": t["clocks"],
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(
-            work, 8 if args.config == 4 and not args.rheo else 16 if args.rheo
-            else args.cpu_requests)
+        n = (args.cpu_requests if args.cpu_requests is not None
+             else 16 if args.rheo else work.config["B"])
+        line["cpu_baseline"], line["parity"] = parity_leg(work, n)
+    if world == 1 and not args.headline_only:
+        # the other workloads, one after another on the same GPU
+        del work
+        torch.cuda.empty_cache()
+        line["per_config"] = {str(c): per_config_entry(c, dev, args, world, sv)
+                              for c in (1, 2, 3, 4)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

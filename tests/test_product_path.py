@@ -66,6 +66,20 @@ def test_reference_arm_prints_the_contract_keys():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["value"] > 0
 
 
+def test_reference_arm_never_loads_the_verifier_library():
+    """The reference arm times the oracle alone: it builds its sample on the
+    CPU and neither loads libspecverify.so nor touches a GPU."""
+    code = ("import bench, speculative_decoding_rejection_gb300 as sv\n"
+            "bench.main(['--impl', 'reference', '--steps', '1', '--warmup', '0', '--config', '2'])\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "assert sv._lib is None and 'libspecverify' not in maps\n"
+            "print('NOT_LOADED')\n")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                         timeout=600, env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert "NOT_LOADED" in out.stdout
+
+
 def test_bench_counts_the_fused_schedule_as_one_launch():
     """Small strict calls run as one fused kernel; the bench's launch claim
     and dominant kernel follow the library's own size test."""
