@@ -251,7 +251,10 @@ int spec_verify_linear_ext(const void *target, int tdt, const void *draft,
  * All calls on a device share that array: calls that overlap on the GPU
  * race, so order them (one stream, or events). The first call on each device
  * looks up the array's address (cudaGetSymbolAddress, with that device
- * current); make it before any stream capture. Nothing is allocated.
+ * current); make it before any stream capture. The address is kept per
+ * device context: the first call after cudaDeviceReset looks it up again,
+ * so make that call before any stream capture as well. Nothing is
+ * allocated.
  *
  *   out_status  optional device int32: receives the call's device status word
  *               (SPEC_OK or a negative spec_status) once the call's work is
@@ -284,7 +287,8 @@ size_t spec_verify_tree_workspace(int B, int n_nodes, int V, int max_depth,
  *   node_token  [n_nodes] int32: the token of each node (roots unused).
  *   parent      [n_nodes] int32: LOCAL parent id, -1 for the root (local
  *               node 0); parent[c] < c. Siblings carry distinct tokens, in
- *               the order they were drawn.
+ *               the order they were drawn (a repeated token is invalid
+ *               input: SPEC_ERR_INVALID_ARG in the status word).
  *   cu_nodes    [B+1] int32 node offsets, cu_nodes[B] = n_nodes, at most
  *               SPEC_MAX_TREE_NODES nodes per tree.
  *   max_depth   bound on the depth of every tree (out width max_depth+1).

@@ -11,16 +11,21 @@
 //   - SPEC_NOALLOC_SCRATCH_BYTES (16 MiB) per GPU, reserved on every GPU that
 //     loads the library and held until the process exits;
 //   - shared by all calls on a device and left holding the last call's
-//     contents; the words that must start at zero (status, work counter) are
-//     reset by the call's own first kernel, everything else is written before
-//     it is read within the call;
+//     contents; the header words that must start at zero (status, work
+//     counters) are cleared by a cudaMemsetAsync on the call's stream before
+//     its first kernel, and everything else is written before it is read
+//     within the call;
 //   - calls whose work overlaps on the GPU (different streams, or different
 //     host threads, without ordering between them) race on it; order them on
 //     one stream or with events.
 // The first call on each device looks up the array's device address with
 // cudaGetSymbolAddress() (with that device current); make that first call
-// before any stream capture. Nothing here calls cudaMalloc, cudaFree or an
-// allocating library routine.
+// before any stream capture. The address belongs to the device's context: a
+// call made after cudaDeviceReset (a new context) looks it up again, so make
+// the first call after a reset before any stream capture too. Nothing here
+// calls cudaMalloc, cudaFree or an allocating library routine.
+#include <cuda.h>   // context types only: the driver calls are resolved at run time
+
 #include <mutex>
 
 #include "common.cuh"
@@ -31,21 +36,60 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SC
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  void *addr;                  // device address of the array in that context
+  unsigned long long ctx_id;   // the context it was looked up in
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device (looked up once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Unique id of the current thread's context (ids are never reused within a
+// process, so a reset device's new context has a new one). Called with
+// g_scratch_mu held.
+int current_context_id(unsigned long long *id) {
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) {
+    void *f0 = nullptr, *f1 = nullptr;
+    cudaDriverEntryPointQueryResult q0, q1;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 12000, cudaEnableDefault, &q0) !=
+            cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q0 != cudaDriverEntryPointSuccess || q1 != cudaDriverEntryPointSuccess)
+      return SPEC_ERR_CUDA;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f0);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f1);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return SPEC_ERR_CUDA;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device context.
 int scratch_address(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_UNSUPPORTED;
+  // makes the device's primary context current on this thread (and creates
+  // it if this thread has not used the device yet)
+  if (cudaSetDevice(dev) != cudaSuccess) return SPEC_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  unsigned long long ctx = 0;
+  const int rc = current_context_id(&ctx);
+  if (rc != SPEC_OK) return rc;
+  ScratchAddr &s = g_scratch_addr[dev];
+  if (s.addr == nullptr || s.ctx_id != ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return SPEC_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    s.addr = p;
+    s.ctx_id = ctx;
   }
-  *out = g_scratch_addr[dev];
+  *out = s.addr;
   return SPEC_OK;
 }
 }  // namespace

@@ -106,7 +106,7 @@ static TreeLayout tree_layout(int B) {
 // ------------------------------------------------------------------ setup
 // One block per tree. The tree's parent ids are staged in shared memory; one
 // thread derives depths in topological order, the block counts children and
-// checks tokens. The header was cleared before the launch; an invalid tree
+// checks tokens (in the vocabulary, distinct among drawn siblings). The header was cleared before the launch; an invalid tree
 // sets the status word and the walk of every tree is skipped.
 constexpr int SETUP_THREADS = 256;
 
@@ -154,6 +154,26 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
   if (ok && !s_bad)
     for (int c = t; c < ti.N; c += SETUP_THREADS)
       if (s_kids[c] > a.max_branch) s_bad = 1;
+  __syncthreads();
+  // drawn siblings carry distinct tokens (drawn without replacement); a
+  // point-mass child may repeat one. The child counts are no longer needed,
+  // so their array holds each node's token, -1 where the node is exempt.
+  if (ok && !s_bad)
+    for (int c = t; c < ti.N; c += SETUP_THREADS)
+      s_kids[c] = (c == 0 || (a.node_fixed != nullptr && a.node_fixed[ti.base + c] != 0))
+                      ? -1
+                      : a.node_token[ti.base + c];
+  __syncthreads();
+  if (ok && !s_bad)
+    for (int c = t + 1; c < ti.N; c += SETUP_THREADS) {
+      const int x = s_kids[c], p = s_par[c];
+      if (x < 0) continue;
+      for (int o = c - 1; o > p; --o)   // earlier siblings lie between the parent and c
+        if (s_par[o] == p && s_kids[o] == x) {
+          s_bad = 1;
+          break;
+        }
+    }
   __syncthreads();
   ok = ok && !s_bad;
   ti.mode = ok ? (greedy ? MODE_GREEDY : MODE_SAMPLE) : MODE_SKIP;

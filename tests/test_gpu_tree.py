@@ -100,13 +100,15 @@ def test_chain_tree_equals_linear_verifier_on_the_gpu(T):
     assert torch.equal(tok_t, tok_l)
 
 
-def test_full_size_tree_workload_on_sampled_trees():
+def test_full_size_tree_workload_whole_batch():
+    """Every tree of the full-size workload against the oracle: tokens,
+    accepted depth and path bit for bit up to the first flagged draw."""
     tb = S.make_tree(4, device=DEV)
     g = gpu_tree(tb)
     assert g["status"] == sv.SPEC_OK
-    req = np.arange(0, tb.B, 4)
-    r = oracle_tree(tb, requests=req)
-    assert_tree_parity(g, r, min_compared=len(req) - 2)
+    r = oracle_tree(tb)
+    assert len(r["requests"]) == tb.B
+    assert_tree_parity(g, r, min_compared=int((r["flag_slot"] < 0).sum()))
     assert np.all((g["accepted"] >= 0) & (g["accepted"] <= tb.max_depth))
 
 
@@ -122,6 +124,31 @@ def test_malformed_tree_sets_the_status_word():
                                           tb.cu_nodes, tb.temperature, 1, max_depth=3,
                                           max_branch=4)
     assert sv.spec_get_status(ws) == sv.SPEC_ERR_INVALID_ARG    # deeper than max_depth
+
+
+def test_repeated_drawn_sibling_sets_the_status_word():
+    """Drawn siblings carry distinct tokens (they were drawn without
+    replacement): a repeat is invalid input; a point-mass child may repeat a
+    drawn sibling's token."""
+    tb = S.make_tree(4, device=DEV, B=3, V=500, input_seed=5)
+    par = tb.parent.cpu().numpy()[:64]
+    kids = {}
+    for c in range(1, 64):
+        kids.setdefault(int(par[c]), []).append(c)
+    first, second = next(v for v in kids.values() if len(v) >= 2)[:2]
+    tok = tb.node_token.clone()
+    tok[second] = tok[first]
+    _, acc, _, ws = sv.spec_verify_tree(tb.target, tb.draft, tok, tb.parent, tb.cu_nodes,
+                                        tb.temperature, 1, max_depth=6, max_branch=4)
+    assert sv.spec_get_status(ws) == sv.SPEC_ERR_INVALID_ARG
+    assert torch.all(acc == -1)
+    nf = torch.zeros_like(tok)
+    nf[second] = 1                             # the repeat is a point mass: allowed
+    _, acc, _, ws = sv.spec_verify_tree(tb.target, tb.draft, tok, tb.parent, tb.cu_nodes,
+                                        tb.temperature, 1, max_depth=6, max_branch=4,
+                                        node_fixed=nf)
+    assert sv.spec_get_status(ws) == sv.SPEC_OK
+    assert torch.all(acc >= 0)
 
 
 def test_walk_reads_only_the_rows_of_visited_nodes():
@@ -194,6 +221,5 @@ def test_full_size_tree_workload_with_point_mass_children():
     nf = random_fixed(tb, 0.5, 4)
     g = gpu_tree(tb, node_fixed=nf)
     assert g["status"] == sv.SPEC_OK
-    req = np.arange(1, tb.B, 4)
-    assert_tree_parity(g, oracle_tree(tb, requests=req, node_fixed=nf),
-                       min_compared=len(req) - 2)
+    r = oracle_tree(tb, node_fixed=nf)
+    assert_tree_parity(g, r, min_compared=int((r["flag_slot"] < 0).sum()))
