@@ -50,15 +50,15 @@ FALLBACK_HBM_GBS = 6800.0
 # 460.19 MB read + 3.43 MB written (the per-chunk partial statistics).
 ROWPASS_TRAFFIC = {"source_sha1": "6f64b6019569898dcbfb786b84f81e6a98e4f7e3",
                    "dram_per_algorithmic_byte": (460192768 + 3425280) / 460089344}
-# The same for the streaming verifier (position-lazy schedule), per byte of
-# the rows the schedule must read (target rows 1..n+1, dense draft rows
-# 1..min(n+1, K) of sampling requests). Captured on the full B=1024, K=4,
-# V=201088 workload (one pass): 2708.1 MB read + 23.3 MB written for
-# 1975.1 MB; the excess is the residual rows read a second time and rows
-# read before a rejection made them unneeded, so the ratio holds for this
+# The same for the streaming verifier (position-lazy schedule, the plain
+# call's schedule on dense bf16 logits), per byte of the rows the schedule
+# must read (target rows 1..n+1, dense draft rows 1..min(n+1, K) of sampling
+# requests). Captured on the full B=1024, K=4, V=201088 workload (one pass):
+# 2643.7 MB read + 29.9 MB written for 1975.1 MB; the excess is the residual
+# rows read a second time (they miss L2), so the ratio holds for this
 # workload and source only.
-STREAM_TRAFFIC = {"source_sha1": "5017700c1d26c56531cf5112684a963d1e4d8325",
-                  "dram_per_algorithmic_byte": (2708053248 + 23286528) / 1975086336}
+STREAM_TRAFFIC = {"source_sha1": "00f57b9251426b7296dbf2ac5e3d82211de5284b",
+                  "dram_per_algorithmic_byte": (2643686912 + 29875200) / 1975086336}
 # The top-128 select (two passes, the second mostly from L2), per byte of
 # the draft rows; captured on the full B=256, K=7, V=151936 workload (one
 # pass): 556.56 MB read + 4.54 MB written for 544.54 MB. Valid for these
@@ -104,6 +104,11 @@ def parse(argv=None):
                     help="linear workloads: also emit the per-position KL(p || q)")
     ap.add_argument("--lazy", action="store_true",
                     help="linear workloads: position-lazy verification (rows 1..n+1 only)")
+    ap.add_argument("--eager", action="store_true",
+                    help="linear workloads: force the eager schedule (every row read)")
+    ap.add_argument("--resident", action="store_true",
+                    help="linear workloads: the cluster-resident position-lazy schedule "
+                         "(every needed row read once)")
     ap.add_argument("--rule", default="default", choices=["default", "cactus"],
                     help="linear workloads: the workload's lossless rule, or the relaxed "
                          "CACTUS rule with the recommended low-support guard")
@@ -265,15 +270,19 @@ def shape_config(cfg, rheo=False, B=None, V=None):
             "rule": "strict_top128" if w.get("top128") else "strict"}
 
 
-def linear_variant(config, rule, lazy, kl, ext):
+def linear_variant(config, rule, lazy, kl, ext, eager=False, resident=False):
     """The rule, schedule and output keys a linear call adds to its config."""
     c = dict(config)
     if ext is not None:
         c["rule"] = "cactus(alpha={alpha},max_rank={max_rank},min_prob={min_prob})".format(**ext)
     if kl:
         c["outputs"] = "tokens, counts and per-position KL(p || q)"
-    if lazy:
+    if resident:
+        c["schedule"] = "position-lazy, rows resident in a CTA cluster (each row read once)"
+    elif lazy:
         c["schedule"] = "position-lazy (rows 1..n+1 per request)"
+    elif eager:
+        c["schedule"] = "eager (every row read)"
     return c
 
 
@@ -307,18 +316,20 @@ class LinearWork:
     CACTUS = {"alpha": 0.5, "max_rank": 10, "min_prob": 0.10}
 
     def __init__(self, cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False,
-                 V=None):
+                 V=None, eager=False, resident=False, lb=None):
         import torch
         import speculative_decoding_rejection_gb300 as sv
         from speculative_decoding_rejection_gb300 import synthetic as S
         self.sv = sv
         self.cfg = cfg
-        self.lb = lb = S.make_linear(cfg, device=dev, input_seed=input_seed, **_overrides(B, V))
+        if lb is None:
+            lb = S.make_linear(cfg, device=dev, input_seed=input_seed, **_overrides(B, V))
+        self.lb = lb
         self.rule = sv.SPEC_RULE_STRICT_TOP128 if lb.top128 else sv.SPEC_RULE_STRICT
         self.ext = None
         if rule == "cactus":
             self.rule, self.ext = sv.SPEC_RULE_CACTUS, dict(self.CACTUS)
-        self.lazy = lazy
+        self.eager, self.resident_flag = eager, resident
         self.kl = (torch.empty(lb.draft_tokens.numel(), dtype=torch.float32, device=dev)
                    if kl else None)
         K = torch.diff(lb.cu_draft.cpu().long())
@@ -340,16 +351,28 @@ class LinearWork:
                      torch.empty(lb.B, dtype=torch.int32, device=dev), None)
         self.ws = torch.empty(sv.spec_verify_linear_workspace(lb.B, lb.max_k, lb.V, self.rule),
                               dtype=torch.uint8, device=dev)
-        self.config = linear_variant(shape_config(cfg, B=B, V=V), rule, lazy, kl, self.ext)
-        # the position-lazy schedule of dense bf16 logits (V % 8 == 0, no KL)
-        # runs as one persistent kernel: setup, streaming verifier, final draws
-        self.stream = (lazy and not lb.top128 and not kl and lb.V % 8 == 0
-                       and lb.target.dtype == torch.bfloat16)
+        self.config = linear_variant(shape_config(cfg, B=B, V=V), rule, lazy, kl, self.ext,
+                                     eager, resident)
+        # the library's schedule (include/specverify.h): dense bf16 logits
+        # with V % 8 == 0 and no KL stream position-lazily in one persistent
+        # kernel (setup, streaming verifier, final draws) when asked, and for
+        # a plain strict call without per-position outputs; the resident
+        # schedule (setup, one cluster kernel that also draws) when asked,
+        # under the strict rule with 16384 <= V <= 204800
+        bf16 = lb.target.dtype == torch.bfloat16
+        streamable = not lb.top128 and not kl and lb.V % 8 == 0 and bf16
+        self.resident = (resident and streamable and self.ext is None
+                         and 16384 <= lb.V <= 204800)
+        plain = not (lazy or resident or eager or kl) and self.ext is None
+        self.stream = streamable and not self.resident and (lazy or resident or plain)
+        lazy = lazy or resident or self.stream
+        self.lazy = lazy
         if lazy:
             # rounds: a row pass and a decision launch per position; around
             # them the setup, the top-128 select or the residual sums, and
             # the final draws
-            self.launches = 3 if self.stream else 3 + 2 * (lb.max_k + 1)
+            self.launches = (2 if self.resident else 3 if self.stream
+                             else 3 + 2 * (lb.max_k + 1))
         # small calls of the strict or greedy rule on dense logits or
         # probabilities run as one fused kernel (the library's own test:
         # rows of at most 8192 logits, at most 1 MiB of rows per request and
@@ -358,14 +381,18 @@ class LinearWork:
         sv.spec_set_fused_limit(limit)
         esz = lb.target.element_size()
         per_req = (lb.max_k + 1) * lb.V * esz + lb.max_k * lb.V * lb.draft.element_size()
-        self.fused = (not lazy and not kl and self.ext is None and not lb.top128
+        self.fused = (not (lazy or eager) and not kl and self.ext is None and not lb.top128
                       and lb.V <= 8192 and per_req <= 1 << 20 and lb.B * per_req <= limit)
         if self.fused:
             self.launches = 1
             self.kernel = "k_verify_small"
             self.config["schedule"] = "fused (one block per request)"
+            self.stream = self.lazy = False
+        elif self.stream and "schedule" not in self.config:
+            self.config["schedule"] = "position-lazy streaming (rows 1..n+1 per request)"
         if self.kernel is None:
-            self.kernel = ("k_verify_stream" if self.stream
+            self.kernel = ("k_verify_resident" if self.resident
+                           else "k_verify_stream" if self.stream
                            else "k_row_pass rounds with k_lazy_decide (one span)" if lazy
                            else "k_row_pass")
 
@@ -377,16 +404,25 @@ class LinearWork:
     def call(self, inputs=None):
         lb = self.lb
         t = inputs or self.input_tensors()
-        if self.ext is not None or self.lazy or self.kl is not None:
+        if (self.ext is not None or self.kl is not None or self.eager or self.resident_flag
+                or (self.lazy and not self.plain_call())):
             self.sv.spec_verify_linear_ext(t["target"], t["draft"], t["draft_tokens"],
                                            t["cu_draft"], t["temperature"], lb.seed,
                                            max_k=lb.max_k, rule=self.rule, workspace=self.ws,
-                                           out=self.outs + (None, self.kl), lazy=self.lazy,
+                                           out=self.outs + (None, self.kl),
+                                           lazy=self.lazy and not self.resident_flag,
+                                           resident=self.resident_flag, eager=self.eager,
                                            **(self.ext or {}))
             return
         self.sv.spec_verify_linear(t["target"], t["draft"], t["draft_tokens"], t["cu_draft"],
                                    t["temperature"], lb.seed, max_k=lb.max_k, rule=self.rule,
                                    workspace=self.ws, out=self.outs)
+
+    def plain_call(self):
+        """The workload's own call, spec_verify_linear without options (its
+        schedule is the library's choice)."""
+        return "schedule" not in self.config or self.config["schedule"].startswith(
+            ("position-lazy streaming", "fused"))
 
     def result_tensors(self):
         return [self.outs[0], self.outs[1]] + ([self.kl] if self.kl is not None else [])
@@ -601,12 +637,12 @@ class RheoWork:
 
 
 def make_work(cfg, dev, input_seed=None, B=None, rule=None, lazy=False, kl=False, rheo=False,
-              V=None):
+              V=None, eager=False, resident=False):
     if rheo:
         return RheoWork(dev, input_seed, B)
     if cfg == 4:
         return TreeWork(cfg, dev, input_seed, B)
-    return LinearWork(cfg, dev, input_seed, B, rule, lazy, kl, V)
+    return LinearWork(cfg, dev, input_seed, B, rule, lazy, kl, V, eager, resident)
 
 
 def cpu_baseline(work, n_units):
@@ -874,7 +910,8 @@ def main(argv=None):
         sv.spec_set_fused_limit(args.fused_limit)
     seed_base = S.INPUT_SEED_BASE + (0x100 if args.rheo else args.config)
     work = make_work(args.config, dev, input_seed=seed_base + 7919 * rank, B=args.B, V=args.V,
-                     rule=args.rule, lazy=args.lazy, kl=args.kl, rheo=args.rheo)
+                     rule=args.rule, lazy=args.lazy, kl=args.kl, rheo=args.rheo,
+                     eager=args.eager, resident=args.resident)
     unit = getattr(work, "unit", UNIT)
     t = timed_calls(work, sv, dev, args.steps, args.warmup, world)
     ms_step = t["ms_step"]
@@ -943,6 +980,16 @@ def main(argv=None):
         n = (args.cpu_requests if args.cpu_requests is not None
              else 16 if args.rheo else work.config["B"])
         line["cpu_baseline"], line["parity"] = parity_leg(work, n)
+    if isinstance(work, LinearWork) and work.stream and work.plain_call() and world == 1:
+        # the same inputs on the eager schedule (every row read), for comparison
+        ew = LinearWork(args.config, dev, eager=True, lb=work.lb)
+        te = timed_calls(ew, sv, dev, args.steps, args.warmup, world)
+        line["eager"] = {"schedule": ew.config["schedule"], "ms_per_step": te["ms_step"],
+                         "value": work.positions / (te["ms_step"] * 1e-3),
+                         "roofline": roofline(ew, te, args),
+                         "algorithmic_bytes_per_step": ew.tgt_bytes + ew.drf_bytes,
+                         "clocks": te["clocks"]}
+        del ew
     if world == 1 and not args.headline_only:
         # the other workloads, one after another on the same GPU
         del work

@@ -141,6 +141,13 @@ size_t spec_verify_linear_workspace(int B, int max_k, int V, int rule);
  *                skip.
  *   workspace    device scratch, >= spec_verify_linear_workspace(...) bytes,
  *                256-byte aligned, contents need no initialisation.
+ * Schedule: a call with out_pq NULL, draft logits, bf16 target and draft
+ * rows, V a multiple of 8 and rule SPEC_RULE_STRICT or SPEC_RULE_GREEDY
+ * runs the position-lazy streaming schedule (SPEC_EXT_LAZY below): a
+ * request's rows after its first rejection are not used, so a row there
+ * without a finite logit is not reported. Other calls read every row (the
+ * eager schedule); spec_verify_linear_ext with SPEC_EXT_EAGER forces it.
+ * Both give the same tokens and counts up to the rounding of the row sums.
  * Returns SPEC_OK or a negative spec_status.
  */
 int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
@@ -175,7 +182,8 @@ size_t spec_set_fused_limit(size_t bytes);
  *             SPEC_RULE_CACTUS only.
  *   min_prob  guard: reject d_i when p_i(d_i) < min_prob; 0 = off.
  *             SPEC_RULE_CACTUS only.
- *   flags     0 or SPEC_EXT_LAZY: position-lazy verification. Position
+ *   flags     0, SPEC_EXT_LAZY, SPEC_EXT_RESIDENT or SPEC_EXT_EAGER.
+ *             SPEC_EXT_LAZY: position-lazy verification. Position
  *             i is decided only when drafts 1..i-1 were accepted, so a
  *             request's decisions use rows 1..n+1 only (nalar.dev "Penolakan
  *             memendekkan pekerjaan speculative": proposals after a rejected
@@ -189,6 +197,20 @@ size_t spec_set_fused_limit(size_t bytes);
  *             run one row pass and one decision per position (max_k + 1
  *             rounds), read rows 1..n+1 only and do not check the tokens
  *             after n+1. The top-128 rule still cuts every draft row.
+ *             SPEC_EXT_RESIDENT: the position-lazy schedule with every
+ *             needed row read from HBM exactly once. A cluster of 8 CTAs
+ *             holds the current position's target and draft rows in shared
+ *             memory (1/8 each) while it decides, and draws the final token
+ *             from that copy. Same results as SPEC_EXT_LAZY. It reads fewer bytes
+ *             but waits on a cluster-wide exchange per position, so it is
+ *             slower on a GPU of its own (B = 1024, K = 4, V = 201088:
+ *             0.97 ms against 0.54 ms); it suits calls that share HBM with
+ *             other work. Takes the strict or greedy rule on dense bf16
+ *             logits with V a multiple of 8 and 16384 <= V <= 204800, and
+ *             no rank or KL output; other calls run as SPEC_EXT_LAZY.
+ *             SPEC_EXT_EAGER: read every row of every position (the
+ *             eager schedule), also where a plain call would take the
+ *             position-lazy one. Not combined with the other two.
  *   out_rank  optional device [R_d] int32: the target rank of every draft
  *             token (every request and rule; also after the first
  *             rejection unless lazy). NULL to skip.
@@ -211,6 +233,8 @@ size_t spec_set_fused_limit(size_t bytes);
  * requests (T < 0.05) keep the greedy rule.
  */
 #define SPEC_EXT_LAZY 1
+#define SPEC_EXT_RESIDENT 2
+#define SPEC_EXT_EAGER 4
 typedef struct {
   float alpha;
   int32_t max_rank;

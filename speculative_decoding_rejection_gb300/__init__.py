@@ -35,6 +35,8 @@ SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS, SPEC_DRAFT_SPARSE128 = 0, 1, 2
 SPEC_RULE_STRICT, SPEC_RULE_GREEDY, SPEC_RULE_STRICT_TOP128, SPEC_RULE_CACTUS = 0, 1, 2, 3
 SPEC_TOPK = 128
 SPEC_EXT_LAZY = 1
+SPEC_EXT_RESIDENT = 2
+SPEC_EXT_EAGER = 4
 SPEC_RHEO_MAX_CANDIDATES = 8192
 
 LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
@@ -199,11 +201,13 @@ def spec_verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed:
 def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, seed: int, *,
                            max_k: int, rule: int = SPEC_RULE_STRICT,
                            draft_kind: int = SPEC_DRAFT_LOGITS, draft_idx=None, alpha=0.0,
-                           max_rank=0, min_prob=0.0, lazy=False, want_pq=False,
-                           want_rank=False, want_kl=False, seed_dev=None, workspace=None, out=None,
-                           stream=None):
+                           max_rank=0, min_prob=0.0, lazy=False, resident=False, eager=False,
+                           want_pq=False, want_rank=False, want_kl=False, seed_dev=None,
+                           workspace=None, out=None, stream=None):
     """spec_verify_linear with the relaxed CACTUS rule's options and target
-    ranks.
+    ranks. `lazy`, `resident` and `eager` set SPEC_EXT_LAZY,
+    SPEC_EXT_RESIDENT and SPEC_EXT_EAGER (the schedules of
+    include/specverify.h).
 
     Returns (tokens, accepted, pq or None, rank [R_d] int32 or None,
     kl [R_d] f32 or None, workspace).
@@ -224,8 +228,10 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
         kl = torch.empty(draft_tokens.numel(), dtype=torch.float32, device=dev) if want_kl else None
     else:
         tokens, accepted, pq, rank, kl = out
-    ext = SpecLinearExt(float(alpha), int(max_rank), float(min_prob),
-                        SPEC_EXT_LAZY if lazy else 0, _ptr(rank), _ptr(kl), _ptr(seed_dev))
+    flags = ((SPEC_EXT_LAZY if lazy else 0) | (SPEC_EXT_RESIDENT if resident else 0)
+             | (SPEC_EXT_EAGER if eager else 0))
+    ext = SpecLinearExt(float(alpha), int(max_rank), float(min_prob), flags, _ptr(rank),
+                        _ptr(kl), _ptr(seed_dev))
     ddt = _dtype_code(draft) if draft is not None else SPEC_BF16
     code = lib().spec_verify_linear_ext(
         _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(draft_idx),

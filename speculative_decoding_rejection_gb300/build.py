@@ -17,7 +17,8 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = ROOT / "_build"
 LIB = PKG / "libspecverify.so"
-SOURCES = ["rowpass.cu", "linear.cu", "stream.cu", "small.cu", "topk.cu", "tree.cu", "rheo.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["rowpass.cu", "linear.cu", "stream.cu", "resident.cu", "small.cu", "topk.cu", "tree.cu",
+           "rheo.cu", "api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -15,7 +15,7 @@ constexpr int TILE_BYTES = 16384;   // one TMA bulk copy = one pipeline stage
 constexpr int LAZY_CHUNK_BYTES = 32768;
 constexpr int CHUNK_BYTES = 131072; // one unit of dynamic work in the row pass
 // The streaming verifier's unit of work: one completion count per chunk.
-constexpr int STREAM_CHUNK_BYTES = 262144;
+constexpr int STREAM_CHUNK_BYTES = 131072;
 // Row pass shape, chosen by measurement on GB300: six CTAs per SM, each one
 // producer lane and four consumer warps over a two-stage ring of 16 KB TMA
 // copies (192 KB of copies in flight per SM); a consumer thread takes eight

@@ -51,7 +51,7 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
   L.list = o; o += align256(sizeof(RowTask) * (size_t)std::max(L.rows_max, 2LL * B));
   // eager: one slot per listed row; lazy: two per request (its rows of the
   // current round), in finer chunks
-  L.nch_max_stream = nchunks(V, SPEC_F32, STREAM_CHUNK_BYTES);
+  L.nch_max_stream = nchunks(V, SPEC_BF16, STREAM_CHUNK_BYTES);   // bf16 rows only
   L.part = o;
   o += align256(sizeof(Part) * RS_CONS_WARPS *
                 std::max({(size_t)L.rows_max * L.nch_max, (size_t)2 * B * L.nch_max_lazy,
@@ -911,7 +911,9 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   if (ext != nullptr &&
       (!(ext->alpha >= 0.f) || !isfinite(ext->alpha) || ext->max_rank < 0 ||
        !(ext->min_prob >= 0.f) || !isfinite(ext->min_prob) ||
-       (ext->flags & ~SPEC_EXT_LAZY) != 0 || !aligned(ext->out_kl, 4) ||
+       (ext->flags & ~(SPEC_EXT_LAZY | SPEC_EXT_RESIDENT | SPEC_EXT_EAGER)) != 0 ||
+       ((ext->flags & SPEC_EXT_EAGER) && (ext->flags & ~SPEC_EXT_EAGER)) ||
+       !aligned(ext->out_kl, 4) ||
        !aligned(ext->out_rank, 4) || !aligned(ext->seed_dev, 8)))
     return SPEC_ERR_INVALID_ARG;
   if (dk == SPEC_DRAFT_SPARSE128 && (ddt != SPEC_F32 || draft_idx == nullptr || draft == nullptr))
@@ -959,7 +961,8 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
   a.d_row_bytes = dk == SPEC_DRAFT_SPARSE128 ? (long long)SPEC_TOPK * 4
                                              : (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
-  const bool lazy = ext && (ext->flags & SPEC_EXT_LAZY);
+  const int flags = ext ? ext->flags : 0;
+  const bool lazy = (flags & (SPEC_EXT_LAZY | SPEC_EXT_RESIDENT)) != 0;
   const bool want_kl = ext && ext->out_kl != nullptr;
   if (want_kl && (dk != SPEC_DRAFT_LOGITS || rule == SPEC_RULE_STRICT_TOP128 || tdt != ddt ||
                   ((long long)V * (tdt == SPEC_BF16 ? 2 : 4)) % 16 != 0))
@@ -979,7 +982,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.max_rank = ext ? ext->max_rank : 0;
   a.out_rank = ext ? ext->out_rank : nullptr;
   a.want_rank = a.out_rank != nullptr || (rule == SPEC_RULE_CACTUS && a.max_rank > 0);
-  a.lazy = ext && (ext->flags & SPEC_EXT_LAZY) ? 1 : 0;
+  a.lazy = lazy ? 1 : 0;
   a.want_kl = want_kl ? 1 : 0;
   a.out_kl = want_kl ? ext->out_kl : nullptr;
   a.kl_part = reinterpret_cast<float *>(ws + L.kl_part);
@@ -1008,8 +1011,19 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.cap_d = B;
   a.n_res_items = (a.ntiles + RES_TILES_PER_ITEM - 1) / RES_TILES_PER_ITEM;
   if (small_supported(a, ext)) return launch_verify_small(a, st);
-  if (stream_supported(a)) {
-    // partial slots by absolute row (as the eager schedule), 64 KB chunks
+  if ((flags & SPEC_EXT_RESIDENT) && resident_supported(a)) {
+    // position-lazy schedule with each position's rows resident on chip
+    // (setup, then one persistent cluster kernel that also draws)
+    a.lazy = 0;
+    return launch_verify_resident(a, st);
+  }
+  // the streaming schedule: asked for, or a plain call (no per-position
+  // outputs, no option) whose inputs it takes
+  const bool plain = !(flags & SPEC_EXT_EAGER) && out_pq == nullptr && !want_kl &&
+                     a.out_rank == nullptr && (rule == SPEC_RULE_STRICT || rule == SPEC_RULE_GREEDY);
+  if ((a.lazy || plain) && stream_supported(a)) {
+    // partial slots by absolute row (as the eager schedule), in the
+    // streaming verifier's chunks
     a.lazy = 0;
     a.chunk_bytes = STREAM_CHUNK_BYTES;
     a.nch_t = nchunks(V, tdt, a.chunk_bytes);

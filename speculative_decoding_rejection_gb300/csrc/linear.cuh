@@ -278,6 +278,13 @@ static __device__ void finish_request(const LinearArgs &a, int b, const ReqInfo 
 bool stream_supported(const LinearArgs &a);
 int launch_verify_stream(const LinearArgs &a, cudaStream_t stream);
 
+// The cluster-resident verifier (the position-lazy schedule with each
+// position's rows held in the shared memory of a CTA cluster, so every row
+// is read from HBM once) and the inputs it covers: the strict rule on dense
+// bf16 logits, V % 8 == 0, V in [16384, 204800], no rank or KL outputs.
+bool resident_supported(const LinearArgs &a);
+int launch_verify_resident(const LinearArgs &a, cudaStream_t stream);
+
 // The fused small-batch verifier (one kernel, one block per request) and the
 // calls it takes.
 bool small_supported(const LinearArgs &a, const spec_linear_ext *ext);

@@ -15,28 +15,30 @@
 //
 // How (GB300): the CTA shape of the TMA row pass (one producer lane and four
 // consumer warps over a two-stage ring of 16 KB bulk copies, six CTAs per
-// SM) over two work sources.
+// SM), plus one service warp, over two work sources.
 //   - The static list holds every position's rows in layer order: position 1
 //     of every request, then position 2, and so on, each row split into
 //     256 KB chunks. A producer skips a chunk of request b at position j once
 //     b is known to have rejected an earlier position; by the time a layer
 //     comes up the previous layer's decisions are mostly known, so the rows
 //     after a rejection are mostly never read.
-//   - Chunk ends are aggregated per CTA: each consumer warp leaves its
-//     partial in shared memory, and the last of the four publishes them and
-//     counts one completion of the position with a release atomic.
+//   - Rows are split in 128 KB chunks (smaller chunks measured slower; the
+//     residual's second read mostly misses L2 at every chunk size tried).
+//   - Chunk ends go to a service warp: each consumer warp leaves its partial
+//     in a shared-memory queue record and goes on streaming; the CTA's sixth
+//     warp publishes the four partials and counts one completion of the
+//     position with a release atomic, off the consumers' path.
 //   - A position is decided by whichever of two events comes second: its
 //     rows complete, or the previous position accepted (an atomic join). An
 //     acceptance whose next position is already complete decides that one
-//     too, in the same warp.
+//     too, in the same service warp.
 //   - A rejection of a sampling request appends its residual entry: the two
 //     rows just decided on, streamed once more as tile pairs whose sums of
 //     max(0, p - q) land in the job's tile-sum slots. Producers serve these
-//     entries first, so the re-read follows the first read as closely as the
-//     ring allows (on a batch of a thousand requests most of it still comes
-//     from HBM, as the row traffic shows). The final draws (these
-//     and the bonus draws) are queued as jobs for the final-draw kernel,
-//     which runs after this kernel as in the multi-launch schedule.
+//     entries first, so the re-read follows the first read closely. The
+//     final draws (these and the bonus draws) are queued as jobs for the
+//     final-draw kernel, which runs after this kernel as in the multi-launch
+//     schedule.
 // Partials written by other CTAs are read through L2 (ld.global.cg) after an
 // acquire; entries are published with a release store of their ready flag.
 // Every wait is bounded (2 s of %globaltimer): on expiry the status word
@@ -67,6 +69,14 @@ constexpr int F_DRAFT = 1 << 13;    // the draft tensor
 constexpr int F_RES = 1 << 14;      // a residual tile pair
 // bits 16-19 / 20-23: unaligned head / tail elements of the chunk
 
+// CTA of the streaming verifier: the producer warp (lane 0 issues copies),
+// four consumer warps, the service warp.
+constexpr int ST_SERVICE_WARP = 1 + RS_CONS_WARPS;
+constexpr int ST_THREADS = 32 * (2 + RS_CONS_WARPS);
+constexpr int ST_CTAS_PER_SM = 6;
+constexpr int ST_RANK_CTAS_PER_SM = 5;
+constexpr int NQ = 8;   // chunk-end records in flight per CTA
+
 struct StreamSmem {
   uint64_t full[NSTAGE];
   uint64_t empty[NSTAGE];
@@ -77,13 +87,15 @@ struct StreamSmem {
                        // residual: {request, items of the entry, job, first tile}
   float4 law[NSTAGE];  // residual stages: m_t, 1/S_t, m_d, 1/S_d
   float thr[NSTAGE];   // rank threshold of a target row (+inf: none)
-  // chunk ends: each consumer warp leaves its partial (row chunks) or its tile
-  // sums (residual items) in the slot of the chunk's last stage, double
-  // buffered by the parity of that stage's chunk-end count; the last of the
-  // four warps to count (in cend) publishes them
-  Part cp[NSTAGE][2][RS_CONS_WARPS];
-  float ct[NSTAGE][2][RS_CONS_WARPS][RES_TILES_PER_ITEM];
-  unsigned cend[NSTAGE];
+  // chunk-end queue, consumers to the service warp: record e sits in slot
+  // e % NQ; every consumer warp leaves its partial (row chunks) or its tile
+  // sums (residual items) there and arrives on qfull, the service warp
+  // arrives on qempty once it has taken the record
+  uint64_t qfull[NQ];
+  uint64_t qempty[NQ];
+  int4 qm0[NQ], qm1[NQ], qm2[NQ];   // the chunk's last stage's m0, m1, m2 (m0.x < 0: end)
+  Part qp[NQ][RS_CONS_WARPS];
+  float qt[NQ][RS_CONS_WARPS][RES_TILES_PER_ITEM];
   int abort;
   int skip;            // the setup rejected the inputs: no work
 };
@@ -128,45 +140,48 @@ __device__ __forceinline__ Job ldcg_job(const Job *j) {
 }
 
 // ------------------------------------------------------------------ setup
-// One thread per request: its record, its first rejection (none), its
-// position counters (position 0 needs no acceptance), its residual entry's
-// flag and count, and the draft tokens' logits z_t(d_i) (also the rank
-// count's threshold) and z_d(d_i), gathered once so a decision needs no
-// dependent load. Every draft token must be a vocabulary id (the eager
+// One thread per (request b, position j): position j's counters (position 0
+// needs no acceptance) and, for a draft position, the draft token's logits
+// z_t(d_j) (also the rank count's threshold) and z_d(d_j), gathered once so
+// a decision needs no dependent load; thread (b, 0) also writes the
+// request's record, its first rejection (none) and its residual entry's
+// flag and count. Every draft token must be a vocabulary id (the eager
 // schedule checks them all, so this one does too).
-__global__ void __launch_bounds__(64) k_setup_stream(const LinearArgs a) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= a.B) return;
+constexpr int SETUP_STREAM_THREADS = 128;
+
+__global__ void __launch_bounds__(SETUP_STREAM_THREADS) k_setup_stream(const LinearArgs a) {
   const int W = a.max_k + 1;
-  a.ready_d[b] = 0;
-  a.ready_d[a.cap_d + b] = 0;
-  a.rej_at[b] = INT_MAX;
-  for (int j = 0; j < W; ++j) {
-    a.pos_done[b * W + j] = 0;
-    a.pos_join[b * W + j] = j == 0;
-  }
+  const long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (g >= (long long)a.B * W) return;
+  const int b = (int)(g / W), j = (int)(g % W);
+  a.pos_done[g] = 0;
+  a.pos_join[g] = j == 0;
   ReqInfo r;
-  const bool ok = load_request(a, b, r);
-  a.req[b] = r;
-  if (!ok) {
-    a.hdr->setup_bad = 1;
+  const bool ok = load_request(a, b, r);   // every thread of b: the same record
+  if (j == 0) {
+    a.ready_d[b] = 0;
+    a.ready_d[a.cap_d + b] = 0;
+    a.rej_at[b] = INT_MAX;
+    a.req[b] = r;
+    if (!ok) a.hdr->setup_bad = 1;
+  }
+  if (!ok || j > r.K) return;
+  if (j == r.K) {
+    a.rank_thr[r.t0 + r.K] = INFINITY;
     return;
   }
   const bool drow = r.mode == MODE_SAMPLE && a.stream_draft;
-  for (int i = 0; i < r.K; ++i) {
-    const int d = a.tokens[r.d0 + i];
-    const bool dok = (unsigned)d < (unsigned)a.V;
-    if (!dok) {
-      set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-      a.hdr->setup_bad = 1;
-    }
-    a.rank_thr[r.t0 + i] =
-        dok ? load_elem(a.target + (long long)(r.t0 + i) * a.t_row_bytes, a.tdt, d) : INFINITY;
-    if (drow)
-      a.zd_at[r.d0 + i] =
-          dok ? load_elem(a.draft + (long long)(r.d0 + i) * a.d_row_bytes, a.ddt, d) : 0.f;
+  const int d = a.tokens[r.d0 + j];
+  const bool dok = (unsigned)d < (unsigned)a.V;
+  if (!dok) {
+    set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+    a.hdr->setup_bad = 1;
   }
-  a.rank_thr[r.t0 + r.K] = INFINITY;
+  a.rank_thr[r.t0 + j] =
+      dok ? load_elem(a.target + (long long)(r.t0 + j) * a.t_row_bytes, a.tdt, d) : INFINITY;
+  if (drow)
+    a.zd_at[r.d0 + j] =
+        dok ? load_elem(a.draft + (long long)(r.d0 + j) * a.d_row_bytes, a.ddt, d) : 0.f;
 }
 
 // --------------------------------------------------------------- producer
@@ -174,6 +189,33 @@ __device__ __forceinline__ bool acquire_stage(StreamSmem &sh, long long it, vola
   const int s = (int)(it % NSTAGE);
   const long long use = it / NSTAGE;
   return use == 0 || mbar_wait_bounded(&sh.empty[s], (uint32_t)((use - 1) & 1), abort);
+}
+
+// The producer's held ticket of the dynamic queue (residual items).
+struct DynTicket {
+  unsigned long long t, n;   // the ticket, and the number of tickets in all
+};
+
+__device__ bool issue_res_item(const LinearArgs &a, StreamSmem &sh, unsigned char *stage_buf,
+                               long long &it, volatile int *abort, const StreamEntry &E, int g);
+
+// Serves the held residual ticket if its entry is published (a relaxed poll,
+// then an acquire), and takes the next ticket. False when a wait gave up.
+__device__ __forceinline__ bool serve_ready_ticket(const LinearArgs &a, StreamSmem &sh,
+                                                   unsigned char *stage_buf, long long &it,
+                                                   volatile int *abort, DynTicket &dy,
+                                                   bool &served) {
+  served = false;
+  if (dy.t >= dy.n) return true;
+  const int e = (int)(dy.t / (unsigned)a.n_res_items);
+  if (!*(volatile int *)(a.ready_d + e)) return true;
+  fence_acquire();
+  const StreamEntry E = ldcg_entry(a.ent_d + e);
+  if (!issue_res_item(a, sh, stage_buf, it, abort, E, (int)(dy.t % (unsigned)a.n_res_items)))
+    return false;
+  dy.t = atomicAdd(&a.hdr->work_d, 1ull);
+  served = true;
+  return true;
 }
 
 // Streams chunk `chunk` of one row into the ring: its 16-byte aligned
@@ -410,53 +452,31 @@ __device__ __noinline__ void stream_decide(const LinearArgs &a, int b, int j, in
   }
 }
 
-// A consumer warp at the end of a chunk (row partial p) or a residual item
-// (tile sums rs) on stage slot s, before it releases the stage: it leaves its
-// result in the slot's buffer of parity `par` and counts itself in cend[s].
-// Counting before the release keeps the slot from being refilled, and so from
-// reaching its next chunk end, until all four warps have counted. Returns
-// true in every lane of the last warp to count: the closer.
-__device__ __forceinline__ bool chunk_end_count(StreamSmem &sh, int s, int par, int cw, int lane,
-                                                bool res, const Part &p,
-                                                const float (&rs)[RES_TILES_PER_ITEM]) {
-  unsigned old = 0;
-  if (lane == 0) {
-    if (res) {
-#pragma unroll
-      for (int t = 0; t < RES_TILES_PER_ITEM; ++t) sh.ct[s][par][cw][t] = rs[t];
-    } else {
-      sh.cp[s][par][cw] = p;
-    }
-    __threadfence_block();
-    old = atomicAdd(&sh.cend[s], 1u);
-  }
-  return (__shfl_sync(0xffffffffu, old, 0) & 3u) == 3u;
-}
-
-// The closer, after releasing the stage: the four warps' results to global
-// memory, one completion of the position's rows (or of the residual entry),
-// and, for the last completion, the position's join (its decision when the
-// previous position was accepted) or the end of the request. Only this warp
-// waits on global memory.
-__device__ __forceinline__ void chunk_close(const LinearArgs &a, StreamSmem &sh, int s, int par,
-                                            int lane, bool res, const int4 m0, const int4 m1,
-                                            const int4 m2) {
+// The service warp on chunk-end record q (a row chunk, or a residual item):
+// the four consumer warps' results to global memory, the record's slot back
+// to the consumers, one completion of the position's rows (or of the
+// residual entry), and, for the last completion, the position's join (its
+// decision when the previous position was accepted) or the end of the
+// request. Only this warp waits on global memory.
+__device__ __forceinline__ void service_record(const LinearArgs &a, StreamSmem &sh, int q,
+                                               int lane, const int4 m0, const int4 m1,
+                                               const int4 m2) {
+  const bool res = (m0.w & F_RES) != 0;
   int go = 0;
   if (lane == 0) {
-    __threadfence_block();
     int *count;
     if (res) {   // m2.z: job, m2.w: first tile, m1.w: tiles in the item
       for (int t = 0; t < m1.w; ++t)
         reinterpret_cast<float4 *>(a.tsum)[(long long)m2.z * a.ntiles + m2.w + t] =
-            make_float4(sh.ct[s][par][0][t], sh.ct[s][par][1][t], sh.ct[s][par][2][t],
-                        sh.ct[s][par][3][t]);
+            make_float4(sh.qt[q][0][t], sh.qt[q][1][t], sh.qt[q][2][t], sh.qt[q][3][t]);
       count = a.ready_d + a.cap_d + m2.x;   // the residual entry's own count
     } else {
       Part *dst = a.part + ((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS;
 #pragma unroll
-      for (int w = 0; w < RS_CONS_WARPS; ++w) dst[w] = sh.cp[s][par][w];
+      for (int w = 0; w < RS_CONS_WARPS; ++w) dst[w] = sh.qp[q][w];
       count = a.pos_done + m2.x * (a.max_k + 1) + (m2.z & 0xffff);
     }
+    mbar_arrive(&sh.qempty[q]);   // the record is in registers and global memory
     if (atom_add_release(count, 1) + 1 == m2.y) {
       fence_acquire();
       go = res ? 1 : join_second(a, m2.x, m2.z & 0xffff);
@@ -468,9 +488,38 @@ __device__ __forceinline__ void chunk_close(const LinearArgs &a, StreamSmem &sh,
                      __int_as_float(m1.x), lane);
 }
 
+// A consumer warp at chunk end e (row partial p, or residual tile sums rs):
+// waits until record slot e % NQ is free, leaves its result there (warp 0 of
+// the consumers also the stage's metadata) and arrives on the slot. False
+// when the wait gave up.
+__device__ __forceinline__ bool push_record(StreamSmem &sh, unsigned e, int cw, int lane,
+                                            volatile int *abort, bool res, const Part &p,
+                                            const float (&rs)[RES_TILES_PER_ITEM], const int4 m0,
+                                            const int4 m1, const int4 m2) {
+  const int q = (int)(e % NQ);
+  if (e >= NQ && !mbar_wait_bounded(&sh.qempty[q], (uint32_t)((e / NQ - 1) & 1), abort))
+    return false;
+  if (lane == 0) {
+    if (res) {
+#pragma unroll
+      for (int t = 0; t < RES_TILES_PER_ITEM; ++t) sh.qt[q][cw][t] = rs[t];
+    } else {
+      sh.qp[q][cw] = p;
+    }
+    if (cw == 0) {
+      sh.qm0[q] = m0;
+      sh.qm1[q] = m1;
+      sh.qm2[q] = m2;
+    }
+    mbar_arrive(&sh.qfull[q]);
+  }
+  __syncwarp();
+  return true;
+}
+
 // ------------------------------------------------------------------ kernel
 template <bool RANK>
-__global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM)
+__global__ void __launch_bounds__(ST_THREADS, RANK ? ST_RANK_CTAS_PER_SM : ST_CTAS_PER_SM)
     k_verify_stream(const LinearArgs a) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ StreamSmem sh;
@@ -481,8 +530,11 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], RS_CONS_WARPS);
     }
+    for (int q = 0; q < NQ; ++q) {
+      mbar_init(&sh.qfull[q], RS_CONS_WARPS);
+      mbar_init(&sh.qempty[q], 1);
+    }
     sh.abort = 0;
-    for (int q = 0; q < NSTAGE; ++q) sh.cend[q] = 0;
     // the setup's verdict (fixed before this kernel starts); errors found
     // while it runs go to the status word without stopping the other requests
     sh.skip = *(volatile int *)&a.hdr->setup_bad;
@@ -511,20 +563,15 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
         (unsigned long long)(a.max_k + 1) * (unsigned)a.B * (unsigned)a.stride;
     const unsigned long long n_dyn = (unsigned long long)a.cap_d * a.n_res_items;
     unsigned long long st_t = atomicAdd(&a.hdr->work_s, 1ull);
-    unsigned long long dy_t = atomicAdd(&a.hdr->work_d, 1ull);
+    DynTicket dy{atomicAdd(&a.hdr->work_d, 1ull), n_dyn};
     while (true) {
       // 1. the held residual ticket, once its entry exists
-      const int e = (int)(dy_t / (unsigned)a.n_res_items);
-      if (dy_t < n_dyn && ld_acquire(a.ready_d + e)) {
-        const StreamEntry E = ldcg_entry(a.ent_d + e);
-        if (!issue_res_item(a, sh, stage_buf, it, abort, E,
-                            (int)(dy_t % (unsigned)a.n_res_items))) {
-          ok = false;
-          break;
-        }
-        dy_t = atomicAdd(&a.hdr->work_d, 1ull);
-        continue;
+      bool served;
+      if (!serve_ready_ticket(a, sh, stage_buf, it, abort, dy, served)) {
+        ok = false;
+        break;
       }
+      if (served) continue;
       // 2. the static list meanwhile
       if (st_t < n_static) {
         const unsigned long long next = atomicAdd(&a.hdr->work_s, 1ull);
@@ -537,9 +584,10 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
       }
       // 3. nothing else: wait for the ticket's entry, the last request or an error
       // (1: entry ready, 2: every request finished, 3: give up)
+      const int e = (int)(dy.t / (unsigned)a.n_res_items);
       const int outcome = poll_bounded(
           [&]() -> int {
-            if (dy_t < n_dyn && ld_acquire(a.ready_d + e)) return 1;
+            if (dy.t < n_dyn && ld_acquire(a.ready_d + e)) return 1;
             if (*(volatile int *)&a.hdr->n_done >= a.B) return 2;
             if (*(volatile int *)&a.hdr->status == SPEC_ERR_TIMEOUT || *abort) return 3;
             return 0;
@@ -569,13 +617,27 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
     return;
   }
 
+  if (warp == ST_SERVICE_WARP) {
+    // ------------------------------------------------------------- service
+    for (unsigned e = 0;; ++e) {
+      const int q = (int)(e % NQ);
+      if (!mbar_wait_bounded(&sh.qfull[q], (uint32_t)((e / NQ) & 1), abort)) {
+        if (!*abort) set_status(a.hdr, SPEC_ERR_TIMEOUT, -4);
+        *abort = 1;
+        return;
+      }
+      const int4 m0 = sh.qm0[q];
+      if (m0.x < 0) return;   // the consumers reached the end marker
+      service_record(a, sh, q, lane, m0, sh.qm1[q], sh.qm2[q]);
+    }
+  }
+
   // -------------------------------------------------------------- consumers
-  static_assert(NSTAGE == 2, "chunk-end counters are kept per stage slot");
   const int cw = warp - 1;
   const int ctid = threadIdx.x - 32;
   RunState st{NO_MAX, pk2(0.f, 0.f), 0x7fffffff, 0, 0u};
   float rsum[RES_TILES_PER_ITEM] = {};
-  unsigned ends0 = 0, ends1 = 0;   // chunk ends seen on each stage slot
+  unsigned ends = 0;   // chunk-end records pushed (the same count in every consumer warp)
   for (long long it = 0;; ++it) {
     const int s = (int)(it % NSTAGE);
     if (!mbar_wait_bounded(&sh.full[s], (uint32_t)((it / NSTAGE) & 1), abort)) {
@@ -584,7 +646,10 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
       return;
     }
     const int4 m0 = sh.m0[s];
-    if (m0.x < 0) return;
+    if (m0.x < 0) {   // end of work: an end record tells the service warp
+      push_record(sh, ends, cw, lane, abort, false, Part{}, rsum, m0, m0, m0);
+      return;
+    }
     const int4 m1 = sh.m1[s];
     const int4 m2 = sh.m2[s];
     const unsigned char *buf = stage_buf + (size_t)s * TILE_BYTES;
@@ -618,29 +683,39 @@ __global__ void __launch_bounds__(RS_THREADS, RANK ? RS_RANK_CTAS_PER_SM : RS_CT
         p = finish_row_chunk<RANK>(st, c);
       }
     }
-    bool closer = false;
-    int par = 0;
-    if (last) {
-      unsigned &e = s ? ends1 : ends0;
-      par = (int)(e & 1u);
-      ++e;
-      closer = chunk_end_count(sh, s, par, cw, lane, res, p, rsum);
-    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
-    if (closer) chunk_close(a, sh, s, par, lane, res, m0, m1, m2);
+    if (last) {
+      if (!push_record(sh, ends, cw, lane, abort, res, p, rsum, m0, m1, m2)) {
+        if (!*abort) set_status(a.hdr, SPEC_ERR_TIMEOUT, -5);
+        *abort = 1;
+        return;
+      }
+      ++ends;
+    }
   }
 }
 
+// The streaming setup on its own (the cluster-resident verifier uses its
+// request records and gathered draft logits).
+int launch_setup_stream(const LinearArgs &a, cudaStream_t stream) {
+  const long long n_setup = (long long)a.B * (a.max_k + 1);
+  k_setup_stream<<<(unsigned)((n_setup + SETUP_STREAM_THREADS - 1) / SETUP_STREAM_THREADS),
+                   SETUP_STREAM_THREADS, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 bool stream_supported(const LinearArgs &a) {
-  return a.lazy && a.dk == SPEC_DRAFT_LOGITS && a.rule != SPEC_RULE_STRICT_TOP128 && !a.want_kl &&
+  return a.dk == SPEC_DRAFT_LOGITS && a.rule != SPEC_RULE_STRICT_TOP128 && !a.want_kl &&
          a.tdt == SPEC_BF16 && a.ddt == SPEC_BF16 && a.V % 8 == 0;
 }
 
 int launch_verify_stream(const LinearArgs &a, cudaStream_t stream) {
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
-  k_setup_stream<<<(a.B + 63) / 64, 64, 0, stream>>>(a);
+  const long long n_setup = (long long)a.B * (a.max_k + 1);
+  k_setup_stream<<<(unsigned)((n_setup + SETUP_STREAM_THREADS - 1) / SETUP_STREAM_THREADS),
+                   SETUP_STREAM_THREADS, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   const size_t smem = (size_t)NSTAGE * TILE_BYTES;
   auto kern = a.want_rank ? k_verify_stream<true> : k_verify_stream<false>;
@@ -650,7 +725,7 @@ int launch_verify_stream(const LinearArgs &a, cudaStream_t stream) {
   cudaEvent_t before, after;
   take_row_pass_events(&before, &after);
   if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  kern<<<(a.want_rank ? RS_RANK_CTAS_PER_SM : RS_CTAS_PER_SM) * sms, RS_THREADS, smem, stream>>>(a);
+  kern<<<(a.want_rank ? ST_RANK_CTAS_PER_SM : ST_CTAS_PER_SM) * sms, ST_THREADS, smem, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;

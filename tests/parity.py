@@ -17,24 +17,29 @@ PROB_ATOL = 1e-30
 
 
 def gpu_linear(lb, rule=sv.SPEC_RULE_STRICT, draft_kind=sv.SPEC_DRAFT_LOGITS, draft=None,
-               draft_idx=None, ext=None, lazy=False, kl=False, rank=True):
-    """Runs the CUDA verifier; `ext` (a dict of alpha / max_rank / min_prob)
-    or `lazy` goes through spec_verify_linear_ext, which also returns target
-    ranks unless `rank` is False."""
+               draft_idx=None, ext=None, lazy=False, kl=False, rank=True, resident=False,
+               eager=False, plain=False):
+    """Runs the CUDA verifier; `ext` (a dict of alpha / max_rank / min_prob),
+    `lazy`, `resident` or `eager` go through spec_verify_linear_ext, which
+    also returns target ranks unless `rank` is False. `plain` calls
+    spec_verify_linear without p(d), q(d) (the library picks the schedule);
+    the other plain calls ask for them."""
     draft = lb.draft if draft is None else draft
-    if ext is None and not lazy and not kl:
+    if ext is None and not (lazy or kl or resident or eager):
         tokens, acc, pq, ws = sv.spec_verify_linear(
             lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
-            max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx, want_pq=True)
+            max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx,
+            want_pq=not plain)
         rank = None
     else:
         tokens, acc, pq, rank, klv, ws = sv.spec_verify_linear_ext(
             lb.target, draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
             max_k=lb.max_k, rule=rule, draft_kind=draft_kind, draft_idx=draft_idx,
-            want_pq=True, want_rank=rank, want_kl=kl, lazy=lazy, **(ext or {}))
+            want_pq=True, want_rank=rank, want_kl=kl, lazy=lazy, resident=resident,
+            eager=eager, **(ext or {}))
     status = sv.spec_get_status(ws)
     out = dict(tokens=tokens.cpu().numpy(), accepted=acc.cpu().numpy(),
-               pq=pq.cpu().numpy().astype(np.float64), status=status)
+               pq=None if pq is None else pq.cpu().numpy().astype(np.float64), status=status)
     if rank is not None:
         out["rank"] = rank.cpu().numpy().astype(np.int64)
     if kl:
@@ -79,7 +84,7 @@ def assert_linear_parity(gpu, ref, cu_draft, min_compared=1):
             n_flag += 1
         rows.extend(range(int(cu[b]), int(cu[b + 1])))
     rows = np.asarray(rows, dtype=np.int64)
-    if rows.size:
+    if rows.size and gpu["pq"] is not None:
         assert_probs_close(gpu["pq"][rows], ref["pq"][rows], "p(d), q(d)")
         if "rank" in gpu:   # integer counts: bit-exact
             bad = gpu["rank"][rows] != ref["rank"][rows]

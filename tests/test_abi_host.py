@@ -44,12 +44,16 @@ def test_workspace_sizes():
 FAKE = 1 << 20   # a 256-byte-aligned non-null value; never dereferenced
 
 
-def lin(L, **kw):
+def lin_args(**kw):
     args = dict(target=FAKE, tdt=1, draft=FAKE, ddt=1, dk=0, draft_idx=None, tokens=FAKE,
                 cu=FAKE, temp=FAKE, B=4, V=1000, max_k=4, seed=1, rule=0, out_tokens=FAKE,
                 out_acc=FAKE, out_pq=None, ws=FAKE, ws_bytes=1 << 30, stream=None)
     args.update(kw)
-    return L.spec_verify_linear(*args.values())
+    return args
+
+
+def lin(L, **kw):
+    return L.spec_verify_linear(*lin_args(**kw).values())
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -74,6 +78,19 @@ def lin(L, **kw):
 ])
 def test_linear_rejects_bad_arguments_on_the_host(L, kw, code):
     assert lin(L, **kw) == code
+
+
+@pytest.mark.parametrize("flags", [sv.SPEC_EXT_EAGER | sv.SPEC_EXT_LAZY,
+                                   sv.SPEC_EXT_EAGER | sv.SPEC_EXT_RESIDENT, 8, -1])
+def test_linear_ext_rejects_bad_schedule_flags_on_the_host(L, flags):
+    """The eager schedule combines with neither position-lazy one; unknown
+    flag bits are invalid. Nothing is launched (the pointers are fake)."""
+    import ctypes
+    ext = sv.SpecLinearExt(0.0, 0, 0.0, flags, None, None, None)
+    a = lin_args()
+    code = L.spec_verify_linear_ext(*list(a.values())[:14], ctypes.byref(ext),
+                                    *list(a.values())[14:])
+    assert code == sv.SPEC_ERR_INVALID_ARG
 
 
 def test_topk_rejects_bad_arguments_on_the_host(L):

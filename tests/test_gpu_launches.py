@@ -14,7 +14,9 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 
 CASES = [
-    ("eager", dict(cfg=5, B=64)),
+    ("plain call (streaming)", dict(cfg=5, B=64)),
+    ("eager", dict(cfg=5, B=64, eager=True)),
+    ("resident", dict(cfg=5, B=64, resident=True)),
     ("top-128", dict(cfg=3, B=16)),
     ("fused", dict(cfg=1)),
     ("stream", dict(cfg=5, B=64, lazy=True)),

@@ -211,6 +211,12 @@ def test_full_size_workloads_whole_batch(cfg):
     if cfg == 5:   # greedy requests are never flagged
         greedy = lb.temperature.cpu().numpy() < 0.05
         assert greedy.any() and np.all(r["flag_slot"][greedy] < 0)
+        # the plain call (no p(d), q(d)) takes the position-lazy streaming
+        # schedule: the same parity on the whole batch
+        p = gpu_linear(lb, rule=rule, plain=True)
+        assert p["status"] == sv.SPEC_OK and p["pq"] is None
+        assert np.array_equal(p["accepted"], g["accepted"])
+        assert_linear_parity(p, r, lb.cu_draft.cpu(), min_compared=unflagged)
     # whole-batch invariants
     acc = g["accepted"]
     K = np.diff(lb.cu_draft.cpu().numpy())
@@ -388,14 +394,14 @@ def test_cactus_argument_errors():
 
 
 # ---------------------------------------------- position-lazy verification
-def assert_lazy_matches(g, ref, lb):
+def assert_lazy_matches(g, ref, lb, min_compared=10):
     """Tokens and counts as the oracle; p(d), q(d) and ranks on the read
     positions, NaN / -1 exactly on the unread ones."""
     lz = O.lazy_view(ref, lb.cu_draft.cpu().numpy())
     assert np.array_equal(np.isnan(g["pq"][:, 0]), np.isnan(lz["pq"][:, 0]))
     if "rank" in g:
         assert np.array_equal(g["rank"] == -1, lz["rank"] == -1)
-    assert_linear_parity(g, lz, lb.cu_draft.cpu(), min_compared=10)
+    assert_linear_parity(g, lz, lb.cu_draft.cpu(), min_compared=min_compared)
 
 
 LAZY_CASES = [
@@ -476,6 +482,60 @@ def test_stream_schedule_full_size_workload5_whole_batch():
     unflagged = int((ref["flag_slot"] < 0).sum())
     n_full, n_flag = assert_linear_parity(g, lz, lb.cu_draft.cpu(), min_compared=unflagged)
     print(f"{n_full} requests compared in full, {n_flag} flagged")
+
+
+# The cluster-resident schedule (SPEC_EXT_RESIDENT): strict rule, dense bf16
+# logits, 16384 <= V <= 204800. Fewer requests than clusters, ragged and
+# empty drafts, greedy and sampling requests, the smallest and largest V,
+# slices of unequal length (V / 8 not a multiple of 8).
+RESIDENT_CASES = [
+    dict(B=1, K=4, V=16384, sigma=0.8, T=1.0),
+    dict(B=40, K=(0, 6), V=65536, sigma=0.9, T=[0.0, 0.5, 1.0, 1.5] * 10),
+    dict(B=16, K=3, V=204800, sigma=1.0, T=0.9),
+    dict(B=24, K=(1, 5), V=30008, sigma=0.4, T=[0.7, 0.02, 1.2] * 8),
+    dict(B=70, K=4, V=201088, sigma=1.3, T=0.8),
+]
+
+
+@pytest.mark.parametrize("over", RESIDENT_CASES)
+def test_resident_schedule_equals_eager_and_the_oracle(over):
+    lb = S.make_linear(2, device=DEV, input_seed=6161, dtype="bf16", **over)
+    g = gpu_linear(lb, resident=True, rank=False)
+    assert g["status"] == sv.SPEC_OK
+    e = gpu_linear(lb, eager=True, rank=False)
+    same = (g["tokens"] == e["tokens"]).all(1)
+    assert np.array_equal(g["accepted"], e["accepted"])
+    ref = oracle_linear(lb)
+    for b in np.nonzero(~same)[0]:   # the schedules sum rows in different orders
+        assert ref["flag_slot"][b] >= 0, ("differs from eager on an unflagged draw", b)
+    assert_lazy_matches(g, ref, lb, min_compared=int((ref["flag_slot"] < 0).sum()))
+    again = gpu_linear(lb, resident=True, rank=False)   # bitwise deterministic
+    assert np.array_equal(again["tokens"], g["tokens"])
+    assert np.array_equal(again["pq"], g["pq"], equal_nan=True)
+
+
+def test_resident_schedule_full_size_workload5_whole_batch():
+    """B = 1024, K = 4, V = 201088: every request against the oracle."""
+    lb = S.make_linear(5, device=DEV)
+    g = gpu_linear(lb, resident=True, rank=False)
+    assert g["status"] == sv.SPEC_OK
+    ref = oracle_linear(lb)
+    lz = O.lazy_view(ref, lb.cu_draft.cpu().numpy())
+    unflagged = int((ref["flag_slot"] < 0).sum())
+    n_full, n_flag = assert_linear_parity(g, lz, lb.cu_draft.cpu(), min_compared=unflagged)
+    print(f"resident: {n_full} requests compared in full, {n_flag} flagged")
+
+
+def test_resident_schedule_reports_invalid_inputs():
+    lb = S.make_linear(2, device=DEV, B=6, K=3, V=16384, dtype="bf16", T=1.0, input_seed=3)
+    assert gpu_linear(lb, resident=True, rank=False)["status"] == sv.SPEC_OK
+    bad = lb.draft_tokens.clone()
+    bad[4] = lb.V                               # a draft token outside the vocabulary
+    b2 = S.LinearBatch(**{**lb.__dict__, "draft_tokens": bad})
+    g = gpu_linear(b2, resident=True, rank=False)
+    assert g["status"] == sv.SPEC_ERR_INVALID_ARG
+    assert np.all(g["accepted"] == -1)
+    assert gpu_linear(lb, resident=True, rank=False)["status"] == sv.SPEC_OK
 
 
 def test_stream_schedule_invalid_inputs_and_empty_rows():
