@@ -84,7 +84,9 @@ typedef enum {
   SPEC_ERR_UNSUPPORTED = -2, /* valid but outside this build's limits        */
   SPEC_ERR_WORKSPACE = -3,   /* workspace NULL, misaligned or too small      */
   SPEC_ERR_CUDA = -4,        /* a CUDA runtime call failed                   */
-  SPEC_ERR_TIMEOUT = -5      /* a bounded device-side wait ran out           */
+  SPEC_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out           */
+  SPEC_ERR_BOUNDS = -6       /* checked build only: an access outside the
+                                call's buffers (detail: its source line)     */
 } spec_status;
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
@@ -459,6 +461,22 @@ int spec_get_status(const void *workspace, spec_stream_t stream,
 int spec_uniforms(uint64_t seed, const int32_t *b, const int32_t *pos,
                   const int32_t *stream_id, int n, float *out,
                   spec_stream_t stream);
+
+/*
+ * Self-test of the bounds-checked build (libspecverify_checked.so, built
+ * with SPEC_CHECKED; no counterpart on the pages: a test aid). That build
+ * checks every global access of the kernels against the byte ranges of the
+ * call's buffers (inputs, outputs, workspace), skips an access outside them
+ * (a load gives 0, a store or copy is dropped) and reports it in the status
+ * word as SPEC_ERR_BOUNDS, with the source line of the access as detail.
+ * This call registers only the first 256 bytes of `workspace` (at least 512
+ * bytes, 256-byte aligned, caller-owned) and reads the word after them, so
+ * the status word then reads SPEC_ERR_BOUNDS; no memory outside the
+ * workspace is touched. Calls that overlap on the device share the checked
+ * build's range lists and must be ordered. The product library returns
+ * SPEC_ERR_UNSUPPORTED.
+ */
+int spec_check_selftest(void *workspace, size_t ws_bytes, spec_stream_t stream);
 
 /*
  * Self-test of the device-side bounded waits (failure detection without a

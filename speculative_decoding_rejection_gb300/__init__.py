@@ -21,7 +21,7 @@ __all__ = [
     "spec_verify_tree_workspace", "spec_verify_tree_ext", "draft_topk_softmax",
     "draft_topk_softmax_workspace", "spec_get_status", "spec_uniforms",
     "spec_profile_row_pass", "spec_rheo_expand", "spec_rheo_expand_workspace",
-    "spec_set_fused_limit", "SpecError",
+    "spec_set_fused_limit", "SpecError", "use_checked_library", "spec_check_selftest",
 ]
 
 SPEC_OK = 0
@@ -30,6 +30,7 @@ SPEC_ERR_UNSUPPORTED = -2
 SPEC_ERR_WORKSPACE = -3
 SPEC_ERR_CUDA = -4
 SPEC_ERR_TIMEOUT = -5
+SPEC_ERR_BOUNDS = -6
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS, SPEC_DRAFT_SPARSE128 = 0, 1, 2
 SPEC_RULE_STRICT, SPEC_RULE_GREEDY, SPEC_RULE_STRICT_TOP128, SPEC_RULE_CACTUS = 0, 1, 2, 3
@@ -40,9 +41,14 @@ SPEC_EXT_EAGER = 4
 SPEC_RHEO_MAX_CANDIDATES = 8192
 
 LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
+# The same library built with SPEC_CHECKED: every global access of the
+# kernels checked against the call's buffers (include/specverify.h,
+# SPEC_ERR_BOUNDS); a test build.
+CHECKED_LIB_PATH = Path(__file__).resolve().parent / "libspecverify_checked.so"
 HEADER = Path(__file__).resolve().parent.parent / "include" / "specverify.h"
 
 _lib = None
+_lib_path = LIB_PATH
 _vp, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
 class SpecLinearExt(ctypes.Structure):
     """spec_linear_ext of include/specverify.h."""
@@ -78,6 +84,7 @@ _SIGS = {
     "spec_uniforms": (_i32, [_u64, _vp, _vp, _vp, _i32, _vp, _vp]),
     "spec_profile_row_pass": (_i32, [_vp, _vp]),
     "spec_wait_selftest": (_i32, [_i32, ctypes.c_ulonglong, _vp, _vp]),
+    "spec_check_selftest": (_i32, [_vp, _sz, _vp]),
     "spec_verify_linear_noalloc": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32,
                                           _i32, _i32, _u64, _i32, _vp, _vp, _vp, _vp, _vp]),
 }
@@ -89,14 +96,24 @@ class SpecError(RuntimeError):
         self.code = code
 
 
+def use_checked_library(on: bool) -> None:
+    """Routes every call of this module to the bounds-checked build (on) or
+    to the product library (off). The first call after a switch loads the
+    chosen library."""
+    global _lib, _lib_path
+    path = CHECKED_LIB_PATH if on else LIB_PATH
+    if path != _lib_path:
+        _lib_path, _lib = path, None
+
+
 def lib() -> ctypes.CDLL:
     """The loaded C library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not LIB_PATH.exists():
-            raise RuntimeError(f"{LIB_PATH.name} is not built; run "
+        if not _lib_path.exists():
+            raise RuntimeError(f"{_lib_path.name} is not built; run "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
-        L = ctypes.CDLL(str(LIB_PATH))
+        L = ctypes.CDLL(str(_lib_path))
         for name, (res, args) in _SIGS.items():
             fn = getattr(L, name)
             fn.restype = res
@@ -379,6 +396,17 @@ def spec_wait_selftest(kind: int, limit_ns: int, workspace=None, stream=None):
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda") if workspace is None else workspace
     _check(lib().spec_wait_selftest(int(kind), ctypes.c_ulonglong(limit_ns), _ptr(ws),
                                     _stream(stream)), "spec_wait_selftest")
+    return ws
+
+
+def spec_check_selftest(workspace=None, stream=None):
+    """Runs the bounds-checked build's self-test (use_checked_library(True)
+    first); returns the 512-byte workspace, whose status word then reads
+    SPEC_ERR_BOUNDS. The product library raises SPEC_ERR_UNSUPPORTED."""
+    torch = _torch()
+    ws = torch.zeros(512, dtype=torch.uint8, device="cuda") if workspace is None else workspace
+    _check(lib().spec_check_selftest(_ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream)),
+           "spec_check_selftest")
     return ws
 
 

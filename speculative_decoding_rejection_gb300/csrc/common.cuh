@@ -54,6 +54,84 @@ struct WsHeader {        // first 256 bytes of every workspace
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
+// ------------------------------------------------------- checked build
+// Built with SPEC_CHECKED (libspecverify_checked.so), every global access
+// of the kernels goes through the accessors below, which check it against
+// the byte ranges of the buffers of the call being run (its inputs,
+// outputs and workspace). An access outside them is skipped (a load gives
+// zero, a store or a copy is dropped, a skipped bulk copy still completes
+// its barrier's transaction) and reported in the status word as
+// SPEC_ERR_BOUNDS with the source line of the access as detail; nothing
+// traps. The entry point lists the call's ranges (check_begin, check_add)
+// and every launcher copies the list to its translation unit's device copy
+// before its kernels (check_upload). Without SPEC_CHECKED the accessors are
+// the plain accesses.
+constexpr int CHECK_RANGES = 24;
+struct CheckTable {
+  int n;
+  WsHeader *hdr;                           // the call's status word
+  unsigned long long lo[CHECK_RANGES];     // byte ranges [lo, hi)
+  unsigned long long hi[CHECK_RANGES];
+};
+#ifdef SPEC_CHECKED
+static __device__ CheckTable g_check;   // this translation unit's copy
+static __device__ __noinline__ bool gchk_slow(unsigned long long lo, unsigned long long hi, int line) {
+  for (int i = 0; i < g_check.n; ++i)
+    if (lo >= g_check.lo[i] && hi <= g_check.hi[i]) return true;
+  WsHeader *h = g_check.hdr;
+  if (h != nullptr && atomicCAS(&h->status, 0, SPEC_ERR_BOUNDS) == 0) atomicExch(&h->detail, line);
+  return false;
+}
+__device__ __forceinline__ bool gchk(const void *p, unsigned long long bytes, int line) {
+  const unsigned long long lo = (unsigned long long)p;
+  return gchk_slow(lo, lo + bytes, line);
+}
+#else
+__device__ __forceinline__ bool gchk(const void *, unsigned long long, int) { return true; }
+#endif
+// Checked global accesses: plain load, non-coherent load, L2-only load,
+// store, and a range test for atomics and copies.
+template <class T>
+__device__ __forceinline__ T gld(const T *p, int line) {
+  return gchk(p, sizeof(T), line) ? *p : T{};
+}
+template <class T>
+__device__ __forceinline__ T gldg(const T *p, int line) {
+  return gchk(p, sizeof(T), line) ? __ldg(p) : T{};
+}
+template <class T>
+__device__ __forceinline__ T gldcg(const T *p, int line) {
+  return gchk(p, sizeof(T), line) ? __ldcg(p) : T{};
+}
+template <class T, class U>
+__device__ __forceinline__ void gst(T *p, const U &v, int line) {
+  if (gchk(p, sizeof(T), line)) *p = v;
+}
+#ifdef SPEC_CHECKED
+CheckTable &host_check_table();   // the list of the call being set up (this host thread)
+void check_begin(WsHeader *hdr);
+void check_add(const void *p, unsigned long long bytes);
+// This translation unit's device copy of the list, before its kernels.
+static inline int check_upload(cudaStream_t st) {
+  return cudaMemcpyToSymbolAsync(g_check, &host_check_table(), sizeof(CheckTable), 0,
+                                 cudaMemcpyHostToDevice, st) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+// A device int (the row count cu[B] that sizes a call's buffers), read
+// synchronously: the checked build is a test build.
+int check_read_int(const int32_t *dev, cudaStream_t st, int *out);
+#else
+static inline int check_upload(cudaStream_t) { return SPEC_OK; }
+static inline void check_begin(WsHeader *) {}
+static inline void check_add(const void *, unsigned long long) {}
+#endif
+#define GLD(p) ::sv::gld((p), __LINE__)
+#define GLDG(p) ::sv::gldg((p), __LINE__)
+#define GLDCG(p) ::sv::gldcg((p), __LINE__)
+#define GST(p, ...) ::sv::gst((p), (__VA_ARGS__), __LINE__)
+#define GCHK(p, n) ::sv::gchk((p), (n), __LINE__)
+
 struct RowTask {         // one row (or row pair) streamed by the row pass
   int slot;              // index into the partial-statistics array
   int row;               // row index within its tensor
@@ -96,7 +174,7 @@ struct RowStat { float m, S; int idx; };
 // A chunk partial read through L2 only: in the streaming verifier it was
 // written by another CTA of the same running kernel.
 __device__ __forceinline__ Part ldcg_part(const Part *p) {
-  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
+  const int4 v = GLDCG(reinterpret_cast<const int4 *>(p));
   return Part{__int_as_float(v.x), __int_as_float(v.y), v.z, v.w};
 }
 
@@ -109,6 +187,7 @@ __device__ __forceinline__ bool row_empty(float m) { return !(m > NO_MAX); }
 __device__ __forceinline__ void set_status(WsHeader *h, int code, int detail) {
   if (atomicCAS(&h->status, 0, code) == 0) atomicExch(&h->detail, detail);
 }
+
 
 // ------------------------------------------------------ counter uniforms
 // SplitMix64 output function (Steele, Lea & Flood 2014) of x + gamma.
@@ -178,10 +257,10 @@ __device__ __forceinline__ uint32_t bgt2(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ float load_elem(const void *row, int dtype, long long i) {
   if (dtype == SPEC_BF16) {
-    const uint16_t v = __ldg(reinterpret_cast<const unsigned short *>(row) + i);
+    const uint16_t v = GLDG(reinterpret_cast<const unsigned short *>(row) + i);
     return __uint_as_float((uint32_t)v << 16);
   }
-  return __ldg(reinterpret_cast<const float *>(row) + i);
+  return GLDG(reinterpret_cast<const float *>(row) + i);
 }
 
 __device__ __forceinline__ int dtype_size(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
@@ -246,7 +325,7 @@ __device__ __forceinline__ void load_ept(const char *row, int dt, bool vec_ok, i
       const uint4 *p = reinterpret_cast<const uint4 *>(row + 2LL * x0);
 #pragma unroll
       for (int q = 0; q < SAMPLE_EPT / 8; ++q) {
-        const uint4 w = __ldg(p + q);
+        const uint4 w = GLDG(p + q);
         z[8 * q + 0] = bf16lo(w.x); z[8 * q + 1] = bf16hi(w.x);
         z[8 * q + 2] = bf16lo(w.y); z[8 * q + 3] = bf16hi(w.y);
         z[8 * q + 4] = bf16lo(w.z); z[8 * q + 5] = bf16hi(w.z);
@@ -256,7 +335,7 @@ __device__ __forceinline__ void load_ept(const char *row, int dt, bool vec_ok, i
       const uint4 *p = reinterpret_cast<const uint4 *>(row + 4LL * x0);
 #pragma unroll
       for (int q = 0; q < SAMPLE_EPT / 4; ++q) {
-        const uint4 w = __ldg(p + q);
+        const uint4 w = GLDG(p + q);
         z[4 * q + 0] = __uint_as_float(w.x); z[4 * q + 1] = __uint_as_float(w.y);
         z[4 * q + 2] = __uint_as_float(w.z); z[4 * q + 3] = __uint_as_float(w.w);
       }
@@ -401,13 +480,19 @@ __device__ __forceinline__ int poll_bounded(Check check, int timeout, unsigned l
 __device__ __forceinline__ void prefetch_l2(const void *p, long long bytes) {
   const uintptr_t a0 = ((uintptr_t)p + 15) & ~(uintptr_t)15;
   const uintptr_t a1 = ((uintptr_t)p + (uintptr_t)bytes) & ~(uintptr_t)15;
-  if (a1 > a0)
+  if (a1 > a0 && GCHK((const void *)a0, a1 - a0))
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"((uint32_t)(a1 - a0))
                  : "memory");
 }
 
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
                                         uint64_t *bar) {
+  if (!GCHK(src, bytes)) {   // checked build: the copy is dropped, its bytes still count
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+    return;
+  }
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),

@@ -90,53 +90,51 @@ __global__ void __launch_bounds__(64) k_setup_linear(const LinearArgs a) {
   if (gtid == 0) a.hdr->n_list = a.lazy ? 2 * a.B : (int)a.rows_max;
   const long long dmax = a.rows_max - a.rt_max;
   if (!a.lazy) {
-    const long long Rd = a.B > 0 ? min(max((long long)a.cu[a.B], 0LL), dmax) : 0;
+    const long long Rd = a.B > 0 ? min(max((long long)GLD(a.cu + (a.B)), 0LL), dmax) : 0;
     const long long Rt = min(Rd + a.B, (long long)a.rt_max);
-    for (long long p = Rt + gtid; p < a.rt_max; p += gsize) a.list[p].slot = -1;
-    for (long long p = a.rt_max + Rd + gtid; p < a.rows_max; p += gsize) a.list[p].slot = -1;
+    for (long long p = Rt + gtid; p < a.rt_max; p += gsize) GST(&a.list[p].slot, -1);
+    for (long long p = a.rt_max + Rd + gtid; p < a.rows_max; p += gsize) GST(&a.list[p].slot, -1);
   }
   const int b = gtid;
   if (b >= a.B) return;
   if (a.lazy) {   // idle until the request validates
-    a.list[b].slot = -1;
-    a.list[a.B + b].slot = -1;
+    GST(&a.list[b].slot, -1);
+    GST(&a.list[a.B + b].slot, -1);
   }
   ReqInfo r;
   if (!load_request(a, b, r)) {
-    a.req[b] = r;
+    GST(a.req + (b), r);
     return;
   }
   const int K = r.K;
-  a.req[b] = r;
+  GST(a.req + (b), r);
   const bool drafts = r.mode == MODE_SAMPLE && a.stream_draft;
   // with KL, a draft row travels with its target row as one pair entry
   const bool pairs = drafts && a.want_kl;
   if (a.lazy) {
     if (pairs && K > 0) {
-      a.list[b] = RowTask{b, r.t0, ROW_PAIR, r.c, a.B + b, r.d0};
-      a.list[a.B + b].slot = -1;
+      GST(a.list + (b), RowTask{b, r.t0, ROW_PAIR, r.c, a.B + b, r.d0});
+      GST(&a.list[a.B + b].slot, -1);
     } else {
-      a.list[b] = RowTask{b, r.t0, 0, r.c};
-      a.list[a.B + b] = RowTask{drafts && K > 0 ? a.B + b : -1, r.d0, 1, r.c};
+      GST(a.list + (b), RowTask{b, r.t0, 0, r.c});
+      GST(a.list + (a.B + b), RowTask{drafts && K > 0 ? a.B + b : -1, r.d0, 1, r.c});
     }
   } else {
     for (int i = 0; i <= K; ++i)
-      a.list[r.t0 + i] = pairs && i < K
+      GST(a.list + (r.t0 + i), pairs && i < K
                              ? RowTask{r.t0 + i, r.t0 + i, ROW_PAIR, r.c, a.rt_max + r.d0 + i, r.d0 + i}
-                             : RowTask{r.t0 + i, r.t0 + i, 0, r.c};
+                             : RowTask{r.t0 + i, r.t0 + i, 0, r.c});
     for (int i = 0; i < K; ++i)
-      a.list[a.rt_max + r.d0 + i] =
-          RowTask{drafts && !pairs ? a.rt_max + r.d0 + i : -1, r.d0 + i, 1, r.c};
+      GST(a.list + (a.rt_max + r.d0 + i), RowTask{drafts && !pairs ? a.rt_max + r.d0 + i : -1, r.d0 + i, 1, r.c});
   }
   if (a.want_rank) {   // threshold of the rank count: the draft token's target logit
     for (int i = 0; i < K; ++i) {
-      const int d = a.tokens[r.d0 + i];
-      a.rank_thr[r.t0 + i] =
-          (unsigned)d < (unsigned)a.V
+      const int d = GLD(a.tokens + (r.d0 + i));
+      GST(a.rank_thr + (r.t0 + i), (unsigned)d < (unsigned)a.V
               ? load_elem(a.target + (long long)(r.t0 + i) * a.t_row_bytes, a.tdt, d)
-              : INFINITY;   // reported by the accept scan
+              : INFINITY);   // reported by the accept scan
     }
-    a.rank_thr[r.t0 + K] = INFINITY;
+    GST(a.rank_thr + (r.t0 + K), INFINITY);
   }
 }
 
@@ -206,11 +204,11 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
   int32_t *out = a.out_tokens + (long long)b * W;
   // inputs rejected by the setup (or an expired wait): no request is verified
   if (*(volatile int *)&a.hdr->status != SPEC_OK) {
-    for (int j = lane; j < W; j += 32) out[j] = -1;
-    if (lane == 0) a.out_accepted[b] = -1;
+    for (int j = lane; j < W; j += 32) GST(out + j, -1);
+    if (lane == 0) GST(a.out_accepted + (b), -1);
     return;
   }
-  const ReqInfo r = a.req[b];
+  const ReqInfo r = GLD(a.req + (b));
   const int K = r.K;
   const float c = r.c;
   const bool sample = r.mode == MODE_SAMPLE;
@@ -229,7 +227,7 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
     int d = -1;
     float zt = 0.f, zq = 0.f;
     if (lane < cnt) {
-      d = a.tokens[r.d0 + i];
+      d = GLD(a.tokens + (r.d0 + i));
       if (dense && (unsigned)d < (unsigned)a.V) {
         zt = load_elem(a.target + (long long)(r.t0 + i) * a.t_row_bytes, a.tdt, d);
         zq = load_elem(a.draft + (long long)(r.d0 + i) * a.d_row_bytes, a.ddt, d);
@@ -273,7 +271,7 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
         }
       }
     }
-    if (a.out_kl && lane < cnt) a.out_kl[r.d0 + base + lane] = kl;
+    if (a.out_kl && lane < cnt) GST(a.out_kl + (r.d0 + base + lane), kl);
     // (a sparse law's q(d) is searched by each lane for its own position: the
     // positions' searches run side by side)
     const bool rej =
@@ -308,16 +306,16 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
   const int W = a.max_k + 1;
   int32_t *out = a.out_tokens + (long long)b * W;
   if (*(volatile int *)&a.hdr->status != SPEC_OK) {
-    for (int j = lane; j < W; j += 32) out[j] = -1;
+    for (int j = lane; j < W; j += 32) GST(out + j, -1);
     if (lane == 0) {
-      a.out_accepted[b] = -1;
-      a.list[b].slot = -1;
-      a.list[a.B + b].slot = -1;
+      GST(a.out_accepted + (b), -1);
+      GST(&a.list[b].slot, -1);
+      GST(&a.list[a.B + b].slot, -1);
     }
     return;
   }
-  if (a.list[b].slot < 0) return;   // finished in an earlier round
-  const ReqInfo r = a.req[b];
+  if (GLD(&a.list[b].slot) < 0) return;   // finished in an earlier round
+  const ReqInfo r = GLD(a.req + (b));
   const int K = r.K, j = a.round;
   const float c = r.c;
   const bool sample = r.mode == MODE_SAMPLE;
@@ -330,10 +328,10 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
     if (a.out_kl) {
       const float kl = sample && a.stream_draft ? warp_pair_kl(a, tslot(a, r, b, j), ds, c, lane)
                                                 : __int_as_float(0x7fc00000);
-      if (lane == 0) a.out_kl[r.d0 + j] = kl;
+      if (lane == 0) GST(a.out_kl + (r.d0 + j), kl);
     }
     // a sparse draft's q(d): the warp searches the row's 128 ids together
-    const float qs = sample && a.sparse ? warp_sparse_q(a, r.d0 + j, a.tokens[r.d0 + j], lane)
+    const float qs = sample && a.sparse ? warp_sparse_q(a, r.d0 + j, GLD(a.tokens + (r.d0 + j)), lane)
                                         : -1.f;
     const bool rej = __shfl_sync(
         0xffffffffu, lane == 0 && position_rejects(a, b, r, j, sample, ts, ds, rank, qs), 0);
@@ -341,11 +339,11 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
       if (lane == 0) {
         const bool drow = sample && a.stream_draft && j + 1 < K;
         if (drow && a.want_kl) {
-          a.list[b] = RowTask{b, r.t0 + j + 1, ROW_PAIR, c, a.B + b, r.d0 + j + 1};
-          a.list[a.B + b].slot = -1;
+          GST(a.list + (b), RowTask{b, r.t0 + j + 1, ROW_PAIR, c, a.B + b, r.d0 + j + 1});
+          GST(&a.list[a.B + b].slot, -1);
         } else {
-          a.list[b] = RowTask{b, r.t0 + j + 1, 0, c};
-          a.list[a.B + b] = RowTask{drow ? a.B + b : -1, r.d0 + j + 1, 1, c};
+          GST(a.list + (b), RowTask{b, r.t0 + j + 1, 0, c});
+          GST(a.list + (a.B + b), RowTask{drow ? a.B + b : -1, r.d0 + j + 1, 1, c});
         }
       }
       return;
@@ -356,15 +354,15 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_lazy_decide(const LinearA
   // positions after n+1 were never read
   for (int i = n + 1 + lane; i < K; i += 32) {
     if (a.out_pq) {
-      a.out_pq[2LL * (r.d0 + i)] = __int_as_float(0x7fc00000);
-      a.out_pq[2LL * (r.d0 + i) + 1] = __int_as_float(0x7fc00000);
+      GST(a.out_pq + (2LL * (r.d0 + i)), __int_as_float(0x7fc00000));
+      GST(a.out_pq + (2LL * (r.d0 + i) + 1), __int_as_float(0x7fc00000));
     }
-    if (a.out_rank) a.out_rank[r.d0 + i] = -1;
-    if (a.out_kl) a.out_kl[r.d0 + i] = __int_as_float(0x7fc00000);
+    if (a.out_rank) GST(a.out_rank + (r.d0 + i), -1);
+    if (a.out_kl) GST(a.out_kl + (r.d0 + i), __int_as_float(0x7fc00000));
   }
   if (lane == 0) {
-    a.list[b].slot = -1;
-    a.list[a.B + b].slot = -1;
+    GST(&a.list[b].slot, -1);
+    GST(&a.list[a.B + b].slot, -1);
   }
 }
 
@@ -454,7 +452,7 @@ __device__ __forceinline__ void load_raw_ept(const char *row, int dt, bool vec_o
   const uint4 *p = reinterpret_cast<const uint4 *>(row + (long long)esz * x0);
 #pragma unroll
   for (int k = 0; k < SAMPLE_EPT / 4; ++k)
-    if (k < SAMPLE_EPT * esz / 16) r.v[k] = __ldg(p + k);
+    if (k < SAMPLE_EPT * esz / 16) r.v[k] = GLDG(p + k);
 }
 // The logits of a RawEpt, as load_ept gives them.
 __device__ __forceinline__ void raw_to_z(const RawEpt &r, const char *row, int dt, bool vec_ok,
@@ -521,7 +519,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_tiles(const LinearArg
     if (item >= n_items) return;
     const int ja = (int)(item / ipj);
     const int j0 = (int)(item % ipj) * TILES_PER_ITEM;
-    const Job job = a.jobs_a[ja];
+    const Job job = GLD(a.jobs_a + (ja));
     const JobRows q = job_rows(a, job);
     const int xa = j0 * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
     const bool fast = DK == SPEC_DRAFT_LOGITS && a.tdt == SPEC_BF16 && a.ddt == SPEC_BF16 &&
@@ -534,8 +532,8 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_tiles(const LinearArg
       for (int u = 0; u < TILES_PER_ITEM; ++u) {
         const uint4 *pt = reinterpret_cast<const uint4 *>(q.trow + 2LL * (xa + u * SAMPLE_TILE));
         const uint4 *pd = reinterpret_cast<const uint4 *>(q.drow + 2LL * (xa + u * SAMPLE_TILE));
-        rt[u][0] = __ldg(pt); rt[u][1] = __ldg(pt + 1);
-        rd[u][0] = __ldg(pd); rd[u][1] = __ldg(pd + 1);
+        rt[u][0] = GLDG(pt); rt[u][1] = GLDG(pt + 1);
+        rd[u][0] = GLDG(pd); rd[u][1] = GLDG(pd + 1);
       }
 #pragma unroll
       for (int u = 0; u < TILES_PER_ITEM; ++u) {
@@ -555,8 +553,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_tiles(const LinearArg
         }
         const float t = block_sum(s, sh);
         if (threadIdx.x < RS_CONS_WARPS)
-          a.tsum[((long long)ja * a.ntiles + j0 + u) * RS_CONS_WARPS + threadIdx.x] =
-              threadIdx.x == 0 ? t : 0.f;
+          GST(a.tsum + (((long long)ja * a.ntiles + j0 + u) * RS_CONS_WARPS + threadIdx.x), threadIdx.x == 0 ? t : 0.f);
       }
     } else {
       for (int u = 0; u < TILES_PER_ITEM && j0 + u < a.ntiles; ++u) {
@@ -573,8 +570,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_tiles(const LinearArg
         }
         const float t = block_sum(s, sh);
         if (threadIdx.x < RS_CONS_WARPS)
-          a.tsum[((long long)ja * a.ntiles + j0 + u) * RS_CONS_WARPS + threadIdx.x] =
-              threadIdx.x == 0 ? t : 0.f;
+          GST(a.tsum + (((long long)ja * a.ntiles + j0 + u) * RS_CONS_WARPS + threadIdx.x), threadIdx.x == 0 ? t : 0.f);
       }
     }
   }
@@ -621,7 +617,7 @@ __device__ int fine_draw(const LinearArgs &a, SampleSmem &sh, const JobRows &q, 
 template <int DK, bool BATCH>
 __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, const JobRows &q,
                           int kind, float u) {
-  const ReqInfo r = a.req[job.b];
+  const ReqInfo r = GLD(a.req + (job.b));
   const int esz = dtype_size(a.tdt);
   const int chunk_elems = a.chunk_bytes / esz;
   const int tpc = chunk_elems / SAMPLE_TILE;  // tiles per chunk
@@ -630,7 +626,7 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
   for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
     float m = 0.f;
     for (int w = 0; w < RS_CONS_WARPS; ++w) {
-      const Part p = pp[ch * RS_CONS_WARPS + w];
+      const Part p = GLD(pp + ch * RS_CONS_WARPS + w);
       m += p.S * ex2((p.m - q.mt) * q.c);
     }
     sh.corr[ch] = m * q.invSt;   // chunk mass of p
@@ -757,7 +753,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArg
   const int nb = *(volatile int *)&a.hdr->n_jobs_b;
   if (g >= na + nb) return;
   const bool dense = g < na;
-  const Job job = dense ? a.jobs_a[g] : a.jobs_b[g - na];
+  const Job job = dense ? GLD(a.jobs_a + (g)) : GLD(a.jobs_b + (g - na));
   const JobRows q = job_rows(a, job);
   const float u = uniform24(seed_of(a), (uint32_t)job.b, (uint32_t)(job.n + 1), job.kind == 1 ? 1u : 2u);
   int x = -1;
@@ -767,7 +763,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArg
     const float *ts4 = a.tsum + (long long)g * a.ntiles * RS_CONS_WARPS;
     for (int j = threadIdx.x; j < a.ntiles; j += blockDim.x) {
       float t = 0.f;
-      for (int w = 0; w < RS_CONS_WARPS; ++w) t += ts4[j * RS_CONS_WARPS + w];
+      for (int w = 0; w < RS_CONS_WARPS; ++w) t += GLD(ts4 + j * RS_CONS_WARPS + w);
       sh.corr[j] = t;
     }
     __syncthreads();
@@ -797,14 +793,14 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArg
     }
     // no residual mass (p == q): the same u draws from p
   } else if (DK == SPEC_DRAFT_SPARSE128 && job.kind == 1) {
-    const ReqInfo r = a.req[job.b];
+    const ReqInfo r = GLD(a.req + (job.b));
     const int t = threadIdx.x;
     if (t < SPEC_TOPK) {   // the row's sparse law, sorted by id (bitonic)
       const long long row = (long long)(r.d0 + job.n) * SPEC_TOPK + t;
-      const int id = a.draft_idx[row];
+      const int id = GLD(a.draft_idx + (row));
       const bool ok = id >= 0 && id < a.V;
       sh.s_idx[t] = ok ? id : 0x7fffffff;
-      sh.s_prob[t] = ok ? a.sparse_prob[row] : 0.f;
+      sh.s_prob[t] = ok ? GLD(a.sparse_prob + (row)) : 0.f;
     }
     __syncthreads();
     // the internal top-128 returns its ids ascending (-1 padding last); a
@@ -839,7 +835,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) k_sample_final(const LinearArg
     x = chunk_draw<DK, JOBS == SAMPLE_JOBS_B>(a, sh, job, q, 2, u);
   if (threadIdx.x == 0) {
     if (x < 0) set_status(a.hdr, SPEC_ERR_INVALID_ARG, job.b);   // a row without mass
-    a.out_tokens[(long long)job.b * (a.max_k + 1) + job.n] = x;
+    GST(a.out_tokens + ((long long)job.b * (a.max_k + 1) + job.n), x);
   }
 }
 
@@ -1002,6 +998,28 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
 
   if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
+#ifdef SPEC_CHECKED
+  {   // the call's buffers, sized by its row count cu_draft[B]
+    int Rd = 0;
+    if (check_read_int(cu_draft + B, st, &Rd) != SPEC_OK) return SPEC_ERR_CUDA;
+    const long long rd = Rd > 0 ? Rd : 0;
+    check_begin(a.hdr);
+    check_add(workspace, L.total);
+    check_add(target, (rd + B) * a.t_row_bytes);
+    check_add(draft, rd * a.d_row_bytes);
+    check_add(draft_idx, rd * SPEC_TOPK * 4);
+    check_add(draft_tokens, rd * 4);
+    check_add(cu_draft, (B + 1) * 4ull);
+    check_add(temperature, B * 4ull);
+    check_add(out_tokens, (unsigned long long)B * (max_k + 1) * 4);
+    check_add(out_accepted, B * 4ull);
+    check_add(out_pq, rd * 8);
+    check_add(a.out_rank, rd * 4);
+    check_add(a.out_kl, rd * 4);
+    check_add(a.seed_dev, 8);
+  }
+#endif
+  if (check_upload(st) != SPEC_OK) return SPEC_ERR_CUDA;
   a.ent_d = reinterpret_cast<StreamEntry *>(ws + L.ent_d);
   a.ready_d = reinterpret_cast<int *>(ws + L.ready_d);
   a.pos_done = reinterpret_cast<int *>(ws + L.pos_done);

@@ -76,21 +76,22 @@ struct LinearArgs {
 // The call's seed: from device memory when the caller gave a pointer (so a
 // captured CUDA graph draws new uniforms after the caller writes a new seed).
 __device__ __forceinline__ uint64_t seed_of(const LinearArgs &a) {
-  return a.seed_dev != nullptr ? __ldg(a.seed_dev) : a.seed;
+  return a.seed_dev != nullptr ? GLDG(a.seed_dev) : a.seed;
 }
 
 __device__ __forceinline__ bool load_request(const LinearArgs &a, int b, ReqInfo &r) {
-  const int K = a.cu[b + 1] - a.cu[b];
-  const float T = a.temp[b];
+  const int cb = GLD(a.cu + b), cb1 = GLD(a.cu + b + 1);
+  const int K = cb1 - cb;
+  const float T = GLD(a.temp + b);
   const long long dmax = a.rows_max - a.rt_max;
-  r.t0 = a.cu[b] + b;
-  r.d0 = a.cu[b];
+  r.t0 = cb + b;
+  r.d0 = cb;
   r.K = K;
   r.n = 0;
   r.pad[0] = r.pad[1] = 0;
   const bool greedy = a.rule == SPEC_RULE_GREEDY || T < SPEC_GREEDY_T;
-  bool ok = (b > 0 || a.cu[0] == 0) && K >= 0 && K <= a.max_k && a.cu[b] >= 0 &&
-            (long long)a.cu[b + 1] <= dmax && T >= 0.f && isfinite(T);
+  bool ok = (b > 0 || cb == 0) && K >= 0 && K <= a.max_k && cb >= 0 &&
+            (long long)cb1 <= dmax && T >= 0.f && isfinite(T);
   if (ok && !greedy && a.draft == nullptr) ok = false;
   if (!ok) {
     set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
@@ -142,7 +143,7 @@ __device__ __forceinline__ float warp_pair_kl(const LinearArgs &a, int tslot_, c
   int idx = 0x7fffffff;
   for (int i = lane; i < n; i += 32) {
     const Part q = ldcg_part(a.part + base + i);
-    merge_stat_a(m, S, idx, A, q.m, q.S, q.idx, __ldcg(a.kl_part + base + i), c);
+    merge_stat_a(m, S, idx, A, q.m, q.S, q.idx, GLDCG(a.kl_part + base + i), c);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -163,7 +164,7 @@ static __device__ float draft_prob_at(const LinearArgs &a, int row, int d, float
     const int32_t *ids = a.draft_idx + (long long)row * SPEC_TOPK;
     const float *pr = a.sparse_prob + (long long)row * SPEC_TOPK;
     for (int k = 0; k < SPEC_TOPK; ++k)
-      if (ids[k] == d) return pr[k];
+      if (GLD(ids + k) == d) return GLD(pr + k);
     return 0.f;
   }
   const char *drow = a.draft + (long long)row * a.d_row_bytes;
@@ -178,8 +179,8 @@ static __device__ float draft_prob_at(const LinearArgs &a, int row, int d, float
 __device__ __forceinline__ float warp_sparse_q(const LinearArgs &a, int row, int d, int lane) {
   const long long base = (long long)row * SPEC_TOPK;
   for (int k0 = 0; k0 < SPEC_TOPK; k0 += 32) {
-    const unsigned m = __ballot_sync(0xffffffffu, a.draft_idx[base + k0 + lane] == d);
-    if (m) return a.sparse_prob[base + k0 + __ffs(m) - 1];
+    const unsigned m = __ballot_sync(0xffffffffu, GLD(a.draft_idx + base + k0 + lane) == d);
+    if (m) return GLD(a.sparse_prob + base + k0 + __ffs(m) - 1);
   }
   return 0.f;
 }
@@ -222,10 +223,10 @@ static __device__ bool position_rejects_z(const LinearArgs &a, int b, const ReqI
     rej = true;
   }
   if (a.out_pq) {
-    a.out_pq[2LL * (r.d0 + i)] = pd;
-    a.out_pq[2LL * (r.d0 + i) + 1] = qd;
+    GST(a.out_pq + 2LL * (r.d0 + i), pd);
+    GST(a.out_pq + 2LL * (r.d0 + i) + 1, qd);
   }
-  if (a.out_rank) a.out_rank[r.d0 + i] = rank;
+  if (a.out_rank) GST(a.out_rank + r.d0 + i, rank);
   return rej;
 }
 
@@ -234,7 +235,7 @@ static __device__ bool position_rejects_z(const LinearArgs &a, int b, const ReqI
 static __device__ bool position_rejects(const LinearArgs &a, int b, const ReqInfo &r, int i,
                                         bool sample, const RowStat &ts, const RowStat &ds,
                                         int rank, float q_given = -1.f) {
-  const int d = a.tokens[r.d0 + i];
+  const int d = GLD(a.tokens + r.d0 + i);
   const bool dok = (unsigned)d < (unsigned)a.V;
   float zt = 0.f, zq = 0.f;
   bool q_is_prob = true;
@@ -259,16 +260,16 @@ static __device__ void finish_request(const LinearArgs &a, int b, const ReqInfo 
                                const RowStat &tf, const RowStat &df, int lane) {
   const int W = a.max_k + 1;
   int32_t *out = a.out_tokens + (long long)b * W;
-  for (int j = lane; j < W; j += 32) out[j] = j < n ? a.tokens[r.d0 + j] : -1;
+  for (int j = lane; j < W; j += 32) GST(out + j, j < n ? GLD(a.tokens + r.d0 + j) : -1);
   __syncwarp();
   if (lane == 0) {
-    a.out_accepted[b] = n;
+    GST(a.out_accepted + b, n);
     if (!sample) {
-      out[n] = tf.idx;
+      GST(out + n, tf.idx);
     } else {
       const Job j{b, n, n < r.K ? 1 : 2, 0, tf.m, tf.S, df.m, df.S};
-      if (j.kind == 1 && !a.sparse) a.jobs_a[atomicAdd(&a.hdr->n_jobs_a, 1)] = j;
-      else a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = j;
+      if (j.kind == 1 && !a.sparse) GST(a.jobs_a + atomicAdd(&a.hdr->n_jobs_a, 1), j);
+      else GST(a.jobs_b + atomicAdd(&a.hdr->n_jobs_b, 1), j);
     }
   }
 }
@@ -298,7 +299,7 @@ struct JobRows {
 };
 
 __device__ __forceinline__ JobRows job_rows(const LinearArgs &a, const Job &j) {
-  const ReqInfo r = a.req[j.b];
+  const ReqInfo r = GLD(a.req + j.b);
   JobRows q;
   q.trow = a.target + (long long)(r.t0 + j.n) * a.t_row_bytes;
   q.tvec = ((uintptr_t)q.trow & 15) == 0;

@@ -325,8 +325,8 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
     const int W = a.max_k + 1;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)a.B * W;
          i += (long long)gridDim.x * blockDim.x) {
-      a.out_tokens[i] = -1;
-      if (i < a.B) a.out_accepted[i] = -1;
+      GST(a.out_tokens + (i), -1);
+      if (i < a.B) GST(a.out_accepted + (i), -1);
     }
     cluster.sync();
     return;
@@ -346,7 +346,7 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
 
   int b = cid;   // the first request of this cluster; then the leader's picks
   ReqInfo r{};
-  if (b < a.B) r = a.req[b];
+  if (b < a.B) r = GLD(a.req + (b));
   while (b < a.B && !failed) {
     const bool sample = r.mode == MODE_SAMPLE;
     const float c = r.c;
@@ -368,9 +368,9 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
       int d = -1, nxt = -1;
       float zt = 0.f, zd = 0.f;
       if (j < r.K) {
-        d = __ldg(a.tokens + r.d0 + j);
-        zt = __ldcg(a.rank_thr + r.t0 + j);
-        if (need_d) zd = __ldcg(a.zd_at + r.d0 + j);
+        d = GLDG(a.tokens + r.d0 + j);
+        zt = GLDCG(a.rank_thr + r.t0 + j);
+        if (need_d) zd = GLDCG(a.zd_at + r.d0 + j);
       }
       if (threadIdx.x == 0 && j == 0 && rank == 0)
         nxt = ncl + (int)atomicAdd(&a.hdr->work, 1u);
@@ -436,7 +436,7 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
       }
       if (j == 0) {
         next = sh.msg[par][0].next;
-        if (next < a.B) rn = a.req[next];   // early: used after this request
+        if (next < a.B) rn = GLD(a.req + (next));   // early: used after this request
       }
       if (j == r.K) {
         n = j;
@@ -461,8 +461,8 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
       if (rank == 0 && threadIdx.x == 0) {
         if (!dok || row_empty(ts.m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
         if (a.out_pq) {
-          a.out_pq[2LL * (r.d0 + j)] = pdv;
-          a.out_pq[2LL * (r.d0 + j) + 1] = qdv;
+          GST(a.out_pq + (2LL * (r.d0 + j)), pdv);
+          GST(a.out_pq + (2LL * (r.d0 + j) + 1), qdv);
         }
       }
       if (rej) {
@@ -476,15 +476,15 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
     if (rank == 0) {
       int32_t *out = a.out_tokens + (long long)b * W;
       for (int jj = threadIdx.x; jj < W; jj += RC_THREADS)
-        if (jj != n) out[jj] = jj < n ? a.tokens[r.d0 + jj] : -1;
+        if (jj != n) GST(out + jj, jj < n ? GLD(a.tokens + (r.d0 + jj)) : -1);
       if (a.out_pq)
         for (int i = n + 1 + threadIdx.x; i < r.K; i += RC_THREADS) {
-          a.out_pq[2LL * (r.d0 + i)] = __int_as_float(0x7fc00000);
-          a.out_pq[2LL * (r.d0 + i) + 1] = __int_as_float(0x7fc00000);
+          GST(a.out_pq + (2LL * (r.d0 + i)), __int_as_float(0x7fc00000));
+          GST(a.out_pq + (2LL * (r.d0 + i) + 1), __int_as_float(0x7fc00000));
         }
       if (threadIdx.x == 0) {
-        a.out_accepted[b] = n;
-        if (!sample) out[n] = ts.idx;   // greedy: the target's argmax
+        GST(a.out_accepted + (b), n);
+        if (!sample) GST(out + n, ts.idx);   // greedy: the target's argmax
       }
     }
     // 6. the final draw (sampling requests) from position n's slices, which
@@ -565,7 +565,7 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
       }
       if (owner == rank && threadIdx.x == 0) {
         if (x < 0) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);   // a row without mass
-        a.out_tokens[(long long)b * W + n] = x;
+        GST(a.out_tokens + ((long long)b * W + n), x);
       }
     }
     __syncthreads();   // the slices are free for the next request's copies
@@ -588,6 +588,7 @@ bool resident_supported(const LinearArgs &a) {
 int launch_setup_stream(const LinearArgs &a, cudaStream_t stream);
 
 int launch_verify_resident(const LinearArgs &a, cudaStream_t stream) {
+  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
   static int clusters = -1;   // co-resident clusters of this shape, asked once
   const size_t smem = RC_DYN_SMEM;
   if (cudaFuncSetAttribute(k_verify_resident, cudaFuncAttributeMaxDynamicSharedMemorySize,

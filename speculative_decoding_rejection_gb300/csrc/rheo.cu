@@ -49,15 +49,15 @@ __global__ void k_rheo_validate(RheoArgs a) {
   }
   __syncthreads();
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
-    const int n = a.cu[b + 1] - a.cu[b];
-    const float T = a.temp[b];
+    const int n = GLD(a.cu + (b + 1)) - GLD(a.cu + (b));
+    const float T = GLD(a.temp + (b));
     if (n < 0 || !(T >= 0.f) || !isfinite(T)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
     else if ((long long)n * a.K > a.cap) set_status(a.hdr, SPEC_ERR_UNSUPPORTED, b);
   }
-  if (threadIdx.x == 0 && (a.cu[0] != 0 || a.cu[a.B] != a.F))
+  if (threadIdx.x == 0 && (GLD(a.cu + (0)) != 0 || GLD(a.cu + (a.B)) != a.F))
     set_status(a.hdr, SPEC_ERR_INVALID_ARG, a.B);
   for (int f = threadIdx.x; f < a.F; f += blockDim.x) {
-    const float s = a.fscore[f];
+    const float s = GLD(a.fscore + (f));
     if (isnan(s) || s == INFINITY) set_status(a.hdr, SPEC_ERR_INVALID_ARG, f);
   }
 }
@@ -72,11 +72,11 @@ __global__ void __launch_bounds__(RH_SELECT_THREADS) k_rheo_select(RheoArgs a, i
   extern __shared__ unsigned long long sk[];
   const int b = blockIdx.x;
   int32_t *out = a.keep + (size_t)b * a.n_keep;
-  const int lo = a.cu[b], hi = a.cu[b + 1];
+  const int lo = GLD(a.cu + (b)), hi = GLD(a.cu + (b + 1));
   const bool ok = a.hdr->status == 0 && lo >= 0 && hi <= a.F && lo <= hi &&
                   (long long)(hi - lo) * a.K <= P_max;
   if (!ok) {
-    for (int i = threadIdx.x; i < a.n_keep; i += blockDim.x) out[i] = -1;
+    for (int i = threadIdx.x; i < a.n_keep; i += blockDim.x) GST(out + i, -1);
     return;
   }
   const int n = (hi - lo) * a.K;
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(RH_SELECT_THREADS) k_rheo_select(RheoArgs a, i
   int P = 1;
   while (P < n) P <<= 1;
   for (int i = threadIdx.x; i < P; i += blockDim.x)
-    sk[i] = i < n ? ((unsigned long long)(~ordered_bits(a.score[base + i])) << 32) | (uint32_t)i
+    sk[i] = i < n ? ((unsigned long long)(~ordered_bits(GLD(a.score + (base + i)))) << 32) | (uint32_t)i
                   : ~0ull;
   __syncthreads();
   for (int k = 2; k <= P; k <<= 1) {
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(RH_SELECT_THREADS) k_rheo_select(RheoArgs a, i
     }
   }
   for (int i = threadIdx.x; i < a.n_keep; i += blockDim.x)
-    out[i] = i < n ? (int32_t)(base + (long long)(uint32_t)(sk[i] & 0xffffffffull)) : -1;
+    GST(out + i, i < n ? (int32_t)(base + (long long)(uint32_t)(sk[i] & 0xffffffffull)) : -1);
 }
 
 inline size_t rheo_ws_bytes(int) { return 256; }   // the status header
@@ -168,6 +168,20 @@ extern "C" int spec_rheo_expand(const void *draft, int ddt, const int32_t *cu_fr
   epi.score = child_score;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+#ifdef SPEC_CHECKED
+  check_begin(a.hdr);
+  check_add(workspace, rheo_ws_bytes(F));
+  check_add(draft, (unsigned long long)F * V * (ddt == SPEC_BF16 ? 2 : 4));
+  check_add(cu_frontier, (B + 1) * 4ull);
+  check_add(frontier_score, F * 4ull);
+  check_add(temperature, B * 4ull);
+  check_add(child_token, (unsigned long long)F * K * 4);
+  check_add(child_qproxy, (unsigned long long)F * K * 4);
+  check_add(child_qtrue, (unsigned long long)F * K * 4);
+  check_add(child_score, (unsigned long long)F * K * 4);
+  check_add(keep, (unsigned long long)B * n_keep * 4);
+#endif
+  if (check_upload(st) != SPEC_OK) return SPEC_ERR_CUDA;
   k_rheo_validate<<<1, 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (F > 0) {

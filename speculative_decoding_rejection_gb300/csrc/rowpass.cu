@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(RS_THREADS,
       const long long next = atomicAdd(counter, 1u);
       const int ja = (int)(item / ipj);
       const int g = (int)(item % ipj);
-      const Job job = a.jobs[ja];
-      const ReqInfo r = a.req[job.b];
+      const Job job = GLD(a.jobs + (ja));
+      const ReqInfo r = GLD(a.req + (job.b));
       const uint64_t trow = (uint64_t)(a.base[0] + (long long)(r.t0 + job.n) * a.row_bytes[0]);
       const uint64_t drow = (uint64_t)(a.base[1] + (long long)(r.d0 + job.n) * a.row_bytes[1]);
       const int j1 = min(a.ntiles, (g + 1) * RES_TILES_PER_ITEM);
@@ -110,9 +110,9 @@ __global__ void __launch_bounds__(RS_THREADS,
       const long long next = atomicAdd(counter, 1u);  // one item ahead
       const int entry = (int)(item / a.nch_max);
       const int chunk = (int)(item % a.nch_max);
-      const RowTask t = a.list[entry];
+      const RowTask t = GLD(a.list + (entry));
       const int w = t.which;
-      const float thr = RANK && w != 1 && t.slot >= 0 ? a.rank_thr[t.row] : INFINITY;
+      const float thr = RANK && w != 1 && t.slot >= 0 ? GLD(a.rank_thr + (t.row)) : INFINITY;
       if (PAIR && w == ROW_PAIR) {
         // target row and draft row side by side: each stage holds up to
         // TILE_BYTES/2 of both (same dtype, 16-byte aligned rows)
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(RS_THREADS,
     if (m0.w & (1 << 14)) {   // residual tile pair
       const int ja = m0.x, j = m0.y, ne = m0.w & 0x3fff;
       if (ja != res_job) {
-        const Job job = a.jobs[ja];
+        const Job job = GLD(a.jobs + (ja));
         res_law = ResLaw{job.mt, 1.f / job.St, job.md, job.Sd > 0.f ? 1.f / job.Sd : 0.f,
                          __int_as_float(m1.x)};
         res_job = ja;
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(RS_THREADS,
       if (lane == 0) mbar_arrive(&sh.empty[s]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
-      if (lane == 0) a.tsum4[((long long)ja * a.ntiles + j) * RS_CONS_WARPS + cw] = rs;
+      if (lane == 0) GST(a.tsum4 + (((long long)ja * a.ntiles + j) * RS_CONS_WARPS + cw), rs);
       continue;
     }
     if (PAIR && (m0.w & (1 << 15))) {   // target row + draft row
@@ -273,10 +273,9 @@ __global__ void __launch_bounds__(RS_THREADS,
         }
         if (lane == 0) {
           const long long k = ((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS + cw;
-          a.part[k] = Part{m, S, idx, cnt};
-          a.part[((long long)m1.z * a.nch_max + m0.y) * RS_CONS_WARPS + cw] =
-              Part{md, Sd, 0x7fffffff, 0};
-          a.kl_part[k] = A;
+          GST(a.part + (k), Part{m, S, idx, cnt});
+          GST(a.part + (((long long)m1.z * a.nch_max + m0.y) * RS_CONS_WARPS + cw), Part{md, Sd, 0x7fffffff, 0});
+          GST(a.kl_part + (k), A);
         }
         ps = PairState{NO_MAX, 0.f, 0.f, 0x7fffffff, 0, NO_MAX, 0.f};
       }
@@ -302,7 +301,7 @@ __global__ void __launch_bounds__(RS_THREADS,
         consume_head_tail(row, dt, m0.w, m1.z, m1.w, c, thr, lane, st);
       }
       const Part p = finish_row_chunk<RANK>(st, c);
-      if (lane == 0) a.part[((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS + cw] = p;
+      if (lane == 0) GST(a.part + (((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS + cw), p);
     }
   }
 }
@@ -339,6 +338,7 @@ void take_row_pass_events(cudaEvent_t *before, cudaEvent_t *after) {
 }
 
 int launch_row_pass(const RowPassArgs &a, cudaStream_t stream) {
+  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
   const size_t smem = (size_t)NSTAGE * TILE_BYTES;

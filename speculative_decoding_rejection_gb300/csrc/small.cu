@@ -182,8 +182,8 @@ __global__ void __launch_bounds__(SMALL_THREADS) k_verify_small(const LinearArgs
   ReqInfo r;
   load_request(a, b, r);
   if (sh.bad) {
-    for (int j = threadIdx.x; j < W; j += blockDim.x) out[j] = -1;
-    if (threadIdx.x == 0) a.out_accepted[b] = -1;
+    for (int j = threadIdx.x; j < W; j += blockDim.x) GST(out + j, -1);
+    if (threadIdx.x == 0) GST(a.out_accepted + (b), -1);
     return;
   }
   const int K = r.K;
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(SMALL_THREADS) k_verify_small(const LinearArgs
   // each position's token and the two logits (or q(d)) its coin needs, all
   // loaded at once
   for (int i = threadIdx.x; i < K; i += blockDim.x) {
-    const int d = a.tokens[r.d0 + i];
+    const int d = GLD(a.tokens + (r.d0 + i));
     const bool dok = (unsigned)d < (unsigned)a.V;
     float zt = 0.f, zq = 0.f;
     if (sample && dok && !row_empty(sh.ts[i].m)) {
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(SMALL_THREADS) k_verify_small(const LinearArgs
   }
   __syncthreads();
   const int n = sh.n;
-  for (int j = threadIdx.x; j < W; j += blockDim.x) out[j] = j < n ? a.tokens[r.d0 + j] : -1;
+  for (int j = threadIdx.x; j < W; j += blockDim.x) GST(out + j, j < n ? GLD(a.tokens + (r.d0 + j)) : -1);
   __syncthreads();
   int x;
   if (!sample) {
@@ -259,14 +259,15 @@ __global__ void __launch_bounds__(SMALL_THREADS) k_verify_small(const LinearArgs
       set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);   // a row without mass
       x = -1;
     }
-    out[n] = x;
-    a.out_accepted[b] = n;
+    GST(out + n, x);
+    GST(a.out_accepted + (b), n);
   }
 }
 
 }  // namespace
 
 int launch_verify_small(const LinearArgs &a, cudaStream_t stream) {
+  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
   cudaEvent_t before, after;
   take_row_pass_events(&before, &after);
   if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;

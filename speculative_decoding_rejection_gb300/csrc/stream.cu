@@ -104,6 +104,7 @@ struct StreamSmem {
 // Returns the old value; this thread's earlier writes are visible to any
 // thread that acquires the new one.
 __device__ __forceinline__ int atom_add_release(int *p, int v) {
+  if (!GCHK(p, 4)) return -1;
   int old;
   asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;"
                : "=r"(old)
@@ -115,26 +116,28 @@ __device__ __forceinline__ void fence_acquire() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 __device__ __forceinline__ void st_release(int *p, int v) {
+  if (!GCHK(p, 4)) return;
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ int ld_acquire(const int *p) {
+  if (!GCHK(p, 4)) return 0;
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ StreamEntry ldcg_entry(const StreamEntry *e) {
   const int4 *p = reinterpret_cast<const int4 *>(e);
-  const int4 x = __ldcg(p), y = __ldcg(p + 1);
+  const int4 x = GLDCG(p), y = GLDCG(p + 1);
   return StreamEntry{x.x, x.y, x.z, x.w, __int_as_float(y.x), {0, 0, 0}};
 }
 __device__ __forceinline__ void st_entry(StreamEntry *e, const StreamEntry &v) {
   int4 *p = reinterpret_cast<int4 *>(e);
-  p[0] = make_int4(v.b, v.trow, v.drow, v.job);
-  p[1] = make_int4(__float_as_int(v.c), 0, 0, 0);
+  GST(p, make_int4(v.b, v.trow, v.drow, v.job));
+  GST(p + 1, make_int4(__float_as_int(v.c), 0, 0, 0));
 }
 __device__ __forceinline__ Job ldcg_job(const Job *j) {
   const int4 *p = reinterpret_cast<const int4 *>(j);
-  const int4 x = __ldcg(p), y = __ldcg(p + 1);
+  const int4 x = GLDCG(p), y = GLDCG(p + 1);
   return Job{x.x, x.y, x.z, x.w, __int_as_float(y.x), __int_as_float(y.y), __int_as_float(y.z),
              __int_as_float(y.w)};
 }
@@ -154,34 +157,32 @@ __global__ void __launch_bounds__(SETUP_STREAM_THREADS) k_setup_stream(const Lin
   const long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (g >= (long long)a.B * W) return;
   const int b = (int)(g / W), j = (int)(g % W);
-  a.pos_done[g] = 0;
-  a.pos_join[g] = j == 0;
+  GST(a.pos_done + (g), 0);
+  GST(a.pos_join + (g), j == 0);
   ReqInfo r;
   const bool ok = load_request(a, b, r);   // every thread of b: the same record
   if (j == 0) {
-    a.ready_d[b] = 0;
-    a.ready_d[a.cap_d + b] = 0;
-    a.rej_at[b] = INT_MAX;
-    a.req[b] = r;
+    GST(a.ready_d + (b), 0);
+    GST(a.ready_d + (a.cap_d + b), 0);
+    GST(a.rej_at + (b), INT_MAX);
+    GST(a.req + (b), r);
     if (!ok) a.hdr->setup_bad = 1;
   }
   if (!ok || j > r.K) return;
   if (j == r.K) {
-    a.rank_thr[r.t0 + r.K] = INFINITY;
+    GST(a.rank_thr + (r.t0 + r.K), INFINITY);
     return;
   }
   const bool drow = r.mode == MODE_SAMPLE && a.stream_draft;
-  const int d = a.tokens[r.d0 + j];
+  const int d = GLD(a.tokens + (r.d0 + j));
   const bool dok = (unsigned)d < (unsigned)a.V;
   if (!dok) {
     set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
     a.hdr->setup_bad = 1;
   }
-  a.rank_thr[r.t0 + j] =
-      dok ? load_elem(a.target + (long long)(r.t0 + j) * a.t_row_bytes, a.tdt, d) : INFINITY;
+  GST(a.rank_thr + (r.t0 + j), dok ? load_elem(a.target + (long long)(r.t0 + j) * a.t_row_bytes, a.tdt, d) : INFINITY);
   if (drow)
-    a.zd_at[r.d0 + j] =
-        dok ? load_elem(a.draft + (long long)(r.d0 + j) * a.d_row_bytes, a.ddt, d) : 0.f;
+    GST(a.zd_at + (r.d0 + j), dok ? load_elem(a.draft + (long long)(r.d0 + j) * a.d_row_bytes, a.ddt, d) : 0.f);
 }
 
 // --------------------------------------------------------------- producer
@@ -208,7 +209,7 @@ __device__ __forceinline__ bool serve_ready_ticket(const LinearArgs &a, StreamSm
   served = false;
   if (dy.t >= dy.n) return true;
   const int e = (int)(dy.t / (unsigned)a.n_res_items);
-  if (!*(volatile int *)(a.ready_d + e)) return true;
+  if (!GCHK(a.ready_d + e, 4) || !*(volatile int *)(a.ready_d + e)) return true;
   fence_acquire();
   const StreamEntry E = ldcg_entry(a.ent_d + e);
   if (!issue_res_item(a, sh, stage_buf, it, abort, E, (int)(dy.t % (unsigned)a.n_res_items)))
@@ -234,7 +235,7 @@ __device__ bool issue_row_chunk(const LinearArgs &a, StreamSmem &sh, unsigned ch
   if (A1 <= A0) A0 = A1 = cb1;   // no aligned interior: all scalar
   const int ntile = A1 > A0 ? (int)((A1 - A0 + TILE_BYTES - 1) / TILE_BYTES) : 1;
   const int head_n = (int)((A0 - cb0) / esz), tail_n = (int)((cb1 - A1) / esz);
-  const float thr = RANK && !draft ? a.rank_thr[row] : INFINITY;
+  const float thr = RANK && !draft ? GLD(a.rank_thr + (row)) : INFINITY;
   for (int tl = 0; tl < ntile; ++tl) {
     if (!acquire_stage(sh, it, abort)) return false;
     const int s = (int)(it % NSTAGE);
@@ -270,8 +271,8 @@ __device__ bool issue_static(const LinearArgs &a, StreamSmem &sh, unsigned char 
   const unsigned long long e = t / (unsigned)a.stride;
   const int k = (int)(t % (unsigned)a.stride);
   const int j = (int)(e / (unsigned)a.B), b = (int)(e % (unsigned)a.B);
-  const ReqInfo r = a.req[b];
-  const int rej = __ldcg(a.rej_at + b);
+  const ReqInfo r = GLD(a.req + (b));
+  const int rej = GLDCG(a.rej_at + b);
   if (r.mode == MODE_SKIP || j > r.K || j > rej) return true;
   const bool drow = r.mode == MODE_SAMPLE && a.stream_draft && j < r.K;
   const int4 m2 = make_int4(b, a.nch_t + (drow ? a.nch_d : 0), j | (r.K << 16), r.t0 + j);
@@ -349,7 +350,8 @@ __device__ __forceinline__ RowStat lane_parts_stat(const Part &p, bool have, flo
 // Adds one event to position j's join (rows complete, previous position
 // accepted); true for the second of the two.
 __device__ __forceinline__ bool join_second(const LinearArgs &a, int b, int j) {
-  const bool second = atomicAdd(a.pos_join + b * (a.max_k + 1) + j, 1) == 1;
+  int *pj = a.pos_join + b * (a.max_k + 1) + j;
+  const bool second = GCHK(pj, 4) && atomicAdd(pj, 1) == 1;
   if (second) __threadfence();
   return second;
 }
@@ -382,9 +384,9 @@ __device__ __noinline__ void stream_decide(const LinearArgs &a, int b, int j, in
     if (fast && th) tp = ldcg_part(a.part + (long long)tslot * a.nch_max * RS_CONS_WARPS + lane);
     if (fast && dh) dp = ldcg_part(a.part + (long long)dslot * a.nch_max * RS_CONS_WARPS + lane);
     if (j < K) {
-      d = a.tokens[r.d0 + j];
-      zt = __ldcg(a.rank_thr + r.t0 + j);
-      if (drow) zd = __ldcg(a.zd_at + r.d0 + j);
+      d = GLD(a.tokens + (r.d0 + j));
+      zt = GLDCG(a.rank_thr + r.t0 + j);
+      if (drow) zd = GLDCG(a.zd_at + r.d0 + j);
     }
     const RowStat ts = fast ? lane_parts_stat(tp, th, c) : target_stat(a, tslot, c, lane);
     RowStat ds{NO_MAX, 0.f, 0x7fffffff};
@@ -412,23 +414,23 @@ __device__ __noinline__ void stream_decide(const LinearArgs &a, int b, int j, in
         continue;
       }
       n = j;
-      if (lane == 0) a.rej_at[b] = j;   // later positions' rows are no longer read
+      if (lane == 0) GST(a.rej_at + (b), j);   // later positions' rows are no longer read
     }
     // positions after n+1 are not reported
     for (int i = n + 1 + lane; i < K; i += 32) {
       if (a.out_pq) {
-        a.out_pq[2LL * (r.d0 + i)] = __int_as_float(0x7fc00000);
-        a.out_pq[2LL * (r.d0 + i) + 1] = __int_as_float(0x7fc00000);
+        GST(a.out_pq + (2LL * (r.d0 + i)), __int_as_float(0x7fc00000));
+        GST(a.out_pq + (2LL * (r.d0 + i) + 1), __int_as_float(0x7fc00000));
       }
-      if (a.out_rank) a.out_rank[r.d0 + i] = -1;
+      if (a.out_rank) GST(a.out_rank + (r.d0 + i), -1);
     }
     const int W = a.max_k + 1;
     int32_t *out = a.out_tokens + (long long)b * W;
-    for (int jj = lane; jj < W; jj += 32) out[jj] = jj < n ? a.tokens[r.d0 + jj] : -1;
-    if (lane == 0) a.out_accepted[b] = n;
+    for (int jj = lane; jj < W; jj += 32) GST(out + jj, jj < n ? GLD(a.tokens + (r.d0 + jj)) : -1);
+    if (lane == 0) GST(a.out_accepted + (b), n);
     __syncwarp();
     if (!sample) {   // greedy: the target's argmax replaces the rejected draft
-      if (lane == 0) out[n] = ts.idx;
+      if (lane == 0) GST(out + n, ts.idx);
       finish_one(a, lane);
       return;
     }
@@ -437,13 +439,13 @@ __device__ __noinline__ void stream_decide(const LinearArgs &a, int b, int j, in
       if (residual) {
         // the residual's tile sums are summed in this kernel, the draw after it
         const int ja = atomicAdd(&a.hdr->n_jobs_a, 1);
-        a.jobs_a[ja] = Job{b, n, 1, 0, ts.m, ts.S, ds.m, ds.S};
+        GST(a.jobs_a + (ja), Job{b, n, 1, 0, ts.m, ts.S, ds.m, ds.S});
         const int e = atomicAdd(&a.hdr->n_alloc_d, 1);   // < B: one per request
         st_entry(a.ent_d + e, StreamEntry{b, r.t0 + n, r.d0 + n, ja, c, {0, 0, 0}});
         __threadfence();
         st_release(a.ready_d + e, 1);
       } else {   // bonus draw from p_{K+1}, after this kernel
-        a.jobs_b[atomicAdd(&a.hdr->n_jobs_b, 1)] = Job{b, n, 2, 0, ts.m, ts.S, 0.f, 0.f};
+        GST(a.jobs_b + (atomicAdd(&a.hdr->n_jobs_b, 1)), Job{b, n, 2, 0, ts.m, ts.S, 0.f, 0.f});
       }
     }
     if (!residual) finish_one(a, lane);
@@ -467,13 +469,13 @@ __device__ __forceinline__ void service_record(const LinearArgs &a, StreamSmem &
     int *count;
     if (res) {   // m2.z: job, m2.w: first tile, m1.w: tiles in the item
       for (int t = 0; t < m1.w; ++t)
-        reinterpret_cast<float4 *>(a.tsum)[(long long)m2.z * a.ntiles + m2.w + t] =
-            make_float4(sh.qt[q][0][t], sh.qt[q][1][t], sh.qt[q][2][t], sh.qt[q][3][t]);
+        GST(reinterpret_cast<float4 *>(a.tsum) + (long long)m2.z * a.ntiles + m2.w + t,
+            make_float4(sh.qt[q][0][t], sh.qt[q][1][t], sh.qt[q][2][t], sh.qt[q][3][t]));
       count = a.ready_d + a.cap_d + m2.x;   // the residual entry's own count
     } else {
       Part *dst = a.part + ((long long)m0.x * a.nch_max + m0.y) * RS_CONS_WARPS;
 #pragma unroll
-      for (int w = 0; w < RS_CONS_WARPS; ++w) dst[w] = sh.qp[q][w];
+      for (int w = 0; w < RS_CONS_WARPS; ++w) GST(dst + w, sh.qp[q][w]);
       count = a.pos_done + m2.x * (a.max_k + 1) + (m2.z & 0xffff);
     }
     mbar_arrive(&sh.qempty[q]);   // the record is in registers and global memory
@@ -545,8 +547,8 @@ __global__ void __launch_bounds__(ST_THREADS, RANK ? ST_RANK_CTAS_PER_SM : ST_CT
     const int W = a.max_k + 1;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)a.B * W;
          i += (long long)gridDim.x * blockDim.x) {
-      a.out_tokens[i] = -1;
-      if (i < a.B) a.out_accepted[i] = -1;
+      GST(a.out_tokens + (i), -1);
+      if (i < a.B) GST(a.out_accepted + (i), -1);
     }
     return;
   }
@@ -699,6 +701,7 @@ __global__ void __launch_bounds__(ST_THREADS, RANK ? ST_RANK_CTAS_PER_SM : ST_CT
 // The streaming setup on its own (the cluster-resident verifier uses its
 // request records and gathered draft logits).
 int launch_setup_stream(const LinearArgs &a, cudaStream_t stream) {
+  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
   const long long n_setup = (long long)a.B * (a.max_k + 1);
   k_setup_stream<<<(unsigned)((n_setup + SETUP_STREAM_THREADS - 1) / SETUP_STREAM_THREADS),
                    SETUP_STREAM_THREADS, 0, stream>>>(a);
@@ -711,6 +714,7 @@ bool stream_supported(const LinearArgs &a) {
 }
 
 int launch_verify_stream(const LinearArgs &a, cudaStream_t stream) {
+  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
   const long long n_setup = (long long)a.B * (a.max_k + 1);

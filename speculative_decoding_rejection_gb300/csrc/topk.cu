@@ -101,8 +101,8 @@ __device__ __forceinline__ float value_of_bits(uint32_t bits, bool bf16) {
 }
 
 __device__ __forceinline__ uint32_t load_bits(const char *row, bool bf16, int i) {
-  return bf16 ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + i)
-              : __ldg(reinterpret_cast<const uint32_t *>(row) + i);
+  return bf16 ? (uint32_t)GLDG(reinterpret_cast<const unsigned short *>(row) + i)
+              : GLDG(reinterpret_cast<const uint32_t *>(row) + i);
 }
 
 // Calls f(bits, index) once for every element of the row, spread over the
@@ -118,7 +118,7 @@ __device__ __forceinline__ void for_each_elem(const char *row, int V, F &&f) {
   const uint4 *vp = reinterpret_cast<const uint4 *>(row + (long long)head * ESZ);
 #pragma unroll 4
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-    const uint4 w = __ldg(vp + v);
+    const uint4 w = GLDG(vp + v);
     const int e = head + v * PER;
     if (BF16) {
       f(w.x & 0xffffu, e + 0); f(w.x >> 16, e + 1); f(w.y & 0xffffu, e + 2); f(w.y >> 16, e + 3);
@@ -199,7 +199,7 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh, float pre
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int v = v0 + u * TK_THREADS;
-      w[u] = v < nvec ? __ldg(vp + v) : make_uint4(NINF2, NINF2, NINF2, NINF2);
+      w[u] = v < nvec ? GLDG(vp + v) : make_uint4(NINF2, NINF2, NINF2, NINF2);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -234,7 +234,7 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh, float pre
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int v = v0 + u * TK_THREADS;
-      wv[u] = v < nvec ? __ldg(vp + v) : make_uint4(NINF2, NINF2, NINF2, NINF2);
+      wv[u] = v < nvec ? GLDG(vp + v) : make_uint4(NINF2, NINF2, NINF2, NINF2);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -349,7 +349,7 @@ __device__ void rheo_epilogue(const TopkArgs &a, TopkSmem &sh, int r, int ksel) 
     const int ps = sh.probe_lo < SPEC_TOPK ? sh.probe_lo : max(sh.probe_hi, 0);
     const int prk = rank_of[ps];
     const size_t out0 = (size_t)r * h.K;
-    const float fs = h.fscore[r];
+    const float fs = GLD(h.fscore + (r));
     int slot = -1;
     float pr = qu;
     if (t == ps) {
@@ -360,10 +360,10 @@ __device__ void rheo_epilogue(const TopkArgs &a, TopkSmem &sh, int r, int ksel) 
       if (rr < h.K - 1) slot = rr < h.m ? rr : rr + 1;
     }
     if (slot >= 0) {
-      h.token[out0 + slot] = sh.sel_idx[t];
-      if (h.qproxy) h.qproxy[out0 + slot] = pr;
-      if (h.qtrue) h.qtrue[out0 + slot] = qt;
-      h.score[out0 + slot] = fs + logf(pr);
+      GST(h.token + (out0 + slot), sh.sel_idx[t]);
+      if (h.qproxy) GST(h.qproxy + (out0 + slot), pr);
+      if (h.qtrue) GST(h.qtrue + (out0 + slot), qt);
+      GST(h.score + (out0 + slot), fs + logf(pr));
     }
   }
   __syncthreads();
@@ -383,13 +383,13 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
     while (hi - lo > 1) {
       const int step = (hi - lo + 31) / 32;
       const int probe = lo + t * step;
-      const bool le = probe < hi && a.cu[probe] <= r;
+      const bool le = probe < hi && GLD(a.cu + (probe)) <= r;
       const unsigned m = __ballot_sync(0xffffffffu, le);
       const int last = 31 - __clz(m);        // lane 0 always qualifies (cu[lo] <= r)
       lo = lo + last * step;
       hi = min(hi, lo + step);
     }
-    if (t == 0) sh.T = a.temp[lo];
+    if (t == 0) sh.T = GLD(a.temp + (lo));
   }
   __syncthreads();
   const float T = sh.T;
@@ -468,7 +468,7 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
         if (BF16) {
 #pragma unroll
           for (int q = 0; q < TK_EPT / 8; ++q) {
-            const uint4 w = __ldg(p + q);
+            const uint4 w = GLDG(p + q);
             bits[8 * q + 0] = w.x & 0xffffu; bits[8 * q + 1] = w.x >> 16;
             bits[8 * q + 2] = w.y & 0xffffu; bits[8 * q + 3] = w.y >> 16;
             bits[8 * q + 4] = w.z & 0xffffu; bits[8 * q + 5] = w.z >> 16;
@@ -477,7 +477,7 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
         } else {
 #pragma unroll
           for (int q = 0; q < TK_EPT / 4; ++q) {
-            const uint4 w = __ldg(p + q);
+            const uint4 w = GLDG(p + q);
             bits[4 * q + 0] = w.x; bits[4 * q + 1] = w.y;
             bits[4 * q + 2] = w.z; bits[4 * q + 3] = w.w;
           }
@@ -571,8 +571,8 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
   __syncthreads();
   if (t < SPEC_TOPK && a.out_idx != nullptr) {
     const bool ok = t < ksel;
-    a.out_idx[(long long)r * SPEC_TOPK + t] = ok ? sh.sel_idx[t] : -1;
-    a.out_prob[(long long)r * SPEC_TOPK + t] = ok ? sh.sel_e[t] / sh.S : 0.f;
+    GST(a.out_idx + ((long long)r * SPEC_TOPK + t), ok ? sh.sel_idx[t] : -1);
+    GST(a.out_prob + ((long long)r * SPEC_TOPK + t), ok ? sh.sel_e[t] / sh.S : 0.f);
   }
   if (a.has_rh) rheo_epilogue(a, sh, r, ksel);
   __syncthreads();
@@ -586,7 +586,7 @@ __global__ void __launch_bounds__(TK_THREADS, TK_CTAS_PER_SM) k_topk128(const To
     sh.delta = 0.5f;
   }
   __syncthreads();
-  const int rows = min(a.rows_bound, a.cu[a.B]);
+  const int rows = min(a.rows_bound, GLD(a.cu + (a.B)));
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     if (a.dtype == SPEC_BF16) topk_row<true>(a, sh, r);
     else topk_row<false>(a, sh, r);
@@ -601,17 +601,18 @@ __global__ void k_topk_validate(const TopkArgs a) {
   }
   __syncthreads();
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
-    const int K = a.cu[b + 1] - a.cu[b];
-    const float T = a.temp[b];
-    if ((b == 0 && a.cu[0] != 0) || K < 0 || !(T >= 0.f) || !isfinite(T))
+    const int K = GLD(a.cu + (b + 1)) - GLD(a.cu + (b));
+    const float T = GLD(a.temp + (b));
+    if ((b == 0 && GLD(a.cu + (0)) != 0) || K < 0 || !(T >= 0.f) || !isfinite(T))
       set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
   }
-  if (threadIdx.x == 0 && a.cu[a.B] > a.rows_bound) set_status(a.hdr, SPEC_ERR_INVALID_ARG, a.B);
+  if (threadIdx.x == 0 && GLD(a.cu + (a.B)) > a.rows_bound) set_status(a.hdr, SPEC_ERR_INVALID_ARG, a.B);
 }
 
 int launch_topk128(const void *logits, int dtype, int rows_bound, int V, const int32_t *cu_rows,
                    const float *temperature, int B, int32_t *out_idx, float *out_prob,
                    WsHeader *hdr, cudaStream_t stream, const RheoEpi *rh) {
+  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
   TopkArgs a{};
   a.has_rh = rh != nullptr;
   if (rh) a.rh = *rh;
@@ -668,6 +669,16 @@ extern "C" int draft_topk_softmax(const void *draft_logits, int dt, int rows, in
   a.rows_bound = rows;
   a.hdr = hdr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+#ifdef SPEC_CHECKED
+  check_begin(hdr);
+  check_add(workspace, TOPK_WS);
+  check_add(draft_logits, (unsigned long long)rows * V * (dt == SPEC_BF16 ? 2 : 4));
+  check_add(cu_rows, (B + 1) * 4ull);
+  check_add(temperature, B * 4ull);
+  check_add(out_idx, (unsigned long long)rows * SPEC_TOPK * 4);
+  check_add(out_prob, (unsigned long long)rows * SPEC_TOPK * 4);
+#endif
+  if (check_upload(st) != SPEC_OK) return SPEC_ERR_CUDA;
   k_topk_validate<<<1, 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   return launch_topk128(draft_logits, dt, rows, V, cu_rows, temperature, B, out_idx, out_prob,

@@ -87,7 +87,7 @@ struct TreeArgs {
 
 // The call's seed: from device memory when the caller gave a pointer.
 __device__ __forceinline__ uint64_t tree_seed(const TreeArgs &a) {
-  return a.seed_dev != nullptr ? __ldg(a.seed_dev) : a.seed;
+  return a.seed_dev != nullptr ? GLDG(a.seed_dev) : a.seed;
 }
 
 struct TreeLayout {
@@ -117,22 +117,22 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
   __shared__ int s_bad;
   const int b = blockIdx.x, t = threadIdx.x;
   TreeInfo ti;
-  ti.base = a.cu[b];
-  ti.N = a.cu[b + 1] - a.cu[b];
-  const float T = a.temp[b];
+  ti.base = GLD(a.cu + (b));
+  ti.N = GLD(a.cu + (b + 1)) - GLD(a.cu + (b));
+  const float T = GLD(a.temp + (b));
   const bool greedy = T < SPEC_GREEDY_T;
-  bool ok = (b > 0 || a.cu[0] == 0) && ti.base >= 0 && ti.N >= 1 &&
-            ti.N <= SPEC_MAX_TREE_NODES && a.cu[b + 1] <= a.n_nodes && T >= 0.f && isfinite(T);
+  bool ok = (b > 0 || GLD(a.cu + (0)) == 0) && ti.base >= 0 && ti.N >= 1 &&
+            ti.N <= SPEC_MAX_TREE_NODES && GLD(a.cu + (b + 1)) <= a.n_nodes && T >= 0.f && isfinite(T);
   if (ok && !greedy && a.draft == nullptr) ok = false;
   if (t == 0) s_bad = !ok;
   __syncthreads();
   if (ok) {
     for (int c = t; c < ti.N; c += SETUP_THREADS) {
-      const int p = a.parent[ti.base + c];
+      const int p = GLD(a.parent + (ti.base + c));
       s_par[c] = p;
       s_kids[c] = 0;
       const bool good = c == 0 ? p == -1
-                               : (p >= 0 && p < c && (unsigned)a.node_token[ti.base + c] <
+                               : (p >= 0 && p < c && (unsigned)GLD(a.node_token + (ti.base + c)) <
                                                           (unsigned)a.V);
       if (!good) s_bad = 1;
     }
@@ -160,9 +160,9 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
   // so their array holds each node's token, -1 where the node is exempt.
   if (ok && !s_bad)
     for (int c = t; c < ti.N; c += SETUP_THREADS)
-      s_kids[c] = (c == 0 || (a.node_fixed != nullptr && a.node_fixed[ti.base + c] != 0))
+      s_kids[c] = (c == 0 || (a.node_fixed != nullptr && GLD(a.node_fixed + (ti.base + c)) != 0))
                       ? -1
-                      : a.node_token[ti.base + c];
+                      : GLD(a.node_token + (ti.base + c));
   __syncthreads();
   if (ok && !s_bad)
     for (int c = t + 1; c < ti.N; c += SETUP_THREADS) {
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
   ti.mode = ok ? (greedy ? MODE_GREEDY : MODE_SAMPLE) : MODE_SKIP;
   ti.c = (ok && !greedy) ? (float)(1.4426950408889634 / (double)T) : 0.f;
   if (t == 0) {
-    a.tree[b] = ti;
+    GST(a.tree + (b), ti);
     if (!ok) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
   }
 }
@@ -561,7 +561,7 @@ __device__ __forceinline__ void write_final(const TreeArgs &a, int b, int depth,
     set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);   // a row without mass
     x = -1;
   }
-  a.out_tokens[(long long)b * (a.max_depth + 1) + depth] = x;
+  GST(a.out_tokens + ((long long)b * (a.max_depth + 1) + depth), x);
 }
 
 // The walk of tree b on the CTA of cluster rank `rank`. Every exit of this
@@ -600,11 +600,11 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       const int per = (t.N + blockDim.x - 1) / blockDim.x;
       const int c0 = min(t.N, (int)threadIdx.x * per), c1 = min(t.N, c0 + per);
       int n = 0;
-      for (int cc = c0; cc < c1; ++cc) n += a.parent[t.base + cc] == v && cc > 0;
+      for (int cc = c0; cc < c1; ++cc) n += GLD(a.parent + (t.base + cc)) == v && cc > 0;
       int tot;
       int off = block_excl_scan_int(n, reinterpret_cast<int *>(sh.scratch), &tot);
       for (int cc = c0; cc < c1; ++cc)
-        if (a.parent[t.base + cc] == v && cc > 0) {
+        if (GLD(a.parent + (t.base + cc)) == v && cc > 0) {
           if (off < SPEC_MAX_TREE_BRANCH) sh.kids[off] = cc;
           ++off;
         }
@@ -614,9 +614,9 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       const int j = threadIdx.x;
       if (j < sh.nk) {
         const long long rv = t.base + v;
-        const int x = a.node_token[t.base + sh.kids[j]];
+        const int x = GLD(a.node_token + (t.base + sh.kids[j]));
         sh.kx[j] = x;
-        sh.kfix[j] = a.node_fixed != nullptr && a.node_fixed[t.base + sh.kids[j]] != 0;
+        sh.kfix[j] = a.node_fixed != nullptr && GLD(a.node_fixed + (t.base + sh.kids[j])) != 0;
         if (t.mode != MODE_GREEDY && (unsigned)x < (unsigned)a.V) {
           sh.kzt[j] = load_elem(a.target + rv * a.t_row_bytes, a.tdt, x);
           sh.kzd[j] = load_elem(a.draft + rv * a.d_row_bytes, a.ddt, x);
@@ -652,16 +652,16 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       __syncthreads();
       if (ac >= 0 && depth < a.max_depth) {
         if (rank == 0 && threadIdx.x == 0) {
-          out[depth] = ts.idx;   // the accepted child's token is the argmax
-          if (path) path[depth] = ac;
+          GST(out + depth, ts.idx);   // the accepted child's token is the argmax
+          if (path) GST(path + depth, ac);
         }
         v = ac;
         ++depth;
         continue;
       }
       if (rank == 0 && threadIdx.x == 0) {
-        out[depth] = ts.idx;
-        a.out_accepted[b] = depth;
+        GST(out + depth, ts.idx);
+        GST(a.out_accepted + (b), depth);
       }
       return;
     }
@@ -683,7 +683,7 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
                                     uniform24(tree_seed(a), (uint32_t)b, (uint32_t)(v + 1), 2), sl,
                                     rank);
       if (x != -1 && threadIdx.x == 0) write_final(a, b, depth, x);
-      if (rank == 0 && threadIdx.x == 0) a.out_accepted[b] = depth;
+      if (rank == 0 && threadIdx.x == 0) GST(a.out_accepted + (b), depth);
       return;
     }
     nl.drow = a.draft + (long long)row * a.d_row_bytes;
@@ -756,8 +756,8 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     }
     if (accepted >= 0 && depth < a.max_depth) {
       if (rank == 0 && threadIdx.x == 0) {
-        out[depth] = a.node_token[t.base + accepted];
-        if (path) path[depth] = accepted;
+        GST(out + depth, GLD(a.node_token + (t.base + accepted)));
+        if (path) GST(path + depth, accepted);
       }
       v = accepted;
       ++depth;
@@ -775,7 +775,7 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     const int x = weight_draw<DK>(a, sh, nl, c, L, residual,
                                   uniform24(tree_seed(a), (uint32_t)b, (uint32_t)(v + 1), 1), sl, rank);
     if (x != -1 && threadIdx.x == 0) write_final(a, b, depth, x);
-    if (rank == 0 && threadIdx.x == 0) a.out_accepted[b] = depth;
+    if (rank == 0 && threadIdx.x == 0) GST(a.out_accepted + (b), depth);
     return;
   }
 }
@@ -788,12 +788,12 @@ __global__ void __cluster_dims__(WALK_CLUSTER, 1, 1) __launch_bounds__(WALK_THRE
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / WALK_CLUSTER;
-  const TreeInfo t = a.tree[b];
+  const TreeInfo t = GLD(a.tree + (b));
   const int W = a.max_depth + 1;
   if (rank == 0)
     for (int j = threadIdx.x; j < W; j += blockDim.x) {
-      a.out_tokens[(long long)b * W + j] = -1;
-      if (a.out_path) a.out_path[(long long)b * W + j] = -1;
+      GST(a.out_tokens + ((long long)b * W + j), -1);
+      if (a.out_path) GST(a.out_path + ((long long)b * W + j), -1);
     }
   // Whether to walk is decided once for the whole cluster: the status word
   // can change under a running walk (another tree without mass), so each CTA
@@ -817,7 +817,7 @@ __global__ void __cluster_dims__(WALK_CLUSTER, 1, 1) __launch_bounds__(WALK_THRE
     walk_tree<DK>(a, sh, t, b, rank, cluster, a.staged ? rows_sm : nullptr,
                   a.staged ? rows_sm + a.dsm_off : nullptr);
   else if (rank == 0 && threadIdx.x == 0)
-    a.out_accepted[b] = -1;
+    GST(a.out_accepted + (b), -1);
   cluster.sync();
 }
 
@@ -898,6 +898,22 @@ static int verify_tree(const void *target, int tdt, const void *draft, int ddt, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return SPEC_ERR_CUDA;
   if (B == 0) return SPEC_OK;
+#ifdef SPEC_CHECKED
+  check_begin(a.hdr);
+  check_add(workspace, L.total);
+  check_add(target, (unsigned long long)n_nodes * a.t_row_bytes);
+  check_add(draft, (unsigned long long)n_nodes * a.d_row_bytes);
+  check_add(node_token, n_nodes * 4ull);
+  check_add(parent, n_nodes * 4ull);
+  check_add(node_fixed, n_nodes * 4ull);
+  check_add(cu_nodes, (B + 1) * 4ull);
+  check_add(temperature, B * 4ull);
+  check_add(out_tokens, (unsigned long long)B * (max_depth + 1) * 4);
+  check_add(out_accepted, B * 4ull);
+  check_add(out_path, (unsigned long long)B * (max_depth + 1) * 4);
+  check_add(seed_dev, 8);
+#endif
+  if (check_upload(st) != SPEC_OK) return SPEC_ERR_CUDA;
   k_setup_tree<<<B, SETUP_THREADS, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   // profiling events, if registered, bracket the walk

@@ -116,7 +116,7 @@ def test_status_and_uniform_argument_checks(L):
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sv, "_lib", None)
-    monkeypatch.setattr(sv, "LIB_PATH", tmp_path / "missing.so")
+    monkeypatch.setattr(sv, "_lib_path", tmp_path / "missing.so")
     with pytest.raises(RuntimeError, match="not built"):
         sv.lib()
 
