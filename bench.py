@@ -365,6 +365,7 @@ class LinearWork:
                          and 16384 <= lb.V <= 204800)
         plain = not (lazy or resident or eager or kl) and self.ext is None
         self.stream = streamable and not self.resident and (lazy or resident or plain)
+        asked_lazy = lazy or resident
         lazy = lazy or resident or self.stream
         self.lazy = lazy
         if lazy:
@@ -381,12 +382,21 @@ class LinearWork:
         sv.spec_set_fused_limit(limit)
         esz = lb.target.element_size()
         per_req = (lb.max_k + 1) * lb.V * esz + lb.max_k * lb.V * lb.draft.element_size()
-        self.fused = (not (lazy or eager) and not kl and self.ext is None and not lb.top128
+        self.fused = (not (asked_lazy or eager) and not kl and self.ext is None and not lb.top128
                       and lb.V <= 8192 and per_req <= 1 << 20 and lb.B * per_req <= limit)
-        if self.fused:
-            self.launches = 1
-            self.kernel = "k_verify_small"
-            self.config["schedule"] = "fused (one block per request)"
+        # longer bf16 rows in calls of at most 128 requests and 8 drafts whose
+        # row slices fit a cluster's shared memory: one cluster per request
+        # (setup, then the cluster kernel)
+        slice_ = (lb.V // 8 + 7) // 8 * 8
+        self.cluster_small = (not self.fused and not (asked_lazy or eager) and not kl
+                              and self.ext is None and not lb.top128 and bf16 and lb.V % 8 == 0
+                              and lb.max_k <= 8 and lb.B <= 128 and limit > 0
+                              and (2 * lb.max_k + 1) * slice_ * 2 <= 204800)
+        if self.fused or self.cluster_small:
+            self.launches = 1 if self.fused else 2
+            self.kernel = "k_verify_small" if self.fused else "k_verify_cluster_small"
+            self.config["schedule"] = ("fused (one block per request)" if self.fused else
+                                       "one cluster per request, its rows resident")
             self.stream = self.lazy = False
         elif self.stream and "schedule" not in self.config:
             self.config["schedule"] = "position-lazy streaming (rows 1..n+1 per request)"
@@ -422,7 +432,7 @@ class LinearWork:
         """The workload's own call, spec_verify_linear without options (its
         schedule is the library's choice)."""
         return "schedule" not in self.config or self.config["schedule"].startswith(
-            ("position-lazy streaming", "fused"))
+            ("position-lazy streaming", "fused", "one cluster per request"))
 
     def result_tensors(self):
         return [self.outs[0], self.outs[1]] + ([self.kl] if self.kl is not None else [])

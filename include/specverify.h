@@ -143,7 +143,8 @@ size_t spec_verify_linear_workspace(int B, int max_k, int V, int rule);
  *                skip.
  *   workspace    device scratch, >= spec_verify_linear_workspace(...) bytes,
  *                256-byte aligned, contents need no initialisation.
- * Schedule: a call with out_pq NULL, draft logits, bf16 target and draft
+ * Schedule: small calls run as one fused kernel (spec_set_fused_limit). Any
+ * other call with out_pq NULL, draft logits, bf16 target and draft
  * rows, V a multiple of 8 and rule SPEC_RULE_STRICT or SPEC_RULE_GREEDY
  * runs the position-lazy streaming schedule (SPEC_EXT_LAZY below): a
  * request's rows after its first rejection are not used, so a row there
@@ -167,10 +168,16 @@ int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
  * most 8192, a request's rows ((max_k + 1) target rows and max_k draft rows)
  * total at most 1 MiB and all B requests' rows at most `bytes`. Such calls
  * are decode steps over short rows, where one launch costs less than the
- * multi-kernel schedule. Same results either way, up to the rounding of the row sums.
- * `bytes` = 0 turns the fused kernel off; the default is 32 MiB. A
- * process-wide setting, read when a call is made. Returns the previous
- * value.
+ * multi-kernel schedule. A call of the same rules on bf16 draft logits with
+ * longer rows (V a multiple of 8), at most 128 requests and at most 8
+ * drafts each, whose (2 max_k + 1) row slices of V/8 logits fit 100 KB of
+ * shared memory (V up to about 37000 at max_k = 5), runs as one cluster
+ * kernel instead: a cluster of 8 CTAs per request holds all of the
+ * request's rows on chip, exchanges their statistics once and draws the
+ * final token from that copy. Same results either way, up to the rounding
+ * of the row sums. `bytes` = 0 turns both kernels off; the default is
+ * 32 MiB. A process-wide setting, read when a call is made. Returns the
+ * previous value.
  */
 size_t spec_set_fused_limit(size_t bytes);
 

@@ -1029,6 +1029,7 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   a.cap_d = B;
   a.n_res_items = (a.ntiles + RES_TILES_PER_ITEM - 1) / RES_TILES_PER_ITEM;
   if (small_supported(a, ext)) return launch_verify_small(a, st);
+  if (cluster_small_supported(a, ext, g_small_limit)) return launch_verify_cluster_small(a, st);
   if ((flags & SPEC_EXT_RESIDENT) && resident_supported(a)) {
     // position-lazy schedule with each position's rows resident on chip
     // (setup, then one persistent cluster kernel that also draws)

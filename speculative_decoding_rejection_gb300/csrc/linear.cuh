@@ -286,6 +286,15 @@ int launch_verify_stream(const LinearArgs &a, cudaStream_t stream);
 bool resident_supported(const LinearArgs &a);
 int launch_verify_resident(const LinearArgs &a, cudaStream_t stream);
 
+// Small calls whose rows are too long for the fused kernel (at most 128
+// requests, dense bf16 logits, V % 8 == 0, at most 8 drafts, every row of a
+// request fitting a cluster's shared memory; off when `limit_bytes`, the
+// fused limit, is 0): one cluster per request, all of its rows resident at
+// once, two exchanges per request.
+bool cluster_small_supported(const LinearArgs &a, const spec_linear_ext *ext,
+                             size_t limit_bytes);
+int launch_verify_cluster_small(const LinearArgs &a, cudaStream_t stream);
+
 // The fused small-batch verifier (one kernel, one block per request) and the
 // calls it takes.
 bool small_supported(const LinearArgs &a, const spec_linear_ext *ext);

@@ -36,7 +36,9 @@
 // at the start of each request and sends it with its first statistics.
 // Every wait is bounded (2 s of %globaltimer); on expiry the status word
 // gets SPEC_ERR_TIMEOUT and the cluster stops.
+#include <algorithm>
 #include <climits>
+#include <cstddef>
 
 #include <cooperative_groups.h>
 
@@ -60,7 +62,8 @@ constexpr int RC_SLICE_MAX = 25600;                    // elements of a slice a 
 constexpr int RC_MIN_V = 16384;                        // smaller rows: other schedules
 constexpr size_t RC_DYN_SMEM = (size_t)2 * RC_SLICE_MAX * 2;   // target + draft slice, bf16
 
-struct RcMsg {        // one CTA's slice statistics of a position (32 bytes)
+struct alignas(16) RcMsg {   // one CTA's slice statistics of a position (32 bytes), stored
+                             // to peers as two 16-byte vectors: 16-byte aligned
   float tm, tS;       // target slice: max, sum of 2^((z - tm) c)
   int tidx;           // lowest index of the target slice's max
   float dm, dS;       // draft slice (sampling positions)
@@ -82,6 +85,7 @@ struct RcSmem {
   int abort;
   int skip;
 };
+static_assert(offsetof(RcSmem, msg) % 16 == 0, "peer stores are 16-byte vectors");
 
 // ------------------------------------------------------- cluster helpers
 __device__ __forceinline__ uint32_t cluster_addr(const void *local, int rank) {
@@ -259,7 +263,8 @@ __device__ __forceinline__ void slice_weights(const unsigned char *tb, const uns
 // over the slice), else the slice's last element of positive weight, -1 if
 // none; without, -1 and only the slice total in *total. Every thread returns
 // the same values.
-__device__ int slice_draw(RcSmem &sh, int warp, int lane, const unsigned char *tb,
+template <class Smem>
+__device__ int slice_draw(Smem &sh, int warp, int lane, const unsigned char *tb,
                           const unsigned char *db, int e0, int nvec, float c, float mt,
                           float invSt, float md, float invSd, bool search, float carry,
                           float target, float *total) {
@@ -576,29 +581,322 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
   cluster.sync();   // no CTA leaves while a peer may still write to it
 }
 
-}  // namespace
+// ------------------------------------------- small calls: whole requests
+// Small calls with rows longer than the fused kernel takes (dense bf16
+// logits, V % 8 == 0, at most RQ_MAX_K drafts): a cluster verifies one
+// request at a time with all of its rows resident at once. Lane i of warp 0
+// copies the CTA's slice of the request's row i (target rows 1..K+1, then
+// draft rows 1..K) into shared memory; each warp reduces whole row slices;
+// one exchange carries every position's slice statistics; every CTA then
+// decides all positions on the same merged bits, and the final token is
+// drawn from the resident rows with one more exchange. Two exchanges per
+// request, however many drafts it has.
+constexpr int RQ_MAX_K = 8;
+constexpr int RQ_ROWS = 2 * RQ_MAX_K + 1;
+// A cluster takes one request at a time, so the call's time grows with the
+// rounds of requests per cluster: above this many requests the streaming
+// and eager schedules, which spread every row over the whole GPU, are faster.
+constexpr int RQ_MAX_B = 128;
 
-bool resident_supported(const LinearArgs &a) {
-  return a.dk == SPEC_DRAFT_LOGITS && a.rule == SPEC_RULE_STRICT && !a.want_kl &&
-         !a.want_rank && a.out_rank == nullptr && a.tdt == SPEC_BF16 && a.ddt == SPEC_BF16 &&
-         a.V % 8 == 0 && a.V >= RC_MIN_V &&
-         (a.V / 8 + RC_CLUSTER - 1) / RC_CLUSTER * 8 <= RC_SLICE_MAX;
+struct RqSmem {
+  uint64_t bar[RQ_ROWS];                  // row slice landed
+  uint64_t xch, xch2;
+  RcMsg msg[2][RC_CLUSTER][RQ_MAX_K + 1];  // by parity, sender, position
+  float tot[2][RC_CLUSTER];
+  Part rows[RQ_ROWS];                     // this CTA's slice statistics per row
+  RowStat ts[RQ_MAX_K + 1], ds[RQ_MAX_K + 1];   // merged, per position
+  int d[RQ_MAX_K];
+  float zt[RQ_MAX_K], zd[RQ_MAX_K];
+  float scan[RC_WARPS + 1];
+  int xmin, xlast;
+  int n, next;
+  int abort;
+  int skip;
+};
+static_assert(offsetof(RqSmem, msg) % 16 == 0, "peer stores are 16-byte vectors");
+
+// Running statistics of one warp over vectors lane, lane + 32, ... of a
+// bf16 slice (element index e0 + 8 v).
+template <bool SOFTMAX>
+__device__ __forceinline__ void warp_consume(const unsigned char *buf, int nvec, int lane, int e0,
+                                             float c, RunState &st) {
+  for (int v = lane; v < nvec; v += 32)
+    consume_vec<SOFTMAX, true>(lds128(buf + 16 * v), e0 + 8 * v, c, st, INFINITY);
 }
 
-int launch_setup_stream(const LinearArgs &a, cudaStream_t stream);
+__global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS, RC_CTAS_PER_SM)
+    k_verify_cluster_small(const RcArgs ra) {
+  extern __shared__ __align__(128) unsigned char dsmem[];
+  __shared__ RqSmem sh;
+  const LinearArgs &a = ra.a;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int cid = (int)(blockIdx.x / RC_CLUSTER), ncl = (int)(gridDim.x / RC_CLUSTER);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-int launch_verify_resident(const LinearArgs &a, cudaStream_t stream) {
-  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
-  static int clusters = -1;   // co-resident clusters of this shape, asked once
-  const size_t smem = RC_DYN_SMEM;
-  if (cudaFuncSetAttribute(k_verify_resident, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  if (clusters < 0) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < RQ_ROWS; ++i) mbar_init(&sh.bar[i], 1);
+    mbar_init(&sh.xch, RC_CLUSTER);
+    mbar_init(&sh.xch2, RC_CLUSTER);
+    sh.abort = 0;
+    sh.skip = *(volatile int *)&a.hdr->setup_bad;
+    fence_mbar_init();
+  }
+  cluster.sync();   // barriers initialised everywhere before any remote arrival
+  if (sh.skip) {    // inputs rejected by the setup: nothing is verified
+    const int W = a.max_k + 1;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)a.B * W;
+         i += (long long)gridDim.x * blockDim.x) {
+      GST(a.out_tokens + i, -1);
+      if (i < a.B) GST(a.out_accepted + i, -1);
+    }
+    cluster.sync();
+    return;
+  }
+  const int V = a.V, W = a.max_k + 1;
+  const int e0 = min(V, rank * ra.slice);
+  const int nvec = (min(V, e0 + ra.slice) - e0) / 8;
+  const size_t rbytes = (size_t)ra.slice * 2;   // row stride in shared memory
+  volatile int *abort = &sh.abort;
+  const uint64_t seed = seed_of(a);
+  unsigned row_ct[RQ_ROWS];   // phases of each row barrier used (thread-private copies agree)
+  for (int i = 0; i < RQ_ROWS; ++i) row_ct[i] = 0;
+  unsigned xch_ct = 0, xch2_ct = 0;
+  bool failed = false;
+
+  int b = cid;
+  while (b < a.B && !failed) {
+    const ReqInfo r = GLD(a.req + b);
+    const bool sample = r.mode == MODE_SAMPLE;
+    const float c = r.c;
+    const int K = r.K;
+    const int nrows = K + 1 + (sample ? K : 0);
+    // 1. every row slice of the request, one bulk copy each; the decision
+    // inputs; the cluster's next request (rank 0)
+    if (warp == 0 && lane < nrows) {
+      const bool tgt = lane <= K;
+      const char *row = tgt ? a.target + (long long)(r.t0 + lane) * a.t_row_bytes
+                            : a.draft + (long long)(r.d0 + lane - K - 1) * a.d_row_bytes;
+      const uint32_t nb = (uint32_t)nvec * 16u;
+      if (nb > 0) {
+        mbar_arrive_tx(&sh.bar[lane], nb);
+        bulk_g2s(dsmem + lane * rbytes, row + 2LL * e0, nb, &sh.bar[lane]);
+      } else {
+        mbar_arrive(&sh.bar[lane]);
+      }
+    }
+    if (threadIdx.x < K) {
+      const int j = threadIdx.x;
+      sh.d[j] = GLD(a.tokens + r.d0 + j);
+      sh.zt[j] = GLDCG(a.rank_thr + r.t0 + j);
+      sh.zd[j] = sample ? GLDCG(a.zd_at + r.d0 + j) : 0.f;
+    }
+    int nxt = -1;
+    if (threadIdx.x == 0 && rank == 0) nxt = ncl + (int)atomicAdd(&a.hdr->work, 1u);
+    // 2. slice statistics, one row per warp at a time
+    for (int i = warp; i < nrows; i += RC_WARPS) {
+      if (!mbar_wait_bounded(&sh.bar[i], row_ct[i] & 1u, abort)) {
+        *abort = 1;
+        failed = true;
+        break;
+      }
+      RunState st{NO_MAX, pk2(0.f, 0.f), INT_MAX, 0, 0u};
+      if (c != 0.f) warp_consume<true>(dsmem + i * rbytes, nvec, lane, e0, c, st);
+      else warp_consume<false>(dsmem + i * rbytes, nvec, lane, e0, c, st);
+      const Part p = finish_row_chunk<false>(st, c);
+      if (lane == 0) sh.rows[i] = p;
+    }
+    for (int i = 0; i < nrows; ++i) ++row_ct[i];
+    failed = __syncthreads_or(failed);
+    if (failed) break;
+    // 3. one exchange: lane k of warp 0 sends every position's slice
+    // statistics to rank k
+    const int par = (int)(xch_ct & 1u);
+    if (warp == 0) {
+      const int nx = __shfl_sync(0xffffffffu, nxt, 0);
+      if (lane < RC_CLUSTER) {
+        for (int p = 0; p <= K; ++p) {
+          const Part t = sh.rows[p];
+          const Part d = sample && p < K ? sh.rows[K + 1 + p] : Part{NO_MAX, 0.f, INT_MAX, 0};
+          const uint32_t m = cluster_addr(&sh.msg[par][rank][p], lane);
+          st_cluster_v4(m, make_uint4(__float_as_uint(t.m), __float_as_uint(t.S), (unsigned)t.idx,
+                                      __float_as_uint(d.m)));
+          st_cluster_v4(m + 16, make_uint4(__float_as_uint(d.S), (unsigned)nx, 0u, 0u));
+        }
+        mbar_arrive_cluster(cluster_addr(&sh.xch, lane));
+      }
+    }
+    failed = !mbar_wait_cluster_bounded(&sh.xch, xch_ct & 1u, abort);
+    ++xch_ct;
+    failed = __syncthreads_or(failed);
+    if (failed) break;
+    // 4. merged statistics per position (rank order: the same bits in every
+    // CTA), then the decisions in order; p(d), q(d) for every position
+    if ((int)threadIdx.x <= K) {
+      const int p = threadIdx.x;
+      RowStat ts{NO_MAX, 0.f, INT_MAX}, ds{NO_MAX, 0.f, INT_MAX};
+      for (int k = 0; k < RC_CLUSTER; ++k) {
+        const RcMsg &m = sh.msg[par][k][p];
+        merge_stat(ts.m, ts.S, ts.idx, m.tm, m.tS, m.tidx, c);
+        if (sample && p < K) merge_stat(ds.m, ds.S, ds.idx, m.dm, m.dS, INT_MAX, c);
+      }
+      sh.ts[p] = ts;
+      sh.ds[p] = ds;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int n = K;
+      for (int j = 0; j < K; ++j) {
+        const int d = sh.d[j];
+        const RowStat ts = sh.ts[j], ds = sh.ds[j];
+        const bool dok = (unsigned)d < (unsigned)V;
+        float pdv, qdv;
+        bool rej;
+        if (!sample) {
+          rej = !(dok && d == ts.idx);
+          pdv = rej ? 0.f : 1.f;
+          qdv = -1.f;
+        } else if (dok && !row_empty(ts.m)) {
+          pdv = ex2((sh.zt[j] - ts.m) * c) / ts.S;
+          qdv = row_empty(ds.m) ? 0.f : ex2((sh.zd[j] - ds.m) * c) / ds.S;
+          const float acc = qdv <= pdv ? 1.f : pdv / qdv;
+          rej = !(uniform24(seed, (uint32_t)b, (uint32_t)(j + 1), 0) < acc);
+        } else {
+          pdv = qdv = 0.f;
+          rej = true;
+        }
+        if (rank == 0) {
+          if (!dok || row_empty(ts.m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+          if (a.out_pq) {
+            GST(a.out_pq + 2LL * (r.d0 + j), pdv);
+            GST(a.out_pq + 2LL * (r.d0 + j) + 1, qdv);
+          }
+        }
+        if (rej && n == K) n = j;
+      }
+      if (rank == 0 && row_empty(sh.ts[K].m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+      sh.n = n;
+      sh.next = sh.msg[par][0][0].next;
+    }
+    __syncthreads();
+    const int n = sh.n, next = sh.next;
+    // 5. commit: the accepted drafts, then -1 after the final slot
+    if (rank == 0) {
+      int32_t *out = a.out_tokens + (long long)b * W;
+      for (int jj = threadIdx.x; jj < W; jj += RC_THREADS)
+        if (jj != n) GST(out + jj, jj < n ? sh.d[jj] : -1);
+      if (threadIdx.x == 0) {
+        GST(a.out_accepted + b, n);
+        if (!sample) GST(out + n, sh.ts[n].idx);   // greedy: the target's argmax
+      }
+    }
+    // 6. the final draw from position n's resident rows
+    if (sample) {
+      const RowStat ts = sh.ts[n], ds = sh.ds[n];
+      const unsigned char *tb = dsmem + n * rbytes;
+      const unsigned char *db = dsmem + (K + 1 + n) * rbytes;
+      const float invSt = 1.f / ts.S;
+      int owner = -1, x = -1;
+      float carry = 0.f, target = 0.f;
+      bool from_p = true;
+      const float u = uniform24(seed, (uint32_t)b, (uint32_t)(n + 1), n < K ? 1u : 2u);
+      if (n < K) {
+        const float invSd = ds.S > 0.f ? 1.f / ds.S : 0.f;
+        float R;
+        slice_draw(sh, warp, lane, tb, db, e0, nvec, c, ts.m, invSt, ds.m, invSd, false, 0.f,
+                      0.f, &R);
+        const int p2 = (int)(xch2_ct & 1u);
+        if (warp == 0 && lane < RC_CLUSTER) {
+          st_cluster_f32(cluster_addr(&sh.tot[p2][rank], lane), R);
+          mbar_arrive_cluster(cluster_addr(&sh.xch2, lane));
+        }
+        failed = !mbar_wait_cluster_bounded(&sh.xch2, xch2_ct & 1u, abort);
+        ++xch2_ct;
+        failed = __syncthreads_or(failed);
+        if (failed) break;
+        float Z = 0.f;
+        int klast = -1;
+        for (int k = 0; k < RC_CLUSTER; ++k) {
+          Z += sh.tot[p2][k];
+          if (sh.tot[p2][k] > 0.f) klast = k;
+        }
+        if (Z > 0.f) {
+          target = u * Z;
+          for (int k = 0; k < RC_CLUSTER; ++k) {
+            const float nc = carry + sh.tot[p2][k];
+            if (nc > target) {
+              owner = k;
+              break;
+            }
+            carry = nc;
+          }
+          if (owner < 0) owner = klast;
+          from_p = false;
+          if (owner == rank) {   // its slice total is positive: x >= 0
+            float dummy;
+            x = slice_draw(sh, warp, lane, tb, db, e0, nvec, c, ts.m, invSt, ds.m, invSd,
+                              true, carry, target, &dummy);
+          }
+        }
+      }
+      if (from_p) {   // bonus, or a residual without mass: p by slice masses
+        float Zp = 0.f, mk[RC_CLUSTER];
+        int klast = -1;
+        for (int k = 0; k < RC_CLUSTER; ++k) {
+          const RcMsg &m = sh.msg[par][k][n];
+          mk[k] = m.tS > 0.f ? m.tS * ex2((m.tm - ts.m) * c) * invSt : 0.f;
+          Zp += mk[k];
+          if (mk[k] > 0.f) klast = k;
+        }
+        target = u * Zp;
+        for (int k = 0; k < RC_CLUSTER && Zp > 0.f; ++k) {
+          const float nc = carry + mk[k];
+          if (nc > target) {
+            owner = k;
+            break;
+          }
+          carry = nc;
+        }
+        if (owner < 0) owner = klast;
+        if (owner == rank) {
+          float dummy;
+          x = slice_draw(sh, warp, lane, tb, nullptr, e0, nvec, c, ts.m, invSt, 0.f, 0.f, true,
+                            carry, target, &dummy);
+        }
+        if (owner < 0) owner = 0;   // no mass anywhere: rank 0 reports it
+      }
+      if (owner == rank && threadIdx.x == 0) {
+        if (x < 0) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);   // a row without mass
+        GST(a.out_tokens + (long long)b * W + n, x);
+      }
+    }
+    __syncthreads();   // the rows are free for the next request's copies
+    b = next;
+  }
+  if (failed && threadIdx.x == 0) set_status(a.hdr, SPEC_ERR_TIMEOUT, -7);
+  cluster.sync();   // no CTA leaves while a peer may still write to it
+}
+
+}  // namespace
+
+bool cluster_small_supported(const LinearArgs &a, const spec_linear_ext *ext,
+                             size_t limit_bytes) {
+  if (limit_bytes == 0 || a.B > RQ_MAX_B) return false;
+  if (ext != nullptr && (ext->flags != 0 || ext->out_kl != nullptr || ext->out_rank != nullptr))
+    return false;
+  if ((a.rule != SPEC_RULE_STRICT && a.rule != SPEC_RULE_GREEDY) || a.dk != SPEC_DRAFT_LOGITS ||
+      a.tdt != SPEC_BF16 || a.ddt != SPEC_BF16 || a.V % 8 != 0 || a.max_k > RQ_MAX_K)
+    return false;
+  const size_t slice = (size_t)(a.V / 8 + RC_CLUSTER - 1) / RC_CLUSTER * 8;
+  return (size_t)(2 * a.max_k + 1) * slice * 2 <= RC_DYN_SMEM;
+}
+
+static int cluster_count(const void *kernel, int *cache) {
+  if (*cache < 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(RC_CLUSTER * num_sms(), 1, 1);
     cfg.blockDim = dim3(RC_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = RC_DYN_SMEM;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = RC_CLUSTER;
@@ -607,10 +905,47 @@ int launch_verify_resident(const LinearArgs &a, cudaStream_t stream) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_verify_resident, &cfg) != cudaSuccess || n <= 0)
-      return SPEC_ERR_CUDA;
-    clusters = n;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) return -1;
+    *cache = n;
   }
+  return *cache;
+}
+
+int launch_setup_stream(const LinearArgs &a, cudaStream_t stream);
+
+int launch_verify_cluster_small(const LinearArgs &a, cudaStream_t stream) {
+  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
+  static int clusters = -1;   // co-resident clusters of this shape, asked once
+  if (cudaFuncSetAttribute(k_verify_cluster_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)RC_DYN_SMEM) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  const int n = cluster_count((const void *)k_verify_cluster_small, &clusters);
+  if (n <= 0) return SPEC_ERR_CUDA;
+  const int rc = launch_setup_stream(a, stream);
+  if (rc != SPEC_OK) return rc;
+  RcArgs ra;
+  ra.a = a;
+  ra.slice = (a.V / 8 + RC_CLUSTER - 1) / RC_CLUSTER * 8;
+  const int grid_clusters = std::min(n, a.B);
+  k_verify_cluster_small<<<RC_CLUSTER * grid_clusters, RC_THREADS, RC_DYN_SMEM, stream>>>(ra);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+bool resident_supported(const LinearArgs &a) {
+  return a.dk == SPEC_DRAFT_LOGITS && a.rule == SPEC_RULE_STRICT && !a.want_kl &&
+         !a.want_rank && a.out_rank == nullptr && a.tdt == SPEC_BF16 && a.ddt == SPEC_BF16 &&
+         a.V % 8 == 0 && a.V >= RC_MIN_V &&
+         (a.V / 8 + RC_CLUSTER - 1) / RC_CLUSTER * 8 <= RC_SLICE_MAX;
+}
+
+int launch_verify_resident(const LinearArgs &a, cudaStream_t stream) {
+  if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
+  static int clusters = -1;   // co-resident clusters of this shape, asked once
+  const size_t smem = RC_DYN_SMEM;
+  if (cudaFuncSetAttribute(k_verify_resident, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (cluster_count((const void *)k_verify_resident, &clusters) <= 0) return SPEC_ERR_CUDA;
   const int rc = launch_setup_stream(a, stream);
   if (rc != SPEC_OK) return rc;
   RcArgs ra;

@@ -73,6 +73,7 @@ LINEAR_CASES = [
     ("kl", dict(cfg=1, B=4, K=3, V=16, dtype="bf16"), dict(kl=True), 0, False),
     ("resident", dict(cfg=1, B=2, K=2, V=16384, dtype="bf16"), dict(resident=True, rank=False),
      0, True),
+    ("cluster-small", dict(cfg=1, B=4, K=3, V=16384, dtype="bf16"), {}, 32 << 20, False),
 ]
 
 

@@ -19,6 +19,7 @@ CASES = [
     ("resident", dict(cfg=5, B=64, resident=True)),
     ("top-128", dict(cfg=3, B=16)),
     ("fused", dict(cfg=1)),
+    ("cluster per request", dict(cfg=2)),
     ("stream", dict(cfg=5, B=64, lazy=True)),
     ("lazy rounds", dict(cfg=3, B=16, lazy=True)),
     ("cactus", dict(cfg=5, B=64, rule="cactus")),

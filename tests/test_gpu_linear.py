@@ -538,6 +538,50 @@ def test_resident_schedule_reports_invalid_inputs():
     assert gpu_linear(lb, resident=True, rank=False)["status"] == sv.SPEC_OK
 
 
+# Small calls of longer bf16 rows (at most 128 requests and 8 drafts, row
+# slices of V/8 fitting a cluster's shared memory) run as one cluster per
+# request with every row resident: the same results as the multi-kernel path
+# and the oracle, p(d) and q(d) for every position (every row is read).
+CLUSTER_SMALL_CASES = [
+    dict(B=64, K=(1, 5), V=32000, sigma=0.7, T=[0.0, 0.7] * 32),
+    dict(B=1, K=8, V=16384, sigma=0.2, T=1.0),
+    dict(B=128, K=(0, 4), V=20000, sigma=1.2, T=("uniform", 0.0, 1.4)),
+    dict(B=37, K=3, V=36864, sigma=0.9, T=[1.3, 0.5, 0.01] * 12 + [0.9]),
+    dict(B=9, K=(2, 8), V=9000, sigma=0.5, T=0.8),
+]
+
+
+@pytest.mark.parametrize("over", CLUSTER_SMALL_CASES)
+def test_cluster_small_calls_equal_the_multi_kernel_path_and_the_oracle(over):
+    lb = S.make_linear(2, device=DEV, input_seed=7272, dtype="bf16", **over)
+    old = sv.spec_set_fused_limit(32 << 20)
+    try:
+        g = gpu_linear(lb)
+        assert g["status"] == sv.SPEC_OK
+        again = gpu_linear(lb)                      # bitwise deterministic
+        assert np.array_equal(again["tokens"], g["tokens"])
+        assert np.array_equal(again["pq"], g["pq"])
+        sv.spec_set_fused_limit(0)
+        e = gpu_linear(lb)                          # the multi-kernel path
+    finally:
+        sv.spec_set_fused_limit(old)
+    assert np.array_equal(g["accepted"], e["accepted"])
+    ref = oracle_linear(lb)
+    for b in np.nonzero((g["tokens"] != e["tokens"]).any(1))[0]:
+        assert ref["flag_slot"][b] >= 0, ("differs from the multi-kernel path unflagged", b)
+    assert_linear_parity(g, ref, lb.cu_draft.cpu(), min_compared=int((ref["flag_slot"] < 0).sum()))
+
+
+def test_cluster_small_reports_invalid_inputs():
+    lb = S.make_linear(2, device=DEV, B=6, K=3, V=16384, dtype="bf16", T=1.0, input_seed=3)
+    assert gpu_linear(lb)["status"] == sv.SPEC_OK
+    bad = lb.draft_tokens.clone()
+    bad[2] = -5
+    b2 = S.LinearBatch(**{**lb.__dict__, "draft_tokens": bad})
+    g = gpu_linear(b2)
+    assert g["status"] == sv.SPEC_ERR_INVALID_ARG and np.all(g["accepted"] == -1)
+
+
 def test_stream_schedule_invalid_inputs_and_empty_rows():
     lb = S.make_linear(1, device=DEV, B=6, K=3, V=4096, dtype="bf16", T=1.0, input_seed=3)
     clean = gpu_linear(lb, lazy=True)
