@@ -815,6 +815,8 @@ def timed_calls(work, sv, dev, steps, warmup, world):
             ev_s[k].record()
         sv.spec_profile_row_pass(ev_b[k], ev_a[k])
         work.call()
+        if k == 0 and sv.spec_profile_pending():
+            raise RuntimeError(f"{work.kernel}: the call recorded no profiling events")
         if flush:
             ev_e[k].record()
     e1.record()

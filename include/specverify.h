@@ -511,11 +511,19 @@ int spec_wait_selftest(int kind, unsigned long long limit_ns, void *workspace,
  * row once), the top-128 select under SPEC_RULE_STRICT_TOP128, the streaming
  * kernel of a position-lazy call (SPEC_EXT_LAZY) or,
  * on its multi-launch schedule, all its rounds (every row pass and every
- * per-round decision), the walk of a tree call, and the top-128 select of
- * spec_rheo_expand. So
+ * per-round decision), the one kernel of a small call (fused or one cluster
+ * per request), the cluster-resident kernel (SPEC_EXT_RESIDENT), the walk of
+ * a tree call, and the top-128 select of spec_rheo_expand. So
  * cudaEventElapsedTime(before, after) is that kernel's duration.
  */
 int spec_profile_row_pass(void *before, void *after);
+
+/*
+ * 1 while events registered with spec_profile_row_pass on the calling host
+ * thread have not been taken by a call, else 0: after a call it tells whether
+ * that call recorded them.
+ */
+int spec_profile_pending(void);
 
 #ifdef __cplusplus
 }

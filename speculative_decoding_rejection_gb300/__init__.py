@@ -20,7 +20,7 @@ __all__ = [
     "spec_verify_linear", "spec_verify_linear_ext", "spec_verify_linear_workspace", "spec_verify_tree",
     "spec_verify_tree_workspace", "spec_verify_tree_ext", "draft_topk_softmax",
     "draft_topk_softmax_workspace", "spec_get_status", "spec_uniforms",
-    "spec_profile_row_pass", "spec_rheo_expand", "spec_rheo_expand_workspace",
+    "spec_profile_row_pass", "spec_profile_pending", "spec_rheo_expand", "spec_rheo_expand_workspace",
     "spec_set_fused_limit", "SpecError", "use_checked_library", "spec_check_selftest",
 ]
 
@@ -83,6 +83,7 @@ _SIGS = {
     "spec_set_fused_limit": (_sz, [_sz]),
     "spec_uniforms": (_i32, [_u64, _vp, _vp, _vp, _i32, _vp, _vp]),
     "spec_profile_row_pass": (_i32, [_vp, _vp]),
+    "spec_profile_pending": (_i32, []),
     "spec_wait_selftest": (_i32, [_i32, ctypes.c_ulonglong, _vp, _vp]),
     "spec_check_selftest": (_i32, [_vp, _sz, _vp]),
     "spec_verify_linear_noalloc": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i32,
@@ -420,3 +421,9 @@ def spec_profile_row_pass(before=None, after=None):
             e.record()
         return ctypes.c_void_p(e.cuda_event)
     _check(lib().spec_profile_row_pass(ev(before), ev(after)), "spec_profile_row_pass")
+
+
+def spec_profile_pending() -> bool:
+    """True while events registered with spec_profile_row_pass have not been
+    taken by a call: after a call, whether that call recorded them."""
+    return bool(lib().spec_profile_pending())

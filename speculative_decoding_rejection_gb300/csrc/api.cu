@@ -150,3 +150,5 @@ extern "C" int spec_profile_row_pass(void *before, void *after) {
   set_row_pass_events(reinterpret_cast<cudaEvent_t>(before), reinterpret_cast<cudaEvent_t>(after));
   return SPEC_OK;
 }
+
+extern "C" int spec_profile_pending(void) { return row_pass_events_pending() ? 1 : 0; }

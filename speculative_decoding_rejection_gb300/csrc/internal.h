@@ -51,6 +51,7 @@ struct RowPassArgs {
 
 int num_sms();
 void set_row_pass_events(cudaEvent_t before, cudaEvent_t after);
+bool row_pass_events_pending();
 // Hands the registered events to a caller that brackets several launches
 // itself (and unregisters them).
 void take_row_pass_events(cudaEvent_t *before, cudaEvent_t *after);

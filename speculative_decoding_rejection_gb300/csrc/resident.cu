@@ -927,8 +927,13 @@ int launch_verify_cluster_small(const LinearArgs &a, cudaStream_t stream) {
   ra.a = a;
   ra.slice = (a.V / 8 + RC_CLUSTER - 1) / RC_CLUSTER * 8;
   const int grid_clusters = std::min(n, a.B);
+  cudaEvent_t before, after;
+  take_row_pass_events(&before, &after);
+  if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   k_verify_cluster_small<<<RC_CLUSTER * grid_clusters, RC_THREADS, RC_DYN_SMEM, stream>>>(ra);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
 }
 
 bool resident_supported(const LinearArgs &a) {

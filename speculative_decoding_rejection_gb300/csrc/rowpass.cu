@@ -337,6 +337,8 @@ void take_row_pass_events(cudaEvent_t *before, cudaEvent_t *after) {
   prof_before = prof_after = nullptr;
 }
 
+bool row_pass_events_pending() { return prof_before != nullptr || prof_after != nullptr; }
+
 int launch_row_pass(const RowPassArgs &a, cudaStream_t stream) {
   if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
   const int sms = num_sms();

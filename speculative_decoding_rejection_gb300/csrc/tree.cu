@@ -20,16 +20,19 @@
 // u(seed, b, v + 1, 1) (residual) or u(seed, b, v + 1, 2) (bonus), so a chain
 // tree reproduces the linear verifier draw for draw.
 //
-// Pipeline: a one-block-per-tree setup kernel validates every tree; then a
-// cluster of CTAs per tree walks it. The walk reads only the rows of the
-// nodes it visits (the others never enter the decision): at each visited
+// Pipeline: a one-block-per-tree setup kernel validates every tree and
+// writes its child lists (per node: the children in node-index order, each
+// with its token, the parent's two logits at that token and its own list);
+// then a cluster of CTAs per tree walks it. The walk reads only the rows of
+// the nodes it visits (the others never enter the decision): at each visited
 // node the cluster first reduces the node's target row (and, for a sampling
 // node with children, its draft row) to max / normaliser / argmax, each CTA
 // over its vocabulary slice, then tests the children. When the slices fit,
-// each CTA copies its slice of the node's rows into shared memory with one
-// TMA bulk copy per row as it reaches the node (the target row at once, the
-// draft row once the node's children are known), and every pass over the
-// node (statistics, residuals, the final draw) reads shared memory. The residual laws are
+// each CTA copies its slices of the node's rows into shared memory with one
+// TMA bulk copy per row as soon as it reaches the node (the node's record
+// says whether it has children), loads the children's records meanwhile,
+// and every pass over the node (statistics, residuals, the final draw) reads
+// shared memory, bf16 slices with packed arithmetic. The residual laws are
 // never stored: every pass recomputes
 // p_j(y) from p(y) and q(y) through the chain of normalisers, which are
 // scalars. A token rejected at step k has q_k > p_k, so p_{k+1} is exactly 0
@@ -59,11 +62,30 @@ constexpr int MAX_SLICE_TILES = (MAX_WALK_TILES + WALK_CLUSTER - 1) / WALK_CLUST
 constexpr size_t WALK_STAGE_MAX = 96 * 1024;
 
 struct TreeInfo {
-  int base;   // first node row
-  int N;      // nodes
-  int mode;   // ReqMode
-  float c;    // log2(e)/T
+  int base;        // first node row
+  int N;           // nodes
+  int mode;        // ReqMode
+  float c;         // log2(e)/T
+  int root_kids;   // children of the root (its list starts at 0)
+  int pad[3];
 };
+
+// One child in its parent's list (the setup writes every tree's lists, each
+// parent's children contiguous in node-index order): x packs the child's local
+// id (bits 0-11), its own number of children (bits 12-18), its point-mass flag
+// (bit 19) and the start of its own list (bits 20-31); y is its token; z, w
+// the bits of the parent's target and draft logits (or probability) at that
+// token, which the child's coin needs (0 in greedy trees).
+struct KidRec {
+  int x, y;
+  float z, w;
+};
+__device__ __forceinline__ int kid_id(int x) { return x & 0xfff; }
+__device__ __forceinline__ int kid_count(int x) { return (x >> 12) & 0x7f; }
+__device__ __forceinline__ int kid_fixed(int x) { return (x >> 19) & 1; }
+__device__ __forceinline__ int kid_start(int x) { return (int)((unsigned)x >> 20); }
+static_assert(SPEC_MAX_TREE_NODES <= 4096 && SPEC_MAX_TREE_BRANCH <= 127,
+              "child records pack ids and counts in 12 and 7 bits");
 
 struct TreeArgs {
   const char *target;
@@ -80,6 +102,7 @@ struct TreeArgs {
   int32_t *out_tokens, *out_accepted, *out_path;
   WsHeader *hdr;
   TreeInfo *tree;
+  KidRec *kids;   // [n_nodes]: every tree's child lists at its node rows
   long long t_row_bytes, d_row_bytes;
   int staged;    // row slices are copied to shared memory
   int dsm_off;   // byte offset of the draft slice in the dynamic shared memory
@@ -91,14 +114,15 @@ __device__ __forceinline__ uint64_t tree_seed(const TreeArgs &a) {
 }
 
 struct TreeLayout {
-  size_t hdr, tree, total;
+  size_t hdr, tree, kids, total;
 };
 
-static TreeLayout tree_layout(int B) {
+static TreeLayout tree_layout(int B, int n_nodes) {
   TreeLayout L;
   size_t o = 0;
   L.hdr = o;  o += align256(sizeof(WsHeader));
   L.tree = o; o += align256(sizeof(TreeInfo) * (size_t)B);
+  L.kids = o; o += align256(sizeof(KidRec) * (size_t)n_nodes);
   L.total = o;
   return L;
 }
@@ -106,8 +130,11 @@ static TreeLayout tree_layout(int B) {
 // ------------------------------------------------------------------ setup
 // One block per tree. The tree's parent ids are staged in shared memory; one
 // thread derives depths in topological order, the block counts children and
-// checks tokens (in the vocabulary, distinct among drawn siblings). The header was cleared before the launch; an invalid tree
-// sets the status word and the walk of every tree is skipped.
+// checks tokens (in the vocabulary, distinct among drawn siblings). The header
+// was cleared before the launch; an invalid tree sets the status word and the
+// walk of every tree is skipped. A valid tree's child lists are written for
+// the walk: the list starts are an exclusive scan of the child counts, and a
+// child's place in its list is the number of its earlier siblings.
 constexpr int SETUP_THREADS = 256;
 
 __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) {
@@ -119,6 +146,8 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
   TreeInfo ti;
   ti.base = GLD(a.cu + (b));
   ti.N = GLD(a.cu + (b + 1)) - GLD(a.cu + (b));
+  ti.root_kids = 0;
+  ti.pad[0] = ti.pad[1] = ti.pad[2] = 0;
   const float T = GLD(a.temp + (b));
   const bool greedy = T < SPEC_GREEDY_T;
   bool ok = (b > 0 || GLD(a.cu + (0)) == 0) && ti.base >= 0 && ti.N >= 1 &&
@@ -155,6 +184,16 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
     for (int c = t; c < ti.N; c += SETUP_THREADS)
       if (s_kids[c] > a.max_branch) s_bad = 1;
   __syncthreads();
+  // the depths are checked: their array now holds each node's list start
+  if (ok && !s_bad && t == 0) {
+    int start = 0;
+    for (int c = 0; c < ti.N; ++c) {
+      s_depth[c] = (unsigned short)start;
+      start += s_kids[c];
+    }
+    ti.root_kids = s_kids[0];
+  }
+  __syncthreads();
   // drawn siblings carry distinct tokens (drawn without replacement); a
   // point-mass child may repeat one. The child counts are no longer needed,
   // so their array holds each node's token, -1 where the node is exempt.
@@ -167,12 +206,28 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
   if (ok && !s_bad)
     for (int c = t + 1; c < ti.N; c += SETUP_THREADS) {
       const int x = s_kids[c], p = s_par[c];
-      if (x < 0) continue;
-      for (int o = c - 1; o > p; --o)   // earlier siblings lie between the parent and c
-        if (s_par[o] == p && s_kids[o] == x) {
-          s_bad = 1;
-          break;
+      int rank = 0;   // earlier siblings lie between the parent and c
+      for (int o = c - 1; o > p; --o)
+        if (s_par[o] == p) {
+          ++rank;
+          if (x >= 0 && s_kids[o] == x) s_bad = 1;
         }
+      // c's record in its parent's list
+      const int own = (int)s_depth[c];
+      const int n_own = (c + 1 < ti.N ? (int)s_depth[c + 1] : ti.N - 1) - own;
+      const int fixed = a.node_fixed != nullptr && GLD(a.node_fixed + (ti.base + c)) != 0;
+      const int tok = GLD(a.node_token + (ti.base + c));
+      KidRec r;
+      r.x = c | (n_own << 12) | (fixed << 19) | (own << 20);
+      r.y = tok;
+      r.z = 0.f;
+      r.w = 0.f;
+      if (!greedy) {
+        const long long rp = (long long)ti.base + p;
+        r.z = load_elem(a.target + rp * a.t_row_bytes, a.tdt, tok);
+        r.w = load_elem(a.draft + rp * a.d_row_bytes, a.ddt, tok);
+      }
+      GST(a.kids + (ti.base + (int)s_depth[p] + rank), r);
     }
   __syncthreads();
   ok = ok && !s_bad;
@@ -188,26 +243,33 @@ __global__ void __launch_bounds__(SETUP_THREADS) k_setup_tree(const TreeArgs a) 
 struct WalkSmem {
   float tsum[MAX_SLICE_TILES];           // tile totals of this CTA's slice
   float wsum[64 * (WALK_THREADS / 32)];  // per-warp tile sums of one batch
-  float zr[2];                           // this slice's total, by pass parity
+  float zx[2][WALK_CLUSTER];             // every slice's total, pushed by its CTA, by pass parity
   float zall[WALK_CLUSTER];              // every slice's total of the last pass
   float scratch[33];
-  int kids[SPEC_MAX_TREE_BRANCH];
-  int kx[SPEC_MAX_TREE_BRANCH];          // children's tokens
-  int kfix[SPEC_MAX_TREE_BRANCH + 1];    // point-mass child (its level of the chain)
-  float kzt[SPEC_MAX_TREE_BRANCH];       // target logit at each child's token
-  float kzd[SPEC_MAX_TREE_BRANCH];       // draft logit (or probability) there
+  // the children of the node being walked, by node parity (the threads decide
+  // its coins without a barrier, so a fast one may load the next node's while
+  // a slow one still reads these)
+  int kids[2][SPEC_MAX_TREE_BRANCH];
+  int knext[2][SPEC_MAX_TREE_BRANCH];    // each child's packed record (its own list)
+  int kx[2][SPEC_MAX_TREE_BRANCH];       // children's tokens
+  int kfix[2][SPEC_MAX_TREE_BRANCH + 1]; // point-mass child (its level of the chain)
+  float kzt[2][SPEC_MAX_TREE_BRANCH];    // target logit at each child's token
+  float kzd[2][SPEC_MAX_TREE_BRANCH];    // draft logit (or probability) there
+  float ucoin[2][SPEC_MAX_TREE_BRANCH];  // the uniform of each child's coin
   float s[SPEC_MAX_TREE_BRANCH + 1];     // 1 / (1 - q(E_j))
   float rinv[SPEC_MAX_TREE_BRANCH + 1];  // 1 / Z_j
   int skip[SPEC_MAX_TREE_BRANCH + 1];    // Z_j == 0: p_{j+1} = p_j
   RowStat wst[WALK_THREADS / 32][2];     // per-warp statistics of a node pass (target, draft)
-  RowStat st[2][2];                      // this slice's statistics, by pass parity (target, draft)
+  RowStat xst[2][WALK_CLUSTER][2];       // every slice's statistics, pushed by its CTA, by pass
+                                         // parity (target, draft)
   RowStat node[2];                       // the node's statistics (target, draft)
   uint64_t bar_t, bar_d;                 // completion of the staged target / draft slice
-  int nk, jstar, xmin, xlast, rstar, accepted_child, par, ok, go, never;
-  float carry, target, Z, pfix;
+  int jstar, xmin, xlast, rstar, par, ok, go, never;
+  float carry, target, Z;
 };
 
 struct NodeLaw {        // p(y) = 2^((zt - mt) c) / St, q(y) likewise or given
+  const int *kx, *kfix;             // the node's children: tokens, point-mass flags
   const char *trow, *drow;
   const unsigned char *tsm, *dsm;   // this CTA's staged slices, or null
   long long e0;                     // first element of the slice
@@ -269,11 +331,11 @@ __device__ __forceinline__ void wait_slice(const TreeArgs &a, WalkSmem &sh, uint
 }
 
 // Thread 0 copies this CTA's slice [e0, e1) of `row` into `dst`, completion
-// on `bar`.
+// on `bar` (one bulk copy: splitting it to reduce pieces as they land
+// measured slower).
 __device__ __forceinline__ void stage_slice(uint64_t *bar, unsigned char *dst, const char *row,
                                             int esz, long long e0, long long e1) {
   const uint32_t bytes = (uint32_t)((e1 - e0) * esz);
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_arrive_tx(bar, bytes);
   bulk_g2s(dst, row + e0 * esz, bytes, bar);
 }
@@ -289,14 +351,35 @@ __device__ __forceinline__ Slice my_slice(int V, int rank) {
 // p(y), q(y) of token y through the chain of normalisers. A point-mass level
 // removes its own token and rescales the rest.
 __device__ __forceinline__ float chain_weight(float p, float q, int y, int L, bool residual,
-                                              const WalkSmem &sh) {
+                                              const WalkSmem &sh, const NodeLaw &nl) {
   for (int i = 0; i < L; ++i) {
     if (sh.skip[i]) continue;
-    p = sh.kfix[i] ? (y == sh.kx[i] ? 0.f : p * sh.rinv[i])
+    p = nl.kfix[i] ? (y == nl.kx[i] ? 0.f : p * sh.rinv[i])
                    : fmaxf(0.f, p - q * sh.s[i]) * sh.rinv[i];
   }
   if (!residual) return p;
-  return sh.kfix[L] ? (y == sh.kx[L] ? 0.f : p) : fmaxf(0.f, p - q * sh.s[L]);
+  return nl.kfix[L] ? (y == nl.kx[L] ? 0.f : p) : fmaxf(0.f, p - q * sh.s[L]);
+}
+
+// p(y) (and q(y)) of the SAMPLE_EPT elements x0.. of a staged bf16 slice,
+// two per packed operation: the same roundings per element as the scalar
+// form (an exact bf16 widening, then f32 subtract, multiply, 2^x, multiply).
+__device__ __forceinline__ void staged_law_bf16(const unsigned char *sm, long long e0, int x0,
+                                                float m, float c, float inv, float *out) {
+  const unsigned char *p = sm + ((long long)x0 - e0) * 2;
+  const f32x2 c2 = pk2(c, c), i2 = pk2(inv, inv);
+#pragma unroll
+  for (int h = 0; h < SAMPLE_EPT / 8; ++h) {
+    const uint4 v = lds128(p + 16 * h);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const f32x2 t = mul2(bsub2(wv[q], m), c2);
+      const f32x2 e = mul2(pk2(ex2(lo2(t)), ex2(hi2(t))), i2);
+      out[8 * h + 2 * q] = lo2(e);
+      out[8 * h + 2 * q + 1] = hi2(e);
+    }
+  }
 }
 
 template <int DK>
@@ -304,24 +387,34 @@ __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkS
                                                   const NodeLaw &nl, float c, int L,
                                                   bool residual, int j, float *w) {
   const int x0 = j * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
-  float zt[SAMPLE_EPT], zd[SAMPLE_EPT];
-  load_row_ept(nl.trow, nl.tsm, nl.e0, a.tdt, nl.tvec, x0, a.V, -INFINITY, zt);
+  const bool full = x0 + SAMPLE_EPT <= a.V;
+  if (full && nl.tsm != nullptr && a.tdt == SPEC_BF16) {
+    staged_law_bf16(nl.tsm, nl.e0, x0, nl.mt, c, nl.invSt, w);
+  } else {
+    float zt[SAMPLE_EPT];
+    load_row_ept(nl.trow, nl.tsm, nl.e0, a.tdt, nl.tvec, x0, a.V, -INFINITY, zt);
 #pragma unroll
-  for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = ex2((zt[k] - nl.mt) * c) * nl.invSt;
+    for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = ex2((zt[k] - nl.mt) * c) * nl.invSt;
+  }
   if (L == 0 && !residual) return;
-  load_row_ept(nl.drow, nl.dsm, nl.e0, a.ddt, nl.dvec, x0, a.V,
-               DK == SPEC_DRAFT_PROBS ? 0.f : -INFINITY, zd);
   float q[SAMPLE_EPT];
+  if (DK == SPEC_DRAFT_LOGITS && full && nl.dsm != nullptr && a.ddt == SPEC_BF16) {
+    staged_law_bf16(nl.dsm, nl.e0, x0, nl.md, c, nl.invSd, q);
+  } else {
+    float zd[SAMPLE_EPT];
+    load_row_ept(nl.drow, nl.dsm, nl.e0, a.ddt, nl.dvec, x0, a.V,
+                 DK == SPEC_DRAFT_PROBS ? 0.f : -INFINITY, zd);
 #pragma unroll
-  for (int k = 0; k < SAMPLE_EPT; ++k)
-    q[k] = DK == SPEC_DRAFT_PROBS ? zd[k] : ex2((zd[k] - nl.md) * c) * nl.invSd;
+    for (int k = 0; k < SAMPLE_EPT; ++k)
+      q[k] = DK == SPEC_DRAFT_PROBS ? zd[k] : ex2((zd[k] - nl.md) * c) * nl.invSd;
+  }
   // the chain level by level over all elements (the same operations per
   // element as chain_weight, so the same bits)
   for (int i = 0; i < L; ++i) {
     if (sh.skip[i]) continue;
     const float si = sh.s[i], ri = sh.rinv[i];
-    if (sh.kfix[i]) {
-      const int xi = sh.kx[i];
+    if (nl.kfix[i]) {
+      const int xi = nl.kx[i];
 #pragma unroll
       for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = x0 + k == xi ? 0.f : w[k] * ri;
     } else {
@@ -330,8 +423,8 @@ __device__ __forceinline__ void tile_weights_tree(const TreeArgs &a, const WalkS
     }
   }
   if (residual) {
-    if (sh.kfix[L]) {
-      const int xL = sh.kx[L];
+    if (nl.kfix[L]) {
+      const int xL = nl.kx[L];
 #pragma unroll
       for (int k = 0; k < SAMPLE_EPT; ++k) w[k] = x0 + k == xL ? 0.f : w[k];
     } else {
@@ -372,18 +465,18 @@ __device__ void weight_pass(const TreeArgs &a, WalkSmem &sh, const NodeLaw &nl, 
     __syncthreads();
   }
   const int par = sh.par;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < WALK_CLUSTER) {   // this slice's total into every CTA's slot for it
     float Zr = 0.f;
     for (int j = sl.j0; j < sl.j1; ++j) Zr += sh.tsum[j - sl.j0];
-    sh.zr[par] = Zr;
+    *cluster.map_shared_rank(&sh.zx[par][cluster.block_rank()], (int)threadIdx.x) = Zr;
   }
-  cluster.sync();   // every slice total written (slots alternate by parity)
-  if (threadIdx.x < WALK_CLUSTER)   // one remote read per thread, in parallel
-    sh.zall[threadIdx.x] = *cluster.map_shared_rank(&sh.zr[par], (int)threadIdx.x);
-  __syncthreads();
+  cluster.sync();   // every slice total pushed (slots alternate by parity)
   if (threadIdx.x == 0) {
     float Z = 0.f;
-    for (int r = 0; r < WALK_CLUSTER; ++r) Z += sh.zall[r];
+    for (int r = 0; r < WALK_CLUSTER; ++r) {
+      sh.zall[r] = sh.zx[par][r];
+      Z += sh.zall[r];
+    }
     sh.Z = Z;
     sh.par = par ^ 1;
   }
@@ -488,6 +581,50 @@ __device__ __forceinline__ void stat_update(const float *z, int x0, float c, flo
   }
 }
 
+// One thread's statistics of a staged bf16 slice of nv 16-byte vectors
+// (element e0 first; vectors t, t + WALK_THREADS, ...), merged into its
+// running (m, S, idx): the max through packed bf16 maxima and its lowest
+// index, then the sum of 2^((z - max) c) (none when c is 0) with packed
+// subtracts, multiplies and adds, one 2^x per element.
+__device__ __forceinline__ void slice_stats_bf16(const unsigned char *sm, int nv, long long e0,
+                                                 float c, float &m, float &S, int &idx) {
+  float vm = NO_MAX;
+  int vb = -1;
+  for (int v = (int)threadIdx.x; v < nv; v += WALK_THREADS) {
+    const uint4 w = lds128(sm + 16 * (size_t)v);
+    const uint32_t a2 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+    const float x = fmaxf(bf16lo(a2), bf16hi(a2));
+    if (x > vm) {
+      vm = x;
+      vb = v;
+    }
+  }
+  if (vb < 0) return;   // nothing finite here
+  int jb = 7;
+  {
+    const uint4 w = lds128(sm + 16 * (size_t)vb);
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 7; k >= 0; --k)
+      if (((k & 1) ? bf16hi(q[k >> 1]) : bf16lo(q[k >> 1])) == vm) jb = k;
+  }
+  float ps = 0.f;
+  if (c != 0.f) {
+    const f32x2 c2 = pk2(c, c);
+    f32x2 acc = pk2(0.f, 0.f);
+    for (int v = (int)threadIdx.x; v < nv; v += WALK_THREADS) {
+      const uint4 w = lds128(sm + 16 * (size_t)v);
+      const f32x2 t0 = mul2(bsub2(w.x, vm), c2), t1 = mul2(bsub2(w.y, vm), c2);
+      const f32x2 t2 = mul2(bsub2(w.z, vm), c2), t3 = mul2(bsub2(w.w, vm), c2);
+      const f32x2 s01 = add2(pk2(ex2(lo2(t0)), ex2(hi2(t0))), pk2(ex2(lo2(t1)), ex2(hi2(t1))));
+      const f32x2 s23 = add2(pk2(ex2(lo2(t2)), ex2(hi2(t2))), pk2(ex2(lo2(t3)), ex2(hi2(t3))));
+      acc = add2(acc, add2(s01, s23));
+    }
+    ps = lo2(acc) + hi2(acc);
+  }
+  merge_stat(m, S, idx, vm, ps, (int)(e0 + 8LL * vb + jb), c);
+}
+
 // Statistics of node rows computed by the cluster: every CTA reduces its
 // vocabulary slice of the target row (and, when `drow` is set, of the draft
 // row), the slices are exchanged through distributed shared memory and merged
@@ -500,19 +637,27 @@ __device__ void node_stats(const TreeArgs &a, WalkSmem &sh, const char *trow, co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool tvec = ((uintptr_t)trow & 15) == 0, dvec = drow && ((uintptr_t)drow & 15) == 0;
   const long long e0 = (long long)sl.j0 * WALK_TILE;
-  if (tsm != nullptr) wait_slice(a, sh, &sh.bar_t, pt);
-  if (drow && dsm != nullptr) wait_slice(a, sh, &sh.bar_d, pd);
   float m = NO_MAX, S = 0.f, md = NO_MAX, Sd = 0.f;
   int idx = 0x7fffffff, idd = 0x7fffffff;
-  float z[SAMPLE_EPT];
+  if (tsm != nullptr) wait_slice(a, sh, &sh.bar_t, pt);
+  if (drow && dsm != nullptr) wait_slice(a, sh, &sh.bar_d, pd);
+  if (tsm != nullptr && a.tdt == SPEC_BF16 &&
+      (drow == nullptr || (dsm != nullptr && a.ddt == SPEC_BF16))) {
+    // staged bf16 slices (whole 16-byte vectors: staging needs V % 8 == 0)
+    const int nv = (int)((min((long long)sl.j1 * WALK_TILE, (long long)a.V) - e0) / 8);
+    slice_stats_bf16(tsm, nv, e0, c, m, S, idx);
+    if (drow) slice_stats_bf16(dsm, nv, e0, c, md, Sd, idd);
+  } else {
+    float z[SAMPLE_EPT];
 #pragma unroll 2
-  for (int j = sl.j0; j < sl.j1; ++j) {
-    const int x0 = j * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
-    load_row_ept(trow, tsm, e0, a.tdt, tvec, x0, a.V, -INFINITY, z);
-    stat_update(z, x0, c, m, S, idx);
-    if (drow) {
-      load_row_ept(drow, dsm, e0, a.ddt, dvec, x0, a.V, -INFINITY, z);
-      stat_update(z, x0, c, md, Sd, idd);
+    for (int j = sl.j0; j < sl.j1; ++j) {
+      const int x0 = j * WALK_TILE + (int)threadIdx.x * SAMPLE_EPT;
+      load_row_ept(trow, tsm, e0, a.tdt, tvec, x0, a.V, -INFINITY, z);
+      stat_update(z, x0, c, m, S, idx);
+      if (drow) {
+        load_row_ept(drow, dsm, e0, a.ddt, dvec, x0, a.V, -INFINITY, z);
+        stat_update(z, x0, c, md, Sd, idd);
+      }
     }
   }
 #pragma unroll
@@ -532,28 +677,28 @@ __device__ void node_stats(const TreeArgs &a, WalkSmem &sh, const char *trow, co
   }
   __syncthreads();
   const int par = sh.par;
-  if (threadIdx.x < 2) {   // thread 0: the target row, thread 1: the draft row
-    const int r = threadIdx.x;
+  if (threadIdx.x < 2 * WALK_CLUSTER) {
+    // this slice's statistics of row r (0: target, 1: draft) into CTA k's slot
+    // for them; the 8 threads of a row merge the warps in the same order
+    const int r = threadIdx.x & 1, k = threadIdx.x >> 1;
     RowStat q{NO_MAX, 0.f, 0x7fffffff};
     for (int w = 0; w < WALK_THREADS / 32; ++w)
       merge_stat(q.m, q.S, q.idx, sh.wst[w][r].m, sh.wst[w][r].S, sh.wst[w][r].idx, c);
-    sh.st[par][r] = q;
+    *cluster.map_shared_rank(&sh.xst[par][cluster.block_rank()][r], k) = q;
   }
-  cluster.sync();   // every slice's statistics written (slots alternate by parity)
+  cluster.sync();   // every slice's statistics pushed (slots alternate by parity)
   if (threadIdx.x < 2) {
     const int r = threadIdx.x;
     RowStat q{NO_MAX, 0.f, 0x7fffffff};
-    for (int k = 0; k < WALK_CLUSTER; ++k) {
-      const RowStat *o = cluster.map_shared_rank(&sh.st[par][r], k);
-      merge_stat(q.m, q.S, q.idx, o->m, o->S, o->idx, c);
-    }
+    for (int k = 0; k < WALK_CLUSTER; ++k)
+      merge_stat(q.m, q.S, q.idx, sh.xst[par][k][r].m, sh.xst[par][k][r].S, sh.xst[par][k][r].idx,
+                 c);
     sh.node[r] = q;
   }
   __syncthreads();
   if (threadIdx.x == 0) sh.par = par ^ 1;
   ts = sh.node[0];
   ds = sh.node[1];
-  __syncthreads();
 }
 
 __device__ __forceinline__ void write_final(const TreeArgs &a, int b, int depth, int x) {
@@ -583,73 +728,58 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
   const bool has_slice = sl.j1 > sl.j0;
   if (!has_slice) tsm = dsm = nullptr;
   uint32_t pt = 0, pd = 0;   // phases of the staged-slice barriers
+  int kst = 0, nk = t.root_kids;   // the current node's child list: start, length
+  int kb = 0;                      // the node's children buffer (node parity)
   while (true) {
-    // this CTA's slice of node v's target row into shared memory (or L2),
-    // and of its draft row into L2, while the node is set up
+    const long long rv = t.base + v;
+    const int row = t.base + v;
+    // a sampling node with children tests them against its draft row
+    const bool use_d = t.mode != MODE_GREEDY && nk > 0;
+    const bool stage_d = dsm != nullptr && use_d;
+    // this CTA's slices of node v's rows into shared memory (or L2) first,
+    // so the copies overlap the loads of the children
     if (threadIdx.x == 0 && has_slice) {
-      const long long rv = t.base + v;
-      if (tsm != nullptr)
+      if (tsm != nullptr) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         stage_slice(&sh.bar_t, tsm, a.target + rv * a.t_row_bytes, esz_t, se0, se1);
-      else
+        if (stage_d) stage_slice(&sh.bar_d, dsm, a.draft + rv * a.d_row_bytes, esz_d, se0, se1);
+      } else {
         prefetch_l2(a.target + rv * a.t_row_bytes + se0 * esz_t, (se1 - se0) * esz_t);
-      if (t.mode != MODE_GREEDY && a.draft != nullptr)
+      }
+      if (!stage_d && use_d && a.draft != nullptr)
         prefetch_l2(a.draft + rv * a.d_row_bytes + se0 * esz_d, (se1 - se0) * esz_d);
     }
-    // children of v in node-index order (block-wide ordered compaction)
-    {
-      const int per = (t.N + blockDim.x - 1) / blockDim.x;
-      const int c0 = min(t.N, (int)threadIdx.x * per), c1 = min(t.N, c0 + per);
-      int n = 0;
-      for (int cc = c0; cc < c1; ++cc) n += GLD(a.parent + (t.base + cc)) == v && cc > 0;
-      int tot;
-      int off = block_excl_scan_int(n, reinterpret_cast<int *>(sh.scratch), &tot);
-      for (int cc = c0; cc < c1; ++cc)
-        if (GLD(a.parent + (t.base + cc)) == v && cc > 0) {
-          if (off < SPEC_MAX_TREE_BRANCH) sh.kids[off] = cc;
-          ++off;
-        }
-      if (threadIdx.x == 0) sh.nk = min(tot, SPEC_MAX_TREE_BRANCH);
-      __syncthreads();
-      // the children's tokens and the logits the coins need, one thread each
+    // the children in node-index order, with the logits and the uniforms
+    // their coins need, one thread each (read after the statistics' barriers)
+    if ((int)threadIdx.x < nk) {
       const int j = threadIdx.x;
-      if (j < sh.nk) {
-        const long long rv = t.base + v;
-        const int x = GLD(a.node_token + (t.base + sh.kids[j]));
-        sh.kx[j] = x;
-        sh.kfix[j] = a.node_fixed != nullptr && GLD(a.node_fixed + (t.base + sh.kids[j])) != 0;
-        if (t.mode != MODE_GREEDY && (unsigned)x < (unsigned)a.V) {
-          sh.kzt[j] = load_elem(a.target + rv * a.t_row_bytes, a.tdt, x);
-          sh.kzd[j] = load_elem(a.draft + rv * a.d_row_bytes, a.ddt, x);
-        }
-      }
-      __syncthreads();
+      const KidRec r = GLD(a.kids + (t.base + kst + j));
+      sh.kids[kb][j] = kid_id(r.x);
+      sh.knext[kb][j] = r.x;
+      sh.kx[kb][j] = r.y;
+      sh.kfix[kb][j] = kid_fixed(r.x);
+      sh.kzt[kb][j] = r.z;
+      sh.kzd[kb][j] = r.w;
+      sh.ucoin[kb][j] = uniform24(tree_seed(a), (uint32_t)b, (uint32_t)kid_id(r.x), 0);
     }
-    const int nk = sh.nk;
-    const int row = t.base + v;
     // the node's statistics: its target row, and its draft row when a
     // sampling node has children to test
     const char *trow = a.target + (long long)row * a.t_row_bytes;
-    const bool want_d = t.mode != MODE_GREEDY && nk > 0 && DK == SPEC_DRAFT_LOGITS;
-    // a sampling node with children tests them against its draft row: stage
-    // this CTA's slice of it too
-    const bool stage_d = dsm != nullptr && t.mode != MODE_GREEDY && nk > 0;
-    if (stage_d && threadIdx.x == 0)
-      stage_slice(&sh.bar_d, dsm, a.draft + (long long)row * a.d_row_bytes, esz_d, se0, se1);
+    const bool want_d = use_d && DK == SPEC_DRAFT_LOGITS;
     RowStat ts, dstat;
     node_stats(a, sh, trow, want_d ? a.draft + (long long)row * a.d_row_bytes : nullptr, tsm,
                want_d ? dsm : nullptr, pt, pd, c, sl, cluster, ts, dstat);
     if (tsm != nullptr) pt ^= 1;
     if (stage_d && !want_d) wait_slice(a, sh, &sh.bar_d, pd);   // draft probabilities
     if (stage_d) pd ^= 1;
-    if (t.mode == MODE_GREEDY) {
-      if (threadIdx.x == 0) {
-        sh.accepted_child = -1;
-        for (int j = 0; j < nk; ++j)
-          if (sh.kx[j] == ts.idx) { sh.accepted_child = sh.kids[j]; break; }
-      }
-      __syncthreads();
-      const int ac = sh.accepted_child;
-      __syncthreads();
+    if (t.mode == MODE_GREEDY) {   // every thread finds the same child
+      int ac = -1, anext = 0;
+      for (int j = 0; j < nk; ++j)
+        if (sh.kx[kb][j] == ts.idx) {
+          ac = sh.kids[kb][j];
+          anext = sh.knext[kb][j];
+          break;
+        }
       if (ac >= 0 && depth < a.max_depth) {
         if (rank == 0 && threadIdx.x == 0) {
           GST(out + depth, ts.idx);   // the accepted child's token is the argmax
@@ -657,6 +787,9 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
         }
         v = ac;
         ++depth;
+        kst = kid_start(anext);
+        nk = kid_count(anext);
+        kb ^= 1;
         continue;
       }
       if (rank == 0 && threadIdx.x == 0) {
@@ -666,6 +799,8 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       return;
     }
     NodeLaw nl;
+    nl.kx = sh.kx[kb];
+    nl.kfix = sh.kfix[kb];
     nl.trow = trow;
     nl.tsm = tsm;
     nl.dsm = stage_d ? dsm : nullptr;
@@ -692,41 +827,26 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
       nl.md = dstat.m;
       nl.invSd = 1.f / dstat.S;
     }
-    if (threadIdx.x == 0) {
-      sh.s[0] = 1.f;
-      sh.skip[0] = 0;
-      sh.rinv[0] = 1.f;
-    }
-    __syncthreads();
     float qE = 0.f;
-    int accepted = -1, L = 0;
+    int accepted = -1, acc_next = 0, acc_tok = -1, L = 0;
     bool passed = false;   // the tile totals of level L's residual are in sh
     for (int j = 0; j < nk; ++j) {
       // coin of child j at its token x, with p_j(x) and q_j(x) from the chain
-      // (a point mass has q_j(x) = 1)
-      if (threadIdx.x == 0) {
-        const int ch = sh.kids[j];
-        const float p = ex2((sh.kzt[j] - nl.mt) * c) * nl.invSt;
-        const float qx = DK == SPEC_DRAFT_PROBS ? sh.kzd[j]
-                                                : ex2((sh.kzd[j] - nl.md) * c) * nl.invSd;
-        const float pj = chain_weight(p, qx, sh.kx[j], j, false, sh);
-        const float qj = sh.kfix[j] ? 1.f : qx * sh.s[j];
-        const float acc = qj <= pj ? 1.f : pj / qj;
-        const bool ok = uniform24(tree_seed(a), (uint32_t)b, (uint32_t)ch, 0) < acc;
-        sh.accepted_child = ok ? ch : -1;
-        sh.carry = qx;   // q(x), for q(E)
-        sh.pfix = pj;
-      }
-      __syncthreads();
-      const int ac = sh.accepted_child;
-      const float qx = sh.carry;
-      const float pj = sh.pfix;
-      __syncthreads();
-      if (ac >= 0) {
-        accepted = ac;
+      // (a point mass has q_j(x) = 1), taken by every thread on the same
+      // shared values
+      const float p = ex2((sh.kzt[kb][j] - nl.mt) * c) * nl.invSt;
+      const float qx = DK == SPEC_DRAFT_PROBS ? sh.kzd[kb][j]
+                                              : ex2((sh.kzd[kb][j] - nl.md) * c) * nl.invSd;
+      const float pj = chain_weight(p, qx, sh.kx[kb][j], j, false, sh, nl);
+      const float qj = sh.kfix[kb][j] ? 1.f : qx * sh.s[j];
+      const float acc = qj <= pj ? 1.f : pj / qj;
+      if (sh.ucoin[kb][j] < acc) {
+        accepted = sh.kids[kb][j];
+        acc_next = sh.knext[kb][j];
+        acc_tok = sh.kx[kb][j];
         break;
       }
-      if (sh.kfix[j]) {
+      if (sh.kfix[kb][j]) {
         // point-mass rejection: p_{j+1} = p_j without x over Z_j = 1 - p_j(x)
         L = j;
         passed = false;
@@ -756,11 +876,14 @@ __device__ __forceinline__ void walk_tree(const TreeArgs &a, WalkSmem &sh, const
     }
     if (accepted >= 0 && depth < a.max_depth) {
       if (rank == 0 && threadIdx.x == 0) {
-        GST(out + depth, GLD(a.node_token + (t.base + accepted)));
+        GST(out + depth, acc_tok);
         if (path) GST(path + depth, accepted);
       }
       v = accepted;
       ++depth;
+      kst = kid_start(acc_next);
+      nk = kid_count(acc_next);
+      kb ^= 1;
       continue;
     }
     // all tested children rejected: draw from p_{L+1} = norm(residual at L),
@@ -802,6 +925,7 @@ __global__ void __cluster_dims__(WALK_CLUSTER, 1, 1) __launch_bounds__(WALK_THRE
     sh.ok = t.mode != MODE_SKIP && *(volatile int *)&a.hdr->status == SPEC_OK;
     sh.par = 0;
     sh.never = 0;
+    sh.s[0] = 1.f;   // level 0 of the draft law is q itself
     mbar_init(&sh.bar_t, 1);
     mbar_init(&sh.bar_d, 1);
     fence_mbar_init();
@@ -830,7 +954,7 @@ extern "C" size_t spec_verify_tree_workspace(int B, int n_nodes, int V, int max_
   if (B < 0 || n_nodes < B || V <= 0 || V > SPEC_MAX_V) return 0;
   if (max_depth < 0 || max_depth > SPEC_MAX_TREE_DEPTH) return 0;
   if (max_branch < 1 || max_branch > SPEC_MAX_TREE_BRANCH) return 0;
-  return tree_layout(B).total;
+  return tree_layout(B, n_nodes).total;
 }
 
 static int verify_tree(const void *target, int tdt, const void *draft, int ddt, int dk,
@@ -856,7 +980,7 @@ static int verify_tree(const void *target, int tdt, const void *draft, int ddt, 
       !aligned(out_tokens, 4) || !aligned(out_accepted, 4) || !aligned(out_path, 4) ||
       !aligned(node_fixed, 4) || !aligned(seed_dev, 8))
     return SPEC_ERR_INVALID_ARG;
-  const TreeLayout L = tree_layout(B);
+  const TreeLayout L = tree_layout(B, n_nodes);
   if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < L.total)
     return SPEC_ERR_WORKSPACE;
   char *ws = static_cast<char *>(workspace);
@@ -883,6 +1007,7 @@ static int verify_tree(const void *target, int tdt, const void *draft, int ddt, 
   a.out_path = out_path;
   a.hdr = reinterpret_cast<WsHeader *>(ws + L.hdr);
   a.tree = reinterpret_cast<TreeInfo *>(ws + L.tree);
+  a.kids = reinterpret_cast<KidRec *>(ws + L.kids);
   a.t_row_bytes = (long long)V * (tdt == SPEC_BF16 ? 2 : 4);
   a.d_row_bytes = (long long)V * (ddt == SPEC_BF16 ? 2 : 4);
   // stage the row slices in shared memory when they fit and every slice

@@ -51,3 +51,25 @@ def test_launch_count_matches_the_bench_claim(name, case):
     if not kernels:
         pytest.skip("the profiler recorded no kernels here")
     assert len(kernels) == work.launches, (name, kernels)
+
+
+@pytest.mark.parametrize("name,case", CASES, ids=[c[0] for c in CASES])
+def test_profiling_events_bracket_a_kernel_of_the_call(name, case):
+    """The two events the bench reads its kernel time from are taken and
+    recorded by the call itself, inside the call's own interval."""
+    import bench
+    import speculative_decoding_rejection_gb300 as sv
+    case = dict(case)
+    cfg = case.pop("cfg")
+    work = bench.make_work(cfg, DEV, **case)
+    work.call()
+    torch.cuda.synchronize()
+    e0, e1, eb, ea = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    e0.record()
+    sv.spec_profile_row_pass(eb, ea)
+    work.call()
+    assert not sv.spec_profile_pending(), name
+    e1.record()
+    torch.cuda.synchronize()
+    inner, outer = eb.elapsed_time(ea), e0.elapsed_time(e1)
+    assert 0.0 < inner <= outer, (name, inner, outer)
