@@ -391,7 +391,7 @@ class LinearWork:
         self.cluster_small = (not self.fused and not (asked_lazy or eager) and not kl
                               and self.ext is None and not lb.top128 and bf16 and lb.V % 8 == 0
                               and lb.max_k <= 8 and lb.B <= 128 and limit > 0
-                              and (2 * lb.max_k + 1) * slice_ * 2 <= 204800)
+                              and (2 * lb.max_k + 1) * slice_ * 2 <= 102400)
         if self.fused or self.cluster_small:
             self.launches = 1 if self.fused else 2
             self.kernel = "k_verify_small" if self.fused else "k_verify_cluster_small"

@@ -18,12 +18,13 @@
 // SM), plus one service warp, over two work sources.
 //   - The static list holds every position's rows in layer order: position 1
 //     of every request, then position 2, and so on, each row split into
-//     256 KB chunks. A producer skips a chunk of request b at position j once
+//     chunks. A producer skips a chunk of request b at position j once
 //     b is known to have rejected an earlier position; by the time a layer
 //     comes up the previous layer's decisions are mostly known, so the rows
 //     after a rejection are mostly never read.
 //   - Rows are split in 128 KB chunks (smaller chunks measured slower; the
-//     residual's second read mostly misses L2 at every chunk size tried).
+//     residual's second read mostly misses L2 at every chunk size tried:
+//     it comes long after the first read, once the position is decided).
 //   - Chunk ends go to a service warp: each consumer warp leaves its partial
 //     in a shared-memory queue record and goes on streaming; the CTA's sixth
 //     warp publishes the four partials and counts one completion of the

@@ -581,16 +581,12 @@ __device__ __forceinline__ void stat_update(const float *z, int x0, float c, flo
   }
 }
 
-// One thread's statistics of a staged bf16 slice of nv 16-byte vectors
-// (element e0 first; vectors t, t + WALK_THREADS, ...), merged into its
-// running (m, S, idx): the max through packed bf16 maxima and its lowest
-// index, then the sum of 2^((z - max) c) (none when c is 0) with packed
-// subtracts, multiplies and adds, one 2^x per element.
-__device__ __forceinline__ void slice_stats_bf16(const unsigned char *sm, int nv, long long e0,
-                                                 float c, float &m, float &S, int &idx) {
-  float vm = NO_MAX;
-  int vb = -1;
-  for (int v = (int)threadIdx.x; v < nv; v += WALK_THREADS) {
+// Running max of one thread's vectors of a staged bf16 slice (vectors t,
+// t + WALK_THREADS, ... < nv) through packed bf16 maxima, and the first
+// vector holding it (-1: nothing finite).
+__device__ __forceinline__ void slice_max_bf16(const unsigned char *sm, int v, int nv, float &vm,
+                                               int &vb) {
+  for (; v < nv; v += WALK_THREADS) {
     const uint4 w = lds128(sm + 16 * (size_t)v);
     const uint32_t a2 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
     const float x = fmaxf(bf16lo(a2), bf16hi(a2));
@@ -599,30 +595,67 @@ __device__ __forceinline__ void slice_stats_bf16(const unsigned char *sm, int nv
       vb = v;
     }
   }
-  if (vb < 0) return;   // nothing finite here
+}
+
+// Lowest element index holding vm in vector vb.
+__device__ __forceinline__ int first_in_vec(const unsigned char *sm, int vb, float vm,
+                                            long long e0) {
+  const uint4 w = lds128(sm + 16 * (size_t)vb);
+  const uint32_t q[4] = {w.x, w.y, w.z, w.w};
   int jb = 7;
-  {
-    const uint4 w = lds128(sm + 16 * (size_t)vb);
-    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int k = 7; k >= 0; --k)
-      if (((k & 1) ? bf16hi(q[k >> 1]) : bf16lo(q[k >> 1])) == vm) jb = k;
-  }
-  float ps = 0.f;
-  if (c != 0.f) {
-    const f32x2 c2 = pk2(c, c);
-    f32x2 acc = pk2(0.f, 0.f);
-    for (int v = (int)threadIdx.x; v < nv; v += WALK_THREADS) {
-      const uint4 w = lds128(sm + 16 * (size_t)v);
-      const f32x2 t0 = mul2(bsub2(w.x, vm), c2), t1 = mul2(bsub2(w.y, vm), c2);
-      const f32x2 t2 = mul2(bsub2(w.z, vm), c2), t3 = mul2(bsub2(w.w, vm), c2);
-      const f32x2 s01 = add2(pk2(ex2(lo2(t0)), ex2(hi2(t0))), pk2(ex2(lo2(t1)), ex2(hi2(t1))));
-      const f32x2 s23 = add2(pk2(ex2(lo2(t2)), ex2(hi2(t2))), pk2(ex2(lo2(t3)), ex2(hi2(t3))));
-      acc = add2(acc, add2(s01, s23));
+  for (int k = 7; k >= 0; --k)
+    if (((k & 1) ? bf16hi(q[k >> 1]) : bf16lo(q[k >> 1])) == vm) jb = k;
+  return (int)(e0 + 8LL * vb + jb);
+}
+
+// Sum of 2^((z - m) c) over the 8 elements of one vector, as packed pairs.
+__device__ __forceinline__ f32x2 vec_exp_sum(const uint4 w, float m, f32x2 c2) {
+  const f32x2 t0 = mul2(bsub2(w.x, m), c2), t1 = mul2(bsub2(w.y, m), c2);
+  const f32x2 t2 = mul2(bsub2(w.z, m), c2), t3 = mul2(bsub2(w.w, m), c2);
+  const f32x2 s01 = add2(pk2(ex2(lo2(t0)), ex2(hi2(t0))), pk2(ex2(lo2(t1)), ex2(hi2(t1))));
+  const f32x2 s23 = add2(pk2(ex2(lo2(t2)), ex2(hi2(t2))), pk2(ex2(lo2(t3)), ex2(hi2(t3))));
+  return add2(s01, s23);
+}
+
+// One thread's statistics of the staged bf16 slices of a node's target row
+// and, when `dsm` is set, its draft row (nv 16-byte vectors each, element e0
+// first; vectors t, t + WALK_THREADS, ...): per row the max through packed
+// bf16 maxima and its lowest index, then the sum of 2^((z - max) c) (none
+// when c is 0), the two rows' vectors taken in the same loop so their
+// loads and 2^x overlap.
+__device__ __forceinline__ void slice_stats_bf16(const unsigned char *tsm,
+                                                 const unsigned char *dsm, int nv, long long e0,
+                                                 float c, RowStat &t, RowStat &d) {
+  const int v0 = (int)threadIdx.x;
+  float tm = NO_MAX, dm = NO_MAX;
+  int tb = -1, db = -1;
+  slice_max_bf16(tsm, v0, nv, tm, tb);
+  if (dsm != nullptr) slice_max_bf16(dsm, v0, nv, dm, db);
+  t = RowStat{NO_MAX, 0.f, 0x7fffffff};
+  d = RowStat{NO_MAX, 0.f, 0x7fffffff};
+  if (tb >= 0) t = RowStat{tm, 0.f, first_in_vec(tsm, tb, tm, e0)};
+  if (db >= 0) d = RowStat{dm, 0.f, first_in_vec(dsm, db, dm, e0)};
+  if (c == 0.f) return;
+  const f32x2 c2 = pk2(c, c);
+  f32x2 at = pk2(0.f, 0.f), ad = pk2(0.f, 0.f);
+  if (dsm != nullptr && tb >= 0 && db >= 0) {
+    for (int v = v0; v < nv; v += WALK_THREADS) {
+      const uint4 wt = lds128(tsm + 16 * (size_t)v);
+      const uint4 wd = lds128(dsm + 16 * (size_t)v);
+      at = add2(at, vec_exp_sum(wt, tm, c2));
+      ad = add2(ad, vec_exp_sum(wd, dm, c2));
     }
-    ps = lo2(acc) + hi2(acc);
+  } else {
+    if (tb >= 0)
+      for (int v = v0; v < nv; v += WALK_THREADS)
+        at = add2(at, vec_exp_sum(lds128(tsm + 16 * (size_t)v), tm, c2));
+    if (dsm != nullptr && db >= 0)
+      for (int v = v0; v < nv; v += WALK_THREADS)
+        ad = add2(ad, vec_exp_sum(lds128(dsm + 16 * (size_t)v), dm, c2));
   }
-  merge_stat(m, S, idx, vm, ps, (int)(e0 + 8LL * vb + jb), c);
+  t.S = lo2(at) + hi2(at);
+  d.S = lo2(ad) + hi2(ad);
 }
 
 // Statistics of node rows computed by the cluster: every CTA reduces its
@@ -645,8 +678,14 @@ __device__ void node_stats(const TreeArgs &a, WalkSmem &sh, const char *trow, co
       (drow == nullptr || (dsm != nullptr && a.ddt == SPEC_BF16))) {
     // staged bf16 slices (whole 16-byte vectors: staging needs V % 8 == 0)
     const int nv = (int)((min((long long)sl.j1 * WALK_TILE, (long long)a.V) - e0) / 8);
-    slice_stats_bf16(tsm, nv, e0, c, m, S, idx);
-    if (drow) slice_stats_bf16(dsm, nv, e0, c, md, Sd, idd);
+    RowStat t, d;
+    slice_stats_bf16(tsm, drow ? dsm : nullptr, nv, e0, c, t, d);
+    m = t.m;
+    S = t.S;
+    idx = t.idx;
+    md = d.m;
+    Sd = d.S;
+    idd = d.idx;
   } else {
     float z[SAMPLE_EPT];
 #pragma unroll 2
