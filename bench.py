@@ -386,17 +386,17 @@ class LinearWork:
                       and lb.V <= 8192 and per_req <= 1 << 20 and lb.B * per_req <= limit)
         # longer bf16 rows in calls of at most 128 requests and 8 drafts whose
         # row slices fit a cluster's shared memory: one cluster per request
-        # (setup, then the cluster kernel)
+        # (one launch; the rows pass through shared-memory buffers)
         slice_ = (lb.V // 8 + 7) // 8 * 8
         self.cluster_small = (not self.fused and not (asked_lazy or eager) and not kl
                               and self.ext is None and not lb.top128 and bf16 and lb.V % 8 == 0
                               and lb.max_k <= 8 and lb.B <= 128 and limit > 0
                               and (2 * lb.max_k + 1) * slice_ * 2 <= 102400)
         if self.fused or self.cluster_small:
-            self.launches = 1 if self.fused else 2
+            self.launches = 1
             self.kernel = "k_verify_small" if self.fused else "k_verify_cluster_small"
             self.config["schedule"] = ("fused (one block per request)" if self.fused else
-                                       "one cluster per request, its rows resident")
+                                       "one cluster per request")
             self.stream = self.lazy = False
         elif self.stream and "schedule" not in self.config:
             self.config["schedule"] = "position-lazy streaming (rows 1..n+1 per request)"

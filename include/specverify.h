@@ -172,10 +172,10 @@ int spec_verify_linear(const void *target, int tdt, const void *draft, int ddt,
  * longer rows (V a multiple of 8), at most 128 requests and at most 8
  * drafts each, whose (2 max_k + 1) row slices of V/8 logits fit 100 KB of
  * shared memory (V up to about 37000 at max_k = 5), runs as one cluster
- * kernel instead: a cluster of 8 CTAs per request holds all of the
- * request's rows on chip, exchanges their statistics once and draws the
- * final token from that copy. Same results either way, up to the rounding
- * of the row sums. `bytes` = 0 turns both kernels off; the default is
+ * kernel instead: a cluster of 8 CTAs per request streams the request's
+ * rows through a few row-slice buffers per CTA, exchanges their statistics
+ * once and draws the final token from the two rows it needs, copied again.
+ * Same results either way, up to the rounding of the row sums. `bytes` = 0 turns both kernels off; the default is
  * 32 MiB. A process-wide setting, read when a call is made. Returns the
  * previous value.
  */

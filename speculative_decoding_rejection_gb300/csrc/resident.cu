@@ -37,6 +37,9 @@
 // Every wait is bounded (2 s of %globaltimer); on expiry the status word
 // gets SPEC_ERR_TIMEOUT and the cluster stops.
 #include <algorithm>
+#include <mutex>
+#include <utility>
+#include <vector>
 #include <climits>
 #include <cstddef>
 
@@ -158,6 +161,7 @@ __device__ __forceinline__ float cta_excl_scan(float v, float *scratch, int warp
 struct RcArgs {
   LinearArgs a;
   int slice;      // elements per CTA slice (a multiple of 8)
+  int nbuf;       // one cluster per request: row-slice buffers per CTA
 };
 
 // The CTA's slice of a row: elements [e0, e0 + nel), as nvec 16-byte
@@ -583,23 +587,32 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
 
 // ------------------------------------------- small calls: whole requests
 // Small calls with rows longer than the fused kernel takes (dense bf16
-// logits, V % 8 == 0, at most RQ_MAX_K drafts): a cluster verifies one
-// request at a time with all of its rows resident at once. Lane i of warp 0
-// copies the CTA's slice of the request's row i (target rows 1..K+1, then
-// draft rows 1..K) into shared memory; each warp reduces whole row slices;
-// one exchange carries every position's slice statistics; every CTA then
-// decides all positions on the same merged bits, and the final token is
-// drawn from the resident rows with one more exchange. Two exchanges per
-// request, however many drafts it has.
+// logits, V % 8 == 0, at most RQ_MAX_K drafts, at most RQ_MAX_B requests):
+// one launch, a cluster per request. Every CTA first validates the whole
+// call. The request's rows (target rows 1..K+1, then draft rows 1..K) pass
+// through a few row-slice buffers per CTA, as many rows at a time as there
+// are buffers: lane i of warp 0 copies the CTA's slice of a row into buffer
+// i, and one warp reduces each buffer. One exchange carries every
+// position's slice statistics; every CTA then decides all positions on the
+// same merged bits. The final draw copies the two rows it needs again (they
+// are still in L2) and finds the token with one more exchange. Two
+// exchanges per request, however many drafts it has; with few buffers
+// (48 KB for V = 32000) four CTAs share an SM, so a call of up to about 76
+// requests has all its clusters at once.
 constexpr int RQ_MAX_K = 8;
 constexpr int RQ_ROWS = 2 * RQ_MAX_K + 1;
+// Row-slice buffers per CTA: as many slices as fit this many bytes (at least
+// two, for the final draw's row pair), so that short rows run four CTAs per
+// SM and every request of a call up to RQ_MAX_B has its cluster at once.
+constexpr size_t RQ_BUF_BYTES = 48 * 1024;
+constexpr int RQ_CTAS_PER_SM = 4;
 // A cluster takes one request at a time, so the call's time grows with the
 // rounds of requests per cluster: above this many requests the streaming
 // and eager schedules, which spread every row over the whole GPU, are faster.
 constexpr int RQ_MAX_B = 128;
 
 struct RqSmem {
-  uint64_t bar[RQ_ROWS];                  // row slice landed
+  uint64_t bar[RQ_ROWS];                  // row-slice buffer filled
   uint64_t xch, xch2;
   RcMsg msg[2][RC_CLUSTER][RQ_MAX_K + 1];  // by parity, sender, position
   float tot[2][RC_CLUSTER];
@@ -611,7 +624,6 @@ struct RqSmem {
   int xmin, xlast;
   int n, next;
   int abort;
-  int skip;
 };
 static_assert(offsetof(RqSmem, msg) % 16 == 0, "peer stores are 16-byte vectors");
 
@@ -624,7 +636,7 @@ __device__ __forceinline__ void warp_consume(const unsigned char *buf, int nvec,
     consume_vec<SOFTMAX, true>(lds128(buf + 16 * v), e0 + 8 * v, c, st, INFINITY);
 }
 
-__global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS, RC_CTAS_PER_SM)
+__global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS, RQ_CTAS_PER_SM)
     k_verify_cluster_small(const RcArgs ra) {
   extern __shared__ __align__(128) unsigned char dsmem[];
   __shared__ RqSmem sh;
@@ -639,12 +651,77 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
     mbar_init(&sh.xch, RC_CLUSTER);
     mbar_init(&sh.xch2, RC_CLUSTER);
     sh.abort = 0;
-    sh.skip = *(volatile int *)&a.hdr->setup_bad;
     fence_mbar_init();
   }
+  __syncthreads();   // this CTA's barriers are ready for its own copies
+  const int V = a.V, W = a.max_k + 1;
+  const int e0 = min(V, rank * ra.slice);
+  const int nvec = (min(V, e0 + ra.slice) - e0) / 8;
+  const size_t rbytes = (size_t)ra.slice * 2;   // row stride in shared memory
+  volatile int *abort = &sh.abort;
+  const uint64_t seed = seed_of(a);
+  // phase parities of each buffer's barrier, one bit per buffer: uses issued
+  // and uses completed (a buffer has at most one copy in flight; every thread
+  // keeps the same bits)
+  unsigned par_issued = 0, par_done = 0;
+  const int nb = ra.nbuf;
+  unsigned xch_ct = 0, xch2_ct = 0;
+  bool failed = false;
+  // row i of request rq (target rows 0..K, then draft rows) into buffer q
+  auto issue_row = [&](const ReqInfo &rq, int i, int q) {
+    const bool tgt = i <= rq.K;
+    const char *row = tgt ? a.target + (long long)(rq.t0 + i) * a.t_row_bytes
+                          : a.draft + (long long)(rq.d0 + i - rq.K - 1) * a.d_row_bytes;
+    const uint32_t nbytes = (uint32_t)nvec * 16u;
+    if (nbytes > 0) {
+      // the buffer was read by this CTA's threads before the last barrier
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_tx(&sh.bar[q], nbytes);
+      bulk_g2s(dsmem + q * rbytes, row + 2LL * e0, nbytes, &sh.bar[q]);
+    } else {
+      mbar_arrive(&sh.bar[q]);
+    }
+  };
+  auto rows_of = [](const ReqInfo &rq) {
+    return rq.K + 1 + (rq.mode == MODE_SAMPLE ? rq.K : 0);
+  };
+
+  // The cluster's first request: when its record is valid (its rows are then
+  // in bounds), its first rows are copied while the call is validated.
+  int b = cid;
+  ReqInfo r{};
+  const bool pre = b < a.B && load_request(a, b, r);
+  unsigned pre_used = 0;
+  if (pre) {
+    const int cnt = min(nb, rows_of(r));
+    if (warp == 0 && lane < cnt) issue_row(r, lane, lane);
+    pre_used = (1u << cnt) - 1u;
+    par_issued ^= pre_used;
+  }
+  // Every CTA validates the whole call (B <= RQ_MAX_B requests: one record
+  // and up to RQ_MAX_K tokens per thread), so every CTA reaches the same
+  // verdict without a grid-wide barrier: with any request invalid, none is
+  // verified.
+  bool bad = false;
+  for (int bb = threadIdx.x; bb < a.B; bb += RC_THREADS) {
+    ReqInfo rq;
+    if (!load_request(a, bb, rq)) {
+      bad = true;
+      continue;
+    }
+    for (int j = 0; j < rq.K; ++j)
+      if ((unsigned)GLD(a.tokens + rq.d0 + j) >= (unsigned)a.V) {
+        set_status(a.hdr, SPEC_ERR_INVALID_ARG, bb);
+        bad = true;
+      }
+  }
+  bad = __syncthreads_or(bad);
   cluster.sync();   // barriers initialised everywhere before any remote arrival
-  if (sh.skip) {    // inputs rejected by the setup: nothing is verified
-    const int W = a.max_k + 1;
+  if (bad) {
+    // the first rows' copies in flight, waited for (bounded) before leaving
+    volatile int never = 0;
+    for (int q = 0; q < nb; ++q)
+      if ((pre_used >> q) & 1u) mbar_wait_bounded(&sh.bar[q], 0u, &never);
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)a.B * W;
          i += (long long)gridDim.x * blockDim.x) {
       GST(a.out_tokens + i, -1);
@@ -653,61 +730,52 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
     cluster.sync();
     return;
   }
-  const int V = a.V, W = a.max_k + 1;
-  const int e0 = min(V, rank * ra.slice);
-  const int nvec = (min(V, e0 + ra.slice) - e0) / 8;
-  const size_t rbytes = (size_t)ra.slice * 2;   // row stride in shared memory
-  volatile int *abort = &sh.abort;
-  const uint64_t seed = seed_of(a);
-  unsigned row_ct[RQ_ROWS];   // phases of each row barrier used (thread-private copies agree)
-  for (int i = 0; i < RQ_ROWS; ++i) row_ct[i] = 0;
-  unsigned xch_ct = 0, xch2_ct = 0;
-  bool failed = false;
 
-  int b = cid;
+  bool first = pre;   // this request's first rows are already on their way
   while (b < a.B && !failed) {
-    const ReqInfo r = GLD(a.req + b);
+    if (!first) load_request(a, b, r);   // valid: checked above
     const bool sample = r.mode == MODE_SAMPLE;
     const float c = r.c;
     const int K = r.K;
-    const int nrows = K + 1 + (sample ? K : 0);
-    // 1. every row slice of the request, one bulk copy each; the decision
-    // inputs; the cluster's next request (rank 0)
-    if (warp == 0 && lane < nrows) {
-      const bool tgt = lane <= K;
-      const char *row = tgt ? a.target + (long long)(r.t0 + lane) * a.t_row_bytes
-                            : a.draft + (long long)(r.d0 + lane - K - 1) * a.d_row_bytes;
-      const uint32_t nb = (uint32_t)nvec * 16u;
-      if (nb > 0) {
-        mbar_arrive_tx(&sh.bar[lane], nb);
-        bulk_g2s(dsmem + lane * rbytes, row + 2LL * e0, nb, &sh.bar[lane]);
-      } else {
-        mbar_arrive(&sh.bar[lane]);
-      }
-    }
+    const int nrows = rows_of(r);
+    // 1. the decision inputs (the drafts and both logits at each draft); the
+    // cluster's next request (rank 0)
     if (threadIdx.x < K) {
       const int j = threadIdx.x;
-      sh.d[j] = GLD(a.tokens + r.d0 + j);
-      sh.zt[j] = GLDCG(a.rank_thr + r.t0 + j);
-      sh.zd[j] = sample ? GLDCG(a.zd_at + r.d0 + j) : 0.f;
+      const int d = GLD(a.tokens + r.d0 + j);
+      sh.d[j] = d;
+      sh.zt[j] = load_elem(a.target + (long long)(r.t0 + j) * a.t_row_bytes, a.tdt, d);
+      sh.zd[j] = sample ? load_elem(a.draft + (long long)(r.d0 + j) * a.d_row_bytes, a.ddt, d)
+                        : 0.f;
     }
     int nxt = -1;
     if (threadIdx.x == 0 && rank == 0) nxt = ncl + (int)atomicAdd(&a.hdr->work, 1u);
-    // 2. slice statistics, one row per warp at a time
-    for (int i = warp; i < nrows; i += RC_WARPS) {
-      if (!mbar_wait_bounded(&sh.bar[i], row_ct[i] & 1u, abort)) {
-        *abort = 1;
-        failed = true;
-        break;
+    // 2. slice statistics of every row: the rows pass through the nb
+    // buffers, nb at a time (one bulk copy each), one warp per row
+    for (int i0 = 0; i0 < nrows && !failed; i0 += nb) {
+      const int cnt = min(nb, nrows - i0);
+      const unsigned used = (1u << cnt) - 1u;
+      if (first) {
+        first = false;   // issued before the validation
+      } else {
+        if (warp == 0 && lane < cnt) issue_row(r, i0 + lane, lane);
+        par_issued ^= used;
       }
-      RunState st{NO_MAX, pk2(0.f, 0.f), INT_MAX, 0, 0u};
-      if (c != 0.f) warp_consume<true>(dsmem + i * rbytes, nvec, lane, e0, c, st);
-      else warp_consume<false>(dsmem + i * rbytes, nvec, lane, e0, c, st);
-      const Part p = finish_row_chunk<false>(st, c);
-      if (lane == 0) sh.rows[i] = p;
+      for (int q = warp; q < cnt; q += RC_WARPS) {
+        if (!mbar_wait_bounded(&sh.bar[q], (par_done >> q) & 1u, abort)) {
+          *abort = 1;
+          failed = true;
+          break;
+        }
+        RunState st{NO_MAX, pk2(0.f, 0.f), INT_MAX, 0, 0u};
+        if (c != 0.f) warp_consume<true>(dsmem + q * rbytes, nvec, lane, e0, c, st);
+        else warp_consume<false>(dsmem + q * rbytes, nvec, lane, e0, c, st);
+        const Part p = finish_row_chunk<false>(st, c);
+        if (lane == 0) sh.rows[i0 + q] = p;
+      }
+      failed = __syncthreads_or(failed);   // every buffer read before it is refilled
+      if (!failed) par_done ^= used;
     }
-    for (int i = 0; i < nrows; ++i) ++row_ct[i];
-    failed = __syncthreads_or(failed);
     if (failed) break;
     // 3. one exchange: lane k of warp 0 sends every position's slice
     // statistics to rank k
@@ -744,14 +812,14 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
       sh.ds[p] = ds;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int n = K;
-      for (int j = 0; j < K; ++j) {
+    if (warp == 0) {   // position j on lane j (K <= RQ_MAX_K < 32); the first rejection ends it
+      bool rej = false;
+      if (lane < K) {
+        const int j = lane;
         const int d = sh.d[j];
         const RowStat ts = sh.ts[j], ds = sh.ds[j];
         const bool dok = (unsigned)d < (unsigned)V;
         float pdv, qdv;
-        bool rej;
         if (!sample) {
           rej = !(dok && d == ts.idx);
           pdv = rej ? 0.f : 1.f;
@@ -772,11 +840,13 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
             GST(a.out_pq + 2LL * (r.d0 + j) + 1, qdv);
           }
         }
-        if (rej && n == K) n = j;
       }
-      if (rank == 0 && row_empty(sh.ts[K].m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
-      sh.n = n;
-      sh.next = sh.msg[par][0][0].next;
+      const unsigned rm = __ballot_sync(0xffffffffu, rej);
+      if (lane == 0) {
+        if (rank == 0 && row_empty(sh.ts[K].m)) set_status(a.hdr, SPEC_ERR_INVALID_ARG, b);
+        sh.n = rm ? __ffs(rm) - 1 : K;
+        sh.next = sh.msg[par][0][0].next;
+      }
     }
     __syncthreads();
     const int n = sh.n, next = sh.next;
@@ -790,11 +860,21 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
         if (!sample) GST(out + n, sh.ts[n].idx);   // greedy: the target's argmax
       }
     }
-    // 6. the final draw from position n's resident rows
+    // 6. the final draw from position n's rows, copied again (from L2) into
+    // buffers 0 and 1
     if (sample) {
+      const int nfin = n < K ? 2 : 1;
+      const unsigned used = (1u << nfin) - 1u;
+      if (warp == 0 && lane < nfin) issue_row(r, lane == 0 ? n : K + 1 + n, lane);
+      par_issued ^= used;
+      for (int q = 0; q < nfin && !failed; ++q)
+        failed = !mbar_wait_bounded(&sh.bar[q], (par_done >> q) & 1u, abort);
+      failed = __syncthreads_or(failed);
+      if (failed) break;
+      par_done ^= used;
       const RowStat ts = sh.ts[n], ds = sh.ds[n];
-      const unsigned char *tb = dsmem + n * rbytes;
-      const unsigned char *db = dsmem + (K + 1 + n) * rbytes;
+      const unsigned char *tb = dsmem;
+      const unsigned char *db = dsmem + rbytes;
       const float invSt = 1.f / ts.S;
       int owner = -1, x = -1;
       float carry = 0.f, target = 0.f;
@@ -870,10 +950,16 @@ __global__ void __cluster_dims__(RC_CLUSTER, 1, 1) __launch_bounds__(RC_THREADS,
         GST(a.out_tokens + (long long)b * W + n, x);
       }
     }
-    __syncthreads();   // the rows are free for the next request's copies
+    __syncthreads();   // the buffers are free for the next request's copies
     b = next;
   }
-  if (failed && threadIdx.x == 0) set_status(a.hdr, SPEC_ERR_TIMEOUT, -7);
+  if (failed) {
+    if (threadIdx.x == 0) set_status(a.hdr, SPEC_ERR_TIMEOUT, -7);
+    // this CTA's copies still in flight: wait for them (bounded) before leaving
+    volatile int never = 0;
+    for (int q = 0; q < nb; ++q)
+      if (((par_done ^ par_issued) >> q) & 1u) mbar_wait_bounded(&sh.bar[q], (par_done >> q) & 1u, &never);
+  }
   cluster.sync();   // no CTA leaves while a peer may still write to it
 }
 
@@ -913,24 +999,56 @@ static int cluster_count(const void *kernel, int *cache) {
 
 int launch_setup_stream(const LinearArgs &a, cudaStream_t stream);
 
+// Co-resident clusters of the one-cluster-per-request kernel with `smem`
+// bytes of buffers per CTA (asked once per size).
+static int cluster_small_count(size_t smem) {
+  static std::mutex mu;
+  static std::vector<std::pair<size_t, int>> known;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto &k : known)
+    if (k.first == smem) return k.second;
+  if (cudaFuncSetAttribute(k_verify_cluster_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(RC_CLUSTER * num_sms(), 1, 1);
+  cfg.blockDim = dim3(RC_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = RC_CLUSTER;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (const void *)k_verify_cluster_small, &cfg) !=
+          cudaSuccess ||
+      n <= 0)
+    return -1;
+  known.emplace_back(smem, n);
+  return n;
+}
+
 int launch_verify_cluster_small(const LinearArgs &a, cudaStream_t stream) {
   if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
-  static int clusters = -1;   // co-resident clusters of this shape, asked once
-  if (cudaFuncSetAttribute(k_verify_cluster_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)RC_DYN_SMEM) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  const int n = cluster_count((const void *)k_verify_cluster_small, &clusters);
-  if (n <= 0) return SPEC_ERR_CUDA;
-  const int rc = launch_setup_stream(a, stream);
-  if (rc != SPEC_OK) return rc;
   RcArgs ra;
   ra.a = a;
   ra.slice = (a.V / 8 + RC_CLUSTER - 1) / RC_CLUSTER * 8;
+  const size_t slice_bytes = (size_t)ra.slice * 2;
+  ra.nbuf = (int)std::min<size_t>(std::max<size_t>(RQ_BUF_BYTES / slice_bytes, 2),
+                                  (size_t)(2 * a.max_k + 1));
+  const size_t smem = (size_t)ra.nbuf * slice_bytes;
+  const int n = cluster_small_count(smem);
+  if (n <= 0) return SPEC_ERR_CUDA;
+  if (cudaFuncSetAttribute(k_verify_cluster_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   const int grid_clusters = std::min(n, a.B);
   cudaEvent_t before, after;
   take_row_pass_events(&before, &after);
   if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  k_verify_cluster_small<<<RC_CLUSTER * grid_clusters, RC_THREADS, RC_DYN_SMEM, stream>>>(ra);
+  k_verify_cluster_small<<<RC_CLUSTER * grid_clusters, RC_THREADS, smem, stream>>>(ra);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
