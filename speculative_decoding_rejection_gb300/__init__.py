@@ -183,6 +183,17 @@ def spec_verify_linear_workspace(B: int, max_k: int, V: int, rule: int = SPEC_RU
     return int(lib().spec_verify_linear_workspace(B, max_k, V, rule))
 
 
+def _linear_workspace(B, max_k, V, rule, device, workspace):
+    # a caller's workspace goes to the library as it is: the call checks its
+    # size (SPEC_ERR_WORKSPACE) without a second query on this path
+    if workspace is not None:
+        return workspace
+    ws_bytes = spec_verify_linear_workspace(B, max_k, V, rule)
+    if ws_bytes == 0:
+        raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_linear_workspace")
+    return _workspace(ws_bytes, device)
+
+
 def spec_verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed: int, *,
                        max_k: int, rule: int = SPEC_RULE_STRICT,
                        draft_kind: int = SPEC_DRAFT_LOGITS, draft_idx=None, want_pq=False,
@@ -196,10 +207,7 @@ def spec_verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed:
     B = cu_draft.numel() - 1
     V = target.shape[1]
     dev = target.device
-    ws_bytes = spec_verify_linear_workspace(B, max_k, V, rule)
-    if ws_bytes == 0:
-        raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_linear_workspace")
-    ws = _workspace(ws_bytes, dev, workspace)
+    ws = _linear_workspace(B, max_k, V, rule, dev, workspace)
     if out is None:
         tokens = torch.empty(B, max_k + 1, dtype=torch.int32, device=dev)
         accepted = torch.empty(B, dtype=torch.int32, device=dev)
@@ -211,7 +219,7 @@ def spec_verify_linear(target, draft, draft_tokens, cu_draft, temperature, seed:
         _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(draft_idx),
         _ptr(draft_tokens), _ptr(cu_draft), _ptr(temperature), B, V, max_k,
         ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), rule, _ptr(tokens), _ptr(accepted),
-        _ptr(pq), _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+        _ptr(pq), _ptr(ws), ctypes.c_size_t(ws.numel() * ws.element_size()), _stream(stream))
     _check(code, "spec_verify_linear")
     return tokens, accepted, pq, ws
 
@@ -234,10 +242,7 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
     B = cu_draft.numel() - 1
     V = target.shape[1]
     dev = target.device
-    ws_bytes = spec_verify_linear_workspace(B, max_k, V, rule)
-    if ws_bytes == 0:
-        raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_linear_workspace")
-    ws = _workspace(ws_bytes, dev, workspace)
+    ws = _linear_workspace(B, max_k, V, rule, dev, workspace)
     if out is None:
         tokens = torch.empty(B, max_k + 1, dtype=torch.int32, device=dev)
         accepted = torch.empty(B, dtype=torch.int32, device=dev)
@@ -255,7 +260,7 @@ def spec_verify_linear_ext(target, draft, draft_tokens, cu_draft, temperature, s
         _ptr(target), _dtype_code(target), _ptr(draft), ddt, draft_kind, _ptr(draft_idx),
         _ptr(draft_tokens), _ptr(cu_draft), _ptr(temperature), B, V, max_k,
         ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), rule, ctypes.byref(ext), _ptr(tokens),
-        _ptr(accepted), _ptr(pq), _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+        _ptr(accepted), _ptr(pq), _ptr(ws), ctypes.c_size_t(ws.numel() * ws.element_size()), _stream(stream))
     _check(code, "spec_verify_linear_ext")
     return tokens, accepted, pq, rank, kl, ws
 
@@ -294,7 +299,7 @@ def spec_verify_tree(target, draft, node_token, parent, cu_nodes, temperature, s
             _ptr(parent))
     mid = (_ptr(cu_nodes), _ptr(temperature), B, n_nodes, V, max_depth, max_branch,
            ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF))
-    tail = (_ptr(tokens), _ptr(accepted), _ptr(path), _ptr(ws), ctypes.c_size_t(ws.numel()),
+    tail = (_ptr(tokens), _ptr(accepted), _ptr(path), _ptr(ws), ctypes.c_size_t(ws.numel() * ws.element_size()),
             _stream(stream))
     if node_fixed is None and seed_dev is None:
         code = lib().spec_verify_tree(*head, *mid, *tail)
@@ -326,7 +331,7 @@ def draft_topk_softmax(draft_logits, cu_rows, temperature, *, workspace=None, ou
     code = lib().draft_topk_softmax(
         _ptr(draft_logits), _dtype_code(draft_logits), rows, V, _ptr(cu_rows),
         _ptr(temperature), B, SPEC_TOPK, _ptr(idx), _ptr(prob), _ptr(ws),
-        ctypes.c_size_t(ws.numel()), _stream(stream))
+        ctypes.c_size_t(ws.numel() * ws.element_size()), _stream(stream))
     _check(code, "draft_topk_softmax")
     return idx, prob, ws
 
@@ -360,7 +365,7 @@ def spec_rheo_expand(draft, cu_frontier, frontier_score, temperature, seed: int,
         _ptr(draft), _dtype_code(draft), _ptr(cu_frontier), _ptr(frontier_score),
         _ptr(temperature), B, F, V, K, m, ctypes.c_float(eps), n_keep, ctypes.c_uint64(seed),
         level, _ptr(token), _ptr(qproxy), _ptr(qtrue), _ptr(score),
-        _ptr(keep) if n_keep > 0 else None, _ptr(ws), ctypes.c_size_t(ws.numel()),
+        _ptr(keep) if n_keep > 0 else None, _ptr(ws), ctypes.c_size_t(ws.numel() * ws.element_size()),
         _stream(stream))
     _check(code, "spec_rheo_expand")
     return token, qproxy, qtrue, score, keep, ws
@@ -406,7 +411,7 @@ def spec_check_selftest(workspace=None, stream=None):
     SPEC_ERR_BOUNDS. The product library raises SPEC_ERR_UNSUPPORTED."""
     torch = _torch()
     ws = torch.zeros(512, dtype=torch.uint8, device="cuda") if workspace is None else workspace
-    _check(lib().spec_check_selftest(_ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream)),
+    _check(lib().spec_check_selftest(_ptr(ws), ctypes.c_size_t(ws.numel() * ws.element_size()), _stream(stream)),
            "spec_check_selftest")
     return ws
 
