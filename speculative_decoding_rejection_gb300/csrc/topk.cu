@@ -209,24 +209,27 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh, float pre
         gather_candidates(w[u], v0 + u * TK_THREADS, pred, sh);
     }
   }
-  float m = fmaxf(bf16lo(pm), bf16hi(pm));
-  // descending bitonic sort of the warp's 32 maxima
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1)
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, m, j);
-      m = (((lane & k) == 0) == ((lane & j) == 0)) ? fmaxf(m, o) : fminf(m, o);
-    }
-  if (lane == SPEC_TOPK / TK_WARPS - 1) sh.tmax[warp] = m;
   __syncthreads();
   const int n1 = sh.cand_n;
   const bool held = predicted && n1 >= SPEC_TOPK && n1 <= CAND_CAP;
-  __syncthreads();   // every thread has read the count before it is reset
-  if (!held && t == 0) sh.cand_n = 0;
-  __syncthreads();
-  float bound = sh.tmax[0];
-  for (int w = 1; w < TK_WARPS; ++w) bound = fminf(bound, sh.tmax[w]);
+  float bound = -INFINITY;
+  if (!held) {   // the same branch in every thread
+    float m = fmaxf(bf16lo(pm), bf16hi(pm));
+    // descending bitonic sort of the warp's 32 maxima
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, m, j);
+        m = (((lane & k) == 0) == ((lane & j) == 0)) ? fmaxf(m, o) : fminf(m, o);
+      }
+    if (lane == SPEC_TOPK / TK_WARPS - 1) sh.tmax[warp] = m;
+    __syncthreads();   // also: every thread has read the count before it is reset
+    if (t == 0) sh.cand_n = 0;
+    __syncthreads();
+    bound = sh.tmax[0];
+    for (int w = 1; w < TK_WARPS; ++w) bound = fminf(bound, sh.tmax[w]);
+  }
   // the second pass (from L2), eight loads in flight again; a group of 8
   // logits is looked at only when its packed maximum reaches the bound
   for (int v0 = t; v0 < nvec && !held; v0 += 8 * TK_THREADS) {
@@ -248,11 +251,16 @@ __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh, float pre
   __syncthreads();
   const int n = sh.cand_n;
   if (n > CAND_CAP) return false;
-  for (int i = t; i < n; i += TK_THREADS) {
-    const unsigned long long ci = sh.cand[i];
+  // each candidate's rank, counted by a pair of threads (each half the
+  // candidates); every lane runs the same number of rounds
+  for (int base = 0; base < n; base += TK_THREADS / 2) {
+    const int i = base + (t >> 1);
+    const unsigned long long ci = i < n ? sh.cand[i] : 0ull;
     int r = 0;
-    for (int j = 0; j < n; ++j) r += sh.cand[j] > ci;
-    if (r < SPEC_TOPK) {
+    if (i < n)
+      for (int j = t & 1; j < n; j += 2) r += sh.cand[j] > ci;
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    if (i < n && (t & 1) == 0 && r < SPEC_TOPK) {
       sh.sel_idx[r] = (int)~(unsigned)(ci & 0xffffffffull);
       sh.sel_val[r] = value_of_key16((unsigned)(ci >> 32));
     }
