@@ -42,41 +42,45 @@ METRIC = ("verified draft positions/sec and achieved HBM GB/s (% of GB300 peak),
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM traffic of the row pass per algorithmic byte, from an ncu capture of
-# a smaller case of the same kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum over the algorithmic bytes it streams). Each figure
-# below is valid only for the sources it was taken on (KERNEL_SOURCES).
-# Captured on B=128, K=4, V=201088 bf16 (460.09 MB streamed by the launch):
-# 460.19 MB read + 3.43 MB written (the per-chunk partial statistics).
-ROWPASS_TRAFFIC = {"source_sha1": "6f64b6019569898dcbfb786b84f81e6a98e4f7e3",
-                   "dram_per_algorithmic_byte": (460192768 + 3425280) / 460089344}
-# The same for the streaming verifier (position-lazy schedule, the plain
-# call's schedule on dense bf16 logits), per byte of the rows the schedule
-# must read (target rows 1..n+1, dense draft rows 1..min(n+1, K) of sampling
-# requests). Captured on the full B=1024, K=4, V=201088 workload (one pass):
-# 2643.7 MB read + 29.9 MB written for 1975.1 MB; the excess is the residual
-# rows read a second time (they miss L2), so the ratio holds for this
-# workload and source only.
-STREAM_TRAFFIC = {"source_sha1": "00f57b9251426b7296dbf2ac5e3d82211de5284b",
-                  "dram_per_algorithmic_byte": (2643686912 + 29875200) / 1975086336}
-# The top-128 select (two passes, the second mostly from L2), per byte of
-# the draft rows; captured on the full B=256, K=7, V=151936 workload (one
-# pass): 556.56 MB read + 4.54 MB written for 544.54 MB. Valid for these
-# sources and this workload.
-TOPK_TRAFFIC = {"source_sha1": "e8249b1d1907a23dfa3f849dc81e33617e583623",
-                "dram_per_algorithmic_byte": (556563456 + 4540928) / 544538624}
-# The top-128 select with its construction epilogue on the construction
+# DRAM traffic of the dominant kernels per algorithmic byte, each from a
+# one-pass ncu capture (dram__bytes_read.sum + dram__bytes_write.sum over the
+# algorithmic bytes the launch must read). Each figure holds only for the
+# sources it was taken on (KERNEL_SOURCES, by SHA-1) and the workload named.
+# The eager row pass, captured on B=128, K=4, V=201088 bf16 (460.09 MB
+# streamed by the statistics launch): 460.19 MB read + 3.17 MB written (the
+# per-chunk partial statistics); traffic grows with the rows streamed.
+ROWPASS_TRAFFIC = {"source_sha1": "3577cae51a1dcd972e7af68969dbf9da5b401e55",
+                   "dram_per_algorithmic_byte": (460191232 + 3168000) / 460089344}
+# The streaming verifier (the plain call's schedule on dense bf16 logits),
+# per byte of the rows the schedule must read (target rows 1..n+1, dense
+# draft rows 1..min(n+1, K) of sampling requests), on the full B=1024, K=4,
+# V=201088 workload: 2641.1 MB read + 30.0 MB written for 1975.1 MB. The
+# excess is the residual row pairs read a second time (they miss L2).
+STREAM_TRAFFIC = {"source_sha1": "6ef51a705a9c6a095f2a4b7b45d874d0c63dee94",
+                  "dram_per_algorithmic_byte": (2641137920 + 29974016) / 1975086336}
+# The top-128 select (two passes, the second mostly skipped or from L2), per
+# byte of the draft rows, on the full B=256, K=7, V=151936 workload: 560.00 MB
+# read + 4.53 MB written for 544.54 MB.
+TOPK_TRAFFIC = {"source_sha1": "2aa5bd2a171ba72a2817a6025a25feaf74beb522",
+                "dram_per_algorithmic_byte": (559997696 + 4530176) / 544538624}
+# The same kernel with its construction epilogue on the construction
 # workload (640 frontier rows, V = 128256 bf16; L2 flushed before the call):
-# 164.55 MB read + 3.21 MB written for 164.17 MB (most of the write is
-# dirty lines of the L2 flush buffer, written back as the rows evict them).
-# Valid for these sources and workload.
-RHEO_TRAFFIC = {"source_sha1": "e8249b1d1907a23dfa3f849dc81e33617e583623",
-                "dram_per_algorithmic_byte": (164545024 + 3206912) / 164167680}
-# The tree walk (no row pass: only visited nodes' rows), per byte of those
-# rows' first read; captured on the full 32-tree workload (one pass): 63.30 MB
-# read + 0.49 MB written for 59.25 MB. Valid for these sources and workload.
-TREE_TRAFFIC = {"source_sha1": "0a249bdc0ac97606bbfcbb25420fbb6d07129a26",
-                "dram_per_algorithmic_byte": (63298560 + 493056) / 59254272}
+# 165.83 MB read + 3.20 MB written for 164.17 MB (most of the write is dirty
+# lines of the L2 flush buffer, written back as the rows evict them).
+RHEO_TRAFFIC = {"source_sha1": "2aa5bd2a171ba72a2817a6025a25feaf74beb522",
+                "dram_per_algorithmic_byte": (165833984 + 3201792) / 164167680}
+# The tree walk (only visited nodes' rows), per byte of those rows, on the
+# full 32-tree workload: 59.44 MB read + 0.34 MB written for 59.25 MB.
+TREE_TRAFFIC = {"source_sha1": "409168754d629f24d98e3b77afcda753d38a4028",
+                "dram_per_algorithmic_byte": (59441408 + 336640) / 59254272}
+# One cluster per request, on the 64-request, V = 32000 workload (L2 flushed):
+# 20.87 MB read, nothing written back, for 20.80 MB of rows.
+CLUSTER_TRAFFIC = {"source_sha1": "cb8c22284ccff900aef63a86a0ae60b80ca077ae",
+                   "dram_per_algorithmic_byte": (20869632 + 0) / 20800000}
+# The cluster-resident schedule on the full B=1024 workload: 1975.56 MB read
+# + 3.77 MB written for 1975.09 MB of first reads (each row read once).
+RESIDENT_TRAFFIC = {"source_sha1": "cb8c22284ccff900aef63a86a0ae60b80ca077ae",
+                    "dram_per_algorithmic_byte": (1975558656 + 3765248) / 1975086336}
 
 
 def parse(argv=None):
@@ -133,6 +137,7 @@ KERNEL_SOURCES = {
     "stream": ("stream.cu", "linear.cuh", "rowpass.cuh", "common.cuh", "internal.h"),
     "topk": ("topk.cu", "common.cuh", "internal.h"),
     "tree": ("tree.cu", "common.cuh", "internal.h"),
+    "resident": ("resident.cu", "linear.cuh", "rowpass.cuh", "common.cuh", "internal.h"),
 }
 
 
@@ -859,6 +864,12 @@ def traffic_for(work, args):
     if (kernel == "k_verify_stream" and ext is None and full and work.cfg == 5
             and STREAM_TRAFFIC["source_sha1"] == source_sha1("stream")):
         return STREAM_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    if (kernel == "k_verify_cluster_small" and full and work.cfg == 2
+            and CLUSTER_TRAFFIC["source_sha1"] == source_sha1("resident")):
+        return CLUSTER_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    if (kernel == "k_verify_resident" and full and work.cfg == 5
+            and RESIDENT_TRAFFIC["source_sha1"] == source_sha1("resident")):
+        return RESIDENT_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
     return None
 
 

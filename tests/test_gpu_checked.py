@@ -68,6 +68,8 @@ LINEAR_CASES = [
     ("top-128", dict(cfg=3, B=3, K=2, V=16), dict(rule=sv.SPEC_RULE_STRICT_TOP128), 0, False),
     ("top-128-fast-select", dict(cfg=3, B=2, K=2, V=4096),
      dict(rule=sv.SPEC_RULE_STRICT_TOP128), 0, False),
+    ("top-128-longer-rows", dict(cfg=3, B=2, K=3, V=16384),
+     dict(rule=sv.SPEC_RULE_STRICT_TOP128), 0, False),
     ("cactus-rank", dict(cfg=1, B=4, K=3, V=16, dtype="bf16"),
      dict(rule=sv.SPEC_RULE_CACTUS, ext=dict(alpha=0.3, max_rank=3, min_prob=0.01)), 0, False),
     ("kl", dict(cfg=1, B=4, K=3, V=16, dtype="bf16"), dict(kl=True), 0, False),
@@ -111,7 +113,7 @@ def test_linear_draft_probabilities_and_sparse_laws_checked():
     assert_linear_parity(g, ref, lb.cu_draft.cpu(), min_compared=int((ref["flag_slot"] < 0).sum()))
 
 
-@pytest.mark.parametrize("V,dtype", [(16, "f32"), (4096, "bf16")])
+@pytest.mark.parametrize("V,dtype", [(16, "f32"), (4096, "bf16"), (16384, "bf16")])
 def test_draft_topk_softmax_checked(V, dtype):
     lb = S.make_linear(3, device=DEV, B=3, K=2, V=V, dtype=dtype, T=[1.0, 0.0, 0.6],
                        input_seed=9000 + V)
