@@ -1074,6 +1074,7 @@ int launch_verify_resident(const LinearArgs &a, cudaStream_t stream) {
   RcArgs ra;
   ra.a = a;
   ra.slice = (a.V / 8 + RC_CLUSTER - 1) / RC_CLUSTER * 8;
+  ra.nbuf = 0;   // (the small-call kernel's)
   cudaEvent_t before, after;
   take_row_pass_events(&before, &after);
   if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
