@@ -56,7 +56,7 @@ ROWPASS_TRAFFIC = {"source_sha1": "3577cae51a1dcd972e7af68969dbf9da5b401e55",
 # draft rows 1..min(n+1, K) of sampling requests), on the full B=1024, K=4,
 # V=201088 workload: 2641.1 MB read + 30.0 MB written for 1975.1 MB. The
 # excess is the residual row pairs read a second time (they miss L2).
-STREAM_TRAFFIC = {"source_sha1": "6ef51a705a9c6a095f2a4b7b45d874d0c63dee94",
+STREAM_TRAFFIC = {"source_sha1": "30f8be954baca99450c4ea7487c41cdb8d856165",
                   "dram_per_algorithmic_byte": (2641137920 + 29974016) / 1975086336}
 # The top-128 select (two passes, the second mostly skipped or from L2), per
 # byte of the draft rows, on the full B=256, K=7, V=151936 workload: 560.00 MB
@@ -75,11 +75,11 @@ TREE_TRAFFIC = {"source_sha1": "409168754d629f24d98e3b77afcda753d38a4028",
                 "dram_per_algorithmic_byte": (59441408 + 336640) / 59254272}
 # One cluster per request, on the 64-request, V = 32000 workload (L2 flushed):
 # 20.87 MB read, nothing written back, for 20.80 MB of rows.
-CLUSTER_TRAFFIC = {"source_sha1": "e1288b4d39add2e9d94e627398942ce997407886",
+CLUSTER_TRAFFIC = {"source_sha1": "a6affc5777faca7eb26c74fcd896ec72c768cf8e",
                    "dram_per_algorithmic_byte": (20869632 + 0) / 20800000}
 # The cluster-resident schedule on the full B=1024 workload: 1975.56 MB read
 # + 3.77 MB written for 1975.09 MB of first reads (each row read once).
-RESIDENT_TRAFFIC = {"source_sha1": "e1288b4d39add2e9d94e627398942ce997407886",
+RESIDENT_TRAFFIC = {"source_sha1": "a6affc5777faca7eb26c74fcd896ec72c768cf8e",
                     "dram_per_algorithmic_byte": (1975558656 + 3765248) / 1975086336}
 
 

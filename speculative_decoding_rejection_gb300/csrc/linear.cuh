@@ -287,10 +287,10 @@ bool resident_supported(const LinearArgs &a);
 int launch_verify_resident(const LinearArgs &a, cudaStream_t stream);
 
 // Small calls whose rows are too long for the fused kernel (at most 128
-// requests, dense bf16 logits, V % 8 == 0, at most 8 drafts, every row of a
-// request fitting a cluster's shared memory; off when `limit_bytes`, the
-// fused limit, is 0): one cluster per request, all of its rows resident at
-// once, two exchanges per request.
+// requests, dense bf16 logits, V % 8 == 0, at most 8 drafts, a request's
+// 2K+1 row slices within 100 KB per CTA; off when `limit_bytes`, the fused
+// limit, is 0): one launch, one cluster per request, the rows through a few
+// shared-memory buffers per CTA, two exchanges per request.
 bool cluster_small_supported(const LinearArgs &a, const spec_linear_ext *ext,
                              size_t limit_bytes);
 int launch_verify_cluster_small(const LinearArgs &a, cudaStream_t stream);
