@@ -75,11 +75,11 @@ TREE_TRAFFIC = {"source_sha1": "409168754d629f24d98e3b77afcda753d38a4028",
                 "dram_per_algorithmic_byte": (59441408 + 336640) / 59254272}
 # One cluster per request, on the 64-request, V = 32000 workload (L2 flushed):
 # 20.87 MB read, nothing written back, for 20.80 MB of rows.
-CLUSTER_TRAFFIC = {"source_sha1": "a6affc5777faca7eb26c74fcd896ec72c768cf8e",
+CLUSTER_TRAFFIC = {"source_sha1": "ec60ff9f88dca5a57074f1110cc1d2f55c83a72e",
                    "dram_per_algorithmic_byte": (20869632 + 0) / 20800000}
 # The cluster-resident schedule on the full B=1024 workload: 1975.56 MB read
 # + 3.77 MB written for 1975.09 MB of first reads (each row read once).
-RESIDENT_TRAFFIC = {"source_sha1": "a6affc5777faca7eb26c74fcd896ec72c768cf8e",
+RESIDENT_TRAFFIC = {"source_sha1": "ec60ff9f88dca5a57074f1110cc1d2f55c83a72e",
                     "dram_per_algorithmic_byte": (1975558656 + 3765248) / 1975086336}
 
 

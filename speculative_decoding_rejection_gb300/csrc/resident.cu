@@ -977,8 +977,14 @@ bool cluster_small_supported(const LinearArgs &a, const spec_linear_ext *ext,
   return (size_t)(2 * a.max_k + 1) * slice * 2 <= RC_DYN_SMEM;
 }
 
-static int cluster_count(const void *kernel, int *cache) {
-  if (*cache < 0) {
+// Co-resident clusters of the cluster-resident kernel on the current device
+// (asked once per device).
+static int cluster_count(const void *kernel) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  int *c = &cache[dev];
+  if (*c <= 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(RC_CLUSTER * num_sms(), 1, 1);
     cfg.blockDim = dim3(RC_THREADS, 1, 1);
@@ -992,21 +998,24 @@ static int cluster_count(const void *kernel, int *cache) {
     cfg.numAttrs = 1;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) return -1;
-    *cache = n;
+    *c = n;
   }
-  return *cache;
+  return *c;
 }
 
 int launch_setup_stream(const LinearArgs &a, cudaStream_t stream);
 
 // Co-resident clusters of the one-cluster-per-request kernel with `smem`
-// bytes of buffers per CTA (asked once per size).
+// bytes of buffers per CTA on the current device (asked once per device and
+// size).
 static int cluster_small_count(size_t smem) {
   static std::mutex mu;
-  static std::vector<std::pair<size_t, int>> known;
+  static std::vector<std::pair<std::pair<int, size_t>, int>> known;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   std::lock_guard<std::mutex> lock(mu);
   for (const auto &k : known)
-    if (k.first == smem) return k.second;
+    if (k.first.first == dev && k.first.second == smem) return k.second;
   if (cudaFuncSetAttribute(k_verify_cluster_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return -1;
@@ -1026,7 +1035,7 @@ static int cluster_small_count(size_t smem) {
           cudaSuccess ||
       n <= 0)
     return -1;
-  known.emplace_back(smem, n);
+  known.push_back({{dev, smem}, n});
   return n;
 }
 
@@ -1063,12 +1072,12 @@ bool resident_supported(const LinearArgs &a) {
 
 int launch_verify_resident(const LinearArgs &a, cudaStream_t stream) {
   if (check_upload(stream) != SPEC_OK) return SPEC_ERR_CUDA;
-  static int clusters = -1;   // co-resident clusters of this shape, asked once
   const size_t smem = RC_DYN_SMEM;
   if (cudaFuncSetAttribute(k_verify_resident, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  if (cluster_count((const void *)k_verify_resident, &clusters) <= 0) return SPEC_ERR_CUDA;
+  const int clusters = cluster_count((const void *)k_verify_resident);
+  if (clusters <= 0) return SPEC_ERR_CUDA;
   const int rc = launch_setup_stream(a, stream);
   if (rc != SPEC_OK) return rc;
   RcArgs ra;
