@@ -49,20 +49,21 @@ FALLBACK_HBM_GBS = 6800.0
 # The eager row pass, captured on B=128, K=4, V=201088 bf16 (460.09 MB
 # streamed by the statistics launch): 460.19 MB read + 3.17 MB written (the
 # per-chunk partial statistics); traffic grows with the rows streamed.
-ROWPASS_TRAFFIC = {"source_sha1": "3577cae51a1dcd972e7af68969dbf9da5b401e55",
+ROWPASS_TRAFFIC = {"source_sha1": "089bca83aabd9d0b574cae9517613beb42256896",
                    "dram_per_algorithmic_byte": (460191232 + 3168000) / 460089344}
 # The streaming verifier (the plain call's schedule on dense bf16 logits),
 # per byte of the rows the schedule must read (target rows 1..n+1, dense
 # draft rows 1..min(n+1, K) of sampling requests), on the full B=1024, K=4,
 # V=201088 workload: 2641.1 MB read + 30.0 MB written for 1975.1 MB. The
 # excess is the residual row pairs read a second time (they miss L2).
-STREAM_TRAFFIC = {"source_sha1": "30f8be954baca99450c4ea7487c41cdb8d856165",
+STREAM_TRAFFIC = {"source_sha1": "a6f5f03f598101c9d0d7ae74d9c884fdd548d402",
                   "dram_per_algorithmic_byte": (2641137920 + 29974016) / 1975086336}
-# The top-128 select (two passes, the second mostly skipped or from L2), per
-# byte of the draft rows, on the full B=256, K=7, V=151936 workload: 560.00 MB
-# read + 4.53 MB written for 544.54 MB.
-TOPK_TRAFFIC = {"source_sha1": "2aa5bd2a171ba72a2817a6025a25feaf74beb522",
-                "dram_per_algorithmic_byte": (559997696 + 4530176) / 544538624}
+# The scan launch of the top-128 select (every draft row streamed once through
+# a TMA ring; the candidate lists written), per byte of the draft rows, on the
+# full B=256, K=7, V=151936 workload: 544.65 MB read + 5.63 MB written for
+# 544.54 MB.
+TOPK_TRAFFIC = {"source_sha1": "2ecf548e3f90159ca2d13b7c6604fc8b3f663677",
+                "dram_per_algorithmic_byte": (544654080 + 5634560) / 544538624}
 # The same kernel with its construction epilogue on the construction
 # workload (640 frontier rows, V = 128256 bf16; L2 flushed before the call):
 # 165.83 MB read + 3.20 MB written for 164.17 MB (most of the write is dirty
@@ -71,15 +72,15 @@ RHEO_TRAFFIC = {"source_sha1": "2aa5bd2a171ba72a2817a6025a25feaf74beb522",
                 "dram_per_algorithmic_byte": (165833984 + 3201792) / 164167680}
 # The tree walk (only visited nodes' rows), per byte of those rows, on the
 # full 32-tree workload: 59.44 MB read + 0.34 MB written for 59.25 MB.
-TREE_TRAFFIC = {"source_sha1": "409168754d629f24d98e3b77afcda753d38a4028",
+TREE_TRAFFIC = {"source_sha1": "8408c697af22d8b9f9984139dea723ecc0fe3d37",
                 "dram_per_algorithmic_byte": (59441408 + 336640) / 59254272}
 # One cluster per request, on the 64-request, V = 32000 workload (L2 flushed):
 # 20.87 MB read, nothing written back, for 20.80 MB of rows.
-CLUSTER_TRAFFIC = {"source_sha1": "ec60ff9f88dca5a57074f1110cc1d2f55c83a72e",
+CLUSTER_TRAFFIC = {"source_sha1": "8062fccebf60030901430de34f2c8e9b257607f0",
                    "dram_per_algorithmic_byte": (20869632 + 0) / 20800000}
 # The cluster-resident schedule on the full B=1024 workload: 1975.56 MB read
 # + 3.77 MB written for 1975.09 MB of first reads (each row read once).
-RESIDENT_TRAFFIC = {"source_sha1": "ec60ff9f88dca5a57074f1110cc1d2f55c83a72e",
+RESIDENT_TRAFFIC = {"source_sha1": "8062fccebf60030901430de34f2c8e9b257607f0",
                     "dram_per_algorithmic_byte": (1975558656 + 3765248) / 1975086336}
 
 
@@ -347,11 +348,16 @@ class LinearWork:
         # top-128 select, which then dominates, reads every draft row
         self.rowpass_bytes = (lb.draft.numel() * lb.draft.element_size() if lb.top128
                               else self.tgt_bytes + self.drf_bytes)
-        self.kernel = "k_topk128" if lb.top128 else None
+        # the top-128 select of bf16 rows with V % 8 == 0 and V >= 4096 runs
+        # as a scan launch (which reads the rows) and a finishing launch
+        topk_split = (lb.top128 and lb.draft.dtype == torch.bfloat16 and lb.V % 8 == 0
+                      and lb.V >= 4096)
+        self.kernel = (("k_topk128_scan" if topk_split else "k_topk128") if lb.top128
+                       else None)
         # setup, row pass, accept, final draws, + the residual sums (dense
         # drafts) or the top-128 select (truncation); the header memset is
         # not ours
-        self.launches = 5
+        self.launches = 6 if topk_split else 5
         self.outs = (torch.empty(lb.B, lb.max_k + 1, dtype=torch.int32, device=dev),
                      torch.empty(lb.B, dtype=torch.int32, device=dev), None)
         self.ws = torch.empty(sv.spec_verify_linear_workspace(lb.B, lb.max_k, lb.V, self.rule),
@@ -378,7 +384,7 @@ class LinearWork:
             # them the setup, the top-128 select or the residual sums, and
             # the final draws
             self.launches = (2 if self.resident else 3 if self.stream
-                             else 3 + 2 * (lb.max_k + 1))
+                             else 3 + 2 * (lb.max_k + 1) + (1 if topk_split else 0))
         # small calls of the strict or greedy rule on dense logits or
         # probabilities run as one fused kernel (the library's own test:
         # rows of at most 8192 logits, at most 1 MiB of rows per request and
@@ -781,10 +787,13 @@ def l2_size(dev):
 
 def timed_calls(work, sv, dev, steps, warmup, world):
     """W warm-up calls, then `steps` calls bracketed by a barrier and a
-    device synchronisation, timed with CUDA events on the calling stream;
-    the library records two more events around the dominant kernel of each
-    call. Returns the step time (max over ranks), that kernel's mean time,
-    whether L2 was flushed, and the clocks sampled meanwhile."""
+    device synchronisation, timed with CUDA events on the calling stream.
+    A second pass of `steps` calls, after the timed one, has the library
+    record two more events around the dominant kernel of each call (those
+    records would add some microseconds to a short call, so the step time is
+    taken without them). Returns the step time (max over ranks), that
+    kernel's mean time, whether L2 was flushed, and the clocks sampled
+    during the timed calls."""
     import torch
     for _ in range(max(3, warmup)):
         work.call()
@@ -815,21 +824,25 @@ def timed_calls(work, sv, dev, steps, warmup, world):
     torch.cuda.synchronize()
     e0.record()
     for k in range(K):
-        # the events of the dominant kernel are registered before the call's
-        # interval opens (registering is host work, not part of the call)
-        sv.spec_profile_row_pass(ev_b[k], ev_a[k])
         if flush:
             scratch.fill_(k & 255)
             ev_s[k].record()
         work.call()
-        if k == 0 and sv.spec_profile_pending():
-            raise RuntimeError(f"{work.kernel}: the call recorded no profiling events")
         if flush:
             ev_e[k].record()
     e1.record()
     torch.cuda.synchronize()
     barrier(world)
     clocks.stop()
+    # the dominant kernel's duration, from the same calls repeated
+    for k in range(K):
+        sv.spec_profile_row_pass(ev_b[k], ev_a[k])
+        if flush:
+            scratch.fill_(k & 255)
+        work.call()
+        if k == 0 and sv.spec_profile_pending():
+            raise RuntimeError(f"{work.kernel}: the call recorded no profiling events")
+    torch.cuda.synchronize()
     sv.spec_profile_row_pass(None, None)
     if flush:
         ms_step = max_over_ranks(statistics.mean(s_.elapsed_time(e_) for s_, e_ in
@@ -852,12 +865,12 @@ def traffic_for(work, args):
     if kernel == "k_row_pass" and getattr(work, "kl", None) is None and ext is None:
         if ROWPASS_TRAFFIC["source_sha1"] == source_sha1("rowpass"):
             return ROWPASS_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-    if kernel == "k_topk128" and full:
-        if isinstance(work, RheoWork):
-            if RHEO_TRAFFIC["source_sha1"] == source_sha1("topk"):
-                return RHEO_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
-        elif work.cfg == 3 and TOPK_TRAFFIC["source_sha1"] == source_sha1("topk"):
-            return TOPK_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    if (kernel == "k_topk128" and full and isinstance(work, RheoWork)
+            and RHEO_TRAFFIC["source_sha1"] == source_sha1("topk")):
+        return RHEO_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
+    if (kernel == "k_topk128_scan" and full and work.cfg == 3
+            and TOPK_TRAFFIC["source_sha1"] == source_sha1("topk")):
+        return TOPK_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes
     if (kernel == "k_tree_walk" and full and work.cfg == 4
             and TREE_TRAFFIC["source_sha1"] == source_sha1("tree")):
         return TREE_TRAFFIC["dram_per_algorithmic_byte"] * work.rowpass_bytes

@@ -374,7 +374,11 @@ int spec_verify_tree_ext(const void *target, int tdt, const void *draft,
                          void *workspace, size_t ws_bytes,
                          spec_stream_t stream);
 
-/* Bytes of workspace draft_topk_softmax needs (0 on invalid sizes). */
+/*
+ * Bytes of workspace draft_topk_softmax needs (0 on invalid sizes): a
+ * 256-byte header, and for V % 8 == 0 with V >= 4096 the candidate lists of
+ * the two-launch select (4 KB and 4 bytes per row).
+ */
 size_t draft_topk_softmax_workspace(int rows, int V);
 
 /*
@@ -385,7 +389,9 @@ size_t draft_topk_softmax_workspace(int rows, int V);
  * argmax. When V < 128 the tail slots hold id -1 and probability 0.
  *
  *   draft_logits [rows, V] (dt); cu_rows [B+1] int32 with cu_rows[B] = rows;
- *   k must be 128; out_idx [rows, 128] int32; out_prob [rows, 128] f32.
+ *   k must be 128; out_idx [rows, 128] int32; out_prob [rows, 128] f32;
+ *   workspace of draft_topk_softmax_workspace(rows, V) bytes, 256-byte
+ *   aligned (smaller or misaligned: SPEC_ERR_WORKSPACE).
  */
 int draft_topk_softmax(const void *draft_logits, int dt, int rows, int V,
                        const int32_t *cu_rows, const float *temperature, int B,
@@ -503,13 +509,16 @@ int spec_wait_selftest(int kind, unsigned long long limit_ns, void *workspace,
 
 /*
  * Profiling aid. Registers two CUDA events (cudaEvent_t, created by the
- * caller) for the next spec_verify_linear / spec_verify_tree call made by
- * the calling host thread: that call records `before` immediately before it
- * launches its dominant kernel and `after` immediately after, on the call's
- * stream, then forgets them. Pass NULLs to clear. The dominant kernel is the
+ * caller) for the next spec_verify_linear, spec_verify_tree,
+ * draft_topk_softmax or spec_rheo_expand call made by the calling host
+ * thread: that call records `before` immediately before it launches its
+ * dominant kernel and `after` immediately after, on the call's stream, then
+ * forgets them. Pass NULLs to clear. The dominant kernel is the
  * row-statistics pass of an eager linear call (it streams every vocabulary
- * row once), the top-128 select under SPEC_RULE_STRICT_TOP128, the streaming
- * kernel of a position-lazy call (SPEC_EXT_LAZY) or,
+ * row once), the top-128 select under SPEC_RULE_STRICT_TOP128 and in
+ * draft_topk_softmax (for bf16 rows with V % 8 == 0 and V >= 4096, its scan
+ * launch, which reads every row; the short finishing launch follows), the
+ * streaming kernel of a position-lazy call (SPEC_EXT_LAZY) or,
  * on its multi-launch schedule, all its rounds (every row pass and every
  * per-round decision), the one kernel of a small call (fused or one cluster
  * per request), the cluster-resident kernel (SPEC_EXT_RESIDENT), the walk of

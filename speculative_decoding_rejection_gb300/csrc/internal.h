@@ -79,11 +79,17 @@ struct RheoEpi {
 // Top-128 select + softmax over draft rows. Row r belongs to the request b
 // with cu_rows[b] <= r < cu_rows[b+1]; rows >= cu_rows[B] are skipped.
 // out_idx / out_prob may be NULL when `rh` is given: the rows then feed the
-// RheoSampling epilogue instead.
+// RheoSampling epilogue instead. With `lists` (topk_list_bytes(rows_bound)
+// bytes, 256-byte aligned) and rows topk_two_launch() takes, the select runs
+// as a scan launch and a finishing launch; otherwise as one launch. The
+// events, if given, are recorded around the launch that reads the rows.
 int launch_topk128(const void *logits, int dtype, int rows_bound, int V,
                    const int32_t *cu_rows, const float *temperature, int B,
                    int32_t *out_idx, float *out_prob, WsHeader *hdr,
-                   cudaStream_t stream, const RheoEpi *rh = nullptr);
+                   cudaStream_t stream, const RheoEpi *rh = nullptr, void *lists = nullptr,
+                   cudaEvent_t before = nullptr, cudaEvent_t after = nullptr);
+size_t topk_list_bytes(long long rows);
+bool topk_two_launch(int dtype, int V, bool epilogue);
 
 bool aligned(const void *p, size_t a);
 

@@ -29,7 +29,8 @@
 namespace sv {
 
 struct LinearLayout {
-  size_t hdr, err, req, jobs_a, jobs_b, tsum, list, part, kl_part, tk_idx, tk_prob, rank_thr;
+  size_t hdr, err, req, jobs_a, jobs_b, tsum, list, part, kl_part, tk_idx, tk_prob, tk_list;
+  size_t rank_thr;
   size_t ent_d, ready_d, pos_done, pos_join, rej_at, zd_at, total;
   int nch_max, nch_max_lazy, nch_max_stream;
   long long rows_max;
@@ -62,6 +63,8 @@ static LinearLayout linear_layout(int B, int max_k, int V, int rule) {
                 std::max((size_t)B * (max_k + 1) * L.nch_max, (size_t)B * L.nch_max_lazy));
   L.tk_idx = o;  o += align256(sizeof(int32_t) * tk);
   L.tk_prob = o; o += align256(sizeof(float) * tk);
+  L.tk_list = o;   // the top-128 select's candidate lists
+  o += rule == SPEC_RULE_STRICT_TOP128 ? topk_list_bytes((long long)B * max_k) : 0;
   L.rank_thr = o; o += align256(sizeof(float) * (size_t)B * (max_k + 1));
   // streaming verifier: residual entries (32 B) and their ready flags,
   // per-position counters, first rejections
@@ -1062,15 +1065,15 @@ extern "C" int spec_verify_linear_ext(const void *target, int tdt, const void *d
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (rule == SPEC_RULE_STRICT_TOP128) {
     // the top-128 select reads every draft row and dominates this rule's
-    // call: profiling events, if registered, bracket it
+    // call: profiling events, if registered, bracket its launch that reads
+    // the rows
     cudaEvent_t before, after;
     take_row_pass_events(&before, &after);
-    if (before && cudaEventRecord(before, st) != cudaSuccess) return SPEC_ERR_CUDA;
     const int rc = launch_topk128(draft, ddt, B * max_k, V, cu_draft, temperature, B,
                                   reinterpret_cast<int32_t *>(ws + L.tk_idx),
-                                  reinterpret_cast<float *>(ws + L.tk_prob), a.hdr, st);
+                                  reinterpret_cast<float *>(ws + L.tk_prob), a.hdr, st, nullptr,
+                                  ws + L.tk_list, before, after);
     if (rc != SPEC_OK) return rc;
-    if (after && cudaEventRecord(after, st) != cudaSuccess) return SPEC_ERR_CUDA;
   }
   RowPassArgs rp;
   rp.base[0] = a.target;

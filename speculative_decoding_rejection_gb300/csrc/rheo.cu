@@ -189,11 +189,9 @@ extern "C" int spec_rheo_expand(const void *draft, int ddt, const int32_t *cu_fr
     // row and dominates the call: profiling events, if registered, bracket it
     cudaEvent_t before, after;
     take_row_pass_events(&before, &after);
-    if (before && cudaEventRecord(before, st) != cudaSuccess) return SPEC_ERR_CUDA;
     const int rc = launch_topk128(draft, ddt, F, V, cu_frontier, temperature, B, nullptr,
-                                  nullptr, a.hdr, st, &epi);
+                                  nullptr, a.hdr, st, &epi, nullptr, before, after);
     if (rc != SPEC_OK) return rc;
-    if (after && cudaEventRecord(after, st) != cudaSuccess) return SPEC_ERR_CUDA;
   }
   if (B > 0 && n_keep > 0) {
     // shared memory for the largest tree the call can hold
