@@ -199,6 +199,29 @@ __device__ __forceinline__ RowStat shfl_stat(const RowStat &s, int src) {
                  __shfl_sync(0xffffffffu, s.idx, src)};
 }
 
+// q(d) of sparse draft row `row` for one lane: the probability listed with
+// id d, 0 when d is not listed. 16-byte loads, eight in flight, no early
+// exit, where the ids are 16-byte aligned (the top-128 scratch); a caller's
+// ids need only 4-byte alignment and are read one by one.
+__device__ __forceinline__ float lane_sparse_q(const LinearArgs &a, int row, int d) {
+  const int32_t *ids = a.draft_idx + (long long)row * SPEC_TOPK;
+  int hit = -1;
+  if (((uintptr_t)ids & 15) == 0) {
+    const int4 *ids4 = reinterpret_cast<const int4 *>(ids);
+#pragma unroll 8
+    for (int k = 0; k < SPEC_TOPK / 4; ++k) {
+      const int4 v = GLD(ids4 + k);
+      if (hit < 0)
+        hit = v.x == d ? 4 * k : v.y == d ? 4 * k + 1 : v.z == d ? 4 * k + 2
+            : v.w == d ? 4 * k + 3 : -1;
+    }
+  } else {
+    for (int k = 0; k < SPEC_TOPK && hit < 0; ++k)
+      if (GLD(ids + k) == d) hit = k;
+  }
+  return hit >= 0 ? GLD(a.sparse_prob + ((long long)row * SPEC_TOPK + hit)) : 0.f;
+}
+
 __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a) {
   const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -280,7 +303,10 @@ __global__ void __launch_bounds__(ACCEPT_WARPS * 32) k_accept(const LinearArgs a
     const bool rej =
         lane < cnt && (dense ? position_rejects_z(a, b, r, i, sample, ts, ds, rank, d, zt, zq,
                                                   false)
-                             : position_rejects(a, b, r, i, sample, ts, ds, rank));
+                             : position_rejects(a, b, r, i, sample, ts, ds, rank,
+                                                a.sparse && sample && (unsigned)d < (unsigned)a.V
+                                                    ? lane_sparse_q(a, r.d0 + i, d)
+                                                    : -1.f));
     const unsigned bal = __ballot_sync(0xffffffffu, rej);
     if (n == K && bal) {
       n = base + __ffs(bal) - 1;
@@ -626,24 +652,27 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
   const int tpc = chunk_elems / SAMPLE_TILE;  // tiles per chunk
   const int nch = a.nch_t;
   const Part *pp = a.part + (long long)tslot(a, r, job.b, job.n) * a.nch_max * RS_CONS_WARPS;
-  for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
-    float m = 0.f;
-    for (int w = 0; w < RS_CONS_WARPS; ++w) {
-      const Part p = GLD(pp + ch * RS_CONS_WARPS + w);
-      m += p.S * ex2((p.m - q.mt) * q.c);
-    }
-    sh.corr[ch] = m * q.invSt;   // chunk mass of p
-  }
   const bool sparse_res = kind == 1 && DK == SPEC_DRAFT_SPARSE128;
   if (sparse_res && threadIdx.x < sh.n_sparse) {   // min(p, q) at every listed id
     const int id = sh.s_idx[threadIdx.x];
     const float p = ex2((load_elem(q.trow, a.tdt, id) - q.mt) * q.c) * q.invSt;
     sh.pmin[threadIdx.x] = fminf(p, sh.s_prob[threadIdx.x]);
   }
+  if (sparse_res) __syncthreads();
+  for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
+    float m = 0.f;
+    for (int w = 0; w < RS_CONS_WARPS; ++w) {
+      const Part p = GLD(pp + ch * RS_CONS_WARPS + w);
+      m += p.S * ex2((p.m - q.mt) * q.c);
+    }
+    m *= q.invSt;   // chunk mass of p
+    if (sparse_res)   // less min(p, q) at the chunk's listed ids, in id order
+      for (int k = 0; k < sh.n_sparse; ++k)
+        if (sh.s_idx[k] / chunk_elems == ch) m -= sh.pmin[k];
+    sh.corr[ch] = m;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (sparse_res)
-      for (int k = 0; k < sh.n_sparse; ++k) sh.corr[sh.s_idx[k] / chunk_elems] -= sh.pmin[k];
     float Z = 0.f;
     for (int ch = 0; ch < nch; ++ch) Z += fmaxf(sh.corr[ch], 0.f);
     sh.Z = Z;
@@ -689,8 +718,10 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
         const int x0 = j * SAMPLE_TILE + (int)threadIdx.x * SAMPLE_EPT;
         float z[SAMPLE_EPT];
         raw_to_z(raw[u], q.trow, a.tdt, q.tvec, x0, a.V, z);
-        tile_weights_z<DK>(a, sh, z, x0, q.drow, q.dvec, kind, q.c, q.mt, q.invSt, q.md,
-                           q.invSd, w);
+        // a residual against a sparse law sums p here; the listed ids'
+        // min(p, q) come off each tile's sum below
+        tile_weights_z<DK>(a, sh, z, x0, q.drow, q.dvec, sparse_res ? 2 : kind, q.c, q.mt,
+                           q.invSt, q.md, q.invSd, w);
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < SAMPLE_EPT; ++k) s += w[k];
@@ -717,6 +748,14 @@ __device__ int chunk_draw(const LinearArgs &a, SampleSmem &sh, const Job &job, c
     float t = 0.f;
     for (int q2 = 0; q2 < SAMPLE_THREADS / 32; ++q2)
       t += sh.cwarp[threadIdx.x * (SAMPLE_THREADS / 32) + q2];
+    if (BATCH && sparse_res) {   // max(0, p - q) = p - min(p, q) at the listed ids
+      const int x_lo = (j0 + (int)threadIdx.x) * SAMPLE_TILE, x_hi = x_lo + SAMPLE_TILE;
+      for (int k = 0; k < sh.n_sparse; ++k) {
+        const int id = sh.s_idx[k];
+        if (id >= x_lo && id < x_hi) t -= sh.pmin[k];
+      }
+      t = fmaxf(t, 0.f);
+    }
     sh.csum[threadIdx.x] = t;
   }
   __syncthreads();
