@@ -49,38 +49,38 @@ FALLBACK_HBM_GBS = 6800.0
 # The eager row pass, captured on B=128, K=4, V=201088 bf16 (460.09 MB
 # streamed by the statistics launch): 460.19 MB read + 3.17 MB written (the
 # per-chunk partial statistics); traffic grows with the rows streamed.
-ROWPASS_TRAFFIC = {"source_sha1": "089bca83aabd9d0b574cae9517613beb42256896",
+ROWPASS_TRAFFIC = {"source_sha1": "b64fa69e6b7a8f0b74ddcaf7fbfeba501e17658a",
                    "dram_per_algorithmic_byte": (460191232 + 3168000) / 460089344}
 # The streaming verifier (the plain call's schedule on dense bf16 logits),
 # per byte of the rows the schedule must read (target rows 1..n+1, dense
 # draft rows 1..min(n+1, K) of sampling requests), on the full B=1024, K=4,
 # V=201088 workload: 2641.1 MB read + 30.0 MB written for 1975.1 MB. The
 # excess is the residual row pairs read a second time (they miss L2).
-STREAM_TRAFFIC = {"source_sha1": "a6f5f03f598101c9d0d7ae74d9c884fdd548d402",
+STREAM_TRAFFIC = {"source_sha1": "2969cb4758d155e2c045fd3171419fb89a51f543",
                   "dram_per_algorithmic_byte": (2641137920 + 29974016) / 1975086336}
 # The scan launch of the top-128 select (every draft row streamed once through
 # a TMA ring; the candidate lists written), per byte of the draft rows, on the
 # full B=256, K=7, V=151936 workload: 544.65 MB read + 5.63 MB written for
 # 544.54 MB.
-TOPK_TRAFFIC = {"source_sha1": "2ecf548e3f90159ca2d13b7c6604fc8b3f663677",
+TOPK_TRAFFIC = {"source_sha1": "48b164570fb41322b175f33fae7a4fdf8c94bbc7",
                 "dram_per_algorithmic_byte": (544654080 + 5634560) / 544538624}
-# The same kernel with its construction epilogue on the construction
+# The one-launch select with its construction epilogue on the construction
 # workload (640 frontier rows, V = 128256 bf16; L2 flushed before the call):
-# 165.83 MB read + 3.20 MB written for 164.17 MB (most of the write is dirty
+# 164.78 MB read + 2.97 MB written for 164.17 MB (most of the write is dirty
 # lines of the L2 flush buffer, written back as the rows evict them).
-RHEO_TRAFFIC = {"source_sha1": "2aa5bd2a171ba72a2817a6025a25feaf74beb522",
-                "dram_per_algorithmic_byte": (165833984 + 3201792) / 164167680}
+RHEO_TRAFFIC = {"source_sha1": "48b164570fb41322b175f33fae7a4fdf8c94bbc7",
+                "dram_per_algorithmic_byte": (164779776 + 2966528) / 164167680}
 # The tree walk (only visited nodes' rows), per byte of those rows, on the
 # full 32-tree workload: 59.44 MB read + 0.34 MB written for 59.25 MB.
-TREE_TRAFFIC = {"source_sha1": "8408c697af22d8b9f9984139dea723ecc0fe3d37",
+TREE_TRAFFIC = {"source_sha1": "7f9144f91ac9588f720bdc63aa129edc5d43c268",
                 "dram_per_algorithmic_byte": (59441408 + 336640) / 59254272}
 # One cluster per request, on the 64-request, V = 32000 workload (L2 flushed):
 # 20.87 MB read, nothing written back, for 20.80 MB of rows.
-CLUSTER_TRAFFIC = {"source_sha1": "8062fccebf60030901430de34f2c8e9b257607f0",
+CLUSTER_TRAFFIC = {"source_sha1": "3b6b97034da52ff5ea8b44dc3ff4aaf922a994de",
                    "dram_per_algorithmic_byte": (20869632 + 0) / 20800000}
 # The cluster-resident schedule on the full B=1024 workload: 1975.56 MB read
 # + 3.77 MB written for 1975.09 MB of first reads (each row read once).
-RESIDENT_TRAFFIC = {"source_sha1": "8062fccebf60030901430de34f2c8e9b257607f0",
+RESIDENT_TRAFFIC = {"source_sha1": "3b6b97034da52ff5ea8b44dc3ff4aaf922a994de",
                     "dram_per_algorithmic_byte": (1975558656 + 3765248) / 1975086336}
 
 
