@@ -145,6 +145,30 @@ def test_top128_rule_reduced_workload3():
     assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=20)
 
 
+def test_top128_rule_ragged_drafts_after_a_full_call_on_one_workspace():
+    """Under the top-128 rule the select's scratch holds B * max_k rows. A
+    call with every request at max_k fills them all; a ragged call on the
+    same workspace has fewer rows, and the scan marks the rest empty, so the
+    finishing launch never reads the lists the first call left there. Both
+    calls against the oracle (bf16, V % 8 == 0: the two-launch select)."""
+    full = S.make_linear(3, device=DEV, B=24, K=7, V=20480, input_seed=40)
+    rag = S.make_linear(3, device=DEV, B=24, K=(1, 7), V=20480, input_seed=41)
+    assert rag.max_k == full.max_k == 7
+    assert int(rag.cu_draft[-1]) < 24 * 7
+    rule = sv.SPEC_RULE_STRICT_TOP128
+    ws = torch.empty(sv.spec_verify_linear_workspace(24, 7, 20480, rule), dtype=torch.uint8,
+                     device=DEV)
+    for lb in (full, rag):
+        tokens, acc, pq, _ = sv.spec_verify_linear(
+            lb.target, lb.draft, lb.draft_tokens, lb.cu_draft, lb.temperature, lb.seed,
+            max_k=7, rule=rule, want_pq=True, workspace=ws)
+        g = dict(tokens=tokens.cpu().numpy(), accepted=acc.cpu().numpy(),
+                 pq=pq.cpu().numpy().astype(np.float64), status=sv.spec_get_status(ws))
+        assert g["status"] == sv.SPEC_OK
+        r = oracle_linear(lb, rule=rule)
+        assert_linear_parity(g, r, lb.cu_draft.cpu(), min_compared=18)
+
+
 @pytest.mark.usefixtures("schedule")
 def test_greedy_rule_forces_prefix_matching():
     lb = S.make_linear(1, device=DEV, B=16, K=6, V=2048, input_seed=4)
