@@ -62,13 +62,13 @@ STREAM_TRAFFIC = {"source_sha1": "2969cb4758d155e2c045fd3171419fb89a51f543",
 # a TMA ring; the candidate lists written), per byte of the draft rows, on the
 # full B=256, K=7, V=151936 workload: 544.65 MB read + 5.63 MB written for
 # 544.54 MB.
-TOPK_TRAFFIC = {"source_sha1": "48b164570fb41322b175f33fae7a4fdf8c94bbc7",
+TOPK_TRAFFIC = {"source_sha1": "bee0425e69af33d175a654a92c313afa23fd80c0",
                 "dram_per_algorithmic_byte": (544654080 + 5634560) / 544538624}
 # The one-launch select with its construction epilogue on the construction
 # workload (640 frontier rows, V = 128256 bf16; L2 flushed before the call):
 # 164.78 MB read + 2.97 MB written for 164.17 MB (most of the write is dirty
 # lines of the L2 flush buffer, written back as the rows evict them).
-RHEO_TRAFFIC = {"source_sha1": "48b164570fb41322b175f33fae7a4fdf8c94bbc7",
+RHEO_TRAFFIC = {"source_sha1": "bee0425e69af33d175a654a92c313afa23fd80c0",
                 "dram_per_algorithmic_byte": (164779776 + 2966528) / 164167680}
 # The tree walk (only visited nodes' rows), per byte of those rows, on the
 # full 32-tree workload: 59.44 MB read + 0.34 MB written for 59.25 MB.

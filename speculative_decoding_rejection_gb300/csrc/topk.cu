@@ -2,6 +2,12 @@
 // Top-128": the draft logits keep their 128 largest entries, the rest is set
 // to -inf, and the softmax runs over the survivors).
 //
+// bf16 rows with V a multiple of 8 and V >= 4096, outside the RheoSampling
+// epilogue, take two launches: k_topk128_scan streams the rows and leaves a
+// candidate list per row, and k_topk128_finish selects, orders and softmaxes
+// (see the two-launch section below). Everything else takes one launch,
+// k_topk128:
+//
 // One 512-thread CTA per row at a time, two CTAs per SM, rows taken in grid
 // strides (measured faster than 4 x 256 or 8 x 128 threads per SM). bf16 rows
 // (V a multiple of 8, V >= 4096) take the fast path, each pass keeping eight
@@ -155,23 +161,8 @@ __device__ __forceinline__ float value_of_key16(unsigned key) {
   return __uint_as_float(bits << 16);
 }
 
-// Fast selection for bf16 rows with V % 8 == 0 and V >= 8 * TK_THREADS
-// (every row 16-byte aligned, every thread holds elements). A packed max pass
-// leaves each thread's maximum; every warp sorts its 32 maxima with a
-// shuffle bitonic network, and the smallest of the warps' 8th-largest
-// maxima is a lower bound on the 128-th largest element (16 warps x 8
-// threads each hold an element at least that large). A second pass, read
-// back from L2 (one row per CTA, two CTAs per SM, keeps the rows in flight
-// far below L2), gathers the elements at or above the bound — a few hundred
-// on logit rows — and the exact top 128 (ties to the lower id) is ranked
-// among them in shared memory. Returns false, having written no selection,
-// when the candidates overflow CAND_CAP.
-//
-// With a predicted bound `pred` (finite: the block's previous row's 128th
-// largest logit minus a margin), the max pass also gathers the elements at or
-// above pred. When at least 128 are found, every element of the top 128 is
-// among them (the 128th largest is then >= pred), so the second pass is
-// skipped; otherwise (too few, or an overflow) the second pass runs as above.
+// Appends the elements of 16-byte group v (eight bf16) at or above `bound`
+// to the candidates, as composite keys (order-preserving key << 32 | ~id).
 __device__ __forceinline__ void gather_candidates(const uint4 &w, int v, float bound,
                                                   TopkSmem &sh) {
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
@@ -313,6 +304,23 @@ __device__ __forceinline__ void predict_next(TopkSmem &sh, float v128, bool pred
   else if (held && n1 > 4 * SPEC_TOPK) sh.delta = fmaxf(sh.delta * 0.5f, 1.f / 64.f);
 }
 
+// Fast selection for bf16 rows with V % 8 == 0 and V >= 8 * TK_THREADS
+// (every row 16-byte aligned, every thread holds elements). A packed max pass
+// leaves each thread's maximum; every warp sorts its 32 maxima with a
+// shuffle bitonic network, and the smallest of the warps' 8th-largest
+// maxima is a lower bound on the 128-th largest element (16 warps x 8
+// threads each hold an element at least that large). A second pass, read
+// back from L2 (one row per CTA, two CTAs per SM, keeps the rows in flight
+// far below L2), gathers the elements at or above the bound — a few hundred
+// on logit rows — and the exact top 128 (ties to the lower id) is ranked
+// among them in shared memory. Returns false, having written no selection,
+// when the candidates overflow CAND_CAP.
+//
+// With a predicted bound `pred` (finite: the block's previous row's 128th
+// largest logit minus a margin), the max pass also gathers the elements at or
+// above pred. When at least 128 are found, every element of the top 128 is
+// among them (the 128th largest is then >= pred), so the second pass is
+// skipped; otherwise (too few, or an overflow) the second pass runs as above.
 __device__ bool select_bf16_fast(const char *row, int V, TopkSmem &sh, float pred) {
   int n1;
   bool held;
