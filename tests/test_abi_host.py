@@ -41,6 +41,30 @@ def test_workspace_sizes():
     assert sv.draft_topk_softmax_workspace(10, 0) == 0
 
 
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("rows,V", [(10, 4096), (1792, 151936), (7, 4088), (7, 4095),
+                                    (3, 100)])
+def test_top128_workspace_holds_the_candidate_lists(rows, V):
+    """The two-launch select (V % 8 == 0, V >= 4096) keeps per row a list of
+    512 eight-byte keys and one count word after the 256-byte header; other
+    shapes take the one-launch select and need the header only."""
+    lists = V % 8 == 0 and V >= 4096
+    want = 256 + ((_align256(rows * 512 * 8) + _align256(rows * 4)) if lists else 0)
+    assert sv.draft_topk_softmax_workspace(rows, V) == want
+
+
+def test_top128_workload_fits_the_no_alloc_scratch():
+    """B=256, K=7, V=151936 under the top-128 rule (its candidate lists
+    included) fits the 16 MiB the no-alloc entry point holds."""
+    need = sv.spec_verify_linear_workspace(256, 7, 151936, sv.SPEC_RULE_STRICT_TOP128)
+    assert 0 < need <= 16 << 20
+    # the lists are part of it: 1792 rows x 4 KB
+    assert need - sv.spec_verify_linear_workspace(256, 7, 151936, sv.SPEC_RULE_STRICT) > 1792 * 4096
+
+
 FAKE = 1 << 20   # a 256-byte-aligned non-null value; never dereferenced
 
 
@@ -100,7 +124,9 @@ def test_topk_rejects_bad_arguments_on_the_host(L):
     for kw, code in [(dict(k=64), sv.SPEC_ERR_UNSUPPORTED), (dict(V=0), sv.SPEC_ERR_INVALID_ARG),
                      (dict(dt=4), sv.SPEC_ERR_INVALID_ARG), (dict(cu=None), sv.SPEC_ERR_INVALID_ARG),
                      (dict(logits=FAKE + 4), sv.SPEC_ERR_INVALID_ARG),
-                     (dict(ws=None), sv.SPEC_ERR_WORKSPACE), (dict(ws_bytes=8), sv.SPEC_ERR_WORKSPACE)]:
+                     (dict(ws=None), sv.SPEC_ERR_WORKSPACE), (dict(ws_bytes=8), sv.SPEC_ERR_WORKSPACE),
+                     # rows the two-launch select takes need their candidate lists too
+                     (dict(V=4096, ws_bytes=256), sv.SPEC_ERR_WORKSPACE)]:
         a = dict(ok)
         a.update(kw)
         assert f(*a.values()) == code, kw
