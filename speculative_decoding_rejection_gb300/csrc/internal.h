@@ -81,15 +81,18 @@ struct RheoEpi {
 // out_idx / out_prob may be NULL when `rh` is given: the rows then feed the
 // RheoSampling epilogue instead. With `lists` (topk_list_bytes(rows_bound)
 // bytes, 256-byte aligned) and rows topk_two_launch() takes, the select runs
-// as a scan launch and a finishing launch; otherwise as one launch. The
-// events, if given, are recorded around the launch that reads the rows.
+// as a scan launch and a finishing launch (which also runs the epilogue);
+// otherwise as one launch. The events, if given, are recorded around the
+// launch that reads the rows.
 int launch_topk128(const void *logits, int dtype, int rows_bound, int V,
                    const int32_t *cu_rows, const float *temperature, int B,
                    int32_t *out_idx, float *out_prob, WsHeader *hdr,
                    cudaStream_t stream, const RheoEpi *rh = nullptr, void *lists = nullptr,
                    cudaEvent_t before = nullptr, cudaEvent_t after = nullptr);
 size_t topk_list_bytes(long long rows);
-bool topk_two_launch(int dtype, int V, bool epilogue);
+// topk_list_bytes(rows) when V suits the two-launch select (any dtype), else 0
+size_t topk_list_bytes_for(long long rows, int V);
+bool topk_two_launch(int dtype, int V);
 
 bool aligned(const void *p, size_t a);
 

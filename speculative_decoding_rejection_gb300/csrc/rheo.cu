@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(RH_SELECT_THREADS) k_rheo_select(RheoArgs a, i
     GST(out + i, i < n ? (int32_t)(base + (long long)(uint32_t)(sk[i] & 0xffffffffull)) : -1);
 }
 
-inline size_t rheo_ws_bytes(int) { return 256; }   // the status header
+// the status header, then the top-128 select's candidate lists
+inline size_t rheo_ws_bytes(int F, int V) { return 256 + topk_list_bytes_for(F, V); }
 
 }  // namespace
 }  // namespace sv
@@ -116,7 +117,7 @@ using namespace sv;
 
 extern "C" size_t spec_rheo_expand_workspace(int F, int V) {
   if (F < 0 || F > (1 << 24) || V <= 0 || V > SPEC_MAX_V) return 0;
-  return rheo_ws_bytes(F);
+  return rheo_ws_bytes(F, V);
 }
 
 extern "C" int spec_rheo_expand(const void *draft, int ddt, const int32_t *cu_frontier,
@@ -140,7 +141,7 @@ extern "C" int spec_rheo_expand(const void *draft, int ddt, const int32_t *cu_fr
       !aligned(temperature, 4) || !aligned(child_token, 4) || !aligned(child_qproxy, 4) ||
       !aligned(child_qtrue, 4) || !aligned(child_score, 4) || !aligned(keep, 4))
     return SPEC_ERR_INVALID_ARG;
-  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < rheo_ws_bytes(F))
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < rheo_ws_bytes(F, V))
     return SPEC_ERR_WORKSPACE;
 
   RheoArgs a{};
@@ -170,7 +171,7 @@ extern "C" int spec_rheo_expand(const void *draft, int ddt, const int32_t *cu_fr
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 #ifdef SPEC_CHECKED
   check_begin(a.hdr);
-  check_add(workspace, rheo_ws_bytes(F));
+  check_add(workspace, rheo_ws_bytes(F, V));
   check_add(draft, (unsigned long long)F * V * (ddt == SPEC_BF16 ? 2 : 4));
   check_add(cu_frontier, (B + 1) * 4ull);
   check_add(frontier_score, F * 4ull);
@@ -186,11 +187,13 @@ extern "C" int spec_rheo_expand(const void *draft, int ddt, const int32_t *cu_fr
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (F > 0) {
     // the top-128 select with its expansion epilogue streams every frontier
-    // row and dominates the call: profiling events, if registered, bracket it
+    // row and dominates the call: profiling events, if registered, bracket
+    // its launch that reads the rows
     cudaEvent_t before, after;
     take_row_pass_events(&before, &after);
+    void *lists = rheo_ws_bytes(F, V) > 256 ? static_cast<char *>(workspace) + 256 : nullptr;
     const int rc = launch_topk128(draft, ddt, F, V, cu_frontier, temperature, B, nullptr,
-                                  nullptr, a.hdr, st, &epi, nullptr, before, after);
+                                  nullptr, a.hdr, st, &epi, lists, before, after);
     if (rc != SPEC_OK) return rc;
   }
   if (B > 0 && n_keep > 0) {

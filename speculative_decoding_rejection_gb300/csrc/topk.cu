@@ -558,14 +558,10 @@ __device__ void select_radix(const char *row, int V, TopkSmem &sh) {
   __syncthreads();
 }
 
-template <bool BF16>
-__device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
-  const char *row = a.logits + (long long)r * a.row_bytes;
-  const int V = a.V;
+// Row r's request (largest b with cu[b] <= r) -> sh.T: warp 0 narrows the
+// range 32-fold per step with one load per lane. Ends with a block barrier.
+__device__ void row_temperature(const TopkArgs &a, TopkSmem &sh, int r) {
   const int t = threadIdx.x;
-
-  // request of this row (largest b with cu[b] <= r) -> temperature: warp 0
-  // narrows the range 32-fold per step with one load per lane
   if (t < 32) {
     int lo = 0, hi = a.B;
     while (hi - lo > 1) {
@@ -580,9 +576,16 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
     if (t == 0) sh.T = GLD(a.temp + (lo));
   }
   __syncthreads();
-  const float T = sh.T;
-  const bool greedy = !(T >= SPEC_GREEDY_T);
+}
 
+__device__ void finish_row(const TopkArgs &a, TopkSmem &sh, int r, int ksel);
+
+template <bool BF16>
+__device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
+  const char *row = a.logits + (long long)r * a.row_bytes;
+  const int V = a.V;
+  const int t = threadIdx.x;
+  row_temperature(a, sh, r);
   const int ksel = min(SPEC_TOPK, V);
   if (V <= SPEC_TOPK) {
     if (t < SPEC_TOPK) {
@@ -596,7 +599,16 @@ __device__ void topk_row(const TopkArgs &a, TopkSmem &sh, int r) {
   } else {
     select_radix<BF16>(row, V, sh);
   }
+  finish_row(a, sh, r, ksel);
+}
 
+// The rest of a row once its ksel survivors are in sel_idx / sel_val (in any
+// order) and its temperature in sh.T: id order, softmax, the outputs and the
+// construction epilogue.
+__device__ void finish_row(const TopkArgs &a, TopkSmem &sh, int r, int ksel) {
+  const int t = threadIdx.x;
+  const float T = sh.T;
+  const bool greedy = !(T >= SPEC_GREEDY_T);
   // order the survivors by id: each finds its place by counting smaller ids
   // (ids are distinct; padding slots carry INT_MAX and stay at the end)
   {
@@ -1095,6 +1107,64 @@ __global__ void __launch_bounds__(TF_THREADS) k_topk128_finish(const TopkArgs a)
   }
 }
 
+// The finishing launch for rows with the construction epilogue: one
+// 512-thread block per row takes the top 128 from the scan's list as
+// k_topk128_finish does (keys above the 128th largest, the lowest ids among
+// ties at it), then runs the one-launch kernel's id order, softmax and
+// epilogue on them.
+__global__ void __launch_bounds__(TK_THREADS) k_topk128_finish_rows(const TopkArgs a) {
+  __shared__ TopkSmem sh;
+  if (a.hdr->status != SPEC_OK) return;   // the lists were not written
+  const int t = threadIdx.x;
+  int *tie = reinterpret_cast<int *>(sh.cand);   // ids whose key equals the 128th
+  static_assert(sizeof(sh.cand) >= TK_GCAP * sizeof(int), "the ties fit");
+  // rows past the call's are marked empty by the scan
+  for (int r = blockIdx.x; r < a.rows_bound; r += gridDim.x) {
+    const int packed = GLD(a.cnt + r);
+    const int n = packed & 0xffff;
+    const unsigned k128 = (unsigned)packed >> 16;
+    if (n == 0) continue;
+    if (n < SPEC_TOPK || n > TK_GCAP) {   // not a list the scan leaves
+      if (t == 0) set_status(a.hdr, SPEC_ERR_INVALID_ARG, r);
+      continue;
+    }
+    if (t == 0) sh.cand_n = sh.lt_count = 0;
+    row_temperature(a, sh, r);   // ends with a barrier
+    if (t < n) {
+      const unsigned long long c = GLD(a.cand + ((long long)r * TK_GCAP + t));
+      const unsigned key = (unsigned)(c >> 32);
+      const int id = (int)~(unsigned)(c & 0xffffffffull);
+      if (key > k128) {
+        const int p = atomicAdd(&sh.cand_n, 1);
+        if (p < SPEC_TOPK) {
+          sh.sel_idx[p] = id;
+          sh.sel_val[p] = value_of_key16(key);
+        }
+      } else if (key == k128) {
+        tie[atomicAdd(&sh.lt_count, 1)] = id;
+      }
+    }
+    __syncthreads();
+    const int ngt = sh.cand_n, nt = sh.lt_count, need = SPEC_TOPK - ngt;
+    if (ngt >= SPEC_TOPK || nt < need) {   // cannot happen: k128 is the 128th largest key
+      if (t == 0) set_status(a.hdr, SPEC_ERR_INVALID_ARG, r);
+      __syncthreads();
+      continue;
+    }
+    if (t < nt) {   // the `need` lowest ids among the ties
+      const int id = tie[t];
+      int rank = 0;
+      for (int j = 0; j < nt; ++j) rank += tie[j] < id;
+      if (rank < need) {
+        sh.sel_idx[ngt + rank] = id;
+        sh.sel_val[ngt + rank] = value_of_key16(k128);
+      }
+    }
+    __syncthreads();
+    finish_row(a, sh, r, SPEC_TOPK);
+  }
+}
+
 __global__ void k_topk_validate(const TopkArgs a) {
   // one block: reset the status word, check offsets and temperatures
   if (threadIdx.x == 0) {
@@ -1111,13 +1181,17 @@ __global__ void k_topk_validate(const TopkArgs a) {
   if (threadIdx.x == 0 && GLD(a.cu + (a.B)) > a.rows_bound) set_status(a.hdr, SPEC_ERR_INVALID_ARG, a.B);
 }
 
+size_t topk_list_bytes_for(long long rows, int V) {
+  return V % 8 == 0 && V >= 8 * TK_THREADS ? topk_list_bytes(rows) : 0;
+}
+
 size_t topk_list_bytes(long long rows) {
   return align256(sizeof(unsigned long long) * (size_t)rows * TK_GCAP) +
          align256(sizeof(int) * (size_t)rows);
 }
 
-bool topk_two_launch(int dtype, int V, bool epilogue) {
-  return dtype == SPEC_BF16 && V % 8 == 0 && V >= 8 * TK_THREADS && !epilogue;
+bool topk_two_launch(int dtype, int V) {
+  return dtype == SPEC_BF16 && V % 8 == 0 && V >= 8 * TK_THREADS;
 }
 
 int launch_topk128(const void *logits, int dtype, int rows_bound, int V, const int32_t *cu_rows,
@@ -1144,7 +1218,7 @@ int launch_topk128(const void *logits, int dtype, int rows_bound, int V, const i
   if (sms <= 0) return SPEC_ERR_CUDA;
   const int grid = min(rows_bound, TK_CTAS_PER_SM * sms);
   if (before && cudaEventRecord(before, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (lists != nullptr && topk_two_launch(dtype, V, rh != nullptr)) {
+  if (lists != nullptr && topk_two_launch(dtype, V)) {
     const int sgrid = min(rows_bound, TS_CPS * sms);
     a.cand = static_cast<unsigned long long *>(lists);
     a.cnt = reinterpret_cast<int *>(static_cast<char *>(lists) +
@@ -1157,7 +1231,10 @@ int launch_topk128(const void *logits, int dtype, int rows_bound, int V, const i
     k_topk128_scan<TS_NS, TS_STAGE, TS_CPS><<<sgrid, TK_THREADS, ring_bytes, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
     if (after && cudaEventRecord(after, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-    k_topk128_finish<<<min(rows_bound, 16 * sms), TF_THREADS, 0, stream>>>(a);
+    if (rh != nullptr)
+      k_topk128_finish_rows<<<min(rows_bound, 4 * sms), TK_THREADS, 0, stream>>>(a);
+    else
+      k_topk128_finish<<<min(rows_bound, 16 * sms), TF_THREADS, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
   k_topk128<<<grid, TK_THREADS, 0, stream>>>(a);
@@ -1175,7 +1252,7 @@ using namespace sv;
 extern "C" size_t draft_topk_softmax_workspace(int rows, int V) {
   if (rows < 0 || V <= 0 || V > SPEC_MAX_V) return 0;
   // the header, then the candidate lists of the two-launch select
-  return TOPK_WS + (V % 8 == 0 && V >= 8 * TK_THREADS ? topk_list_bytes(rows) : 0);
+  return TOPK_WS + topk_list_bytes_for(rows, V);
 }
 
 extern "C" int draft_topk_softmax(const void *draft_logits, int dt, int rows, int V,
