@@ -49,38 +49,38 @@ FALLBACK_HBM_GBS = 6800.0
 # The eager row pass, captured on B=128, K=4, V=201088 bf16 (460.09 MB
 # streamed by the statistics launch): 460.19 MB read + 3.17 MB written (the
 # per-chunk partial statistics); traffic grows with the rows streamed.
-ROWPASS_TRAFFIC = {"source_sha1": "8c1c60744f8272afb5bc79374639bfe0a2deda16",
+ROWPASS_TRAFFIC = {"source_sha1": "9878f7b237af20ab178ca224a5091735221d7f8b",
                    "dram_per_algorithmic_byte": (460191232 + 3168000) / 460089344}
 # The streaming verifier (the plain call's schedule on dense bf16 logits),
 # per byte of the rows the schedule must read (target rows 1..n+1, dense
 # draft rows 1..min(n+1, K) of sampling requests), on the full B=1024, K=4,
 # V=201088 workload: 2641.1 MB read + 30.0 MB written for 1975.1 MB. The
 # excess is the residual row pairs read a second time (they miss L2).
-STREAM_TRAFFIC = {"source_sha1": "c5d8952a6ec6a20d7802d5280db408d153e7559c",
+STREAM_TRAFFIC = {"source_sha1": "d08b101f3f959ee87d8d759e447d40cde7e2009f",
                   "dram_per_algorithmic_byte": (2641137920 + 29974016) / 1975086336}
 # The scan launch of the top-128 select (every draft row streamed once through
 # a TMA ring; the candidate lists written), per byte of the draft rows, on the
 # full B=256, K=7, V=151936 workload: 544.65 MB read + 5.63 MB written for
 # 544.54 MB.
-TOPK_TRAFFIC = {"source_sha1": "41dc2716af97c6b703cca7333039df27e655b287",
+TOPK_TRAFFIC = {"source_sha1": "ed7ecf1a0747b8da35cd79b1383b1b98545c0ea0",
                 "dram_per_algorithmic_byte": (544654080 + 5634560) / 544538624}
 # The scan launch of the top-128 select on the construction workload (640
 # frontier rows, V = 128256 bf16; L2 flushed before the call): 164.25 MB read
 # + 3.03 MB written for 164.17 MB (most of the write is dirty lines of the L2
 # flush buffer, written back as the rows evict them).
-RHEO_TRAFFIC = {"source_sha1": "41dc2716af97c6b703cca7333039df27e655b287",
+RHEO_TRAFFIC = {"source_sha1": "ed7ecf1a0747b8da35cd79b1383b1b98545c0ea0",
                 "dram_per_algorithmic_byte": (164250624 + 3033856) / 164167680}
 # The tree walk (only visited nodes' rows), per byte of those rows, on the
 # full 32-tree workload: 59.44 MB read + 0.34 MB written for 59.25 MB.
-TREE_TRAFFIC = {"source_sha1": "552b1d2986ca4a69daf3527a193b435fbdc15f08",
+TREE_TRAFFIC = {"source_sha1": "eb4d59e452da4f1cc7d8c74d221cdbde618aaa9b",
                 "dram_per_algorithmic_byte": (59441408 + 336640) / 59254272}
 # One cluster per request, on the 64-request, V = 32000 workload (L2 flushed):
 # 20.87 MB read, nothing written back, for 20.80 MB of rows.
-CLUSTER_TRAFFIC = {"source_sha1": "3b806471f90f81269886118cc136363e739bd16b",
+CLUSTER_TRAFFIC = {"source_sha1": "717c67a9cac4e35bdb735988e27010492532521e",
                    "dram_per_algorithmic_byte": (20869632 + 0) / 20800000}
 # The cluster-resident schedule on the full B=1024 workload: 1975.56 MB read
 # + 3.77 MB written for 1975.09 MB of first reads (each row read once).
-RESIDENT_TRAFFIC = {"source_sha1": "3b806471f90f81269886118cc136363e739bd16b",
+RESIDENT_TRAFFIC = {"source_sha1": "717c67a9cac4e35bdb735988e27010492532521e",
                     "dram_per_algorithmic_byte": (1975558656 + 3765248) / 1975086336}
 
 

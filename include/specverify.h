@@ -449,6 +449,11 @@ int draft_topk_softmax(const void *draft_logits, int dt, int rows, int V,
  * candidate limit (SPEC_ERR_UNSUPPORTED); outputs are then unspecified.
  */
 #define SPEC_RHEO_MAX_CANDIDATES 8192
+/*
+ * Bytes of workspace spec_rheo_expand needs (0 on invalid sizes): a 256-byte
+ * header, and for V % 8 == 0 with V >= 4096 the candidate lists of the
+ * two-launch top-128 select (4 KB and 4 bytes per frontier row).
+ */
 size_t spec_rheo_expand_workspace(int F, int V);
 int spec_rheo_expand(const void *draft, int ddt, const int32_t *cu_frontier,
                      const float *frontier_score, const float *temperature,

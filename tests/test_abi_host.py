@@ -56,6 +56,15 @@ def test_top128_workspace_holds_the_candidate_lists(rows, V):
     assert sv.draft_topk_softmax_workspace(rows, V) == want
 
 
+@pytest.mark.parametrize("F,V", [(640, 128256), (8, 1000), (8, 4100)])
+def test_construction_workspace_holds_the_candidate_lists(F, V):
+    """spec_rheo_expand's workspace: the 256-byte header, and the candidate
+    lists of the two-launch select when its rows take it."""
+    lists = V % 8 == 0 and V >= 4096
+    want = 256 + ((_align256(F * 512 * 8) + _align256(F * 4)) if lists else 0)
+    assert sv.spec_rheo_expand_workspace(F, V) == want
+
+
 def test_top128_workload_fits_the_no_alloc_scratch():
     """B=256, K=7, V=151936 under the top-128 rule (its candidate lists
     included) fits the 16 MiB the no-alloc entry point holds."""
